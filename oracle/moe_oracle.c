@@ -1,0 +1,262 @@
+/*
+ * CPU oracle for the sparse-MoE feed-forward layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may include, link,
+ * load or call this file: only the test suite, the package's smoke check and
+ * the benchmark's CPU-baseline leg use it.  It shares no code, header, table
+ * or helper with the CUDA path.
+ *
+ * What it computes is the plain definition of the layer, in double precision,
+ * from the exact values of the bf16/fp32 inputs.  Source: "Step3.5 Flash
+ * 大模型技术深度解析：稀疏 MoE、混合注意力与 MTP 的高效推理革命" (jsqmd.com),
+ *   §3.2.1  expert configuration: 288 routed experts + 1 always-on shared
+ *           expert per MoE layer, each an independent FFN;
+ *   §3.2.2  top-8 routing: a linear router followed by a softmax gives every
+ *           expert a probability; the 8 most probable routed experts plus the
+ *           shared expert run; their 9 outputs are summed with weights.
+ * Readings taken where that page is silent (each also listed in the design
+ * notes): the expert FFN is SiLU-gated, h = silu(x.Wg) * (x.Wu), o = h.Wd;
+ * the combine weight of a routed expert is its softmax probability over all
+ * routed experts, NOT renormalised over the top-k; the shared expert's weight
+ * is 1; equal probabilities are ordered by the lower expert index.
+ *
+ * Layouts (row-major):
+ *   x          [T][d]          bf16 bit patterns (uint16)
+ *   w_router   [E][d]          fp32
+ *   w_gate_up  [G][2F][d]      bf16; rows 0..F-1 = gate, F..2F-1 = up;
+ *                              G = E + has_shared, group E = shared expert
+ *   w_down     [G][d][F]       bf16
+ * No function here keeps state; every buffer is owned by the caller.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* bf16 bit pattern -> exact double (bf16 is the top half of an fp32). */
+static double bf16_to_double(uint16_t b) {
+  uint32_t u = ((uint32_t)b) << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+static void set_threads(int n_threads) {
+#ifdef _OPENMP
+  if (n_threads > 0) omp_set_num_threads(n_threads);
+#else
+  (void)n_threads;
+#endif
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+/*
+ * Router of §3.2.2 for one token: z_e = sum_i x_i * Wr[e][i] (summed in i
+ * order), p = softmax(z) computed with the maximum subtracted first.
+ * Writes p[0..E).
+ */
+static void route_token(const uint16_t* x_t, const float* w_router, int d, int E, double* p) {
+  double zmax = -INFINITY;
+  for (int e = 0; e < E; ++e) {
+    const float* wr = w_router + (size_t)e * d;
+    double z = 0.0;
+    for (int i = 0; i < d; ++i) z += bf16_to_double(x_t[i]) * (double)wr[i];
+    p[e] = z;
+    if (z > zmax) zmax = z;
+  }
+  double s = 0.0;
+  for (int e = 0; e < E; ++e) {
+    p[e] = exp(p[e] - zmax);
+    s += p[e];
+  }
+  for (int e = 0; e < E; ++e) p[e] /= s;
+}
+
+/*
+ * Top-k of §3.2.2: the k experts with the highest probability, in
+ * descending order of probability, equal probabilities taken lower index
+ * first.  Done as k rounds of "pick the best expert not yet picked".
+ * gap = p(k-th) - p((k+1)-th), +inf when every expert is picked.
+ */
+static void topk_token(const double* p, int E, int k, int* idx, double* w, double* gap) {
+  unsigned char* taken = (unsigned char*)calloc((size_t)E, 1);
+  for (int j = 0; j < k; ++j) {
+    int best = -1;
+    for (int e = 0; e < E; ++e) {
+      if (taken[e]) continue;
+      if (best < 0 || p[e] > p[best]) best = e; /* strict '>' keeps the lower index on ties */
+    }
+    taken[best] = 1;
+    idx[j] = best;
+    w[j] = p[best];
+  }
+  if (gap) {
+    int next = -1;
+    for (int e = 0; e < E; ++e) {
+      if (taken[e]) continue;
+      if (next < 0 || p[e] > p[next]) next = e;
+    }
+    *gap = (next < 0) ? INFINITY : (w[k - 1] - p[next]);
+  }
+  free(taken);
+}
+
+/*
+ * Routing for T tokens.  Any of p_out / w_out / gap_out may be NULL.
+ * Returns 0, or -1 on bad arguments.
+ */
+int oracle_route(const uint16_t* x, const float* w_router, int T, int d, int E, int k,
+                 double* p_out, int* idx_out, double* w_out, double* gap_out, int n_threads) {
+  if (T < 0 || d <= 0 || E <= 0 || k <= 0 || k > E || !x || !w_router || !idx_out) return -1;
+  set_threads(n_threads);
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 4) reduction(| : bad)
+  for (int t = 0; t < T; ++t) {
+    double* p = (double*)malloc(sizeof(double) * (size_t)E);
+    double* w = (double*)malloc(sizeof(double) * (size_t)k);
+    if (!p || !w) { bad = 1; free(p); free(w); continue; }
+    route_token(x + (size_t)t * d, w_router, d, E, p);
+    topk_token(p, E, k, idx_out + (size_t)t * k, w, gap_out ? gap_out + t : NULL);
+    if (p_out) memcpy(p_out + (size_t)t * E, p, sizeof(double) * (size_t)E);
+    if (w_out) memcpy(w_out + (size_t)t * k, w, sizeof(double) * (size_t)k);
+    free(p);
+    free(w);
+  }
+  return bad ? -1 : 0;
+}
+
+/*
+ * Dispatch implied by §3.2.2 (each token's rows go to its chosen experts):
+ *   counts[e]   = number of (t, j) with idx[t][j] == e
+ *   offsets[e]  = counts[0] + ... + counts[e-1], e = 0..E;
+ *   offsets[E+1]= offsets[E] + T  (the shared expert's T rows, token order)
+ *   perm[pos]   = assignment id a = t*k + j, listed expert by expert and,
+ *                 inside one expert, by increasing token index.
+ * Built by visiting experts in order and, for each, tokens in order.
+ */
+int oracle_dispatch(const int* idx, int T, int E, int k, int* counts, int* offsets, int* perm) {
+  if (T < 0 || E <= 0 || k <= 0 || !idx || !counts || !offsets) return -1;
+  for (int e = 0; e < E; ++e) counts[e] = 0;
+  for (long a = 0; a < (long)T * k; ++a) {
+    int e = idx[a];
+    if (e < 0 || e >= E) return -1;
+    counts[e]++;
+  }
+  offsets[0] = 0;
+  for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+  offsets[E + 1] = offsets[E] + T;
+  if (perm) {
+    long pos = 0;
+    for (int e = 0; e < E; ++e)
+      for (int t = 0; t < T; ++t)
+        for (int j = 0; j < k; ++j)
+          if (idx[(size_t)t * k + j] == e) perm[pos++] = t * k + j;
+  }
+  return 0;
+}
+
+/*
+ * One expert FFN (§3.2.1: each expert is an independent FFN; SiLU-gated
+ * reading): g = Wg.x, u = Wu.x, h = g * sigmoid(g) * u, o = Wd.h, all in
+ * double, no intermediate rounding.  scale multiplies o into acc.
+ */
+static void expert_ffn_acc(const uint16_t* x_t, const uint16_t* w_gu, const uint16_t* w_d, int d, int F,
+                           double scale, double* h, double* acc) {
+  for (int f = 0; f < F; ++f) {
+    const uint16_t* wg = w_gu + (size_t)f * d;
+    const uint16_t* wu = w_gu + (size_t)(F + f) * d;
+    double g = 0.0, u = 0.0;
+    for (int i = 0; i < d; ++i) {
+      double xi = bf16_to_double(x_t[i]);
+      g += bf16_to_double(wg[i]) * xi;
+      u += bf16_to_double(wu[i]) * xi;
+    }
+    h[f] = g * (1.0 / (1.0 + exp(-g))) * u;
+  }
+  for (int o = 0; o < d; ++o) {
+    const uint16_t* wd = w_d + (size_t)o * F;
+    double s = 0.0;
+    for (int f = 0; f < F; ++f) s += bf16_to_double(wd[f]) * h[f];
+    acc[o] += scale * s;
+  }
+}
+
+/*
+ * Layer output (§3.2.2 step 3) for the tokens listed in `tokens`:
+ *   y[t] = sum_{j<k} p[t, idx[t][j]] * FFN_{idx[t][j]}(x_t) + FFN_shared(x_t)
+ * summed in slot order, then the shared expert.  If sel is non-NULL it gives
+ * the k experts per listed token ([n_tokens][k]) instead of the oracle's own
+ * top-k; the weights are still the oracle's probabilities of those experts.
+ * w_gate_up / w_down hold E + has_shared groups.  y is [n_tokens][d].
+ */
+int oracle_forward(const uint16_t* x, const float* w_router, const uint16_t* w_gate_up, const uint16_t* w_down,
+                   int T, int d, int E, int k, int F, int has_shared, const int* tokens, int n_tokens,
+                   const int* sel, double* y, int n_threads) {
+  if (T < 0 || d <= 0 || E <= 0 || k <= 0 || k > E || F <= 0 || n_tokens < 0) return -1;
+  if (!x || !w_router || !w_gate_up || !w_down || !tokens || !y) return -1;
+  for (int i = 0; i < n_tokens; ++i)
+    if (tokens[i] < 0 || tokens[i] >= T) return -1;
+  if (sel)
+    for (long i = 0; i < (long)n_tokens * k; ++i)
+      if (sel[i] < 0 || sel[i] >= E) return -1;
+  set_threads(n_threads);
+  const size_t gu_stride = (size_t)2 * F * d, d_stride = (size_t)d * F;
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+  for (int i = 0; i < n_tokens; ++i) {
+    const int t = tokens[i];
+    const uint16_t* x_t = x + (size_t)t * d;
+    double* p = (double*)malloc(sizeof(double) * (size_t)E);
+    double* h = (double*)malloc(sizeof(double) * (size_t)F);
+    int* ids = (int*)malloc(sizeof(int) * (size_t)k);
+    double* w = (double*)malloc(sizeof(double) * (size_t)k);
+    if (!p || !h || !ids || !w) { bad = 1; free(p); free(h); free(ids); free(w); continue; }
+    route_token(x_t, w_router, d, E, p);
+    if (sel) {
+      for (int j = 0; j < k; ++j) { ids[j] = sel[(size_t)i * k + j]; w[j] = p[ids[j]]; }
+    } else {
+      topk_token(p, E, k, ids, w, NULL);
+    }
+    double* acc = y + (size_t)i * d;
+    for (int o = 0; o < d; ++o) acc[o] = 0.0;
+    for (int j = 0; j < k; ++j)
+      expert_ffn_acc(x_t, w_gate_up + ids[j] * gu_stride, w_down + ids[j] * d_stride, d, F, w[j], h, acc);
+    if (has_shared)
+      expert_ffn_acc(x_t, w_gate_up + (size_t)E * gu_stride, w_down + (size_t)E * d_stride, d, F, 1.0, h, acc);
+    free(p); free(h); free(ids); free(w);
+  }
+  return bad ? -1 : 0;
+}
+
+/*
+ * One expert FFN over a batch of rows, exposed so that tests can pin the
+ * FFN against a library matmul: out[r] = FFN_g(x[rows[r]]) with scale 1.
+ */
+int oracle_expert_ffn(const uint16_t* x, const uint16_t* w_gate_up, const uint16_t* w_down, int d, int F,
+                      int group, const int* rows, int n_rows, double* out, int n_threads) {
+  if (d <= 0 || F <= 0 || group < 0 || n_rows < 0 || !x || !w_gate_up || !w_down || !rows || !out) return -1;
+  set_threads(n_threads);
+  const uint16_t* gu = w_gate_up + (size_t)group * 2 * F * d;
+  const uint16_t* dn = w_down + (size_t)group * d * F;
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+  for (int r = 0; r < n_rows; ++r) {
+    double* h = (double*)malloc(sizeof(double) * (size_t)F);
+    if (!h) { bad = 1; continue; }
+    double* acc = out + (size_t)r * d;
+    for (int o = 0; o < d; ++o) acc[o] = 0.0;
+    expert_ffn_acc(x + (size_t)rows[r] * d, gu, dn, d, F, 1.0, h, acc);
+    free(h);
+  }
+  return bad ? -1 : 0;
+}
