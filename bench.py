@@ -1,0 +1,386 @@
+"""Benchmark of the sparse-MoE layer (Step 3.5 Flash shape) on GB300.
+
+One step = one moe_forward over one batch of synthetic tokens: router,
+softmax/top-8, dispatch, the grouped expert GEMMs (288 routed + 1 shared
+expert), and the combine.  Default workload: the decode batch, T=128 tokens,
+d=4096, 288+1 experts, top-8, expert width 1280 (bf16 weights, 9.09 GB).
+
+Prints one JSON line.  `value` = tokens/s over the timed steps (device time,
+CUDA events, inputs resident in HBM); `e2e` = the same through the host-buffer
+entry point (pinned host x in, host y out, copies inside the timed region);
+`roofline` = the gate/up grouped GEMM (the dominant kernel) against the
+measured HBM copy bandwidth; `cpu_baseline` = the CPU oracle on a bounded
+sample of the same workload.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+                  [--workload decode|prefill|skew|T=<n>]
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs its own replica of
+the layer on its own batch (weak scaling, no data-path collective); the
+time is the max over ranks and `value` counts every rank's tokens.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "MoE-layer tokens/s at 1 GB300 (d=4096,E=288,top-8) and % of HBM/tensor roofline"
+N_X_BUFFERS = 4  # distinct token batches cycled through the timed steps
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def workload(name: str):
+    from expert_routed_ffn_gemm_gb300 import synth
+
+    if name == "decode":
+        return synth.FLASH_DECODE, None
+    if name == "prefill":
+        return synth.FLASH_PREFILL, None
+    if name == "skew":
+        return synth.FLASH_SKEW, "zipf"
+    if name.startswith("T="):
+        return synth.FLASH_DECODE.with_tokens(int(name[2:])), None
+    raise SystemExit(f"unknown workload {name}")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                self.out = ""
+
+    def summary(self):
+        if not self.out:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.strip().splitlines():
+            f = [v.strip() for v in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        load = [v for v in sm if smax and v > 0.3 * smax] or sm
+        return {"sm_mhz": statistics.median(load) if load else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def algorithmic_bytes(shape, touched: int):
+    """Bytes the layer must move: the weights of every expert group with at
+    least one row (routed experts touched + the shared expert), the router
+    weights, x in and y out."""
+    d, F, E, T = shape.d, shape.F, shape.E, shape.T
+    per_group = 3 * d * F * 2
+    return (touched + (1 if shape.has_shared else 0)) * per_group + E * d * 4 + T * d * 2 * 2
+
+
+def gateup_bytes(shape, touched: int):
+    """Algorithmic bytes of one gate/up GEMM launch: W_gu of every group with
+    rows, the gathered rows read once, H written once."""
+    d, F, T, k = shape.d, shape.F, shape.T, shape.k
+    groups = touched + (1 if shape.has_shared else 0)
+    R = T * k + (T if shape.has_shared else 0)
+    return groups * 2 * F * d * 2 + R * d * 2 + R * F * 2
+
+
+def layer_flops(shape):
+    d, F, E, T, k = shape.d, shape.F, shape.E, shape.T, shape.k
+    return T * ((k + (1 if shape.has_shared else 0)) * 6 * d * F + 2 * d * E)
+
+
+def cpu_oracle_rate(inp_host, shape, budget_s: float, max_tokens: int):
+    """CPU oracle throughput (tokens/s) on the first tokens of the batch, in
+    chunks until `budget_s` seconds are spent or `max_tokens` are done."""
+    import numpy as np
+
+    import oracle
+
+    xb, wr, wgu, wd = inp_host
+    n, spent, chunk = 0, 0.0, 4
+    while spent < budget_s and n < max_tokens:
+        toks = np.arange(n, min(n + chunk, shape.T, max_tokens), dtype=np.int32)
+        if toks.size == 0:
+            break
+        t0 = time.perf_counter()
+        oracle.forward(xb, wr, wgu, wd, shape.k, has_shared=shape.has_shared, tokens=toks)
+        spent += time.perf_counter() - t0
+        n += toks.size
+        chunk = min(64, chunk * 2)
+    return n / spent, n, spent, oracle.max_threads()
+
+
+def host_copy(inp):
+    from expert_routed_ffn_gemm_gb300 import synth
+
+    return (synth.bf16_bits(inp.x), inp.w_router.detach().cpu().numpy(), synth.bf16_bits(inp.w_gate_up),
+            synth.bf16_bits(inp.w_down))
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the CPU oracle as it stands, timed per step on a
+    bounded sample of the workload's tokens."""
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    from expert_routed_ffn_gemm_gb300 import synth
+
+    shape, skew = workload(args.workload)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = synth.make_inputs(shape, seed=0, device=dev, skew=skew)
+    xb, wr, wgu, wd = host_copy(inp)
+    del inp
+    sample = min(shape.T, args.ref_tokens)
+    for _ in range(args.warmup):
+        oracle.forward(xb, wr, wgu, wd, shape.k, tokens=np.arange(min(2, sample), dtype=np.int32))
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        start = (s * sample) % shape.T
+        toks = (np.arange(sample) + start) % shape.T
+        oracle.forward(xb, wr, wgu, wd, shape.k, tokens=toks.astype(np.int32))
+    el = time.perf_counter() - t0
+    tok_s = sample * args.steps / el
+    cores = oracle.max_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights)",
+        "config": {"workload": f"{args.workload}: T={shape.T}, d={shape.d}, E={shape.E}+1, k={shape.k}, "
+                               f"F={shape.F}", "tokens_per_step_sampled": sample},
+        "cpu_baseline": {"value": tok_s, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{sample} tokens of the T={shape.T} batch per step"},
+        "e2e": {"value": tok_s, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_native(args, world, rank, local):
+    import numpy as np
+
+    from expert_routed_ffn_gemm_gb300 import binding, synth
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    shape, skew = workload(args.workload)
+    hbm_gbs, tf_burst, tf_sust, peak_kind = peaks()
+
+    inp = synth.make_inputs(shape, seed=rank, device=dev, skew=skew)
+    xs = [inp.x] + [synth.make_tokens(shape, seed=1000 + 31 * rank + i, device=dev, skew=skew)
+                    for i in range(N_X_BUFFERS - 1)]
+    layer = binding.MoeLayer(inp.w_router, inp.w_gate_up, inp.w_down, shape.k, shape.T)
+    y = torch.empty((shape.T, shape.d), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    # units of work of each batch: routed experts with at least one row
+    touched = []
+    for x in xs:
+        _, _, _, offsets, _ = layer.route(x, with_gap=False)
+        off = offsets.cpu().numpy()
+        touched.append(int(np.count_nonzero(np.diff(off[:shape.E + 1]))))
+
+    for i in range(args.warmup):
+        layer.forward(xs[i % N_X_BUFFERS], y)
+    torch.cuda.synchronize()
+    if layer.check() != binding.MOE_OK:
+        raise RuntimeError("device error during warm-up")
+
+    # ---- timed region: device time, inputs resident -------------------------
+    layer.profile_enable(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for i in range(args.steps):
+            layer.forward(xs[i % N_X_BUFFERS], y)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = ev0.elapsed_time(ev1)
+    stages, n_prof = layer.profile_read()
+    layer.profile_enable(False)
+    ms_max = max_over_ranks(ms, world)
+    if layer.check() != binding.MOE_OK:
+        raise RuntimeError("device error in the timed region")
+    if not torch.isfinite(y.float()).all():
+        raise RuntimeError("non-finite output")
+
+    # ---- end to end through the host-buffer entry point ---------------------
+    x_host = [x.cpu().pin_memory() for x in xs]
+    y_host = torch.empty((shape.T, shape.d), dtype=torch.bfloat16).pin_memory()
+    for i in range(2):
+        layer.forward_host(x_host[i % N_X_BUFFERS], y_host)
+    barrier(world)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        layer.forward_host(x_host[i % N_X_BUFFERS], y_host)
+    e2e_s = time.perf_counter() - t0
+    barrier(world)
+    e2e_s = max_over_ranks(e2e_s, world)
+
+    tokens_total = shape.T * args.steps * world
+    value = tokens_total / (ms_max / 1e3)
+    e2e = tokens_total / e2e_s
+
+    # ---- roofline of the dominant kernel (gate/up grouped GEMM) -------------
+    steps_prof = max(1, n_prof)
+    gu_ms = stages["gate_up_gemm"] / steps_prof
+    mean_touched = sum(touched[i % N_X_BUFFERS] for i in range(args.steps)) / args.steps
+    gu_bytes = gateup_bytes(shape, mean_touched)
+    gu_gbs = gu_bytes / (gu_ms / 1e3) / 1e9
+    layer_bytes = algorithmic_bytes(shape, mean_touched)
+    step_s = ms_max / 1e3 / args.steps
+    layer_hbm_frac = layer_bytes / step_s / 1e9 / hbm_gbs
+    layer_tc_frac = layer_flops(shape) / step_s / 1e12 / tf_sust
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 tokens, N(0,0.02) weights, random init)",
+        "config": {
+            "workload": f"{args.workload}: T={shape.T} tokens, d={shape.d}, E={shape.E} routed + 1 shared, "
+                        f"top-{shape.k}, expert width {shape.F}, SiLU-gated",
+            "tokens_per_step_per_gpu": shape.T,
+            "l2": f"inputs larger than L2: {layer_bytes / 1e9:.2f} GB of expert weights read per step; "
+                  f"{N_X_BUFFERS} token batches cycled",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+            "experts_touched_mean": mean_touched,
+        },
+        "roofline": {
+            "kernel": "gate_up_gemm (tcgen05 grouped GEMM, fused SiLU-gate)",
+            "bound": "hbm", "achieved": gu_gbs, "peak": hbm_gbs, "unit": "GB/s", "frac": gu_gbs / hbm_gbs,
+            "peak_kind": peak_kind, "traffic": None, "ms_per_launch": gu_ms,
+            "algorithmic_bytes_per_launch": gu_bytes,
+        },
+        "layer_roofline": {"hbm_frac": layer_hbm_frac, "tensor_frac_sustained": layer_tc_frac,
+                           "bytes_per_step": layer_bytes, "flops_per_step": layer_flops(shape)},
+        "stage_ms_per_step": {k: v / steps_prof for k, v in stages.items()},
+        "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": shape.T * shape.d * 2,
+                "d2h_bytes_per_step": shape.T * shape.d * 2},
+        "gpu_launches": 6 * args.steps,
+        "clocks": clk.summary(),
+    }
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        inp_host = host_copy(inp)
+        rate, n, spent, cores = cpu_oracle_rate(inp_host, shape, budget_s=args.cpu_budget, max_tokens=shape.T)
+        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": f"first {n} tokens of the T={shape.T} batch ({spent:.1f} s)"}
+    layer.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--ref-tokens", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        import __graft_entry__
+
+        if rank == 0 or world == 1:
+            __graft_entry__.build()
+        barrier(world)
+        run_native(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,243 @@
+"""ctypes binding of libmoe.so (C ABI in include/moe.h).
+
+Argument marshalling only: every step of the layer runs in the library's
+CUDA kernels.  The functions keep the C names (moe_init, moe_route,
+moe_forward, moe_forward_host, moe_check, moe_set_wait_limit, moe_free,
+moe_status_string, moe_selftest_wait_timeout) and take torch tensors where
+the C functions take pointers; a non-zero status raises MoeError.
+``MoeLayer`` bundles a handle with the weight tensors it borrows.
+
+The library must have been built (``__graft_entry__.build()`` or
+``python -m expert_routed_ffn_gemm_gb300.build``); loading raises otherwise.
+There is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_TOO_MANY_TOKENS = 2
+MOE_ERR_UNSUPPORTED = 3
+MOE_ERR_CUDA = 4
+MOE_ERR_DEVICE = 5
+MOE_ERR_NO_DEVICE = 6
+
+EXPORTED = ("moe_init", "moe_route", "moe_forward", "moe_forward_host", "moe_check", "moe_set_wait_limit",
+            "moe_profile_enable", "moe_profile_read", "moe_free", "moe_status_string",
+            "moe_selftest_wait_timeout")
+PROFILE_STAGES = ("routing", "dispatch", "gather", "gate_up_gemm", "down_gemm", "combine")
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {moe_status_string(status)} (status {status})")
+
+
+class moe_config(ctypes.Structure):
+    _fields_ = [("d_model", ctypes.c_int), ("n_experts", ctypes.c_int), ("top_k", ctypes.c_int),
+                ("ffn_width", ctypes.c_int), ("has_shared", ctypes.c_int), ("max_tokens", ctypes.c_int),
+                ("out_fp32", ctypes.c_int)]
+
+
+class moe_weights(ctypes.Structure):
+    _fields_ = [("w_router", ctypes.c_void_p), ("w_gate_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load():
+    """Load libmoe.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build the CUDA library first (__graft_entry__.build())")
+        lib = ctypes.CDLL(path)
+        vp, i, ull = ctypes.c_void_p, ctypes.c_int, ctypes.c_ulonglong
+        lib.moe_init.argtypes = [ctypes.POINTER(moe_config), ctypes.POINTER(moe_weights), ctypes.POINTER(vp)]
+        lib.moe_route.argtypes = [vp, vp, i, vp, vp, vp, vp, vp, vp]
+        lib.moe_forward.argtypes = [vp, vp, i, vp, vp]
+        lib.moe_forward_host.argtypes = [vp, vp, i, vp, vp]
+        lib.moe_check.argtypes = [vp, vp]
+        lib.moe_set_wait_limit.argtypes = [vp, ull]
+        lib.moe_profile_enable.argtypes = [vp, i]
+        lib.moe_profile_read.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int)]
+        lib.moe_free.argtypes = [vp]
+        lib.moe_status_string.argtypes = [i]
+        lib.moe_status_string.restype = ctypes.c_char_p
+        lib.moe_selftest_wait_timeout.argtypes = [ull, vp]
+        for name in EXPORTED:
+            if name != "moe_status_string":
+                getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def moe_status_string(status: int) -> str:
+    return load().moe_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != MOE_OK:
+        raise MoeError(status, where)
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libmoe must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def moe_init(cfg: moe_config, w_router: torch.Tensor, w_gate_up: torch.Tensor, w_down: torch.Tensor) -> int:
+    w = moe_weights(_ptr(w_router), _ptr(w_gate_up), _ptr(w_down))
+    h = ctypes.c_void_p()
+    _check(load().moe_init(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)), "moe_init")
+    return h.value
+
+
+def moe_route(h: int, x, T: int, idx, prob, perm, offsets, gap=None, stream=None) -> None:
+    _check(load().moe_route(h, _ptr(x), int(T), _ptr(idx), _ptr(prob), _ptr(perm), _ptr(offsets), _ptr(gap),
+                            _stream(stream)), "moe_route")
+
+
+def moe_forward(h: int, x, T: int, y, stream=None) -> None:
+    _check(load().moe_forward(h, _ptr(x), int(T), _ptr(y), _stream(stream)), "moe_forward")
+
+
+def moe_forward_host(h: int, x_host: torch.Tensor, T: int, y_host: torch.Tensor, stream=None) -> None:
+    if x_host.is_cuda or y_host.is_cuda:
+        raise ValueError("moe_forward_host takes host tensors")
+    _check(load().moe_forward_host(h, _ptr(x_host), int(T), _ptr(y_host), _stream(stream)), "moe_forward_host")
+
+
+def moe_check(h: int, stream=None) -> int:
+    """Returns the status (does not raise): MOE_OK or MOE_ERR_DEVICE/CUDA."""
+    return int(load().moe_check(h, _stream(stream)))
+
+
+def moe_set_wait_limit(h: int, ns: int) -> None:
+    _check(load().moe_set_wait_limit(h, int(ns)), "moe_set_wait_limit")
+
+
+def moe_profile_enable(h: int, enable: bool) -> None:
+    _check(load().moe_profile_enable(h, int(bool(enable))), "moe_profile_enable")
+
+
+def moe_profile_read(h: int):
+    """Returns ({stage: total ms}, number of recorded calls) and clears the record."""
+    ms = (ctypes.c_float * len(PROFILE_STAGES))()
+    n = ctypes.c_int()
+    _check(load().moe_profile_read(h, ms, ctypes.byref(n)), "moe_profile_read")
+    return dict(zip(PROFILE_STAGES, [float(v) for v in ms])), int(n.value)
+
+
+def moe_free(h: int) -> None:
+    _check(load().moe_free(h), "moe_free")
+
+
+def moe_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
+    return int(load().moe_selftest_wait_timeout(int(limit_ns), _stream(stream)))
+
+
+class MoeLayer:
+    """A handle plus the device weight tensors it borrows.
+
+    w_router fp32 [E, d]; w_gate_up bf16 [E+1, 2F, d] (gate rows, then up
+    rows; group E is the shared expert); w_down bf16 [E+1, d, F].
+    """
+
+    def __init__(self, w_router, w_gate_up, w_down, top_k: int, max_tokens: int, has_shared: bool = True,
+                 out_fp32: bool = False):
+        E, d = w_router.shape
+        G, twoF, d2 = w_gate_up.shape
+        F = twoF // 2
+        if d2 != d or G != E + int(has_shared) or tuple(w_down.shape) != (G, d, F):
+            raise ValueError("weight shapes do not match [E,d], [G,2F,d], [G,d,F]")
+        if w_router.dtype != torch.float32 or w_gate_up.dtype != torch.bfloat16 or w_down.dtype != torch.bfloat16:
+            raise TypeError("w_router must be fp32 and the expert weights bf16")
+        self.weights = (w_router, w_gate_up, w_down)  # kept alive: the handle borrows them
+        self.d, self.E, self.k, self.F = d, E, top_k, F
+        self.has_shared, self.out_fp32, self.max_tokens = has_shared, out_fp32, max_tokens
+        self.device = w_gate_up.device
+        cfg = moe_config(d, E, top_k, F, int(has_shared), max_tokens, int(out_fp32))
+        self.handle = moe_init(cfg, w_router, w_gate_up, w_down)
+
+    def route(self, x: torch.Tensor, stream=None, with_gap: bool = True):
+        T = x.shape[0]
+        dev = x.device
+        idx = torch.empty((T, self.k), dtype=torch.int32, device=dev)
+        prob = torch.empty((T, self.k), dtype=torch.float32, device=dev)
+        perm = torch.empty((T * self.k,), dtype=torch.int32, device=dev)
+        offsets = torch.empty((self.E + 2,), dtype=torch.int32, device=dev)
+        gap = torch.empty((T,), dtype=torch.float32, device=dev) if with_gap else None
+        moe_route(self.handle, x, T, idx, prob, perm, offsets, gap, stream)
+        return idx, prob, perm, offsets, gap
+
+    def forward(self, x: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        T = x.shape[0]
+        if y is None:
+            y = torch.empty((T, self.d), dtype=torch.float32 if self.out_fp32 else torch.bfloat16,
+                            device=x.device)
+        moe_forward(self.handle, x, T, y, stream)
+        return y
+
+    __call__ = forward
+
+    def forward_host(self, x_host: torch.Tensor, y_host: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        T = x_host.shape[0]
+        if y_host is None:
+            y_host = torch.empty((T, self.d), dtype=torch.float32 if self.out_fp32 else torch.bfloat16,
+                                 pin_memory=True)
+        moe_forward_host(self.handle, x_host, T, y_host, stream)
+        return y_host
+
+    def check(self, stream=None) -> int:
+        return moe_check(self.handle, stream)
+
+    def set_wait_limit(self, ns: int) -> None:
+        moe_set_wait_limit(self.handle, ns)
+
+    def profile_enable(self, enable: bool = True) -> None:
+        moe_profile_enable(self.handle, enable)
+
+    def profile_read(self):
+        return moe_profile_read(self.handle)
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            moe_free(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,168 @@
+// K2 dispatch, the row gather, and K5 combine.
+//
+// "Step3.5 Flash 大模型技术深度解析" (jsqmd.com) §3.2.2: every token runs its 8
+// chosen routed experts plus the shared expert, and the 9 outputs are summed
+// with weights.  Dispatch lays the (token, expert) pairs out expert by expert so
+// that each expert's rows are one contiguous block (the grouped GEMM's rows);
+// combine gathers a token's rows back and sums them.  Both are deterministic:
+// dispatch orders rows inside an expert by token index with block-local ranks
+// (no order-dependent atomics), combine sums in a fixed order.
+#include "kernels.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kDispatchThreads = 256;
+
+// Block-wide exclusive scan of one int per thread (256 threads); returns the
+// thread's exclusive prefix and writes the block total to *total.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  int base = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < kDispatchThreads / 32; ++w) {
+    const int s = warp_sums[w];
+    base += (w < warp) ? s : 0;
+    tot += s;
+  }
+  __syncthreads();
+  *total = tot;
+  return base + incl - v;
+}
+
+// Block e < E: offset of expert e, then a stable compaction over tokens of the
+// assignments (t, j) with idx[t][j] == e.  Block 0 also writes offsets[].
+__global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(const int* __restrict__ idx,
+                                                                    const int* __restrict__ counts, int T, int E,
+                                                                    int k, int has_shared, int* __restrict__ offsets,
+                                                                    int* __restrict__ perm, int* __restrict__ inv) {
+  __shared__ int warp_sums[kDispatchThreads / 32];
+  const int e = blockIdx.x;
+
+  // offset of expert e = counts[0] + ... + counts[e-1]
+  int part = 0;
+  for (int i = threadIdx.x; i < e; i += kDispatchThreads) part += counts[i];
+  int base_e;
+  block_exclusive_scan(part, warp_sums, &base_e);
+
+  if (e == 0) {
+    // offsets[0..E]: each thread scans a contiguous run of experts
+    const int per = (E + kDispatchThreads - 1) / kDispatchThreads;
+    const int b = threadIdx.x * per;
+    int local = 0;
+    for (int i = b; i < min(E, b + per); ++i) local += counts[i];
+    int total;
+    const int pre = block_exclusive_scan(local, warp_sums, &total);
+    int run = pre;
+    for (int i = b; i < min(E, b + per); ++i) {
+      offsets[i] = run;
+      run += counts[i];
+    }
+    if (threadIdx.x == 0) {
+      offsets[E] = total;
+      offsets[E + 1] = total + (has_shared ? T : 0);
+    }
+  }
+
+  int running = 0;
+  for (int t0 = 0; t0 < T; t0 += kDispatchThreads) {
+    const int t = t0 + threadIdx.x;
+    int jsel = -1;
+    if (t < T) {
+      const int* row = idx + static_cast<size_t>(t) * k;
+      for (int j = 0; j < k; ++j)
+        if (__ldg(row + j) == e) jsel = j;
+    }
+    int chunk_total;
+    const int r = block_exclusive_scan(jsel >= 0 ? 1 : 0, warp_sums, &chunk_total);
+    if (jsel >= 0) {
+      const int pos = base_e + running + r;
+      const int a = t * k + jsel;
+      perm[pos] = a;
+      inv[a] = pos;
+    }
+    running += chunk_total;
+  }
+}
+
+// One warp per dispatch row: xp[pos] = x[token(pos)], 16-byte vectors.
+__global__ void __launch_bounds__(256) gather_kernel(const bf16* __restrict__ x, const int* __restrict__ perm,
+                                                     int T, int k, int d, int rows, bf16* __restrict__ xp) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (warp >= rows) return;
+  const int Tk = T * k;
+  const int t = (warp < Tk) ? (__ldg(perm + warp) / k) : (warp - Tk);
+  const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * d);
+  uint4* dst = reinterpret_cast<uint4*>(xp + static_cast<size_t>(warp) * d);
+  for (int c = lane; c < d / 8; c += 32) dst[c] = __ldg(src + c);
+}
+
+// One block per token: y[t] = Yp[inv[t*k+0]] + ... + Yp[inv[t*k+k-1]] + Yp[T*k+t],
+// summed in fp32 in that order (Yp rows are fp32).
+__global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ yp, const int* __restrict__ inv,
+                                                      int T, int k, int d, int has_shared, void* __restrict__ y,
+                                                      int out_fp32) {
+  const int t = blockIdx.x;
+  __shared__ int pos[kMaxTopK + 1];
+  if (threadIdx.x < k) pos[threadIdx.x] = __ldg(inv + static_cast<size_t>(t) * k + threadIdx.x);
+  if (threadIdx.x == 0) pos[k] = T * k + t;
+  __syncthreads();
+  const int nterms = k + (has_shared ? 1 : 0);
+  for (int c = threadIdx.x; c < d / 8; c += blockDim.x) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < nterms; ++j) {
+      const float4* src = reinterpret_cast<const float4*>(yp + static_cast<size_t>(pos[j]) * d) + 2 * c;
+      const float4 a = __ldcs(src), b = __ldcs(src + 1);
+      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    }
+    if (out_fp32) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(y) + static_cast<size_t>(t) * d) + 2 * c;
+      dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    } else {
+      uint4 o;
+      uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 pr = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+        ow[i] = *reinterpret_cast<const uint32_t*>(&pr);
+      }
+      reinterpret_cast<uint4*>(static_cast<bf16*>(y) + static_cast<size_t>(t) * d)[c] = o;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const int* idx, const int* counts, int T, int E, int k, int has_shared, int* offsets,
+                            int* perm, int* inv, cudaStream_t stream) {
+  dispatch_kernel<<<E, kDispatchThreads, 0, stream>>>(idx, counts, T, E, k, has_shared, offsets, perm, inv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const bf16* x, const int* perm, int T, int k, int d, int has_shared, bf16* xp,
+                          cudaStream_t stream) {
+  const int rows = T * k + (has_shared ? T : 0);
+  if (rows == 0) return cudaSuccess;
+  const int blocks = (rows + 7) / 8;
+  gather_kernel<<<blocks, 256, 0, stream>>>(x, perm, T, k, d, rows, xp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const float* yp, const int* inv, int T, int k, int d, int has_shared, void* y,
+                           int out_fp32, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  combine_kernel<<<T, 128, 0, stream>>>(yp, inv, T, k, d, has_shared, y, out_fp32);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

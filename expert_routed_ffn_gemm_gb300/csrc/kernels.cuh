@@ -1,0 +1,72 @@
+// Internal interface between the C-ABI layer (moe_api.cu) and the kernels.
+// Every launch_* function enqueues on `stream` and returns the launch status.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace moe {
+
+using bf16 = __nv_bfloat16;
+
+constexpr int kBlockM = 128;  // weight rows per tensor-core tile (M of tcgen05.mma)
+constexpr int kBlockK = 64;   // K elements per pipeline stage (one 128-byte swizzle row)
+constexpr int kMaxExperts = 512;
+constexpr int kMaxTopK = 32;
+constexpr int kRouterTok = 16;  // tokens per router block
+constexpr int kRouterExp = 32;  // experts per router block
+
+// Token-tile widths (N of tcgen05.mma) the grouped GEMMs are built for.
+constexpr int kNumTileN = 5;
+constexpr int kTileN[kNumTileN] = {16, 32, 64, 128, 256};
+
+// K1: router logits (fp32), softmax, top-k, per-expert counts.
+cudaError_t launch_router(const bf16* x, const float* w_router, int T, int d, int E, int k, float* logits,
+                          int* tickets, int* idx, float* prob, float* gap, int* counts, cudaStream_t stream);
+
+// K2: offsets (exclusive scan of counts, shared group appended) and the
+// stable expert-major permutation perm / its inverse inv.
+cudaError_t launch_dispatch(const int* idx, const int* counts, int T, int E, int k, int has_shared, int* offsets,
+                            int* perm, int* inv, cudaStream_t stream);
+
+// Gather of token rows into dispatch order: xp[pos] = x[token(pos)].
+cudaError_t launch_gather(const bf16* x, const int* perm, int T, int k, int d, int has_shared, bf16* xp,
+                          cudaStream_t stream);
+
+struct GemmArgs {
+  const int* offsets;  // [G+1] row offsets of the groups in dispatch order
+  const int* perm;     // [T*k] (down projection: gate weight lookup)
+  const float* prob;   // [T*k] (down projection)
+  void* out;           // H_hi bf16 [R][F] (gate/up) or Yp fp32 [R][d] (down)
+  void* out2;          // H_lo bf16 [R][F] (gate/up): H = H_hi + H_lo to ~16 bits
+  uint32_t* err;       // device error word
+  unsigned long long wait_limit_ns;
+  int G;               // groups (E + has_shared)
+  int K;               // reduction length: d (gate/up) or F (down)
+  int rows_per_group;  // weight rows per group: 2F (gate/up) or d (down)
+  int m_tiles;         // output-feature tiles per group: F/128 or d/128
+  int F;               // expert width (gate/up: offset of the up rows)
+  int out_ld;          // row length of out
+  int Tk;              // T*k: dispatch positions >= Tk belong to the shared expert
+};
+
+// K3/K4: tcgen05 grouped GEMMs over the groups' row blocks.  `tile_n` must be
+// one of kTileN.  gateup = true: H = silu(X Wg^T) * (X Wu^T), stored as the
+// bf16 pair (H_hi, H_lo); map_act = X rows, map_act2 unused.  false:
+// Yp = w * ((H_hi + H_lo) Wd^T); map_act = H_hi rows, map_act2 = H_lo rows.
+cudaError_t launch_expert_gemm(bool gateup, int tile_n, const CUtensorMap* map_w, const CUtensorMap* map_act,
+                               const CUtensorMap* map_act2, const GemmArgs& a, int num_sms, cudaStream_t stream);
+int expert_gemm_smem_bytes(bool gateup, int tile_n);
+// Opts every grouped-GEMM instantiation into its dynamic shared memory size
+// on the current device (once per device, before the first launch).
+cudaError_t expert_gemm_prepare();
+
+// K5: y[t] = sum_j Yp[inv[t*k+j]] + Yp[T*k + t], fp32 in fixed order.
+cudaError_t launch_combine(const float* yp, const int* inv, int T, int k, int d, int has_shared, void* y,
+                           int out_fp32, cudaStream_t stream);
+
+// Bounded-wait self test: waits on a barrier that never completes.
+cudaError_t launch_wait_selftest(uint32_t* err, unsigned long long limit_ns, cudaStream_t stream);
+
+}  // namespace moe

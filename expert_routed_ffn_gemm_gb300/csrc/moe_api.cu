@@ -1,0 +1,458 @@
+// C ABI of libmoe.so (declared in include/moe.h): argument checks, workspace,
+// TMA descriptors and the launch sequence of the layer of "Step3.5 Flash
+// 大模型技术深度解析" (jsqmd.com) §3.2.1-§3.2.2:
+//   router (K1) -> dispatch (K2) -> row gather -> gate/up GEMM (K3)
+//   -> down GEMM (K4) -> combine (K5),
+// all enqueued on the caller's stream with no host synchronisation.
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <array>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "../../include/moe.h"
+#include "kernels.cuh"
+
+using moe::bf16;
+
+constexpr int kProfStages = 6;
+constexpr int kProfEvents = kProfStages + 1;
+constexpr int kProfMaxCalls = 4096;
+
+struct moe_handle {
+  uint32_t magic;
+  moe_config cfg;
+  moe_weights w;
+  int device;
+  int num_sms;
+  int G;
+  int tile_gateup;  // 0 = choose per call
+  int tile_down;
+  unsigned long long wait_limit_ns;
+  // workspace (one cudaMalloc)
+  void* ws;
+  int* counts;   // [E]
+  int* tickets;  // [ceil(Tmax/16)]
+  float* logits; // [Tmax][E]
+  int* idx;      // [Tmax*k]
+  float* prob;   // [Tmax*k]
+  int* perm;     // [Tmax*k]
+  int* inv;      // [Tmax*k]
+  int* offsets;  // [E+2]
+  void* xpyp;    // [(k+1)*Tmax][d]: gathered rows (bf16), then the expert outputs (fp32)
+  bf16* hbuf;    // [(k+1)*Tmax][F] H_hi
+  bf16* hbuf_lo; // [(k+1)*Tmax][F] H_lo = bf16(H - H_hi)
+  bf16* x_stage; // [Tmax][d] (host entry point)
+  void* y_stage; // [Tmax][d] bf16 or fp32 (host entry point)
+  uint32_t* err; // device error word
+  CUtensorMap map_wgu;                  // W_gu as [G*2F][d], box 64 x 128
+  CUtensorMap map_wd;                   // W_d  as [G*d][F], box 64 x 128
+  CUtensorMap map_xp[moe::kNumTileN];   // Xp   as [Rmax][d], box 64 x BN
+  CUtensorMap map_h[moe::kNumTileN];    // H_hi as [Rmax][F], box 64 x BN
+  CUtensorMap map_hlo[moe::kNumTileN];  // H_lo as [Rmax][F], box 64 x BN
+  // per-stage timing (moe_profile_enable)
+  bool profiling;
+  int n_prof;
+  std::vector<std::array<cudaEvent_t, kProfEvents>> prof;
+};
+
+namespace {
+
+constexpr uint32_t kMagic = 0x4d6f4531u;  // "MoE1"
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool load_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// 2-D bf16 tensor map over a row-major [rows][cols] matrix, box = 64 columns
+// (128 bytes, the swizzle width) x box_rows rows, 128-byte swizzle.
+bool encode_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(moe::kBlockK), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool is_device_ptr(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+bool valid_handle(const moe_handle* h) { return h != nullptr && h->magic == kMagic; }
+
+int tile_from_env(const char* name) {
+  const char* v = std::getenv(name);
+  if (!v) return 0;
+  const int t = std::atoi(v);
+  for (int i = 0; i < moe::kNumTileN; ++i)
+    if (moe::kTileN[i] == t) return t;
+  return 0;
+}
+
+int tile_index(int tile_n) {
+  for (int i = 0; i < moe::kNumTileN; ++i)
+    if (moe::kTileN[i] == tile_n) return i;
+  return -1;
+}
+
+// Token-tile width for a mean of `mean_rows` rows per routed expert: the
+// smallest width that holds a typical group in one tile, at most `cap`.
+int choose_tile(double mean_rows, int cap) {
+  for (int i = 0; i < moe::kNumTileN; ++i)
+    if (moe::kTileN[i] >= cap || mean_rows * 1.15 <= moe::kTileN[i]) return moe::kTileN[i];
+  return cap;
+}
+
+#define MOE_CUDA(call)                    \
+  do {                                    \
+    if ((call) != cudaSuccess) {          \
+      return MOE_ERR_CUDA;                \
+    }                                     \
+  } while (0)
+
+int check_call(const moe_handle* h, const void* x, int T) {
+  if (!valid_handle(h)) return MOE_ERR_INVALID_ARG;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (T > h->cfg.max_tokens) return MOE_ERR_TOO_MANY_TOKENS;
+  if (T > 0 && (x == nullptr || !aligned(x, 16))) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+// K1 + K2 into the given buffers.
+int enqueue_route(moe_handle* h, const void* x, int T, int* idx, float* prob, int* perm, int* offsets, float* gap,
+                  cudaStream_t s) {
+  const moe_config& c = h->cfg;
+  MOE_CUDA(cudaMemsetAsync(h->counts, 0, sizeof(int) * c.n_experts, s));
+  MOE_CUDA(moe::launch_router(static_cast<const bf16*>(x), h->w.w_router, T, c.d_model, c.n_experts, c.top_k,
+                              h->logits, h->tickets, idx, prob, gap, h->counts, s));
+  MOE_CUDA(moe::launch_dispatch(idx, h->counts, T, c.n_experts, c.top_k, c.has_shared, offsets, perm, h->inv, s));
+  return MOE_OK;
+}
+
+// Event slot of this call when profiling (nullptr otherwise).
+cudaEvent_t* prof_slot(moe_handle* h) {
+  if (!h->profiling || h->n_prof >= kProfMaxCalls) return nullptr;
+  if (h->n_prof == static_cast<int>(h->prof.size())) {
+    std::array<cudaEvent_t, kProfEvents> ev{};
+    for (auto& e : ev)
+      if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    h->prof.push_back(ev);
+  }
+  return h->prof[h->n_prof++].data();
+}
+
+#define MOE_MARK(i) \
+  if (ev) MOE_CUDA(cudaEventRecord(ev[i], s))
+
+int enqueue_forward(moe_handle* h, const void* x, int T, void* y, cudaStream_t s) {
+  const moe_config& c = h->cfg;
+  cudaEvent_t* ev = prof_slot(h);
+  MOE_MARK(0);
+  MOE_CUDA(cudaMemsetAsync(h->counts, 0, sizeof(int) * c.n_experts, s));
+  MOE_CUDA(moe::launch_router(static_cast<const bf16*>(x), h->w.w_router, T, c.d_model, c.n_experts, c.top_k,
+                              h->logits, h->tickets, h->idx, h->prob, nullptr, h->counts, s));
+  MOE_MARK(1);
+  MOE_CUDA(moe::launch_dispatch(h->idx, h->counts, T, c.n_experts, c.top_k, c.has_shared, h->offsets, h->perm,
+                                h->inv, s));
+  MOE_MARK(2);
+  MOE_CUDA(moe::launch_gather(static_cast<const bf16*>(x), h->perm, T, c.top_k, c.d_model, c.has_shared,
+                              static_cast<bf16*>(h->xpyp), s));
+  const double mean_rows = static_cast<double>(T) * c.top_k / c.n_experts;
+  const int bn1 = h->tile_gateup ? h->tile_gateup : choose_tile(mean_rows, 128);
+  const int bn2 = h->tile_down ? h->tile_down : choose_tile(mean_rows, 128);
+
+  moe::GemmArgs a{};
+  a.offsets = h->offsets;
+  a.perm = h->perm;
+  a.prob = h->prob;
+  a.err = h->err;
+  a.wait_limit_ns = h->wait_limit_ns;
+  a.G = h->G;
+  a.F = c.ffn_width;
+  a.Tk = T * c.top_k;
+
+  a.out = h->hbuf;
+  a.out2 = h->hbuf_lo;
+  a.K = c.d_model;
+  a.rows_per_group = 2 * c.ffn_width;
+  a.m_tiles = c.ffn_width / moe::kBlockM;
+  a.out_ld = c.ffn_width;
+  MOE_MARK(3);
+  const int i1 = tile_index(bn1), i2 = tile_index(bn2);
+  MOE_CUDA(moe::launch_expert_gemm(true, bn1, &h->map_wgu, &h->map_xp[i1], &h->map_xp[i1], a, h->num_sms, s));
+  MOE_MARK(4);
+
+  a.out = h->xpyp;
+  a.out2 = nullptr;
+  a.K = c.ffn_width;
+  a.rows_per_group = c.d_model;
+  a.m_tiles = c.d_model / moe::kBlockM;
+  a.out_ld = c.d_model;
+  MOE_CUDA(moe::launch_expert_gemm(false, bn2, &h->map_wd, &h->map_h[i2], &h->map_hlo[i2], a, h->num_sms, s));
+  MOE_MARK(5);
+  MOE_CUDA(moe::launch_combine(static_cast<const float*>(h->xpyp), h->inv, T, c.top_k, c.d_model, c.has_shared,
+                               y, c.out_fp32, s));
+  MOE_MARK(6);
+  return MOE_OK;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_TOO_MANY_TOKENS: return "T exceeds max_tokens of the handle";
+    case MOE_ERR_UNSUPPORTED: return "unsupported layer shape";
+    case MOE_ERR_CUDA: return "CUDA call failed";
+    case MOE_ERR_DEVICE: return "a kernel reported a failure (pipeline wait limit exceeded)";
+    case MOE_ERR_NO_DEVICE: return "no compute capability 10.3 (GB300) device is current";
+    default: return "unknown status";
+  }
+}
+
+int moe_init(const moe_config* cfg, const moe_weights* w, moe_handle** out) {
+  if (out == nullptr) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (cfg == nullptr || w == nullptr) return MOE_ERR_INVALID_ARG;
+  const moe_config c = *cfg;
+  if (c.d_model <= 0 || c.n_experts <= 0 || c.top_k <= 0 || c.ffn_width <= 0 || c.max_tokens <= 0)
+    return MOE_ERR_INVALID_ARG;
+  if (c.has_shared != 0 && c.has_shared != 1) return MOE_ERR_INVALID_ARG;
+  if (c.out_fp32 != 0 && c.out_fp32 != 1) return MOE_ERR_INVALID_ARG;
+  if (c.d_model % 128 != 0 || c.ffn_width % 128 != 0 || c.n_experts > moe::kMaxExperts ||
+      c.top_k > c.n_experts || c.top_k > moe::kMaxTopK || c.max_tokens > (1 << 20))
+    return MOE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(c.top_k + 1) * c.max_tokens >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
+  if (w->w_router == nullptr || w->w_gate_up == nullptr || w->w_down == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned(w->w_router, 16) || !aligned(w->w_gate_up, 16) || !aligned(w->w_down, 16))
+    return MOE_ERR_INVALID_ARG;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_NO_DEVICE;
+  }
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_NO_DEVICE;
+  }
+  if (major != 10 || minor != 3) return MOE_ERR_NO_DEVICE;
+  if (!is_device_ptr(w->w_router) || !is_device_ptr(w->w_gate_up) || !is_device_ptr(w->w_down))
+    return MOE_ERR_INVALID_ARG;
+  if (!load_encode()) return MOE_ERR_CUDA;
+  if (moe::expert_gemm_prepare() != cudaSuccess) return MOE_ERR_CUDA;
+
+  moe_handle* h = new (std::nothrow) moe_handle();
+  if (h == nullptr) return MOE_ERR_CUDA;
+  h->cfg = c;
+  h->w = *w;
+  h->device = dev;
+  h->num_sms = sms;
+  h->G = c.n_experts + c.has_shared;
+  h->tile_gateup = tile_from_env("MOE_TILE_N_GATEUP");
+  h->tile_down = tile_from_env("MOE_TILE_N_DOWN");
+  h->wait_limit_ns = kDefaultWaitNs;
+
+  const size_t Tmax = static_cast<size_t>(c.max_tokens);
+  const size_t E = c.n_experts, k = c.top_k, d = c.d_model, F = c.ffn_width;
+  const size_t R = (k + 1) * Tmax;
+  const size_t n_tickets = (Tmax + moe::kRouterTok - 1) / moe::kRouterTok;
+  size_t off = 0;
+  auto carve = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+  };
+  const size_t o_counts = carve(4 * E), o_tickets = carve(4 * n_tickets), o_logits = carve(4 * Tmax * E),
+               o_idx = carve(4 * Tmax * k), o_prob = carve(4 * Tmax * k), o_perm = carve(4 * Tmax * k),
+               o_inv = carve(4 * Tmax * k), o_offsets = carve(4 * (E + 2)), o_err = carve(16),
+               o_xpyp = carve(4 * R * d), o_h = carve(2 * R * F), o_hlo = carve(2 * R * F),
+               o_xs = carve(2 * Tmax * d),
+               o_ys = carve((c.out_fp32 ? 4 : 2) * Tmax * d);
+  if (cudaMalloc(&h->ws, off) != cudaSuccess) {
+    cudaGetLastError();
+    delete h;
+    return MOE_ERR_CUDA;
+  }
+  char* b = static_cast<char*>(h->ws);
+  h->counts = reinterpret_cast<int*>(b + o_counts);
+  h->tickets = reinterpret_cast<int*>(b + o_tickets);
+  h->logits = reinterpret_cast<float*>(b + o_logits);
+  h->idx = reinterpret_cast<int*>(b + o_idx);
+  h->prob = reinterpret_cast<float*>(b + o_prob);
+  h->perm = reinterpret_cast<int*>(b + o_perm);
+  h->inv = reinterpret_cast<int*>(b + o_inv);
+  h->offsets = reinterpret_cast<int*>(b + o_offsets);
+  h->err = reinterpret_cast<uint32_t*>(b + o_err);
+  h->xpyp = b + o_xpyp;
+  h->hbuf = reinterpret_cast<bf16*>(b + o_h);
+  h->hbuf_lo = reinterpret_cast<bf16*>(b + o_hlo);
+  h->x_stage = reinterpret_cast<bf16*>(b + o_xs);
+  h->y_stage = b + o_ys;
+
+  bool ok = cudaMemset(h->ws, 0, o_xpyp) == cudaSuccess;  // small buffers: tickets, err, counts
+  const size_t G = h->G;
+  ok = ok && encode_2d(&h->map_wgu, w->w_gate_up, G * 2 * F, d, moe::kBlockM);
+  ok = ok && encode_2d(&h->map_wd, w->w_down, G * d, F, moe::kBlockM);
+  for (int i = 0; ok && i < moe::kNumTileN; ++i) {
+    ok = ok && encode_2d(&h->map_xp[i], h->xpyp, R, d, moe::kTileN[i]);
+    ok = ok && encode_2d(&h->map_h[i], h->hbuf, R, F, moe::kTileN[i]);
+    ok = ok && encode_2d(&h->map_hlo[i], h->hbuf_lo, R, F, moe::kTileN[i]);
+  }
+  ok = ok && cudaDeviceSynchronize() == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    cudaFree(h->ws);
+    delete h;
+    return MOE_ERR_CUDA;
+  }
+  h->magic = kMagic;
+  *out = h;
+  return MOE_OK;
+}
+
+int moe_route(moe_handle* h, const void* x, int T, int* idx, float* prob, int* perm, int* offsets, float* gap,
+              void* stream) {
+  int rc = check_call(h, x, T);
+  if (rc != MOE_OK) return rc;
+  if (idx == nullptr || prob == nullptr || perm == nullptr || offsets == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned(idx, 4) || !aligned(prob, 4) || !aligned(perm, 4) || !aligned(offsets, 4) || !aligned(gap, 4))
+    return MOE_ERR_INVALID_ARG;
+  if (T > 0 && !is_device_ptr(x)) return MOE_ERR_INVALID_ARG;
+  if (!is_device_ptr(idx) || !is_device_ptr(prob) || !is_device_ptr(perm) || !is_device_ptr(offsets) ||
+      (gap != nullptr && !is_device_ptr(gap)))
+    return MOE_ERR_INVALID_ARG;
+  return enqueue_route(h, x, T, idx, prob, perm, offsets, gap, static_cast<cudaStream_t>(stream));
+}
+
+int moe_forward(moe_handle* h, const void* x, int T, void* y, void* stream) {
+  int rc = check_call(h, x, T);
+  if (rc != MOE_OK) return rc;
+  if (T == 0) return MOE_OK;
+  if (y == nullptr || !aligned(y, 16)) return MOE_ERR_INVALID_ARG;
+  if (!is_device_ptr(x) || !is_device_ptr(y)) return MOE_ERR_INVALID_ARG;
+  return enqueue_forward(h, x, T, y, static_cast<cudaStream_t>(stream));
+}
+
+int moe_forward_host(moe_handle* h, const void* x_host, int T, void* y_host, void* stream) {
+  if (!valid_handle(h)) return MOE_ERR_INVALID_ARG;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (T > h->cfg.max_tokens) return MOE_ERR_TOO_MANY_TOKENS;
+  if (T == 0) return MOE_OK;
+  if (x_host == nullptr || y_host == nullptr) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t d = h->cfg.d_model;
+  const size_t xbytes = 2 * d * static_cast<size_t>(T);
+  const size_t ybytes = (h->cfg.out_fp32 ? 4 : 2) * d * static_cast<size_t>(T);
+  MOE_CUDA(cudaMemcpyAsync(h->x_stage, x_host, xbytes, cudaMemcpyHostToDevice, s));
+  const int rc = enqueue_forward(h, h->x_stage, T, h->y_stage, s);
+  if (rc != MOE_OK) return rc;
+  MOE_CUDA(cudaMemcpyAsync(y_host, h->y_stage, ybytes, cudaMemcpyDeviceToHost, s));
+  MOE_CUDA(cudaStreamSynchronize(s));
+  return MOE_OK;
+}
+
+int moe_check(moe_handle* h, void* stream) {
+  if (!valid_handle(h)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  uint32_t e = 0;
+  MOE_CUDA(cudaMemcpyAsync(&e, h->err, sizeof e, cudaMemcpyDeviceToHost, s));
+  MOE_CUDA(cudaMemsetAsync(h->err, 0, sizeof e, s));
+  MOE_CUDA(cudaStreamSynchronize(s));
+  return e ? MOE_ERR_DEVICE : MOE_OK;
+}
+
+int moe_set_wait_limit(moe_handle* h, unsigned long long ns) {
+  if (!valid_handle(h)) return MOE_ERR_INVALID_ARG;
+  h->wait_limit_ns = ns ? ns : kDefaultWaitNs;
+  return MOE_OK;
+}
+
+int moe_profile_enable(moe_handle* h, int enable) {
+  if (!valid_handle(h)) return MOE_ERR_INVALID_ARG;
+  h->profiling = enable != 0;
+  if (!h->profiling) h->n_prof = 0;
+  return MOE_OK;
+}
+
+int moe_profile_read(moe_handle* h, float* ms, int* n_calls) {
+  if (!valid_handle(h) || ms == nullptr || n_calls == nullptr) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < kProfStages; ++i) ms[i] = 0.f;
+  *n_calls = h->n_prof;
+  for (int c = 0; c < h->n_prof; ++c) {
+    auto& ev = h->prof[c];
+    MOE_CUDA(cudaEventSynchronize(ev[kProfStages]));
+    for (int i = 0; i < kProfStages; ++i) {
+      float t = 0.f;
+      MOE_CUDA(cudaEventElapsedTime(&t, ev[i], ev[i + 1]));
+      ms[i] += t;
+    }
+  }
+  h->n_prof = 0;
+  return MOE_OK;
+}
+
+int moe_free(moe_handle* h) {
+  if (!valid_handle(h)) return MOE_ERR_INVALID_ARG;
+  h->magic = 0;
+  const bool ok = cudaDeviceSynchronize() == cudaSuccess;
+  for (auto& ev : h->prof)
+    for (auto e : ev) cudaEventDestroy(e);
+  const bool freed = cudaFree(h->ws) == cudaSuccess;
+  delete h;
+  return (ok && freed) ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int moe_selftest_wait_timeout(unsigned long long limit_ns, void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t* err = nullptr;
+  if (cudaMalloc(&err, sizeof(uint32_t)) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  uint32_t e = 0;
+  bool ok = cudaMemsetAsync(err, 0, sizeof(uint32_t), s) == cudaSuccess;
+  ok = ok && moe::launch_wait_selftest(err, limit_ns, s) == cudaSuccess;
+  ok = ok && cudaMemcpyAsync(&e, err, sizeof e, cudaMemcpyDeviceToHost, s) == cudaSuccess;
+  ok = ok && cudaStreamSynchronize(s) == cudaSuccess;
+  cudaFree(err);
+  if (!ok) return MOE_ERR_CUDA;
+  return e ? MOE_ERR_DEVICE : MOE_OK;
+}
+
+}  // extern "C"

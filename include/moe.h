@@ -1,0 +1,173 @@
+/*
+ * moe.h — C ABI of libmoe.so, the GB300 (sm_103a) sparse-MoE feed-forward layer.
+ *
+ * The layer is the MoE FFN sublayer described in "Step3.5 Flash 大模型技术深度
+ * 解析：稀疏 MoE、混合注意力与 MTP 的高效推理革命" (jsqmd.com):
+ *   §3.2.1  each MoE layer holds E routed experts (288) and one always-on
+ *           shared expert, each an independent FFN;
+ *   §3.2.2  a linear router followed by a softmax scores every routed expert,
+ *           the k most probable (top-8) plus the shared expert run, and their
+ *           outputs are summed with weights.
+ * Readings where that page is silent: the expert FFN is SiLU-gated,
+ *   y_e(x) = W_d[e] · (silu(W_g[e]·x) ⊙ (W_u[e]·x));
+ * a routed expert's weight is its softmax probability over all E experts (not
+ * renormalised over the top-k); the shared expert's weight is 1; equal
+ * probabilities rank the lower expert index first.  The layer maps the
+ * sublayer input x to the FFN output (no norm, no residual add).
+ *
+ * Conventions shared by every entry point:
+ *   - All tensors are dense row-major.  bf16 is IEEE bfloat16 bit patterns.
+ *   - Device pointers must point to memory of the device that was current at
+ *     moe_init, 16-byte aligned.  The caller owns every buffer it passes.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
+ *     is asynchronous on it and never synchronises the device, except
+ *     moe_check and moe_forward_host, which say so.
+ *   - A handle holds one workspace: calls on one handle must be ordered (one
+ *     stream, or ordered by the caller).  Different handles are independent.
+ *   - Return value: MOE_OK (0) or one of the MOE_ERR_* codes below.  Argument
+ *     errors are found on the host before anything is enqueued; nothing traps
+ *     on the device.  Device-side failures (a pipeline wait that exceeded its
+ *     time limit) set an error word that moe_check reports.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG 1     /* null / misaligned pointer, bad size, bad handle      */
+#define MOE_ERR_TOO_MANY_TOKENS 2 /* T > max_tokens of the handle                         */
+#define MOE_ERR_UNSUPPORTED 3     /* shape outside the supported set (see moe_config)     */
+#define MOE_ERR_CUDA 4            /* a CUDA runtime/driver call failed                    */
+#define MOE_ERR_DEVICE 5          /* a kernel reported a failure (moe_check)              */
+#define MOE_ERR_NO_DEVICE 6       /* no sm_100-family (Blackwell) device current          */
+
+/*
+ * Layer shape.  Supported set: d_model % 128 == 0, ffn_width % 128 == 0,
+ * 1 <= n_experts <= 512, 1 <= top_k <= min(n_experts, 32), has_shared in {0,1},
+ * 1 <= max_tokens <= 1<<20 with (top_k+1)*max_tokens < 2^31.
+ */
+typedef struct moe_config {
+  int d_model;    /* d: hidden size (4096 for Step 3.5 Flash)                    */
+  int n_experts;  /* E: routed experts (288)                                      */
+  int top_k;      /* k: routed experts per token (8)                              */
+  int ffn_width;  /* F: expert FFN width (1280)                                   */
+  int has_shared; /* 1: add the always-on shared expert (group index E)           */
+  int max_tokens; /* largest T any later call may pass; sizes the workspace       */
+  int out_fp32;   /* 0: y is bf16 [T][d]; 1: y is fp32 [T][d]                     */
+} moe_config;
+
+/*
+ * Weights, all device pointers, borrowed (not copied): they must stay alive
+ * and unchanged until moe_free.  G = n_experts + has_shared groups; group E is
+ * the shared expert.
+ *   w_router   fp32 [E][d]
+ *   w_gate_up  bf16 [G][2F][d]   rows 0..F-1 are the gate projection W_g,
+ *                                rows F..2F-1 the up projection W_u
+ *   w_down     bf16 [G][d][F]
+ */
+typedef struct moe_weights {
+  const float* w_router;
+  const void* w_gate_up;
+  const void* w_down;
+} moe_weights;
+
+typedef struct moe_handle moe_handle;
+
+/*
+ * Validates cfg and w, allocates the workspace for cfg->max_tokens on the
+ * current device, builds the TMA descriptors of the weights and writes a new
+ * handle to *out.  Synchronous.  On failure *out is set to NULL and nothing
+ * stays allocated.
+ */
+int moe_init(const moe_config* cfg, const moe_weights* w, moe_handle** out);
+
+/*
+ * Routing only (§3.2.2 router + softmax + top-k, and the dispatch order):
+ *   x        bf16 [T][d]   layer input, device
+ *   idx      int  [T][k]   chosen experts, by descending probability (ties:
+ *                          lower index first), device
+ *   prob     fp32 [T][k]   their softmax probabilities (over all E), device
+ *   perm     int  [T*k]    assignment ids a = t*k + j listed expert by expert,
+ *                          inside one expert by increasing t, device
+ *   offsets  int  [E+2]    offsets[e] = rows of experts < e; offsets[E+1] =
+ *                          offsets[E] + T (the shared expert's rows, token
+ *                          order, implicit in perm), device
+ *   gap      fp32 [T] or NULL: p(k-th) - p((k+1)-th) per token (+inf if k == E),
+ *                          device
+ * 0 <= T <= max_tokens.  Results are deterministic run to run.
+ */
+int moe_route(moe_handle* h, const void* x, int T, int* idx, float* prob, int* perm, int* offsets,
+              float* gap, void* stream);
+
+/*
+ * The whole layer: routing, dispatch, the grouped expert FFNs (the shared
+ * expert as one more group), and the gate-weighted combine
+ *   y[t] = sum_{j<k} prob[t][j] * y_{idx[t][j]}(x_t)  +  y_shared(x_t),
+ * summed in slot order then the shared expert, in fp32, without atomics
+ * (bit-identical run to run).
+ *   x  bf16 [T][d], device;  y  [T][d] bf16 or fp32 (cfg.out_fp32), device.
+ * 0 <= T <= max_tokens; T == 0 enqueues nothing.
+ */
+int moe_forward(moe_handle* h, const void* x, int T, void* y, void* stream);
+
+/*
+ * moe_forward on host buffers: copies x (host, bf16 [T][d]) to the handle's
+ * staging buffer, runs the layer and copies y back to host memory (bf16 or
+ * fp32 per cfg.out_fp32), all on `stream`, then synchronises that stream.
+ * Host buffers should be page-locked for the copies to be asynchronous.
+ */
+int moe_forward_host(moe_handle* h, const void* x_host, int T, void* y_host, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the handle's device error word.
+ * Returns MOE_OK, MOE_ERR_DEVICE if a kernel since the last check gave up on a
+ * pipeline wait, or MOE_ERR_CUDA if the stream reports an error.
+ */
+int moe_check(moe_handle* h, void* stream);
+
+/*
+ * Upper bound, in nanoseconds, on every pipeline wait inside the kernels of
+ * this handle (default 2e9).  A wait that exceeds it makes the kernel record
+ * MOE_ERR_DEVICE, drain the copies it started, release its tensor memory and
+ * return.  0 restores the default.
+ */
+int moe_set_wait_limit(moe_handle* h, unsigned long long ns);
+
+/*
+ * Per-stage timing.  enable != 0: every later moe_forward / moe_forward_host on
+ * this handle also records CUDA events on its stream at the boundaries of its
+ * six stages (0 routing, 1 dispatch, 2 row gather, 3 gate/up GEMM, 4 down GEMM,
+ * 5 combine); up to 4096 calls are kept, later calls are not recorded.
+ * enable == 0 stops recording and discards the record.
+ */
+int moe_profile_enable(moe_handle* h, int enable);
+
+/*
+ * Waits for the recorded events, writes the total milliseconds of each stage
+ * over the recorded calls to ms[0..5] and the number of calls to *n_calls,
+ * then clears the record (recording stays as it was).
+ */
+int moe_profile_read(moe_handle* h, float* ms, int* n_calls);
+
+/* Frees the handle and its workspace (synchronises the device first). */
+int moe_free(moe_handle* h);
+
+/* Static description of a status code; never NULL. */
+const char* moe_status_string(int status);
+
+/*
+ * Launches one kernel that waits on a barrier nothing ever arrives at, with a
+ * limit of `limit_ns`, on `stream`, then synchronises it.  Returns
+ * MOE_ERR_DEVICE when the wait gave up as designed (the expected result),
+ * MOE_OK if it did not.  Exercises the bounded-wait path without a fault.
+ */
+int moe_selftest_wait_timeout(unsigned long long limit_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

@@ -1,0 +1,241 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bars (see moe_check.py): routing and dispatch bit-exact outside near-ties,
+probabilities within the derived fp32 bound, layer output within
+2e-2 * RMS of the oracle.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from expert_routed_ffn_gemm_gb300 import binding, synth
+
+from moe_check import check_output, check_routing, cpu, host_bits, sample_tokens, to_dev
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+def make_layer(inp, max_tokens=None, tiles=(0, 0), out_fp32=False, has_shared=True):
+    x, wr, wgu, wd = to_dev(inp, DEV)
+    old = {kk: os.environ.get(kk) for kk in ("MOE_TILE_N_GATEUP", "MOE_TILE_N_DOWN")}
+    os.environ["MOE_TILE_N_GATEUP"] = str(tiles[0])
+    os.environ["MOE_TILE_N_DOWN"] = str(tiles[1])
+    try:
+        layer = binding.MoeLayer(wr, wgu, wd, inp.shape.k, max_tokens or max(1, inp.shape.T),
+                                 has_shared=has_shared, out_fp32=out_fp32)
+    finally:
+        for kk, v in old.items():
+            if v is None:
+                os.environ.pop(kk, None)
+            else:
+                os.environ[kk] = v
+    return layer, x
+
+
+def run_and_check(inp, tiles=(0, 0), tokens=None, out_fp32=False, max_tokens=None):
+    shape = inp.shape
+    layer, x = make_layer(inp, max_tokens=max_tokens, tiles=tiles, out_fp32=out_fp32,
+                          has_shared=shape.has_shared)
+    idx, prob, perm, offsets, gap = layer.route(x)
+    y = layer.forward(x)
+    assert layer.check() == binding.MOE_OK
+    xb, wr, wgu, wd = host_bits(inp)
+    idx_h = cpu(idx)
+    near, _ = check_routing(xb, wr, shape.k, idx_h, cpu(prob), cpu(gap), cpu(perm), cpu(offsets),
+                            has_shared=shape.has_shared)
+    y_h = cpu(y.float())
+    if tokens is None:
+        tokens = np.arange(shape.T, dtype=np.int32)
+    else:
+        tokens = sample_tokens(shape.T, idx_h, tokens, seed=1, extra=near)
+    ratio = check_output(xb, wr, wgu, wd, shape.k, y_h[tokens], idx_h, tokens=tokens,
+                         has_shared=shape.has_shared)
+    layer.close()
+    return ratio, len(near)
+
+
+def test_tiny_workload():
+    inp = synth.make_inputs(synth.TINY, seed=0)
+    run_and_check(inp)
+
+
+@pytest.mark.parametrize("tiles", [(16, 16), (32, 32), (64, 64), (128, 128), (256, 256), (16, 256), (128, 16)])
+def test_tile_widths_ragged(tiles):
+    # 300 tokens over 16 experts (top-2): ~37 rows per expert, ragged in every
+    # tile width, several token tiles per group for the small widths.
+    shape = synth.LayerShape(T=300, d=256, E=16, k=2, F=128)
+    inp = synth.make_inputs(shape, seed=3)
+    run_and_check(inp, tiles=tiles)
+
+
+@pytest.mark.parametrize("T", [1, 2, 7, 33, 129])
+def test_token_counts(T):
+    shape = synth.LayerShape(T=T, d=256, E=16, k=2, F=128)
+    inp = synth.make_inputs(shape, seed=10 + T)
+    run_and_check(inp, max_tokens=200)
+
+
+def test_several_weight_tiles_and_k_steps():
+    # F = 256 -> 2 gate/up weight tiles, d = 512 -> 4 down weight tiles and 8 K steps.
+    shape = synth.LayerShape(T=200, d=512, E=32, k=4, F=256)
+    inp = synth.make_inputs(shape, seed=5)
+    run_and_check(inp)
+
+
+def test_every_expert_selected():
+    # k == E: all experts run for every token; gap is +inf.
+    shape = synth.LayerShape(T=40, d=256, E=8, k=8, F=128)
+    inp = synth.make_inputs(shape, seed=6)
+    run_and_check(inp)
+
+
+def test_without_shared_expert():
+    shape = synth.LayerShape(T=50, d=256, E=12, k=3, F=128, has_shared=False)
+    inp = synth.make_inputs(shape, seed=7)
+    run_and_check(inp)
+
+
+def test_one_hot_expert_and_empty_experts():
+    # A huge bias on expert 5 (feature 0 set to 1): every token picks it first;
+    # most experts receive no rows.
+    shape = synth.LayerShape(T=96, d=256, E=16, k=2, F=128)
+    inp = synth.make_inputs(shape, seed=8)
+    inp.x[:, 0] = 1.0
+    inp.w_router[:, 0] = -20.0
+    inp.w_router[5, 0] = 20.0
+    inp.w_router[9, 0] = 10.0
+    layer, x = make_layer(inp)
+    idx, prob, perm, offsets, gap = layer.route(x)
+    off = cpu(offsets)
+    assert off[5 + 1] - off[5] == 96
+    run_and_check(inp)
+
+
+def test_uniform_router_tie_rule():
+    # W_r = 0: every probability is 1/E and the lower indices win.
+    shape = synth.LayerShape(T=20, d=256, E=16, k=4, F=128)
+    inp = synth.make_inputs(shape, seed=9)
+    inp.w_router.zero_()
+    layer, x = make_layer(inp)
+    idx, prob, perm, offsets, gap = layer.route(x)
+    assert np.all(cpu(idx) == np.arange(4)[None, :])
+    assert np.all(cpu(prob) == np.float32(1.0 / 16))
+    y = layer.forward(x)
+    xb, wr, wgu, wd = host_bits(inp)
+    check_output(xb, wr, wgu, wd, 4, cpu(y.float()), cpu(idx))
+    layer.close()
+
+
+def test_fp32_output():
+    inp = synth.make_inputs(synth.TINY, seed=11)
+    run_and_check(inp, out_fp32=True)
+
+
+def test_deterministic_run_to_run():
+    shape = synth.LayerShape(T=500, d=256, E=16, k=2, F=128)
+    inp = synth.make_inputs(shape, seed=12)
+    layer, x = make_layer(inp)
+    a = [t.clone() for t in layer.route(x)]
+    y1 = layer.forward(x).clone()
+    b = layer.route(x)
+    y2 = layer.forward(x)
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+    assert torch.equal(y1, y2)
+    layer.close()
+
+
+def test_host_entry_point_matches_device_entry_point():
+    inp = synth.make_inputs(synth.TINY, seed=13)
+    layer, x = make_layer(inp)
+    y_dev = layer.forward(x)
+    x_host = inp.x.clone().pin_memory()
+    y_host = layer.forward_host(x_host)
+    assert torch.equal(y_dev.cpu(), y_host)
+    layer.close()
+
+
+def test_zero_tokens_and_limits():
+    inp = synth.make_inputs(synth.TINY, seed=14)
+    layer, x = make_layer(inp, max_tokens=64)
+    y = torch.empty((0, 256), dtype=torch.bfloat16, device=DEV)
+    binding.moe_forward(layer.handle, x[:0], 0, y)
+    big = torch.zeros((65, 256), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(binding.MoeError) as e:
+        layer.forward(big)
+    assert e.value.status == binding.MOE_ERR_TOO_MANY_TOKENS
+    with pytest.raises(binding.MoeError) as e:
+        binding.moe_forward(layer.handle, x.cpu(), 64, torch.empty_like(x))
+    assert e.value.status == binding.MOE_ERR_INVALID_ARG
+    assert layer.check() == binding.MOE_OK
+    layer.close()
+
+
+def test_bounded_wait_reports_instead_of_hanging():
+    # A barrier nothing arrives at: the kernel gives up after 1 ms and the
+    # host reads the error status; the context stays usable.
+    assert binding.moe_selftest_wait_timeout(1_000_000) == binding.MOE_ERR_DEVICE
+    inp = synth.make_inputs(synth.TINY, seed=15)
+    run_and_check(inp)
+
+
+# ---------------------------------------------------------------- full size --
+
+@pytest.fixture(scope="module")
+def flash_weights():
+    shape = synth.FLASH_DECODE
+    inp = synth.make_inputs(shape, seed=0, device=DEV)
+    host = host_bits(inp)
+    yield inp, host
+    del inp
+
+
+def flash_case(flash_weights, T, seed, n_sample=None, skew=None):
+    inp, (_, wr_h, wgu_h, wd_h) = flash_weights
+    shape = synth.FLASH_DECODE.with_tokens(T)
+    x = synth.make_tokens(shape, seed=seed, device=DEV, skew=skew)
+    wr = inp.w_router
+    wr_h2 = wr_h
+    if skew is not None:
+        wr = inp.w_router.clone()
+        ranks = torch.randperm(shape.E, generator=synth.make_generator(seed, "cpu")).double() + 1.0
+        bias = -synth.SKEW_ALPHA * synth.SKEW_S * torch.log(ranks)
+        bias = torch.where(ranks > synth.SKEW_LIVE, torch.full_like(bias, -30.0), bias)
+        wr[:, 0] = bias.to(torch.float32).to(DEV)
+        wr_h2 = cpu(wr)
+    layer = binding.MoeLayer(wr, inp.w_gate_up, inp.w_down, shape.k, T)
+    idx, prob, perm, offsets, gap = layer.route(x)
+    y = layer.forward(x)
+    assert layer.check() == binding.MOE_OK
+    xb = synth.bf16_bits(x)
+    idx_h = cpu(idx)
+    near, _ = check_routing(xb, wr_h2, shape.k, idx_h, cpu(prob), cpu(gap), cpu(perm), cpu(offsets))
+    tokens = np.arange(T, dtype=np.int32) if n_sample is None else sample_tokens(T, idx_h, n_sample, seed, near)
+    y_h = cpu(y[torch.from_numpy(tokens).long().to(DEV)].float())
+    ratio = check_output(xb, wr_h2, wgu_h, wd_h, shape.k, y_h, idx_h, tokens=tokens)
+    layer.close()
+    return ratio
+
+
+def test_flash_decode_all_tokens(flash_weights):
+    # d=4096, 288 routed + 1 shared, top-8, width 1280, T=128 (decode batch)
+    flash_case(flash_weights, 128, seed=100)
+
+
+def test_flash_prefill_sampled(flash_weights):
+    # T=8192: routing and dispatch on every token, output on a seeded sample
+    # plus every near-tie token plus one token per used expert.
+    flash_case(flash_weights, 8192, seed=101, n_sample=128)
+
+
+def test_flash_skewed_sampled(flash_weights):
+    # Zipf-skewed routing, T=4096: hottest expert ~10x the mean, 40 unused.
+    flash_case(flash_weights, 4096, seed=102, n_sample=64, skew="zipf")
+
+
+@pytest.mark.parametrize("T", [1, 8, 512])
+def test_flash_sweep_points(flash_weights, T):
+    flash_case(flash_weights, T, seed=200 + T, n_sample=None if T <= 8 else 64)
