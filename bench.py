@@ -49,18 +49,26 @@ def peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def workload(name: str):
+def workload(name: str, experts: int = 0):
+    """(shape, skew) of a named workload; `experts` > 0 replaces E (smaller
+    cases of the same kernels, e.g. for profiler captures)."""
+    from dataclasses import replace
+
     from expert_routed_ffn_gemm_gb300 import synth
 
     if name == "decode":
-        return synth.FLASH_DECODE, None
-    if name == "prefill":
-        return synth.FLASH_PREFILL, None
-    if name == "skew":
-        return synth.FLASH_SKEW, "zipf"
-    if name.startswith("T="):
-        return synth.FLASH_DECODE.with_tokens(int(name[2:])), None
-    raise SystemExit(f"unknown workload {name}")
+        shape, skew = synth.FLASH_DECODE, None
+    elif name == "prefill":
+        shape, skew = synth.FLASH_PREFILL, None
+    elif name == "skew":
+        shape, skew = synth.FLASH_SKEW, "zipf"
+    elif name.startswith("T="):
+        shape, skew = synth.FLASH_DECODE.with_tokens(int(name[2:])), None
+    else:
+        raise SystemExit(f"unknown workload {name}")
+    if experts > 0:
+        shape = replace(shape, E=experts)
+    return shape, skew
 
 
 class ClockSampler:
@@ -139,9 +147,16 @@ def max_over_ranks(v: float, world: int) -> float:
         return v
     import torch.distributed as dist
 
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cpu" if dist.get_backend() == "gloo" else "cuda"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate(tokens_per_rank: int, steps: int, elapsed_s_per_rank: float, world: int) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    slowest = max_over_ranks(elapsed_s_per_rank, world)
+    return tokens_per_rank * steps * world / slowest
 
 
 def algorithmic_bytes(shape, touched: int):
@@ -205,7 +220,7 @@ def run_reference(args, world, rank):
     import oracle
     from expert_routed_ffn_gemm_gb300 import synth
 
-    shape, skew = workload(args.workload)
+    shape, skew = workload(args.workload, args.experts)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = synth.make_inputs(shape, seed=0, device=dev, skew=skew)
     xb, wr, wgu, wd = host_copy(inp)
@@ -242,7 +257,7 @@ def run_native(args, world, rank, local):
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    shape, skew = workload(args.workload)
+    shape, skew = workload(args.workload, args.experts)
     hbm_gbs, tf_burst, tf_sust, peak_kind = peaks()
 
     inp = synth.make_inputs(shape, seed=rank, device=dev, skew=skew)
@@ -297,11 +312,10 @@ def run_native(args, world, rank, local):
         layer.forward_host(x_host[i % N_X_BUFFERS], y_host)
     e2e_s = time.perf_counter() - t0
     barrier(world)
-    e2e_s = max_over_ranks(e2e_s, world)
+    e2e = aggregate(shape.T, args.steps, e2e_s, world)
 
     tokens_total = shape.T * args.steps * world
     value = tokens_total / (ms_max / 1e3)
-    e2e = tokens_total / e2e_s
 
     # ---- roofline of the dominant kernel (gate/up grouped GEMM) -------------
     steps_prof = max(1, n_prof)
@@ -360,6 +374,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default="decode")
+    ap.add_argument("--experts", type=int, default=0, help="override the routed expert count (smaller cases)")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -2,21 +2,27 @@
 // (each expert an independent FFN; one shared expert always on) run as grouped
 // GEMMs over the dispatch order of §3.2.2, the shared expert being the last
 // group:
-//   gate/up (K3):  H[r, f]  = silu(X[r] . Wg[g, f]) * (X[r] . Wu[g, f])
-//   down    (K4):  Yp[r, o] = w_r * (H[r] . Wd[g, o]),  w_r = the row's routing
-//                  probability (1 for the shared expert); Yp is kept in fp32
-// for every row r of group g.
+//   gate/up (K3):  H[r, f]  = silu(X[r] . Wg[g, f]) * (X[r] . Wu[g, f])   (bf16)
+//   down    (K4):  Yp[r, o] = w_r * (H[r] . Wd[g, o])                       (fp32)
+// for every row r of group g, w_r = the row's routing probability (1 for the
+// shared expert).
 //
 // Design (sm_103a): a persistent, warp-specialised kernel, one CTA per SM.
-// The weight matrix is the MMA's M operand (128 weight rows per tile) and the
-// group's token rows are its N operand (16..256 columns), so that a decode-size
-// group of a few tokens still streams whole 128-row weight tiles.
-//   warp 0      TMA producer: weight tile(s) + token tile per K step into a
-//               STAGES-deep shared-memory ring (128-byte swizzle)
-//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer; accumulators
-//               live in tensor memory, double-buffered when they fit
-//   warps 2..5  epilogue: tcgen05.ld, SiLU-gate (bf16 H) or gate-weight scale
-//               (fp32 Yp)
+// The weights are the MMA's M operand (128 weight rows per tile) and the
+// group's token rows its N operand (16..256 columns), so that a decode-size
+// group of a few tokens still streams whole weight tiles at full width.
+//   warp 0      TMA producer: one weight tile + one token tile per K step into
+//               a STAGES-deep shared-memory ring (128-byte swizzle)
+//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer; two
+//               accumulators in tensor memory so the epilogue of one work item
+//               overlaps the MMAs of the next
+//   warps 2..5  epilogue: tcgen05.ld, then the SiLU gate (K3) or the
+//               gate-weight scale (K4), stores to global memory
+// K3 builds each 128-row weight tile from 64 gate rows (tile rows 0..63) and the
+// 64 up rows of the same features (rows 64..127), two TMA boxes of 64 rows, so
+// one MMA produces both halves of the gate in one accumulator of N columns; the
+// epilogue warps holding gate rows and those holding up rows swap half of each
+// 16-column chunk through shared memory.
 // Work items are (group, token tile, weight tile) with the weight tile fastest,
 // so the CTAs running at one time share a group's token rows in L2 while each
 // weight tile is streamed from HBM once per token tile.  The per-group tile
@@ -33,26 +39,25 @@ constexpr int kThreads = 192;
 constexpr int kEpilogueWarp0 = 2;
 constexpr int kMaxGroups = kMaxExperts + 1;
 constexpr uint64_t kDrainLimitNs = 2000000000ull;
+constexpr uint32_t kEpilogueBar = 1;  // named barrier of the 4 epilogue warps
 
 template <bool GATEUP, int BN>
 struct Cfg {
   static constexpr int A_BYTES = kBlockM * kBlockK * 2;  // one 128 x 64 bf16 weight tile
-  static constexpr int NUM_A = GATEUP ? 2 : 1;           // gate + up tiles, or the down tile
   static constexpr int B_BYTES = BN * kBlockK * 2;       // BN x 64 bf16 token tile
-  static constexpr int NUM_B = GATEUP ? 1 : 2;           // X rows, or the H_hi and H_lo rows
-  static constexpr int STAGE_BYTES = NUM_A * A_BYTES + NUM_B * B_BYTES;  // multiple of 1024
-  static constexpr int RING_BUDGET = 200 * 1024;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // multiple of 1024
+  static constexpr int RING_BUDGET = 196 * 1024;
   static constexpr int STAGES_RAW = RING_BUDGET / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
-  static constexpr int ACC_COLS = GATEUP ? 2 * BN : BN;  // fp32 columns of one accumulator
-  static constexpr int NACC = (2 * ACC_COLS <= 512) ? 2 : 1;
-  static constexpr int TMEM_RAW = NACC * ACC_COLS;
+  static constexpr int NACC = 2;
+  static constexpr int TMEM_RAW = NACC * BN;
   static constexpr int TMEM_COLS = TMEM_RAW <= 32 ? 32 : TMEM_RAW <= 64 ? 64 : TMEM_RAW <= 128 ? 128
                                                                        : TMEM_RAW <= 256 ? 256 : 512;
   // barriers: full[S], empty[S], acc_full[NACC], acc_empty[NACC], drain
   static constexpr int NUM_BARS = 2 * STAGES + 2 * NACC + 1;
-  static constexpr int AUX_BYTES = NUM_BARS * 8 + 16 + (kMaxGroups + 1) * 4;
-  static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STAGES * STAGE_BYTES + AUX_BYTES;
+  static constexpr int XCHG_BYTES = GATEUP ? 2 * 2 * 64 * 8 * 4 : 0;  // [parity][dir][64 f][8 cols] fp32
+  static constexpr int AUX_BYTES = NUM_BARS * 8 + 16 + 32 + (kMaxGroups + 1) * 4;
+  static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STAGES * STAGE_BYTES + XCHG_BYTES + AUX_BYTES;
   static_assert(STAGE_BYTES % 1024 == 0, "stage must keep 1024-byte alignment");
   static_assert(STAGES >= 2, "ring too shallow");
   static_assert(SMEM_BYTES <= 232448, "exceeds shared memory per block");
@@ -109,12 +114,13 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
 template <bool GATEUP, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_act,
-                       const __grid_constant__ CUtensorMap map_act2, const GemmArgs args) {
+                       const GemmArgs args) {
   using C = Cfg<GATEUP, BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  float* xchg = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES + C::XCHG_BYTES);
   uint64_t* full = bars;
   uint64_t* empty = bars + C::STAGES;
   uint64_t* acc_full = bars + 2 * C::STAGES;
@@ -122,7 +128,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* drain = acc_empty + C::NACC;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  int* tile_start = reinterpret_cast<int*>(tmem_holder + 4);
+  volatile int* s_ok = reinterpret_cast<volatile int*>(tmem_holder + 4);  // [2 parities][4 warps]
+  int* tile_start = reinterpret_cast<int*>(tmem_holder + 12);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = args.G;
@@ -141,7 +148,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
     tma_prefetch_desc(&map_w);
     tma_prefetch_desc(&map_act);
-    if (!GATEUP) tma_prefetch_desc(&map_act2);
   }
   if (warp == 1) {
     tmem_alloc(tmem_holder, C::TMEM_COLS);
@@ -180,16 +186,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------------- producer --
-      const uint64_t pol_w = policy_evict_first();
-      const uint64_t pol_act = policy_evict_last();
+      const uint64_t pol_w = policy_evict_first();   // weights: streamed once
+      const uint64_t pol_act = policy_evict_last();  // token rows: re-read by the other weight tiles
       const int k_steps = args.K / kBlockK;
       uint32_t stage = 0, phase = 0;
       long issued = 0;
-      for (int item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x) {
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < n_items && !*abort_flag; item += gridDim.x) {
         const Item it = decode_item(item, args.m_tiles, tile_start, G);
-        const int row_w = it.g * args.rows_per_group + it.m * kBlockM;
+        // K3: gate rows 64m.. of group g, then the up rows F + 64m..; K4: rows 128m..
+        const int row_w = it.g * args.rows_per_group + it.m * (GATEUP ? kBlockM / 2 : kBlockM);
         const int row_act = __ldg(args.offsets + it.g) + it.n * BN;
-        bool ok = true;
         for (int kb = 0; kb < k_steps; ++kb) {
           if (!wait_or_abort(&empty[stage], phase ^ 1u, limit, abort_flag)) {
             record_abort(abort_flag, args.err);
@@ -199,26 +206,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* st = ring + stage * C::STAGE_BYTES;
           mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
           tma_load_2d(st, &map_w, &full[stage], kb * kBlockK, row_w, pol_w);
-          if (GATEUP) tma_load_2d(st + C::A_BYTES, &map_w, &full[stage], kb * kBlockK, row_w + args.F, pol_w);
-          tma_load_2d(st + C::NUM_A * C::A_BYTES, &map_act, &full[stage], kb * kBlockK, row_act, pol_act);
-          if (!GATEUP)
-            tma_load_2d(st + C::NUM_A * C::A_BYTES + C::B_BYTES, &map_act2, &full[stage], kb * kBlockK, row_act,
-                        pol_act);
+          if (GATEUP) tma_load_2d(st + C::A_BYTES / 2, &map_w, &full[stage], kb * kBlockK, row_w + args.F, pol_w);
+          tma_load_2d(st + C::A_BYTES, &map_act, &full[stage], kb * kBlockK, row_act, pol_act);
           ++issued;
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
-        if (!ok) break;
       }
       // Drain: the last load issued into each stage must have landed before
       // this CTA may exit (they always complete; the wait is bounded anyway).
       for (int s = 0; s < C::STAGES; ++s) {
         if (issued <= s) break;
         const long last = s + ((issued - 1 - s) / C::STAGES) * C::STAGES;
-        const uint32_t par = static_cast<uint32_t>((last / C::STAGES) & 1);
-        mbar_wait(&full[s], par, kDrainLimitNs);
+        mbar_wait(&full[s], static_cast<uint32_t>((last / C::STAGES) & 1), kDrainLimitNs);
       }
     }
   } else if (warp == 1) {
@@ -226,15 +228,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // --------------------------------------------------------------- MMA --
       const int k_steps = args.K / kBlockK;
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-      bool issued_any = false;
-      for (int item = blockIdx.x; item < n_items && !*abort_flag; item += gridDim.x) {
+      bool issued_any = false, ok = true;
+      for (int item = blockIdx.x; ok && item < n_items && !*abort_flag; item += gridDim.x) {
         if (!wait_or_abort(&acc_empty[acc], acc_phase ^ 1u, limit, abort_flag)) {
           record_abort(abort_flag, args.err);
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * C::ACC_COLS;
-        bool ok = true;
+        const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kb = 0; kb < k_steps; ++kb) {
           if (!wait_or_abort(&full[stage], phase, limit, abort_flag)) {
             record_abort(abort_flag, args.err);
@@ -243,22 +244,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t st = smem_u32(ring + stage * C::STAGE_BYTES);
-          const uint64_t a0 = smem_desc_sw128(st);
-          const uint64_t a1 = smem_desc_sw128(st + C::A_BYTES);
-          const uint64_t b = smem_desc_sw128(st + C::NUM_A * C::A_BYTES);
-          const uint64_t b_lo = smem_desc_sw128(st + C::NUM_A * C::A_BYTES + C::B_BYTES);
+          const uint64_t a = smem_desc_sw128(st);
+          const uint64_t b = smem_desc_sw128(st + C::A_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < kBlockK / 16; ++kk) {
-            const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
-            // +32 bytes along K inside the swizzle atom = +2 in the address field
-            tc_mma_bf16(d_tmem, a0 + 2 * kk, b + 2 * kk, C::IDESC, accum);
-            if (GATEUP) {
-              tc_mma_bf16(d_tmem + BN, a1 + 2 * kk, b + 2 * kk, C::IDESC, accum);
-            } else {
-              // H = H_hi + H_lo: the low part goes into the same accumulator
-              tc_mma_bf16(d_tmem, a0 + 2 * kk, b_lo + 2 * kk, C::IDESC, 1u);
-            }
-          }
+          for (int kk = 0; kk < kBlockK / 16; ++kk)  // +32 B along K = +2 in the address field
+            tc_mma_bf16(d_tmem, a + 2 * kk, b + 2 * kk, C::IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
           issued_any = true;
           tc_commit(&empty[stage]);
           if (++stage == C::STAGES) {
@@ -283,48 +273,89 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue --
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
-    uint32_t acc = 0, acc_phase = 0;
+    uint32_t acc = 0, acc_phase = 0, it_par = 0, chunk_par = 0;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
       const Item it = decode_item(item, args.m_tiles, tile_start, G);
       const int g_row0 = __ldg(args.offsets + it.g);
       const int g_rows = __ldg(args.offsets + it.g + 1) - g_row0;
       const int row0 = g_row0 + it.n * BN;
       const int valid = min(BN, g_rows - it.n * BN);
-      // warp-uniform outcome: the tcgen05.ld below are .sync.aligned
-      if (!__all_sync(0xffffffffu, wait_or_abort(&acc_full[acc], acc_phase, limit, abort_flag))) {
-        if (lane == 0) record_abort(abort_flag, args.err);
+      // K4: the gate weight of every column of this tile, lane l holding
+      // columns l, l+32, ... (loaded while the MMAs still run).
+      constexpr int kWRegs = (BN + 31) / 32;
+      float wreg[kWRegs];
+      if (!GATEUP) {
+#pragma unroll
+        for (int i = 0; i < kWRegs; ++i) {
+          const int c = i * 32 + lane;
+          const int pos = row0 + c;
+          wreg[i] = (c < valid) ? ((pos < args.Tk) ? __ldg(args.prob + __ldg(args.perm + pos)) : 1.0f) : 0.0f;
+        }
+      }
+      // One decision for all four epilogue warps (they meet at named barriers).
+      const bool ok = __all_sync(0xffffffffu, wait_or_abort(&acc_full[acc], acc_phase, limit, abort_flag));
+      if (lane == 0) s_ok[it_par * 4 + q] = ok ? 1 : 0;
+      named_bar_sync(kEpilogueBar, 128);
+      const bool all_ok = s_ok[it_par * 4 + 0] && s_ok[it_par * 4 + 1] && s_ok[it_par * 4 + 2] &&
+                          s_ok[it_par * 4 + 3];
+      it_par ^= 1u;
+      if (!all_ok) {
+        if (lane == 0 && !ok) record_abort(abort_flag, args.err);
         break;
       }
       tc_fence_after();
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ACC_COLS;
-      const int feat = it.m * kBlockM + row;
-      for (int c0 = 0; c0 < BN && c0 < valid; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld16(taddr + c0, v);
-        if (GATEUP) {
-          uint32_t u[16];
-          tmem_ld16(taddr + BN + c0, u);
-          tmem_ld_wait();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      if (GATEUP) {
+        // rows 0..63: gate of feature 64m + row; rows 64..127: up of feature 64m + row - 64
+        const bool is_gate = q < 2;
+        const int fl = row & 63;
+        const int feat = it.m * (kBlockM / 2) + fl;
+        bf16* H = static_cast<bf16*>(args.out);
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            if (c0 + c < valid) {
-              const float h = silu_mul(__uint_as_float(v[c]), __uint_as_float(u[c]));
-              const bf16 hi = __float2bfloat16_rn(h);
-              const size_t o = static_cast<size_t>(row0 + c0 + c) * args.out_ld + feat;
-              static_cast<bf16*>(args.out)[o] = hi;
-              static_cast<bf16*>(args.out2)[o] = __float2bfloat16_rn(h - __bfloat162float(hi));
-            }
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          if (c0 >= valid) break;
+          uint32_t v[16];
+          tmem_ld16(taddr + c0, v);
+          tmem_ld_wait();
+          // gate threads keep columns 0..7 of the chunk and hand over 8..15;
+          // up threads keep 8..15 and hand over 0..7
+          float* mine_out = xchg + ((chunk_par * 2 + (is_gate ? 1 : 0)) * 64 + fl) * 8;
+          const float* peer_in = xchg + ((chunk_par * 2 + (is_gate ? 0 : 1)) * 64 + fl) * 8;
+          float give[8], keep[8];  // compile-time register indices only
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            give[c] = __uint_as_float(is_gate ? v[8 + c] : v[c]);
+            keep[c] = __uint_as_float(is_gate ? v[c] : v[8 + c]);
           }
-        } else {
+          reinterpret_cast<float4*>(mine_out)[0] = make_float4(give[0], give[1], give[2], give[3]);
+          reinterpret_cast<float4*>(mine_out)[1] = make_float4(give[4], give[5], give[6], give[7]);
+          named_bar_sync(kEpilogueBar, 128);
+          const float4 p0 = reinterpret_cast<const float4*>(peer_in)[0];
+          const float4 p1 = reinterpret_cast<const float4*>(peer_in)[1];
+          const float peer[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+          const int col0 = c0 + (is_gate ? 0 : 8);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const float h = is_gate ? silu_mul(keep[c], peer[c]) : silu_mul(peer[c], keep[c]);
+            if (col0 + c < valid)
+              H[static_cast<size_t>(row0 + col0 + c) * args.out_ld + feat] = __float2bfloat16_rn(h);
+          }
+          chunk_par ^= 1u;
+        }
+      } else {
+        const int feat = it.m * kBlockM + row;
+        float* Y = static_cast<float*>(args.out);
+#pragma unroll
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          if (c0 >= valid) break;
+          uint32_t v[16];
+          tmem_ld16(taddr + c0, v);
           tmem_ld_wait();
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
-            if (c0 + c < valid) {
-              const int pos = row0 + c0 + c;
-              const float w = (pos < args.Tk) ? __ldg(args.prob + __ldg(args.perm + pos)) : 1.0f;
-              static_cast<float*>(args.out)[static_cast<size_t>(pos) * args.out_ld + feat] =
-                  w * __uint_as_float(v[c]);
-            }
+            const int col = c0 + c;
+            const float w = __shfl_sync(0xffffffffu, wreg[col >> 5], col & 31);
+            if (col < valid) Y[static_cast<size_t>(row0 + col) * args.out_ld + feat] = w * __uint_as_float(v[c]);
           }
         }
       }
@@ -348,11 +379,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <bool GATEUP, int BN>
-cudaError_t launch_one(const CUtensorMap* map_w, const CUtensorMap* map_act, const CUtensorMap* map_act2,
-                       const GemmArgs& a, int num_sms,
+cudaError_t launch_one(const CUtensorMap* map_w, const CUtensorMap* map_act, const GemmArgs& a, int num_sms,
                        cudaStream_t stream) {
-  using C = Cfg<GATEUP, BN>;
-  expert_gemm_kernel<GATEUP, BN><<<num_sms, kThreads, C::SMEM_BYTES, stream>>>(*map_w, *map_act, *map_act2, a);
+  expert_gemm_kernel<GATEUP, BN><<<num_sms, kThreads, Cfg<GATEUP, BN>::SMEM_BYTES, stream>>>(*map_w, *map_act, a);
   return cudaGetLastError();
 }
 
@@ -373,28 +402,15 @@ cudaError_t prepare_all() {
 }
 
 template <bool GATEUP>
-cudaError_t dispatch_bn(int tile_n, const CUtensorMap* map_w, const CUtensorMap* map_act, const CUtensorMap* map_act2,
-                        const GemmArgs& a,
+cudaError_t dispatch_bn(int tile_n, const CUtensorMap* map_w, const CUtensorMap* map_act, const GemmArgs& a,
                         int num_sms, cudaStream_t stream) {
   switch (tile_n) {
-    case 16: return launch_one<GATEUP, 16>(map_w, map_act, map_act2, a, num_sms, stream);
-    case 32: return launch_one<GATEUP, 32>(map_w, map_act, map_act2, a, num_sms, stream);
-    case 64: return launch_one<GATEUP, 64>(map_w, map_act, map_act2, a, num_sms, stream);
-    case 128: return launch_one<GATEUP, 128>(map_w, map_act, map_act2, a, num_sms, stream);
-    case 256: return launch_one<GATEUP, 256>(map_w, map_act, map_act2, a, num_sms, stream);
+    case 16: return launch_one<GATEUP, 16>(map_w, map_act, a, num_sms, stream);
+    case 32: return launch_one<GATEUP, 32>(map_w, map_act, a, num_sms, stream);
+    case 64: return launch_one<GATEUP, 64>(map_w, map_act, a, num_sms, stream);
+    case 128: return launch_one<GATEUP, 128>(map_w, map_act, a, num_sms, stream);
+    case 256: return launch_one<GATEUP, 256>(map_w, map_act, a, num_sms, stream);
     default: return cudaErrorInvalidValue;
-  }
-}
-
-template <bool GATEUP>
-int smem_bn(int tile_n) {
-  switch (tile_n) {
-    case 16: return Cfg<GATEUP, 16>::SMEM_BYTES;
-    case 32: return Cfg<GATEUP, 32>::SMEM_BYTES;
-    case 64: return Cfg<GATEUP, 64>::SMEM_BYTES;
-    case 128: return Cfg<GATEUP, 128>::SMEM_BYTES;
-    case 256: return Cfg<GATEUP, 256>::SMEM_BYTES;
-    default: return -1;
   }
 }
 
@@ -411,17 +427,15 @@ __global__ void wait_selftest_kernel(uint32_t* err, unsigned long long limit_ns)
 }  // namespace
 
 cudaError_t launch_expert_gemm(bool gateup, int tile_n, const CUtensorMap* map_w, const CUtensorMap* map_act,
-                               const CUtensorMap* map_act2, const GemmArgs& a, int num_sms, cudaStream_t stream) {
-  return gateup ? dispatch_bn<true>(tile_n, map_w, map_act, map_act2, a, num_sms, stream)
-                : dispatch_bn<false>(tile_n, map_w, map_act, map_act2, a, num_sms, stream);
+                               const GemmArgs& a, int num_sms, cudaStream_t stream) {
+  return gateup ? dispatch_bn<true>(tile_n, map_w, map_act, a, num_sms, stream)
+                : dispatch_bn<false>(tile_n, map_w, map_act, a, num_sms, stream);
 }
 
 cudaError_t expert_gemm_prepare() {
   const cudaError_t e = prepare_all<true>();
   return e != cudaSuccess ? e : prepare_all<false>();
 }
-
-int expert_gemm_smem_bytes(bool gateup, int tile_n) { return gateup ? smem_bn<true>(tile_n) : smem_bn<false>(tile_n); }
 
 cudaError_t launch_wait_selftest(uint32_t* err, unsigned long long limit_ns, cudaStream_t stream) {
   wait_selftest_kernel<<<1, 32, 0, stream>>>(err, limit_ns);

@@ -14,16 +14,29 @@ constexpr int kBlockM = 128;  // weight rows per tensor-core tile (M of tcgen05.
 constexpr int kBlockK = 64;   // K elements per pipeline stage (one 128-byte swizzle row)
 constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 32;
-constexpr int kRouterTok = 16;  // tokens per router block
-constexpr int kRouterExp = 32;  // experts per router block
+constexpr int kMaxKSplit = 16;  // K splits of the router GEMM
 
 // Token-tile widths (N of tcgen05.mma) the grouped GEMMs are built for.
 constexpr int kNumTileN = 5;
 constexpr int kTileN[kNumTileN] = {16, 32, 64, 128, 256};
 
-// K1: router logits (fp32), softmax, top-k, per-expert counts.
-cudaError_t launch_router(const bf16* x, const float* w_router, int T, int d, int E, int k, float* logits,
-                          int* tickets, int* idx, float* prob, float* gap, int* counts, cudaStream_t stream);
+// K1 on the tensor cores: partial logits of a K split, then softmax/top-k.
+struct RouterGemmArgs {
+  float* partial;  // [ksplit][T][E] fp32 partial logits
+  uint32_t* err;
+  unsigned long long wait_limit_ns;
+  int T, d, E;
+  int e_pad;    // rows per slice of the split router weights (multiple of 128)
+  int m_tiles;  // e_pad / 128
+  int ksplit;   // K splits (1..16)
+};
+cudaError_t launch_router_gemm(int tile_n, const CUtensorMap* map_w3, const CUtensorMap* map_x,
+                               const RouterGemmArgs& a, int num_sms, cudaStream_t stream);
+cudaError_t launch_router_topk(const float* partial, int ksplit, int T, int E, int k, int* idx, float* prob,
+                               float* gap, int* counts, cudaStream_t stream);
+// W_r fp32 [E][d] -> bf16 slices [3][e_pad][d] with hi + mid + lo = W_r.
+cudaError_t launch_split_router(const float* w, int E, int d, int e_pad, bf16* w3, cudaStream_t stream);
+cudaError_t router_gemm_prepare();
 
 // K2: offsets (exclusive scan of counts, shared group appended) and the
 // stable expert-major permutation perm / its inverse inv.
@@ -38,8 +51,7 @@ struct GemmArgs {
   const int* offsets;  // [G+1] row offsets of the groups in dispatch order
   const int* perm;     // [T*k] (down projection: gate weight lookup)
   const float* prob;   // [T*k] (down projection)
-  void* out;           // H_hi bf16 [R][F] (gate/up) or Yp fp32 [R][d] (down)
-  void* out2;          // H_lo bf16 [R][F] (gate/up): H = H_hi + H_lo to ~16 bits
+  void* out;           // H bf16 [R][F] (gate/up) or Yp fp32 [R][d] (down)
   uint32_t* err;       // device error word
   unsigned long long wait_limit_ns;
   int G;               // groups (E + has_shared)
@@ -52,12 +64,11 @@ struct GemmArgs {
 };
 
 // K3/K4: tcgen05 grouped GEMMs over the groups' row blocks.  `tile_n` must be
-// one of kTileN.  gateup = true: H = silu(X Wg^T) * (X Wu^T), stored as the
-// bf16 pair (H_hi, H_lo); map_act = X rows, map_act2 unused.  false:
-// Yp = w * ((H_hi + H_lo) Wd^T); map_act = H_hi rows, map_act2 = H_lo rows.
+// one of kTileN.  gateup = true: H = silu(X Wg^T) * (X Wu^T) (map_w box: 64
+// rows, m_tiles = F/64); false: Yp = w * (H Wd^T) (map_w box: 128 rows,
+// m_tiles = d/128).  map_act: the token rows (X or H), box tile_n rows.
 cudaError_t launch_expert_gemm(bool gateup, int tile_n, const CUtensorMap* map_w, const CUtensorMap* map_act,
-                               const CUtensorMap* map_act2, const GemmArgs& a, int num_sms, cudaStream_t stream);
-int expert_gemm_smem_bytes(bool gateup, int tile_n);
+                               const GemmArgs& a, int num_sms, cudaStream_t stream);
 // Opts every grouped-GEMM instantiation into its dynamic shared memory size
 // on the current device (once per device, before the first launch).
 cudaError_t expert_gemm_prepare();

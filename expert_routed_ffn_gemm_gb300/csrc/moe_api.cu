@@ -33,27 +33,28 @@ struct moe_handle {
   int tile_gateup;  // 0 = choose per call
   int tile_down;
   unsigned long long wait_limit_ns;
+  int router_m_tiles;      // ceil(E / 128)
+  long long partial_rows;  // capacity of `partial` in (split, token) rows
   // workspace (one cudaMalloc)
   void* ws;
-  int* counts;   // [E]
-  int* tickets;  // [ceil(Tmax/16)]
-  float* logits; // [Tmax][E]
-  int* idx;      // [Tmax*k]
-  float* prob;   // [Tmax*k]
-  int* perm;     // [Tmax*k]
-  int* inv;      // [Tmax*k]
-  int* offsets;  // [E+2]
-  void* xpyp;    // [(k+1)*Tmax][d]: gathered rows (bf16), then the expert outputs (fp32)
-  bf16* hbuf;    // [(k+1)*Tmax][F] H_hi
-  bf16* hbuf_lo; // [(k+1)*Tmax][F] H_lo = bf16(H - H_hi)
-  bf16* x_stage; // [Tmax][d] (host entry point)
-  void* y_stage; // [Tmax][d] bf16 or fp32 (host entry point)
-  uint32_t* err; // device error word
-  CUtensorMap map_wgu;                  // W_gu as [G*2F][d], box 64 x 128
+  int* counts;     // [E]
+  float* partial;  // [partial_rows][E] router partial logits
+  bf16* w3;        // [3][router_m_tiles*128][d] bf16 slices of W_r (hi, mid, lo)
+  int* idx;        // [Tmax*k]
+  float* prob;     // [Tmax*k]
+  int* perm;       // [Tmax*k]
+  int* inv;        // [Tmax*k]
+  int* offsets;    // [E+2]
+  void* xpyp;      // [(k+1)*Tmax][d]: gathered rows (bf16), then the expert outputs (fp32)
+  bf16* hbuf;      // [(k+1)*Tmax][F] H
+  bf16* x_stage;   // [Tmax][d] (host entry point)
+  void* y_stage;   // [Tmax][d] bf16 or fp32 (host entry point)
+  uint32_t* err;   // device error word
+  CUtensorMap map_w3;                   // W_r slices as [3*e_pad][d], box 64 x 128
+  CUtensorMap map_wgu;                  // W_gu as [G*2F][d], box 64 x 64
   CUtensorMap map_wd;                   // W_d  as [G*d][F], box 64 x 128
   CUtensorMap map_xp[moe::kNumTileN];   // Xp   as [Rmax][d], box 64 x BN
-  CUtensorMap map_h[moe::kNumTileN];    // H_hi as [Rmax][F], box 64 x BN
-  CUtensorMap map_hlo[moe::kNumTileN];  // H_lo as [Rmax][F], box 64 x BN
+  CUtensorMap map_h[moe::kNumTileN];    // H    as [Rmax][F], box 64 x BN
   // per-stage timing (moe_profile_enable)
   bool profiling;
   int n_prof;
@@ -144,13 +145,45 @@ int check_call(const moe_handle* h, const void* x, int T) {
   return MOE_OK;
 }
 
+// K1: router GEMM (K split across CTAs when there are few token tiles) and
+// softmax/top-k into idx/prob/gap, counts per expert.
+int enqueue_router(moe_handle* h, const void* x, int T, int* idx, float* prob, float* gap, cudaStream_t s) {
+  const moe_config& c = h->cfg;
+  MOE_CUDA(cudaMemsetAsync(h->counts, 0, sizeof(int) * c.n_experts, s));
+  if (T == 0) return MOE_OK;
+  const int bn = T <= 32 ? 16 : (T <= 1024 ? 64 : 128);
+  const int n_tt = (T + bn - 1) / bn;
+  const int k_total = 3 * c.d_model / moe::kBlockK;
+  int ks = h->num_sms / (n_tt * h->router_m_tiles);
+  ks = ks < 1 ? 1 : (ks > moe::kMaxKSplit ? moe::kMaxKSplit : ks);
+  ks = ks > k_total ? k_total : ks;
+  while (ks > 1 && static_cast<long long>(ks) * T > h->partial_rows) --ks;
+  // every split must own at least one K step: ks = ceil(k_total / ceil(k_total / ks))
+  const int k_per = (k_total + ks - 1) / ks;
+  ks = (k_total + k_per - 1) / k_per;
+  CUtensorMap map_x;
+  if (!encode_2d(&map_x, x, static_cast<uint64_t>(T), static_cast<uint64_t>(c.d_model), bn)) return MOE_ERR_CUDA;
+  moe::RouterGemmArgs ra{};
+  ra.partial = h->partial;
+  ra.err = h->err;
+  ra.wait_limit_ns = h->wait_limit_ns;
+  ra.T = T;
+  ra.d = c.d_model;
+  ra.E = c.n_experts;
+  ra.e_pad = h->router_m_tiles * moe::kBlockM;
+  ra.m_tiles = h->router_m_tiles;
+  ra.ksplit = ks;
+  MOE_CUDA(moe::launch_router_gemm(bn, &h->map_w3, &map_x, ra, h->num_sms, s));
+  MOE_CUDA(moe::launch_router_topk(h->partial, ks, T, c.n_experts, c.top_k, idx, prob, gap, h->counts, s));
+  return MOE_OK;
+}
+
 // K1 + K2 into the given buffers.
 int enqueue_route(moe_handle* h, const void* x, int T, int* idx, float* prob, int* perm, int* offsets, float* gap,
                   cudaStream_t s) {
   const moe_config& c = h->cfg;
-  MOE_CUDA(cudaMemsetAsync(h->counts, 0, sizeof(int) * c.n_experts, s));
-  MOE_CUDA(moe::launch_router(static_cast<const bf16*>(x), h->w.w_router, T, c.d_model, c.n_experts, c.top_k,
-                              h->logits, h->tickets, idx, prob, gap, h->counts, s));
+  const int rc = enqueue_router(h, x, T, idx, prob, gap, s);
+  if (rc != MOE_OK) return rc;
   MOE_CUDA(moe::launch_dispatch(idx, h->counts, T, c.n_experts, c.top_k, c.has_shared, offsets, perm, h->inv, s));
   return MOE_OK;
 }
@@ -174,9 +207,8 @@ int enqueue_forward(moe_handle* h, const void* x, int T, void* y, cudaStream_t s
   const moe_config& c = h->cfg;
   cudaEvent_t* ev = prof_slot(h);
   MOE_MARK(0);
-  MOE_CUDA(cudaMemsetAsync(h->counts, 0, sizeof(int) * c.n_experts, s));
-  MOE_CUDA(moe::launch_router(static_cast<const bf16*>(x), h->w.w_router, T, c.d_model, c.n_experts, c.top_k,
-                              h->logits, h->tickets, h->idx, h->prob, nullptr, h->counts, s));
+  const int rc = enqueue_router(h, x, T, h->idx, h->prob, nullptr, s);
+  if (rc != MOE_OK) return rc;
   MOE_MARK(1);
   MOE_CUDA(moe::launch_dispatch(h->idx, h->counts, T, c.n_experts, c.top_k, c.has_shared, h->offsets, h->perm,
                                 h->inv, s));
@@ -184,8 +216,8 @@ int enqueue_forward(moe_handle* h, const void* x, int T, void* y, cudaStream_t s
   MOE_CUDA(moe::launch_gather(static_cast<const bf16*>(x), h->perm, T, c.top_k, c.d_model, c.has_shared,
                               static_cast<bf16*>(h->xpyp), s));
   const double mean_rows = static_cast<double>(T) * c.top_k / c.n_experts;
-  const int bn1 = h->tile_gateup ? h->tile_gateup : choose_tile(mean_rows, 128);
-  const int bn2 = h->tile_down ? h->tile_down : choose_tile(mean_rows, 128);
+  const int bn1 = h->tile_gateup ? h->tile_gateup : choose_tile(mean_rows, 256);
+  const int bn2 = h->tile_down ? h->tile_down : choose_tile(mean_rows, 256);
 
   moe::GemmArgs a{};
   a.offsets = h->offsets;
@@ -198,23 +230,21 @@ int enqueue_forward(moe_handle* h, const void* x, int T, void* y, cudaStream_t s
   a.Tk = T * c.top_k;
 
   a.out = h->hbuf;
-  a.out2 = h->hbuf_lo;
   a.K = c.d_model;
   a.rows_per_group = 2 * c.ffn_width;
-  a.m_tiles = c.ffn_width / moe::kBlockM;
+  a.m_tiles = c.ffn_width / (moe::kBlockM / 2);
   a.out_ld = c.ffn_width;
   MOE_MARK(3);
   const int i1 = tile_index(bn1), i2 = tile_index(bn2);
-  MOE_CUDA(moe::launch_expert_gemm(true, bn1, &h->map_wgu, &h->map_xp[i1], &h->map_xp[i1], a, h->num_sms, s));
+  MOE_CUDA(moe::launch_expert_gemm(true, bn1, &h->map_wgu, &h->map_xp[i1], a, h->num_sms, s));
   MOE_MARK(4);
 
   a.out = h->xpyp;
-  a.out2 = nullptr;
   a.K = c.ffn_width;
   a.rows_per_group = c.d_model;
   a.m_tiles = c.d_model / moe::kBlockM;
   a.out_ld = c.d_model;
-  MOE_CUDA(moe::launch_expert_gemm(false, bn2, &h->map_wd, &h->map_h[i2], &h->map_hlo[i2], a, h->num_sms, s));
+  MOE_CUDA(moe::launch_expert_gemm(false, bn2, &h->map_wd, &h->map_h[i2], a, h->num_sms, s));
   MOE_MARK(5);
   MOE_CUDA(moe::launch_combine(static_cast<const float*>(h->xpyp), h->inv, T, c.top_k, c.d_model, c.has_shared,
                                y, c.out_fp32, s));
@@ -274,7 +304,7 @@ int moe_init(const moe_config* cfg, const moe_weights* w, moe_handle** out) {
   if (!is_device_ptr(w->w_router) || !is_device_ptr(w->w_gate_up) || !is_device_ptr(w->w_down))
     return MOE_ERR_INVALID_ARG;
   if (!load_encode()) return MOE_ERR_CUDA;
-  if (moe::expert_gemm_prepare() != cudaSuccess) return MOE_ERR_CUDA;
+  if (moe::expert_gemm_prepare() != cudaSuccess || moe::router_gemm_prepare() != cudaSuccess) return MOE_ERR_CUDA;
 
   moe_handle* h = new (std::nothrow) moe_handle();
   if (h == nullptr) return MOE_ERR_CUDA;
@@ -286,22 +316,25 @@ int moe_init(const moe_config* cfg, const moe_weights* w, moe_handle** out) {
   h->tile_gateup = tile_from_env("MOE_TILE_N_GATEUP");
   h->tile_down = tile_from_env("MOE_TILE_N_DOWN");
   h->wait_limit_ns = kDefaultWaitNs;
+  h->router_m_tiles = (c.n_experts + moe::kBlockM - 1) / moe::kBlockM;
 
   const size_t Tmax = static_cast<size_t>(c.max_tokens);
   const size_t E = c.n_experts, k = c.top_k, d = c.d_model, F = c.ffn_width;
   const size_t R = (k + 1) * Tmax;
-  const size_t n_tickets = (Tmax + moe::kRouterTok - 1) / moe::kRouterTok;
+  const size_t e_pad = static_cast<size_t>(h->router_m_tiles) * moe::kBlockM;
+  // partial logits: room for 16 K splits of up to 2048 tokens, or one of Tmax
+  const size_t p_rows = Tmax > 16 * 2048 ? Tmax : (Tmax < 2048 ? 16 * Tmax : 16 * 2048);
+  h->partial_rows = static_cast<long long>(p_rows);
   size_t off = 0;
   auto carve = [&](size_t bytes) {
     const size_t at = off;
     off = align_up(off + bytes, 256);
     return at;
   };
-  const size_t o_counts = carve(4 * E), o_tickets = carve(4 * n_tickets), o_logits = carve(4 * Tmax * E),
-               o_idx = carve(4 * Tmax * k), o_prob = carve(4 * Tmax * k), o_perm = carve(4 * Tmax * k),
-               o_inv = carve(4 * Tmax * k), o_offsets = carve(4 * (E + 2)), o_err = carve(16),
-               o_xpyp = carve(4 * R * d), o_h = carve(2 * R * F), o_hlo = carve(2 * R * F),
-               o_xs = carve(2 * Tmax * d),
+  const size_t o_counts = carve(4 * E), o_err = carve(16), o_offsets = carve(4 * (E + 2)),
+               o_partial = carve(4 * p_rows * E), o_w3 = carve(2 * 3 * e_pad * d), o_idx = carve(4 * Tmax * k),
+               o_prob = carve(4 * Tmax * k), o_perm = carve(4 * Tmax * k), o_inv = carve(4 * Tmax * k),
+               o_xpyp = carve(4 * R * d), o_h = carve(2 * R * F), o_xs = carve(2 * Tmax * d),
                o_ys = carve((c.out_fp32 ? 4 : 2) * Tmax * d);
   if (cudaMalloc(&h->ws, off) != cudaSuccess) {
     cudaGetLastError();
@@ -310,28 +343,29 @@ int moe_init(const moe_config* cfg, const moe_weights* w, moe_handle** out) {
   }
   char* b = static_cast<char*>(h->ws);
   h->counts = reinterpret_cast<int*>(b + o_counts);
-  h->tickets = reinterpret_cast<int*>(b + o_tickets);
-  h->logits = reinterpret_cast<float*>(b + o_logits);
+  h->err = reinterpret_cast<uint32_t*>(b + o_err);
+  h->offsets = reinterpret_cast<int*>(b + o_offsets);
+  h->partial = reinterpret_cast<float*>(b + o_partial);
+  h->w3 = reinterpret_cast<bf16*>(b + o_w3);
   h->idx = reinterpret_cast<int*>(b + o_idx);
   h->prob = reinterpret_cast<float*>(b + o_prob);
   h->perm = reinterpret_cast<int*>(b + o_perm);
   h->inv = reinterpret_cast<int*>(b + o_inv);
-  h->offsets = reinterpret_cast<int*>(b + o_offsets);
-  h->err = reinterpret_cast<uint32_t*>(b + o_err);
   h->xpyp = b + o_xpyp;
   h->hbuf = reinterpret_cast<bf16*>(b + o_h);
-  h->hbuf_lo = reinterpret_cast<bf16*>(b + o_hlo);
   h->x_stage = reinterpret_cast<bf16*>(b + o_xs);
   h->y_stage = b + o_ys;
 
-  bool ok = cudaMemset(h->ws, 0, o_xpyp) == cudaSuccess;  // small buffers: tickets, err, counts
+  bool ok = cudaMemset(h->ws, 0, o_partial) == cudaSuccess;  // counts, error word, offsets
+  ok = ok && moe::launch_split_router(w->w_router, c.n_experts, c.d_model, static_cast<int>(e_pad), h->w3,
+                                      nullptr) == cudaSuccess;
   const size_t G = h->G;
-  ok = ok && encode_2d(&h->map_wgu, w->w_gate_up, G * 2 * F, d, moe::kBlockM);
+  ok = ok && encode_2d(&h->map_w3, h->w3, 3 * e_pad, d, moe::kBlockM);
+  ok = ok && encode_2d(&h->map_wgu, w->w_gate_up, G * 2 * F, d, moe::kBlockM / 2);
   ok = ok && encode_2d(&h->map_wd, w->w_down, G * d, F, moe::kBlockM);
   for (int i = 0; ok && i < moe::kNumTileN; ++i) {
     ok = ok && encode_2d(&h->map_xp[i], h->xpyp, R, d, moe::kTileN[i]);
     ok = ok && encode_2d(&h->map_h[i], h->hbuf, R, F, moe::kTileN[i]);
-    ok = ok && encode_2d(&h->map_hlo[i], h->hbuf_lo, R, F, moe::kTileN[i]);
   }
   ok = ok && cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {

@@ -1,0 +1,391 @@
+// K1 on the tensor cores — the router of "Step3.5 Flash 大模型技术深度解析"
+// (jsqmd.com) §3.2.2: one logit per routed expert from a linear layer, then a
+// softmax over all experts and the k most probable ones.
+//
+// The logit GEMM z = x . W_r^T keeps fp32 accuracy on bf16 tensor cores: W_r
+// (fp32) is held as three bf16 slices hi + mid + lo (together 24 significand
+// bits, the fp32 significand), x is bf16 already, so each product x_i * slice
+// is exact in fp32 and z = x.hi + x.mid + x.lo is accumulated in fp32 by
+// tcgen05.mma over an effective K of 3d.  The expert rows are the MMA's M
+// operand (128 per tile) and token rows its N operand, as in the expert GEMMs.
+// K is split across CTAs when there are few token tiles (decode); each split
+// writes its partial logits and the top-k kernel sums the splits in a fixed
+// order, so results are identical run to run.
+//
+// router_topk_kernel: one warp per token; lane l holds experts l, l+32, ...;
+// max / sum / argmax by xor-shuffle butterflies (every lane ends with the same
+// bits); ties go to the lower expert index.
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+#include <cfloat>
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr uint64_t kDrainLimitNs = 2000000000ull;
+
+template <int BN>
+struct RCfg {
+  static constexpr int A_BYTES = kBlockM * kBlockK * 2;
+  static constexpr int B_BYTES = BN * kBlockK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES_RAW = (160 * 1024) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+  static constexpr int NACC = (2 * BN <= 512) ? 2 : 1;
+  static constexpr int TMEM_RAW = NACC * BN;
+  static constexpr int TMEM_COLS = TMEM_RAW <= 32 ? 32 : TMEM_RAW <= 64 ? 64 : TMEM_RAW <= 128 ? 128
+                                                                       : TMEM_RAW <= 256 ? 256 : 512;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * NACC + 1;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
+  static_assert(STAGES >= 2, "ring too shallow");
+  static constexpr uint32_t IDESC = idesc_bf16_f32(kBlockM, BN);
+};
+
+struct RItem {
+  int tt, m, ks;
+};
+
+__device__ __forceinline__ RItem decode_ritem(int item, int m_tiles, int ksplit) {
+  RItem it;
+  it.ks = item % ksplit;
+  const int r = item / ksplit;
+  it.m = r % m_tiles;
+  it.tt = r / m_tiles;
+  return it;
+}
+
+__device__ __forceinline__ bool rwait(uint64_t* bar, uint32_t parity, uint64_t limit_ns, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t spins = 0;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((++spins & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+  }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    router_gemm_kernel(const __grid_constant__ CUtensorMap map_w3, const __grid_constant__ CUtensorMap map_x,
+                       const RouterGemmArgs args) {
+  using C = RCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::STAGES;
+  uint64_t* acc_full = bars + 2 * C::STAGES;
+  uint64_t* acc_empty = acc_full + C::NACC;
+  uint64_t* drain = acc_empty + C::NACC;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_tt = (args.T + BN - 1) / BN;
+  const int n_items = n_tt * args.m_tiles * args.ksplit;
+  const int k_total = 3 * (args.d / kBlockK);                     // hi, mid, lo slices
+  const int k_per = (k_total + args.ksplit - 1) / args.ksplit;    // K steps per split
+  const int kd = args.d / kBlockK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < C::NACC; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&map_w3);
+    tma_prefetch_desc(&map_x);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const uint64_t limit = args.wait_limit_ns;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_last();  // W slices and x are re-read by other CTAs
+      uint32_t stage = 0, phase = 0;
+      long issued = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < n_items && !*abort_flag; item += gridDim.x) {
+        const RItem it = decode_ritem(item, args.m_tiles, args.ksplit);
+        const int kb0 = it.ks * k_per, kb1 = min(k_total, kb0 + k_per);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!rwait(&empty[stage], phase ^ 1u, limit, abort_flag)) {
+            *abort_flag = 1;
+            atomicOr(args.err, kErrWaitTimeout);
+            ok = false;
+            break;
+          }
+          const int slice = kb / kd, kc = (kb - slice * kd) * kBlockK;
+          uint8_t* st = ring + stage * C::STAGE_BYTES;
+          mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+          tma_load_2d(st, &map_w3, &full[stage], kc, slice * args.e_pad + it.m * kBlockM, pol);
+          tma_load_2d(st + C::A_BYTES, &map_x, &full[stage], kc, it.tt * BN, pol);
+          ++issued;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      for (int s = 0; s < C::STAGES; ++s) {
+        if (issued <= s) break;
+        const long last = s + ((issued - 1 - s) / C::STAGES) * C::STAGES;
+        mbar_wait(&full[s], static_cast<uint32_t>((last / C::STAGES) & 1), kDrainLimitNs);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool issued_any = false, ok = true;
+      for (int item = blockIdx.x; ok && item < n_items && !*abort_flag; item += gridDim.x) {
+        const RItem it = decode_ritem(item, args.m_tiles, args.ksplit);
+        const int kb0 = it.ks * k_per, kb1 = min(k_total, kb0 + k_per);
+        if (!rwait(&acc_empty[acc], acc_phase ^ 1u, limit, abort_flag)) {
+          *abort_flag = 1;
+          atomicOr(args.err, kErrWaitTimeout);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!rwait(&full[stage], phase, limit, abort_flag)) {
+            *abort_flag = 1;
+            atomicOr(args.err, kErrWaitTimeout);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = smem_u32(ring + stage * C::STAGE_BYTES);
+          const uint64_t a = smem_desc_sw128(st);
+          const uint64_t b = smem_desc_sw128(st + C::A_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < kBlockK / 16; ++kk)
+            tc_mma_bf16(d_tmem, a + 2 * kk, b + 2 * kk, C::IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
+          issued_any = true;
+          tc_commit(&empty[stage]);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&acc_full[acc]);
+        if (++acc == C::NACC) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (issued_any) {
+        tc_commit(drain);
+        mbar_wait(drain, 0, kDrainLimitNs);
+      }
+    }
+  } else {
+    const int q = warp & 3;
+    const int e = q * 32 + lane;  // expert row within the m tile
+    uint32_t acc = 0, acc_phase = 0;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+      const RItem it = decode_ritem(item, args.m_tiles, args.ksplit);
+      const int t0 = it.tt * BN;
+      const int valid = min(BN, args.T - t0);
+      const int expert = it.m * kBlockM + e;
+      if (!__all_sync(0xffffffffu, rwait(&acc_full[acc], acc_phase, limit, abort_flag))) {
+        if (lane == 0) {
+          *abort_flag = 1;
+          atomicOr(args.err, kErrWaitTimeout);
+        }
+        break;
+      }
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      float* part = args.partial + static_cast<size_t>(it.ks) * args.T * args.E;
+#pragma unroll
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        if (c0 >= valid) break;
+        uint32_t v[16];
+        tmem_ld16(taddr + c0, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          if (c0 + c < valid && expert < args.E)
+            part[static_cast<size_t>(t0 + c0 + c) * args.E + expert] = __uint_as_float(v[c]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      if (++acc == C::NACC) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+constexpr int kMaxPerLane = kMaxExperts / 32;
+
+__device__ __forceinline__ bool better(float v, int e, float ov, int oe) { return v > ov || (v == ov && e < oe); }
+
+// One warp per token: logits = sum of the K-split partials (fixed order),
+// softmax, top-k (ties: lower index), gap, per-expert counts.
+__global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ partial, int ksplit, int T,
+                                                          int E, int k, int* __restrict__ idx,
+                                                          float* __restrict__ prob, float* __restrict__ gap,
+                                                          int* counts) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  float p[kMaxPerLane];
+  float zmax = -FLT_MAX;
+#pragma unroll
+  for (int i = 0; i < kMaxPerLane; ++i) {
+    const int e = lane + 32 * i;
+    float z = -FLT_MAX;
+    if (e < E) {
+      z = __ldg(partial + static_cast<size_t>(t) * E + e);
+      for (int s = 1; s < ksplit; ++s) z += __ldg(partial + (static_cast<size_t>(s) * T + t) * E + e);
+    }
+    p[i] = z;
+    zmax = fmaxf(zmax, z);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, off));
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < kMaxPerLane; ++i) {
+    const int e = lane + 32 * i;
+    p[i] = (e < E) ? expf(p[i] - zmax) : 0.f;
+    s += p[i];
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+#pragma unroll
+  for (int i = 0; i < kMaxPerLane; ++i) p[i] = p[i] / s;
+
+  uint32_t taken = 0;
+  float pk = 0.f;
+  for (int j = 0; j <= k; ++j) {
+    float bv = -1.f;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u) && p[i] > bv) {  // e grows with i: '>' keeps the lower index
+        bv = p[i];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+      if (better(ov, oe, bv, be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if (j < k) {
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      if (lane == 0) {
+        idx[static_cast<size_t>(t) * k + j] = be;
+        prob[static_cast<size_t>(t) * k + j] = bv;
+        atomicAdd(&counts[be], 1);
+      }
+      pk = bv;
+    } else if (gap != nullptr && lane == 0) {
+      gap[t] = (be == 0x7fffffff) ? __int_as_float(0x7f800000) : (pk - bv);
+    }
+  }
+}
+
+// W_r fp32 [E][d] -> three bf16 slices [3][e_pad][d]: hi = rn(w), mid = rn(w - hi),
+// lo = rn(w - hi - mid); rows E..e_pad-1 are zero.
+__global__ void split_router_kernel(const float* __restrict__ w, int E, int d, int e_pad, bf16* __restrict__ w3) {
+  const size_t n = static_cast<size_t>(e_pad) * d;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t row = i / d;
+    const float v = row < static_cast<size_t>(E) ? w[i] : 0.f;
+    const bf16 hi = __float2bfloat16_rn(v);
+    const float r1 = v - __bfloat162float(hi);
+    const bf16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);
+    w3[i] = hi;
+    w3[n + i] = mid;
+    w3[2 * n + i] = __float2bfloat16_rn(r2);
+  }
+}
+
+template <int BN>
+cudaError_t launch_rg(const CUtensorMap* map_w3, const CUtensorMap* map_x, const RouterGemmArgs& a, int grid,
+                      cudaStream_t stream) {
+  router_gemm_kernel<BN><<<grid, kThreads, RCfg<BN>::SMEM_BYTES, stream>>>(*map_w3, *map_x, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t router_gemm_prepare() {
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(router_gemm_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                RCfg<16>::SMEM_BYTES)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(router_gemm_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                RCfg<64>::SMEM_BYTES)) != cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(router_gemm_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              RCfg<128>::SMEM_BYTES);
+}
+
+cudaError_t launch_router_gemm(int tile_n, const CUtensorMap* map_w3, const CUtensorMap* map_x,
+                               const RouterGemmArgs& a, int num_sms, cudaStream_t stream) {
+  const int n_items = (a.T + tile_n - 1) / tile_n * a.m_tiles * a.ksplit;
+  const int grid = n_items < num_sms ? n_items : num_sms;
+  if (grid <= 0) return cudaSuccess;
+  switch (tile_n) {
+    case 16: return launch_rg<16>(map_w3, map_x, a, grid, stream);
+    case 64: return launch_rg<64>(map_w3, map_x, a, grid, stream);
+    case 128: return launch_rg<128>(map_w3, map_x, a, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_router_topk(const float* partial, int ksplit, int T, int E, int k, int* idx, float* prob,
+                               float* gap, int* counts, cudaStream_t stream) {
+  if (T <= 0) return cudaSuccess;
+  router_topk_kernel<<<(T + 7) / 8, 256, 0, stream>>>(partial, ksplit, T, E, k, idx, prob, gap, counts);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split_router(const float* w, int E, int d, int e_pad, bf16* w3, cudaStream_t stream) {
+  split_router_kernel<<<1024, 256, 0, stream>>>(w, E, d, e_pad, w3);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

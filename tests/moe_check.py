@@ -7,7 +7,12 @@ Tolerances (stated once, used by every parity test):
   under the oracle's probabilities to within NEAR_TIE, and the output is
   compared with the oracle recomputed for the GPU's choice;
 * probabilities: within the fp32 error bound derived in ``prob_bound``;
-* layer output: max |y_gpu - y_oracle| <= OUT_TOL * RMS(y_oracle).
+* layer output: |y_gpu - y_oracle| <= OUT_TOL * RMS(y_oracle) everywhere
+  when y is fp32.  When y is stored as bf16, the storage itself moves each
+  value by up to half a bf16 ulp of y (2^-9 relative), which past about
+  5 RMS alone exceeds 2e-2 RMS; that half ulp of y_oracle is added to the
+  bound element by element, so the check measures the computation and not
+  the output format.
 """
 from __future__ import annotations
 
@@ -31,12 +36,14 @@ def host_bits(inp: synth.LayerInputs):
 
 
 def prob_bound(x_bits, w_router, tokens, o_p):
-    """Per-token bound on |p_gpu - p_oracle| for an fp32 router.
+    """Per-token bound on |p_gpu - p_oracle| for the fp32-accurate router.
 
-    Each logit is a dot product of length d summed in fp32 (at most d terms
-    in one chain): its error is at most gamma_d * sum_i |x_i w_i|, with
-    gamma_n = n u / (1 - n u) and u = 2^-24.  log p_e = z_e - logsumexp(z)
-    then moves by at most 2 max_e dz_e.  The fp32 softmax adds: rounding of
+    Each logit is x . W_r computed as x . hi + x . mid + x . lo over three
+    bf16 slices of W_r (residual below 2^-24 |w|), every product exact, summed
+    in fp32: at most n = 3d terms, each addition off by at most 2u (u = 2^-24,
+    2u allowing accumulators that truncate), so |dz| <= gamma * sum_i |x_i w_i|
+    with gamma = 2 n u / (1 - 2 n u) + u.  log p_e = z_e - logsumexp(z) then
+    moves by at most 2 max_e dz_e.  The fp32 softmax adds: rounding of
     z - max (relative error of exp(.) up to range * u, range = max z - min z),
     expf itself (2 ulp), the E-term sum ((E - 1) u) and the division (u).
     """
@@ -45,7 +52,8 @@ def prob_bound(x_bits, w_router, tokens, o_p):
     d = xf.shape[1]
     E = wa.shape[0]
     u = 2.0 ** -24
-    gamma = d * u / (1 - d * u)
+    n = 3 * d
+    gamma = 2 * n * u / (1 - 2 * n * u) + u
     dz = gamma * (np.abs(xf) @ wa.T)  # [n_tok, E]
     p = o_p[tokens]
     with np.errstate(divide="ignore"):
@@ -56,20 +64,37 @@ def prob_bound(x_bits, w_router, tokens, o_p):
 
 
 def check_routing(x_bits, w_router, k, idx, prob, gap=None, perm=None, offsets=None, has_shared=True):
-    """Returns (near-tie token list, oracle idx)."""
+    """Returns (near-tie token list, oracle idx).
+
+    Near-ties come in two kinds.  Boundary: the oracle's gap between the
+    k-th and (k+1)-th probability is below NEAR_TIE, so the chosen set itself
+    is decided by rounding.  Order: two adjacent probabilities inside the
+    top-k are closer than NEAR_TIE, so only their order (the slot index j)
+    is decided by rounding.  Every other token must match the oracle's idx
+    bit for bit; order near-ties must match as a set, with an order that is
+    non-increasing under the oracle's probabilities to within NEAR_TIE;
+    boundary near-ties must pick k distinct experts none of which is more
+    than NEAR_TIE below the oracle's k-th probability.
+    """
     T = x_bits.shape[0]
     E = w_router.shape[0]
     o_idx, o_w, o_gap, o_p = oracle.route(x_bits, w_router, k, want_p=True)
-    near = np.nonzero(o_gap < NEAR_TIE)[0]
-    sure = o_gap >= NEAR_TIE
+    boundary = o_gap < NEAR_TIE
+    order = np.zeros(T, bool)
+    if k > 1:
+        order = (np.diff(o_w, axis=1) > -NEAR_TIE).any(axis=1) & ~boundary
+    sure = ~boundary & ~order
     assert idx.shape == (T, k)
     np.testing.assert_array_equal(idx[sure], o_idx[sure])
-    # every token: k distinct experts in range, ordered by oracle probability
     assert idx.min() >= 0 and idx.max() < E
-    for t in near:
+    for t in np.nonzero(order)[0]:
+        assert sorted(idx[t].tolist()) == sorted(o_idx[t].tolist())
+        assert np.all(np.diff(o_p[t, idx[t]]) <= NEAR_TIE)
+    for t in np.nonzero(boundary)[0]:
         assert len(set(idx[t].tolist())) == k
         kth = o_w[t, k - 1]
         assert np.all(o_p[t, idx[t]] >= kth - NEAR_TIE)
+    near = np.nonzero(~sure)[0]
     # probabilities of the chosen experts
     tok = np.arange(T)
     bound = prob_bound(x_bits, w_router, tok, o_p)
@@ -91,8 +116,16 @@ def check_routing(x_bits, w_router, k, idx, prob, gap=None, perm=None, offsets=N
     return near, o_idx
 
 
-def check_output(x_bits, w_router, wgu_bits, wd_bits, k, y_gpu, sel, tokens=None, has_shared=True, tol=OUT_TOL):
-    """Compares y_gpu (rows = tokens) with the oracle for the GPU's selection."""
+def half_ulp_bf16(v: np.ndarray) -> np.ndarray:
+    """Half a bf16 ulp at |v| (8 significand bits): 2^(floor(log2|v|) - 8)."""
+    _, e = np.frexp(np.abs(v))  # |v| = m 2^e, m in [0.5, 1)
+    return np.ldexp(1.0, e - 9)
+
+
+def check_output(x_bits, w_router, wgu_bits, wd_bits, k, y_gpu, sel, tokens=None, has_shared=True, tol=OUT_TOL,
+                 out_bf16=True):
+    """Compares y_gpu (rows = tokens) with the oracle for the GPU's selection;
+    returns max|err| / RMS."""
     T = x_bits.shape[0]
     if tokens is None:
         tokens = np.arange(T, dtype=np.int32)
@@ -100,10 +133,15 @@ def check_output(x_bits, w_router, wgu_bits, wd_bits, k, y_gpu, sel, tokens=None
                            sel=np.ascontiguousarray(sel[tokens]))
     y = y_gpu.astype(np.float64)
     assert np.all(np.isfinite(y))
-    err = np.abs(y - y_ref).max() if y.size else 0.0
-    rms = np.sqrt((y_ref ** 2).mean()) if y.size else 1.0
-    assert err <= tol * rms, f"max|err| {err:.4e} > {tol} * rms {rms:.4e} (ratio {err / rms:.3e})"
-    return err / rms
+    if not y.size:
+        return 0.0
+    diff = np.abs(y - y_ref)
+    rms = np.sqrt((y_ref ** 2).mean())
+    bound = tol * rms + (half_ulp_bf16(y_ref) if out_bf16 else 0.0)
+    worst = np.unravel_index(np.argmax(diff - bound), diff.shape)
+    assert np.all(diff <= bound), (f"|err| {diff[worst]:.4e} > bound {bound[worst] if out_bf16 else bound:.4e} "
+                                   f"at {worst} (y_ref {y_ref[worst]:.4e}, rms {rms:.4e})")
+    return diff.max() / rms
 
 
 def sample_tokens(T, idx, n_random, seed, extra=()):

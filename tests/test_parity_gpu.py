@@ -52,7 +52,7 @@ def run_and_check(inp, tiles=(0, 0), tokens=None, out_fp32=False, max_tokens=Non
     else:
         tokens = sample_tokens(shape.T, idx_h, tokens, seed=1, extra=near)
     ratio = check_output(xb, wr, wgu, wd, shape.k, y_h[tokens], idx_h, tokens=tokens,
-                         has_shared=shape.has_shared)
+                         has_shared=shape.has_shared, out_bf16=not out_fp32)
     layer.close()
     return ratio, len(near)
 
@@ -193,7 +193,7 @@ def flash_weights():
     del inp
 
 
-def flash_case(flash_weights, T, seed, n_sample=None, skew=None):
+def flash_case(flash_weights, T, seed, n_sample=None, skew=None, out_fp32=False):
     inp, (_, wr_h, wgu_h, wd_h) = flash_weights
     shape = synth.FLASH_DECODE.with_tokens(T)
     x = synth.make_tokens(shape, seed=seed, device=DEV, skew=skew)
@@ -206,7 +206,7 @@ def flash_case(flash_weights, T, seed, n_sample=None, skew=None):
         bias = torch.where(ranks > synth.SKEW_LIVE, torch.full_like(bias, -30.0), bias)
         wr[:, 0] = bias.to(torch.float32).to(DEV)
         wr_h2 = cpu(wr)
-    layer = binding.MoeLayer(wr, inp.w_gate_up, inp.w_down, shape.k, T)
+    layer = binding.MoeLayer(wr, inp.w_gate_up, inp.w_down, shape.k, T, out_fp32=out_fp32)
     idx, prob, perm, offsets, gap = layer.route(x)
     y = layer.forward(x)
     assert layer.check() == binding.MOE_OK
@@ -215,14 +215,15 @@ def flash_case(flash_weights, T, seed, n_sample=None, skew=None):
     near, _ = check_routing(xb, wr_h2, shape.k, idx_h, cpu(prob), cpu(gap), cpu(perm), cpu(offsets))
     tokens = np.arange(T, dtype=np.int32) if n_sample is None else sample_tokens(T, idx_h, n_sample, seed, near)
     y_h = cpu(y[torch.from_numpy(tokens).long().to(DEV)].float())
-    ratio = check_output(xb, wr_h2, wgu_h, wd_h, shape.k, y_h, idx_h, tokens=tokens)
+    ratio = check_output(xb, wr_h2, wgu_h, wd_h, shape.k, y_h, idx_h, tokens=tokens, out_bf16=not out_fp32)
     layer.close()
     return ratio
 
 
-def test_flash_decode_all_tokens(flash_weights):
+@pytest.mark.parametrize("out_fp32", [False, True])
+def test_flash_decode_all_tokens(flash_weights, out_fp32):
     # d=4096, 288 routed + 1 shared, top-8, width 1280, T=128 (decode batch)
-    flash_case(flash_weights, 128, seed=100)
+    flash_case(flash_weights, 128, seed=100, out_fp32=out_fp32)
 
 
 def test_flash_prefill_sampled(flash_weights):
@@ -231,9 +232,10 @@ def test_flash_prefill_sampled(flash_weights):
     flash_case(flash_weights, 8192, seed=101, n_sample=128)
 
 
-def test_flash_skewed_sampled(flash_weights):
+@pytest.mark.parametrize("out_fp32", [False, True])
+def test_flash_skewed_sampled(flash_weights, out_fp32):
     # Zipf-skewed routing, T=4096: hottest expert ~10x the mean, 40 unused.
-    flash_case(flash_weights, 4096, seed=102, n_sample=64, skew="zipf")
+    flash_case(flash_weights, 4096, seed=102, n_sample=64, skew="zipf", out_fp32=out_fp32)
 
 
 @pytest.mark.parametrize("T", [1, 8, 512])
