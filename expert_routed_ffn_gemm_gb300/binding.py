@@ -31,7 +31,7 @@ MOE_ERR_NO_DEVICE = 6
 
 EXPORTED = ("moe_init", "moe_route", "moe_forward", "moe_forward_host", "moe_check", "moe_set_wait_limit",
             "moe_profile_enable", "moe_profile_read", "moe_free", "moe_status_string",
-            "moe_selftest_wait_timeout")
+            "moe_selftest_wait_timeout", "moe_dispatch_noalloc")
 PROFILE_STAGES = ("routing", "dispatch", "gather", "gate_up_gemm", "down_gemm", "combine")
 
 
@@ -82,6 +82,7 @@ def load():
         lib.moe_status_string.argtypes = [i]
         lib.moe_status_string.restype = ctypes.c_char_p
         lib.moe_selftest_wait_timeout.argtypes = [ull, vp]
+        lib.moe_dispatch_noalloc.argtypes = [vp, i, i, i, i, vp, vp, vp]
         for name in EXPORTED:
             if name != "moe_status_string":
                 getattr(lib, name).restype = ctypes.c_int
@@ -165,6 +166,14 @@ def moe_free(h: int) -> None:
 
 def moe_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
     return int(load().moe_selftest_wait_timeout(int(limit_ns), _stream(stream)))
+
+
+def moe_dispatch_noalloc(idx, T: int, n_experts: int, top_k: int, has_shared: bool, offsets, perm,
+                         stream=None) -> None:
+    """Dispatch order from existing routing without any device allocation
+    (for callers that must not call cudaMalloc); see include/moe.h."""
+    _check(load().moe_dispatch_noalloc(_ptr(idx), int(T), int(n_experts), int(top_k), int(bool(has_shared)),
+                                       _ptr(offsets), _ptr(perm), _stream(stream)), "moe_dispatch_noalloc")
 
 
 class MoeLayer:

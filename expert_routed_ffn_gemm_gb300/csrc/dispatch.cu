@@ -7,6 +7,9 @@
 // combine gathers a token's rows back and sums them.  Both are deterministic:
 // dispatch orders rows inside an expert by token index with block-local ranks
 // (no order-dependent atomics), combine sums in a fixed order.
+#include <mutex>
+
+#include "../../include/moe.h"
 #include "kernels.cuh"
 
 namespace moe {
@@ -165,4 +168,122 @@ cudaError_t launch_combine(const float* yp, const int* inv, int T, int k, int d,
   return cudaGetLastError();
 }
 
+// ----------------------------------------------------------------------------
+// Allocation-free dispatch (moe_dispatch_noalloc in include/moe.h).
+//
+// Its only scratch, the per-expert row counts, lives in the file-scope device
+// array below instead of a handle's workspace, so the entry point needs no
+// moe_init and never allocates.  The array holds kNoAllocMaxExperts ints on
+// every GPU that loads this library, for the life of the process.
+namespace {
+
+constexpr int kNoAllocMaxExperts = kMaxExperts;
+__device__ __align__(256) int g_noalloc_counts[kNoAllocMaxExperts];
+
+// counts[e] = number of entries of idx equal to e; entries outside [0, E) are skipped.
+__global__ void noalloc_histogram_kernel(const int* __restrict__ idx, long long n, int E, int* counts) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int e = __ldg(idx + i);
+    if (e >= 0 && e < E) atomicAdd(&counts[e], 1);
+  }
+}
+
+// dispatch_kernel without the inverse permutation: block e < E writes the
+// stable expert-major positions of expert e's rows.
+__global__ void __launch_bounds__(kDispatchThreads) noalloc_dispatch_kernel(const int* __restrict__ idx,
+                                                                            const int* __restrict__ counts, int T,
+                                                                            int E, int k, int has_shared,
+                                                                            int* __restrict__ offsets,
+                                                                            int* __restrict__ perm) {
+  __shared__ int warp_sums[kDispatchThreads / 32];
+  const int e = blockIdx.x;
+  int part = 0;
+  for (int i = threadIdx.x; i < e; i += kDispatchThreads) part += counts[i];
+  int base_e;
+  block_exclusive_scan(part, warp_sums, &base_e);
+  if (e == 0) {
+    const int per = (E + kDispatchThreads - 1) / kDispatchThreads;
+    const int b = threadIdx.x * per;
+    int local = 0;
+    for (int i = b; i < min(E, b + per); ++i) local += counts[i];
+    int total;
+    int run = block_exclusive_scan(local, warp_sums, &total);
+    for (int i = b; i < min(E, b + per); ++i) {
+      offsets[i] = run;
+      run += counts[i];
+    }
+    if (threadIdx.x == 0) {
+      offsets[E] = total;
+      offsets[E + 1] = total + (has_shared ? T : 0);
+    }
+  }
+  int running = 0;
+  for (int t0 = 0; t0 < T; t0 += kDispatchThreads) {
+    const int t = t0 + threadIdx.x;
+    int jsel = -1;
+    if (t < T) {
+      const int* row = idx + static_cast<size_t>(t) * k;
+      for (int j = 0; j < k; ++j)
+        if (__ldg(row + j) == e) jsel = j;
+    }
+    int chunk_total;
+    const int r = block_exclusive_scan(jsel >= 0 ? 1 : 0, warp_sums, &chunk_total);
+    if (jsel >= 0) perm[base_e + running + r] = t * k + jsel;
+    running += chunk_total;
+  }
+}
+
+// Device address of g_noalloc_counts, looked up once per device.
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+int* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+cudaError_t noalloc_counts(int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_counts);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = static_cast<int*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
 }  // namespace moe
+
+extern "C" int moe_dispatch_noalloc(const int* idx, int T, int n_experts, int top_k, int has_shared, int* offsets,
+                                    int* perm, void* stream) {
+  if (T < 0 || n_experts <= 0 || top_k <= 0 || top_k > n_experts || (has_shared != 0 && has_shared != 1))
+    return MOE_ERR_INVALID_ARG;
+  if (n_experts > moe::kNoAllocMaxExperts || top_k > moe::kMaxTopK) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(top_k + 1) * T >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
+  if (offsets == nullptr || (T > 0 && (idx == nullptr || perm == nullptr))) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(idx) | reinterpret_cast<uintptr_t>(offsets) |
+       reinterpret_cast<uintptr_t>(perm)) & 3u)
+    return MOE_ERR_INVALID_ARG;
+  int* counts = nullptr;
+  if (moe::noalloc_counts(&counts) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the array keeps the previous call's counts: clear it first
+  if (cudaMemsetAsync(counts, 0, sizeof(int) * n_experts, s) != cudaSuccess) return MOE_ERR_CUDA;
+  const long long n = static_cast<long long>(T) * top_k;
+  if (n > 0) {
+    const int blocks = static_cast<int>((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);
+    moe::noalloc_histogram_kernel<<<blocks, 256, 0, s>>>(idx, n, n_experts, counts);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  moe::noalloc_dispatch_kernel<<<n_experts, moe::kDispatchThreads, 0, s>>>(idx, counts, T, n_experts, top_k,
+                                                                           has_shared, offsets, perm);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

@@ -152,6 +152,32 @@ int moe_profile_enable(moe_handle* h, int enable);
  */
 int moe_profile_read(moe_handle* h, float* ms, int* n_calls);
 
+/*
+ * moe_dispatch_noalloc — the dispatch step alone (offsets and perm, exactly as
+ * moe_route writes them) from routing the caller already has, without a handle
+ * and without allocating any device memory.  The paper has no counterpart for
+ * this entry point; it exists for callers that cannot call cudaMalloc: code
+ * whose device memory is owned by another allocator or memory pool that must
+ * not be bypassed, and latency-critical loops that cannot afford cudaMalloc's
+ * implicit device synchronisation.
+ *   idx      int [T][k] device: expert ids in [0, n_experts), distinct within
+ *            a row (ids outside the range are ignored: their perm slots are
+ *            left unwritten)
+ *   offsets  int [n_experts+2] device (output, as in moe_route)
+ *   perm     int [T*k] device (output, as in moe_route)
+ * Its scratch (per-expert row counts) is a fixed array of 512 ints in the
+ * library's own device memory, present on every GPU that loads the library
+ * until the process exits.  Limits: n_experts <= 512 and top_k <= 32 (beyond
+ * them: MOE_ERR_UNSUPPORTED); 4-byte aligned pointers.  The array is cleared at
+ * the start of every call, but it is shared: calls whose work overlaps on the
+ * GPU (different streams, or different host threads on one device) race and
+ * give wrong results; order them.  The first call on each device looks the
+ * array's address up (with that device current), so make that first call
+ * before any stream capture.  Asynchronous on `stream`.
+ */
+int moe_dispatch_noalloc(const int* idx, int T, int n_experts, int top_k, int has_shared, int* offsets, int* perm,
+                         void* stream);
+
 /* Frees the handle and its workspace (synchronises the device first). */
 int moe_free(moe_handle* h);
 
