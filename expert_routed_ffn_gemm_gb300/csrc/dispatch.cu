@@ -109,8 +109,9 @@ __global__ void __launch_bounds__(256) gather_kernel(const bf16* __restrict__ x,
 }
 
 // One block per token: y[t] = Yp[inv[t*k+0]] + ... + Yp[inv[t*k+k-1]] + Yp[T*k+t],
-// summed in fp32 in that order (Yp rows are fp32).
-__global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ yp, const int* __restrict__ inv,
+// summed in fp32 in that order (Yp rows are fp32).  d/8 threads (<= 1024): one
+// 8-element chunk each, so every load of a token is in flight at once.
+__global__ void __launch_bounds__(1024) combine_kernel(const float* __restrict__ yp, const int* __restrict__ inv,
                                                       int T, int k, int d, int has_shared, void* __restrict__ y,
                                                       int out_fp32) {
   const int t = blockIdx.x;
@@ -164,7 +165,9 @@ cudaError_t launch_gather(const bf16* x, const int* perm, int T, int k, int d, i
 cudaError_t launch_combine(const float* yp, const int* inv, int T, int k, int d, int has_shared, void* y,
                            int out_fp32, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
-  combine_kernel<<<T, 128, 0, stream>>>(yp, inv, T, k, d, has_shared, y, out_fp32);
+  const int chunks = d / 8;
+  const int threads = chunks > 1024 ? 1024 : (chunks < 32 ? 32 : chunks);
+  combine_kernel<<<T, threads, 0, stream>>>(yp, inv, T, k, d, has_shared, y, out_fp32);
   return cudaGetLastError();
 }
 

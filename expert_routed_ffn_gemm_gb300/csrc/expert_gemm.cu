@@ -189,13 +189,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_w = policy_evict_first();   // weights: streamed once
       const uint64_t pol_act = policy_evict_last();  // token rows: re-read by the other weight tiles
       const int k_steps = args.K / kBlockK;
+      // K3: gate rows 64m.. of group g, then the up rows F + 64m..; K4: rows 128m..
+      auto weight_row = [&](const Item& it) {
+        return it.g * args.rows_per_group + it.m * (GATEUP ? kBlockM / 2 : kBlockM);
+      };
       uint32_t stage = 0, phase = 0;
       long issued = 0;
       bool ok = true;
       for (int item = blockIdx.x; ok && item < n_items && !*abort_flag; item += gridDim.x) {
         const Item it = decode_item(item, args.m_tiles, tile_start, G);
-        // K3: gate rows 64m.. of group g, then the up rows F + 64m..; K4: rows 128m..
-        const int row_w = it.g * args.rows_per_group + it.m * (GATEUP ? kBlockM / 2 : kBlockM);
+        const int row_w = weight_row(it);
         const int row_act = __ldg(args.offsets + it.g) + it.n * BN;
         for (int kb = 0; kb < k_steps; ++kb) {
           if (!wait_or_abort(&empty[stage], phase ^ 1u, limit, abort_flag)) {

@@ -154,7 +154,10 @@ int enqueue_router(moe_handle* h, const void* x, int T, int* idx, float* prob, f
   const int bn = T <= 32 ? 16 : (T <= 1024 ? 64 : 128);
   const int n_tt = (T + bn - 1) / bn;
   const int k_total = 3 * c.d_model / moe::kBlockK;
-  int ks = h->num_sms / (n_tt * h->router_m_tiles);
+  // K splits: about four waves of work items over the SMs (balances the last
+  // wave at large T, fills the GPU at small T)
+  const int base_items = n_tt * h->router_m_tiles;
+  int ks = (4 * h->num_sms + base_items / 2) / base_items;
   ks = ks < 1 ? 1 : (ks > moe::kMaxKSplit ? moe::kMaxKSplit : ks);
   ks = ks > k_total ? k_total : ks;
   while (ks > 1 && static_cast<long long>(ks) * T > h->partial_rows) --ks;

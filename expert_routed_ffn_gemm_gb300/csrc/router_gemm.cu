@@ -254,25 +254,31 @@ __device__ __forceinline__ bool better(float v, int e, float ov, int oe) { retur
 
 // One warp per token: logits = sum of the K-split partials (fixed order),
 // softmax, top-k (ties: lower index), gap, per-expert counts.
-__global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ partial, int ksplit, int T,
-                                                          int E, int k, int* __restrict__ idx,
-                                                          float* __restrict__ prob, float* __restrict__ gap,
-                                                          int* counts) {
+__global__ void __launch_bounds__(64) router_topk_kernel(const float* __restrict__ partial, int ksplit, int T,
+                                                         int E, int k, int* __restrict__ idx,
+                                                         float* __restrict__ prob, float* __restrict__ gap,
+                                                         int* counts) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
   float p[kMaxPerLane];
+#pragma unroll
+  for (int i = 0; i < kMaxPerLane; ++i) p[i] = 0.f;
+  // split by split, all of a lane's experts at once (independent loads in flight)
+#pragma unroll 4
+  for (int s = 0; s < ksplit; ++s) {
+    const float* row = partial + (static_cast<size_t>(s) * T + t) * E;
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) p[i] += __ldg(row + e);
+    }
+  }
   float zmax = -FLT_MAX;
 #pragma unroll
   for (int i = 0; i < kMaxPerLane; ++i) {
     const int e = lane + 32 * i;
-    float z = -FLT_MAX;
-    if (e < E) {
-      z = __ldg(partial + static_cast<size_t>(t) * E + e);
-      for (int s = 1; s < ksplit; ++s) z += __ldg(partial + (static_cast<size_t>(s) * T + t) * E + e);
-    }
-    p[i] = z;
-    zmax = fmaxf(zmax, z);
+    if (e < E) zmax = fmaxf(zmax, p[i]);
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, off));
@@ -379,7 +385,7 @@ cudaError_t launch_router_gemm(int tile_n, const CUtensorMap* map_w3, const CUte
 cudaError_t launch_router_topk(const float* partial, int ksplit, int T, int E, int k, int* idx, float* prob,
                                float* gap, int* counts, cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
-  router_topk_kernel<<<(T + 7) / 8, 256, 0, stream>>>(partial, ksplit, T, E, k, idx, prob, gap, counts);
+  router_topk_kernel<<<(T + 1) / 2, 64, 0, stream>>>(partial, ksplit, T, E, k, idx, prob, gap, counts);
   return cudaGetLastError();
 }
 
