@@ -29,17 +29,14 @@
 // counts come from the device-resident dispatch offsets: no host round trip.
 // Every wait is bounded (wait_limit_ns); on timeout the kernel records an error,
 // drains the copies and MMAs it started, frees tensor memory and returns.
-#include "kernels.cuh"
-#include "ptx.cuh"
+#include "gemm_common.cuh"
 
 namespace moe {
 namespace {
 
+using namespace gemm;
+
 constexpr int kThreads = 192;
-constexpr int kEpilogueWarp0 = 2;
-constexpr int kMaxGroups = kMaxExperts + 1;
-constexpr uint64_t kDrainLimitNs = 2000000000ull;
-constexpr uint32_t kEpilogueBar = 1;  // named barrier of the 4 epilogue warps
 
 template <bool GATEUP, int BN>
 struct Cfg {
@@ -63,53 +60,6 @@ struct Cfg {
   static_assert(SMEM_BYTES <= 232448, "exceeds shared memory per block");
   static constexpr uint32_t IDESC = idesc_bf16_f32(kBlockM, BN);
 };
-
-struct Item {
-  int g, n, m;
-};
-
-// item -> (group, token tile inside the group, weight tile); tile_start[g] is
-// the first token tile of group g (prefix over groups of ceil(rows/BN)).
-__device__ __forceinline__ Item decode_item(int item, int m_tiles, const int* tile_start, int G) {
-  Item it;
-  const int tile = item / m_tiles;
-  it.m = item - tile * m_tiles;
-  int lo = 0, hi = G - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (tile_start[mid] <= tile)
-      lo = mid;
-    else
-      hi = mid - 1;
-  }
-  it.g = lo;
-  it.n = tile - tile_start[lo];
-  return it;
-}
-
-__device__ __forceinline__ void record_abort(volatile int* abort_flag, uint32_t* err) {
-  *abort_flag = 1;
-  atomicOr(err, kErrWaitTimeout);
-}
-
-// Bounded wait that also gives up as soon as another role has aborted.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
-                                              volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  uint32_t spins = 0;
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((++spins & 15u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > limit_ns) return false;
-    }
-  }
-}
-
-__device__ __forceinline__ float silu_mul(float g, float u) {
-  return g * __frcp_rn(1.0f + __expf(-g)) * u;
-}
 
 template <bool GATEUP, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -153,29 +103,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_holder, C::TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == kEpilogueWarp0) {
-    // tile_start[0..G]: each lane scans a contiguous run of groups
-    const int per = (G + 31) / 32;
-    const int b = lane * per, e = min(G, b + per);
-    int local = 0;
-    for (int g = b; g < e; ++g) {
-      const int rows = __ldg(args.offsets + g + 1) - __ldg(args.offsets + g);
-      local += (rows + BN - 1) / BN;
-    }
-    int incl = local;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += o;
-    }
-    int run = incl - local;
-    for (int g = b; g < e; ++g) {
-      tile_start[g] = run;
-      const int rows = __ldg(args.offsets + g + 1) - __ldg(args.offsets + g);
-      run += (rows + BN - 1) / BN;
-    }
-    if (lane == 31) tile_start[G] = incl;
-  }
+  if (warp == kEpilogueWarp0) build_tile_start(args.offsets, G, BN, tile_start, lane);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -283,84 +211,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int g_rows = __ldg(args.offsets + it.g + 1) - g_row0;
       const int row0 = g_row0 + it.n * BN;
       const int valid = min(BN, g_rows - it.n * BN);
-      // K4: the gate weight of every column of this tile, lane l holding
-      // columns l, l+32, ... (loaded while the MMAs still run).
-      constexpr int kWRegs = (BN + 31) / 32;
-      float wreg[kWRegs];
-      if (!GATEUP) {
-#pragma unroll
-        for (int i = 0; i < kWRegs; ++i) {
-          const int c = i * 32 + lane;
-          const int pos = row0 + c;
-          wreg[i] = (c < valid) ? ((pos < args.Tk) ? __ldg(args.prob + __ldg(args.perm + pos)) : 1.0f) : 0.0f;
-        }
-      }
-      // One decision for all four epilogue warps (they meet at named barriers).
-      const bool ok = __all_sync(0xffffffffu, wait_or_abort(&acc_full[acc], acc_phase, limit, abort_flag));
-      if (lane == 0) s_ok[it_par * 4 + q] = ok ? 1 : 0;
-      named_bar_sync(kEpilogueBar, 128);
-      const bool all_ok = s_ok[it_par * 4 + 0] && s_ok[it_par * 4 + 1] && s_ok[it_par * 4 + 2] &&
-                          s_ok[it_par * 4 + 3];
-      it_par ^= 1u;
-      if (!all_ok) {
-        if (lane == 0 && !ok) record_abort(abort_flag, args.err);
-        break;
-      }
+      // K4: the gate weight of every column, loaded while the MMAs still run
+      float wreg[(BN + 31) / 32];
+      if (!GATEUP) load_gate_weights<BN>(wreg, row0, valid, lane, args.perm, args.prob, args.Tk);
+      if (!epilogue_wait(&acc_full[acc], acc_phase, limit, abort_flag, s_ok, it_par, q, lane, args.err)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       if (GATEUP) {
         // rows 0..63: gate of feature 64m + row; rows 64..127: up of feature 64m + row - 64
-        const bool is_gate = q < 2;
-        const int fl = row & 63;
-        const int feat = it.m * (kBlockM / 2) + fl;
-        bf16* H = static_cast<bf16*>(args.out);
-#pragma unroll
-        for (int c0 = 0; c0 < BN; c0 += 16) {
-          if (c0 >= valid) break;
-          uint32_t v[16];
-          tmem_ld16(taddr + c0, v);
-          tmem_ld_wait();
-          // gate threads keep columns 0..7 of the chunk and hand over 8..15;
-          // up threads keep 8..15 and hand over 0..7
-          float* mine_out = xchg + ((chunk_par * 2 + (is_gate ? 1 : 0)) * 64 + fl) * 8;
-          const float* peer_in = xchg + ((chunk_par * 2 + (is_gate ? 0 : 1)) * 64 + fl) * 8;
-          float give[8], keep[8];  // compile-time register indices only
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            give[c] = __uint_as_float(is_gate ? v[8 + c] : v[c]);
-            keep[c] = __uint_as_float(is_gate ? v[c] : v[8 + c]);
-          }
-          reinterpret_cast<float4*>(mine_out)[0] = make_float4(give[0], give[1], give[2], give[3]);
-          reinterpret_cast<float4*>(mine_out)[1] = make_float4(give[4], give[5], give[6], give[7]);
-          named_bar_sync(kEpilogueBar, 128);
-          const float4 p0 = reinterpret_cast<const float4*>(peer_in)[0];
-          const float4 p1 = reinterpret_cast<const float4*>(peer_in)[1];
-          const float peer[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-          const int col0 = c0 + (is_gate ? 0 : 8);
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const float h = is_gate ? silu_mul(keep[c], peer[c]) : silu_mul(peer[c], keep[c]);
-            if (col0 + c < valid)
-              H[static_cast<size_t>(row0 + col0 + c) * args.out_ld + feat] = __float2bfloat16_rn(h);
-          }
-          chunk_par ^= 1u;
-        }
+        epilogue_gateup<BN>(taddr, row, it.m * (kBlockM / 2), row0, valid, static_cast<bf16*>(args.out),
+                            args.out_ld, xchg, chunk_par);
       } else {
-        const int feat = it.m * kBlockM + row;
-        float* Y = static_cast<float*>(args.out);
-#pragma unroll
-        for (int c0 = 0; c0 < BN; c0 += 16) {
-          if (c0 >= valid) break;
-          uint32_t v[16];
-          tmem_ld16(taddr + c0, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const int col = c0 + c;
-            const float w = __shfl_sync(0xffffffffu, wreg[col >> 5], col & 31);
-            if (col < valid) Y[static_cast<size_t>(row0 + col) * args.out_ld + feat] = w * __uint_as_float(v[c]);
-          }
-        }
+        epilogue_down<BN>(taddr, it.m * kBlockM + row, row0, valid, wreg, static_cast<float*>(args.out),
+                          args.out_ld);
       }
       tc_fence_before();
       __syncwarp();

@@ -1,0 +1,178 @@
+// Pieces shared by the one-CTA and the CTA-pair grouped expert GEMMs:
+// work-item decoding over the groups' token tiles, bounded waits with a
+// CTA-wide abort flag, and the two epilogues (SiLU gate for gate/up, gate
+// weight scale for down) that read one TMEM accumulator of BN columns.
+#pragma once
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace gemm {
+
+constexpr int kEpilogueWarp0 = 2;  // warps 2..5 are the epilogue
+constexpr int kMaxGroups = kMaxExperts + 1;
+constexpr uint64_t kDrainLimitNs = 2000000000ull;
+constexpr uint32_t kEpilogueBar = 1;  // named barrier of the 4 epilogue warps
+
+struct Item {
+  int g, n, m;
+};
+
+// item -> (group, token tile inside the group, weight tile); tile_start[g] is
+// the first token tile of group g (prefix over groups of ceil(rows/tile)).
+__device__ __forceinline__ Item decode_item(int item, int m_tiles, const int* tile_start, int G) {
+  Item it;
+  const int tile = item / m_tiles;
+  it.m = item - tile * m_tiles;
+  int lo = 0, hi = G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tile_start[mid] <= tile)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  it.g = lo;
+  it.n = tile - tile_start[lo];
+  return it;
+}
+
+// tile_start[0..G] from the dispatch offsets, by one warp: each lane scans a
+// contiguous run of groups, then a warp prefix sum.
+__device__ __forceinline__ void build_tile_start(const int* offsets, int G, int tile, int* tile_start, int lane) {
+  const int per = (G + 31) / 32;
+  const int b = lane * per, e = min(G, b + per);
+  int local = 0;
+  for (int g = b; g < e; ++g) {
+    const int rows = __ldg(offsets + g + 1) - __ldg(offsets + g);
+    local += (rows + tile - 1) / tile;
+  }
+  int incl = local;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  int run = incl - local;
+  for (int g = b; g < e; ++g) {
+    tile_start[g] = run;
+    const int rows = __ldg(offsets + g + 1) - __ldg(offsets + g);
+    run += (rows + tile - 1) / tile;
+  }
+  if (lane == 31) tile_start[G] = incl;
+}
+
+__device__ __forceinline__ void record_abort(volatile int* abort_flag, uint32_t* err) {
+  *abort_flag = 1;
+  atomicOr(err, kErrWaitTimeout);
+}
+
+// Bounded wait that also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
+                                              volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t spins = 0;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((++spins & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return g * __frcp_rn(1.0f + __expf(-g)) * u;
+}
+
+// The epilogue warps' common wait on an accumulator: every warp waits, then
+// all four take one decision (they meet at named barriers afterwards).
+// s_ok is [2][4] ints, it_par alternates per item.  Returns false to abort.
+__device__ __forceinline__ bool epilogue_wait(uint64_t* acc_full, uint32_t parity, uint64_t limit,
+                                              volatile int* abort_flag, volatile int* s_ok, uint32_t& it_par,
+                                              int q, int lane, uint32_t* err) {
+  const bool ok = __all_sync(0xffffffffu, wait_or_abort(acc_full, parity, limit, abort_flag));
+  if (lane == 0) s_ok[it_par * 4 + q] = ok ? 1 : 0;
+  named_bar_sync(kEpilogueBar, 128);
+  const bool all_ok = s_ok[it_par * 4 + 0] && s_ok[it_par * 4 + 1] && s_ok[it_par * 4 + 2] && s_ok[it_par * 4 + 3];
+  it_par ^= 1u;
+  if (!all_ok && lane == 0 && !ok) record_abort(abort_flag, err);
+  return all_ok;
+}
+
+// K3 epilogue over the `valid` columns of a BN-column accumulator whose TMEM
+// rows 0..63 hold gate values and rows 64..127 the up values of the same 64
+// features.  Gate-row threads keep columns 0..7 of each 16-column chunk and
+// hand 8..15 to their up-row partner through xchg ([2][2][64][8] fp32), which
+// hands back 0..7; H[row0 + col][feat_base + (row & 63)] = silu(g) * u.
+template <int BN>
+__device__ __forceinline__ void epilogue_gateup(uint32_t taddr, int row, int feat_base, int row0, int valid,
+                                                bf16* H, int ldh, float* xchg, uint32_t& chunk_par) {
+  const bool is_gate = row < 64;
+  const int fl = row & 63;
+  const int feat = feat_base + fl;
+#pragma unroll
+  for (int c0 = 0; c0 < BN; c0 += 16) {
+    if (c0 >= valid) break;
+    uint32_t v[16];
+    tmem_ld16(taddr + c0, v);
+    tmem_ld_wait();
+    float* mine_out = xchg + ((chunk_par * 2 + (is_gate ? 1 : 0)) * 64 + fl) * 8;
+    const float* peer_in = xchg + ((chunk_par * 2 + (is_gate ? 0 : 1)) * 64 + fl) * 8;
+    float give[8], keep[8];  // compile-time register indices only
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      give[c] = __uint_as_float(is_gate ? v[8 + c] : v[c]);
+      keep[c] = __uint_as_float(is_gate ? v[c] : v[8 + c]);
+    }
+    reinterpret_cast<float4*>(mine_out)[0] = make_float4(give[0], give[1], give[2], give[3]);
+    reinterpret_cast<float4*>(mine_out)[1] = make_float4(give[4], give[5], give[6], give[7]);
+    named_bar_sync(kEpilogueBar, 128);
+    const float4 p0 = reinterpret_cast<const float4*>(peer_in)[0];
+    const float4 p1 = reinterpret_cast<const float4*>(peer_in)[1];
+    const float peer[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+    const int col0 = c0 + (is_gate ? 0 : 8);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const float h = is_gate ? silu_mul(keep[c], peer[c]) : silu_mul(peer[c], keep[c]);
+      if (col0 + c < valid) H[static_cast<size_t>(row0 + col0 + c) * ldh + feat] = __float2bfloat16_rn(h);
+    }
+    chunk_par ^= 1u;
+  }
+}
+
+// K4: the gate weight of every column of a tile, lane l holding columns
+// l, l+32, ... (rows at dispatch positions >= Tk are shared-expert rows: 1).
+template <int BN>
+__device__ __forceinline__ void load_gate_weights(float (&wreg)[(BN + 31) / 32], int row0, int valid, int lane,
+                                                  const int* perm, const float* prob, int Tk) {
+#pragma unroll
+  for (int i = 0; i < (BN + 31) / 32; ++i) {
+    const int c = i * 32 + lane;
+    const int pos = row0 + c;
+    wreg[i] = (c < valid) ? ((pos < Tk) ? __ldg(prob + __ldg(perm + pos)) : 1.0f) : 0.0f;
+  }
+}
+
+// K4 epilogue: Y[row0 + col][feat] = w_col * acc[col] for the valid columns.
+template <int BN>
+__device__ __forceinline__ void epilogue_down(uint32_t taddr, int feat, int row0, int valid,
+                                              const float (&wreg)[(BN + 31) / 32], float* Y, int ldy) {
+#pragma unroll
+  for (int c0 = 0; c0 < BN; c0 += 16) {
+    if (c0 >= valid) break;
+    uint32_t v[16];
+    tmem_ld16(taddr + c0, v);
+    tmem_ld_wait();
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const int col = c0 + c;
+      const float w = __shfl_sync(0xffffffffu, wreg[col >> 5], col & 31);
+      if (col < valid) Y[static_cast<size_t>(row0 + col) * ldy + feat] = w * __uint_as_float(v[c]);
+    }
+  }
+}
+
+}  // namespace gemm
+}  // namespace moe

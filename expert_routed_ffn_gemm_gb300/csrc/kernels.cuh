@@ -73,6 +73,13 @@ cudaError_t launch_expert_gemm(bool gateup, int tile_n, const CUtensorMap* map_w
 // on the current device (once per device, before the first launch).
 cudaError_t expert_gemm_prepare();
 
+// K3/K4 for 256-row token tiles on CTA pairs (clusters of 2, grid = even
+// number of SMs).  a.m_tiles must count pair tiles: F/128 (gate/up, map_w box
+// 64 rows) or d/256 (down, map_w box 128 rows); map_act box: 128 rows.
+cudaError_t launch_expert_gemm_pair(bool gateup, const CUtensorMap* map_w, const CUtensorMap* map_act,
+                                    const GemmArgs& a, int num_sms, cudaStream_t stream);
+cudaError_t expert_gemm_pair_prepare();
+
 // K5: y[t] = sum_j Yp[inv[t*k+j]] + Yp[T*k + t], fp32 in fixed order.
 cudaError_t launch_combine(const float* yp, const int* inv, int T, int k, int d, int has_shared, void* y,
                            int out_fp32, cudaStream_t stream);

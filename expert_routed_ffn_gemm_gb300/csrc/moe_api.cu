@@ -32,6 +32,7 @@ struct moe_handle {
   int G;
   int tile_gateup;  // 0 = choose per call
   int tile_down;
+  bool use_pairs;   // 256-row token tiles on CTA pairs (MOE_PAIR_TILES=0 turns it off)
   unsigned long long wait_limit_ns;
   int router_m_tiles;      // ceil(E / 128)
   long long partial_rows;  // capacity of `partial` in (split, token) rows
@@ -232,22 +233,33 @@ int enqueue_forward(moe_handle* h, const void* x, int T, void* y, cudaStream_t s
   a.F = c.ffn_width;
   a.Tk = T * c.top_k;
 
+  // 256-row token tiles run on CTA pairs (M = 256 weight rows per pair)
+  const int i128 = tile_index(128);
+  const bool pair1 = h->use_pairs && bn1 == 256;
+  const bool pair2 = h->use_pairs && bn2 == 256 && c.d_model % 256 == 0;
+
   a.out = h->hbuf;
   a.K = c.d_model;
   a.rows_per_group = 2 * c.ffn_width;
-  a.m_tiles = c.ffn_width / (moe::kBlockM / 2);
+  a.m_tiles = pair1 ? c.ffn_width / moe::kBlockM : c.ffn_width / (moe::kBlockM / 2);
   a.out_ld = c.ffn_width;
   MOE_MARK(3);
   const int i1 = tile_index(bn1), i2 = tile_index(bn2);
-  MOE_CUDA(moe::launch_expert_gemm(true, bn1, &h->map_wgu, &h->map_xp[i1], a, h->num_sms, s));
+  if (pair1)
+    MOE_CUDA(moe::launch_expert_gemm_pair(true, &h->map_wgu, &h->map_xp[i128], a, h->num_sms, s));
+  else
+    MOE_CUDA(moe::launch_expert_gemm(true, bn1, &h->map_wgu, &h->map_xp[i1], a, h->num_sms, s));
   MOE_MARK(4);
 
   a.out = h->xpyp;
   a.K = c.ffn_width;
   a.rows_per_group = c.d_model;
-  a.m_tiles = c.d_model / moe::kBlockM;
+  a.m_tiles = pair2 ? c.d_model / (2 * moe::kBlockM) : c.d_model / moe::kBlockM;
   a.out_ld = c.d_model;
-  MOE_CUDA(moe::launch_expert_gemm(false, bn2, &h->map_wd, &h->map_h[i2], a, h->num_sms, s));
+  if (pair2)
+    MOE_CUDA(moe::launch_expert_gemm_pair(false, &h->map_wd, &h->map_h[i128], a, h->num_sms, s));
+  else
+    MOE_CUDA(moe::launch_expert_gemm(false, bn2, &h->map_wd, &h->map_h[i2], a, h->num_sms, s));
   MOE_MARK(5);
   MOE_CUDA(moe::launch_combine(static_cast<const float*>(h->xpyp), h->inv, T, c.top_k, c.d_model, c.has_shared,
                                y, c.out_fp32, s));
@@ -307,7 +319,9 @@ int moe_init(const moe_config* cfg, const moe_weights* w, moe_handle** out) {
   if (!is_device_ptr(w->w_router) || !is_device_ptr(w->w_gate_up) || !is_device_ptr(w->w_down))
     return MOE_ERR_INVALID_ARG;
   if (!load_encode()) return MOE_ERR_CUDA;
-  if (moe::expert_gemm_prepare() != cudaSuccess || moe::router_gemm_prepare() != cudaSuccess) return MOE_ERR_CUDA;
+  if (moe::expert_gemm_prepare() != cudaSuccess || moe::expert_gemm_pair_prepare() != cudaSuccess ||
+      moe::router_gemm_prepare() != cudaSuccess)
+    return MOE_ERR_CUDA;
 
   moe_handle* h = new (std::nothrow) moe_handle();
   if (h == nullptr) return MOE_ERR_CUDA;
@@ -318,6 +332,10 @@ int moe_init(const moe_config* cfg, const moe_weights* w, moe_handle** out) {
   h->G = c.n_experts + c.has_shared;
   h->tile_gateup = tile_from_env("MOE_TILE_N_GATEUP");
   h->tile_down = tile_from_env("MOE_TILE_N_DOWN");
+  {
+    const char* v = std::getenv("MOE_PAIR_TILES");
+    h->use_pairs = !(v && v[0] == '0');
+  }
   h->wait_limit_ns = kDefaultWaitNs;
   h->router_m_tiles = (c.n_experts + moe::kBlockM - 1) / moe::kBlockM;
 
