@@ -10,5 +10,6 @@ from .oracle import (  # noqa: F401
     expert_ffn,
     forward,
     max_threads,
+    route_stats,
     route,
 )

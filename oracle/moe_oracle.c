@@ -198,10 +198,12 @@ static void expert_ffn_acc(const uint16_t* x_t, const uint16_t* w_gu, const uint
  * the k experts per listed token ([n_tokens][k]) instead of the oracle's own
  * top-k; the weights are still the oracle's probabilities of those experts.
  * w_gate_up / w_down hold E + has_shared groups.  y is [n_tokens][d].
+ * renormalize != 0 (the per-call variant of §8.2 with a renormalised
+ * top-k): the k weights are divided by their sum, summed in slot order.
  */
-int oracle_forward(const uint16_t* x, const float* w_router, const uint16_t* w_gate_up, const uint16_t* w_down,
-                   int T, int d, int E, int k, int F, int has_shared, const int* tokens, int n_tokens,
-                   const int* sel, double* y, int n_threads) {
+int oracle_forward_ex(const uint16_t* x, const float* w_router, const uint16_t* w_gate_up, const uint16_t* w_down,
+                      int T, int d, int E, int k, int F, int has_shared, const int* tokens, int n_tokens,
+                      const int* sel, int renormalize, double* y, int n_threads) {
   if (T < 0 || d <= 0 || E <= 0 || k <= 0 || k > E || F <= 0 || n_tokens < 0) return -1;
   if (!x || !w_router || !w_gate_up || !w_down || !tokens || !y) return -1;
   for (int i = 0; i < n_tokens; ++i)
@@ -227,6 +229,11 @@ int oracle_forward(const uint16_t* x, const float* w_router, const uint16_t* w_g
     } else {
       topk_token(p, E, k, ids, w, NULL);
     }
+    if (renormalize) {
+      double sum = 0.0;
+      for (int j = 0; j < k; ++j) sum += w[j];
+      for (int j = 0; j < k; ++j) w[j] /= sum;
+    }
     double* acc = y + (size_t)i * d;
     for (int o = 0; o < d; ++o) acc[o] = 0.0;
     for (int j = 0; j < k; ++j)
@@ -236,6 +243,65 @@ int oracle_forward(const uint16_t* x, const float* w_router, const uint16_t* w_g
     free(p); free(h); free(ids); free(w);
   }
   return bad ? -1 : 0;
+}
+
+/* oracle_forward_ex with the raw softmax weights (the §3.2.2 reading). */
+int oracle_forward(const uint16_t* x, const float* w_router, const uint16_t* w_gate_up, const uint16_t* w_down,
+                   int T, int d, int E, int k, int F, int has_shared, const int* tokens, int n_tokens,
+                   const int* sel, double* y, int n_threads) {
+  return oracle_forward_ex(x, w_router, w_gate_up, w_down, T, d, E, k, F, has_shared, tokens, n_tokens, sel, 0, y,
+                           n_threads);
+}
+
+/*
+ * Routing statistics of §3.2.3 (EP group-balanced routing): the E experts
+ * form G groups of E/G consecutive indices.  From the oracle's own routing:
+ *   counts[e]  rows routed to expert e (top-k selections)
+ *   f[g]       share of the T*k selections that fall in group g
+ *   pg[g]      mean over tokens of sum_{e in g} p_e
+ *   summary    [0] L_EP = G * sum_g f[g] * pg[g]; [1] max_e counts / (T*k/E);
+ *              [2] mean over tokens of -sum_e p_e ln p_e; [3] experts with no row
+ */
+int oracle_route_stats(const uint16_t* x, const float* w_router, int T, int d, int E, int k, int G, int* counts,
+                       double* f, double* pg, double* summary, int n_threads) {
+  if (T <= 0 || d <= 0 || E <= 0 || k <= 0 || k > E || G <= 0 || E % G != 0) return -1;
+  if (!x || !w_router || !counts || !f || !pg || !summary) return -1;
+  double* p = (double*)malloc(sizeof(double) * (size_t)T * E);
+  int* idx = (int*)malloc(sizeof(int) * (size_t)T * k);
+  if (!p || !idx) { free(p); free(idx); return -1; }
+  if (oracle_route(x, w_router, T, d, E, k, p, idx, NULL, NULL, n_threads) != 0) { free(p); free(idx); return -1; }
+  const int per = E / G;
+  for (int e = 0; e < E; ++e) counts[e] = 0;
+  for (long a = 0; a < (long)T * k; ++a) counts[idx[a]]++;
+  double entropy = 0.0;
+  for (int g = 0; g < G; ++g) pg[g] = 0.0;
+  for (int t = 0; t < T; ++t) {
+    const double* pt = p + (size_t)t * E;
+    for (int e = 0; e < E; ++e) {
+      pg[e / per] += pt[e];
+      if (pt[e] > 0.0) entropy -= pt[e] * log(pt[e]);
+    }
+  }
+  double lep = 0.0;
+  int max_c = 0, empty = 0;
+  for (int e = 0; e < E; ++e) {
+    if (counts[e] > max_c) max_c = counts[e];
+    if (counts[e] == 0) ++empty;
+  }
+  for (int g = 0; g < G; ++g) {
+    long cg = 0;
+    for (int e = g * per; e < (g + 1) * per; ++e) cg += counts[e];
+    f[g] = (double)cg / ((double)T * k);
+    pg[g] /= T;
+    lep += f[g] * pg[g];
+  }
+  summary[0] = G * lep;
+  summary[1] = max_c / ((double)T * k / E);
+  summary[2] = entropy / T;
+  summary[3] = empty;
+  free(p);
+  free(idx);
+  return 0;
 }
 
 /*

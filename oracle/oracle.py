@@ -52,11 +52,18 @@ def _load():
             lib.oracle_forward.argtypes = [_u16p, _f32p, _u16p, _u16p, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                            _i32p, ctypes.c_int, ctypes.c_void_p, _f64p, ctypes.c_int]
+            lib.oracle_forward_ex.argtypes = [_u16p, _f32p, _u16p, _u16p, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                              _i32p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, _f64p,
+                                              ctypes.c_int]
+            lib.oracle_route_stats.argtypes = [_u16p, _f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, _i32p, _f64p, _f64p, _f64p,
+                                               ctypes.c_int]
             lib.oracle_expert_ffn.argtypes = [_u16p, _u16p, _u16p, ctypes.c_int, ctypes.c_int,
                                               ctypes.c_int, _i32p, ctypes.c_int, _f64p, ctypes.c_int]
             lib.oracle_max_threads.argtypes = []
-            for f in ("oracle_route", "oracle_dispatch", "oracle_forward", "oracle_expert_ffn",
-                      "oracle_max_threads"):
+            for f in ("oracle_route", "oracle_dispatch", "oracle_forward", "oracle_forward_ex",
+                      "oracle_route_stats", "oracle_expert_ffn", "oracle_max_threads"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -113,10 +120,11 @@ def dispatch(idx, n_experts: int):
 
 
 def forward(x_bits, w_router, w_gate_up_bits, w_down_bits, k: int, *, has_shared: bool = True,
-            tokens=None, sel=None, threads: int = 0) -> np.ndarray:
+            tokens=None, sel=None, renormalize: bool = False, threads: int = 0) -> np.ndarray:
     """Layer output in float64 for ``tokens`` (all tokens by default).
 
-    ``sel`` ([len(tokens), k] int32) replaces the oracle's own top-k choice.
+    ``sel`` ([len(tokens), k] int32) replaces the oracle's own top-k choice;
+    ``renormalize`` divides the k weights by their sum.
     """
     x = _u16(x_bits)
     wr = np.ascontiguousarray(w_router, dtype=np.float32)
@@ -137,11 +145,28 @@ def forward(x_bits, w_router, w_gate_up_bits, w_down_bits, k: int, *, has_shared
         if sel.shape != (n, k):
             raise ValueError("sel must be [len(tokens), k]")
     y = np.zeros((n, d), np.float64)
-    rc = _load().oracle_forward(x, wr, wgu, wd, T, d, E, k, F, int(has_shared), tokens, n,
-                                _ptr(sel), y, threads)
+    rc = _load().oracle_forward_ex(x, wr, wgu, wd, T, d, E, k, F, int(has_shared), tokens, n,
+                                   _ptr(sel), int(bool(renormalize)), y, threads)
     if rc != 0:
         raise ValueError("oracle_forward rejected its arguments")
     return y
+
+
+def route_stats(x_bits, w_router, k: int, n_groups: int, threads: int = 0):
+    """Routing statistics (see moe_oracle.c): (counts [E] int32, f [G], p [G],
+    summary [4] = L_EP, max/mean load, mean entropy, empty experts)."""
+    x = _u16(x_bits)
+    wr = np.ascontiguousarray(w_router, dtype=np.float32)
+    T, d = x.shape
+    E = wr.shape[0]
+    counts = np.zeros((E,), np.int32)
+    f = np.zeros((n_groups,), np.float64)
+    p = np.zeros((n_groups,), np.float64)
+    summary = np.zeros((4,), np.float64)
+    rc = _load().oracle_route_stats(x, wr, T, d, E, k, n_groups, counts, f, p, summary, threads)
+    if rc != 0:
+        raise ValueError("oracle_route_stats rejected its arguments")
+    return counts, f, p, summary
 
 
 def expert_ffn(x_bits, w_gate_up_bits, w_down_bits, group: int, rows=None, threads: int = 0) -> np.ndarray:

@@ -327,3 +327,80 @@ def test_skew_recipe_shape():
     counts = np.bincount(idx.ravel(), minlength=288)
     assert (counts == 0).sum() >= 40
     assert counts.max() / counts.mean() > 4.0
+
+
+# ---- per-call routing variants and routing statistics ----------------------
+
+def library_forward_renorm(x, wr, wgu, wd, k):
+    """library_forward with the k weights divided by their sum."""
+    X = f64_of(x)
+    p = scipy.special.softmax(X @ wr.astype(np.float64).T, axis=1)
+    T, E = p.shape
+    Wgu = torch.from_numpy(f64_of(wgu))
+    Wd = torch.from_numpy(f64_of(wd))
+    F = Wgu.shape[1] // 2
+    Xt = torch.from_numpy(X)
+    y = torch.zeros(T, X.shape[1], dtype=torch.float64)
+    idx = np.stack([np.lexsort((np.arange(E), -p[t]))[:k] for t in range(T)])
+    wsel = p[np.arange(T)[:, None], idx]
+    wsel = wsel / wsel.sum(axis=1, keepdims=True)
+    for g in range(E + 1):
+        o = (torch.nn.functional.silu(Xt @ Wgu[g, :F].T) * (Xt @ Wgu[g, F:].T)) @ Wd[g].T
+        if g == E:
+            y += o
+        else:
+            y += torch.from_numpy(np.where(idx == g, wsel, 0.0).sum(1))[:, None] * o
+    return y.numpy()
+
+
+@pytest.mark.parametrize("k", [2, 5])
+def test_renormalized_forward_matches_library(k):
+    shape, x, wr, wgu, wd = rand_layer(50 + k, T=11, d=64, E=9, k=k, F=32)
+    y = oracle.forward(x, wr, wgu, wd, k, renormalize=True)
+    np.testing.assert_allclose(y, library_forward_renorm(x, wr, wgu, wd, k), rtol=1e-11, atol=1e-13)
+
+
+def test_renormalize_changes_nothing_when_k_equals_E():
+    shape, x, wr, wgu, wd = rand_layer(55, T=6, d=64, E=5, k=5, F=32)
+    np.testing.assert_allclose(oracle.forward(x, wr, wgu, wd, 5, renormalize=True),
+                               oracle.forward(x, wr, wgu, wd, 5), rtol=1e-13, atol=1e-15)
+
+
+def test_route_stats_uniform_router_closed_form():
+    # W_r = 0: p = 1/E for every expert, the tie rule picks experts 0..k-1, so
+    # all T*k rows land in group 0: f = (1, 0, ...), p_g = 1/G, L_EP = 1,
+    # max/mean load = E/k, entropy = ln E, E - k experts without rows.
+    shape, x, wr, wgu, wd = rand_layer(56, T=10, d=64, E=24, k=3, F=32)
+    counts, f, pg, summary = oracle.route_stats(x, np.zeros_like(wr), 3, 6)
+    np.testing.assert_array_equal(counts, np.array([10, 10, 10] + [0] * 21))
+    np.testing.assert_array_equal(f, np.array([1.0, 0, 0, 0, 0, 0]))
+    np.testing.assert_allclose(pg, 1.0 / 6, rtol=1e-14)
+    np.testing.assert_allclose(summary, [1.0, 24 / 3, math.log(24), 21], rtol=1e-13)
+
+
+def test_route_stats_brute_force():
+    shape, x, wr, wgu, wd = rand_layer(57, T=7, d=16, E=8, k=2, F=8)
+    counts, f, pg, summary = oracle.route_stats(x, wr, 2, 4)
+    X = f64_of(x).tolist()
+    W = wr.astype(np.float64).tolist()
+    c = [0] * 8
+    mass = [0.0] * 4
+    ent = 0.0
+    for t in range(7):
+        z = [sum(X[t][i] * W[e][i] for i in range(16)) for e in range(8)]
+        m = max(z)
+        ex = [math.exp(v - m) for v in z]
+        s = sum(ex)
+        p = [v / s for v in ex]
+        for e in sorted(range(8), key=lambda e: (-p[e], e))[:2]:
+            c[e] += 1
+        for e in range(8):
+            mass[e // 2] += p[e]
+            ent -= p[e] * math.log(p[e])
+    fb = [(c[2 * g] + c[2 * g + 1]) / 14 for g in range(4)]
+    pb = [mv / 7 for mv in mass]
+    assert counts.tolist() == c
+    np.testing.assert_allclose(f, fb, rtol=1e-14)
+    np.testing.assert_allclose(pg, pb, rtol=1e-12)
+    np.testing.assert_allclose(summary, [4 * sum(a * b for a, b in zip(fb, pb)), max(c) / (14 / 8), ent / 7,
+                                         c.count(0)], rtol=1e-12)
