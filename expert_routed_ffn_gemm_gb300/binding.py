@@ -31,7 +31,8 @@ MOE_ERR_NO_DEVICE = 6
 
 EXPORTED = ("moe_init", "moe_route", "moe_forward", "moe_forward_host", "moe_check", "moe_set_wait_limit",
             "moe_profile_enable", "moe_profile_read", "moe_free", "moe_status_string",
-            "moe_selftest_wait_timeout", "moe_dispatch_noalloc")
+            "moe_selftest_wait_timeout", "moe_dispatch_noalloc", "moe_route_ex", "moe_forward_ex",
+            "moe_route_stats")
 PROFILE_STAGES = ("routing", "dispatch", "gather", "gate_up_gemm", "down_gemm", "combine")
 
 
@@ -49,6 +50,16 @@ class moe_config(ctypes.Structure):
 
 class moe_weights(ctypes.Structure):
     _fields_ = [("w_router", ctypes.c_void_p), ("w_gate_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p)]
+
+
+class moe_call_options(ctypes.Structure):
+    _fields_ = [("top_k", ctypes.c_int), ("renormalize", ctypes.c_int)]
+
+
+def _opts(top_k, renormalize):
+    if top_k is None and not renormalize:
+        return None
+    return ctypes.byref(moe_call_options(int(top_k or 0), int(bool(renormalize))))
 
 
 _lib = None
@@ -83,6 +94,9 @@ def load():
         lib.moe_status_string.restype = ctypes.c_char_p
         lib.moe_selftest_wait_timeout.argtypes = [ull, vp]
         lib.moe_dispatch_noalloc.argtypes = [vp, i, i, i, i, vp, vp, vp]
+        lib.moe_route_ex.argtypes = [vp, vp, i, vp, vp, vp, vp, vp, vp, vp]
+        lib.moe_forward_ex.argtypes = [vp, vp, i, vp, vp, vp]
+        lib.moe_route_stats.argtypes = [vp, vp, i, i, vp, vp, vp, vp, vp]
         for name in EXPORTED:
             if name != "moe_status_string":
                 getattr(lib, name).restype = ctypes.c_int
@@ -131,6 +145,21 @@ def moe_route(h: int, x, T: int, idx, prob, perm, offsets, gap=None, stream=None
 
 def moe_forward(h: int, x, T: int, y, stream=None) -> None:
     _check(load().moe_forward(h, _ptr(x), int(T), _ptr(y), _stream(stream)), "moe_forward")
+
+
+def moe_route_ex(h: int, x, T: int, top_k, renormalize, idx, prob, perm, offsets, gap=None, stream=None) -> None:
+    _check(load().moe_route_ex(h, _ptr(x), int(T), _opts(top_k, renormalize), _ptr(idx), _ptr(prob), _ptr(perm),
+                               _ptr(offsets), _ptr(gap), _stream(stream)), "moe_route_ex")
+
+
+def moe_forward_ex(h: int, x, T: int, top_k, renormalize, y, stream=None) -> None:
+    _check(load().moe_forward_ex(h, _ptr(x), int(T), _opts(top_k, renormalize), _ptr(y), _stream(stream)),
+           "moe_forward_ex")
+
+
+def moe_route_stats(h: int, x, T: int, n_groups: int, counts, group_f, group_p, summary, stream=None) -> None:
+    _check(load().moe_route_stats(h, _ptr(x), int(T), int(n_groups), _ptr(counts), _ptr(group_f), _ptr(group_p),
+                                  _ptr(summary), _stream(stream)), "moe_route_stats")
 
 
 def moe_forward_host(h: int, x_host: torch.Tensor, T: int, y_host: torch.Tensor, stream=None) -> None:
@@ -199,24 +228,44 @@ class MoeLayer:
         cfg = moe_config(d, E, top_k, F, int(has_shared), max_tokens, int(out_fp32))
         self.handle = moe_init(cfg, w_router, w_gate_up, w_down)
 
-    def route(self, x: torch.Tensor, stream=None, with_gap: bool = True):
+    def route(self, x: torch.Tensor, stream=None, with_gap: bool = True, top_k: int | None = None,
+              renormalize: bool = False):
         T = x.shape[0]
         dev = x.device
-        idx = torch.empty((T, self.k), dtype=torch.int32, device=dev)
-        prob = torch.empty((T, self.k), dtype=torch.float32, device=dev)
-        perm = torch.empty((T * self.k,), dtype=torch.int32, device=dev)
+        k = top_k or self.k
+        idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+        prob = torch.empty((T, k), dtype=torch.float32, device=dev)
+        perm = torch.empty((T * k,), dtype=torch.int32, device=dev)
         offsets = torch.empty((self.E + 2,), dtype=torch.int32, device=dev)
         gap = torch.empty((T,), dtype=torch.float32, device=dev) if with_gap else None
-        moe_route(self.handle, x, T, idx, prob, perm, offsets, gap, stream)
+        if top_k is None and not renormalize:
+            moe_route(self.handle, x, T, idx, prob, perm, offsets, gap, stream)
+        else:
+            moe_route_ex(self.handle, x, T, top_k, renormalize, idx, prob, perm, offsets, gap, stream)
         return idx, prob, perm, offsets, gap
 
-    def forward(self, x: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    def forward(self, x: torch.Tensor, y: torch.Tensor | None = None, stream=None, top_k: int | None = None,
+                renormalize: bool = False) -> torch.Tensor:
         T = x.shape[0]
         if y is None:
             y = torch.empty((T, self.d), dtype=torch.float32 if self.out_fp32 else torch.bfloat16,
                             device=x.device)
-        moe_forward(self.handle, x, T, y, stream)
+        if top_k is None and not renormalize:
+            moe_forward(self.handle, x, T, y, stream)
+        else:
+            moe_forward_ex(self.handle, x, T, top_k, renormalize, y, stream)
         return y
+
+    def route_stats(self, x: torch.Tensor, n_groups: int, stream=None):
+        """(counts [E] int32, group_f [G], group_p [G], summary [4]) on the device."""
+        T = x.shape[0]
+        dev = x.device
+        counts = torch.empty((self.E,), dtype=torch.int32, device=dev)
+        group_f = torch.empty((n_groups,), dtype=torch.float32, device=dev)
+        group_p = torch.empty((n_groups,), dtype=torch.float32, device=dev)
+        summary = torch.empty((4,), dtype=torch.float32, device=dev)
+        moe_route_stats(self.handle, x, T, n_groups, counts, group_f, group_p, summary, stream)
+        return counts, group_f, group_p, summary
 
     __call__ = forward
 

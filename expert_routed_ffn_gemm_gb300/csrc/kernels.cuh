@@ -15,6 +15,7 @@ constexpr int kBlockK = 64;   // K elements per pipeline stage (one 128-byte swi
 constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 32;
 constexpr int kMaxKSplit = 16;  // K splits of the router GEMM
+constexpr int kMaxStatGroups = 64;  // expert groups of the routing statistics
 
 // Token-tile widths (N of tcgen05.mma) the grouped GEMMs are built for.
 constexpr int kNumTileN = 5;
@@ -32,8 +33,14 @@ struct RouterGemmArgs {
 };
 cudaError_t launch_router_gemm(int tile_n, const CUtensorMap* map_w3, const CUtensorMap* map_x,
                                const RouterGemmArgs& a, int num_sms, cudaStream_t stream);
-cudaError_t launch_router_topk(const float* partial, int ksplit, int T, int E, int k, int* idx, float* prob,
-                               float* gap, int* counts, cudaStream_t stream);
+// renorm != 0 divides the k weights by their sum; tokstats (or NULL) gets per
+// token the probability mass of each of n_groups expert groups and the entropy.
+cudaError_t launch_router_topk(const float* partial, int ksplit, int T, int E, int k, int renorm, int* idx,
+                               float* prob, float* gap, int* counts, float* tokstats, int n_groups,
+                               cudaStream_t stream);
+// Routing statistics from tokstats and counts (one block, fixed summation order).
+cudaError_t launch_route_stats(const float* tokstats, const int* counts, int T, int E, int k, int n_groups,
+                               float* group_f, float* group_p, float* summary, cudaStream_t stream);
 // W_r fp32 [E][d] -> bf16 slices [3][e_pad][d] with hi + mid + lo = W_r.
 cudaError_t launch_split_router(const float* w, int E, int d, int e_pad, bf16* w3, cudaStream_t stream);
 cudaError_t router_gemm_prepare();

@@ -46,15 +46,16 @@ struct moe_handle {
   int* perm;       // [Tmax*k]
   int* inv;        // [Tmax*k]
   int* offsets;    // [E+2]
-  void* xpyp;      // [(k+1)*Tmax][d]: gathered rows (bf16), then the expert outputs (fp32)
+  float* yp;       // [(k+1)*Tmax][d]: token rows in dispatch order (bf16), then the expert outputs
   bf16* hbuf;      // [(k+1)*Tmax][F] H
   bf16* x_stage;   // [Tmax][d] (host entry point)
   void* y_stage;   // [Tmax][d] bf16 or fp32 (host entry point)
   uint32_t* err;   // device error word
+  float* tokstats; // [Tmax][kMaxStatGroups + 1] per-token group masses and entropy
   CUtensorMap map_w3;                   // W_r slices as [3*e_pad][d], box 64 x 128
   CUtensorMap map_wgu;                  // W_gu as [G*2F][d], box 64 x 64
   CUtensorMap map_wd;                   // W_d  as [G*d][F], box 64 x 128
-  CUtensorMap map_xp[moe::kNumTileN];   // Xp   as [Rmax][d], box 64 x BN
+  CUtensorMap map_xp[moe::kNumTileN];   // Xp   as [Rmax][d] bf16 (in yp), box 64 x BN
   CUtensorMap map_h[moe::kNumTileN];    // H    as [Rmax][F], box 64 x BN
   // per-stage timing (moe_profile_enable)
   bool profiling;
@@ -146,9 +147,18 @@ int check_call(const moe_handle* h, const void* x, int T) {
   return MOE_OK;
 }
 
+// Per-call routing choice: k experts per token (<= the handle's top_k) and
+// whether the k weights are renormalised to sum to 1.
+struct CallOpts {
+  int k;
+  int renorm;
+};
+
 // K1: router GEMM (K split across CTAs when there are few token tiles) and
-// softmax/top-k into idx/prob/gap, counts per expert.
-int enqueue_router(moe_handle* h, const void* x, int T, int* idx, float* prob, float* gap, cudaStream_t s) {
+// softmax/top-k into idx/prob/gap, counts per expert; with tokstats, the
+// per-token group masses and entropy for the routing statistics.
+int enqueue_router(moe_handle* h, const void* x, int T, CallOpts o, int* idx, float* prob, float* gap,
+                   float* tokstats, int n_groups, cudaStream_t s) {
   const moe_config& c = h->cfg;
   MOE_CUDA(cudaMemsetAsync(h->counts, 0, sizeof(int) * c.n_experts, s));
   if (T == 0) return MOE_OK;
@@ -178,17 +188,30 @@ int enqueue_router(moe_handle* h, const void* x, int T, int* idx, float* prob, f
   ra.m_tiles = h->router_m_tiles;
   ra.ksplit = ks;
   MOE_CUDA(moe::launch_router_gemm(bn, &h->map_w3, &map_x, ra, h->num_sms, s));
-  MOE_CUDA(moe::launch_router_topk(h->partial, ks, T, c.n_experts, c.top_k, idx, prob, gap, h->counts, s));
+  MOE_CUDA(moe::launch_router_topk(h->partial, ks, T, c.n_experts, o.k, o.renorm, idx, prob, gap, h->counts,
+                                   tokstats, n_groups, s));
   return MOE_OK;
 }
 
 // K1 + K2 into the given buffers.
-int enqueue_route(moe_handle* h, const void* x, int T, int* idx, float* prob, int* perm, int* offsets, float* gap,
-                  cudaStream_t s) {
+int enqueue_route(moe_handle* h, const void* x, int T, CallOpts o, int* idx, float* prob, int* perm, int* offsets,
+                  float* gap, cudaStream_t s) {
   const moe_config& c = h->cfg;
-  const int rc = enqueue_router(h, x, T, idx, prob, gap, s);
+  const int rc = enqueue_router(h, x, T, o, idx, prob, gap, nullptr, 0, s);
   if (rc != MOE_OK) return rc;
-  MOE_CUDA(moe::launch_dispatch(idx, h->counts, T, c.n_experts, c.top_k, c.has_shared, offsets, perm, h->inv, s));
+  MOE_CUDA(moe::launch_dispatch(idx, h->counts, T, c.n_experts, o.k, c.has_shared, offsets, perm, h->inv, s));
+  return MOE_OK;
+}
+
+// Options of a call: NULL = the handle's top_k, no renormalisation.
+int resolve_opts(const moe_handle* h, const moe_call_options* opt, CallOpts* o) {
+  o->k = h->cfg.top_k;
+  o->renorm = 0;
+  if (opt == nullptr) return MOE_OK;
+  if (opt->top_k < 0 || opt->top_k > h->cfg.top_k) return MOE_ERR_INVALID_ARG;
+  if (opt->renormalize != 0 && opt->renormalize != 1) return MOE_ERR_INVALID_ARG;
+  if (opt->top_k > 0) o->k = opt->top_k;
+  o->renorm = opt->renormalize;
   return MOE_OK;
 }
 
@@ -207,19 +230,21 @@ cudaEvent_t* prof_slot(moe_handle* h) {
 #define MOE_MARK(i) \
   if (ev) MOE_CUDA(cudaEventRecord(ev[i], s))
 
-int enqueue_forward(moe_handle* h, const void* x, int T, void* y, cudaStream_t s) {
+int enqueue_forward(moe_handle* h, const void* x, int T, CallOpts o, void* y, cudaStream_t s) {
   const moe_config& c = h->cfg;
   cudaEvent_t* ev = prof_slot(h);
   MOE_MARK(0);
-  const int rc = enqueue_router(h, x, T, h->idx, h->prob, nullptr, s);
+  const int rc = enqueue_router(h, x, T, o, h->idx, h->prob, nullptr, nullptr, 0, s);
   if (rc != MOE_OK) return rc;
   MOE_MARK(1);
-  MOE_CUDA(moe::launch_dispatch(h->idx, h->counts, T, c.n_experts, c.top_k, c.has_shared, h->offsets, h->perm,
-                                h->inv, s));
+  MOE_CUDA(moe::launch_dispatch(h->idx, h->counts, T, c.n_experts, o.k, c.has_shared, h->offsets, h->perm, h->inv,
+                                s));
   MOE_MARK(2);
-  MOE_CUDA(moe::launch_gather(static_cast<const bf16*>(x), h->perm, T, c.top_k, c.d_model, c.has_shared,
-                              static_cast<bf16*>(h->xpyp), s));
-  const double mean_rows = static_cast<double>(T) * c.top_k / c.n_experts;
+  // token rows in dispatch order (the yp buffer holds them until the down GEMM)
+  bf16* xp = reinterpret_cast<bf16*>(h->yp);
+  MOE_CUDA(moe::launch_gather(static_cast<const bf16*>(x), h->perm, T, o.k, c.d_model, c.has_shared, xp, s));
+  MOE_MARK(3);
+  const double mean_rows = static_cast<double>(T) * o.k / c.n_experts;
   const int bn1 = h->tile_gateup ? h->tile_gateup : choose_tile(mean_rows, 256);
   const int bn2 = h->tile_down ? h->tile_down : choose_tile(mean_rows, 256);
 
@@ -231,7 +256,7 @@ int enqueue_forward(moe_handle* h, const void* x, int T, void* y, cudaStream_t s
   a.wait_limit_ns = h->wait_limit_ns;
   a.G = h->G;
   a.F = c.ffn_width;
-  a.Tk = T * c.top_k;
+  a.Tk = T * o.k;
 
   // 256-row token tiles run on CTA pairs (M = 256 weight rows per pair)
   const int i128 = tile_index(128);
@@ -243,7 +268,6 @@ int enqueue_forward(moe_handle* h, const void* x, int T, void* y, cudaStream_t s
   a.rows_per_group = 2 * c.ffn_width;
   a.m_tiles = pair1 ? c.ffn_width / moe::kBlockM : c.ffn_width / (moe::kBlockM / 2);
   a.out_ld = c.ffn_width;
-  MOE_MARK(3);
   const int i1 = tile_index(bn1), i2 = tile_index(bn2);
   if (pair1)
     MOE_CUDA(moe::launch_expert_gemm_pair(true, &h->map_wgu, &h->map_xp[i128], a, h->num_sms, s));
@@ -251,7 +275,7 @@ int enqueue_forward(moe_handle* h, const void* x, int T, void* y, cudaStream_t s
     MOE_CUDA(moe::launch_expert_gemm(true, bn1, &h->map_wgu, &h->map_xp[i1], a, h->num_sms, s));
   MOE_MARK(4);
 
-  a.out = h->xpyp;
+  a.out = h->yp;
   a.K = c.ffn_width;
   a.rows_per_group = c.d_model;
   a.m_tiles = pair2 ? c.d_model / (2 * moe::kBlockM) : c.d_model / moe::kBlockM;
@@ -261,8 +285,8 @@ int enqueue_forward(moe_handle* h, const void* x, int T, void* y, cudaStream_t s
   else
     MOE_CUDA(moe::launch_expert_gemm(false, bn2, &h->map_wd, &h->map_h[i2], a, h->num_sms, s));
   MOE_MARK(5);
-  MOE_CUDA(moe::launch_combine(static_cast<const float*>(h->xpyp), h->inv, T, c.top_k, c.d_model, c.has_shared,
-                               y, c.out_fp32, s));
+  MOE_CUDA(moe::launch_combine(static_cast<const float*>(h->yp), h->inv, T, o.k, c.d_model, c.has_shared, y,
+                               c.out_fp32, s));
   MOE_MARK(6);
   return MOE_OK;
 }
@@ -355,8 +379,9 @@ int moe_init(const moe_config* cfg, const moe_weights* w, moe_handle** out) {
   const size_t o_counts = carve(4 * E), o_err = carve(16), o_offsets = carve(4 * (E + 2)),
                o_partial = carve(4 * p_rows * E), o_w3 = carve(2 * 3 * e_pad * d), o_idx = carve(4 * Tmax * k),
                o_prob = carve(4 * Tmax * k), o_perm = carve(4 * Tmax * k), o_inv = carve(4 * Tmax * k),
-               o_xpyp = carve(4 * R * d), o_h = carve(2 * R * F), o_xs = carve(2 * Tmax * d),
-               o_ys = carve((c.out_fp32 ? 4 : 2) * Tmax * d);
+               o_yp = carve(4 * R * d), o_h = carve(2 * R * F), o_xs = carve(2 * Tmax * d),
+               o_ys = carve((c.out_fp32 ? 4 : 2) * Tmax * d),
+               o_tok = carve(4 * Tmax * (moe::kMaxStatGroups + 1));
   if (cudaMalloc(&h->ws, off) != cudaSuccess) {
     cudaGetLastError();
     delete h;
@@ -372,10 +397,11 @@ int moe_init(const moe_config* cfg, const moe_weights* w, moe_handle** out) {
   h->prob = reinterpret_cast<float*>(b + o_prob);
   h->perm = reinterpret_cast<int*>(b + o_perm);
   h->inv = reinterpret_cast<int*>(b + o_inv);
-  h->xpyp = b + o_xpyp;
+  h->yp = reinterpret_cast<float*>(b + o_yp);
   h->hbuf = reinterpret_cast<bf16*>(b + o_h);
   h->x_stage = reinterpret_cast<bf16*>(b + o_xs);
   h->y_stage = b + o_ys;
+  h->tokstats = reinterpret_cast<float*>(b + o_tok);
 
   bool ok = cudaMemset(h->ws, 0, o_partial) == cudaSuccess;  // counts, error word, offsets
   ok = ok && moe::launch_split_router(w->w_router, c.n_experts, c.d_model, static_cast<int>(e_pad), h->w3,
@@ -385,7 +411,7 @@ int moe_init(const moe_config* cfg, const moe_weights* w, moe_handle** out) {
   ok = ok && encode_2d(&h->map_wgu, w->w_gate_up, G * 2 * F, d, moe::kBlockM / 2);
   ok = ok && encode_2d(&h->map_wd, w->w_down, G * d, F, moe::kBlockM);
   for (int i = 0; ok && i < moe::kNumTileN; ++i) {
-    ok = ok && encode_2d(&h->map_xp[i], h->xpyp, R, d, moe::kTileN[i]);
+    ok = ok && encode_2d(&h->map_xp[i], h->yp, R, d, moe::kTileN[i]);
     ok = ok && encode_2d(&h->map_h[i], h->hbuf, R, F, moe::kTileN[i]);
   }
   ok = ok && cudaDeviceSynchronize() == cudaSuccess;
@@ -400,10 +426,12 @@ int moe_init(const moe_config* cfg, const moe_weights* w, moe_handle** out) {
   return MOE_OK;
 }
 
-int moe_route(moe_handle* h, const void* x, int T, int* idx, float* prob, int* perm, int* offsets, float* gap,
-              void* stream) {
+int moe_route_ex(moe_handle* h, const void* x, int T, const moe_call_options* opt, int* idx, float* prob, int* perm,
+                 int* offsets, float* gap, void* stream) {
   int rc = check_call(h, x, T);
   if (rc != MOE_OK) return rc;
+  CallOpts o;
+  if ((rc = resolve_opts(h, opt, &o)) != MOE_OK) return rc;
   if (idx == nullptr || prob == nullptr || perm == nullptr || offsets == nullptr) return MOE_ERR_INVALID_ARG;
   if (!aligned(idx, 4) || !aligned(prob, 4) || !aligned(perm, 4) || !aligned(offsets, 4) || !aligned(gap, 4))
     return MOE_ERR_INVALID_ARG;
@@ -411,16 +439,49 @@ int moe_route(moe_handle* h, const void* x, int T, int* idx, float* prob, int* p
   if (!is_device_ptr(idx) || !is_device_ptr(prob) || !is_device_ptr(perm) || !is_device_ptr(offsets) ||
       (gap != nullptr && !is_device_ptr(gap)))
     return MOE_ERR_INVALID_ARG;
-  return enqueue_route(h, x, T, idx, prob, perm, offsets, gap, static_cast<cudaStream_t>(stream));
+  return enqueue_route(h, x, T, o, idx, prob, perm, offsets, gap, static_cast<cudaStream_t>(stream));
 }
 
-int moe_forward(moe_handle* h, const void* x, int T, void* y, void* stream) {
+int moe_route(moe_handle* h, const void* x, int T, int* idx, float* prob, int* perm, int* offsets, float* gap,
+              void* stream) {
+  return moe_route_ex(h, x, T, nullptr, idx, prob, perm, offsets, gap, stream);
+}
+
+int moe_forward_ex(moe_handle* h, const void* x, int T, const moe_call_options* opt, void* y, void* stream) {
   int rc = check_call(h, x, T);
   if (rc != MOE_OK) return rc;
+  CallOpts o;
+  if ((rc = resolve_opts(h, opt, &o)) != MOE_OK) return rc;
   if (T == 0) return MOE_OK;
   if (y == nullptr || !aligned(y, 16)) return MOE_ERR_INVALID_ARG;
   if (!is_device_ptr(x) || !is_device_ptr(y)) return MOE_ERR_INVALID_ARG;
-  return enqueue_forward(h, x, T, y, static_cast<cudaStream_t>(stream));
+  return enqueue_forward(h, x, T, o, y, static_cast<cudaStream_t>(stream));
+}
+
+int moe_forward(moe_handle* h, const void* x, int T, void* y, void* stream) {
+  return moe_forward_ex(h, x, T, nullptr, y, stream);
+}
+
+int moe_route_stats(moe_handle* h, const void* x, int T, int n_groups, int* counts, float* group_f,
+                    float* group_p, float* summary, void* stream) {
+  int rc = check_call(h, x, T);
+  if (rc != MOE_OK) return rc;
+  const moe_config& c = h->cfg;
+  if (n_groups < 1 || n_groups > moe::kMaxStatGroups || c.n_experts % n_groups != 0) return MOE_ERR_INVALID_ARG;
+  if (counts == nullptr || group_f == nullptr || group_p == nullptr || summary == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned(counts, 4) || !aligned(group_f, 4) || !aligned(group_p, 4) || !aligned(summary, 4))
+    return MOE_ERR_INVALID_ARG;
+  if (T > 0 && !is_device_ptr(x)) return MOE_ERR_INVALID_ARG;
+  if (!is_device_ptr(counts) || !is_device_ptr(group_f) || !is_device_ptr(group_p) || !is_device_ptr(summary))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const CallOpts o{c.top_k, 0};
+  rc = enqueue_router(h, x, T, o, h->idx, h->prob, nullptr, h->tokstats, n_groups, s);
+  if (rc != MOE_OK) return rc;
+  MOE_CUDA(moe::launch_route_stats(h->tokstats, h->counts, T, c.n_experts, c.top_k, n_groups, group_f, group_p,
+                                   summary, s));
+  MOE_CUDA(cudaMemcpyAsync(counts, h->counts, sizeof(int) * c.n_experts, cudaMemcpyDeviceToDevice, s));
+  return MOE_OK;
 }
 
 int moe_forward_host(moe_handle* h, const void* x_host, int T, void* y_host, void* stream) {
@@ -434,7 +495,7 @@ int moe_forward_host(moe_handle* h, const void* x_host, int T, void* y_host, voi
   const size_t xbytes = 2 * d * static_cast<size_t>(T);
   const size_t ybytes = (h->cfg.out_fp32 ? 4 : 2) * d * static_cast<size_t>(T);
   MOE_CUDA(cudaMemcpyAsync(h->x_stage, x_host, xbytes, cudaMemcpyHostToDevice, s));
-  const int rc = enqueue_forward(h, h->x_stage, T, h->y_stage, s);
+  const int rc = enqueue_forward(h, h->x_stage, T, CallOpts{h->cfg.top_k, 0}, h->y_stage, s);
   if (rc != MOE_OK) return rc;
   MOE_CUDA(cudaMemcpyAsync(y_host, h->y_stage, ybytes, cudaMemcpyDeviceToHost, s));
   MOE_CUDA(cudaStreamSynchronize(s));

@@ -253,11 +253,15 @@ constexpr int kMaxPerLane = kMaxExperts / 32;
 __device__ __forceinline__ bool better(float v, int e, float ov, int oe) { return v > ov || (v == ov && e < oe); }
 
 // One warp per token: logits = sum of the K-split partials (fixed order),
-// softmax, top-k (ties: lower index), gap, per-expert counts.
+// softmax, top-k (ties: lower index), gap, per-expert counts.  renorm != 0:
+// the k weights are divided by their sum (summed in slot order).  tokstats
+// (or NULL): per token, the probability mass of each of n_groups equal
+// expert groups, then the entropy -sum p ln p ([T][n_groups + 1]).
 __global__ void __launch_bounds__(64) router_topk_kernel(const float* __restrict__ partial, int ksplit, int T,
-                                                         int E, int k, int* __restrict__ idx,
+                                                         int E, int k, int renorm, int* __restrict__ idx,
                                                          float* __restrict__ prob, float* __restrict__ gap,
-                                                         int* counts) {
+                                                         int* counts, float* __restrict__ tokstats,
+                                                         int n_groups) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -294,8 +298,35 @@ __global__ void __launch_bounds__(64) router_topk_kernel(const float* __restrict
 #pragma unroll
   for (int i = 0; i < kMaxPerLane; ++i) p[i] = p[i] / s;
 
+  if (tokstats != nullptr) {
+    // group masses (group of expert e = e / (E / n_groups)) and entropy
+    const int per_group = E / n_groups;
+    float* out = tokstats + static_cast<size_t>(t) * (n_groups + 1);
+    for (int g = 0; g < n_groups; ++g) {
+      float m = 0.f;
+#pragma unroll
+      for (int i = 0; i < kMaxPerLane; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && e / per_group == g) m += p[i];
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) m += __shfl_xor_sync(0xffffffffu, m, off);
+      if (lane == 0) out[g] = m;
+    }
+    float h = 0.f;
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && p[i] > 0.f) h -= p[i] * logf(p[i]);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) h += __shfl_xor_sync(0xffffffffu, h, off);
+    if (lane == 0) out[n_groups] = h;
+  }
+
   uint32_t taken = 0;
-  float pk = 0.f;
+  float pk = 0.f, sel_sum = 0.f, my_p = 0.f;
+  int my_e = 0;
   for (int j = 0; j <= k; ++j) {
     float bv = -1.f;
     int be = 0x7fffffff;
@@ -318,15 +349,69 @@ __global__ void __launch_bounds__(64) router_topk_kernel(const float* __restrict
     }
     if (j < k) {
       if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      if (lane == 0) {
-        idx[static_cast<size_t>(t) * k + j] = be;
-        prob[static_cast<size_t>(t) * k + j] = bv;
-        atomicAdd(&counts[be], 1);
+      if (lane == j) {  // lane j keeps slot j
+        my_e = be;
+        my_p = bv;
       }
+      sel_sum += bv;  // same value and order in every lane
       pk = bv;
     } else if (gap != nullptr && lane == 0) {
       gap[t] = (be == 0x7fffffff) ? __int_as_float(0x7f800000) : (pk - bv);
     }
+  }
+  if (lane < k) {
+    idx[static_cast<size_t>(t) * k + lane] = my_e;
+    prob[static_cast<size_t>(t) * k + lane] = renorm ? my_p / sel_sum : my_p;
+    atomicAdd(&counts[my_e], 1);
+  }
+}
+
+// Routing statistics over the tokens: group_p[g] = mean over tokens of the
+// group's probability mass, summary[2] = mean entropy (both summed in token
+// order per thread, then a fixed tree: bit-identical run to run);
+// group_f[g] = share of the T*k rows in group g, summary[0] = L_EP =
+// n_groups * sum_g f_g p_g, summary[1] = max/mean rows per expert,
+// summary[3] = experts without rows.  One block of 256 threads.
+__global__ void __launch_bounds__(256) route_stats_kernel(const float* __restrict__ tokstats, const int* counts,
+                                                          int T, int E, int k, int n_groups, float* group_f,
+                                                          float* group_p, float* summary) {
+  __shared__ float red[256];
+  __shared__ float col_sum[kMaxStatGroups + 1];
+  const int cols = n_groups + 1;
+  for (int c = 0; c < cols; ++c) {
+    float acc = 0.f;
+    for (int t = threadIdx.x; t < T; t += 256) acc += tokstats[static_cast<size_t>(t) * cols + c];
+    red[threadIdx.x] = acc;
+    __syncthreads();
+    for (int w = 128; w > 0; w >>= 1) {
+      if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) col_sum[c] = red[0];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const int per_group = E / n_groups;
+    const float rows = static_cast<float>(T) * k;
+    float lep = 0.f;
+    int max_c = 0, empty = 0;
+    for (int e = 0; e < E; ++e) {
+      max_c = max(max_c, counts[e]);
+      empty += counts[e] == 0;
+    }
+    for (int g = 0; g < n_groups; ++g) {
+      int cg = 0;
+      for (int e = g * per_group; e < (g + 1) * per_group; ++e) cg += counts[e];
+      const float f = T > 0 ? cg / rows : 0.f;
+      const float pg = T > 0 ? col_sum[g] / T : 0.f;
+      group_f[g] = f;
+      group_p[g] = pg;
+      lep += f * pg;
+    }
+    summary[0] = n_groups * lep;
+    summary[1] = T > 0 ? max_c / (rows / E) : 0.f;
+    summary[2] = T > 0 ? col_sum[n_groups] / T : 0.f;
+    summary[3] = static_cast<float>(empty);
   }
 }
 
@@ -382,10 +467,18 @@ cudaError_t launch_router_gemm(int tile_n, const CUtensorMap* map_w3, const CUte
   }
 }
 
-cudaError_t launch_router_topk(const float* partial, int ksplit, int T, int E, int k, int* idx, float* prob,
-                               float* gap, int* counts, cudaStream_t stream) {
+cudaError_t launch_router_topk(const float* partial, int ksplit, int T, int E, int k, int renorm, int* idx,
+                               float* prob, float* gap, int* counts, float* tokstats, int n_groups,
+                               cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
-  router_topk_kernel<<<(T + 1) / 2, 64, 0, stream>>>(partial, ksplit, T, E, k, idx, prob, gap, counts);
+  router_topk_kernel<<<(T + 1) / 2, 64, 0, stream>>>(partial, ksplit, T, E, k, renorm, idx, prob, gap, counts,
+                                                     tokstats, n_groups);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_stats(const float* tokstats, const int* counts, int T, int E, int k, int n_groups,
+                               float* group_f, float* group_p, float* summary, cudaStream_t stream) {
+  route_stats_kernel<<<1, 256, 0, stream>>>(tokstats, counts, T, E, k, n_groups, group_f, group_p, summary);
   return cudaGetLastError();
 }
 

@@ -114,6 +114,45 @@ int moe_route(moe_handle* h, const void* x, int T, int* idx, float* prob, int* p
 int moe_forward(moe_handle* h, const void* x, int T, void* y, void* stream);
 
 /*
+ * Per-call routing choices, after "Step3.5 Flash 大模型技术深度解析" (jsqmd.com)
+ * §8.2, which varies the number of experts per token at inference time
+ * (top-4 for simple inputs, top-8 for complex ones).
+ *   top_k        0: the handle's top_k; otherwise 1..cfg.top_k experts per token
+ *   renormalize  0: weights are the softmax probabilities over all E experts;
+ *                1: the k weights are divided by their sum (summed in slot order)
+ */
+typedef struct moe_call_options {
+  int top_k;
+  int renormalize;
+} moe_call_options;
+
+/*
+ * moe_route / moe_forward with per-call options (opt may be NULL = defaults).
+ * With top_k = k' the route outputs are idx/prob [T][k'], perm [T*k'];
+ * prob holds the weights actually used (renormalised if asked).  The gap is
+ * always p(k'-th) - p((k'+1)-th) of the raw probabilities.
+ */
+int moe_route_ex(moe_handle* h, const void* x, int T, const moe_call_options* opt, int* idx, float* prob,
+                 int* perm, int* offsets, float* gap, void* stream);
+int moe_forward_ex(moe_handle* h, const void* x, int T, const moe_call_options* opt, void* y, void* stream);
+
+/*
+ * Routing statistics of a batch (router, softmax and top-k with the handle's
+ * top_k; no expert FFNs), after §3.2.3 of the same page: the E experts form
+ * n_groups equal groups of consecutive indices (8 groups of 36 for EP = 8).
+ *   counts   int   [E]         rows routed to each expert, device
+ *   group_f  fp32  [n_groups]  share of the T*k rows that go to group g, device
+ *   group_p  fp32  [n_groups]  mean over tokens of the group's probability mass, device
+ *   summary  fp32  [4]         device: [0] L_EP = n_groups * sum_g f_g p_g (1 when
+ *                              balanced), [1] max/mean rows per expert, [2] mean
+ *                              router entropy -sum_e p_e ln p_e (nats), [3] experts
+ *                              with no row
+ * 1 <= n_groups <= 64 and n_groups divides E.  Deterministic run to run.
+ */
+int moe_route_stats(moe_handle* h, const void* x, int T, int n_groups, int* counts, float* group_f,
+                    float* group_p, float* summary, void* stream);
+
+/*
  * moe_forward on host buffers: copies x (host, bf16 [T][d]) to the handle's
  * staging buffer, runs the layer and copies y back to host memory (bf16 or
  * fp32 per cfg.out_fp32), all on `stream`, then synchronises that stream.
