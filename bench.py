@@ -177,6 +177,23 @@ def gateup_bytes(shape, touched: int):
     return groups * 2 * F * d * 2 + R * d * 2 + R * F * 2
 
 
+def measured_traffic(args):
+    """DRAM bytes per launch of the gate/up GEMM from the committed ncu capture
+    of the decode workload (profiles/gate_up_decode_T128_dram.md); None for
+    other workloads or when the summary is missing."""
+    if args.workload != "decode" or args.experts:
+        return None
+    path = os.path.join(ROOT, "profiles", "gate_up_decode_T128_dram.md")
+    try:
+        with open(path) as f:
+            for line in f:
+                if line.startswith("traffic_bytes_per_launch:"):
+                    return float(line.split(":", 1)[1])
+    except OSError:
+        pass
+    return None
+
+
 def layer_flops(shape):
     d, F, E, T, k = shape.d, shape.F, shape.E, shape.T, shape.k
     return T * ((k + (1 if shape.has_shared else 0)) * 6 * d * F + 2 * d * E)
@@ -345,7 +362,7 @@ def run_native(args, world, rank, local):
         "roofline": {
             "kernel": "gate_up_gemm (tcgen05 grouped GEMM, fused SiLU-gate)",
             "bound": "hbm", "achieved": gu_gbs, "peak": hbm_gbs, "unit": "GB/s", "frac": gu_gbs / hbm_gbs,
-            "peak_kind": peak_kind, "traffic": None, "ms_per_launch": gu_ms,
+            "peak_kind": peak_kind, "traffic": measured_traffic(args), "ms_per_launch": gu_ms,
             "algorithmic_bytes_per_launch": gu_bytes,
         },
         "layer_roofline": {"hbm_frac": layer_hbm_frac, "tensor_frac_sustained": layer_tc_frac,
