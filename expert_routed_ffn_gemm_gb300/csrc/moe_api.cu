@@ -33,6 +33,7 @@ struct moe_handle {
   int tile_gateup;  // 0 = choose per call
   int tile_down;
   bool use_pairs;   // 256-row token tiles on CTA pairs (MOE_PAIR_TILES=0 turns it off)
+  int router_tile;  // router token tile, 0 = by T (MOE_ROUTER_TILE = 16, 64, 128 or 256)
   unsigned long long wait_limit_ns;
   int router_m_tiles;      // ceil(E / 128)
   long long partial_rows;  // capacity of `partial` in (split, token) rows
@@ -162,7 +163,7 @@ int enqueue_router(moe_handle* h, const void* x, int T, CallOpts o, int* idx, fl
   const moe_config& c = h->cfg;
   MOE_CUDA(cudaMemsetAsync(h->counts, 0, sizeof(int) * c.n_experts, s));
   if (T == 0) return MOE_OK;
-  const int bn = T <= 32 ? 16 : (T <= 1024 ? 64 : 128);
+  const int bn = h->router_tile ? h->router_tile : (T <= 32 ? 16 : (T <= 1024 ? 64 : (T <= 4096 ? 128 : 256)));
   const int n_tt = (T + bn - 1) / bn;
   const int k_total = 3 * c.d_model / moe::kBlockK;
   // K splits: about four waves of work items over the SMs (balances the last
@@ -359,6 +360,8 @@ int moe_init(const moe_config* cfg, const moe_weights* w, moe_handle** out) {
   {
     const char* v = std::getenv("MOE_PAIR_TILES");
     h->use_pairs = !(v && v[0] == '0');
+    const int rt = tile_from_env("MOE_ROUTER_TILE");
+    h->router_tile = (rt == 16 || rt == 64 || rt == 128 || rt == 256) ? rt : 0;
   }
   h->wait_limit_ns = kDefaultWaitNs;
   h->router_m_tiles = (c.n_experts + moe::kBlockM - 1) / moe::kBlockM;

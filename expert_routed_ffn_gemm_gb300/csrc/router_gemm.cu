@@ -12,9 +12,9 @@
 // writes its partial logits and the top-k kernel sums the splits in a fixed
 // order, so results are identical run to run.
 //
-// router_topk_kernel: one warp per token; lane l holds experts l, l+32, ...;
-// max / sum / argmax by xor-shuffle butterflies (every lane ends with the same
-// bits); ties go to the lower expert index.
+// router_topk_kernel: one block of four warps per token sums the K splits; one
+// warp then does softmax and top-k with xor-shuffle butterflies (every lane
+// ends with the same bits); ties go to the lower expert index.
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -31,7 +31,7 @@ struct RCfg {
   static constexpr int A_BYTES = kBlockM * kBlockK * 2;
   static constexpr int B_BYTES = BN * kBlockK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES_RAW = (160 * 1024) / STAGE_BYTES;
+  static constexpr int STAGES_RAW = (192 * 1024) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   static constexpr int NACC = (2 * BN <= 512) ? 2 : 1;
   static constexpr int TMEM_RAW = NACC * BN;
@@ -252,31 +252,62 @@ constexpr int kMaxPerLane = kMaxExperts / 32;
 
 __device__ __forceinline__ bool better(float v, int e, float ov, int oe) { return v > ov || (v == ov && e < oe); }
 
-// One warp per token: logits = sum of the K-split partials (fixed order),
-// softmax, top-k (ties: lower index), gap, per-expert counts.  renorm != 0:
-// the k weights are divided by their sum (summed in slot order).  tokstats
-// (or NULL): per token, the probability mass of each of n_groups equal
-// expert groups, then the entropy -sum p ln p ([T][n_groups + 1]).
-__global__ void __launch_bounds__(64) router_topk_kernel(const float* __restrict__ partial, int ksplit, int T,
-                                                         int E, int k, int renorm, int* __restrict__ idx,
-                                                         float* __restrict__ prob, float* __restrict__ gap,
-                                                         int* counts, float* __restrict__ tokstats,
-                                                         int n_groups) {
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t >= T) return;
+constexpr int kTopkWarps = 4;
+
+// Compare-exchange of two (value, expert) slots: afterwards slot a ranks
+// first (higher value, then lower expert index).
+__device__ __forceinline__ void cx(float& va, int& ea, float& vb, int& eb) {
+  if (better(vb, eb, va, ea)) {
+    const float tv = va;
+    va = vb;
+    vb = tv;
+    const int te = ea;
+    ea = eb;
+    eb = te;
+  }
+}
+
+// One block of 4 warps per token.  Warp w sums the K-split partials
+// s = w, w+4, ... in increasing s; warp 0 then adds the four partial sums in
+// warp order (a fixed order: logits are bit-identical run to run) and does
+// softmax, top-k (ties: lower index), gap and per-expert counts alone.  Lane
+// l holds experts l, l+32, ...; it sorts its own slots once (bitonic network),
+// after which each of the k+1 selection rounds is one xor-butterfly argmax over
+// the 32 lane heads.  renorm != 0: the k weights are divided by their sum
+// (slot order).  tokstats (or NULL): per token, the probability mass of each of
+// n_groups equal expert groups, then the entropy -sum p ln p ([T][n_groups+1]).
+__global__ void __launch_bounds__(kTopkWarps * 32) router_topk_kernel(const float* __restrict__ partial, int ksplit,
+                                                                      int T, int E, int k, int renorm,
+                                                                      int* __restrict__ idx,
+                                                                      float* __restrict__ prob,
+                                                                      float* __restrict__ gap, int* counts,
+                                                                      float* __restrict__ tokstats, int n_groups) {
+  __shared__ float zs[kTopkWarps][kMaxExperts];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t = blockIdx.x;
   float p[kMaxPerLane];
 #pragma unroll
   for (int i = 0; i < kMaxPerLane; ++i) p[i] = 0.f;
-  // split by split, all of a lane's experts at once (independent loads in flight)
 #pragma unroll 4
-  for (int s = 0; s < ksplit; ++s) {
+  for (int s = warp; s < ksplit; s += kTopkWarps) {
     const float* row = partial + (static_cast<size_t>(s) * T + t) * E;
 #pragma unroll
     for (int i = 0; i < kMaxPerLane; ++i) {
       const int e = lane + 32 * i;
       if (e < E) p[i] += __ldg(row + e);
     }
+  }
+#pragma unroll
+  for (int i = 0; i < kMaxPerLane; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) zs[warp][e] = p[i];
+  }
+  __syncthreads();
+  if (warp != 0) return;
+#pragma unroll
+  for (int i = 0; i < kMaxPerLane; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) p[i] = ((zs[0][e] + zs[1][e]) + zs[2][e]) + zs[3][e];
   }
   float zmax = -FLT_MAX;
 #pragma unroll
@@ -324,20 +355,35 @@ __global__ void __launch_bounds__(64) router_topk_kernel(const float* __restrict
     if (lane == 0) out[n_groups] = h;
   }
 
-  uint32_t taken = 0;
+  // this lane's slots, sorted best first (invalid slots: value -1, index max)
+  float sv[kMaxPerLane];
+  int se[kMaxPerLane];
+#pragma unroll
+  for (int i = 0; i < kMaxPerLane; ++i) {
+    const int e = lane + 32 * i;
+    sv[i] = (e < E) ? p[i] : -1.f;
+    se[i] = (e < E) ? e : 0x7fffffff;
+  }
+#pragma unroll
+  for (int size = 2; size <= kMaxPerLane; size <<= 1)
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1)
+#pragma unroll
+      for (int i = 0; i < kMaxPerLane; ++i) {
+        const int j = i ^ stride;
+        if (j > i) {
+          if ((i & size) == 0)
+            cx(sv[i], se[i], sv[j], se[j]);
+          else
+            cx(sv[j], se[j], sv[i], se[i]);
+        }
+      }
+
   float pk = 0.f, sel_sum = 0.f, my_p = 0.f;
   int my_e = 0;
   for (int j = 0; j <= k; ++j) {
-    float bv = -1.f;
-    int be = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u) && p[i] > bv) {  // e grows with i: '>' keeps the lower index
-        bv = p[i];
-        be = e;
-      }
-    }
+    float bv = sv[0];
+    int be = se[0];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
@@ -348,7 +394,15 @@ __global__ void __launch_bounds__(64) router_topk_kernel(const float* __restrict
       }
     }
     if (j < k) {
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      if (be != 0x7fffffff && (be & 31) == lane) {  // the winner pops its head
+#pragma unroll
+        for (int i = 0; i < kMaxPerLane - 1; ++i) {
+          sv[i] = sv[i + 1];
+          se[i] = se[i + 1];
+        }
+        sv[kMaxPerLane - 1] = -1.f;
+        se[kMaxPerLane - 1] = 0x7fffffff;
+      }
       if (lane == j) {  // lane j keeps slot j
         my_e = be;
         my_p = bv;
@@ -450,8 +504,11 @@ cudaError_t router_gemm_prepare() {
   if ((e = cudaFuncSetAttribute(router_gemm_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 RCfg<64>::SMEM_BYTES)) != cudaSuccess)
     return e;
-  return cudaFuncSetAttribute(router_gemm_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              RCfg<128>::SMEM_BYTES);
+  if ((e = cudaFuncSetAttribute(router_gemm_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                RCfg<128>::SMEM_BYTES)) != cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(router_gemm_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              RCfg<256>::SMEM_BYTES);
 }
 
 cudaError_t launch_router_gemm(int tile_n, const CUtensorMap* map_w3, const CUtensorMap* map_x,
@@ -463,6 +520,7 @@ cudaError_t launch_router_gemm(int tile_n, const CUtensorMap* map_w3, const CUte
     case 16: return launch_rg<16>(map_w3, map_x, a, grid, stream);
     case 64: return launch_rg<64>(map_w3, map_x, a, grid, stream);
     case 128: return launch_rg<128>(map_w3, map_x, a, grid, stream);
+    case 256: return launch_rg<256>(map_w3, map_x, a, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -471,7 +529,7 @@ cudaError_t launch_router_topk(const float* partial, int ksplit, int T, int E, i
                                float* prob, float* gap, int* counts, float* tokstats, int n_groups,
                                cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
-  router_topk_kernel<<<(T + 1) / 2, 64, 0, stream>>>(partial, ksplit, T, E, k, renorm, idx, prob, gap, counts,
+  router_topk_kernel<<<T, kTopkWarps * 32, 0, stream>>>(partial, ksplit, T, E, k, renorm, idx, prob, gap, counts,
                                                      tokstats, n_groups);
   return cudaGetLastError();
 }

@@ -238,6 +238,35 @@ def test_flash_skewed_sampled(flash_weights, out_fp32):
     flash_case(flash_weights, 4096, seed=102, n_sample=64, skew="zipf", out_fp32=out_fp32)
 
 
-@pytest.mark.parametrize("T", [1, 8, 512])
+@pytest.mark.parametrize("T", [1, 8, 32, 512, 2048])
 def test_flash_sweep_points(flash_weights, T):
-    flash_case(flash_weights, T, seed=200 + T, n_sample=None if T <= 8 else 64)
+    flash_case(flash_weights, T, seed=200 + T, n_sample=None if T <= 32 else 64)
+
+
+def test_flash_largest_sweep_point(flash_weights):
+    # T=32768: routing and dispatch on every token, output on a sample; fp32 y
+    flash_case(flash_weights, 32768, seed=232, n_sample=48, out_fp32=True)
+
+
+def test_forward_captured_in_a_cuda_graph():
+    # moe_forward enqueues only kernels and a memset on the caller's stream
+    # (no host synchronisation, no allocation), so it can be captured once
+    # and replayed; replays on new inputs match the eager call bit for bit.
+    shape = synth.LayerShape(T=200, d=256, E=16, k=2, F=128)
+    inp = synth.make_inputs(shape, seed=16)
+    layer, x = make_layer(inp)
+    y = torch.empty((shape.T, shape.d), dtype=torch.bfloat16, device=DEV)
+    layer.forward(x, y)  # warm-up outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            layer.forward(x, y, stream=s)
+    for seed in (17, 18):
+        x.copy_(synth.make_tokens(shape, seed=seed, device=DEV))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y, layer.forward(x))
+    assert layer.check() == binding.MOE_OK
+    layer.close()
