@@ -170,11 +170,17 @@ def algorithmic_bytes(shape, touched: int):
 
 def gateup_bytes(shape, touched: int):
     """Algorithmic bytes of one gate/up GEMM launch: W_gu of every group with
-    rows, the gathered rows read once, H written once."""
+    rows, the R dispatch-ordered token rows read once, H written once."""
     d, F, T, k = shape.d, shape.F, shape.T, shape.k
     groups = touched + (1 if shape.has_shared else 0)
     R = T * k + (T if shape.has_shared else 0)
     return groups * 2 * F * d * 2 + R * d * 2 + R * F * 2
+
+
+def gateup_flops(shape):
+    d, F, T, k = shape.d, shape.F, shape.T, shape.k
+    R = T * k + (T if shape.has_shared else 0)
+    return 2 * R * d * 2 * F
 
 
 def measured_traffic(args):
@@ -304,10 +310,13 @@ def run_native(args, world, rank, local):
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         ev0.record(stream)
+        launches = 0
         for i in range(args.steps):
             layer.forward(xs[i % N_X_BUFFERS], y)
+            launches += layer.last_kernel_count()
         ev1.record(stream)
         torch.cuda.synchronize()
+    kernels_per_step = launches // max(1, args.steps)
     barrier(world)
     ms = ev0.elapsed_time(ev1)
     stages, n_prof = layer.profile_read()
@@ -340,6 +349,15 @@ def run_native(args, world, rank, local):
     mean_touched = sum(touched[i % N_X_BUFFERS] for i in range(args.steps)) / args.steps
     gu_bytes = gateup_bytes(shape, mean_touched)
     gu_gbs = gu_bytes / (gu_ms / 1e3) / 1e9
+    gu_tfs = gateup_flops(shape) / (gu_ms / 1e3) / 1e12
+    # the binding roof of the kernel: the larger of its HBM and tensor floors
+    tensor_bound = gateup_flops(shape) / (tf_sust * 1e12) > gu_bytes / (hbm_gbs * 1e9)
+    if tensor_bound:
+        roof = {"bound": "tensor", "achieved": gu_tfs, "peak": tf_sust, "unit": "TFLOP/s",
+                "frac": gu_tfs / tf_sust, "peak_kind": peak_kind + " (sustained bf16)"}
+    else:
+        roof = {"bound": "hbm", "achieved": gu_gbs, "peak": hbm_gbs, "unit": "GB/s", "frac": gu_gbs / hbm_gbs,
+                "peak_kind": peak_kind}
     layer_bytes = algorithmic_bytes(shape, mean_touched)
     step_s = ms_max / 1e3 / args.steps
     layer_hbm_frac = layer_bytes / step_s / 1e9 / hbm_gbs
@@ -361,16 +379,16 @@ def run_native(args, world, rank, local):
         },
         "roofline": {
             "kernel": "gate_up_gemm (tcgen05 grouped GEMM, fused SiLU-gate)",
-            "bound": "hbm", "achieved": gu_gbs, "peak": hbm_gbs, "unit": "GB/s", "frac": gu_gbs / hbm_gbs,
-            "peak_kind": peak_kind, "traffic": measured_traffic(args), "ms_per_launch": gu_ms,
-            "algorithmic_bytes_per_launch": gu_bytes,
+            **roof, "traffic": measured_traffic(args), "ms_per_launch": gu_ms,
+            "algorithmic_bytes_per_launch": gu_bytes, "hbm_frac": gu_gbs / hbm_gbs,
+            "tensor_frac_sustained": gu_tfs / tf_sust,
         },
         "layer_roofline": {"hbm_frac": layer_hbm_frac, "tensor_frac_sustained": layer_tc_frac,
                            "bytes_per_step": layer_bytes, "flops_per_step": layer_flops(shape)},
         "stage_ms_per_step": {k: v / steps_prof for k, v in stages.items()},
         "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": shape.T * shape.d * 2,
                 "d2h_bytes_per_step": shape.T * shape.d * 2},
-        "gpu_launches": 6 * args.steps,
+        "gpu_launches": kernels_per_step * args.steps,
         "clocks": clk.summary(),
     }
 

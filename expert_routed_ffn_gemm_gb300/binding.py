@@ -32,7 +32,7 @@ MOE_ERR_NO_DEVICE = 6
 EXPORTED = ("moe_init", "moe_route", "moe_forward", "moe_forward_host", "moe_check", "moe_set_wait_limit",
             "moe_profile_enable", "moe_profile_read", "moe_free", "moe_status_string",
             "moe_selftest_wait_timeout", "moe_dispatch_noalloc", "moe_route_ex", "moe_forward_ex",
-            "moe_route_stats")
+            "moe_route_stats", "moe_last_kernel_count")
 PROFILE_STAGES = ("routing", "dispatch", "gather", "gate_up_gemm", "down_gemm", "combine")
 
 
@@ -86,6 +86,7 @@ def load():
         lib.moe_forward.argtypes = [vp, vp, i, vp, vp]
         lib.moe_forward_host.argtypes = [vp, vp, i, vp, vp]
         lib.moe_check.argtypes = [vp, vp]
+        lib.moe_last_kernel_count.argtypes = [vp]
         lib.moe_set_wait_limit.argtypes = [vp, ull]
         lib.moe_profile_enable.argtypes = [vp, i]
         lib.moe_profile_read.argtypes = [vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int)]
@@ -166,6 +167,11 @@ def moe_forward_host(h: int, x_host: torch.Tensor, T: int, y_host: torch.Tensor,
     if x_host.is_cuda or y_host.is_cuda:
         raise ValueError("moe_forward_host takes host tensors")
     _check(load().moe_forward_host(h, _ptr(x_host), int(T), _ptr(y_host), _stream(stream)), "moe_forward_host")
+
+
+def moe_last_kernel_count(h: int) -> int:
+    """Kernels the last forward call on the handle enqueued (-1: bad handle)."""
+    return int(load().moe_last_kernel_count(h))
 
 
 def moe_check(h: int, stream=None) -> int:
@@ -279,6 +285,9 @@ class MoeLayer:
 
     def check(self, stream=None) -> int:
         return moe_check(self.handle, stream)
+
+    def last_kernel_count(self) -> int:
+        return moe_last_kernel_count(self.handle)
 
     def set_wait_limit(self, ns: int) -> None:
         moe_set_wait_limit(self.handle, ns)

@@ -34,6 +34,7 @@ struct moe_handle {
   int tile_down;
   bool use_pairs;   // 256-row token tiles on CTA pairs (MOE_PAIR_TILES=0 turns it off)
   int router_tile;  // router token tile, 0 = by T (MOE_ROUTER_TILE = 16, 64, 128 or 256)
+  int last_kernels;   // kernels enqueued by the last forward call
   unsigned long long wait_limit_ns;
   int router_m_tiles;      // ceil(E / 128)
   long long partial_rows;  // capacity of `partial` in (split, token) rows
@@ -248,6 +249,10 @@ int enqueue_forward(moe_handle* h, const void* x, int T, CallOpts o, void* y, cu
   const double mean_rows = static_cast<double>(T) * o.k / c.n_experts;
   const int bn1 = h->tile_gateup ? h->tile_gateup : choose_tile(mean_rows, 256);
   const int bn2 = h->tile_down ? h->tile_down : choose_tile(mean_rows, 256);
+  // 256-row token tiles run on CTA pairs (M = 256 weight rows per pair)
+  const int i128 = tile_index(128);
+  const bool pair1 = h->use_pairs && bn1 == 256;
+  const bool pair2 = h->use_pairs && bn2 == 256 && c.d_model % 256 == 0;
 
   moe::GemmArgs a{};
   a.offsets = h->offsets;
@@ -258,11 +263,6 @@ int enqueue_forward(moe_handle* h, const void* x, int T, CallOpts o, void* y, cu
   a.G = h->G;
   a.F = c.ffn_width;
   a.Tk = T * o.k;
-
-  // 256-row token tiles run on CTA pairs (M = 256 weight rows per pair)
-  const int i128 = tile_index(128);
-  const bool pair1 = h->use_pairs && bn1 == 256;
-  const bool pair2 = h->use_pairs && bn2 == 256 && c.d_model % 256 == 0;
 
   a.out = h->hbuf;
   a.K = c.d_model;
@@ -289,6 +289,7 @@ int enqueue_forward(moe_handle* h, const void* x, int T, CallOpts o, void* y, cu
   MOE_CUDA(moe::launch_combine(static_cast<const float*>(h->yp), h->inv, T, o.k, c.d_model, c.has_shared, y,
                                c.out_fp32, s));
   MOE_MARK(6);
+  h->last_kernels = 7;  // router GEMM, top-k, dispatch, gather, gate/up, down, combine
   return MOE_OK;
 }
 
@@ -455,6 +456,7 @@ int moe_forward_ex(moe_handle* h, const void* x, int T, const moe_call_options* 
   if (rc != MOE_OK) return rc;
   CallOpts o;
   if ((rc = resolve_opts(h, opt, &o)) != MOE_OK) return rc;
+  h->last_kernels = 0;
   if (T == 0) return MOE_OK;
   if (y == nullptr || !aligned(y, 16)) return MOE_ERR_INVALID_ARG;
   if (!is_device_ptr(x) || !is_device_ptr(y)) return MOE_ERR_INVALID_ARG;
@@ -503,6 +505,11 @@ int moe_forward_host(moe_handle* h, const void* x_host, int T, void* y_host, voi
   MOE_CUDA(cudaMemcpyAsync(y_host, h->y_stage, ybytes, cudaMemcpyDeviceToHost, s));
   MOE_CUDA(cudaStreamSynchronize(s));
   return MOE_OK;
+}
+
+int moe_last_kernel_count(const moe_handle* h) {
+  if (h == nullptr || h->magic != kMagic) return -1;
+  return h->last_kernels;
 }
 
 int moe_check(moe_handle* h, void* stream) {

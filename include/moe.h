@@ -168,6 +168,15 @@ int moe_forward_host(moe_handle* h, const void* x_host, int T, void* y_host, voi
 int moe_check(moe_handle* h, void* stream);
 
 /*
+ * Number of kernels the last moe_forward / moe_forward_ex / moe_forward_host
+ * on this handle enqueued (0 after a call with T = 0; otherwise the router
+ * GEMM, top-k, dispatch, row gather, gate/up, down and combine kernels).
+ * Host-only, never synchronises.  Returns -1 for an invalid handle.  No
+ * counterpart in the pages: instrumentation for launch accounting.
+ */
+int moe_last_kernel_count(const moe_handle* h);
+
+/*
  * Upper bound, in nanoseconds, on every pipeline wait inside the kernels of
  * this handle (default 2e9).  A wait that exceeds it makes the kernel record
  * MOE_ERR_DEVICE, drain the copies it started, release its tensor memory and

@@ -18,11 +18,13 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
 
 
-def make_layer(inp, max_tokens=None, tiles=(0, 0), out_fp32=False, has_shared=True):
+def make_layer(inp, max_tokens=None, tiles=(0, 0), out_fp32=False, has_shared=True, env=None):
     x, wr, wgu, wd = to_dev(inp, DEV)
-    old = {kk: os.environ.get(kk) for kk in ("MOE_TILE_N_GATEUP", "MOE_TILE_N_DOWN")}
-    os.environ["MOE_TILE_N_GATEUP"] = str(tiles[0])
-    os.environ["MOE_TILE_N_DOWN"] = str(tiles[1])
+    env = dict(env or {})
+    env.setdefault("MOE_TILE_N_GATEUP", str(tiles[0]))
+    env.setdefault("MOE_TILE_N_DOWN", str(tiles[1]))
+    old = {kk: os.environ.get(kk) for kk in env}
+    os.environ.update(env)
     try:
         layer = binding.MoeLayer(wr, wgu, wd, inp.shape.k, max_tokens or max(1, inp.shape.T),
                                  has_shared=has_shared, out_fp32=out_fp32)
@@ -83,6 +85,16 @@ def test_several_weight_tiles_and_k_steps():
     shape = synth.LayerShape(T=200, d=512, E=32, k=4, F=256)
     inp = synth.make_inputs(shape, seed=5)
     run_and_check(inp)
+
+
+def test_kernel_count_reported():
+    inp = synth.make_inputs(synth.TINY, seed=41)
+    layer, x = make_layer(inp)
+    layer.forward(x)
+    assert layer.last_kernel_count() == 7
+    binding.moe_forward(layer.handle, x[:0], 0, torch.empty_like(x[:0]))
+    assert layer.last_kernel_count() == 0
+    layer.close()
 
 
 def test_every_expert_selected():
