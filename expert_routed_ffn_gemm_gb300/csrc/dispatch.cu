@@ -7,6 +7,8 @@
 // combine gathers a token's rows back and sums them.  Both are deterministic:
 // dispatch orders rows inside an expert by token index with block-local ranks
 // (no order-dependent atomics), combine sums in a fixed order.
+#include <cuda_fp8.h>
+
 #include <mutex>
 
 #include "../../include/moe.h"
@@ -46,7 +48,8 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* 
 __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(const int* __restrict__ idx,
                                                                     const int* __restrict__ counts, int T, int E,
                                                                     int k, int has_shared, int* __restrict__ offsets,
-                                                                    int* __restrict__ perm, int* __restrict__ inv) {
+                                                                    int* __restrict__ perm, int* __restrict__ inv,
+                                                                    int* __restrict__ chunk_base) {
   __shared__ int warp_sums[kDispatchThreads / 32];
   const int e = blockIdx.x;
 
@@ -73,6 +76,19 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(const int* _
       offsets[E] = total;
       offsets[E + 1] = total + (has_shared ? T : 0);
     }
+    // chunk_base[0..E+1]: the same scan over ceil(count / kYpRows)
+    local = 0;
+    for (int i = b; i < min(E, b + per); ++i) local += (counts[i] + kYpRows - 1) / kYpRows;
+    const int cpre = block_exclusive_scan(local, warp_sums, &total);
+    run = cpre;
+    for (int i = b; i < min(E, b + per); ++i) {
+      chunk_base[i] = run;
+      run += (counts[i] + kYpRows - 1) / kYpRows;
+    }
+    if (threadIdx.x == 0) {
+      chunk_base[E] = total;
+      chunk_base[E + 1] = total + (has_shared ? (T + kYpRows - 1) / kYpRows : 0);
+    }
   }
 
   int running = 0;
@@ -96,37 +112,73 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(const int* _
   }
 }
 
-// One warp per dispatch row: xp[pos] = x[token(pos)], 16-byte vectors.
+// One warp per dispatch row: xp[pos] = x[token(pos)], 16-byte vectors; with
+// to_f16 each bf16 value is rewritten as the nearest fp16.
+template <bool TO_F16>
 __global__ void __launch_bounds__(256) gather_kernel(const bf16* __restrict__ x, const int* __restrict__ perm,
-                                                     int T, int k, int d, int rows, bf16* __restrict__ xp) {
+                                                     int T, int k, int d, int rows, void* __restrict__ xp) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (warp >= rows) return;
   const int Tk = T * k;
   const int t = (warp < Tk) ? (__ldg(perm + warp) / k) : (warp - Tk);
   const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * d);
-  uint4* dst = reinterpret_cast<uint4*>(xp + static_cast<size_t>(warp) * d);
-  for (int c = lane; c < d / 8; c += 32) dst[c] = __ldg(src + c);
+  uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(xp) + static_cast<size_t>(warp) * d);
+  for (int c = lane; c < d / 8; c += 32) {
+    uint4 v = __ldg(src + c);
+    if (TO_F16) {
+      uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
+        w[i] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(lo))) |
+               (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(hi))) << 16);
+      }
+    }
+    dst[c] = v;
+  }
 }
 
+// 2^e for an int8 exponent in [-126, 113], exact.
+__device__ __forceinline__ float pow2i(int e) { return __uint_as_float(static_cast<uint32_t>(e + 127) << 23); }
+
 // One block per token: y[t] = Yp[inv[t*k+0]] + ... + Yp[inv[t*k+k-1]] + Yp[T*k+t],
-// summed in fp32 in that order (Yp rows are fp32).  d/8 threads (<= 1024): one
-// 8-element chunk each, so every load of a token is in flight at once.
-__global__ void __launch_bounds__(1024) combine_kernel(const float* __restrict__ yp, const int* __restrict__ inv,
-                                                      int T, int k, int d, int has_shared, void* __restrict__ y,
-                                                      int out_fp32) {
+// summed in fp32 in that order.  Each term is read back exactly as h * 2^e
+// (h fp16 from yp, e the int8 exponent of its feature in the row's chunk).
+// d/8 threads (<= 1024): one 8-element chunk each, so every load of a token is
+// in flight at once.
+__global__ void __launch_bounds__(1024, 1) combine_kernel(const __half* __restrict__ yp,
+                                                          const int8_t* __restrict__ yexp,
+                                                          const int* __restrict__ idx, const int* __restrict__ inv,
+                                                          const int* __restrict__ offsets,
+                                                          const int* __restrict__ chunk_base, int T, int k, int E,
+                                                          int d, int has_shared, void* __restrict__ y,
+                                                          int out_fp32) {
   const int t = blockIdx.x;
   __shared__ int pos[kMaxTopK + 1];
-  if (threadIdx.x < k) pos[threadIdx.x] = __ldg(inv + static_cast<size_t>(t) * k + threadIdx.x);
-  if (threadIdx.x == 0) pos[k] = T * k + t;
+  __shared__ int chunk[kMaxTopK + 1];
+  if (threadIdx.x <= k) {
+    const int j = threadIdx.x;
+    const int g = (j < k) ? __ldg(idx + static_cast<size_t>(t) * k + j) : E;
+    const int p = (j < k) ? __ldg(inv + static_cast<size_t>(t) * k + j) : T * k + t;
+    pos[j] = p;
+    chunk[j] = __ldg(chunk_base + g) + (p - __ldg(offsets + g)) / kYpRows;
+  }
   __syncthreads();
   const int nterms = k + (has_shared ? 1 : 0);
   for (int c = threadIdx.x; c < d / 8; c += blockDim.x) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int j = 0; j < nterms; ++j) {
-      const float4* src = reinterpret_cast<const float4*>(yp + static_cast<size_t>(pos[j]) * d) + 2 * c;
-      const float4 a = __ldcs(src), b = __ldcs(src + 1);
-      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+      const uint4 raw = __ldcs(reinterpret_cast<const uint4*>(yp + static_cast<size_t>(pos[j]) * d) + c);
+      const uint2 ex = __ldg(reinterpret_cast<const uint2*>(yexp + static_cast<size_t>(chunk[j]) * d) + c);
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+      const uint32_t eb[2] = {ex.x, ex.y};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int e0 = static_cast<int8_t>((eb[i >> 1] >> (16 * (i & 1))) & 0xffu);
+        const int e1 = static_cast<int8_t>((eb[i >> 1] >> (16 * (i & 1) + 8)) & 0xffu);
+        acc[2 * i] += __half2float(__ushort_as_half(static_cast<unsigned short>(w[i] & 0xffffu))) * pow2i(e0);
+        acc[2 * i + 1] += __half2float(__ushort_as_half(static_cast<unsigned short>(w[i] >> 16))) * pow2i(e1);
+      }
     }
     if (out_fp32) {
       float4* dst = reinterpret_cast<float4*>(static_cast<float*>(y) + static_cast<size_t>(t) * d) + 2 * c;
@@ -148,26 +200,65 @@ __global__ void __launch_bounds__(1024) combine_kernel(const float* __restrict__
 }  // namespace
 
 cudaError_t launch_dispatch(const int* idx, const int* counts, int T, int E, int k, int has_shared, int* offsets,
-                            int* perm, int* inv, cudaStream_t stream) {
-  dispatch_kernel<<<E, kDispatchThreads, 0, stream>>>(idx, counts, T, E, k, has_shared, offsets, perm, inv);
+                            int* perm, int* inv, int* chunk_base, cudaStream_t stream) {
+  dispatch_kernel<<<E, kDispatchThreads, 0, stream>>>(idx, counts, T, E, k, has_shared, offsets, perm, inv,
+                                                      chunk_base);
   return cudaGetLastError();
 }
 
-cudaError_t launch_gather(const bf16* x, const int* perm, int T, int k, int d, int has_shared, bf16* xp,
-                          cudaStream_t stream) {
+cudaError_t launch_gather(const bf16* x, const int* perm, int T, int k, int d, int has_shared, void* xp,
+                          bool to_f16, cudaStream_t stream) {
   const int rows = T * k + (has_shared ? T : 0);
   if (rows == 0) return cudaSuccess;
   const int blocks = (rows + 7) / 8;
-  gather_kernel<<<blocks, 256, 0, stream>>>(x, perm, T, k, d, rows, xp);
+  if (to_f16)
+    gather_kernel<true><<<blocks, 256, 0, stream>>>(x, perm, T, k, d, rows, xp);
+  else
+    gather_kernel<false><<<blocks, 256, 0, stream>>>(x, perm, T, k, d, rows, xp);
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const float* yp, const int* inv, int T, int k, int d, int has_shared, void* y,
-                           int out_fp32, cudaStream_t stream) {
+// One block per row: the row's largest magnitude by a block reduction, then
+// every element divided by the scale and rounded to E4M3 (satfinite).
+__global__ void __launch_bounds__(256) quantize_e4m3_kernel(const bf16* __restrict__ w, int cols,
+                                                            uint8_t* __restrict__ q, float* __restrict__ s) {
+  __shared__ float red[8];
+  const size_t r = blockIdx.x;
+  const bf16* row = w + r * cols;
+  float amax = 0.f;
+  for (int i = threadIdx.x; i < cols; i += 256) amax = fmaxf(amax, fabsf(__bfloat162float(row[i])));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+  const float sc = __fdiv_rn(amax, 448.0f);
+  if (threadIdx.x == 0) s[r] = sc;
+  for (int i = threadIdx.x; i < cols; i += 256) {
+    const float v = __bfloat162float(row[i]);
+    q[r * cols + i] =
+        sc > 0.f ? static_cast<uint8_t>(__nv_cvt_float_to_fp8(__fdiv_rn(v, sc), __NV_SATFINITE, __NV_E4M3)) : 0;
+  }
+}
+
+cudaError_t launch_quantize_e4m3(const bf16* w, long long rows, int cols, uint8_t* q, float* s,
+                                 cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  if (rows > 0x7fffffffll) return cudaErrorInvalidValue;
+  quantize_e4m3_kernel<<<static_cast<unsigned>(rows), 256, 0, stream>>>(w, cols, q, s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const __half* yp, const int8_t* yexp, const int* idx, const int* inv,
+                           const int* offsets, const int* chunk_base, int T, int k, int E, int d, int has_shared,
+                           void* y, int out_fp32, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   const int chunks = d / 8;
   const int threads = chunks > 1024 ? 1024 : (chunks < 32 ? 32 : chunks);
-  combine_kernel<<<T, threads, 0, stream>>>(yp, inv, T, k, d, has_shared, y, out_fp32);
+  combine_kernel<<<T, threads, 0, stream>>>(yp, yexp, idx, inv, offsets, chunk_base, T, k, E, d, has_shared, y,
+                                            out_fp32);
   return cudaGetLastError();
 }
 

@@ -222,8 +222,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         epilogue_gateup<BN>(taddr, row, it.m * (kBlockM / 2), row0, valid, static_cast<bf16*>(args.out),
                             args.out_ld, xchg, chunk_par);
       } else {
-        epilogue_down<BN>(taddr, it.m * kBlockM + row, row0, valid, wreg, static_cast<float*>(args.out),
-                          args.out_ld);
+        epilogue_down<BN>(taddr, it.m * kBlockM + row, row0, valid, wreg, static_cast<__half*>(args.out),
+                          args.out_exp, args.out_ld, __ldg(args.chunk_base + it.g) + it.n * (BN / kYpRows));
       }
       tc_fence_before();
       __syncwarp();

@@ -246,7 +246,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 static_cast<bf16*>(args.out), args.out_ld, xchg, chunk_par);
       } else {
         epilogue_down<kPairN>(taddr, it.m * 2 * kBlockM + static_cast<int>(rank) * kBlockM + row, row0, valid,
-                              wreg, static_cast<float*>(args.out), args.out_ld);
+                              wreg, static_cast<__half*>(args.out), args.out_exp, args.out_ld,
+                              __ldg(args.chunk_base + it.g) + it.n * (kPairN / kYpRows));
       }
       tc_fence_before();
       __syncwarp();

@@ -3,6 +3,8 @@
 // CTA-wide abort flag, and the two epilogues (SiLU gate for gate/up, gate
 // weight scale for down) that read one TMEM accumulator of BN columns.
 #pragma once
+#include <cuda_fp16.h>
+
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -101,14 +103,20 @@ __device__ __forceinline__ bool epilogue_wait(uint64_t* acc_full, uint32_t parit
   return all_ok;
 }
 
+__device__ __forceinline__ bf16 to_out(float v, bf16*) { return __float2bfloat16_rn(v); }
+__device__ __forceinline__ __half to_out(float v, __half*) { return __float2half_rn(v); }
+
 // K3 epilogue over the `valid` columns of a BN-column accumulator whose TMEM
 // rows 0..63 hold gate values and rows 64..127 the up values of the same 64
 // features.  Gate-row threads keep columns 0..7 of each 16-column chunk and
 // hand 8..15 to their up-row partner through xchg ([2][2][64][8] fp32), which
-// hands back 0..7; H[row0 + col][feat_base + (row & 63)] = silu(g) * u.
-template <int BN>
+// hands back 0..7; H[row0 + col][feat_base + (row & 63)] = silu(g) * u, where
+// g and u are the accumulators times the `scale` of their own weight row (1
+// for bf16 weights).  H is bf16 or fp16 (OutT).
+template <int BN, typename OutT>
 __device__ __forceinline__ void epilogue_gateup(uint32_t taddr, int row, int feat_base, int row0, int valid,
-                                                bf16* H, int ldh, float* xchg, uint32_t& chunk_par) {
+                                                OutT* H, int ldh, float* xchg, uint32_t& chunk_par,
+                                                float scale = 1.0f) {
   const bool is_gate = row < 64;
   const int fl = row & 63;
   const int feat = feat_base + fl;
@@ -123,8 +131,8 @@ __device__ __forceinline__ void epilogue_gateup(uint32_t taddr, int row, int fea
     float give[8], keep[8];  // compile-time register indices only
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-      give[c] = __uint_as_float(is_gate ? v[8 + c] : v[c]);
-      keep[c] = __uint_as_float(is_gate ? v[c] : v[8 + c]);
+      give[c] = scale * __uint_as_float(is_gate ? v[8 + c] : v[c]);
+      keep[c] = scale * __uint_as_float(is_gate ? v[c] : v[8 + c]);
     }
     reinterpret_cast<float4*>(mine_out)[0] = make_float4(give[0], give[1], give[2], give[3]);
     reinterpret_cast<float4*>(mine_out)[1] = make_float4(give[4], give[5], give[6], give[7]);
@@ -136,7 +144,7 @@ __device__ __forceinline__ void epilogue_gateup(uint32_t taddr, int row, int fea
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
       const float h = is_gate ? silu_mul(keep[c], peer[c]) : silu_mul(peer[c], keep[c]);
-      if (col0 + c < valid) H[static_cast<size_t>(row0 + col0 + c) * ldh + feat] = __float2bfloat16_rn(h);
+      if (col0 + c < valid) H[static_cast<size_t>(row0 + col0 + c) * ldh + feat] = to_out(h, H);
     }
     chunk_par ^= 1u;
   }
@@ -155,22 +163,48 @@ __device__ __forceinline__ void load_gate_weights(float (&wreg)[(BN + 31) / 32],
   }
 }
 
-// K4 epilogue: Y[row0 + col][feat] = w_col * acc[col] for the valid columns.
+// Power-of-two exponent for a block of values whose largest magnitude has the
+// fp32 bit pattern `amax`: 2^-e * amax lands in [2^14, 2^15), so every value of
+// the block scaled by 2^-e is an fp16 normal or zero below 2^15 (no overflow)
+// carrying 11 significant bits relative to the block's largest value.  Clamped
+// to [-126, kYpExpMax] so that 2^-e and 2^e are fp32 normals.
+__device__ __forceinline__ int block_exponent(uint32_t amax) {
+  const int e = static_cast<int>((amax >> 23) & 0xffu) - 141;
+  return e < -126 ? -126 : (e > kYpExpMax ? kYpExpMax : e);
+}
+
+// K4 epilogue: Yp[row0 + col][feat] = w_col * (row_scale * acc[col]) for the
+// valid columns (row_scale: the weight row's scale, 1 for bf16 weights),
+// stored scaled: the 16 columns of a chunk are kYpRows consecutive rows of the
+// group, and this thread's feature over them forms one block; its exponent e
+// (from the thread's own maximum, no exchange) goes to Ye[chunk0 + c0/16][feat]
+// and the values to Y as fp16 of value * 2^-e.  chunk0 = the exponent chunk of
+// the tile's first row (tile rows start at multiples of 16 inside the group).
 template <int BN>
 __device__ __forceinline__ void epilogue_down(uint32_t taddr, int feat, int row0, int valid,
-                                              const float (&wreg)[(BN + 31) / 32], float* Y, int ldy) {
+                                              const float (&wreg)[(BN + 31) / 32], __half* Y, int8_t* Ye, int ldy,
+                                              int chunk0, float row_scale = 1.0f) {
+  static_assert(kYpRows == 16, "one exponent chunk per 16-column TMEM load");
 #pragma unroll
   for (int c0 = 0; c0 < BN; c0 += 16) {
     if (c0 >= valid) break;
     uint32_t v[16];
     tmem_ld16(taddr + c0, v);
     tmem_ld_wait();
+    float y[16];
+    uint32_t amax = 0;
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
       const int col = c0 + c;
-      const float w = __shfl_sync(0xffffffffu, wreg[col >> 5], col & 31);
-      if (col < valid) Y[static_cast<size_t>(row0 + col) * ldy + feat] = w * __uint_as_float(v[c]);
+      y[c] = __shfl_sync(0xffffffffu, wreg[col >> 5], col & 31) * (row_scale * __uint_as_float(v[c]));
+      amax = max(amax, __float_as_uint(y[c]) & 0x7fffffffu);
     }
+    const int e = block_exponent(amax);
+    const float down = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, exact
+    Ye[static_cast<size_t>(chunk0 + c0 / 16) * ldy + feat] = static_cast<int8_t>(e);
+#pragma unroll
+    for (int c = 0; c < 16; ++c)
+      if (c0 + c < valid) Y[static_cast<size_t>(row0 + c0 + c) * ldy + feat] = __float2half_rn(y[c] * down);
   }
 }
 

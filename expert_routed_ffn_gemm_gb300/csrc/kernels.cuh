@@ -3,6 +3,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -16,6 +17,14 @@ constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 32;
 constexpr int kMaxKSplit = 16;  // K splits of the router GEMM
 constexpr int kMaxStatGroups = 64;  // expert groups of the routing statistics
+
+// Expert outputs Yp (one row per dispatch position) are kept as fp16 with a
+// power-of-two scale per feature and chunk of kYpRows consecutive rows of one
+// group: value = h * 2^e, h fp16, e int8 in [-126, kYpExpMax].  Chunks are
+// numbered group by group: group g's chunks start at chunk_base[g] =
+// sum over g' < g of ceil(rows(g') / kYpRows); the exponents are [chunk][d].
+constexpr int kYpRows = 16;
+constexpr int kYpExpMax = 113;
 
 // Token-tile widths (N of tcgen05.mma) the grouped GEMMs are built for.
 constexpr int kNumTileN = 5;
@@ -45,20 +54,25 @@ cudaError_t launch_route_stats(const float* tokstats, const int* counts, int T, 
 cudaError_t launch_split_router(const float* w, int E, int d, int e_pad, bf16* w3, cudaStream_t stream);
 cudaError_t router_gemm_prepare();
 
-// K2: offsets (exclusive scan of counts, shared group appended) and the
-// stable expert-major permutation perm / its inverse inv.
+// K2: offsets (exclusive scan of counts, shared group appended), the stable
+// expert-major permutation perm / its inverse inv, and chunk_base [E+2] (the
+// exponent chunks of the expert outputs, see kYpRows).
 cudaError_t launch_dispatch(const int* idx, const int* counts, int T, int E, int k, int has_shared, int* offsets,
-                            int* perm, int* inv, cudaStream_t stream);
+                            int* perm, int* inv, int* chunk_base, cudaStream_t stream);
 
-// Gather of token rows into dispatch order: xp[pos] = x[token(pos)].
-cudaError_t launch_gather(const bf16* x, const int* perm, int T, int k, int d, int has_shared, bf16* xp,
-                          cudaStream_t stream);
+// Gather of token rows into dispatch order: xp[pos] = x[token(pos)]; with
+// to_f16 the rows are written as fp16 (x's bf16 values rounded to nearest).
+cudaError_t launch_gather(const bf16* x, const int* perm, int T, int k, int d, int has_shared, void* xp,
+                          bool to_f16, cudaStream_t stream);
 
 struct GemmArgs {
   const int* offsets;  // [G+1] row offsets of the groups in dispatch order
   const int* perm;     // [T*k] (down projection: gate weight lookup)
   const float* prob;   // [T*k] (down projection)
-  void* out;           // H bf16 [R][F] (gate/up) or Yp fp32 [R][d] (down)
+  void* out;           // H bf16 [R][F] (gate/up) or Yp fp16 [R][d] (down)
+  int8_t* out_exp;     // down: Yp exponents [chunks][d]
+  const int* chunk_base;  // down: [G+1] first exponent chunk of each group
+  const float* w_scale;   // FP8 weights: scale of every weight row [G][rows_per_group]
   uint32_t* err;       // device error word
   unsigned long long wait_limit_ns;
   int G;               // groups (E + has_shared)
@@ -87,9 +101,25 @@ cudaError_t launch_expert_gemm_pair(bool gateup, const CUtensorMap* map_w, const
                                     const GemmArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t expert_gemm_pair_prepare();
 
-// K5: y[t] = sum_j Yp[inv[t*k+j]] + Yp[T*k + t], fp32 in fixed order.
-cudaError_t launch_combine(const float* yp, const int* inv, int T, int k, int d, int has_shared, void* y,
-                           int out_fp32, cudaStream_t stream);
+// K3/K4 with E4M3 weights (one fp32 scale per weight row in a.w_scale) and
+// fp16 activations; tile_n in {16, 32, 64, 128}.  map_w: the E4M3 codes as
+// [G * rows_per_group][K] bytes, box 128 x 64 rows (gate/up) or 128 x 128
+// (down); map_act: the fp16 token rows or H, box 64 x tile_n.
+cudaError_t launch_expert_gemm_fp8(bool gateup, int tile_n, const CUtensorMap* map_w, const CUtensorMap* map_act,
+                                   const GemmArgs& a, int num_sms, cudaStream_t stream);
+cudaError_t expert_gemm_fp8_prepare();
+
+// Per-row E4M3 quantisation of bf16 rows: s[r] = max |w[r]| / 448, q = nearest
+// E4M3 (ties to even, saturating) of w / s (fp32 quotient); zero rows: s = 0, q = 0.
+cudaError_t launch_quantize_e4m3(const bf16* w, long long rows, int cols, uint8_t* q, float* s,
+                                 cudaStream_t stream);
+
+// K5: y[t] = sum_j Yp[inv[t*k+j]] + Yp[T*k + t], fp32 in fixed order, each
+// term read back as h * 2^e from the scaled fp16 Yp and its exponents (the
+// chunk of a row found from its expert idx[t*k+j], offsets and chunk_base).
+cudaError_t launch_combine(const __half* yp, const int8_t* yexp, const int* idx, const int* inv,
+                           const int* offsets, const int* chunk_base, int T, int k, int E, int d, int has_shared,
+                           void* y, int out_fp32, cudaStream_t stream);
 
 // Bounded-wait self test: waits on a barrier that never completes.
 cudaError_t launch_wait_selftest(uint32_t* err, unsigned long long limit_ns, cudaStream_t stream);

@@ -7,6 +7,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstdint>
+#include <algorithm>
 #include <cstdlib>
 #include <cstring>
 #include <array>
@@ -35,6 +36,9 @@ struct moe_handle {
   bool use_pairs;   // 256-row token tiles on CTA pairs (MOE_PAIR_TILES=0 turns it off)
   int router_tile;  // router token tile, 0 = by T (MOE_ROUTER_TILE = 16, 64, 128 or 256)
   int last_kernels;   // kernels enqueued by the last forward call
+  bool fp8;           // E4M3 expert weights with per-row scales (moe_init_fp8)
+  const float* s_gate_up;  // fp8: [G][2F] row scales
+  const float* s_down;     // fp8: [G][d] row scales
   unsigned long long wait_limit_ns;
   int router_m_tiles;      // ceil(E / 128)
   long long partial_rows;  // capacity of `partial` in (split, token) rows
@@ -48,7 +52,11 @@ struct moe_handle {
   int* perm;       // [Tmax*k]
   int* inv;        // [Tmax*k]
   int* offsets;    // [E+2]
-  float* yp;       // [(k+1)*Tmax][d]: token rows in dispatch order (bf16), then the expert outputs
+  void* yp;        // [(k+1)*Tmax][d] 16-bit: token rows in dispatch order (bf16), then the expert
+                   // outputs (fp16, block-scaled by yexp)
+  int8_t* yexp;    // [(k+1)*Tmax/16 + E + 2][d] exponents of the expert outputs (per feature and
+                   // chunk of 16 rows of a group)
+  int* chunk_base; // [E+2] first exponent chunk of each group
   bf16* hbuf;      // [(k+1)*Tmax][F] H
   bf16* x_stage;   // [Tmax][d] (host entry point)
   void* y_stage;   // [Tmax][d] bf16 or fp32 (host entry point)
@@ -57,6 +65,7 @@ struct moe_handle {
   CUtensorMap map_w3;                   // W_r slices as [3*e_pad][d], box 64 x 128
   CUtensorMap map_wgu;                  // W_gu as [G*2F][d], box 64 x 64
   CUtensorMap map_wd;                   // W_d  as [G*d][F], box 64 x 128
+                                        // (fp8: E4M3 bytes, boxes 128 x 64 / 128 x 128)
   CUtensorMap map_xp[moe::kNumTileN];   // Xp   as [Rmax][d] bf16 (in yp), box 64 x BN
   CUtensorMap map_h[moe::kNumTileN];    // H    as [Rmax][F], box 64 x BN
   // per-stage timing (moe_profile_enable)
@@ -87,14 +96,18 @@ bool load_encode() {
 
 // 2-D bf16 tensor map over a row-major [rows][cols] matrix, box = 64 columns
 // (128 bytes, the swizzle width) x box_rows rows, 128-byte swizzle.
-bool encode_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// 2-D row-major map with the 128-byte swizzle: 16-bit elements (box 64
+// columns) or, with bytes = true, 8-bit codes (box 128 columns).
+bool encode_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+               bool bytes = false) {
   cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(moe::kBlockK), box_rows};
+  cuuint64_t strides[1] = {cols * (bytes ? 1 : 2)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(bytes ? 128 : moe::kBlockK), box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = g_encode(map, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                        const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -201,7 +214,8 @@ int enqueue_route(moe_handle* h, const void* x, int T, CallOpts o, int* idx, flo
   const moe_config& c = h->cfg;
   const int rc = enqueue_router(h, x, T, o, idx, prob, gap, nullptr, 0, s);
   if (rc != MOE_OK) return rc;
-  MOE_CUDA(moe::launch_dispatch(idx, h->counts, T, c.n_experts, o.k, c.has_shared, offsets, perm, h->inv, s));
+  MOE_CUDA(moe::launch_dispatch(idx, h->counts, T, c.n_experts, o.k, c.has_shared, offsets, perm, h->inv,
+                                h->chunk_base, s));
   return MOE_OK;
 }
 
@@ -240,15 +254,17 @@ int enqueue_forward(moe_handle* h, const void* x, int T, CallOpts o, void* y, cu
   if (rc != MOE_OK) return rc;
   MOE_MARK(1);
   MOE_CUDA(moe::launch_dispatch(h->idx, h->counts, T, c.n_experts, o.k, c.has_shared, h->offsets, h->perm, h->inv,
-                                s));
+                                h->chunk_base, s));
   MOE_MARK(2);
   // token rows in dispatch order (the yp buffer holds them until the down GEMM)
-  bf16* xp = reinterpret_cast<bf16*>(h->yp);
-  MOE_CUDA(moe::launch_gather(static_cast<const bf16*>(x), h->perm, T, o.k, c.d_model, c.has_shared, xp, s));
+  // (fp8 weights: as fp16, the tensor cores' input type there)
+  MOE_CUDA(moe::launch_gather(static_cast<const bf16*>(x), h->perm, T, o.k, c.d_model, c.has_shared, h->yp, h->fp8,
+                              s));
   MOE_MARK(3);
   const double mean_rows = static_cast<double>(T) * o.k / c.n_experts;
-  const int bn1 = h->tile_gateup ? h->tile_gateup : choose_tile(mean_rows, 256);
-  const int bn2 = h->tile_down ? h->tile_down : choose_tile(mean_rows, 256);
+  const int cap = h->fp8 ? 128 : 256;
+  const int bn1 = h->tile_gateup ? std::min(h->tile_gateup, cap) : choose_tile(mean_rows, cap);
+  const int bn2 = h->tile_down ? std::min(h->tile_down, cap) : choose_tile(mean_rows, cap);
   // 256-row token tiles run on CTA pairs (M = 256 weight rows per pair)
   const int i128 = tile_index(128);
   const bool pair1 = h->use_pairs && bn1 == 256;
@@ -270,24 +286,32 @@ int enqueue_forward(moe_handle* h, const void* x, int T, CallOpts o, void* y, cu
   a.m_tiles = pair1 ? c.ffn_width / moe::kBlockM : c.ffn_width / (moe::kBlockM / 2);
   a.out_ld = c.ffn_width;
   const int i1 = tile_index(bn1), i2 = tile_index(bn2);
-  if (pair1)
+  a.w_scale = h->s_gate_up;
+  if (h->fp8)
+    MOE_CUDA(moe::launch_expert_gemm_fp8(true, bn1, &h->map_wgu, &h->map_xp[i1], a, h->num_sms, s));
+  else if (pair1)
     MOE_CUDA(moe::launch_expert_gemm_pair(true, &h->map_wgu, &h->map_xp[i128], a, h->num_sms, s));
   else
     MOE_CUDA(moe::launch_expert_gemm(true, bn1, &h->map_wgu, &h->map_xp[i1], a, h->num_sms, s));
   MOE_MARK(4);
 
   a.out = h->yp;
+  a.out_exp = h->yexp;
+  a.chunk_base = h->chunk_base;
   a.K = c.ffn_width;
   a.rows_per_group = c.d_model;
   a.m_tiles = pair2 ? c.d_model / (2 * moe::kBlockM) : c.d_model / moe::kBlockM;
   a.out_ld = c.d_model;
-  if (pair2)
+  a.w_scale = h->s_down;
+  if (h->fp8)
+    MOE_CUDA(moe::launch_expert_gemm_fp8(false, bn2, &h->map_wd, &h->map_h[i2], a, h->num_sms, s));
+  else if (pair2)
     MOE_CUDA(moe::launch_expert_gemm_pair(false, &h->map_wd, &h->map_h[i128], a, h->num_sms, s));
   else
     MOE_CUDA(moe::launch_expert_gemm(false, bn2, &h->map_wd, &h->map_h[i2], a, h->num_sms, s));
   MOE_MARK(5);
-  MOE_CUDA(moe::launch_combine(static_cast<const float*>(h->yp), h->inv, T, o.k, c.d_model, c.has_shared, y,
-                               c.out_fp32, s));
+  MOE_CUDA(moe::launch_combine(static_cast<const __half*>(h->yp), h->yexp, h->idx, h->inv, h->offsets,
+                               h->chunk_base, T, o.k, c.n_experts, c.d_model, c.has_shared, y, c.out_fp32, s));
   MOE_MARK(6);
   h->last_kernels = 7;  // router GEMM, top-k, dispatch, gather, gate/up, down, combine
   return MOE_OK;
@@ -312,10 +336,17 @@ const char* moe_status_string(int status) {
   }
 }
 
-int moe_init(const moe_config* cfg, const moe_weights* w, moe_handle** out) {
+}  // extern "C"
+
+namespace {
+
+// moe_init and moe_init_fp8: w holds the router and the two expert weight
+// arrays (bf16, or E4M3 codes when s_gu / s_d, the row scales, are given).
+int init_any(const moe_config* cfg, const moe_weights* w, const float* s_gu, const float* s_d, moe_handle** out) {
   if (out == nullptr) return MOE_ERR_INVALID_ARG;
   *out = nullptr;
   if (cfg == nullptr || w == nullptr) return MOE_ERR_INVALID_ARG;
+  const bool fp8 = s_gu != nullptr;
   const moe_config c = *cfg;
   if (c.d_model <= 0 || c.n_experts <= 0 || c.top_k <= 0 || c.ffn_width <= 0 || c.max_tokens <= 0)
     return MOE_ERR_INVALID_ARG;
@@ -344,15 +375,20 @@ int moe_init(const moe_config* cfg, const moe_weights* w, moe_handle** out) {
   if (major != 10 || minor != 3) return MOE_ERR_NO_DEVICE;
   if (!is_device_ptr(w->w_router) || !is_device_ptr(w->w_gate_up) || !is_device_ptr(w->w_down))
     return MOE_ERR_INVALID_ARG;
+  if (fp8 && (!aligned(s_gu, 4) || !aligned(s_d, 4) || !is_device_ptr(s_gu) || !is_device_ptr(s_d)))
+    return MOE_ERR_INVALID_ARG;
   if (!load_encode()) return MOE_ERR_CUDA;
   if (moe::expert_gemm_prepare() != cudaSuccess || moe::expert_gemm_pair_prepare() != cudaSuccess ||
-      moe::router_gemm_prepare() != cudaSuccess)
+      moe::router_gemm_prepare() != cudaSuccess || moe::expert_gemm_fp8_prepare() != cudaSuccess)
     return MOE_ERR_CUDA;
 
   moe_handle* h = new (std::nothrow) moe_handle();
   if (h == nullptr) return MOE_ERR_CUDA;
   h->cfg = c;
   h->w = *w;
+  h->fp8 = fp8;
+  h->s_gate_up = s_gu;
+  h->s_down = s_d;
   h->device = dev;
   h->num_sms = sms;
   h->G = c.n_experts + c.has_shared;
@@ -383,7 +419,9 @@ int moe_init(const moe_config* cfg, const moe_weights* w, moe_handle** out) {
   const size_t o_counts = carve(4 * E), o_err = carve(16), o_offsets = carve(4 * (E + 2)),
                o_partial = carve(4 * p_rows * E), o_w3 = carve(2 * 3 * e_pad * d), o_idx = carve(4 * Tmax * k),
                o_prob = carve(4 * Tmax * k), o_perm = carve(4 * Tmax * k), o_inv = carve(4 * Tmax * k),
-               o_yp = carve(4 * R * d), o_h = carve(2 * R * F), o_xs = carve(2 * Tmax * d),
+               o_yp = carve(2 * R * d), o_ye = carve((R / moe::kYpRows + E + 2) * d), o_cb = carve(4 * (E + 2)),
+               o_h = carve(2 * R * F),
+               o_xs = carve(2 * Tmax * d),
                o_ys = carve((c.out_fp32 ? 4 : 2) * Tmax * d),
                o_tok = carve(4 * Tmax * (moe::kMaxStatGroups + 1));
   if (cudaMalloc(&h->ws, off) != cudaSuccess) {
@@ -401,7 +439,9 @@ int moe_init(const moe_config* cfg, const moe_weights* w, moe_handle** out) {
   h->prob = reinterpret_cast<float*>(b + o_prob);
   h->perm = reinterpret_cast<int*>(b + o_perm);
   h->inv = reinterpret_cast<int*>(b + o_inv);
-  h->yp = reinterpret_cast<float*>(b + o_yp);
+  h->yp = b + o_yp;
+  h->yexp = reinterpret_cast<int8_t*>(b + o_ye);
+  h->chunk_base = reinterpret_cast<int*>(b + o_cb);
   h->hbuf = reinterpret_cast<bf16*>(b + o_h);
   h->x_stage = reinterpret_cast<bf16*>(b + o_xs);
   h->y_stage = b + o_ys;
@@ -412,8 +452,8 @@ int moe_init(const moe_config* cfg, const moe_weights* w, moe_handle** out) {
                                       nullptr) == cudaSuccess;
   const size_t G = h->G;
   ok = ok && encode_2d(&h->map_w3, h->w3, 3 * e_pad, d, moe::kBlockM);
-  ok = ok && encode_2d(&h->map_wgu, w->w_gate_up, G * 2 * F, d, moe::kBlockM / 2);
-  ok = ok && encode_2d(&h->map_wd, w->w_down, G * d, F, moe::kBlockM);
+  ok = ok && encode_2d(&h->map_wgu, w->w_gate_up, G * 2 * F, d, moe::kBlockM / 2, fp8);
+  ok = ok && encode_2d(&h->map_wd, w->w_down, G * d, F, moe::kBlockM, fp8);
   for (int i = 0; ok && i < moe::kNumTileN; ++i) {
     ok = ok && encode_2d(&h->map_xp[i], h->yp, R, d, moe::kTileN[i]);
     ok = ok && encode_2d(&h->map_h[i], h->hbuf, R, F, moe::kTileN[i]);
@@ -427,6 +467,31 @@ int moe_init(const moe_config* cfg, const moe_weights* w, moe_handle** out) {
   }
   h->magic = kMagic;
   *out = h;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_init(const moe_config* cfg, const moe_weights* w, moe_handle** out) {
+  return init_any(cfg, w, nullptr, nullptr, out);
+}
+
+int moe_init_fp8(const moe_config* cfg, const moe_weights_fp8* w, moe_handle** out) {
+  if (out != nullptr) *out = nullptr;
+  if (w == nullptr || w->s_gate_up == nullptr || w->s_down == nullptr) return MOE_ERR_INVALID_ARG;
+  const moe_weights ww{w->w_router, w->w_gate_up, w->w_down};
+  return init_any(cfg, &ww, w->s_gate_up, w->s_down, out);
+}
+
+int moe_quantize_fp8(const void* w, long long rows, int cols, void* q, float* s, void* stream) {
+  if (rows < 0 || cols <= 0 || rows > 0x7fffffffll) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (w == nullptr || q == nullptr || s == nullptr || !aligned(w, 2) || !aligned(s, 4)) return MOE_ERR_INVALID_ARG;
+  if (!is_device_ptr(w) || !is_device_ptr(q) || !is_device_ptr(s)) return MOE_ERR_INVALID_ARG;
+  MOE_CUDA(moe::launch_quantize_e4m3(static_cast<const bf16*>(w), rows, cols, static_cast<uint8_t*>(q), s,
+                                     static_cast<cudaStream_t>(stream)));
   return MOE_OK;
 }
 

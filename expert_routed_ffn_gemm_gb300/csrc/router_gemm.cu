@@ -12,9 +12,10 @@
 // writes its partial logits and the top-k kernel sums the splits in a fixed
 // order, so results are identical run to run.
 //
-// router_topk_kernel: one block of four warps per token sums the K splits; one
-// warp then does softmax and top-k with xor-shuffle butterflies (every lane
-// ends with the same bits); ties go to the lower expert index.
+// Top-k: below 1024 tokens one block of four warps per token sums the K
+// splits, from 1024 tokens on one warp per token does; one warp then does
+// softmax and top-k with xor-shuffle butterflies (every lane ends with the same
+// bits); ties go to the lower expert index.
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -253,6 +254,7 @@ constexpr int kMaxPerLane = kMaxExperts / 32;
 __device__ __forceinline__ bool better(float v, int e, float ov, int oe) { return v > ov || (v == ov && e < oe); }
 
 constexpr int kTopkWarps = 4;
+constexpr int kTopkWarpMinTokens = 1024;  // from this many tokens on: one warp per token
 
 // Compare-exchange of two (value, expert) slots: afterwards slot a ranks
 // first (higher value, then lower expert index).
@@ -267,48 +269,18 @@ __device__ __forceinline__ void cx(float& va, int& ea, float& vb, int& eb) {
   }
 }
 
-// One block of 4 warps per token.  Warp w sums the K-split partials
-// s = w, w+4, ... in increasing s; warp 0 then adds the four partial sums in
-// warp order (a fixed order: logits are bit-identical run to run) and does
-// softmax, top-k (ties: lower index), gap and per-expert counts alone.  Lane
-// l holds experts l, l+32, ...; it sorts its own slots once (bitonic network),
-// after which each of the k+1 selection rounds is one xor-butterfly argmax over
-// the 32 lane heads.  renorm != 0: the k weights are divided by their sum
-// (slot order).  tokstats (or NULL): per token, the probability mass of each of
-// n_groups equal expert groups, then the entropy -sum p ln p ([T][n_groups+1]).
-__global__ void __launch_bounds__(kTopkWarps * 32) router_topk_kernel(const float* __restrict__ partial, int ksplit,
-                                                                      int T, int E, int k, int renorm,
-                                                                      int* __restrict__ idx,
-                                                                      float* __restrict__ prob,
-                                                                      float* __restrict__ gap, int* counts,
-                                                                      float* __restrict__ tokstats, int n_groups) {
-  __shared__ float zs[kTopkWarps][kMaxExperts];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int t = blockIdx.x;
-  float p[kMaxPerLane];
-#pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) p[i] = 0.f;
-#pragma unroll 4
-  for (int s = warp; s < ksplit; s += kTopkWarps) {
-    const float* row = partial + (static_cast<size_t>(s) * T + t) * E;
-#pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E) p[i] += __ldg(row + e);
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) {
-    const int e = lane + 32 * i;
-    if (e < E) zs[warp][e] = p[i];
-  }
-  __syncthreads();
-  if (warp != 0) return;
-#pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) {
-    const int e = lane + 32 * i;
-    if (e < E) p[i] = ((zs[0][e] + zs[1][e]) + zs[2][e]) + zs[3][e];
-  }
+// Softmax, top-k (ties: lower index), gap, per-expert counts and the optional
+// per-token statistics of token t, by one warp whose lane l holds the summed
+// logits of experts l, l+32, ... in p.  The lane sorts its own slots once
+// (bitonic network), after which each of the k+1 selection rounds is one
+// xor-butterfly argmax over the 32 lane heads.  renorm != 0: the k weights are
+// divided by their sum (slot order).  tokstats (or NULL): the probability mass
+// of each of n_groups equal expert groups, then the entropy -sum p ln p
+// ([T][n_groups+1]).
+__device__ __forceinline__ void finish_token(float (&p)[kMaxPerLane], int t, int lane, int E, int k, int renorm,
+                                             int* __restrict__ idx, float* __restrict__ prob,
+                                             float* __restrict__ gap, int* counts, float* __restrict__ tokstats,
+                                             int n_groups) {
   float zmax = -FLT_MAX;
 #pragma unroll
   for (int i = 0; i < kMaxPerLane; ++i) {
@@ -420,6 +392,70 @@ __global__ void __launch_bounds__(kTopkWarps * 32) router_topk_kernel(const floa
   }
 }
 
+// Few tokens (decode): one block of 4 warps per token.  Warp w sums the K-split
+// partials s = w, w+4, ... in increasing s; warp 0 then adds the four partial
+// sums in warp order (a fixed order: logits are bit-identical run to run) and
+// finishes the token alone.
+__global__ void __launch_bounds__(kTopkWarps * 32) router_topk_kernel(const float* __restrict__ partial, int ksplit,
+                                                                      int T, int E, int k, int renorm,
+                                                                      int* __restrict__ idx,
+                                                                      float* __restrict__ prob,
+                                                                      float* __restrict__ gap, int* counts,
+                                                                      float* __restrict__ tokstats, int n_groups) {
+  __shared__ float zs[kTopkWarps][kMaxExperts];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t = blockIdx.x;
+  float p[kMaxPerLane];
+#pragma unroll
+  for (int i = 0; i < kMaxPerLane; ++i) p[i] = 0.f;
+#pragma unroll 4
+  for (int s = warp; s < ksplit; s += kTopkWarps) {
+    const float* row = partial + (static_cast<size_t>(s) * T + t) * E;
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) p[i] += __ldg(row + e);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kMaxPerLane; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) zs[warp][e] = p[i];
+  }
+  __syncthreads();
+  if (warp != 0) return;
+#pragma unroll
+  for (int i = 0; i < kMaxPerLane; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) p[i] = ((zs[0][e] + zs[1][e]) + zs[2][e]) + zs[3][e];
+  }
+  finish_token(p, t, lane, E, k, renorm, idx, prob, gap, counts, tokstats, n_groups);
+}
+
+// Many tokens (prefill): one warp per token, kTopkTokensPerBlock tokens per
+// block; the warp sums the K-split partials in increasing s and finishes the
+// token, so no warp waits on another.
+constexpr int kTopkTokensPerBlock = 8;
+__global__ void __launch_bounds__(kTopkTokensPerBlock * 32) router_topk_warp_kernel(
+    const float* __restrict__ partial, int ksplit, int T, int E, int k, int renorm, int* __restrict__ idx,
+    float* __restrict__ prob, float* __restrict__ gap, int* counts, float* __restrict__ tokstats, int n_groups) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kTopkTokensPerBlock + (threadIdx.x >> 5);
+  if (t >= T) return;
+  float p[kMaxPerLane];
+#pragma unroll
+  for (int i = 0; i < kMaxPerLane; ++i) p[i] = 0.f;
+  for (int s = 0; s < ksplit; ++s) {
+    const float* row = partial + (static_cast<size_t>(s) * T + t) * E;
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) p[i] += __ldg(row + e);
+    }
+  }
+  finish_token(p, t, lane, E, k, renorm, idx, prob, gap, counts, tokstats, n_groups);
+}
+
 // Routing statistics over the tokens: group_p[g] = mean over tokens of the
 // group's probability mass, summary[2] = mean entropy (both summed in token
 // order per thread, then a fixed tree: bit-identical run to run);
@@ -529,8 +565,14 @@ cudaError_t launch_router_topk(const float* partial, int ksplit, int T, int E, i
                                float* prob, float* gap, int* counts, float* tokstats, int n_groups,
                                cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
-  router_topk_kernel<<<T, kTopkWarps * 32, 0, stream>>>(partial, ksplit, T, E, k, renorm, idx, prob, gap, counts,
-                                                     tokstats, n_groups);
+  if (T >= kTopkWarpMinTokens) {
+    const int blocks = (T + kTopkTokensPerBlock - 1) / kTopkTokensPerBlock;
+    router_topk_warp_kernel<<<blocks, kTopkTokensPerBlock * 32, 0, stream>>>(partial, ksplit, T, E, k, renorm, idx,
+                                                                           prob, gap, counts, tokstats, n_groups);
+  } else {
+    router_topk_kernel<<<T, kTopkWarps * 32, 0, stream>>>(partial, ksplit, T, E, k, renorm, idx, prob, gap,
+                                                         counts, tokstats, n_groups);
+  }
   return cudaGetLastError();
 }
 

@@ -85,6 +85,46 @@ typedef struct moe_handle moe_handle;
 int moe_init(const moe_config* cfg, const moe_weights* w, moe_handle** out);
 
 /*
+ * FP8 expert weights ("Step3.5 Flash 大模型技术深度解析" §8.1: FP8/FP16 mixed-
+ * precision inference; format, scales and the fp16 activations are this
+ * library's reading of that line).  Device pointers, borrowed like moe_weights:
+ *   w_router   fp32 [E][d]
+ *   w_gate_up  [G][2F][d] bytes: OCP FP8 E4M3 codes, same row order as bf16
+ *   s_gate_up  fp32 [G][2F]   the scale of each row of w_gate_up
+ *   w_down     [G][d][F] bytes: E4M3 codes
+ *   s_down     fp32 [G][d]    the scale of each row of w_down
+ * Weight value = E4M3 value of the code * the row's scale (moe_quantize_fp8
+ * produces such codes and scales from bf16 rows).
+ */
+typedef struct moe_weights_fp8 {
+  const float* w_router;
+  const void* w_gate_up;
+  const float* s_gate_up;
+  const void* w_down;
+  const float* s_down;
+} moe_weights_fp8;
+
+/*
+ * moe_init for FP8 expert weights.  The handle then runs the same calls (route,
+ * forward, forward_host, route_stats, ...); inside moe_forward the token rows
+ * and H are fp16 and every product accumulates in fp32.  The activations x and
+ * the gate output H must lie within the fp16 range (|v| < 65504); x's bf16
+ * values in the fp16 normal range are carried over exactly.  Token tiles are
+ * at most 128 rows (no CTA-pair tiles).  Same errors as moe_init.
+ */
+int moe_init_fp8(const moe_config* cfg, const moe_weights_fp8* w, moe_handle** out);
+
+/*
+ * Per-row E4M3 quantisation of a bf16 matrix w [rows][cols] (device):
+ *   s[r] = max_i |w[r][i]| / 448 (fp32),   q[r][i] = E4M3 nearest to w[r][i] / s[r]
+ * (fp32 quotient, ties to even, magnitudes above 448 saturated); a row of
+ * zeros gets s = 0 and codes 0.  q: [rows][cols] bytes, s: fp32 [rows], both
+ * device, caller-owned.  Asynchronous on `stream`.  Needs no handle.
+ * Returns MOE_ERR_INVALID_ARG for null / host pointers or sizes out of range.
+ */
+int moe_quantize_fp8(const void* w, long long rows, int cols, void* q, float* s, void* stream);
+
+/*
  * Routing only (§3.2.2 router + softmax + top-k, and the dispatch order):
  *   x        bf16 [T][d]   layer input, device
  *   idx      int  [T][k]   chosen experts, by descending probability (ties:

@@ -7,9 +7,13 @@ and its binding) never touches it, and it never touches the product path.
 from .oracle import (  # noqa: F401
     build,
     dispatch,
+    e4m3_decode,
+    e4m3_encode,
     expert_ffn,
     forward,
+    forward_fp8,
     max_threads,
+    quantize_e4m3,
     route_stats,
     route,
 )

@@ -26,6 +26,12 @@
  *   w_gate_up  [G][2F][d]      bf16; rows 0..F-1 = gate, F..2F-1 = up;
  *                              G = E + has_shared, group E = shared expert
  *   w_down     [G][d][F]       bf16
+ * FP8 expert weights (§8.1 of the same page: FP8/FP16 mixed-precision
+ * inference; the page gives no format, so the reading is): codes of the OCP
+ * FP8 E4M3 format, one byte per weight, with one fp32 scale per weight row
+ * (see oracle_quantize_e4m3):
+ *   w_gate_up  [G][2F][d] codes, s_gate_up [G][2F];  w_down [G][d][F] codes,
+ *   s_down [G][d]; the weight value is decode(code) * scale of its row.
  * No function here keeps state; every buffer is owned by the caller.
  */
 #include <math.h>
@@ -42,6 +48,49 @@ static double bf16_to_double(uint16_t b) {
   float f;
   memcpy(&f, &u, sizeof f);
   return (double)f;
+}
+
+/*
+ * OCP FP8 E4M3 ("E4M3FN"): sign bit, 4 exponent bits (bias 7), 3 mantissa
+ * bits; exponent field 0 holds the subnormals m * 2^-9; no infinities; the
+ * code with all exponent and mantissa bits set is NaN, so the largest finite
+ * magnitude is 1.75 * 2^8 = 448.  Decoding straight from that definition.
+ */
+static double e4m3_to_double(uint8_t c) {
+  const int sign = (c >> 7) & 1, ef = (c >> 3) & 15, m = c & 7;
+  double v;
+  if (ef == 15 && m == 7) return NAN;
+  if (ef == 0)
+    v = ldexp((double)m, -9);
+  else
+    v = ldexp(1.0 + m / 8.0, ef - 7);
+  return sign ? -v : v;
+}
+
+/*
+ * Nearest E4M3 value of a finite float, ties to the even code, magnitudes
+ * beyond 448 saturated to 448 (saturating conversion).  Computed in double,
+ * where every step below is exact: r is an fp32 value, scaling by powers of
+ * two is exact and rint() rounds half to even.
+ */
+static uint8_t e4m3_from_float(float r) {
+  const uint8_t sign = (r < 0.0f || (r == 0.0f && signbit(r))) ? 0x80 : 0x00;
+  double a = fabs((double)r);
+  if (a >= 448.0) return sign | 0x7e;
+  if (a < ldexp(1.0, -6)) {  /* subnormal range: multiples of 2^-9 */
+    const double m = rint(ldexp(a, 9));  /* 0..8; 8 is the smallest normal */
+    return sign | (uint8_t)m;
+  }
+  int e;
+  frexp(a, &e);  /* a = f * 2^e, f in [0.5, 1) */
+  e -= 1;        /* a = (1 + frac) * 2^e */
+  double m = rint((ldexp(a, -e) - 1.0) * 8.0);  /* 0..8 */
+  if (m == 8.0) {
+    m = 0.0;
+    e += 1;
+  }
+  if (e + 7 > 15 || (e + 7 == 15 && m > 6.0)) return sign | 0x7e;  /* rounds past 448 */
+  return sign | (uint8_t)(((e + 7) << 3) | (int)m);
 }
 
 static void set_threads(int n_threads) {
@@ -170,25 +219,79 @@ int oracle_dispatch(const int* idx, int T, int E, int k, int* counts, int* offse
  * reading): g = Wg.x, u = Wu.x, h = g * sigmoid(g) * u, o = Wd.h, all in
  * double, no intermediate rounding.  scale multiplies o into acc.
  */
-static void expert_ffn_acc(const uint16_t* x_t, const uint16_t* w_gu, const uint16_t* w_d, int d, int F,
-                           double scale, double* h, double* acc) {
+typedef struct {
+  int fp8;               /* 0: bf16 bit patterns; 1: E4M3 codes with per-row scales */
+  const void* gate_up;   /* one group: [2F][d] */
+  const float* s_gu;     /* one group: [2F] (fp8) */
+  const void* down;      /* one group: [d][F] */
+  const float* s_d;      /* one group: [d] (fp8) */
+} group_w;
+
+/* Value of element i of weight row `row` (row length n) of a group matrix. */
+static double wval(int fp8, const void* base, const float* scale, size_t row, int n, int i) {
+  if (fp8) return e4m3_to_double(((const uint8_t*)base)[row * (size_t)n + i]) * (double)scale[row];
+  return bf16_to_double(((const uint16_t*)base)[row * (size_t)n + i]);
+}
+
+static void expert_ffn_acc_w(const uint16_t* x_t, group_w w, int d, int F, double scale, double* h, double* acc) {
   for (int f = 0; f < F; ++f) {
-    const uint16_t* wg = w_gu + (size_t)f * d;
-    const uint16_t* wu = w_gu + (size_t)(F + f) * d;
     double g = 0.0, u = 0.0;
     for (int i = 0; i < d; ++i) {
       double xi = bf16_to_double(x_t[i]);
-      g += bf16_to_double(wg[i]) * xi;
-      u += bf16_to_double(wu[i]) * xi;
+      g += wval(w.fp8, w.gate_up, w.s_gu, (size_t)f, d, i) * xi;
+      u += wval(w.fp8, w.gate_up, w.s_gu, (size_t)(F + f), d, i) * xi;
     }
     h[f] = g * (1.0 / (1.0 + exp(-g))) * u;
   }
   for (int o = 0; o < d; ++o) {
-    const uint16_t* wd = w_d + (size_t)o * F;
     double s = 0.0;
-    for (int f = 0; f < F; ++f) s += bf16_to_double(wd[f]) * h[f];
+    for (int f = 0; f < F; ++f) s += wval(w.fp8, w.down, w.s_d, (size_t)o, F, f) * h[f];
     acc[o] += scale * s;
   }
+}
+
+static void expert_ffn_acc(const uint16_t* x_t, const uint16_t* w_gu, const uint16_t* w_d, int d, int F,
+                           double scale, double* h, double* acc) {
+  group_w w = {0, w_gu, NULL, w_d, NULL};
+  expert_ffn_acc_w(x_t, w, d, F, scale, h, acc);
+}
+
+/* Group g of a weight set of either format. */
+static group_w group_of(int fp8, const void* gate_up, const float* s_gu, const void* down, const float* s_d,
+                        int d, int F, int g) {
+  const size_t esz = fp8 ? 1 : 2;
+  group_w w;
+  w.fp8 = fp8;
+  w.gate_up = (const char*)gate_up + (size_t)g * 2 * F * d * esz;
+  w.down = (const char*)down + (size_t)g * d * F * esz;
+  w.s_gu = fp8 ? s_gu + (size_t)g * 2 * F : NULL;
+  w.s_d = fp8 ? s_d + (size_t)g * d : NULL;
+  return w;
+}
+
+/*
+ * FP8 weight quantisation, one scale per row: s = max_i |w_i| / 448 (an fp32
+ * division), code_i = nearest E4M3 of the fp32 quotient w_i / s (ties to
+ * even, saturating).  A row of zeros gets s = 0 and codes 0.  w holds bf16
+ * bit patterns [rows][cols].
+ */
+int oracle_quantize_e4m3(const uint16_t* w, long rows, int cols, uint8_t* q, float* s) {
+  if (rows < 0 || cols <= 0 || !w || !q || !s) return -1;
+  for (long r = 0; r < rows; ++r) {
+    const uint16_t* wr = w + (size_t)r * cols;
+    float amax = 0.0f;
+    for (int i = 0; i < cols; ++i) {
+      const float v = (float)fabs(bf16_to_double(wr[i]));
+      if (v > amax) amax = v;
+    }
+    const float sc = amax / 448.0f;
+    s[r] = sc;
+    for (int i = 0; i < cols; ++i) {
+      const float v = (float)bf16_to_double(wr[i]);
+      q[(size_t)r * cols + i] = sc > 0.0f ? e4m3_from_float(v / sc) : 0;
+    }
+  }
+  return 0;
 }
 
 /*
@@ -201,18 +304,19 @@ static void expert_ffn_acc(const uint16_t* x_t, const uint16_t* w_gu, const uint
  * renormalize != 0 (the per-call variant of §8.2 with a renormalised
  * top-k): the k weights are divided by their sum, summed in slot order.
  */
-int oracle_forward_ex(const uint16_t* x, const float* w_router, const uint16_t* w_gate_up, const uint16_t* w_down,
-                      int T, int d, int E, int k, int F, int has_shared, const int* tokens, int n_tokens,
-                      const int* sel, int renormalize, double* y, int n_threads) {
+static int forward_any(const uint16_t* x, const float* w_router, int fp8, const void* w_gate_up, const float* s_gu,
+                       const void* w_down, const float* s_d, int T, int d, int E, int k, int F, int has_shared,
+                       const int* tokens, int n_tokens, const int* sel, int renormalize, double* y,
+                       int n_threads) {
   if (T < 0 || d <= 0 || E <= 0 || k <= 0 || k > E || F <= 0 || n_tokens < 0) return -1;
   if (!x || !w_router || !w_gate_up || !w_down || !tokens || !y) return -1;
+  if (fp8 && (!s_gu || !s_d)) return -1;
   for (int i = 0; i < n_tokens; ++i)
     if (tokens[i] < 0 || tokens[i] >= T) return -1;
   if (sel)
     for (long i = 0; i < (long)n_tokens * k; ++i)
       if (sel[i] < 0 || sel[i] >= E) return -1;
   set_threads(n_threads);
-  const size_t gu_stride = (size_t)2 * F * d, d_stride = (size_t)d * F;
   int bad = 0;
 #pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
   for (int i = 0; i < n_tokens; ++i) {
@@ -237,12 +341,42 @@ int oracle_forward_ex(const uint16_t* x, const float* w_router, const uint16_t* 
     double* acc = y + (size_t)i * d;
     for (int o = 0; o < d; ++o) acc[o] = 0.0;
     for (int j = 0; j < k; ++j)
-      expert_ffn_acc(x_t, w_gate_up + ids[j] * gu_stride, w_down + ids[j] * d_stride, d, F, w[j], h, acc);
+      expert_ffn_acc_w(x_t, group_of(fp8, w_gate_up, s_gu, w_down, s_d, d, F, ids[j]), d, F, w[j], h, acc);
     if (has_shared)
-      expert_ffn_acc(x_t, w_gate_up + (size_t)E * gu_stride, w_down + (size_t)E * d_stride, d, F, 1.0, h, acc);
+      expert_ffn_acc_w(x_t, group_of(fp8, w_gate_up, s_gu, w_down, s_d, d, F, E), d, F, 1.0, h, acc);
     free(p); free(h); free(ids); free(w);
   }
   return bad ? -1 : 0;
+}
+
+int oracle_forward_ex(const uint16_t* x, const float* w_router, const uint16_t* w_gate_up, const uint16_t* w_down,
+                      int T, int d, int E, int k, int F, int has_shared, const int* tokens, int n_tokens,
+                      const int* sel, int renormalize, double* y, int n_threads) {
+  return forward_any(x, w_router, 0, w_gate_up, NULL, w_down, NULL, T, d, E, k, F, has_shared, tokens, n_tokens,
+                     sel, renormalize, y, n_threads);
+}
+
+/* oracle_forward_ex with E4M3 expert weights and per-row scales. */
+int oracle_forward_fp8(const uint16_t* x, const float* w_router, const uint8_t* q_gate_up, const float* s_gate_up,
+                       const uint8_t* q_down, const float* s_down, int T, int d, int E, int k, int F, int has_shared,
+                       const int* tokens, int n_tokens, const int* sel, int renormalize, double* y,
+                       int n_threads) {
+  return forward_any(x, w_router, 1, q_gate_up, s_gate_up, q_down, s_down, T, d, E, k, F, has_shared, tokens,
+                     n_tokens, sel, renormalize, y, n_threads);
+}
+
+/* Decode E4M3 codes to double (for pins of the codec). */
+int oracle_e4m3_decode(const uint8_t* q, long n, double* out) {
+  if (n < 0 || !q || !out) return -1;
+  for (long i = 0; i < n; ++i) out[i] = e4m3_to_double(q[i]);
+  return 0;
+}
+
+/* Encode fp32 values to E4M3 codes (nearest, ties to even, saturating). */
+int oracle_e4m3_encode(const float* v, long n, uint8_t* q) {
+  if (n < 0 || !v || !q) return -1;
+  for (long i = 0; i < n; ++i) q[i] = e4m3_from_float(v[i]);
+  return 0;
 }
 
 /* oracle_forward_ex with the raw softmax weights (the §3.2.2 reading). */

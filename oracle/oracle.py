@@ -25,6 +25,7 @@ _i32p = np.ctypeslib.ndpointer(dtype=np.int32, flags="C_CONTIGUOUS")
 _f64p = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
 _f32p = np.ctypeslib.ndpointer(dtype=np.float32, flags="C_CONTIGUOUS")
 _u16p = np.ctypeslib.ndpointer(dtype=np.uint16, flags="C_CONTIGUOUS")
+_u8p = np.ctypeslib.ndpointer(dtype=np.uint8, flags="C_CONTIGUOUS")
 
 
 def build(force: bool = False) -> str:
@@ -61,9 +62,17 @@ def _load():
                                                ctypes.c_int]
             lib.oracle_expert_ffn.argtypes = [_u16p, _u16p, _u16p, ctypes.c_int, ctypes.c_int,
                                               ctypes.c_int, _i32p, ctypes.c_int, _f64p, ctypes.c_int]
+            lib.oracle_forward_fp8.argtypes = [_u16p, _f32p, _u8p, _f32p, _u8p, _f32p, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, _i32p, ctypes.c_int, ctypes.c_void_p,
+                                               ctypes.c_int, _f64p, ctypes.c_int]
+            lib.oracle_quantize_e4m3.argtypes = [_u16p, ctypes.c_long, ctypes.c_int, _u8p, _f32p]
+            lib.oracle_e4m3_decode.argtypes = [_u8p, ctypes.c_long, _f64p]
+            lib.oracle_e4m3_encode.argtypes = [_f32p, ctypes.c_long, _u8p]
             lib.oracle_max_threads.argtypes = []
             for f in ("oracle_route", "oracle_dispatch", "oracle_forward", "oracle_forward_ex",
-                      "oracle_route_stats", "oracle_expert_ffn", "oracle_max_threads"):
+                      "oracle_route_stats", "oracle_expert_ffn", "oracle_max_threads", "oracle_forward_fp8",
+                      "oracle_quantize_e4m3", "oracle_e4m3_decode", "oracle_e4m3_encode"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -150,6 +159,67 @@ def forward(x_bits, w_router, w_gate_up_bits, w_down_bits, k: int, *, has_shared
     if rc != 0:
         raise ValueError("oracle_forward rejected its arguments")
     return y
+
+
+def forward_fp8(x_bits, w_router, q_gate_up, s_gate_up, q_down, s_down, k: int, *, has_shared: bool = True,
+                tokens=None, sel=None, renormalize: bool = False, threads: int = 0) -> np.ndarray:
+    """``forward`` with E4M3 expert weights: codes ``q_*`` (uint8) and one fp32
+    scale per weight row (``s_gate_up`` [G, 2F], ``s_down`` [G, d])."""
+    x = _u16(x_bits)
+    wr = np.ascontiguousarray(w_router, dtype=np.float32)
+    qgu = np.ascontiguousarray(q_gate_up, dtype=np.uint8)
+    qd = np.ascontiguousarray(q_down, dtype=np.uint8)
+    sgu = np.ascontiguousarray(s_gate_up, dtype=np.float32)
+    sd = np.ascontiguousarray(s_down, dtype=np.float32)
+    T, d = x.shape
+    E = wr.shape[0]
+    G = E + (1 if has_shared else 0)
+    F = qgu.shape[1] // 2
+    if qgu.shape != (G, 2 * F, d) or qd.shape != (G, d, F) or sgu.shape != (G, 2 * F) or sd.shape != (G, d):
+        raise ValueError("fp8 weight or scale shapes do not match [G,2F,d] / [G,d,F] / [G,2F] / [G,d]")
+    if tokens is None:
+        tokens = np.arange(T, dtype=np.int32)
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    n = tokens.shape[0]
+    if sel is not None:
+        sel = np.ascontiguousarray(sel, dtype=np.int32)
+        if sel.shape != (n, k):
+            raise ValueError("sel must be [len(tokens), k]")
+    y = np.zeros((n, d), np.float64)
+    rc = _load().oracle_forward_fp8(x, wr, qgu, sgu, qd, sd, T, d, E, k, F, int(has_shared), tokens, n,
+                                    _ptr(sel), int(bool(renormalize)), y, threads)
+    if rc != 0:
+        raise ValueError("oracle_forward_fp8 rejected its arguments")
+    return y
+
+
+def quantize_e4m3(w_bits):
+    """Per-row E4M3 quantisation of bf16 weights ``[..., cols]`` (bit patterns):
+    returns (codes uint8 of the same shape, scales float32 ``[...]``)."""
+    w = _u16(w_bits)
+    cols = w.shape[-1]
+    rows = w.size // cols
+    q = np.zeros(w.shape, np.uint8)
+    s = np.zeros(w.shape[:-1], np.float32)
+    rc = _load().oracle_quantize_e4m3(w.reshape(rows, cols), rows, cols, q.reshape(rows, cols),
+                                      s.reshape(rows))
+    if rc != 0:
+        raise ValueError("oracle_quantize_e4m3 rejected its arguments")
+    return q, s
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    q = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.zeros(q.shape, np.float64)
+    _load().oracle_e4m3_decode(q.reshape(-1), q.size, out.reshape(-1))
+    return out
+
+
+def e4m3_encode(values) -> np.ndarray:
+    v = np.ascontiguousarray(values, dtype=np.float32)
+    q = np.zeros(v.shape, np.uint8)
+    _load().oracle_e4m3_encode(v.reshape(-1), v.size, q.reshape(-1))
+    return q
 
 
 def route_stats(x_bits, w_router, k: int, n_groups: int, threads: int = 0):

@@ -37,9 +37,10 @@ def test_smaller_top_k_per_call(kk):
     layer.close()
 
 
-@pytest.mark.parametrize("kk", [2, 8])
-def test_renormalized_weights(kk):
-    shape = synth.LayerShape(T=120, d=256, E=32, k=8, F=128)
+@pytest.mark.parametrize("kk,T", [(2, 120), (8, 120), (4, 1100)])
+def test_renormalized_weights(kk, T):
+    # T = 1100: the one-warp-per-token top-k kernel (1024 tokens and more)
+    shape = synth.LayerShape(T=T, d=256, E=32, k=8, F=128)
     inp = synth.make_inputs(shape, seed=70 + kk)
     layer, x = layer_of(inp)
     idx, prob, perm, offsets, gap = layer.route(x, top_k=kk, renormalize=True)
@@ -85,10 +86,12 @@ def flash_small_weights():
     return synth.make_inputs(synth.FLASH_DECODE.with_tokens(64), seed=5, device=DEV)
 
 
-@pytest.mark.parametrize("case", ["tiny", "flash"])
+@pytest.mark.parametrize("case", ["tiny", "tiny_many_tokens", "flash"])
 def test_route_stats_match_oracle(case, flash_small_weights):
-    if case == "tiny":
-        inp = synth.make_inputs(synth.LayerShape(T=300, d=256, E=16, k=2, F=128), seed=80)
+    if case.startswith("tiny"):
+        # 1500 tokens: the one-warp-per-token top-k kernel writes the statistics
+        T = 1500 if case == "tiny_many_tokens" else 300
+        inp = synth.make_inputs(synth.LayerShape(T=T, d=256, E=16, k=2, F=128), seed=80)
         G = 4
     else:
         inp = flash_small_weights
