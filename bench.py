@@ -159,22 +159,25 @@ def aggregate(tokens_per_rank: int, steps: int, elapsed_s_per_rank: float, world
     return tokens_per_rank * steps * world / slowest
 
 
-def algorithmic_bytes(shape, touched: int):
+def algorithmic_bytes(shape, touched: int, fp8: bool = False):
     """Bytes the layer must move: the weights of every expert group with at
-    least one row (routed experts touched + the shared expert), the router
-    weights, x in and y out."""
+    least one row (routed experts touched + the shared expert; fp8: one byte
+    per weight plus a 4-byte scale per weight row), the router weights, x in
+    and y out."""
     d, F, E, T = shape.d, shape.F, shape.E, shape.T
-    per_group = 3 * d * F * 2
+    per_group = 3 * d * F + (2 * F + d) * 4 if fp8 else 3 * d * F * 2
     return (touched + (1 if shape.has_shared else 0)) * per_group + E * d * 4 + T * d * 2 * 2
 
 
-def gateup_bytes(shape, touched: int):
+def gateup_bytes(shape, touched: int, fp8: bool = False):
     """Algorithmic bytes of one gate/up GEMM launch: W_gu of every group with
-    rows, the R dispatch-ordered token rows read once, H written once."""
+    rows (fp8: codes + row scales), the R dispatch-ordered token rows read
+    once, H written once."""
     d, F, T, k = shape.d, shape.F, shape.T, shape.k
     groups = touched + (1 if shape.has_shared else 0)
     R = T * k + (T if shape.has_shared else 0)
-    return groups * 2 * F * d * 2 + R * d * 2 + R * F * 2
+    w = 2 * F * d + 2 * F * 4 if fp8 else 2 * F * d * 2
+    return groups * w + R * d * 2 + R * F * 2
 
 
 def gateup_flops(shape):
@@ -187,7 +190,7 @@ def measured_traffic(args):
     """DRAM bytes per launch of the gate/up GEMM from the committed ncu capture
     of the decode workload (profiles/gate_up_decode_T128_dram.md); None for
     other workloads or when the summary is missing."""
-    if args.workload != "decode" or args.experts:
+    if args.workload != "decode" or args.experts or args.weights != "bf16":
         return None
     path = os.path.join(ROOT, "profiles", "gate_up_decode_T128_dram.md")
     try:
@@ -205,9 +208,10 @@ def layer_flops(shape):
     return T * ((k + (1 if shape.has_shared else 0)) * 6 * d * F + 2 * d * E)
 
 
-def cpu_oracle_rate(inp_host, shape, budget_s: float, max_tokens: int):
+def cpu_oracle_rate(inp_host, shape, budget_s: float, max_tokens: int, fp8=None):
     """CPU oracle throughput (tokens/s) on the first tokens of the batch, in
-    chunks until `budget_s` seconds are spent or `max_tokens` are done."""
+    chunks until `budget_s` seconds are spent or `max_tokens` are done.  fp8 =
+    host (q_gate_up, s_gate_up, q_down, s_down): the FP8 oracle forward."""
     import numpy as np
 
     import oracle
@@ -219,7 +223,10 @@ def cpu_oracle_rate(inp_host, shape, budget_s: float, max_tokens: int):
         if toks.size == 0:
             break
         t0 = time.perf_counter()
-        oracle.forward(xb, wr, wgu, wd, shape.k, has_shared=shape.has_shared, tokens=toks)
+        if fp8 is None:
+            oracle.forward(xb, wr, wgu, wd, shape.k, has_shared=shape.has_shared, tokens=toks)
+        else:
+            oracle.forward_fp8(xb, wr, *fp8, shape.k, has_shared=shape.has_shared, tokens=toks)
         spent += time.perf_counter() - t0
         n += toks.size
         chunk = min(64, chunk * 2)
@@ -286,7 +293,16 @@ def run_native(args, world, rank, local):
     inp = synth.make_inputs(shape, seed=rank, device=dev, skew=skew)
     xs = [inp.x] + [synth.make_tokens(shape, seed=1000 + 31 * rank + i, device=dev, skew=skew)
                     for i in range(N_X_BUFFERS - 1)]
-    layer = binding.MoeLayer(inp.w_router, inp.w_gate_up, inp.w_down, shape.k, shape.T)
+    fp8 = args.weights == "fp8"
+    if fp8:
+        # E4M3 codes + row scales of the same synthetic weights, made on the device
+        q_gu, s_gu = binding.moe_quantize_fp8(inp.w_gate_up)
+        q_d, s_d = binding.moe_quantize_fp8(inp.w_down)
+        inp.w_gate_up = inp.w_down = None
+        torch.cuda.synchronize()
+        layer = binding.MoeLayer.fp8(inp.w_router, q_gu, s_gu, q_d, s_d, shape.k, shape.T)
+    else:
+        layer = binding.MoeLayer(inp.w_router, inp.w_gate_up, inp.w_down, shape.k, shape.T)
     y = torch.empty((shape.T, shape.d), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -347,7 +363,7 @@ def run_native(args, world, rank, local):
     steps_prof = max(1, n_prof)
     gu_ms = stages["gate_up_gemm"] / steps_prof
     mean_touched = sum(touched[i % N_X_BUFFERS] for i in range(args.steps)) / args.steps
-    gu_bytes = gateup_bytes(shape, mean_touched)
+    gu_bytes = gateup_bytes(shape, mean_touched, fp8)
     gu_gbs = gu_bytes / (gu_ms / 1e3) / 1e9
     gu_tfs = gateup_flops(shape) / (gu_ms / 1e3) / 1e12
     # the binding roof of the kernel: the larger of its HBM and tensor floors
@@ -358,7 +374,7 @@ def run_native(args, world, rank, local):
     else:
         roof = {"bound": "hbm", "achieved": gu_gbs, "peak": hbm_gbs, "unit": "GB/s", "frac": gu_gbs / hbm_gbs,
                 "peak_kind": peak_kind}
-    layer_bytes = algorithmic_bytes(shape, mean_touched)
+    layer_bytes = algorithmic_bytes(shape, mean_touched, fp8)
     step_s = ms_max / 1e3 / args.steps
     layer_hbm_frac = layer_bytes / step_s / 1e9 / hbm_gbs
     layer_tc_frac = layer_flops(shape) / step_s / 1e12 / tf_sust
@@ -366,11 +382,12 @@ def run_native(args, world, rank, local):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3-weights/f16" if fp8 else "bf16",
         "data": "synthetic (seeded N(0,1) bf16 tokens, N(0,0.02) weights, random init)",
         "config": {
             "workload": f"{args.workload}: T={shape.T} tokens, d={shape.d}, E={shape.E} routed + 1 shared, "
-                        f"top-{shape.k}, expert width {shape.F}, SiLU-gated",
+                        f"top-{shape.k}, expert width {shape.F}, SiLU-gated"
+                        + (", E4M3 expert weights with fp32 row scales, fp16 activations" if fp8 else ""),
             "tokens_per_step_per_gpu": shape.T,
             "l2": f"inputs larger than L2: {layer_bytes / 1e9:.2f} GB of expert weights read per step; "
                   f"{N_X_BUFFERS} token batches cycled",
@@ -378,7 +395,8 @@ def run_native(args, world, rank, local):
             "experts_touched_mean": mean_touched,
         },
         "roofline": {
-            "kernel": "gate_up_gemm (tcgen05 grouped GEMM, fused SiLU-gate)",
+            "kernel": "gate_up_gemm (tcgen05 grouped GEMM, fused SiLU-gate"
+                      + (", E4M3 weights widened into tensor memory)" if fp8 else ")"),
             **roof, "traffic": measured_traffic(args), "ms_per_launch": gu_ms,
             "algorithmic_bytes_per_launch": gu_bytes, "hbm_frac": gu_gbs / hbm_gbs,
             "tensor_frac_sustained": gu_tfs / tf_sust,
@@ -393,8 +411,13 @@ def run_native(args, world, rank, local):
     }
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        inp_host = host_copy(inp)
-        rate, n, spent, cores = cpu_oracle_rate(inp_host, shape, budget_s=args.cpu_budget, max_tokens=shape.T)
+        if fp8:
+            inp_host = (synth.bf16_bits(inp.x), inp.w_router.detach().cpu().numpy(), None, None)
+            fp8_host = tuple(t.cpu().numpy() for t in (q_gu, s_gu, q_d, s_d))
+        else:
+            inp_host, fp8_host = host_copy(inp), None
+        rate, n, spent, cores = cpu_oracle_rate(inp_host, shape, budget_s=args.cpu_budget, max_tokens=shape.T,
+                                                fp8=fp8_host)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                 "sample": f"first {n} tokens of the T={shape.T} batch ({spent:.1f} s)"}
     layer.close()
@@ -413,6 +436,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--weights", choices=["bf16", "fp8"], default="bf16",
+                    help="expert weight format (fp8: E4M3 codes with fp32 row scales)")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")

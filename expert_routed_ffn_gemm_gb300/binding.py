@@ -32,7 +32,7 @@ MOE_ERR_NO_DEVICE = 6
 EXPORTED = ("moe_init", "moe_route", "moe_forward", "moe_forward_host", "moe_check", "moe_set_wait_limit",
             "moe_profile_enable", "moe_profile_read", "moe_free", "moe_status_string",
             "moe_selftest_wait_timeout", "moe_dispatch_noalloc", "moe_route_ex", "moe_forward_ex",
-            "moe_route_stats", "moe_last_kernel_count")
+            "moe_route_stats", "moe_last_kernel_count", "moe_init_fp8", "moe_quantize_fp8")
 PROFILE_STAGES = ("routing", "dispatch", "gather", "gate_up_gemm", "down_gemm", "combine")
 
 
@@ -50,6 +50,11 @@ class moe_config(ctypes.Structure):
 
 class moe_weights(ctypes.Structure):
     _fields_ = [("w_router", ctypes.c_void_p), ("w_gate_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p)]
+
+
+class moe_weights_fp8(ctypes.Structure):
+    _fields_ = [("w_router", ctypes.c_void_p), ("w_gate_up", ctypes.c_void_p), ("s_gate_up", ctypes.c_void_p),
+                ("w_down", ctypes.c_void_p), ("s_down", ctypes.c_void_p)]
 
 
 class moe_call_options(ctypes.Structure):
@@ -82,6 +87,9 @@ def load():
         lib = ctypes.CDLL(path)
         vp, i, ull = ctypes.c_void_p, ctypes.c_int, ctypes.c_ulonglong
         lib.moe_init.argtypes = [ctypes.POINTER(moe_config), ctypes.POINTER(moe_weights), ctypes.POINTER(vp)]
+        lib.moe_init_fp8.argtypes = [ctypes.POINTER(moe_config), ctypes.POINTER(moe_weights_fp8),
+                                     ctypes.POINTER(vp)]
+        lib.moe_quantize_fp8.argtypes = [vp, ctypes.c_longlong, i, vp, vp, vp]
         lib.moe_route.argtypes = [vp, vp, i, vp, vp, vp, vp, vp, vp]
         lib.moe_forward.argtypes = [vp, vp, i, vp, vp]
         lib.moe_forward_host.argtypes = [vp, vp, i, vp, vp]
@@ -137,6 +145,26 @@ def moe_init(cfg: moe_config, w_router: torch.Tensor, w_gate_up: torch.Tensor, w
     h = ctypes.c_void_p()
     _check(load().moe_init(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)), "moe_init")
     return h.value
+
+
+def moe_init_fp8(cfg: moe_config, w_router, q_gate_up, s_gate_up, q_down, s_down) -> int:
+    w = moe_weights_fp8(_ptr(w_router), _ptr(q_gate_up), _ptr(s_gate_up), _ptr(q_down), _ptr(s_down))
+    h = ctypes.c_void_p()
+    _check(load().moe_init_fp8(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)), "moe_init_fp8")
+    return h.value
+
+
+def moe_quantize_fp8(w: torch.Tensor, stream=None):
+    """Per-row E4M3 codes (uint8, same shape) and fp32 scales (shape[:-1]) of a
+    bf16 device tensor, computed on the device (see include/moe.h)."""
+    if w.dtype != torch.bfloat16:
+        raise TypeError("moe_quantize_fp8 takes bf16 weights")
+    cols = w.shape[-1]
+    rows = w.numel() // cols
+    q = torch.empty(w.shape, dtype=torch.uint8, device=w.device)
+    s = torch.empty(w.shape[:-1], dtype=torch.float32, device=w.device)
+    _check(load().moe_quantize_fp8(_ptr(w), rows, cols, _ptr(q), _ptr(s), _stream(stream)), "moe_quantize_fp8")
+    return q, s
 
 
 def moe_route(h: int, x, T: int, idx, prob, perm, offsets, gap=None, stream=None) -> None:
@@ -219,20 +247,34 @@ class MoeLayer:
     """
 
     def __init__(self, w_router, w_gate_up, w_down, top_k: int, max_tokens: int, has_shared: bool = True,
-                 out_fp32: bool = False):
+                 out_fp32: bool = False, scales=None):
         E, d = w_router.shape
         G, twoF, d2 = w_gate_up.shape
         F = twoF // 2
         if d2 != d or G != E + int(has_shared) or tuple(w_down.shape) != (G, d, F):
             raise ValueError("weight shapes do not match [E,d], [G,2F,d], [G,d,F]")
-        if w_router.dtype != torch.float32 or w_gate_up.dtype != torch.bfloat16 or w_down.dtype != torch.bfloat16:
-            raise TypeError("w_router must be fp32 and the expert weights bf16")
-        self.weights = (w_router, w_gate_up, w_down)  # kept alive: the handle borrows them
+        wdt = torch.uint8 if scales is not None else torch.bfloat16
+        if w_router.dtype != torch.float32 or w_gate_up.dtype != wdt or w_down.dtype != wdt:
+            raise TypeError("w_router must be fp32 and the expert weights bf16 (or uint8 E4M3 codes with scales)")
+        self.weights = (w_router, w_gate_up, w_down) + tuple(scales or ())  # borrowed by the handle
         self.d, self.E, self.k, self.F = d, E, top_k, F
         self.has_shared, self.out_fp32, self.max_tokens = has_shared, out_fp32, max_tokens
         self.device = w_gate_up.device
         cfg = moe_config(d, E, top_k, F, int(has_shared), max_tokens, int(out_fp32))
-        self.handle = moe_init(cfg, w_router, w_gate_up, w_down)
+        if scales is None:
+            self.handle = moe_init(cfg, w_router, w_gate_up, w_down)
+        else:
+            s_gu, s_d = scales
+            if tuple(s_gu.shape) != (G, 2 * F) or tuple(s_d.shape) != (G, d):
+                raise ValueError("scales must be [G, 2F] and [G, d]")
+            self.handle = moe_init_fp8(cfg, w_router, w_gate_up, s_gu, w_down, s_d)
+
+    @classmethod
+    def fp8(cls, w_router, q_gate_up, s_gate_up, q_down, s_down, top_k: int, max_tokens: int,
+            has_shared: bool = True, out_fp32: bool = False) -> "MoeLayer":
+        """A layer with E4M3 expert weights (uint8 codes) and fp32 row scales."""
+        return cls(w_router, q_gate_up, q_down, top_k, max_tokens, has_shared, out_fp32,
+                   scales=(s_gate_up, s_down))
 
     def route(self, x: torch.Tensor, stream=None, with_gap: bool = True, top_k: int | None = None,
               renormalize: bool = False):

@@ -14,10 +14,12 @@
 //               tile and the BN x 128 fp16 token tile (two 64-column boxes)
 //   warp 1      TMEM allocator + tcgen05.mma issuer, A read from tensor memory
 //   warps 2..5  epilogue (row scale, SiLU gate or gate-weight scale, stores)
-//   warps 6..9  converters: each thread takes one weight row of the stage from
-//               shared memory (128 bytes), widens it to 64 fp16 pairs and
-//               stores them into a 4-slot ring of A tiles in tensor memory
-//               (columns 256..511; the accumulators use 0..2*BN-1)
+//   warps 6..13 converters, two sets of four: set 0 takes the even K steps,
+//               set 1 the odd ones, so two stages are widened at a time; each
+//               thread takes one weight row of its stage from shared memory
+//               (128 bytes), widens it to 64 fp16 pairs and stores them into a
+//               4-slot ring of A tiles in tensor memory (columns 256..511; the
+//               accumulators use 0..2*BN-1)
 // The widened tile never goes back to shared memory: shared-memory traffic per
 // weight byte stays at one TMA write and one read.
 // Every wait is bounded (wait_limit_ns); on timeout the kernel records an
@@ -29,9 +31,10 @@ namespace {
 
 using namespace gemm;
 
-constexpr int kThreads8 = 320;
+constexpr int kThreads8 = 448;
 constexpr int kKStep8 = 128;           // K elements per stage (one 128-byte E4M3 row)
-constexpr int kConvWarp0 = 6;          // warps 6..9 convert
+constexpr int kConvWarp0 = 6;          // warps 6..13 convert (two sets of four)
+constexpr int kConvSets = 2;
 constexpr int kASlots = 4;             // A tiles in tensor memory
 constexpr uint32_t kAColBase = 256;    // first TMEM column of the A ring
 constexpr uint32_t kAColsPerSlot = 64; // 128 fp16 per row = 64 columns
@@ -208,19 +211,27 @@ __global__ void __launch_bounds__(kThreads8, 1)
   } else if (warp >= kConvWarp0) {
     // -------------------------------------------------------- converters --
     const int q = warp & 3;  // TMEM lane quarter
+    const int set = (warp - kConvWarp0) >> 2;  // 0: even K steps, 1: odd K steps
     const int r = q * 32 + lane;  // weight row of the tile this thread widens
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    uint32_t stage = 0, phase = 0, slot = 0, slot_phase = 0;
+    const long my_items = n_items > static_cast<int>(blockIdx.x)
+                              ? (n_items - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+                              : 0;
+    const long total = my_items * k_steps;  // K steps this CTA runs, over all its items
     bool ok = true;
-    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+    for (long step = set; ok && step < total; step += kConvSets) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-      for (int kb = 0; kb < k_steps; ++kb) {
+      const uint32_t stage = static_cast<uint32_t>(step % C::STAGES);
+      const uint32_t phase = static_cast<uint32_t>((step / C::STAGES) & 1);
+      const uint32_t slot = static_cast<uint32_t>(step % kASlots);
+      const uint32_t slot_phase = static_cast<uint32_t>((step / kASlots) & 1);
+      {
         const bool got = wait_or_abort(&full[stage], phase, limit, abort_flag) &&
                          wait_or_abort(&a_empty[slot], slot_phase ^ 1u, limit, abort_flag);
         if (!__all_sync(0xffffffffu, got)) {
           if (lane == 0) record_abort(abort_flag, args.err);
           ok = false;
-          break;
+          continue;  // leaves the loop (ok is false)
         }
         tc_fence_after();
         // row r of the 128-byte-swizzled E4M3 tile: chunk c at r*128 + ((c ^ (r & 7)) * 16)
@@ -251,14 +262,6 @@ __global__ void __launch_bounds__(kThreads8, 1)
         if (lane == 0) {
           mbar_arrive(&a_full[slot]);
           mbar_arrive(&empty[stage]);
-        }
-        if (++stage == C::STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
-        if (++slot == kASlots) {
-          slot = 0;
-          slot_phase ^= 1u;
         }
       }
     }

@@ -123,14 +123,20 @@ def half_ulp_bf16(v: np.ndarray) -> np.ndarray:
 
 
 def check_output(x_bits, w_router, wgu_bits, wd_bits, k, y_gpu, sel, tokens=None, has_shared=True, tol=OUT_TOL,
-                 out_bf16=True):
+                 out_bf16=True, fp8=None):
     """Compares y_gpu (rows = tokens) with the oracle for the GPU's selection;
-    returns max|err| / RMS."""
+    returns max|err| / RMS.  fp8 = (q_gate_up, s_gate_up, q_down, s_down):
+    the expert weights are E4M3 codes with row scales (wgu_bits / wd_bits
+    unused)."""
     T = x_bits.shape[0]
     if tokens is None:
         tokens = np.arange(T, dtype=np.int32)
-    y_ref = oracle.forward(x_bits, w_router, wgu_bits, wd_bits, k, has_shared=has_shared, tokens=tokens,
-                           sel=np.ascontiguousarray(sel[tokens]))
+    sel_t = np.ascontiguousarray(sel[tokens])
+    if fp8 is None:
+        y_ref = oracle.forward(x_bits, w_router, wgu_bits, wd_bits, k, has_shared=has_shared, tokens=tokens,
+                               sel=sel_t)
+    else:
+        y_ref = oracle.forward_fp8(x_bits, w_router, *fp8, k, has_shared=has_shared, tokens=tokens, sel=sel_t)
     y = y_gpu.astype(np.float64)
     assert np.all(np.isfinite(y))
     if not y.size:

@@ -1,0 +1,100 @@
+"""FP8 expert weights on the GPU (moe_quantize_fp8, moe_init_fp8 + the
+forward) against the oracle: codes and scales bit-exact, routing as in the
+bf16 path, the layer output within the same bound (see moe_check.py) of the
+oracle's forward on the same E4M3 weights ("Step3.5 Flash 大模型技术深度解析"
+§8.1, FP8/FP16 mixed-precision inference)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from expert_routed_ffn_gemm_gb300 import binding, synth
+
+from moe_check import check_output, check_routing, cpu, sample_tokens
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+def quantised(inp):
+    """Device E4M3 codes and scales of the synthetic bf16 expert weights."""
+    q_gu, s_gu = binding.moe_quantize_fp8(inp.w_gate_up.to(DEV))
+    q_d, s_d = binding.moe_quantize_fp8(inp.w_down.to(DEV))
+    torch.cuda.synchronize()
+    return q_gu, s_gu, q_d, s_d
+
+
+def test_quantiser_bit_exact():
+    rng = np.random.default_rng(5)
+    w = rng.normal(0, 0.02, (300, 384)).astype(np.float32)
+    w[7] = 0.0
+    w[9, :5] = [3.0, -500.0, 1e-6, -1e-9, 0.0]
+    w[11] *= 1e-4
+    wb = torch.from_numpy(w).to(torch.bfloat16)
+    q, s = binding.moe_quantize_fp8(wb.to(DEV))
+    oq, os_ = oracle.quantize_e4m3(synth.bf16_bits(wb))
+    np.testing.assert_array_equal(cpu(s), os_)
+    np.testing.assert_array_equal(cpu(q), oq)
+
+
+def fp8_case(shape, seed, tiles=(0, 0), n_sample=None, max_tokens=None, out_fp32=False):
+    import os
+    inp = synth.make_inputs(shape, seed=seed, device=DEV)
+    q_gu, s_gu, q_d, s_d = quantised(inp)
+    inp.w_gate_up = inp.w_down = None  # the bf16 copies are not needed any more
+    old = {k: os.environ.get(k) for k in ("MOE_TILE_N_GATEUP", "MOE_TILE_N_DOWN")}
+    os.environ["MOE_TILE_N_GATEUP"], os.environ["MOE_TILE_N_DOWN"] = str(tiles[0]), str(tiles[1])
+    try:
+        layer = binding.MoeLayer.fp8(inp.w_router, q_gu, s_gu, q_d, s_d, shape.k,
+                                     max_tokens or shape.T, has_shared=shape.has_shared, out_fp32=out_fp32)
+    finally:
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    x = inp.x
+    idx, prob, perm, offsets, gap = layer.route(x)
+    y = layer.forward(x)
+    assert layer.check() == binding.MOE_OK
+    xb = synth.bf16_bits(inp.x)
+    wr = cpu(inp.w_router)
+    idx_h = cpu(idx)
+    near, _ = check_routing(xb, wr, shape.k, idx_h, cpu(prob), cpu(gap), cpu(perm), cpu(offsets),
+                            has_shared=shape.has_shared)
+    fp8 = (cpu(q_gu), cpu(s_gu), cpu(q_d), cpu(s_d))
+    tokens = np.arange(shape.T, dtype=np.int32) if n_sample is None else sample_tokens(shape.T, idx_h, n_sample,
+                                                                                      seed, near)
+    y_h = cpu(y[torch.from_numpy(tokens).long().to(DEV)].float())
+    ratio = check_output(xb, wr, None, None, shape.k, y_h, idx_h, tokens=tokens, has_shared=shape.has_shared,
+                         out_bf16=not out_fp32, fp8=fp8)
+    y2 = layer.forward(x)
+    assert torch.equal(y, y2)
+    layer.close()
+    return ratio
+
+
+def test_fp8_tiny():
+    fp8_case(synth.TINY, seed=0)
+
+
+@pytest.mark.parametrize("tiles", [(16, 16), (32, 32), (64, 64), (128, 128), (16, 128), (128, 16), (256, 256)])
+def test_fp8_tile_widths_ragged(tiles):
+    # 300 tokens, 16 experts, top-2: ragged tiles of every width; d = 512 gives
+    # 4 K steps of 128 per gate/up tile (wraps the 4-slot A ring once)
+    fp8_case(synth.LayerShape(T=300, d=512, E=16, k=2, F=256), seed=21, tiles=tiles)
+
+
+def test_fp8_long_k_and_fp32_output():
+    # d = 2048: 16 K steps per gate/up tile (rings wrap several times)
+    fp8_case(synth.LayerShape(T=96, d=2048, E=8, k=2, F=256), seed=22, out_fp32=True)
+
+
+def test_fp8_without_shared_expert():
+    fp8_case(synth.LayerShape(T=50, d=256, E=12, k=3, F=128, has_shared=False), seed=23)
+
+
+@pytest.mark.parametrize("T", [1, 128])
+def test_fp8_flash_decode(T):
+    # d=4096, 288 routed + 1 shared, top-8, width 1280
+    fp8_case(synth.FLASH_DECODE.with_tokens(T), seed=24, n_sample=None if T == 1 else 48)
