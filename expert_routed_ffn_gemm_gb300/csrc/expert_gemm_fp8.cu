@@ -18,10 +18,13 @@
 //               set 1 the odd ones, so two stages are widened at a time; each
 //               thread takes one weight row of its stage from shared memory
 //               (128 bytes), widens it to 64 fp16 pairs and stores them into a
-//               4-slot ring of A tiles in tensor memory (columns 256..511; the
-//               accumulators use 0..2*BN-1)
+//               ring of A tiles in tensor memory (64 columns each, above the
+//               2*BN accumulator columns: 4 to 7 slots by BN)
 // The widened tile never goes back to shared memory: shared-memory traffic per
-// weight byte stays at one TMA write and one read.
+// weight byte stays at one TMA write and one read.  The E4M3 tiles and the
+// token tiles sit in two separate rings: a weight stage is handed back to the
+// producer as soon as its converters have read it (before the MMAs run), so
+// the bytes in flight from HBM are not held up by the widening and the MMAs.
 // Every wait is bounded (wait_limit_ns); on timeout the kernel records an
 // error, drains what it issued, frees tensor memory and returns.
 #include "gemm_common.cuh"
@@ -35,8 +38,6 @@ constexpr int kThreads8 = 448;
 constexpr int kKStep8 = 128;           // K elements per stage (one 128-byte E4M3 row)
 constexpr int kConvWarp0 = 6;          // warps 6..13 convert (two sets of four)
 constexpr int kConvSets = 2;
-constexpr int kASlots = 4;             // A tiles in tensor memory
-constexpr uint32_t kAColBase = 256;    // first TMEM column of the A ring
 constexpr uint32_t kAColsPerSlot = 64; // 128 fp16 per row = 64 columns
 
 template <bool GATEUP, int BN>
@@ -44,20 +45,25 @@ struct Cfg8 {
   static constexpr int A8_BYTES = kBlockM * kKStep8;      // 128 rows x 128 E4M3
   static constexpr int B_HALF = BN * 128;                 // BN rows x 64 fp16
   static constexpr int B_BYTES = 2 * B_HALF;              // K 0..63 and 64..127
-  static constexpr int STAGE_BYTES = A8_BYTES + B_BYTES;  // multiple of 1024
-  static constexpr int RING_BUDGET = 192 * 1024;
-  static constexpr int STAGES_RAW = RING_BUDGET / STAGE_BYTES;
-  static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
+  // ring depths (weight stages NA, token stages NB) within 192 KB
+  static constexpr int NA = BN <= 32 ? 8 : (BN == 64 ? 6 : 4);
+  static constexpr int NB = BN == 16 ? 12 : (BN == 32 ? 8 : (BN == 64 ? 6 : 4));
+  static constexpr int RING_BYTES = NA * A8_BYTES + NB * B_BYTES;
   static constexpr int NACC = 2;
   static constexpr int TMEM_COLS = 512;
-  // full[S], empty[S], a_full[4], a_empty[4], acc_full[2], acc_empty[2], drain
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * kASlots + 2 * NACC + 1;
+  // A ring in tensor memory: from the first multiple of 64 columns above the
+  // accumulators to column 511 (7 slots for BN <= 32, 6 for 64, 4 for 128)
+  static constexpr uint32_t ACOL0 = ((NACC * BN + 63) / 64) * 64;
+  static constexpr int NSLOT = (TMEM_COLS - static_cast<int>(ACOL0)) / 64;
+  // a8_full[NA], a8_empty[NA], b_full[NB], b_empty[NB], a_full[4], a_empty[4],
+  // acc_full[2], acc_empty[2], drain
+  static constexpr int NUM_BARS = 2 * NA + 2 * NB + 2 * NSLOT + 2 * NACC + 1;
   static constexpr int XCHG_BYTES = GATEUP ? 2 * 2 * 64 * 8 * 4 : 0;
   static constexpr int AUX_BYTES = NUM_BARS * 8 + 16 + 32 + (kMaxGroups + 1) * 4;
-  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + XCHG_BYTES + AUX_BYTES;
+  static constexpr int SMEM_BYTES = 1024 + RING_BYTES + XCHG_BYTES + AUX_BYTES;
   static_assert(BN <= 128, "accumulators must fit below the A ring");
-  static_assert(STAGE_BYTES % 1024 == 0, "stage must keep 1024-byte alignment");
-  static_assert(STAGES >= 2, "ring too shallow");
+  static_assert(B_BYTES % 1024 == 0, "token stages must keep 1024-byte alignment");
+  static_assert(RING_BYTES <= 192 * 1024, "rings exceed their budget");
   static_assert(SMEM_BYTES <= 232448, "exceeds shared memory per block");
   static constexpr uint32_t IDESC = idesc_f16_f32(kBlockM, BN);
 };
@@ -69,14 +75,17 @@ __global__ void __launch_bounds__(kThreads8, 1)
   using C = Cfg8<GATEUP, BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* ring = smem;
-  float* xchg = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE_BYTES);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES + C::XCHG_BYTES);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + C::STAGES;
-  uint64_t* a_full = bars + 2 * C::STAGES;
-  uint64_t* a_empty = a_full + kASlots;
-  uint64_t* acc_full = a_empty + kASlots;
+  uint8_t* ring_a = smem;                          // NA x 16 KB E4M3 tiles
+  uint8_t* ring_b = smem + C::NA * C::A8_BYTES;    // NB x token tiles
+  float* xchg = reinterpret_cast<float*>(smem + C::RING_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::RING_BYTES + C::XCHG_BYTES);
+  uint64_t* a8_full = bars;
+  uint64_t* a8_empty = a8_full + C::NA;
+  uint64_t* b_full = a8_empty + C::NA;
+  uint64_t* b_empty = b_full + C::NB;
+  uint64_t* a_full = b_empty + C::NB;
+  uint64_t* a_empty = a_full + C::NSLOT;
+  uint64_t* acc_full = a_empty + C::NSLOT;
   uint64_t* acc_empty = acc_full + C::NACC;
   uint64_t* drain = acc_empty + C::NACC;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
@@ -88,11 +97,15 @@ __global__ void __launch_bounds__(kThreads8, 1)
   const int G = args.G;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 4 + 1);  // the four converter warps + the MMA commit
+    for (int s = 0; s < C::NA; ++s) {
+      mbar_init(&a8_full[s], 1);
+      mbar_init(&a8_empty[s], 4);  // the four converter warps that read the stage
     }
-    for (int j = 0; j < kASlots; ++j) {
+    for (int s = 0; s < C::NB; ++s) {
+      mbar_init(&b_full[s], 1);
+      mbar_init(&b_empty[s], 1);  // the MMA commit
+    }
+    for (int j = 0; j < C::NSLOT; ++j) {
       mbar_init(&a_full[j], 4);
       mbar_init(&a_empty[j], 1);
     }
@@ -124,7 +137,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
       // ---------------------------------------------------------- producer --
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_act = policy_evict_last();
-      uint32_t stage = 0, phase = 0;
+      uint32_t sa = 0, pa = 0, sb = 0, pb = 0;
       long issued = 0;
       bool ok = true;
       for (int item = blockIdx.x; ok && item < n_items && !*abort_flag; item += gridDim.x) {
@@ -132,34 +145,47 @@ __global__ void __launch_bounds__(kThreads8, 1)
         const int row_w = it.g * args.rows_per_group + it.m * (GATEUP ? kBlockM / 2 : kBlockM);
         const int row_act = __ldg(args.offsets + it.g) + it.n * BN;
         for (int kb = 0; kb < k_steps; ++kb) {
-          if (!wait_or_abort(&empty[stage], phase ^ 1u, limit, abort_flag)) {
+          if (!wait_or_abort(&a8_empty[sa], pa ^ 1u, limit, abort_flag) ||
+              !wait_or_abort(&b_empty[sb], pb ^ 1u, limit, abort_flag)) {
             record_abort(abort_flag, args.err);
             ok = false;
             break;
           }
-          uint8_t* st = ring + stage * C::STAGE_BYTES;
-          mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-          tma_load_2d(st, &map_w, &full[stage], kb * kKStep8, row_w, pol_w);
-          if (GATEUP) tma_load_2d(st + C::A8_BYTES / 2, &map_w, &full[stage], kb * kKStep8, row_w + args.F, pol_w);
-          tma_load_2d(st + C::A8_BYTES, &map_act, &full[stage], kb * kKStep8, row_act, pol_act);
-          tma_load_2d(st + C::A8_BYTES + C::B_HALF, &map_act, &full[stage], kb * kKStep8 + 64, row_act, pol_act);
+          uint8_t* sta = ring_a + sa * C::A8_BYTES;
+          mbar_arrive_expect_tx(&a8_full[sa], C::A8_BYTES);
+          tma_load_2d(sta, &map_w, &a8_full[sa], kb * kKStep8, row_w, pol_w);
+          if (GATEUP) tma_load_2d(sta + C::A8_BYTES / 2, &map_w, &a8_full[sa], kb * kKStep8, row_w + args.F, pol_w);
+          uint8_t* stb = ring_b + sb * C::B_BYTES;
+          mbar_arrive_expect_tx(&b_full[sb], C::B_BYTES);
+          tma_load_2d(stb, &map_act, &b_full[sb], kb * kKStep8, row_act, pol_act);
+          tma_load_2d(stb + C::B_HALF, &map_act, &b_full[sb], kb * kKStep8 + 64, row_act, pol_act);
           ++issued;
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1u;
+          if (++sa == C::NA) {
+            sa = 0;
+            pa ^= 1u;
+          }
+          if (++sb == C::NB) {
+            sb = 0;
+            pb ^= 1u;
           }
         }
       }
-      for (int s = 0; s < C::STAGES; ++s) {
+      // every load issued must have landed before the CTA may exit
+      for (int s = 0; s < C::NA; ++s) {
         if (issued <= s) break;
-        const long last = s + ((issued - 1 - s) / C::STAGES) * C::STAGES;
-        mbar_wait(&full[s], static_cast<uint32_t>((last / C::STAGES) & 1), kDrainLimitNs);
+        const long last = s + ((issued - 1 - s) / C::NA) * C::NA;
+        mbar_wait(&a8_full[s], static_cast<uint32_t>((last / C::NA) & 1), kDrainLimitNs);
+      }
+      for (int s = 0; s < C::NB; ++s) {
+        if (issued <= s) break;
+        const long last = s + ((issued - 1 - s) / C::NB) * C::NB;
+        mbar_wait(&b_full[s], static_cast<uint32_t>((last / C::NB) & 1), kDrainLimitNs);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // --------------------------------------------------------------- MMA --
-      uint32_t stage = 0, phase = 0, slot = 0, slot_phase = 0, acc = 0, acc_phase = 0;
+      uint32_t sb = 0, pb = 0, slot = 0, slot_phase = 0, acc = 0, acc_phase = 0;
       bool issued_any = false, ok = true;
       for (int item = blockIdx.x; ok && item < n_items && !*abort_flag; item += gridDim.x) {
         if (!wait_or_abort(&acc_empty[acc], acc_phase ^ 1u, limit, abort_flag)) {
@@ -169,15 +195,15 @@ __global__ void __launch_bounds__(kThreads8, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kb = 0; kb < k_steps; ++kb) {
-          if (!wait_or_abort(&full[stage], phase, limit, abort_flag) ||
+          if (!wait_or_abort(&b_full[sb], pb, limit, abort_flag) ||
               !wait_or_abort(&a_full[slot], slot_phase, limit, abort_flag)) {
             record_abort(abort_flag, args.err);
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_tmem = tmem_base + kAColBase + slot * kAColsPerSlot;
-          const uint32_t st_b = smem_u32(ring + stage * C::STAGE_BYTES + C::A8_BYTES);
+          const uint32_t a_tmem = tmem_base + C::ACOL0 + slot * kAColsPerSlot;
+          const uint32_t st_b = smem_u32(ring_b + sb * C::B_BYTES);
 #pragma unroll
           for (int kk = 0; kk < kKStep8 / 16; ++kk) {
             // K 16kk..16kk+15: A columns 8kk.., B in half kk/4 at +32 B per 16 K
@@ -185,13 +211,13 @@ __global__ void __launch_bounds__(kThreads8, 1)
             tc_mma_f16_tmem_a(d_tmem, a_tmem + 8 * kk, b, C::IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
           }
           issued_any = true;
-          tc_commit(&empty[stage]);
+          tc_commit(&b_empty[sb]);
           tc_commit(&a_empty[slot]);
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1u;
+          if (++sb == C::NB) {
+            sb = 0;
+            pb ^= 1u;
           }
-          if (++slot == kASlots) {
+          if (++slot == C::NSLOT) {
             slot = 0;
             slot_phase ^= 1u;
           }
@@ -221,12 +247,12 @@ __global__ void __launch_bounds__(kThreads8, 1)
     bool ok = true;
     for (long step = set; ok && step < total; step += kConvSets) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-      const uint32_t stage = static_cast<uint32_t>(step % C::STAGES);
-      const uint32_t phase = static_cast<uint32_t>((step / C::STAGES) & 1);
-      const uint32_t slot = static_cast<uint32_t>(step % kASlots);
-      const uint32_t slot_phase = static_cast<uint32_t>((step / kASlots) & 1);
+      const uint32_t stage = static_cast<uint32_t>(step % C::NA);
+      const uint32_t phase = static_cast<uint32_t>((step / C::NA) & 1);
+      const uint32_t slot = static_cast<uint32_t>(step % C::NSLOT);
+      const uint32_t slot_phase = static_cast<uint32_t>((step / C::NSLOT) & 1);
       {
-        const bool got = wait_or_abort(&full[stage], phase, limit, abort_flag) &&
+        const bool got = wait_or_abort(&a8_full[stage], phase, limit, abort_flag) &&
                          wait_or_abort(&a_empty[slot], slot_phase ^ 1u, limit, abort_flag);
         if (!__all_sync(0xffffffffu, got)) {
           if (lane == 0) record_abort(abort_flag, args.err);
@@ -235,7 +261,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
         }
         tc_fence_after();
         // row r of the 128-byte-swizzled E4M3 tile: chunk c at r*128 + ((c ^ (r & 7)) * 16)
-        const uint8_t* row = ring + stage * C::STAGE_BYTES + r * 128;
+        const uint8_t* row = ring_a + stage * C::A8_BYTES + r * 128;
         uint32_t w[32];
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
@@ -245,24 +271,22 @@ __global__ void __launch_bounds__(kThreads8, 1)
           w[4 * c + 2] = v.z;
           w[4 * c + 3] = v.w;
         }
-        const uint32_t taddr = tmem_base + lane_base + kAColBase + slot * kAColsPerSlot;
+        // widen first: once every value is in registers the stage goes back
+        uint32_t h[64];  // column j: fp16 pair of K 2j, 2j+1
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t h[32];  // columns 32*half.. : fp16 pairs of K 64*half + 2i, +1
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            h[2 * i] = e4m3x2_to_f16x2(w[16 * half + i] & 0xffffu);
-            h[2 * i + 1] = e4m3x2_to_f16x2(w[16 * half + i] >> 16);
-          }
-          tmem_st32(taddr + 32 * half, h);
+        for (int i = 0; i < 32; ++i) {
+          h[2 * i] = e4m3x2_to_f16x2(w[i] & 0xffffu);
+          h[2 * i + 1] = e4m3x2_to_f16x2(w[i] >> 16);
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&a8_empty[stage]);
+        const uint32_t taddr = tmem_base + lane_base + C::ACOL0 + slot * kAColsPerSlot;
+        tmem_st32(taddr, *reinterpret_cast<const uint32_t(*)[32]>(&h[0]));
+        tmem_st32(taddr + 32, *reinterpret_cast<const uint32_t(*)[32]>(&h[32]));
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&a_full[slot]);
-          mbar_arrive(&empty[stage]);
-        }
+        if (lane == 0) mbar_arrive(&a_full[slot]);
       }
     }
   } else {
