@@ -161,6 +161,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool issued_any = false, ok = true;
       for (int item = blockIdx.x; ok && item < n_items && !*abort_flag; item += gridDim.x) {
+        // N of the MMAs: the tile's rows rounded up to 16 (ragged tails)
+        const Item it = decode_item(item, args.m_tiles, tile_start, G);
+        const int rows = __ldg(args.offsets + it.g + 1) - __ldg(args.offsets + it.g) - it.n * BN;
+        const uint32_t idesc = idesc_bf16_f32(kBlockM, mma_width(rows, 16, BN));
         if (!wait_or_abort(&acc_empty[acc], acc_phase ^ 1u, limit, abort_flag)) {
           record_abort(abort_flag, args.err);
           break;
@@ -179,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t b = smem_desc_sw128(st + C::A_BYTES);
 #pragma unroll
           for (int kk = 0; kk < kBlockK / 16; ++kk)  // +32 B along K = +2 in the address field
-            tc_mma_bf16(d_tmem, a + 2 * kk, b + 2 * kk, C::IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+            tc_mma_bf16(d_tmem, a + 2 * kk, b + 2 * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
           issued_any = true;
           tc_commit(&empty[stage]);
           if (++stage == C::STAGES) {

@@ -140,7 +140,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // features per pair tile; K4: 128 rows per CTA, 256 per pair tile.
         const int row_w = GATEUP ? it.g * args.rows_per_group + it.m * kBlockM + static_cast<int>(rank) * 64
                                  : it.g * args.rows_per_group + it.m * 2 * kBlockM + static_cast<int>(rank) * kBlockM;
-        const int row_act = __ldg(args.offsets + it.g) + it.n * kPairN + static_cast<int>(rank) * kHalfN;
+        // the pair MMA takes N/2 token rows from each CTA: N = the tile's rows
+        // rounded up to 32, so the odd CTA's rows start at N/2
+        const int g_row0 = __ldg(args.offsets + it.g);
+        const int n_mma = mma_width(__ldg(args.offsets + it.g + 1) - g_row0 - it.n * kPairN, 32, kPairN);
+        const int row_act = g_row0 + it.n * kPairN + static_cast<int>(rank) * (n_mma / 2);
         for (int kb = 0; kb < k_steps; ++kb) {
           if (!wait_cluster(&empty[stage], phase ^ 1u, limit, abort_flag)) {
             record_abort(abort_flag, args.err);
@@ -177,6 +181,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool issued_any = false, ok = true;
       for (int item = pair; ok && item < n_items && !*abort_flag; item += n_pairs) {
+        const Item it = decode_item(item, args.m_tiles, tile_start, G);
+        const int rows = __ldg(args.offsets + it.g + 1) - __ldg(args.offsets + it.g) - it.n * kPairN;
+        const uint32_t idesc = idesc_bf16_f32(2 * kBlockM, mma_width(rows, 32, kPairN));
         if (!wait_cluster(&acc_empty[acc], acc_phase ^ 1u, limit, abort_flag)) {
           record_abort(abort_flag, args.err);
           break;
@@ -195,7 +202,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint64_t b = smem_desc_sw128(st + C::A_BYTES);
 #pragma unroll
           for (int kk = 0; kk < kBlockK / 16; ++kk)
-            tc_mma_bf16_pair(d_tmem, a + 2 * kk, b + 2 * kk, C::IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+            tc_mma_bf16_pair(d_tmem, a + 2 * kk, b + 2 * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
           issued_any = true;
           tc_commit_pair_multicast(&empty[stage], 0x3);
           if (++stage == C::STAGES) {

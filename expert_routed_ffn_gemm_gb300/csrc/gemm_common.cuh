@@ -64,6 +64,15 @@ __device__ __forceinline__ void build_tile_start(const int* offsets, int G, int 
   if (lane == 31) tile_start[G] = incl;
 }
 
+// MMA width for a token tile with `valid` rows: the rows rounded up to a
+// multiple of `step` (16 for one CTA; 32 for a pair, 16 rows per CTA),
+// at most the tile width.  Columns past it are neither loaded into the MMA
+// nor computed; the epilogue only reads the valid columns.
+__device__ __forceinline__ int mma_width(int valid, int step, int tile) {
+  const int w = (valid + step - 1) / step * step;
+  return w < tile ? w : tile;
+}
+
 __device__ __forceinline__ void record_abort(volatile int* abort_flag, uint32_t* err) {
   *abort_flag = 1;
   atomicOr(err, kErrWaitTimeout);
