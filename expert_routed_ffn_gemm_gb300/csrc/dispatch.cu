@@ -138,6 +138,8 @@ __global__ void __launch_bounds__(256) gather_kernel(const bf16* __restrict__ x,
   }
 }
 
+constexpr int kCombineBatch = 5;  // terms whose loads are in flight together
+
 // 2^e for an int8 exponent in [-126, 113], exact.
 __device__ __forceinline__ float pow2i(int e) { return __uint_as_float(static_cast<uint32_t>(e + 127) << 23); }
 
@@ -167,17 +169,31 @@ __global__ void __launch_bounds__(1024, 1) combine_kernel(const __half* __restri
   const int nterms = k + (has_shared ? 1 : 0);
   for (int c = threadIdx.x; c < d / 8; c += blockDim.x) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < nterms; ++j) {
-      const uint4 raw = __ldcs(reinterpret_cast<const uint4*>(yp + static_cast<size_t>(pos[j]) * d) + c);
-      const uint2 ex = __ldg(reinterpret_cast<const uint2*>(yexp + static_cast<size_t>(chunk[j]) * d) + c);
-      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-      const uint32_t eb[2] = {ex.x, ex.y};
+    // terms in batches of kCombineBatch: every load of a batch is issued
+    // before any of them is summed (the sum itself stays in slot order)
+    for (int j0 = 0; j0 < nterms; j0 += kCombineBatch) {
+      uint4 raw[kCombineBatch];
+      uint2 ex[kCombineBatch];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int e0 = static_cast<int8_t>((eb[i >> 1] >> (16 * (i & 1))) & 0xffu);
-        const int e1 = static_cast<int8_t>((eb[i >> 1] >> (16 * (i & 1) + 8)) & 0xffu);
-        acc[2 * i] += __half2float(__ushort_as_half(static_cast<unsigned short>(w[i] & 0xffffu))) * pow2i(e0);
-        acc[2 * i + 1] += __half2float(__ushort_as_half(static_cast<unsigned short>(w[i] >> 16))) * pow2i(e1);
+      for (int b = 0; b < kCombineBatch; ++b) {
+        if (j0 + b < nterms) {
+          raw[b] = __ldcs(reinterpret_cast<const uint4*>(yp + static_cast<size_t>(pos[j0 + b]) * d) + c);
+          ex[b] = __ldg(reinterpret_cast<const uint2*>(yexp + static_cast<size_t>(chunk[j0 + b]) * d) + c);
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < kCombineBatch; ++b) {
+        if (j0 + b < nterms) {
+          const uint32_t w[4] = {raw[b].x, raw[b].y, raw[b].z, raw[b].w};
+          const uint32_t eb[2] = {ex[b].x, ex[b].y};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int e0 = static_cast<int8_t>((eb[i >> 1] >> (16 * (i & 1))) & 0xffu);
+            const int e1 = static_cast<int8_t>((eb[i >> 1] >> (16 * (i & 1) + 8)) & 0xffu);
+            acc[2 * i] += __half2float(__ushort_as_half(static_cast<unsigned short>(w[i] & 0xffffu))) * pow2i(e0);
+            acc[2 * i + 1] += __half2float(__ushort_as_half(static_cast<unsigned short>(w[i] >> 16))) * pow2i(e1);
+          }
+        }
       }
     }
     if (out_fp32) {

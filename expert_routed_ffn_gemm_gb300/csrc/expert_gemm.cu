@@ -160,11 +160,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int k_steps = args.K / kBlockK;
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool issued_any = false, ok = true;
+      // N of the MMAs: the tile's rows rounded up to 16 (ragged tails); the
+      // next item's descriptor is worked out while this item's MMAs run
+      uint32_t next_idesc =
+          item_idesc(blockIdx.x, n_items, args.m_tiles, tile_start, G, args.offsets, kBlockM, 16, BN);
       for (int item = blockIdx.x; ok && item < n_items && !*abort_flag; item += gridDim.x) {
-        // N of the MMAs: the tile's rows rounded up to 16 (ragged tails)
-        const Item it = decode_item(item, args.m_tiles, tile_start, G);
-        const int rows = __ldg(args.offsets + it.g + 1) - __ldg(args.offsets + it.g) - it.n * BN;
-        const uint32_t idesc = idesc_bf16_f32(kBlockM, mma_width(rows, 16, BN));
+        const uint32_t idesc = next_idesc;
         if (!wait_or_abort(&acc_empty[acc], acc_phase ^ 1u, limit, abort_flag)) {
           record_abort(abort_flag, args.err);
           break;
@@ -190,6 +191,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             stage = 0;
             phase ^= 1u;
           }
+          if (kb == 0)
+            next_idesc = item_idesc(item + gridDim.x, n_items, args.m_tiles, tile_start, G, args.offsets, kBlockM,
+                                    16, BN);
         }
         if (!ok) break;
         tc_commit(&acc_full[acc]);

@@ -180,10 +180,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int k_steps = args.K / kBlockK;
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool issued_any = false, ok = true;
+      // N of the pair MMAs: the tile's rows rounded up to 32; the next
+      // item's descriptor is worked out while this item's MMAs run
+      uint32_t next_idesc =
+          item_idesc(pair, n_items, args.m_tiles, tile_start, G, args.offsets, 2 * kBlockM, 32, kPairN);
       for (int item = pair; ok && item < n_items && !*abort_flag; item += n_pairs) {
-        const Item it = decode_item(item, args.m_tiles, tile_start, G);
-        const int rows = __ldg(args.offsets + it.g + 1) - __ldg(args.offsets + it.g) - it.n * kPairN;
-        const uint32_t idesc = idesc_bf16_f32(2 * kBlockM, mma_width(rows, 32, kPairN));
+        const uint32_t idesc = next_idesc;
         if (!wait_cluster(&acc_empty[acc], acc_phase ^ 1u, limit, abort_flag)) {
           record_abort(abort_flag, args.err);
           break;
@@ -209,6 +211,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             stage = 0;
             phase ^= 1u;
           }
+          if (kb == 0)
+            next_idesc = item_idesc(item + n_pairs, n_items, args.m_tiles, tile_start, G, args.offsets,
+                                    2 * kBlockM, 32, kPairN);
         }
         if (!ok) break;
         tc_commit_pair_multicast(&acc_full[acc], 0x3);

@@ -73,6 +73,16 @@ __device__ __forceinline__ int mma_width(int valid, int step, int tile) {
   return w < tile ? w : tile;
 }
 
+// Instruction descriptor for work item `item` (M rows of weights, N = the
+// item's token rows rounded up to `step`, at most `tile`); 0 past the last item.
+__device__ __forceinline__ uint32_t item_idesc(int item, int n_items, int m_tiles, const int* tile_start, int G,
+                                               const int* offsets, int M, int step, int tile) {
+  if (item >= n_items) return 0;
+  const Item it = decode_item(item, m_tiles, tile_start, G);
+  const int rows = __ldg(offsets + it.g + 1) - __ldg(offsets + it.g) - it.n * tile;
+  return idesc_bf16_f32(M, mma_width(rows, step, tile));
+}
+
 __device__ __forceinline__ void record_abort(volatile int* abort_flag, uint32_t* err) {
   *abort_flag = 1;
   atomicOr(err, kErrWaitTimeout);

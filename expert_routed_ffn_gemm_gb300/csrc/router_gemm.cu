@@ -351,20 +351,18 @@ __device__ __forceinline__ void finish_token(float (&p)[kMaxPerLane], int t, int
         }
       }
 
+  // Selection rounds on the lane heads: probabilities are >= 0, so their bit
+  // patterns order like the values; key = bits + 1 (0 marks an empty head).
+  // One warp max of the keys, then the lowest expert index among the heads
+  // holding it (ties to the lower index).
   float pk = 0.f, sel_sum = 0.f, my_p = 0.f;
   int my_e = 0;
   for (int j = 0; j <= k; ++j) {
-    float bv = sv[0];
-    int be = se[0];
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-      if (better(ov, oe, bv, be)) {
-        bv = ov;
-        be = oe;
-      }
-    }
+    const uint32_t hk = (se[0] != 0x7fffffff) ? __float_as_uint(sv[0]) + 1u : 0u;
+    const uint32_t mk = __reduce_max_sync(0xffffffffu, hk);
+    const int be = static_cast<int>(
+        __reduce_min_sync(0xffffffffu, (mk != 0u && hk == mk) ? static_cast<uint32_t>(se[0]) : 0x7fffffffu));
+    const float bv = mk ? __uint_as_float(mk - 1u) : -1.f;
     if (j < k) {
       if (be != 0x7fffffff && (be & 31) == lane) {  // the winner pops its head
 #pragma unroll
@@ -445,6 +443,7 @@ __global__ void __launch_bounds__(kTopkTokensPerBlock * 32) router_topk_warp_ker
   float p[kMaxPerLane];
 #pragma unroll
   for (int i = 0; i < kMaxPerLane; ++i) p[i] = 0.f;
+#pragma unroll 4
   for (int s = 0; s < ksplit; ++s) {
     const float* row = partial + (static_cast<size_t>(s) * T + t) * E;
 #pragma unroll
