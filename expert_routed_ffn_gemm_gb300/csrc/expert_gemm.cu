@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       long issued = 0;
       bool ok = true;
       for (int item = blockIdx.x; ok && item < n_items && !*abort_flag; item += gridDim.x) {
-        const Item it = decode_item(item, args.m_tiles, tile_start, G);
+        const Item it = decode_item(item, args.m_tiles, tile_start, G, n_items, args.reverse);
         const int row_w = weight_row(it);
         const int row_act = __ldg(args.offsets + it.g) + it.n * BN;
         for (int kb = 0; kb < k_steps; ++kb) {
@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // N of the MMAs: the tile's rows rounded up to 16 (ragged tails); the
       // next item's descriptor is worked out while this item's MMAs run
       uint32_t next_idesc =
-          item_idesc(blockIdx.x, n_items, args.m_tiles, tile_start, G, args.offsets, kBlockM, 16, BN);
+          item_idesc(blockIdx.x, n_items, args.reverse, args.m_tiles, tile_start, G, args.offsets, kBlockM, 16, BN);
       for (int item = blockIdx.x; ok && item < n_items && !*abort_flag; item += gridDim.x) {
         const uint32_t idesc = next_idesc;
         if (!wait_or_abort(&acc_empty[acc], acc_phase ^ 1u, limit, abort_flag)) {
@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             phase ^= 1u;
           }
           if (kb == 0)
-            next_idesc = item_idesc(item + gridDim.x, n_items, args.m_tiles, tile_start, G, args.offsets, kBlockM,
+            next_idesc = item_idesc(item + gridDim.x, n_items, args.reverse, args.m_tiles, tile_start, G, args.offsets, kBlockM,
                                     16, BN);
         }
         if (!ok) break;
@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = q * 32 + lane;
     uint32_t acc = 0, acc_phase = 0, it_par = 0, chunk_par = 0;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-      const Item it = decode_item(item, args.m_tiles, tile_start, G);
+      const Item it = decode_item(item, args.m_tiles, tile_start, G, n_items, args.reverse);
       const int g_row0 = __ldg(args.offsets + it.g);
       const int g_rows = __ldg(args.offsets + it.g + 1) - g_row0;
       const int row0 = g_row0 + it.n * BN;

@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
       long issued = 0;
       bool ok = true;
       for (int item = blockIdx.x; ok && item < n_items && !*abort_flag; item += gridDim.x) {
-        const Item it = decode_item(item, args.m_tiles, tile_start, G);
+        const Item it = decode_item(item, args.m_tiles, tile_start, G, n_items, args.reverse);
         const int row_w = it.g * args.rows_per_group + it.m * (GATEUP ? kBlockM / 2 : kBlockM);
         const int row_act = __ldg(args.offsets + it.g) + it.n * BN;
         for (int kb = 0; kb < k_steps; ++kb) {
@@ -295,7 +295,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
     const int row = q * 32 + lane;
     uint32_t acc = 0, acc_phase = 0, it_par = 0, chunk_par = 0;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-      const Item it = decode_item(item, args.m_tiles, tile_start, G);
+      const Item it = decode_item(item, args.m_tiles, tile_start, G, n_items, args.reverse);
       const int g_row0 = __ldg(args.offsets + it.g);
       const int g_rows = __ldg(args.offsets + it.g + 1) - g_row0;
       const int row0 = g_row0 + it.n * BN;

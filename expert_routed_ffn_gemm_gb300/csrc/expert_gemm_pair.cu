@@ -135,7 +135,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       long issued = 0;
       bool ok = true;
       for (int item = pair; ok && item < n_items && !*abort_flag; item += n_pairs) {
-        const Item it = decode_item(item, args.m_tiles, tile_start, G);
+        const Item it = decode_item(item, args.m_tiles, tile_start, G, n_items, args.reverse);
         // K3: 64 gate rows (+ the matching 64 up rows at +F) per CTA, 128
         // features per pair tile; K4: 128 rows per CTA, 256 per pair tile.
         const int row_w = GATEUP ? it.g * args.rows_per_group + it.m * kBlockM + static_cast<int>(rank) * 64
@@ -183,7 +183,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // N of the pair MMAs: the tile's rows rounded up to 32; the next
       // item's descriptor is worked out while this item's MMAs run
       uint32_t next_idesc =
-          item_idesc(pair, n_items, args.m_tiles, tile_start, G, args.offsets, 2 * kBlockM, 32, kPairN);
+          item_idesc(pair, n_items, args.reverse, args.m_tiles, tile_start, G, args.offsets, 2 * kBlockM, 32, kPairN);
       for (int item = pair; ok && item < n_items && !*abort_flag; item += n_pairs) {
         const uint32_t idesc = next_idesc;
         if (!wait_cluster(&acc_empty[acc], acc_phase ^ 1u, limit, abort_flag)) {
@@ -212,7 +212,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             phase ^= 1u;
           }
           if (kb == 0)
-            next_idesc = item_idesc(item + n_pairs, n_items, args.m_tiles, tile_start, G, args.offsets,
+            next_idesc = item_idesc(item + n_pairs, n_items, args.reverse, args.m_tiles, tile_start, G, args.offsets,
                                     2 * kBlockM, 32, kPairN);
         }
         if (!ok) break;
@@ -233,7 +233,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int row = q * 32 + lane;
     uint32_t acc = 0, acc_phase = 0, it_par = 0, chunk_par = 0;
     for (int item = pair; item < n_items; item += n_pairs) {
-      const Item it = decode_item(item, args.m_tiles, tile_start, G);
+      const Item it = decode_item(item, args.m_tiles, tile_start, G, n_items, args.reverse);
       const int g_row0 = __ldg(args.offsets + it.g);
       const int g_rows = __ldg(args.offsets + it.g + 1) - g_row0;
       const int row0 = g_row0 + it.n * kPairN;

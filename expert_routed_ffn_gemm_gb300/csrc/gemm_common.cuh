@@ -22,7 +22,11 @@ struct Item {
 
 // item -> (group, token tile inside the group, weight tile); tile_start[g] is
 // the first token tile of group g (prefix over groups of ceil(rows/tile)).
-__device__ __forceinline__ Item decode_item(int item, int m_tiles, const int* tile_start, int G) {
+// With `reverse` the items run from the last group to the first (see the
+// gate/up launch: the rows written last by the gather are the ones still in L2).
+__device__ __forceinline__ Item decode_item(int item, int m_tiles, const int* tile_start, int G, int n_items,
+                                            int reverse) {
+  if (reverse) item = n_items - 1 - item;
   Item it;
   const int tile = item / m_tiles;
   it.m = item - tile * m_tiles;
@@ -75,10 +79,11 @@ __device__ __forceinline__ int mma_width(int valid, int step, int tile) {
 
 // Instruction descriptor for work item `item` (M rows of weights, N = the
 // item's token rows rounded up to `step`, at most `tile`); 0 past the last item.
-__device__ __forceinline__ uint32_t item_idesc(int item, int n_items, int m_tiles, const int* tile_start, int G,
-                                               const int* offsets, int M, int step, int tile) {
+__device__ __forceinline__ uint32_t item_idesc(int item, int n_items, int reverse, int m_tiles,
+                                               const int* tile_start, int G, const int* offsets, int M, int step,
+                                               int tile) {
   if (item >= n_items) return 0;
-  const Item it = decode_item(item, m_tiles, tile_start, G);
+  const Item it = decode_item(item, m_tiles, tile_start, G, n_items, reverse);
   const int rows = __ldg(offsets + it.g + 1) - __ldg(offsets + it.g) - it.n * tile;
   return idesc_bf16_f32(M, mma_width(rows, step, tile));
 }

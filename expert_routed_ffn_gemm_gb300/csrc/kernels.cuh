@@ -82,6 +82,7 @@ struct GemmArgs {
   int F;               // expert width (gate/up: offset of the up rows)
   int out_ld;          // row length of out
   int Tk;              // T*k: dispatch positions >= Tk belong to the shared expert
+  int reverse;         // 1: work items in reverse order (last group first)
 };
 
 // K3/K4: tcgen05 grouped GEMMs over the groups' row blocks.  `tile_n` must be

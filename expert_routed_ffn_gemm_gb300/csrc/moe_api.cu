@@ -280,6 +280,10 @@ int enqueue_forward(moe_handle* h, const void* x, int T, CallOpts o, void* y, cu
   a.F = c.ffn_width;
   a.Tk = T * o.k;
 
+  // gate/up runs its items last group first: the gather wrote the rows of the
+  // last groups last, so they are the ones still in L2; the down projection
+  // then runs first group first, over the H rows gate/up wrote last
+  a.reverse = 1;
   a.out = h->hbuf;
   a.K = c.d_model;
   a.rows_per_group = 2 * c.ffn_width;
@@ -295,6 +299,7 @@ int enqueue_forward(moe_handle* h, const void* x, int T, CallOpts o, void* y, cu
     MOE_CUDA(moe::launch_expert_gemm(true, bn1, &h->map_wgu, &h->map_xp[i1], a, h->num_sms, s));
   MOE_MARK(4);
 
+  a.reverse = 0;
   a.out = h->yp;
   a.out_exp = h->yexp;
   a.chunk_base = h->chunk_base;

@@ -80,6 +80,15 @@ def test_token_counts(T):
     run_and_check(inp, max_tokens=200)
 
 
+@pytest.mark.parametrize("T", [5000, 20000])
+def test_many_tokens_small_layer(T):
+    # Many tokens over few experts: 256-token router tiles, one warp per token
+    # in the top-k, groups of hundreds of rows on CTA pairs with ragged tails.
+    shape = synth.LayerShape(T=T, d=256, E=16, k=2, F=128)
+    inp = synth.make_inputs(shape, seed=50 + T % 7)
+    run_and_check(inp, tokens=64)
+
+
 def test_several_weight_tiles_and_k_steps():
     # F = 256 -> 2 gate/up weight tiles, d = 512 -> 4 down weight tiles and 8 K steps.
     shape = synth.LayerShape(T=200, d=512, E=32, k=4, F=256)

@@ -37,7 +37,7 @@ def test_smaller_top_k_per_call(kk):
     layer.close()
 
 
-@pytest.mark.parametrize("kk,T", [(2, 120), (8, 120), (4, 1100)])
+@pytest.mark.parametrize("kk,T", [(2, 120), (8, 120), (4, 1100), (4, 6000)])
 def test_renormalized_weights(kk, T):
     # T = 1100: the one-warp-per-token top-k kernel (1024 tokens and more)
     shape = synth.LayerShape(T=T, d=256, E=32, k=8, F=128)
@@ -86,11 +86,12 @@ def flash_small_weights():
     return synth.make_inputs(synth.FLASH_DECODE.with_tokens(64), seed=5, device=DEV)
 
 
-@pytest.mark.parametrize("case", ["tiny", "tiny_many_tokens", "flash"])
+@pytest.mark.parametrize("case", ["tiny", "tiny_many_tokens", "tiny_256_tiles", "flash"])
 def test_route_stats_match_oracle(case, flash_small_weights):
     if case.startswith("tiny"):
-        # 1500 tokens: the one-warp-per-token top-k kernel writes the statistics
-        T = 1500 if case == "tiny_many_tokens" else 300
+        # 1500 and 6000 tokens: the one-warp-per-token top-k kernel writes the
+        # statistics (6000: 256-token router tiles)
+        T = {"tiny": 300, "tiny_many_tokens": 1500, "tiny_256_tiles": 6000}[case]
         inp = synth.make_inputs(synth.LayerShape(T=T, d=256, E=16, k=2, F=128), seed=80)
         G = 4
     else:
