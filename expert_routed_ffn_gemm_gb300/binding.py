@@ -32,7 +32,8 @@ MOE_ERR_NO_DEVICE = 6
 EXPORTED = ("moe_init", "moe_route", "moe_forward", "moe_forward_host", "moe_check", "moe_set_wait_limit",
             "moe_profile_enable", "moe_profile_read", "moe_free", "moe_status_string",
             "moe_selftest_wait_timeout", "moe_dispatch_noalloc", "moe_route_ex", "moe_forward_ex",
-            "moe_route_stats", "moe_last_kernel_count", "moe_init_fp8", "moe_quantize_fp8")
+            "moe_route_stats", "moe_last_kernel_count", "moe_init_fp8", "moe_quantize_fp8", "moe_ep_init",
+            "moe_ep_dispatch", "moe_ep_experts", "moe_ep_combine")
 PROFILE_STAGES = ("routing", "dispatch", "gather", "gate_up_gemm", "down_gemm", "combine")
 
 
@@ -55,6 +56,11 @@ class moe_weights(ctypes.Structure):
 class moe_weights_fp8(ctypes.Structure):
     _fields_ = [("w_router", ctypes.c_void_p), ("w_gate_up", ctypes.c_void_p), ("s_gate_up", ctypes.c_void_p),
                 ("w_down", ctypes.c_void_p), ("s_down", ctypes.c_void_p)]
+
+
+class moe_ep_config(ctypes.Structure):
+    _fields_ = [("layer", moe_config), ("ep_size", ctypes.c_int), ("ep_rank", ctypes.c_int),
+                ("max_recv_rows", ctypes.c_int)]
 
 
 class moe_call_options(ctypes.Structure):
@@ -90,6 +96,10 @@ def load():
         lib.moe_init_fp8.argtypes = [ctypes.POINTER(moe_config), ctypes.POINTER(moe_weights_fp8),
                                      ctypes.POINTER(vp)]
         lib.moe_quantize_fp8.argtypes = [vp, ctypes.c_longlong, i, vp, vp, vp]
+        lib.moe_ep_init.argtypes = [ctypes.POINTER(moe_ep_config), ctypes.POINTER(moe_weights), ctypes.POINTER(vp)]
+        lib.moe_ep_dispatch.argtypes = [vp, vp, i, vp, vp, vp, ctypes.POINTER(ctypes.c_int), vp]
+        lib.moe_ep_experts.argtypes = [vp, vp, vp, vp, i, vp, vp, ctypes.POINTER(ctypes.c_int), vp]
+        lib.moe_ep_combine.argtypes = [vp, vp, vp, vp, vp]
         lib.moe_route.argtypes = [vp, vp, i, vp, vp, vp, vp, vp, vp]
         lib.moe_forward.argtypes = [vp, vp, i, vp, vp]
         lib.moe_forward_host.argtypes = [vp, vp, i, vp, vp]
@@ -165,6 +175,34 @@ def moe_quantize_fp8(w: torch.Tensor, stream=None):
     s = torch.empty(w.shape[:-1], dtype=torch.float32, device=w.device)
     _check(load().moe_quantize_fp8(_ptr(w), rows, cols, _ptr(q), _ptr(s), _stream(stream)), "moe_quantize_fp8")
     return q, s
+
+
+def moe_ep_init(cfg: moe_ep_config, w_router, w_gate_up_local, w_down_local) -> int:
+    """Expert-parallel handle (moe_weights layout: the router over all experts,
+    this rank's experts then the shared expert)."""
+    w = moe_weights(_ptr(w_router), _ptr(w_gate_up_local), _ptr(w_down_local))
+    h = ctypes.c_void_p()
+    _check(load().moe_ep_init(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)), "moe_ep_init")
+    return h.value
+
+
+def moe_ep_dispatch(h: int, x, T: int, send_rows, send_w, send_counts, ep_size: int, stream=None) -> list[int]:
+    rows = (ctypes.c_int * ep_size)()
+    _check(load().moe_ep_dispatch(h, _ptr(x), int(T), _ptr(send_rows), _ptr(send_w), _ptr(send_counts), rows,
+                                  _stream(stream)), "moe_ep_dispatch")
+    return list(rows)
+
+
+def moe_ep_experts(h: int, recv_rows, recv_counts, recv_w, n_recv: int, out_rows, out_exp, ep_size: int,
+                   stream=None) -> list[int]:
+    chunks = (ctypes.c_int * ep_size)()
+    _check(load().moe_ep_experts(h, _ptr(recv_rows), _ptr(recv_counts), _ptr(recv_w), int(n_recv), _ptr(out_rows),
+                                 _ptr(out_exp), chunks, _stream(stream)), "moe_ep_experts")
+    return list(chunks)
+
+
+def moe_ep_combine(h: int, ret_rows, ret_exp, y, stream=None) -> None:
+    _check(load().moe_ep_combine(h, _ptr(ret_rows), _ptr(ret_exp), _ptr(y), _stream(stream)), "moe_ep_combine")
 
 
 def moe_route(h: int, x, T: int, idx, prob, perm, offsets, gap=None, stream=None) -> None:

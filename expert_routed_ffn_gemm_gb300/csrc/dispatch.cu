@@ -150,6 +150,8 @@ __device__ __forceinline__ float pow2i(int e) { return __uint_as_float(static_ca
 // in flight at once.
 __global__ void __launch_bounds__(1024, 1) combine_kernel(const __half* __restrict__ yp,
                                                           const int8_t* __restrict__ yexp,
+                                                          const __half* __restrict__ yp_routed,
+                                                          const int8_t* __restrict__ yexp_routed,
                                                           const int* __restrict__ idx, const int* __restrict__ inv,
                                                           const int* __restrict__ offsets,
                                                           const int* __restrict__ chunk_base, int T, int k, int E,
@@ -167,6 +169,10 @@ __global__ void __launch_bounds__(1024, 1) combine_kernel(const __half* __restri
   }
   __syncthreads();
   const int nterms = k + (has_shared ? 1 : 0);
+  // routed rows (slots j < k) from yp_routed / yexp_routed when given
+  // (expert parallelism: the rows the experts' owners sent back)
+  const __half* yp_r = yp_routed ? yp_routed : yp;
+  const int8_t* ye_r = yp_routed ? yexp_routed : yexp;
   for (int c = threadIdx.x; c < d / 8; c += blockDim.x) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     // terms in batches of kCombineBatch: every load of a batch is issued
@@ -177,8 +183,11 @@ __global__ void __launch_bounds__(1024, 1) combine_kernel(const __half* __restri
 #pragma unroll
       for (int b = 0; b < kCombineBatch; ++b) {
         if (j0 + b < nterms) {
-          raw[b] = __ldcs(reinterpret_cast<const uint4*>(yp + static_cast<size_t>(pos[j0 + b]) * d) + c);
-          ex[b] = __ldg(reinterpret_cast<const uint2*>(yexp + static_cast<size_t>(chunk[j0 + b]) * d) + c);
+          const bool routed = j0 + b < k;
+          raw[b] = __ldcs(reinterpret_cast<const uint4*>((routed ? yp_r : yp) + static_cast<size_t>(pos[j0 + b]) * d) +
+                          c);
+          ex[b] = __ldg(reinterpret_cast<const uint2*>((routed ? ye_r : yexp) + static_cast<size_t>(chunk[j0 + b]) * d) +
+                        c);
         }
       }
 #pragma unroll
@@ -259,6 +268,57 @@ __global__ void __launch_bounds__(256) quantize_e4m3_kernel(const bf16* __restri
   }
 }
 
+// One block: prefix sums over the (source, expert) groups of the rows and of
+// their 16-row exponent chunks, in source-major order.
+__global__ void ep_groups_kernel(const int* __restrict__ recv_counts, int S, int E_loc, int* __restrict__ offsets,
+                                 int* __restrict__ chunk_base, int* __restrict__ chunks_per_source) {
+  if (threadIdx.x != 0) return;
+  int rows = 0, chunks = 0;
+  for (int s = 0; s < S; ++s) {
+    const int c0 = chunks;
+    for (int e = 0; e < E_loc; ++e) {
+      const int g = s * E_loc + e;
+      offsets[g] = rows;
+      chunk_base[g] = chunks;
+      const int n = recv_counts[g];
+      rows += n;
+      chunks += (n + kYpRows - 1) / kYpRows;
+    }
+    chunks_per_source[s] = chunks - c0;
+  }
+  offsets[S * E_loc] = rows;
+  chunk_base[S * E_loc] = chunks;
+}
+
+__global__ void gather_weights_kernel(const int* __restrict__ perm, const float* __restrict__ prob, int n,
+                                      float* __restrict__ w) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) w[i] = prob[perm[i]];
+}
+
+__global__ void iota_kernel(int* __restrict__ v, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) v[i] = i;
+}
+
+cudaError_t launch_ep_groups(const int* recv_counts, int S, int E_loc, int* offsets, int* chunk_base,
+                             int* chunks_per_source, cudaStream_t stream) {
+  ep_groups_kernel<<<1, 32, 0, stream>>>(recv_counts, S, E_loc, offsets, chunk_base, chunks_per_source);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_weights(const int* perm, const float* prob, int n, float* w, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  gather_weights_kernel<<<(n + 255) / 256, 256, 0, stream>>>(perm, prob, n, w);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_iota(int* v, int n, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  iota_kernel<<<(n + 255) / 256, 256, 0, stream>>>(v, n);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_quantize_e4m3(const bf16* w, long long rows, int cols, uint8_t* q, float* s,
                                  cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
@@ -267,14 +327,14 @@ cudaError_t launch_quantize_e4m3(const bf16* w, long long rows, int cols, uint8_
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const __half* yp, const int8_t* yexp, const int* idx, const int* inv,
-                           const int* offsets, const int* chunk_base, int T, int k, int E, int d, int has_shared,
-                           void* y, int out_fp32, cudaStream_t stream) {
+cudaError_t launch_combine(const __half* yp, const int8_t* yexp, const __half* yp_routed, const int8_t* yexp_routed,
+                           const int* idx, const int* inv, const int* offsets, const int* chunk_base, int T, int k,
+                           int E, int d, int has_shared, void* y, int out_fp32, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   const int chunks = d / 8;
   const int threads = chunks > 1024 ? 1024 : (chunks < 32 ? 32 : chunks);
-  combine_kernel<<<T, threads, 0, stream>>>(yp, yexp, idx, inv, offsets, chunk_base, T, k, E, d, has_shared, y,
-                                            out_fp32);
+  combine_kernel<<<T, threads, 0, stream>>>(yp, yexp, yp_routed, yexp_routed, idx, inv, offsets, chunk_base, T, k,
+                                            E, d, has_shared, y, out_fp32);
   return cudaGetLastError();
 }
 

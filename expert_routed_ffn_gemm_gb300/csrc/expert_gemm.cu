@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int k_steps = args.K / kBlockK;
       // K3: gate rows 64m.. of group g, then the up rows F + 64m..; K4: rows 128m..
       auto weight_row = [&](const Item& it) {
-        return it.g * args.rows_per_group + it.m * (GATEUP ? kBlockM / 2 : kBlockM);
+        return weight_group(args, it.g) * args.rows_per_group + it.m * (GATEUP ? kBlockM / 2 : kBlockM);
       };
       uint32_t stage = 0, phase = 0;
       long issued = 0;

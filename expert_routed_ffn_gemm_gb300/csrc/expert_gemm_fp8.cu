@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
       bool ok = true;
       for (int item = blockIdx.x; ok && item < n_items && !*abort_flag; item += gridDim.x) {
         const Item it = decode_item(item, args.m_tiles, tile_start, G, n_items, args.reverse);
-        const int row_w = it.g * args.rows_per_group + it.m * (GATEUP ? kBlockM / 2 : kBlockM);
+        const int row_w = weight_group(args, it.g) * args.rows_per_group + it.m * (GATEUP ? kBlockM / 2 : kBlockM);
         const int row_act = __ldg(args.offsets + it.g) + it.n * BN;
         for (int kb = 0; kb < k_steps; ++kb) {
           if (!wait_or_abort(&a8_empty[sa], pa ^ 1u, limit, abort_flag) ||
@@ -304,9 +304,11 @@ __global__ void __launch_bounds__(kThreads8, 1)
       if (!GATEUP) load_gate_weights<BN>(wreg, row0, valid, lane, args.perm, args.prob, args.Tk);
       // the scale of this thread's weight row
       const float scale =
-          GATEUP ? __ldg(args.w_scale + static_cast<size_t>(it.g) * args.rows_per_group + (row < 64 ? 0 : args.F) +
+          GATEUP ? __ldg(args.w_scale + static_cast<size_t>(weight_group(args, it.g)) * args.rows_per_group +
+                         (row < 64 ? 0 : args.F) +
                          it.m * (kBlockM / 2) + (row & 63))
-                 : __ldg(args.w_scale + static_cast<size_t>(it.g) * args.rows_per_group + it.m * kBlockM + row);
+                 : __ldg(args.w_scale + static_cast<size_t>(weight_group(args, it.g)) * args.rows_per_group +
+                         it.m * kBlockM + row);
       if (!epilogue_wait(&acc_full[acc], acc_phase, limit, abort_flag, s_ok, it_par, q, lane, args.err)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;

@@ -138,8 +138,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const Item it = decode_item(item, args.m_tiles, tile_start, G, n_items, args.reverse);
         // K3: 64 gate rows (+ the matching 64 up rows at +F) per CTA, 128
         // features per pair tile; K4: 128 rows per CTA, 256 per pair tile.
-        const int row_w = GATEUP ? it.g * args.rows_per_group + it.m * kBlockM + static_cast<int>(rank) * 64
-                                 : it.g * args.rows_per_group + it.m * 2 * kBlockM + static_cast<int>(rank) * kBlockM;
+        const int wg = weight_group(args, it.g);
+        const int row_w = GATEUP ? wg * args.rows_per_group + it.m * kBlockM + static_cast<int>(rank) * 64
+                                 : wg * args.rows_per_group + it.m * 2 * kBlockM + static_cast<int>(rank) * kBlockM;
         // the pair MMA takes N/2 token rows from each CTA: N = the tile's rows
         // rounded up to 32, so the odd CTA's rows start at N/2
         const int g_row0 = __ldg(args.offsets + it.g);

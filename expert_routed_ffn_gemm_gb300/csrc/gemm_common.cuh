@@ -88,6 +88,12 @@ __device__ __forceinline__ uint32_t item_idesc(int item, int n_items, int revers
   return idesc_bf16_f32(M, mma_width(rows, step, tile));
 }
 
+// Weight group of row group g (expert parallelism maps (source, expert) row
+// groups onto the local experts; otherwise the identity).
+__device__ __forceinline__ int weight_group(const GemmArgs& a, int g) {
+  return a.w_group_base + (a.w_group_mod ? g % a.w_group_mod : g);
+}
+
 __device__ __forceinline__ void record_abort(volatile int* abort_flag, uint32_t* err) {
   *abort_flag = 1;
   atomicOr(err, kErrWaitTimeout);

@@ -83,6 +83,8 @@ struct GemmArgs {
   int out_ld;          // row length of out
   int Tk;              // T*k: dispatch positions >= Tk belong to the shared expert
   int reverse;         // 1: work items in reverse order (last group first)
+  int w_group_base;    // weights of group g: w_group_base + (w_group_mod ? g % w_group_mod : g)
+  int w_group_mod;
 };
 
 // K3/K4: tcgen05 grouped GEMMs over the groups' row blocks.  `tile_n` must be
@@ -118,9 +120,21 @@ cudaError_t launch_quantize_e4m3(const bf16* w, long long rows, int cols, uint8_
 // K5: y[t] = sum_j Yp[inv[t*k+j]] + Yp[T*k + t], fp32 in fixed order, each
 // term read back as h * 2^e from the scaled fp16 Yp and its exponents (the
 // chunk of a row found from its expert idx[t*k+j], offsets and chunk_base).
-cudaError_t launch_combine(const __half* yp, const int8_t* yexp, const int* idx, const int* inv,
-                           const int* offsets, const int* chunk_base, int T, int k, int E, int d, int has_shared,
-                           void* y, int out_fp32, cudaStream_t stream);
+// yp_routed / yexp_routed (or NULL): where the routed rows (slots j < k) and
+// their exponent chunks are, if not in yp / yexp (same positions and chunks).
+cudaError_t launch_combine(const __half* yp, const int8_t* yexp, const __half* yp_routed, const int8_t* yexp_routed,
+                           const int* idx, const int* inv, const int* offsets, const int* chunk_base, int T, int k,
+                           int E, int d, int has_shared, void* y, int out_fp32, cudaStream_t stream);
+
+// Expert parallelism helpers.  ep_groups: from recv_counts [S][E_loc] (rows
+// per (source, local expert)), the row offsets [S*E_loc + 1] and exponent
+// chunk bases [S*E_loc + 1] of the (source, expert) groups in source-major
+// order, and the chunks of each source's block [S].  gather_weights:
+// w[pos] = prob[perm[pos]] for pos < n.  iota: v[i] = i for i < n.
+cudaError_t launch_ep_groups(const int* recv_counts, int S, int E_loc, int* offsets, int* chunk_base,
+                             int* chunks_per_source, cudaStream_t stream);
+cudaError_t launch_gather_weights(const int* perm, const float* prob, int n, float* w, cudaStream_t stream);
+cudaError_t launch_iota(int* v, int n, cudaStream_t stream);
 
 // Bounded-wait self test: waits on a barrier that never completes.
 cudaError_t launch_wait_selftest(uint32_t* err, unsigned long long limit_ns, cudaStream_t stream);

@@ -39,6 +39,14 @@ struct moe_handle {
   bool fp8;           // E4M3 expert weights with per-row scales (moe_init_fp8)
   const float* s_gate_up;  // fp8: [G][2F] row scales
   const float* s_down;     // fp8: [G][d] row scales
+  // expert parallelism (moe_ep_init): this rank owns routed experts
+  // [ep_rank * e_loc, (ep_rank + 1) * e_loc); ep_size = 0 for a whole-layer handle
+  int ep_size, ep_rank, e_loc, max_recv;
+  int ep_T;                // tokens of the last moe_ep_dispatch
+  int* ep_offsets;         // [ep_size * e_loc + 1] row offsets of the received (source, expert) groups
+  int* ep_chunk_base;      // [ep_size * e_loc + 1] their exponent chunk bases
+  int* ep_chunks_src;      // [ep_size] exponent chunks per source block
+  int* ep_iota;            // [max_recv] 0, 1, 2, ... (received rows carry their own gate weight)
   unsigned long long wait_limit_ns;
   int router_m_tiles;      // ceil(E / 128)
   long long partial_rows;  // capacity of `partial` in (split, token) rows
@@ -246,6 +254,62 @@ cudaEvent_t* prof_slot(moe_handle* h) {
 #define MOE_MARK(i) \
   if (ev) MOE_CUDA(cudaEventRecord(ev[i], s))
 
+// The grouped FFN over the row groups of `base` (offsets, G, perm/prob/Tk for
+// the gate weights, chunk_base, weight-group mapping): gate/up from the rows
+// behind map_rows (one map per tile width) into H, then down into yout (fp16)
+// and yexp.  mean_rows: mean rows per group (picks the token tile width).
+// ev (or NULL): profiling events 3..5 around the two GEMMs.
+int enqueue_ffn(moe_handle* h, moe::GemmArgs a, double mean_rows, const CUtensorMap* map_rows, void* yout,
+                int8_t* yexp, cudaEvent_t* ev, cudaStream_t s) {
+  const moe_config& c = h->cfg;
+  const int cap = h->fp8 ? 128 : 256;
+  const int bn1 = h->tile_gateup ? std::min(h->tile_gateup, cap) : choose_tile(mean_rows, cap);
+  const int bn2 = h->tile_down ? std::min(h->tile_down, cap) : choose_tile(mean_rows, cap);
+  // 256-row token tiles run on CTA pairs (M = 256 weight rows per pair)
+  const int i128 = tile_index(128);
+  const bool pair1 = h->use_pairs && bn1 == 256;
+  const bool pair2 = h->use_pairs && bn2 == 256 && c.d_model % 256 == 0;
+  a.err = h->err;
+  a.wait_limit_ns = h->wait_limit_ns;
+  a.F = c.ffn_width;
+
+  // gate/up runs its items last group first: the gather wrote the rows of the
+  // last groups last, so they are the ones still in L2; the down projection
+  // then runs first group first, over the H rows gate/up wrote last
+  a.reverse = 1;
+  a.out = h->hbuf;
+  a.K = c.d_model;
+  a.rows_per_group = 2 * c.ffn_width;
+  a.m_tiles = pair1 ? c.ffn_width / moe::kBlockM : c.ffn_width / (moe::kBlockM / 2);
+  a.out_ld = c.ffn_width;
+  const int i1 = tile_index(bn1), i2 = tile_index(bn2);
+  a.w_scale = h->s_gate_up;
+  if (h->fp8)
+    MOE_CUDA(moe::launch_expert_gemm_fp8(true, bn1, &h->map_wgu, &map_rows[i1], a, h->num_sms, s));
+  else if (pair1)
+    MOE_CUDA(moe::launch_expert_gemm_pair(true, &h->map_wgu, &map_rows[i128], a, h->num_sms, s));
+  else
+    MOE_CUDA(moe::launch_expert_gemm(true, bn1, &h->map_wgu, &map_rows[i1], a, h->num_sms, s));
+  MOE_MARK(4);
+
+  a.reverse = 0;
+  a.out = yout;
+  a.out_exp = yexp;
+  a.K = c.ffn_width;
+  a.rows_per_group = c.d_model;
+  a.m_tiles = pair2 ? c.d_model / (2 * moe::kBlockM) : c.d_model / moe::kBlockM;
+  a.out_ld = c.d_model;
+  a.w_scale = h->s_down;
+  if (h->fp8)
+    MOE_CUDA(moe::launch_expert_gemm_fp8(false, bn2, &h->map_wd, &h->map_h[i2], a, h->num_sms, s));
+  else if (pair2)
+    MOE_CUDA(moe::launch_expert_gemm_pair(false, &h->map_wd, &h->map_h[i128], a, h->num_sms, s));
+  else
+    MOE_CUDA(moe::launch_expert_gemm(false, bn2, &h->map_wd, &h->map_h[i2], a, h->num_sms, s));
+  MOE_MARK(5);
+  return MOE_OK;
+}
+
 int enqueue_forward(moe_handle* h, const void* x, int T, CallOpts o, void* y, cudaStream_t s) {
   const moe_config& c = h->cfg;
   cudaEvent_t* ev = prof_slot(h);
@@ -261,62 +325,18 @@ int enqueue_forward(moe_handle* h, const void* x, int T, CallOpts o, void* y, cu
   MOE_CUDA(moe::launch_gather(static_cast<const bf16*>(x), h->perm, T, o.k, c.d_model, c.has_shared, h->yp, h->fp8,
                               s));
   MOE_MARK(3);
-  const double mean_rows = static_cast<double>(T) * o.k / c.n_experts;
-  const int cap = h->fp8 ? 128 : 256;
-  const int bn1 = h->tile_gateup ? std::min(h->tile_gateup, cap) : choose_tile(mean_rows, cap);
-  const int bn2 = h->tile_down ? std::min(h->tile_down, cap) : choose_tile(mean_rows, cap);
-  // 256-row token tiles run on CTA pairs (M = 256 weight rows per pair)
-  const int i128 = tile_index(128);
-  const bool pair1 = h->use_pairs && bn1 == 256;
-  const bool pair2 = h->use_pairs && bn2 == 256 && c.d_model % 256 == 0;
-
   moe::GemmArgs a{};
   a.offsets = h->offsets;
   a.perm = h->perm;
   a.prob = h->prob;
-  a.err = h->err;
-  a.wait_limit_ns = h->wait_limit_ns;
   a.G = h->G;
-  a.F = c.ffn_width;
   a.Tk = T * o.k;
-
-  // gate/up runs its items last group first: the gather wrote the rows of the
-  // last groups last, so they are the ones still in L2; the down projection
-  // then runs first group first, over the H rows gate/up wrote last
-  a.reverse = 1;
-  a.out = h->hbuf;
-  a.K = c.d_model;
-  a.rows_per_group = 2 * c.ffn_width;
-  a.m_tiles = pair1 ? c.ffn_width / moe::kBlockM : c.ffn_width / (moe::kBlockM / 2);
-  a.out_ld = c.ffn_width;
-  const int i1 = tile_index(bn1), i2 = tile_index(bn2);
-  a.w_scale = h->s_gate_up;
-  if (h->fp8)
-    MOE_CUDA(moe::launch_expert_gemm_fp8(true, bn1, &h->map_wgu, &h->map_xp[i1], a, h->num_sms, s));
-  else if (pair1)
-    MOE_CUDA(moe::launch_expert_gemm_pair(true, &h->map_wgu, &h->map_xp[i128], a, h->num_sms, s));
-  else
-    MOE_CUDA(moe::launch_expert_gemm(true, bn1, &h->map_wgu, &h->map_xp[i1], a, h->num_sms, s));
-  MOE_MARK(4);
-
-  a.reverse = 0;
-  a.out = h->yp;
-  a.out_exp = h->yexp;
   a.chunk_base = h->chunk_base;
-  a.K = c.ffn_width;
-  a.rows_per_group = c.d_model;
-  a.m_tiles = pair2 ? c.d_model / (2 * moe::kBlockM) : c.d_model / moe::kBlockM;
-  a.out_ld = c.d_model;
-  a.w_scale = h->s_down;
-  if (h->fp8)
-    MOE_CUDA(moe::launch_expert_gemm_fp8(false, bn2, &h->map_wd, &h->map_h[i2], a, h->num_sms, s));
-  else if (pair2)
-    MOE_CUDA(moe::launch_expert_gemm_pair(false, &h->map_wd, &h->map_h[i128], a, h->num_sms, s));
-  else
-    MOE_CUDA(moe::launch_expert_gemm(false, bn2, &h->map_wd, &h->map_h[i2], a, h->num_sms, s));
-  MOE_MARK(5);
-  MOE_CUDA(moe::launch_combine(static_cast<const __half*>(h->yp), h->yexp, h->idx, h->inv, h->offsets,
-                               h->chunk_base, T, o.k, c.n_experts, c.d_model, c.has_shared, y, c.out_fp32, s));
+  if (int rc2 = enqueue_ffn(h, a, static_cast<double>(T) * o.k / c.n_experts, h->map_xp, h->yp, h->yexp, ev, s))
+    return rc2;
+  MOE_CUDA(moe::launch_combine(static_cast<const __half*>(h->yp), h->yexp, nullptr, nullptr, h->idx, h->inv,
+                               h->offsets, h->chunk_base, T, o.k, c.n_experts, c.d_model, c.has_shared, y, c.out_fp32,
+                               s));
   MOE_MARK(6);
   h->last_kernels = 7;  // router GEMM, top-k, dispatch, gather, gate/up, down, combine
   return MOE_OK;
@@ -347,12 +367,22 @@ namespace {
 
 // moe_init and moe_init_fp8: w holds the router and the two expert weight
 // arrays (bf16, or E4M3 codes when s_gu / s_d, the row scales, are given).
-int init_any(const moe_config* cfg, const moe_weights* w, const float* s_gu, const float* s_d, moe_handle** out) {
+struct EpParams {
+  int size = 0, rank = 0, max_recv = 0;  // size 0: not expert-parallel
+};
+
+int init_any(const moe_config* cfg, const moe_weights* w, const float* s_gu, const float* s_d, moe_handle** out,
+             EpParams ep = EpParams()) {
   if (out == nullptr) return MOE_ERR_INVALID_ARG;
   *out = nullptr;
   if (cfg == nullptr || w == nullptr) return MOE_ERR_INVALID_ARG;
   const bool fp8 = s_gu != nullptr;
   const moe_config c = *cfg;
+  if (ep.size != 0) {
+    if (ep.size < 1 || ep.rank < 0 || ep.rank >= ep.size || ep.max_recv < 0 || c.n_experts <= 0)
+      return MOE_ERR_INVALID_ARG;
+    if (c.n_experts % ep.size != 0 || fp8 || ep.max_recv > (1 << 26)) return MOE_ERR_UNSUPPORTED;
+  }
   if (c.d_model <= 0 || c.n_experts <= 0 || c.top_k <= 0 || c.ffn_width <= 0 || c.max_tokens <= 0)
     return MOE_ERR_INVALID_ARG;
   if (c.has_shared != 0 && c.has_shared != 1) return MOE_ERR_INVALID_ARG;
@@ -397,6 +427,10 @@ int init_any(const moe_config* cfg, const moe_weights* w, const float* s_gu, con
   h->device = dev;
   h->num_sms = sms;
   h->G = c.n_experts + c.has_shared;
+  h->ep_size = ep.size;
+  h->ep_rank = ep.rank;
+  h->e_loc = ep.size ? c.n_experts / ep.size : c.n_experts;
+  h->max_recv = ep.max_recv;
   h->tile_gateup = tile_from_env("MOE_TILE_N_GATEUP");
   h->tile_down = tile_from_env("MOE_TILE_N_DOWN");
   {
@@ -411,6 +445,9 @@ int init_any(const moe_config* cfg, const moe_weights* w, const float* s_gu, con
   const size_t Tmax = static_cast<size_t>(c.max_tokens);
   const size_t E = c.n_experts, k = c.top_k, d = c.d_model, F = c.ffn_width;
   const size_t R = (k + 1) * Tmax;
+  // H rows: this rank's own dispatch rows, or the rows it may receive (EP)
+  const size_t RH = R > static_cast<size_t>(ep.max_recv) ? R : static_cast<size_t>(ep.max_recv);
+  const size_t n_epg = static_cast<size_t>(ep.size) * (ep.size ? c.n_experts / ep.size : 0) + 1;
   const size_t e_pad = static_cast<size_t>(h->router_m_tiles) * moe::kBlockM;
   // partial logits: room for 16 K splits of up to 2048 tokens, or one of Tmax
   const size_t p_rows = Tmax > 16 * 2048 ? Tmax : (Tmax < 2048 ? 16 * Tmax : 16 * 2048);
@@ -425,7 +462,9 @@ int init_any(const moe_config* cfg, const moe_weights* w, const float* s_gu, con
                o_partial = carve(4 * p_rows * E), o_w3 = carve(2 * 3 * e_pad * d), o_idx = carve(4 * Tmax * k),
                o_prob = carve(4 * Tmax * k), o_perm = carve(4 * Tmax * k), o_inv = carve(4 * Tmax * k),
                o_yp = carve(2 * R * d), o_ye = carve((R / moe::kYpRows + E + 2) * d), o_cb = carve(4 * (E + 2)),
-               o_h = carve(2 * R * F),
+               o_h = carve(2 * RH * F),
+               o_epo = carve(4 * n_epg), o_epc = carve(4 * n_epg), o_eps = carve(4 * (ep.size + 1)),
+               o_epi = carve(4 * (static_cast<size_t>(ep.max_recv) + 1)),
                o_xs = carve(2 * Tmax * d),
                o_ys = carve((c.out_fp32 ? 4 : 2) * Tmax * d),
                o_tok = carve(4 * Tmax * (moe::kMaxStatGroups + 1));
@@ -451,17 +490,23 @@ int init_any(const moe_config* cfg, const moe_weights* w, const float* s_gu, con
   h->x_stage = reinterpret_cast<bf16*>(b + o_xs);
   h->y_stage = b + o_ys;
   h->tokstats = reinterpret_cast<float*>(b + o_tok);
+  h->ep_offsets = reinterpret_cast<int*>(b + o_epo);
+  h->ep_chunk_base = reinterpret_cast<int*>(b + o_epc);
+  h->ep_chunks_src = reinterpret_cast<int*>(b + o_eps);
+  h->ep_iota = reinterpret_cast<int*>(b + o_epi);
 
   bool ok = cudaMemset(h->ws, 0, o_partial) == cudaSuccess;  // counts, error word, offsets
   ok = ok && moe::launch_split_router(w->w_router, c.n_experts, c.d_model, static_cast<int>(e_pad), h->w3,
                                       nullptr) == cudaSuccess;
-  const size_t G = h->G;
+  // weight groups held by this handle: all, or (EP) the local experts + shared
+  const size_t G = ep.size ? static_cast<size_t>(h->e_loc + c.has_shared) : static_cast<size_t>(h->G);
+  ok = ok && moe::launch_iota(h->ep_iota, ep.max_recv, nullptr) == cudaSuccess;
   ok = ok && encode_2d(&h->map_w3, h->w3, 3 * e_pad, d, moe::kBlockM);
   ok = ok && encode_2d(&h->map_wgu, w->w_gate_up, G * 2 * F, d, moe::kBlockM / 2, fp8);
   ok = ok && encode_2d(&h->map_wd, w->w_down, G * d, F, moe::kBlockM, fp8);
   for (int i = 0; ok && i < moe::kNumTileN; ++i) {
     ok = ok && encode_2d(&h->map_xp[i], h->yp, R, d, moe::kTileN[i]);
-    ok = ok && encode_2d(&h->map_h[i], h->hbuf, R, F, moe::kTileN[i]);
+    ok = ok && encode_2d(&h->map_h[i], h->hbuf, RH, F, moe::kTileN[i]);
   }
   ok = ok && cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {
@@ -488,6 +533,121 @@ int moe_init_fp8(const moe_config* cfg, const moe_weights_fp8* w, moe_handle** o
   if (w == nullptr || w->s_gate_up == nullptr || w->s_down == nullptr) return MOE_ERR_INVALID_ARG;
   const moe_weights ww{w->w_router, w->w_gate_up, w->w_down};
   return init_any(cfg, &ww, w->s_gate_up, w->s_down, out);
+}
+
+int moe_ep_init(const moe_ep_config* cfg, const moe_ep_weights* w, moe_handle** out) {
+  if (out != nullptr) *out = nullptr;
+  if (cfg == nullptr || w == nullptr || cfg->ep_size < 1) return MOE_ERR_INVALID_ARG;
+  const moe_weights ww{w->w_router, w->w_gate_up, w->w_down};
+  EpParams ep;
+  ep.size = cfg->ep_size;
+  ep.rank = cfg->ep_rank;
+  ep.max_recv = cfg->max_recv_rows;
+  return init_any(&cfg->layer, &ww, nullptr, nullptr, out, ep);
+}
+
+int moe_ep_dispatch(moe_handle* h, const void* x, int T, void* send_rows, float* send_w, int* send_counts,
+                    int* rows_per_rank, void* stream) {
+  int rc = check_call(h, x, T);
+  if (rc != MOE_OK) return rc;
+  if (h->ep_size == 0 || rows_per_rank == nullptr || send_counts == nullptr) return MOE_ERR_INVALID_ARG;
+  const moe_config& c = h->cfg;
+  const int k = c.top_k, E = c.n_experts;
+  if (T > 0 && (send_rows == nullptr || send_w == nullptr || !aligned(send_rows, 16) || !aligned(send_w, 4) ||
+                !is_device_ptr(x) || !is_device_ptr(send_rows) || !is_device_ptr(send_w)))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(send_counts, 4) || !is_device_ptr(send_counts)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  h->ep_T = T;
+  rc = enqueue_router(h, x, T, CallOpts{k, 0}, h->idx, h->prob, nullptr, nullptr, 0, s);
+  if (rc != MOE_OK) return rc;
+  MOE_CUDA(cudaMemcpyAsync(send_counts, h->counts, sizeof(int) * E, cudaMemcpyDeviceToDevice, s));
+  for (int q = 0; q < h->ep_size; ++q) rows_per_rank[q] = 0;
+  if (T == 0) return cudaStreamSynchronize(s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  MOE_CUDA(moe::launch_dispatch(h->idx, h->counts, T, E, k, c.has_shared, h->offsets, h->perm, h->inv,
+                                h->chunk_base, s));
+  // every row in dispatch order (the shared expert's rows stay here for
+  // moe_ep_combine); the routed rows, expert-major, go out rank by rank
+  MOE_CUDA(moe::launch_gather(static_cast<const bf16*>(x), h->perm, T, k, c.d_model, c.has_shared, h->yp, false, s));
+  const size_t Tk = static_cast<size_t>(T) * k;
+  MOE_CUDA(cudaMemcpyAsync(send_rows, h->yp, Tk * c.d_model * 2, cudaMemcpyDeviceToDevice, s));
+  MOE_CUDA(moe::launch_gather_weights(h->perm, h->prob, static_cast<int>(Tk), send_w, s));
+  std::vector<int> off(E + 2);
+  MOE_CUDA(cudaMemcpyAsync(off.data(), h->offsets, sizeof(int) * (E + 2), cudaMemcpyDeviceToHost, s));
+  MOE_CUDA(cudaStreamSynchronize(s));
+  for (int q = 0; q < h->ep_size; ++q) rows_per_rank[q] = off[(q + 1) * h->e_loc] - off[q * h->e_loc];
+  return MOE_OK;
+}
+
+int moe_ep_experts(moe_handle* h, const void* recv_rows, const int* recv_counts, const float* recv_w, int n_recv,
+                   void* out_rows, void* out_exp, int* chunks_per_source, void* stream) {
+  if (!valid_handle(h) || h->ep_size == 0 || recv_counts == nullptr || chunks_per_source == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (n_recv < 0) return MOE_ERR_INVALID_ARG;
+  if (n_recv > h->max_recv) return MOE_ERR_TOO_MANY_TOKENS;
+  if (!aligned(recv_counts, 4) || !is_device_ptr(recv_counts)) return MOE_ERR_INVALID_ARG;
+  if (n_recv > 0 && (recv_rows == nullptr || recv_w == nullptr || out_rows == nullptr || out_exp == nullptr ||
+                     !aligned(recv_rows, 16) || !aligned(recv_w, 4) || !aligned(out_rows, 16) ||
+                     !aligned(out_exp, 16) || !is_device_ptr(recv_rows) || !is_device_ptr(recv_w) ||
+                     !is_device_ptr(out_rows) || !is_device_ptr(out_exp)))
+    return MOE_ERR_INVALID_ARG;
+  const moe_config& c = h->cfg;
+  const int S = h->ep_size, El = h->e_loc, G = S * El;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MOE_CUDA(moe::launch_ep_groups(recv_counts, S, El, h->ep_offsets, h->ep_chunk_base, h->ep_chunks_src, s));
+  std::vector<int> chunks(S);
+  int total = 0;
+  MOE_CUDA(cudaMemcpyAsync(&total, h->ep_offsets + G, sizeof(int), cudaMemcpyDeviceToHost, s));
+  MOE_CUDA(cudaMemcpyAsync(chunks.data(), h->ep_chunks_src, sizeof(int) * S, cudaMemcpyDeviceToHost, s));
+  MOE_CUDA(cudaStreamSynchronize(s));
+  if (total != n_recv) return MOE_ERR_INVALID_ARG;  // the counts must describe exactly the rows given
+  for (int q = 0; q < S; ++q) chunks_per_source[q] = chunks[q];
+  if (n_recv == 0) return MOE_OK;
+  CUtensorMap maps[moe::kNumTileN];
+  for (int i = 0; i < moe::kNumTileN; ++i)
+    if (!encode_2d(&maps[i], recv_rows, static_cast<uint64_t>(n_recv), static_cast<uint64_t>(c.d_model),
+                   moe::kTileN[i]))
+      return MOE_ERR_CUDA;
+  // groups = (source, local expert), source-major; every row carries its own
+  // gate weight (perm = identity, prob = recv_w)
+  moe::GemmArgs a{};
+  a.offsets = h->ep_offsets;
+  a.G = G;
+  a.perm = h->ep_iota;
+  a.prob = recv_w;
+  a.Tk = n_recv;
+  a.chunk_base = h->ep_chunk_base;
+  a.w_group_mod = El;
+  return enqueue_ffn(h, a, static_cast<double>(n_recv) / G, maps, out_rows, static_cast<int8_t*>(out_exp), nullptr,
+                     s);
+}
+
+int moe_ep_combine(moe_handle* h, const void* ret_rows, const void* ret_exp, void* y, void* stream) {
+  if (!valid_handle(h) || h->ep_size == 0) return MOE_ERR_INVALID_ARG;
+  const moe_config& c = h->cfg;
+  const int T = h->ep_T, k = c.top_k;
+  if (T == 0) return MOE_OK;
+  if (y == nullptr || !aligned(y, 16) || !is_device_ptr(y)) return MOE_ERR_INVALID_ARG;
+  if (ret_rows == nullptr || ret_exp == nullptr || !aligned(ret_rows, 16) || !aligned(ret_exp, 8) ||
+      !is_device_ptr(ret_rows) || !is_device_ptr(ret_exp))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (c.has_shared) {
+    // the shared expert on this rank's own tokens: one group, rows [T*k, T*k + T)
+    moe::GemmArgs a{};
+    a.offsets = h->offsets + c.n_experts;
+    a.G = 1;
+    a.perm = h->perm;
+    a.prob = h->prob;
+    a.Tk = T * k;
+    a.chunk_base = h->chunk_base + c.n_experts;
+    a.w_group_base = h->e_loc;
+    if (int rc = enqueue_ffn(h, a, static_cast<double>(T), h->map_xp, h->yp, h->yexp, nullptr, s)) return rc;
+  }
+  MOE_CUDA(moe::launch_combine(static_cast<const __half*>(h->yp), h->yexp, static_cast<const __half*>(ret_rows),
+                               static_cast<const int8_t*>(ret_exp), h->idx, h->inv, h->offsets, h->chunk_base, T, k,
+                               c.n_experts, c.d_model, c.has_shared, y, c.out_fp32, s));
+  return MOE_OK;
 }
 
 int moe_quantize_fp8(const void* w, long long rows, int cols, void* q, float* s, void* stream) {
@@ -524,6 +684,7 @@ int moe_route(moe_handle* h, const void* x, int T, int* idx, float* prob, int* p
 int moe_forward_ex(moe_handle* h, const void* x, int T, const moe_call_options* opt, void* y, void* stream) {
   int rc = check_call(h, x, T);
   if (rc != MOE_OK) return rc;
+  if (h->ep_size != 0) return MOE_ERR_INVALID_ARG;  // an expert-parallel handle holds only its experts
   CallOpts o;
   if ((rc = resolve_opts(h, opt, &o)) != MOE_OK) return rc;
   h->last_kernels = 0;
@@ -560,7 +721,7 @@ int moe_route_stats(moe_handle* h, const void* x, int T, int n_groups, int* coun
 }
 
 int moe_forward_host(moe_handle* h, const void* x_host, int T, void* y_host, void* stream) {
-  if (!valid_handle(h)) return MOE_ERR_INVALID_ARG;
+  if (!valid_handle(h) || h->ep_size != 0) return MOE_ERR_INVALID_ARG;
   if (T < 0) return MOE_ERR_INVALID_ARG;
   if (T > h->cfg.max_tokens) return MOE_ERR_TOO_MANY_TOKENS;
   if (T == 0) return MOE_OK;

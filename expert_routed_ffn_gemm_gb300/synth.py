@@ -76,7 +76,7 @@ def _normal_bf16(gen, shape, std, device, chunk_rows=None):
     dim 0 when ``chunk_rows`` is set (bounds the fp32 temporary)."""
     out = torch.empty(shape, dtype=torch.bfloat16, device=device)
     n0 = shape[0]
-    step = n0 if not chunk_rows else chunk_rows
+    step = max(1, n0 if not chunk_rows else chunk_rows)
     for s in range(0, n0, step):
         e = min(n0, s + step)
         tmp = torch.randn((e - s,) + tuple(shape[1:]), generator=gen, device=device,

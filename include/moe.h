@@ -115,6 +115,81 @@ typedef struct moe_weights_fp8 {
 int moe_init_fp8(const moe_config* cfg, const moe_weights_fp8* w, moe_handle** out);
 
 /*
+ * Expert parallelism (page 2 §3.2.3 and §8.1: EP = 8, the 288 routed experts
+ * spread as 36 per GPU).  Rank r of ep_size owns the routed experts
+ * [r * E_loc, (r + 1) * E_loc), E_loc = n_experts / ep_size, and the shared
+ * expert.  One layer call on a rank is three library phases around two
+ * exchanges that the caller performs (any all-to-all, e.g. NCCL):
+ *   1. moe_ep_dispatch: route this rank's T tokens over all E experts and
+ *      lay the routed rows out expert by expert (rank q's rows are one block);
+ *   -> exchange the counts and the rows (+ their gate weights) to the owners;
+ *   2. moe_ep_experts: run the local experts over the rows received from
+ *      every source (blocks in source order, inside a block expert by expert);
+ *   -> exchange the output rows and their exponent chunks back, per source;
+ *   3. moe_ep_combine: this rank's shared expert and the fixed-order combine.
+ * The rows a rank gets back, concatenated in rank order, line up with its own
+ * dispatch order, and so do their exponent chunks (a (source, expert) block is
+ * cut into 16-row chunks exactly as the source cuts that expert's rows).
+ * Not part of the pages' text: the phase split is this library's; bf16 weights
+ * only.
+ */
+typedef struct moe_ep_config {
+  moe_config layer;   /* the whole layer (n_experts = all routed experts), this rank's max_tokens */
+  int ep_size;        /* ranks, >= 1, divides n_experts                                    */
+  int ep_rank;        /* this rank, 0 <= ep_rank < ep_size                                 */
+  int max_recv_rows;  /* most routed rows moe_ep_experts may be given in one call          */
+} moe_ep_config;
+
+/* w_router fp32 [E][d] (all experts); w_gate_up bf16 [E_loc + has_shared][2F][d]
+ * and w_down bf16 [E_loc + has_shared][d][F]: this rank's experts in order, then
+ * the shared expert.  Device pointers, borrowed until moe_free. */
+typedef struct moe_ep_weights {
+  const float* w_router;
+  const void* w_gate_up;
+  const void* w_down;
+} moe_ep_weights;
+
+/* A handle for phases 1-3 (moe_route also works; moe_forward and
+ * moe_forward_host return MOE_ERR_INVALID_ARG on it).  Same errors as
+ * moe_init, plus MOE_ERR_UNSUPPORTED when ep_size does not divide n_experts. */
+int moe_ep_init(const moe_ep_config* cfg, const moe_ep_weights* w, moe_handle** out);
+
+/*
+ * Phase 1.  x bf16 [T][d] (device, T <= max_tokens).  Writes (device, caller-
+ * owned): send_rows bf16 [T*k][d] (the routed rows in dispatch order: rank 0's
+ * block, then rank 1's, ...), send_w fp32 [T*k] (each row's gate weight),
+ * send_counts int [E] (rows per expert; rank q's part is [q*E_loc, (q+1)*E_loc)),
+ * and rows_per_rank (HOST int [ep_size]).  Synchronises `stream` (the exchange
+ * sizes are needed on the host).  Keeps this call's routing for phase 3.
+ */
+int moe_ep_dispatch(moe_handle* h, const void* x, int T, void* send_rows, float* send_w, int* send_counts,
+                    int* rows_per_rank, void* stream);
+
+/*
+ * Phase 2.  recv_rows bf16 [n_recv][d], recv_w fp32 [n_recv], recv_counts int
+ * [ep_size][E_loc] (device): what every source sent, in source order.
+ * n_recv <= max_recv_rows and must equal the sum of recv_counts
+ * (MOE_ERR_INVALID_ARG otherwise).  Writes out_rows fp16 [n_recv][d] and
+ * out_exp int8 [chunks][d] (device, caller-owned; chunks <= n_recv/16 +
+ * ep_size*E_loc), the outputs w * FFN(row) in the library's scaled fp16
+ * (value = out_rows * 2^out_exp, one exponent per feature and 16-row chunk),
+ * and chunks_per_source (HOST int [ep_size]): the exponent chunks of each
+ * source's block, which follow one another in source order.  Synchronises
+ * `stream` before the GEMMs (to check the counts).
+ */
+int moe_ep_experts(moe_handle* h, const void* recv_rows, const int* recv_counts, const float* recv_w, int n_recv,
+                   void* out_rows, void* out_exp, int* chunks_per_source, void* stream);
+
+/*
+ * Phase 3.  ret_rows fp16 [T*k][d] and ret_exp int8 [chunks][d] (device): the
+ * rows and exponent chunks the owners sent back, concatenated in rank order.
+ * Runs the shared expert on this rank's tokens of the last moe_ep_dispatch and
+ * writes y [T][d] (bf16, or fp32 with out_fp32) with the same fixed-order
+ * combine as moe_forward.  Asynchronous.
+ */
+int moe_ep_combine(moe_handle* h, const void* ret_rows, const void* ret_exp, void* y, void* stream);
+
+/*
  * Per-row E4M3 quantisation of a bf16 matrix w [rows][cols] (device):
  *   s[r] = max_i |w[r][i]| / 448 (fp32),   q[r][i] = E4M3 nearest to w[r][i] / s[r]
  * (fp32 quotient, ties to even, magnitudes above 448 saturated); a row of

@@ -1,0 +1,108 @@
+"""Expert parallelism on one GPU: ranks simulated as threads of one process,
+each with its own library handle holding only its experts, exchanging rows
+through ``LocalExchange`` (no collective, no kernels waiting on each other).
+
+Each rank's output must equal the whole-layer call on the same tokens bit for
+bit (routing, rows and their grouping into 16-row exponent chunks are the
+same), and the oracle within the parity bound (see moe_check.py)."""
+import threading
+
+import numpy as np
+import pytest
+import torch
+
+from expert_routed_ffn_gemm_gb300 import binding, ep, synth
+
+from moe_check import check_output, cpu, host_bits, to_dev
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+def local_weights(inp, r, ep_size):
+    E = inp.shape.E
+    e_loc = E // ep_size
+    sl = slice(r * e_loc, (r + 1) * e_loc)
+    gu = torch.cat([inp.w_gate_up[sl], inp.w_gate_up[E:E + 1]]).contiguous().to(DEV)
+    dn = torch.cat([inp.w_down[sl], inp.w_down[E:E + 1]]).contiguous().to(DEV)
+    return gu, dn
+
+
+def run_ranks(inp, xs, ep_size, max_recv):
+    wr = inp.w_router.to(DEV)
+    backends = []
+    for r in range(ep_size):
+        gu, dn = local_weights(inp, r, ep_size)
+        backends.append(ep.GpuEpBackend(wr, gu, dn, inp.shape.k, max(1, max(x.shape[0] for x in xs)), ep_size, r,
+                                        max_recv))
+    ex = ep.LocalExchange(ep_size)
+    ys, errs = [None] * ep_size, []
+
+    def work(r):
+        try:
+            ys[r] = ep.ep_forward(backends[r], xs[r], ex.for_rank(r))
+            torch.cuda.synchronize()
+        except Exception as e:  # noqa: BLE001 - reported below
+            errs.append(e)
+            ex.barrier.abort()
+
+    threads = [threading.Thread(target=work, args=(r,)) for r in range(ep_size)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=300)
+    if errs:
+        raise errs[0]
+    for b in backends:
+        assert binding.moe_check(b.handle) == binding.MOE_OK
+        b.close()
+    return ys
+
+
+@pytest.mark.parametrize("ep_size,Ts", [(1, [96]), (2, [70, 130]), (4, [40, 0, 65, 17])])
+def test_expert_parallel_matches_whole_layer(ep_size, Ts):
+    shape = synth.LayerShape(T=max(Ts), d=256, E=16, k=2, F=128)
+    inp = synth.make_inputs(shape, seed=60 + ep_size)
+    xs = [synth.make_tokens(shape.with_tokens(T), seed=70 + r, device=DEV) for r, T in enumerate(Ts)]
+    ys = run_ranks(inp, xs, ep_size, max_recv=sum(Ts) * shape.k)
+    _, wr, wgu, wd = to_dev(inp, DEV)
+    whole = binding.MoeLayer(wr, wgu, wd, shape.k, max(Ts))
+    _, wr_h, wgu_h, wd_h = host_bits(inp)
+    for r, (x, y) in enumerate(zip(xs, ys)):
+        if x.shape[0] == 0:
+            continue
+        y_ref = whole.forward(x)
+        assert torch.equal(y, y_ref), f"rank {r}: EP output differs from the whole-layer call"
+        idx, _, _, _, _ = whole.route(x)
+        check_output(synth.bf16_bits(x), wr_h, wgu_h, wd_h, shape.k, cpu(y.float()), cpu(idx))
+    whole.close()
+
+
+def test_expert_parallel_flash_shape():
+    # d=4096, 288 routed experts over 8 ranks (36 each, the pages' EP = 8), top-8
+    shape = synth.FLASH_DECODE.with_tokens(16)
+    inp = synth.make_inputs(shape, seed=80, device=DEV)
+    Ts = [16, 9, 0, 16, 3, 16, 12, 1]
+    xs = [synth.make_tokens(shape.with_tokens(T), seed=90 + r, device=DEV) for r, T in enumerate(Ts)]
+    ys = run_ranks(inp, xs, 8, max_recv=sum(Ts) * shape.k)
+    whole = binding.MoeLayer(inp.w_router, inp.w_gate_up, inp.w_down, shape.k, 16)
+    for x, y in zip(xs, ys):
+        if x.shape[0]:
+            assert torch.equal(y, whole.forward(x))
+    whole.close()
+
+
+def test_expert_parallel_rejects_bad_counts():
+    shape = synth.LayerShape(T=8, d=256, E=8, k=2, F=128)
+    inp = synth.make_inputs(shape, seed=61)
+    gu, dn = local_weights(inp, 0, 2)
+    b = ep.GpuEpBackend(inp.w_router.to(DEV), gu, dn, 2, 8, 2, 0, 64)
+    rows = torch.zeros((10, 256), dtype=torch.bfloat16, device=DEV)
+    counts = torch.tensor([3, 3, 3, 3, 0, 0, 0, 0], dtype=torch.int32, device=DEV)  # sums to 12, not 10
+    w = torch.ones((10,), dtype=torch.float32, device=DEV)
+    with pytest.raises(binding.MoeError) as e:
+        b.experts(rows, counts, w)
+    assert e.value.status == binding.MOE_ERR_INVALID_ARG
+    with pytest.raises(binding.MoeError):  # whole-layer calls are not for an EP handle
+        binding.moe_forward(b.handle, rows[:4], 4, torch.empty_like(rows[:4]))
+    b.close()
