@@ -64,7 +64,7 @@ struct Cfg {
 template <bool GATEUP, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_act,
-                       const GemmArgs args) {
+                       const __grid_constant__ CUtensorMap map_act2, const GemmArgs args) {
   using C = Cfg<GATEUP, BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
     tma_prefetch_desc(&map_w);
     tma_prefetch_desc(&map_act);
+    if (args.act2_from >= 0) tma_prefetch_desc(&map_act2);
   }
   if (warp == 1) {
     tmem_alloc(tmem_holder, C::TMEM_COLS);
@@ -138,7 +139,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
           tma_load_2d(st, &map_w, &full[stage], kb * kBlockK, row_w, pol_w);
           if (GATEUP) tma_load_2d(st + C::A_BYTES / 2, &map_w, &full[stage], kb * kBlockK, row_w + args.F, pol_w);
-          tma_load_2d(st + C::A_BYTES, &map_act, &full[stage], kb * kBlockK, row_act, pol_act);
+          if (args.act2_from >= 0 && row_act >= args.act2_from)
+            tma_load_2d(st + C::A_BYTES, &map_act2, &full[stage], kb * kBlockK, row_act - args.act2_from, pol_act);
+          else
+            tma_load_2d(st + C::A_BYTES, &map_act, &full[stage], kb * kBlockK, row_act, pol_act);
           ++issued;
           if (++stage == C::STAGES) {
             stage = 0;
@@ -253,9 +257,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <bool GATEUP, int BN>
-cudaError_t launch_one(const CUtensorMap* map_w, const CUtensorMap* map_act, const GemmArgs& a, int num_sms,
-                       cudaStream_t stream) {
-  expert_gemm_kernel<GATEUP, BN><<<num_sms, kThreads, Cfg<GATEUP, BN>::SMEM_BYTES, stream>>>(*map_w, *map_act, a);
+cudaError_t launch_one(const CUtensorMap* map_w, const CUtensorMap* map_act, const CUtensorMap* map_act2,
+                       const GemmArgs& a, int num_sms, cudaStream_t stream) {
+  expert_gemm_kernel<GATEUP, BN><<<num_sms, kThreads, Cfg<GATEUP, BN>::SMEM_BYTES, stream>>>(*map_w, *map_act,
+                                                                                          *map_act2, a);
   return cudaGetLastError();
 }
 
@@ -276,14 +281,14 @@ cudaError_t prepare_all() {
 }
 
 template <bool GATEUP>
-cudaError_t dispatch_bn(int tile_n, const CUtensorMap* map_w, const CUtensorMap* map_act, const GemmArgs& a,
-                        int num_sms, cudaStream_t stream) {
+cudaError_t dispatch_bn(int tile_n, const CUtensorMap* map_w, const CUtensorMap* map_act, const CUtensorMap* map_act2,
+                        const GemmArgs& a, int num_sms, cudaStream_t stream) {
   switch (tile_n) {
-    case 16: return launch_one<GATEUP, 16>(map_w, map_act, a, num_sms, stream);
-    case 32: return launch_one<GATEUP, 32>(map_w, map_act, a, num_sms, stream);
-    case 64: return launch_one<GATEUP, 64>(map_w, map_act, a, num_sms, stream);
-    case 128: return launch_one<GATEUP, 128>(map_w, map_act, a, num_sms, stream);
-    case 256: return launch_one<GATEUP, 256>(map_w, map_act, a, num_sms, stream);
+    case 16: return launch_one<GATEUP, 16>(map_w, map_act, map_act2, a, num_sms, stream);
+    case 32: return launch_one<GATEUP, 32>(map_w, map_act, map_act2, a, num_sms, stream);
+    case 64: return launch_one<GATEUP, 64>(map_w, map_act, map_act2, a, num_sms, stream);
+    case 128: return launch_one<GATEUP, 128>(map_w, map_act, map_act2, a, num_sms, stream);
+    case 256: return launch_one<GATEUP, 256>(map_w, map_act, map_act2, a, num_sms, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -301,9 +306,10 @@ __global__ void wait_selftest_kernel(uint32_t* err, unsigned long long limit_ns)
 }  // namespace
 
 cudaError_t launch_expert_gemm(bool gateup, int tile_n, const CUtensorMap* map_w, const CUtensorMap* map_act,
-                               const GemmArgs& a, int num_sms, cudaStream_t stream) {
-  return gateup ? dispatch_bn<true>(tile_n, map_w, map_act, a, num_sms, stream)
-                : dispatch_bn<false>(tile_n, map_w, map_act, a, num_sms, stream);
+                               const CUtensorMap* map_act2, const GemmArgs& a, int num_sms, cudaStream_t stream) {
+  if (map_act2 == nullptr) map_act2 = map_act;
+  return gateup ? dispatch_bn<true>(tile_n, map_w, map_act, map_act2, a, num_sms, stream)
+                : dispatch_bn<false>(tile_n, map_w, map_act, map_act2, a, num_sms, stream);
 }
 
 cudaError_t expert_gemm_prepare() {

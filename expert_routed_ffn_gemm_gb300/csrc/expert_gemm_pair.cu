@@ -76,7 +76,7 @@ __device__ __forceinline__ bool wait_cluster(uint64_t* bar, uint32_t parity, uin
 template <bool GATEUP>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     expert_gemm_pair_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_act,
-                            const GemmArgs args) {
+                            const __grid_constant__ CUtensorMap map_act2, const GemmArgs args) {
   using C = PairCfg<GATEUP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -112,6 +112,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fence_barrier_init();
     tma_prefetch_desc(&map_w);
     tma_prefetch_desc(&map_act);
+    if (args.act2_from >= 0) tma_prefetch_desc(&map_act2);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_holder, C::TMEM_COLS);
@@ -157,7 +158,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
           tma_load_2d_pair(st, &map_w, fb, kb * kBlockK, row_w, pol_w);
           if (GATEUP) tma_load_2d_pair(st + C::A_BYTES / 2, &map_w, fb, kb * kBlockK, row_w + args.F, pol_w);
-          tma_load_2d_pair(st + C::A_BYTES, &map_act, fb, kb * kBlockK, row_act, pol_act);
+          if (args.act2_from >= 0 && row_act >= args.act2_from)
+            tma_load_2d_pair(st + C::A_BYTES, &map_act2, fb, kb * kBlockK, row_act - args.act2_from, pol_act);
+          else
+            tma_load_2d_pair(st + C::A_BYTES, &map_act, fb, kb * kBlockK, row_act, pol_act);
           ++issued;
           if (++stage == C::STAGES) {
             stage = 0;
@@ -300,12 +304,16 @@ cudaError_t expert_gemm_pair_prepare() {
 }
 
 cudaError_t launch_expert_gemm_pair(bool gateup, const CUtensorMap* map_w, const CUtensorMap* map_act,
-                                    const GemmArgs& a, int num_sms, cudaStream_t stream) {
+                                    const CUtensorMap* map_act2, const GemmArgs& a, int num_sms,
+                                    cudaStream_t stream) {
+  if (map_act2 == nullptr) map_act2 = map_act;
   const int grid = num_sms & ~1;
   if (gateup)
-    expert_gemm_pair_kernel<true><<<grid, kThreads, PairCfg<true>::SMEM_BYTES, stream>>>(*map_w, *map_act, a);
+    expert_gemm_pair_kernel<true><<<grid, kThreads, PairCfg<true>::SMEM_BYTES, stream>>>(
+        *map_w, *map_act, *map_act2, a);
   else
-    expert_gemm_pair_kernel<false><<<grid, kThreads, PairCfg<false>::SMEM_BYTES, stream>>>(*map_w, *map_act, a);
+    expert_gemm_pair_kernel<false><<<grid, kThreads, PairCfg<false>::SMEM_BYTES, stream>>>(
+        *map_w, *map_act, *map_act2, a);
   return cudaGetLastError();
 }
 

@@ -85,6 +85,8 @@ struct GemmArgs {
   int reverse;         // 1: work items in reverse order (last group first)
   int w_group_base;    // weights of group g: w_group_base + (w_group_mod ? g % w_group_mod : g)
   int w_group_mod;
+  int act2_from;       // bf16 kernels: token rows from this dispatch position on come through
+                       // map_act2 at row (position - act2_from); -1: all through map_act
 };
 
 // K3/K4: tcgen05 grouped GEMMs over the groups' row blocks.  `tile_n` must be
@@ -92,7 +94,7 @@ struct GemmArgs {
 // rows, m_tiles = F/64); false: Yp = w * (H Wd^T) (map_w box: 128 rows,
 // m_tiles = d/128).  map_act: the token rows (X or H), box tile_n rows.
 cudaError_t launch_expert_gemm(bool gateup, int tile_n, const CUtensorMap* map_w, const CUtensorMap* map_act,
-                               const GemmArgs& a, int num_sms, cudaStream_t stream);
+                               const CUtensorMap* map_act2, const GemmArgs& a, int num_sms, cudaStream_t stream);
 // Opts every grouped-GEMM instantiation into its dynamic shared memory size
 // on the current device (once per device, before the first launch).
 cudaError_t expert_gemm_prepare();
@@ -101,7 +103,8 @@ cudaError_t expert_gemm_prepare();
 // number of SMs).  a.m_tiles must count pair tiles: F/128 (gate/up, map_w box
 // 64 rows) or d/256 (down, map_w box 128 rows); map_act box: 128 rows.
 cudaError_t launch_expert_gemm_pair(bool gateup, const CUtensorMap* map_w, const CUtensorMap* map_act,
-                                    const GemmArgs& a, int num_sms, cudaStream_t stream);
+                                    const CUtensorMap* map_act2, const GemmArgs& a, int num_sms,
+                                    cudaStream_t stream);
 cudaError_t expert_gemm_pair_prepare();
 
 // K3/K4 with E4M3 weights (one fp32 scale per weight row in a.w_scale) and

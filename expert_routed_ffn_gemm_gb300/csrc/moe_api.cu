@@ -260,7 +260,7 @@ cudaEvent_t* prof_slot(moe_handle* h) {
 // and yexp.  mean_rows: mean rows per group (picks the token tile width).
 // ev (or NULL): profiling events 3..5 around the two GEMMs.
 int enqueue_ffn(moe_handle* h, moe::GemmArgs a, double mean_rows, const CUtensorMap* map_rows, void* yout,
-                int8_t* yexp, cudaEvent_t* ev, cudaStream_t s) {
+                int8_t* yexp, cudaEvent_t* ev, cudaStream_t s, const void* rows2 = nullptr, int n_rows2 = 0) {
   const moe_config& c = h->cfg;
   const int cap = h->fp8 ? 128 : 256;
   const int bn1 = h->tile_gateup ? std::min(h->tile_gateup, cap) : choose_tile(mean_rows, cap);
@@ -269,6 +269,17 @@ int enqueue_ffn(moe_handle* h, moe::GemmArgs a, double mean_rows, const CUtensor
   const int i128 = tile_index(128);
   const bool pair1 = h->use_pairs && bn1 == 256;
   const bool pair2 = h->use_pairs && bn2 == 256 && c.d_model % 256 == 0;
+  // gate/up rows from a.act2_from on come from rows2 [n_rows2][d] (bf16 only)
+  CUtensorMap map2;
+  const CUtensorMap* map_act2 = nullptr;
+  if (a.act2_from >= 0 && rows2 != nullptr && !h->fp8) {
+    if (!encode_2d(&map2, rows2, static_cast<uint64_t>(n_rows2), static_cast<uint64_t>(c.d_model),
+                   pair1 ? 128u : static_cast<uint32_t>(bn1)))
+      return MOE_ERR_CUDA;
+    map_act2 = &map2;
+  } else {
+    a.act2_from = -1;
+  }
   a.err = h->err;
   a.wait_limit_ns = h->wait_limit_ns;
   a.F = c.ffn_width;
@@ -287,12 +298,13 @@ int enqueue_ffn(moe_handle* h, moe::GemmArgs a, double mean_rows, const CUtensor
   if (h->fp8)
     MOE_CUDA(moe::launch_expert_gemm_fp8(true, bn1, &h->map_wgu, &map_rows[i1], a, h->num_sms, s));
   else if (pair1)
-    MOE_CUDA(moe::launch_expert_gemm_pair(true, &h->map_wgu, &map_rows[i128], a, h->num_sms, s));
+    MOE_CUDA(moe::launch_expert_gemm_pair(true, &h->map_wgu, &map_rows[i128], map_act2, a, h->num_sms, s));
   else
-    MOE_CUDA(moe::launch_expert_gemm(true, bn1, &h->map_wgu, &map_rows[i1], a, h->num_sms, s));
+    MOE_CUDA(moe::launch_expert_gemm(true, bn1, &h->map_wgu, &map_rows[i1], map_act2, a, h->num_sms, s));
   MOE_MARK(4);
 
   a.reverse = 0;
+  a.act2_from = -1;
   a.out = yout;
   a.out_exp = yexp;
   a.K = c.ffn_width;
@@ -303,9 +315,9 @@ int enqueue_ffn(moe_handle* h, moe::GemmArgs a, double mean_rows, const CUtensor
   if (h->fp8)
     MOE_CUDA(moe::launch_expert_gemm_fp8(false, bn2, &h->map_wd, &h->map_h[i2], a, h->num_sms, s));
   else if (pair2)
-    MOE_CUDA(moe::launch_expert_gemm_pair(false, &h->map_wd, &h->map_h[i128], a, h->num_sms, s));
+    MOE_CUDA(moe::launch_expert_gemm_pair(false, &h->map_wd, &h->map_h[i128], nullptr, a, h->num_sms, s));
   else
-    MOE_CUDA(moe::launch_expert_gemm(false, bn2, &h->map_wd, &h->map_h[i2], a, h->num_sms, s));
+    MOE_CUDA(moe::launch_expert_gemm(false, bn2, &h->map_wd, &h->map_h[i2], nullptr, a, h->num_sms, s));
   MOE_MARK(5);
   return MOE_OK;
 }
@@ -320,10 +332,13 @@ int enqueue_forward(moe_handle* h, const void* x, int T, CallOpts o, void* y, cu
   MOE_CUDA(moe::launch_dispatch(h->idx, h->counts, T, c.n_experts, o.k, c.has_shared, h->offsets, h->perm, h->inv,
                                 h->chunk_base, s));
   MOE_MARK(2);
-  // token rows in dispatch order (the yp buffer holds them until the down GEMM)
-  // (fp8 weights: as fp16, the tensor cores' input type there)
-  MOE_CUDA(moe::launch_gather(static_cast<const bf16*>(x), h->perm, T, o.k, c.d_model, c.has_shared, h->yp, h->fp8,
-                              s));
+  // token rows in dispatch order (the yp buffer holds them until the down
+  // GEMM).  bf16 weights: the routed rows only — the shared expert's rows are
+  // x itself, which its gate/up reads directly.  fp8 weights: every row, as
+  // fp16 (the tensor cores' input type there).
+  const bool shared_from_x = !h->fp8 && c.has_shared;
+  MOE_CUDA(moe::launch_gather(static_cast<const bf16*>(x), h->perm, T, o.k, c.d_model,
+                              shared_from_x ? 0 : c.has_shared, h->yp, h->fp8, s));
   MOE_MARK(3);
   moe::GemmArgs a{};
   a.offsets = h->offsets;
@@ -332,7 +347,9 @@ int enqueue_forward(moe_handle* h, const void* x, int T, CallOpts o, void* y, cu
   a.G = h->G;
   a.Tk = T * o.k;
   a.chunk_base = h->chunk_base;
-  if (int rc2 = enqueue_ffn(h, a, static_cast<double>(T) * o.k / c.n_experts, h->map_xp, h->yp, h->yexp, ev, s))
+  a.act2_from = shared_from_x ? T * o.k : -1;
+  if (int rc2 = enqueue_ffn(h, a, static_cast<double>(T) * o.k / c.n_experts, h->map_xp, h->yp, h->yexp, ev, s,
+                            x, T))
     return rc2;
   MOE_CUDA(moe::launch_combine(static_cast<const __half*>(h->yp), h->yexp, nullptr, nullptr, h->idx, h->inv,
                                h->offsets, h->chunk_base, T, o.k, c.n_experts, c.d_model, c.has_shared, y, c.out_fp32,
