@@ -49,9 +49,10 @@ def peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def workload(name: str, experts: int = 0):
-    """(shape, skew) of a named workload; `experts` > 0 replaces E (smaller
-    cases of the same kernels, e.g. for profiler captures)."""
+def workload(name: str, experts: int = 0, ffn_width: int = 0):
+    """(shape, skew) of a named workload; `experts` > 0 replaces E and
+    `ffn_width` > 0 replaces F (smaller cases of the same kernels, e.g. for
+    profiler captures of the routing, gather and combine kernels)."""
     from dataclasses import replace
 
     from expert_routed_ffn_gemm_gb300 import synth
@@ -68,6 +69,8 @@ def workload(name: str, experts: int = 0):
         raise SystemExit(f"unknown workload {name}")
     if experts > 0:
         shape = replace(shape, E=experts)
+    if ffn_width > 0:
+        shape = replace(shape, F=ffn_width)
     return shape, skew
 
 
@@ -190,7 +193,7 @@ def measured_traffic(args):
     """DRAM bytes per launch of the gate/up GEMM from the committed ncu capture
     of the decode workload (profiles/gate_up_decode_T128_dram.md); None for
     other workloads or when the summary is missing."""
-    if args.workload != "decode" or args.experts or args.weights != "bf16":
+    if args.workload != "decode" or args.experts or args.ffn_width or args.weights != "bf16":
         return None
     path = os.path.join(ROOT, "profiles", "gate_up_decode_T128_dram.md")
     try:
@@ -250,7 +253,7 @@ def run_reference(args, world, rank):
     import oracle
     from expert_routed_ffn_gemm_gb300 import synth
 
-    shape, skew = workload(args.workload, args.experts)
+    shape, skew = workload(args.workload, args.experts, args.ffn_width)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = synth.make_inputs(shape, seed=0, device=dev, skew=skew)
     xb, wr, wgu, wd = host_copy(inp)
@@ -287,7 +290,7 @@ def run_native(args, world, rank, local):
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    shape, skew = workload(args.workload, args.experts)
+    shape, skew = workload(args.workload, args.experts, args.ffn_width)
     hbm_gbs, tf_burst, tf_sust, peak_kind = peaks()
 
     inp = synth.make_inputs(shape, seed=rank, device=dev, skew=skew)
@@ -320,7 +323,11 @@ def run_native(args, world, rank, local):
         raise RuntimeError("device error during warm-up")
 
     # ---- timed region: device time, inputs resident -------------------------
-    layer.profile_enable(True)
+    # The layer's kernels overlap their launch and set-up with the end of the
+    # kernel before them (programmatic dependent launch); events recorded
+    # between kernels would serialise them, so the step time is taken without
+    # the per-stage events, and the per-stage times in a second timed pass of
+    # the same steps with them.
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
@@ -335,13 +342,25 @@ def run_native(args, world, rank, local):
     kernels_per_step = launches // max(1, args.steps)
     barrier(world)
     ms = ev0.elapsed_time(ev1)
-    stages, n_prof = layer.profile_read()
-    layer.profile_enable(False)
     ms_max = max_over_ranks(ms, world)
     if layer.check() != binding.MOE_OK:
         raise RuntimeError("device error in the timed region")
     if not torch.isfinite(y.float()).all():
         raise RuntimeError("non-finite output")
+
+    # ---- the same steps with per-stage events --------------------------------
+    layer.profile_enable(True)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for i in range(args.steps):
+        layer.forward(xs[i % N_X_BUFFERS], y)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms_staged = ev0.elapsed_time(ev1)
+    stages, n_prof = layer.profile_read()
+    layer.profile_enable(False)
+    if layer.check() != binding.MOE_OK:
+        raise RuntimeError("device error in the staged pass")
 
     # ---- end to end through the host-buffer entry point ---------------------
     x_host = [x.cpu().pin_memory() for x in xs]
@@ -404,6 +423,7 @@ def run_native(args, world, rank, local):
         "layer_roofline": {"hbm_frac": layer_hbm_frac, "tensor_frac_sustained": layer_tc_frac,
                            "bytes_per_step": layer_bytes, "flops_per_step": layer_flops(shape)},
         "stage_ms_per_step": {k: v / steps_prof for k, v in stages.items()},
+        "ms_per_step_with_stage_events": ms_staged / args.steps,
         "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": shape.T * shape.d * 2,
                 "d2h_bytes_per_step": shape.T * shape.d * 2},
         "gpu_launches": kernels_per_step * args.steps,
@@ -433,6 +453,7 @@ def main():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default="decode")
     ap.add_argument("--experts", type=int, default=0, help="override the routed expert count (smaller cases)")
+    ap.add_argument("--ffn-width", type=int, default=0, help="override the expert width F, a multiple of 128 (smaller cases)")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -9,6 +9,7 @@
 // (no order-dependent atomics), combine sums in a fixed order.
 #include <cuda_fp8.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "../../include/moe.h"
@@ -43,6 +44,43 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* 
   return base + incl - v;
 }
 
+// offsets[0..E+1] (exclusive prefix of the counts, then the shared expert's T
+// rows) and chunk_base[0..E+1] (the same over ceil(count / kYpRows)), by one
+// block whose threads each scan a contiguous run of experts.  base (shared
+// memory, or NULL) gets offsets[0..E-1] too.
+__device__ void write_offsets(const int* __restrict__ counts, int T, int E, int has_shared, int* __restrict__ offsets,
+                              int* __restrict__ chunk_base, int* warp_sums, int* base) {
+  const int per = (E + kDispatchThreads - 1) / kDispatchThreads;
+  const int b = threadIdx.x * per;
+  int local = 0;
+  for (int i = b; i < min(E, b + per); ++i) local += counts[i];
+  int total;
+  const int pre = block_exclusive_scan(local, warp_sums, &total);
+  int run = pre;
+  for (int i = b; i < min(E, b + per); ++i) {
+    if (offsets != nullptr) offsets[i] = run;
+    if (base != nullptr) base[i] = run;
+    run += counts[i];
+  }
+  if (offsets == nullptr) return;
+  if (threadIdx.x == 0) {
+    offsets[E] = total;
+    offsets[E + 1] = total + (has_shared ? T : 0);
+  }
+  local = 0;
+  for (int i = b; i < min(E, b + per); ++i) local += (counts[i] + kYpRows - 1) / kYpRows;
+  const int cpre = block_exclusive_scan(local, warp_sums, &total);
+  run = cpre;
+  for (int i = b; i < min(E, b + per); ++i) {
+    chunk_base[i] = run;
+    run += (counts[i] + kYpRows - 1) / kYpRows;
+  }
+  if (threadIdx.x == 0) {
+    chunk_base[E] = total;
+    chunk_base[E + 1] = total + (has_shared ? (T + kYpRows - 1) / kYpRows : 0);
+  }
+}
+
 // Block e < E: offset of expert e, then a stable compaction over tokens of the
 // assignments (t, j) with idx[t][j] == e.  Block 0 also writes offsets[].
 __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(const int* __restrict__ idx,
@@ -50,6 +88,8 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(const int* _
                                                                     int k, int has_shared, int* __restrict__ offsets,
                                                                     int* __restrict__ perm, int* __restrict__ inv,
                                                                     int* __restrict__ chunk_base) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ int warp_sums[kDispatchThreads / 32];
   const int e = blockIdx.x;
 
@@ -59,37 +99,7 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(const int* _
   int base_e;
   block_exclusive_scan(part, warp_sums, &base_e);
 
-  if (e == 0) {
-    // offsets[0..E]: each thread scans a contiguous run of experts
-    const int per = (E + kDispatchThreads - 1) / kDispatchThreads;
-    const int b = threadIdx.x * per;
-    int local = 0;
-    for (int i = b; i < min(E, b + per); ++i) local += counts[i];
-    int total;
-    const int pre = block_exclusive_scan(local, warp_sums, &total);
-    int run = pre;
-    for (int i = b; i < min(E, b + per); ++i) {
-      offsets[i] = run;
-      run += counts[i];
-    }
-    if (threadIdx.x == 0) {
-      offsets[E] = total;
-      offsets[E + 1] = total + (has_shared ? T : 0);
-    }
-    // chunk_base[0..E+1]: the same scan over ceil(count / kYpRows)
-    local = 0;
-    for (int i = b; i < min(E, b + per); ++i) local += (counts[i] + kYpRows - 1) / kYpRows;
-    const int cpre = block_exclusive_scan(local, warp_sums, &total);
-    run = cpre;
-    for (int i = b; i < min(E, b + per); ++i) {
-      chunk_base[i] = run;
-      run += (counts[i] + kYpRows - 1) / kYpRows;
-    }
-    if (threadIdx.x == 0) {
-      chunk_base[E] = total;
-      chunk_base[E + 1] = total + (has_shared ? (T + kYpRows - 1) / kYpRows : 0);
-    }
-  }
+  if (e == 0) write_offsets(counts, T, E, has_shared, offsets, chunk_base, warp_sums, nullptr);
 
   int running = 0;
   for (int t0 = 0; t0 < T; t0 += kDispatchThreads) {
@@ -112,29 +122,156 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(const int* _
   }
 }
 
-// One warp per dispatch row: xp[pos] = x[token(pos)], 16-byte vectors; with
-// to_f16 each bf16 value is rewritten as the nearest fp16.
+// Many tokens: the tokens are cut into chunks of kChunkTokens (8 warps x 32
+// lanes, lane l of warp w = token chunk*256 + 32w + l).  A chunk's lane masks
+// mask[w][e] (bit l: that token chose expert e; a token chooses an expert at
+// most once) give every row's rank among the chunk's rows of its expert in
+// token order; hist/scan turn the chunks' counts into each chunk's first row
+// per expert.  Three passes, no atomics outside shared memory, and the same
+// stable token order as dispatch_kernel.
+constexpr int kChunkTokens = kDispatchThreads;
+constexpr int kChunkWarps = kChunkTokens / 32;
+
+__device__ __forceinline__ void chunk_masks(const int* __restrict__ idx, int T, int E, int k, uint32_t* mask) {
+  for (int i = threadIdx.x; i < kChunkWarps * E; i += kChunkTokens) mask[i] = 0u;
+  __syncthreads();
+  const int t = blockIdx.x * kChunkTokens + threadIdx.x;
+  if (t < T) {
+    uint32_t* wm = mask + (threadIdx.x >> 5) * E;
+    const uint32_t bit = 1u << (threadIdx.x & 31);
+    const int* row = idx + static_cast<size_t>(t) * k;
+    for (int j = 0; j < k; ++j) {
+      const int e = __ldg(row + j);
+      if (e >= 0 && e < E) atomicOr(wm + e, bit);
+    }
+  }
+  __syncthreads();
+}
+
+// Pass 1: hist[chunk][e] = rows of expert e among the chunk's tokens.
+__global__ void __launch_bounds__(kChunkTokens) chunk_hist_kernel(const int* __restrict__ idx, int T, int E, int k,
+                                                                  int* __restrict__ hist) {
+  pdl_trigger();
+  pdl_wait();
+  extern __shared__ uint32_t mask[];
+  chunk_masks(idx, T, E, k, mask);
+  for (int e = threadIdx.x; e < E; e += kChunkTokens) {
+    int n = 0;
+#pragma unroll
+    for (int w = 0; w < kChunkWarps; ++w) n += __popc(mask[w * E + e]);
+    hist[static_cast<size_t>(blockIdx.x) * E + e] = n;
+  }
+}
+
+// Pass 2: hist[c][e] becomes the exclusive prefix over chunks c' < c, and
+// counts[e] the total.  Block = 32 experts x kScanParts runs of chunks; each
+// thread sums its run, the runs' sums are scanned in shared memory, then each
+// thread writes its run's prefixes.
+constexpr int kScanParts = 8;
+__global__ void __launch_bounds__(32 * kScanParts) chunk_scan_kernel(int* __restrict__ hist, int n_chunks, int E,
+                                                                     int* __restrict__ counts) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ int part_sum[kScanParts][32];
+  const int ex = threadIdx.x & 31, part = threadIdx.x >> 5;
+  const int e = blockIdx.x * 32 + ex;
+  const int per = (n_chunks + kScanParts - 1) / kScanParts;
+  const int c0 = part * per, c1 = min(n_chunks, c0 + per);
+  int sum = 0;
+  if (e < E)
+    for (int c = c0; c < c1; ++c) sum += hist[static_cast<size_t>(c) * E + e];
+  part_sum[part][ex] = sum;
+  __syncthreads();
+  int run = 0;
+  for (int q = 0; q < part; ++q) run += part_sum[q][ex];
+  if (e < E) {
+    for (int c = c0; c < c1; ++c) {
+      const int v = hist[static_cast<size_t>(c) * E + e];
+      hist[static_cast<size_t>(c) * E + e] = run;
+      run += v;
+    }
+    if (part == kScanParts - 1) counts[e] = run;
+  }
+}
+
+// Pass 3: pos = offsets[e] + first row of the chunk for e + the rows of e in
+// earlier warps of the chunk + the lower lanes of this warp that chose e.
+// Block 0 also writes offsets[] and chunk_base[].
+__global__ void __launch_bounds__(kChunkTokens) chunk_place_kernel(const int* __restrict__ idx,
+                                                                   const int* __restrict__ counts,
+                                                                   const int* __restrict__ chunk_first, int T, int E,
+                                                                   int k, int has_shared, int* __restrict__ offsets,
+                                                                   int* __restrict__ perm, int* __restrict__ inv,
+                                                                   int* __restrict__ chunk_base) {
+  pdl_trigger();
+  pdl_wait();
+  extern __shared__ uint32_t sm[];
+  __shared__ int warp_sums[kDispatchThreads / 32];
+  uint32_t* mask = sm;
+  int* base = reinterpret_cast<int*>(sm + kChunkWarps * E);
+  const bool first = blockIdx.x == 0;
+  write_offsets(counts, T, E, has_shared, first ? offsets : nullptr, chunk_base, warp_sums, base);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kChunkTokens) base[e] += chunk_first[static_cast<size_t>(blockIdx.x) * E + e];
+  chunk_masks(idx, T, E, k, mask);  // its barriers also publish base[]
+  const int t = blockIdx.x * kChunkTokens + threadIdx.x;
+  if (t >= T) return;
+  const int w = threadIdx.x >> 5;
+  const uint32_t below = (1u << (threadIdx.x & 31)) - 1u;
+  const int* row = idx + static_cast<size_t>(t) * k;
+  for (int j = 0; j < k; ++j) {
+    const int e = __ldg(row + j);
+    if (e < 0 || e >= E) continue;
+    int pos = base[e] + __popc(mask[w * E + e] & below);
+    for (int q = 0; q < w; ++q) pos += __popc(mask[q * E + e]);
+    const int a = t * k + j;
+    perm[pos] = a;
+    inv[a] = pos;
+  }
+}
+
+// Rows in dispatch order: xp[inv[t*k + j]] = x[t] for j < k, and with
+// with_shared xp[T*k + t] = x[t] too.  One warp per (token, 1024-element
+// slice of its row): the slice is read once (16-byte vectors) and written to
+// each of the token's rows; with to_f16 each bf16 value is rewritten as the
+// nearest fp16.  x is read exactly once, in order.
+constexpr int kScatterVec = 4;  // 16-byte vectors per lane and slice
 template <bool TO_F16>
-__global__ void __launch_bounds__(256) gather_kernel(const bf16* __restrict__ x, const int* __restrict__ perm,
-                                                     int T, int k, int d, int rows, void* __restrict__ xp) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  if (warp >= rows) return;
-  const int Tk = T * k;
-  const int t = (warp < Tk) ? (__ldg(perm + warp) / k) : (warp - Tk);
+__global__ void __launch_bounds__(256) scatter_rows_kernel(const bf16* __restrict__ x, const int* __restrict__ inv,
+                                                           int T, int k, int d, int with_shared,
+                                                           void* __restrict__ xp) {
+  pdl_trigger();
+  pdl_wait();
+  const int n16 = d / 8;
+  const int slices = (n16 + 32 * kScatterVec - 1) / (32 * kScatterVec);
+  const long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= static_cast<long long>(T) * slices) return;
+  const int t = static_cast<int>(w / slices);
+  const int c0 = static_cast<int>(w - static_cast<long long>(t) * slices) * 32 * kScatterVec + lane;
   const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * d);
-  uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(xp) + static_cast<size_t>(warp) * d);
-  for (int c = lane; c < d / 8; c += 32) {
-    uint4 v = __ldg(src + c);
+  uint4 v[kScatterVec];
+#pragma unroll
+  for (int b = 0; b < kScatterVec; ++b) {
+    if (c0 + 32 * b >= n16) continue;
+    v[b] = __ldg(src + c0 + 32 * b);
     if (TO_F16) {
-      uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+      uint32_t* wv = reinterpret_cast<uint32_t*>(&v[b]);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
-        w[i] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(lo))) |
-               (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(hi))) << 16);
+        const float lo = __uint_as_float(wv[i] << 16), hi = __uint_as_float(wv[i] & 0xffff0000u);
+        wv[i] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(lo))) |
+                (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(hi))) << 16);
       }
     }
-    dst[c] = v;
+  }
+  const int n_dst = k + (with_shared ? 1 : 0);
+  for (int j = 0; j < n_dst; ++j) {
+    const int row = (j < k) ? __ldg(inv + static_cast<size_t>(t) * k + j) : T * k + t;
+    uint4* dst = static_cast<uint4*>(xp) + static_cast<size_t>(row) * n16;
+#pragma unroll
+    for (int b = 0; b < kScatterVec; ++b)
+      if (c0 + 32 * b < n16) dst[c0 + 32 * b] = v[b];
   }
 }
 
@@ -157,6 +294,8 @@ __global__ void __launch_bounds__(1024, 1) combine_kernel(const __half* __restri
                                                           const int* __restrict__ chunk_base, int T, int k, int E,
                                                           int d, int has_shared, void* __restrict__ y,
                                                           int out_fp32) {
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.x;
   __shared__ int pos[kMaxTopK + 1];
   __shared__ int chunk[kMaxTopK + 1];
@@ -222,25 +361,139 @@ __global__ void __launch_bounds__(1024, 1) combine_kernel(const __half* __restri
   }
 }
 
-}  // namespace
+// Sign-extended byte b of w.
+__device__ __forceinline__ int sbyte(uint32_t w, int b) { return static_cast<int>(w << (24 - 8 * b)) >> 24; }
 
-cudaError_t launch_dispatch(const int* idx, const int* counts, int T, int E, int k, int has_shared, int* offsets,
-                            int* perm, int* inv, int* chunk_base, cudaStream_t stream) {
-  dispatch_kernel<<<E, kDispatchThreads, 0, stream>>>(idx, counts, T, E, k, has_shared, offsets, perm, inv,
-                                                      chunk_base);
-  return cudaGetLastError();
+// acc[i] += h_i * 2^e_i for the 8 fp16 values of raw and their 8 exponents.
+__device__ __forceinline__ void accum8(float (&acc)[8], const uint4& raw, const uint2& ex) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t eb = (i < 2) ? ex.x : ex.y;
+    const int b = 2 * (i & 1);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+    acc[2 * i] = fmaf(f.x, pow2i(sbyte(eb, b)), acc[2 * i]);
+    acc[2 * i + 1] = fmaf(f.y, pow2i(sbyte(eb, b + 1)), acc[2 * i + 1]);
+  }
 }
 
-cudaError_t launch_gather(const bf16* x, const int* perm, int T, int k, int d, int has_shared, void* xp,
+// combine_kernel with the number of terms NT = k (+1 with the shared expert)
+// fixed at compile time: the terms' row addresses are worked out once per
+// token, and the loads of each half of the terms are in flight together.
+// Same arithmetic and order as combine_kernel.
+template <int NT>
+__global__ void __launch_bounds__(512, 2) combine_nt_kernel(const __half* __restrict__ yp,
+                                                            const int8_t* __restrict__ yexp,
+                                                            const __half* __restrict__ yp_routed,
+                                                            const int8_t* __restrict__ yexp_routed,
+                                                            const int* __restrict__ idx, const int* __restrict__ inv,
+                                                            const int* __restrict__ offsets,
+                                                            const int* __restrict__ chunk_base, int T, int k, int E,
+                                                            int d, void* __restrict__ y, int out_fp32) {
+  pdl_trigger();
+  pdl_wait();
+  constexpr int B1 = (NT + 1) / 2;
+  const int t = blockIdx.x;
+  __shared__ const uint4* rows[NT];
+  __shared__ const uint2* exps[NT];
+  if (threadIdx.x < NT) {
+    const int j = threadIdx.x;
+    const bool routed = j < k;
+    const int g = routed ? __ldg(idx + static_cast<size_t>(t) * k + j) : E;
+    const int p = routed ? __ldg(inv + static_cast<size_t>(t) * k + j) : T * k + t;
+    const int ch = __ldg(chunk_base + g) + (p - __ldg(offsets + g)) / kYpRows;
+    const __half* ybuf = (routed && yp_routed) ? yp_routed : yp;
+    const int8_t* ebuf = (routed && yp_routed) ? yexp_routed : yexp;
+    rows[j] = reinterpret_cast<const uint4*>(ybuf + static_cast<size_t>(p) * d);
+    exps[j] = reinterpret_cast<const uint2*>(ebuf + static_cast<size_t>(ch) * d);
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < d / 8; c += blockDim.x) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    {
+      uint4 raw[B1];
+      uint2 ex[B1];
+#pragma unroll
+      for (int j = 0; j < B1; ++j) {
+        raw[j] = __ldcs(rows[j] + c);
+        ex[j] = __ldg(exps[j] + c);
+      }
+#pragma unroll
+      for (int j = 0; j < B1; ++j) accum8(acc, raw[j], ex[j]);
+    }
+    if (NT > B1) {
+      uint4 raw[NT - B1 > 0 ? NT - B1 : 1];
+      uint2 ex[NT - B1 > 0 ? NT - B1 : 1];
+#pragma unroll
+      for (int j = B1; j < NT; ++j) {
+        raw[j - B1] = __ldcs(rows[j] + c);
+        ex[j - B1] = __ldg(exps[j] + c);
+      }
+#pragma unroll
+      for (int j = B1; j < NT; ++j) accum8(acc, raw[j - B1], ex[j - B1]);
+    }
+    if (out_fp32) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(y) + static_cast<size_t>(t) * d) + 2 * c;
+      dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    } else {
+      uint4 o;
+      uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 pr = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+        ow[i] = *reinterpret_cast<const uint32_t*>(&pr);
+      }
+      reinterpret_cast<uint4*>(static_cast<bf16*>(y) + static_cast<size_t>(t) * d)[c] = o;
+    }
+  }
+}
+
+}  // namespace
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("MOE_PDL");
+    return !(v != nullptr && v[0] == '0');
+  }();
+  return on;
+}
+
+bool chunked_dispatch(int T) { return T >= kChunkedDispatchMinTokens; }
+
+size_t chunk_hist_ints(int T, int E) { return static_cast<size_t>((T + kChunkTokens - 1) / kChunkTokens) * E; }
+
+cudaError_t launch_chunk_counts(const int* idx, int T, int E, int k, int* hist, int* counts, cudaStream_t stream) {
+  if (T <= 0) return cudaSuccess;
+  const int n_chunks = (T + kChunkTokens - 1) / kChunkTokens;
+  const cudaError_t e = launch_chain(chunk_hist_kernel, dim3(n_chunks), dim3(kChunkTokens),
+                                     sizeof(uint32_t) * kChunkWarps * E, stream, idx, T, E, k, hist);
+  if (e != cudaSuccess) return e;
+  return launch_chain(chunk_scan_kernel, dim3((E + 31) / 32), dim3(32 * kScanParts), 0, stream, hist, n_chunks, E,
+                      counts);
+}
+
+cudaError_t launch_dispatch(const int* idx, const int* counts, int T, int E, int k, int has_shared, int* offsets,
+                            int* perm, int* inv, int* chunk_base, const int* chunk_first, cudaStream_t stream) {
+  if (chunk_first != nullptr && chunked_dispatch(T)) {
+    const int n_chunks = (T + kChunkTokens - 1) / kChunkTokens;
+    return launch_chain(chunk_place_kernel, dim3(n_chunks), dim3(kChunkTokens),
+                        sizeof(uint32_t) * (kChunkWarps + 1) * E, stream, idx, counts, chunk_first, T, E, k,
+                        has_shared, offsets, perm, inv, chunk_base);
+  }
+  return launch_chain(dispatch_kernel, dim3(E), dim3(kDispatchThreads), 0, stream, idx, counts, T, E, k, has_shared,
+                      offsets, perm, inv, chunk_base);
+}
+
+cudaError_t launch_gather(const bf16* x, const int* inv, int T, int k, int d, int has_shared, void* xp,
                           bool to_f16, cudaStream_t stream) {
-  const int rows = T * k + (has_shared ? T : 0);
-  if (rows == 0) return cudaSuccess;
-  const int blocks = (rows + 7) / 8;
-  if (to_f16)
-    gather_kernel<true><<<blocks, 256, 0, stream>>>(x, perm, T, k, d, rows, xp);
-  else
-    gather_kernel<false><<<blocks, 256, 0, stream>>>(x, perm, T, k, d, rows, xp);
-  return cudaGetLastError();
+  if (T <= 0) return cudaSuccess;
+  const int n16 = d / 8;
+  const long long warps = static_cast<long long>(T) * ((n16 + 32 * kScatterVec - 1) / (32 * kScatterVec));
+  const long long blocks = (warps + 7) / 8;
+  if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
+  return launch_chain(to_f16 ? scatter_rows_kernel<true> : scatter_rows_kernel<false>,
+                      dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, x, inv, T, k, d, has_shared, xp);
 }
 
 // One block per row: the row's largest magnitude by a block reduction, then
@@ -272,6 +525,8 @@ __global__ void __launch_bounds__(256) quantize_e4m3_kernel(const bf16* __restri
 // their 16-row exponent chunks, in source-major order.
 __global__ void ep_groups_kernel(const int* __restrict__ recv_counts, int S, int E_loc, int* __restrict__ offsets,
                                  int* __restrict__ chunk_base, int* __restrict__ chunks_per_source) {
+  pdl_trigger();
+  pdl_wait();
   if (threadIdx.x != 0) return;
   int rows = 0, chunks = 0;
   for (int s = 0; s < S; ++s) {
@@ -292,31 +547,33 @@ __global__ void ep_groups_kernel(const int* __restrict__ recv_counts, int S, int
 
 __global__ void gather_weights_kernel(const int* __restrict__ perm, const float* __restrict__ prob, int n,
                                       float* __restrict__ w) {
+  pdl_trigger();
+  pdl_wait();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) w[i] = prob[perm[i]];
 }
 
 __global__ void iota_kernel(int* __restrict__ v, int n) {
+  pdl_trigger();
+  pdl_wait();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) v[i] = i;
 }
 
 cudaError_t launch_ep_groups(const int* recv_counts, int S, int E_loc, int* offsets, int* chunk_base,
                              int* chunks_per_source, cudaStream_t stream) {
-  ep_groups_kernel<<<1, 32, 0, stream>>>(recv_counts, S, E_loc, offsets, chunk_base, chunks_per_source);
-  return cudaGetLastError();
+  return launch_chain(ep_groups_kernel, dim3(1), dim3(32), 0, stream, recv_counts, S, E_loc, offsets, chunk_base,
+                      chunks_per_source);
 }
 
 cudaError_t launch_gather_weights(const int* perm, const float* prob, int n, float* w, cudaStream_t stream) {
   if (n <= 0) return cudaSuccess;
-  gather_weights_kernel<<<(n + 255) / 256, 256, 0, stream>>>(perm, prob, n, w);
-  return cudaGetLastError();
+  return launch_chain(gather_weights_kernel, dim3((n + 255) / 256), dim3(256), 0, stream, perm, prob, n, w);
 }
 
 cudaError_t launch_iota(int* v, int n, cudaStream_t stream) {
   if (n <= 0) return cudaSuccess;
-  iota_kernel<<<(n + 255) / 256, 256, 0, stream>>>(v, n);
-  return cudaGetLastError();
+  return launch_chain(iota_kernel, dim3((n + 255) / 256), dim3(256), 0, stream, v, n);
 }
 
 cudaError_t launch_quantize_e4m3(const bf16* w, long long rows, int cols, uint8_t* q, float* s,
@@ -332,10 +589,15 @@ cudaError_t launch_combine(const __half* yp, const int8_t* yexp, const __half* y
                            int E, int d, int has_shared, void* y, int out_fp32, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   const int chunks = d / 8;
+  const int nterms = k + (has_shared ? 1 : 0);
+  if (chunks <= 512 && (nterms == 9 || nterms == 8)) {
+    const int threads = chunks < 32 ? 32 : chunks;
+    return launch_chain(nterms == 9 ? combine_nt_kernel<9> : combine_nt_kernel<8>, dim3(T), dim3(threads), 0, stream,
+                        yp, yexp, yp_routed, yexp_routed, idx, inv, offsets, chunk_base, T, k, E, d, y, out_fp32);
+  }
   const int threads = chunks > 1024 ? 1024 : (chunks < 32 ? 32 : chunks);
-  combine_kernel<<<T, threads, 0, stream>>>(yp, yexp, yp_routed, yexp_routed, idx, inv, offsets, chunk_base, T, k,
-                                            E, d, has_shared, y, out_fp32);
-  return cudaGetLastError();
+  return launch_chain(combine_kernel, dim3(T), dim3(threads), 0, stream, yp, yexp, yp_routed, yexp_routed, idx, inv,
+                      offsets, chunk_base, T, k, E, d, has_shared, y, out_fp32);
 }
 
 // ----------------------------------------------------------------------------

@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
     tmem_alloc(tmem_holder, C::TMEM_COLS);
     tmem_relinquish();
   }
+  pdl_wait();  // offsets, rows and outputs belong to earlier work in the stream until here
   if (warp == kEpilogueWarp0) build_tile_start(args.offsets, G, BN, tile_start, lane);
   tc_fence_before();
   __syncthreads();
@@ -331,6 +332,10 @@ __global__ void __launch_bounds__(kThreads8, 1)
 
   tc_fence_before();
   __syncthreads();
+  // dependents launch as this grid ends (past the barrier every role has
+  // finished): their blocks would otherwise wait on these SMs for the whole
+  // run of this persistent kernel
+  pdl_trigger();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -341,9 +346,8 @@ __global__ void __launch_bounds__(kThreads8, 1)
 template <bool GATEUP, int BN>
 cudaError_t launch8_one(const CUtensorMap* map_w, const CUtensorMap* map_act, const GemmArgs& a, int num_sms,
                         cudaStream_t stream) {
-  expert_gemm_fp8_kernel<GATEUP, BN><<<num_sms, kThreads8, Cfg8<GATEUP, BN>::SMEM_BYTES, stream>>>(*map_w, *map_act,
-                                                                                                 a);
-  return cudaGetLastError();
+  return launch_chain(expert_gemm_fp8_kernel<GATEUP, BN>, dim3(num_sms), dim3(kThreads8),
+                      Cfg8<GATEUP, BN>::SMEM_BYTES, stream, *map_w, *map_act, a);
 }
 
 template <bool GATEUP, int BN>

@@ -118,6 +118,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tmem_alloc_pair(tmem_holder, C::TMEM_COLS);
     tmem_relinquish_pair();
   }
+  pdl_wait();  // offsets, rows and outputs belong to earlier work in the stream until here
   if (warp == kEpilogueWarp0) build_tile_start(args.offsets, G, kPairN, tile_start, lane);
   tc_fence_before();
   cluster_sync();  // barrier inits of both CTAs visible before any remote arrive
@@ -286,6 +287,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   cluster_sync();
+  // dependents launch as this grid ends (past the barrier every role has
+  // finished): their blocks would otherwise wait on these SMs for the whole
+  // run of this persistent kernel
+  pdl_trigger();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -309,12 +314,10 @@ cudaError_t launch_expert_gemm_pair(bool gateup, const CUtensorMap* map_w, const
   if (map_act2 == nullptr) map_act2 = map_act;
   const int grid = num_sms & ~1;
   if (gateup)
-    expert_gemm_pair_kernel<true><<<grid, kThreads, PairCfg<true>::SMEM_BYTES, stream>>>(
-        *map_w, *map_act, *map_act2, a);
-  else
-    expert_gemm_pair_kernel<false><<<grid, kThreads, PairCfg<false>::SMEM_BYTES, stream>>>(
-        *map_w, *map_act, *map_act2, a);
-  return cudaGetLastError();
+    return launch_chain(expert_gemm_pair_kernel<true>, dim3(grid), dim3(kThreads), PairCfg<true>::SMEM_BYTES, stream,
+                        *map_w, *map_act, *map_act2, a);
+  return launch_chain(expert_gemm_pair_kernel<false>, dim3(grid), dim3(kThreads), PairCfg<false>::SMEM_BYTES, stream,
+                      *map_w, *map_act, *map_act2, a);
 }
 
 }  // namespace moe

@@ -1,6 +1,7 @@
 // Internal interface between the C-ABI layer (moe_api.cu) and the kernels.
 // Every launch_* function enqueues on `stream` and returns the launch status.
 #pragma once
+#include <utility>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -8,6 +9,36 @@
 #include <cstdint>
 
 namespace moe {
+
+// Programmatic dependent launch.  The kernels of a layer call are launched
+// with programmatic stream serialisation (launch_chain): a kernel may start
+// while the one before it in the stream is finishing.  Each calls pdl_wait()
+// before its first access to global memory that earlier work in the stream
+// reads or writes (it returns once those grids have completed and their
+// writes are visible) and pdl_trigger() once the next kernel may be placed:
+// short kernels on entry, the persistent GEMMs at their end (without the
+// launch attribute both are no-ops).  MOE_PDL=0 in the environment turns the
+// attribute off.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_chain(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                         Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 
 using bf16 = __nv_bfloat16;
 
@@ -58,11 +89,22 @@ cudaError_t router_gemm_prepare();
 // expert-major permutation perm / its inverse inv, and chunk_base [E+2] (the
 // exponent chunks of the expert outputs, see kYpRows).
 cudaError_t launch_dispatch(const int* idx, const int* counts, int T, int E, int k, int has_shared, int* offsets,
-                            int* perm, int* inv, int* chunk_base, cudaStream_t stream);
+                            int* perm, int* inv, int* chunk_base, const int* chunk_first, cudaStream_t stream);
+// From kChunkedDispatchMinTokens tokens on, the counts come from per-chunk
+// histograms (launch_chunk_counts: hist [ceil(T/256)][E] becomes each chunk's
+// first row per expert, counts [E] the totals) instead of atomics in the top-k
+// kernel, and launch_dispatch places the rows chunk by chunk from them
+// (chunk_first = that hist; NULL: the per-expert kernel at any T).
+constexpr int kChunkedDispatchMinTokens = 1024;
+bool chunked_dispatch(int T);
+size_t chunk_hist_ints(int T, int E);
+cudaError_t launch_chunk_counts(const int* idx, int T, int E, int k, int* hist, int* counts, cudaStream_t stream);
 
-// Gather of token rows into dispatch order: xp[pos] = x[token(pos)]; with
-// to_f16 the rows are written as fp16 (x's bf16 values rounded to nearest).
-cudaError_t launch_gather(const bf16* x, const int* perm, int T, int k, int d, int has_shared, void* xp,
+// Token rows into dispatch order: xp[inv[t*k + j]] = x[t] (j < k), and with
+// has_shared xp[T*k + t] = x[t]; each row of x is read once and written to
+// its positions.  With to_f16 the rows are written as fp16 (x's bf16 values
+// rounded to nearest).
+cudaError_t launch_gather(const bf16* x, const int* inv, int T, int k, int d, int has_shared, void* xp,
                           bool to_f16, cudaStream_t stream);
 
 struct GemmArgs {

@@ -53,6 +53,7 @@ struct moe_handle {
   // workspace (one cudaMalloc)
   void* ws;
   int* counts;     // [E]
+  int* chunk_hist; // [ceil(Tmax/256)][E] per-chunk rows per expert, then each chunk's first row
   float* partial;  // [partial_rows][E] router partial logits
   bf16* w3;        // [3][router_m_tiles*128][d] bf16 slices of W_r (hi, mid, lo)
   int* idx;        // [Tmax*k]
@@ -183,7 +184,10 @@ struct CallOpts {
 int enqueue_router(moe_handle* h, const void* x, int T, CallOpts o, int* idx, float* prob, float* gap,
                    float* tokstats, int n_groups, cudaStream_t s) {
   const moe_config& c = h->cfg;
-  MOE_CUDA(cudaMemsetAsync(h->counts, 0, sizeof(int) * c.n_experts, s));
+  // many tokens: the counts come from per-chunk histograms after the top-k
+  // kernel (no atomics); otherwise the top-k kernel counts into zeroed counts
+  const bool chunked = moe::chunked_dispatch(T);
+  if (!chunked) MOE_CUDA(cudaMemsetAsync(h->counts, 0, sizeof(int) * c.n_experts, s));
   if (T == 0) return MOE_OK;
   const int bn = h->router_tile ? h->router_tile : (T <= 32 ? 16 : (T <= 1024 ? 64 : (T <= 4096 ? 128 : 256)));
   const int n_tt = (T + bn - 1) / bn;
@@ -211,8 +215,9 @@ int enqueue_router(moe_handle* h, const void* x, int T, CallOpts o, int* idx, fl
   ra.m_tiles = h->router_m_tiles;
   ra.ksplit = ks;
   MOE_CUDA(moe::launch_router_gemm(bn, &h->map_w3, &map_x, ra, h->num_sms, s));
-  MOE_CUDA(moe::launch_router_topk(h->partial, ks, T, c.n_experts, o.k, o.renorm, idx, prob, gap, h->counts,
-                                   tokstats, n_groups, s));
+  MOE_CUDA(moe::launch_router_topk(h->partial, ks, T, c.n_experts, o.k, o.renorm, idx, prob, gap,
+                                   chunked ? nullptr : h->counts, tokstats, n_groups, s));
+  if (chunked) MOE_CUDA(moe::launch_chunk_counts(idx, T, c.n_experts, o.k, h->chunk_hist, h->counts, s));
   return MOE_OK;
 }
 
@@ -223,7 +228,7 @@ int enqueue_route(moe_handle* h, const void* x, int T, CallOpts o, int* idx, flo
   const int rc = enqueue_router(h, x, T, o, idx, prob, gap, nullptr, 0, s);
   if (rc != MOE_OK) return rc;
   MOE_CUDA(moe::launch_dispatch(idx, h->counts, T, c.n_experts, o.k, c.has_shared, offsets, perm, h->inv,
-                                h->chunk_base, s));
+                                h->chunk_base, h->chunk_hist, s));
   return MOE_OK;
 }
 
@@ -330,14 +335,14 @@ int enqueue_forward(moe_handle* h, const void* x, int T, CallOpts o, void* y, cu
   if (rc != MOE_OK) return rc;
   MOE_MARK(1);
   MOE_CUDA(moe::launch_dispatch(h->idx, h->counts, T, c.n_experts, o.k, c.has_shared, h->offsets, h->perm, h->inv,
-                                h->chunk_base, s));
+                                h->chunk_base, h->chunk_hist, s));
   MOE_MARK(2);
   // token rows in dispatch order (the yp buffer holds them until the down
   // GEMM).  bf16 weights: the routed rows only — the shared expert's rows are
   // x itself, which its gate/up reads directly.  fp8 weights: every row, as
   // fp16 (the tensor cores' input type there).
   const bool shared_from_x = !h->fp8 && c.has_shared;
-  MOE_CUDA(moe::launch_gather(static_cast<const bf16*>(x), h->perm, T, o.k, c.d_model,
+  MOE_CUDA(moe::launch_gather(static_cast<const bf16*>(x), h->inv, T, o.k, c.d_model,
                               shared_from_x ? 0 : c.has_shared, h->yp, h->fp8, s));
   MOE_MARK(3);
   moe::GemmArgs a{};
@@ -355,7 +360,9 @@ int enqueue_forward(moe_handle* h, const void* x, int T, CallOpts o, void* y, cu
                                h->offsets, h->chunk_base, T, o.k, c.n_experts, c.d_model, c.has_shared, y, c.out_fp32,
                                s));
   MOE_MARK(6);
-  h->last_kernels = 7;  // router GEMM, top-k, dispatch, gather, gate/up, down, combine
+  // router GEMM, top-k, dispatch, gather, gate/up, down, combine; many
+  // tokens: two more for the chunk histograms and their scan
+  h->last_kernels = moe::chunked_dispatch(T) ? 9 : 7;
   return MOE_OK;
 }
 
@@ -484,7 +491,8 @@ int init_any(const moe_config* cfg, const moe_weights* w, const float* s_gu, con
                o_epi = carve(4 * (static_cast<size_t>(ep.max_recv) + 1)),
                o_xs = carve(2 * Tmax * d),
                o_ys = carve((c.out_fp32 ? 4 : 2) * Tmax * d),
-               o_tok = carve(4 * Tmax * (moe::kMaxStatGroups + 1));
+               o_tok = carve(4 * Tmax * (moe::kMaxStatGroups + 1)),
+               o_ch = carve(4 * moe::chunk_hist_ints(static_cast<int>(Tmax), E));
   if (cudaMalloc(&h->ws, off) != cudaSuccess) {
     cudaGetLastError();
     delete h;
@@ -507,6 +515,7 @@ int init_any(const moe_config* cfg, const moe_weights* w, const float* s_gu, con
   h->x_stage = reinterpret_cast<bf16*>(b + o_xs);
   h->y_stage = b + o_ys;
   h->tokstats = reinterpret_cast<float*>(b + o_tok);
+  h->chunk_hist = reinterpret_cast<int*>(b + o_ch);
   h->ep_offsets = reinterpret_cast<int*>(b + o_epo);
   h->ep_chunk_base = reinterpret_cast<int*>(b + o_epc);
   h->ep_chunks_src = reinterpret_cast<int*>(b + o_eps);
@@ -582,10 +591,10 @@ int moe_ep_dispatch(moe_handle* h, const void* x, int T, void* send_rows, float*
   for (int q = 0; q < h->ep_size; ++q) rows_per_rank[q] = 0;
   if (T == 0) return cudaStreamSynchronize(s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
   MOE_CUDA(moe::launch_dispatch(h->idx, h->counts, T, E, k, c.has_shared, h->offsets, h->perm, h->inv,
-                                h->chunk_base, s));
+                                h->chunk_base, h->chunk_hist, s));
   // every row in dispatch order (the shared expert's rows stay here for
   // moe_ep_combine); the routed rows, expert-major, go out rank by rank
-  MOE_CUDA(moe::launch_gather(static_cast<const bf16*>(x), h->perm, T, k, c.d_model, c.has_shared, h->yp, false, s));
+  MOE_CUDA(moe::launch_gather(static_cast<const bf16*>(x), h->inv, T, k, c.d_model, c.has_shared, h->yp, false, s));
   const size_t Tk = static_cast<size_t>(T) * k;
   MOE_CUDA(cudaMemcpyAsync(send_rows, h->yp, Tk * c.d_model * 2, cudaMemcpyDeviceToDevice, s));
   MOE_CUDA(moe::launch_gather_weights(h->perm, h->prob, static_cast<int>(Tk), send_w, s));

@@ -113,6 +113,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_holder, C::TMEM_COLS);
     tmem_relinquish();
   }
+  pdl_wait();  // x and the partial-logit buffer belong to earlier work in the stream until here
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -242,6 +243,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  // dependents launch as this grid ends (past the barrier every role has
+  // finished): their blocks would otherwise wait on these SMs for the whole
+  // run of this persistent kernel
+  pdl_trigger();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -249,57 +254,55 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-constexpr int kMaxPerLane = kMaxExperts / 32;
-
-__device__ __forceinline__ bool better(float v, int e, float ov, int oe) { return v > ov || (v == ov && e < oe); }
-
 constexpr int kTopkWarps = 4;
 constexpr int kTopkWarpMinTokens = 1024;  // from this many tokens on: one warp per token
 
-// Compare-exchange of two (value, expert) slots: afterwards slot a ranks
-// first (higher value, then lower expert index).
-__device__ __forceinline__ void cx(float& va, int& ea, float& vb, int& eb) {
-  if (better(vb, eb, va, ea)) {
-    const float tv = va;
-    va = vb;
-    vb = tv;
-    const int te = ea;
-    ea = eb;
-    eb = te;
+// Best slot of a lane not yet taken: highest softmax numerator, then lowest
+// slot (= lowest expert index, e = lane + 32 i); -1 when none is left.
+template <int NS>
+__device__ __forceinline__ int lane_head(const float (&q)[NS], uint32_t taken, int lane, int E) {
+  int h = -1;
+  float hv = 0.f;
+#pragma unroll
+  for (int i = 0; i < NS; ++i) {
+    const bool ok = !((taken >> i) & 1u) && lane + 32 * i < E;
+    if (ok && (h < 0 || q[i] > hv)) {
+      h = i;
+      hv = q[i];
+    }
   }
+  return h;
 }
 
-// Softmax, top-k (ties: lower index), gap, per-expert counts and the optional
-// per-token statistics of token t, by one warp whose lane l holds the summed
-// logits of experts l, l+32, ... in p.  The lane sorts its own slots once
-// (bitonic network), after which each of the k+1 selection rounds is one
-// xor-butterfly argmax over the 32 lane heads.  renorm != 0: the k weights are
-// divided by their sum (slot order).  tokstats (or NULL): the probability mass
-// of each of n_groups equal expert groups, then the entropy -sum p ln p
-// ([T][n_groups+1]).
-__device__ __forceinline__ void finish_token(float (&p)[kMaxPerLane], int t, int lane, int E, int k, int renorm,
+// Softmax, top-k (ties: lower index), gap, per-expert counts (counts != NULL)
+// and the optional per-token statistics of token t, by one warp whose lane l
+// holds the summed logits of experts l, l+32, ..., l+32(NS-1) in z.  The
+// ranking uses the softmax numerators q_e = exp(z_e - max z), which order the
+// experts as the probabilities q_e / sum q do; each of the k+1 selection
+// rounds is one warp max over the lanes' heads, then the lowest expert index
+// among the heads holding it; only the winning lane finds its next head.
+// renorm != 0: the k weights are divided by their sum (slot order).  tokstats
+// (or NULL): the probability mass of each of n_groups equal expert groups,
+// then the entropy -sum p ln p ([T][n_groups+1]).
+template <int NS>
+__device__ __forceinline__ void finish_token(float (&q)[NS], int t, int lane, int E, int k, int renorm,
                                              int* __restrict__ idx, float* __restrict__ prob,
                                              float* __restrict__ gap, int* counts, float* __restrict__ tokstats,
                                              int n_groups) {
   float zmax = -FLT_MAX;
 #pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) {
-    const int e = lane + 32 * i;
-    if (e < E) zmax = fmaxf(zmax, p[i]);
-  }
+  for (int i = 0; i < NS; ++i)
+    if (lane + 32 * i < E) zmax = fmaxf(zmax, q[i]);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, off));
   float s = 0.f;
 #pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) {
-    const int e = lane + 32 * i;
-    p[i] = (e < E) ? expf(p[i] - zmax) : 0.f;
-    s += p[i];
+  for (int i = 0; i < NS; ++i) {
+    q[i] = (lane + 32 * i < E) ? expf(q[i] - zmax) : 0.f;
+    s += q[i];
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-#pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) p[i] = p[i] / s;
 
   if (tokstats != nullptr) {
     // group masses (group of expert e = e / (E / n_groups)) and entropy
@@ -308,9 +311,9 @@ __device__ __forceinline__ void finish_token(float (&p)[kMaxPerLane], int t, int
     for (int g = 0; g < n_groups; ++g) {
       float m = 0.f;
 #pragma unroll
-      for (int i = 0; i < kMaxPerLane; ++i) {
+      for (int i = 0; i < NS; ++i) {
         const int e = lane + 32 * i;
-        if (e < E && e / per_group == g) m += p[i];
+        if (e < E && e / per_group == g) m += q[i] / s;
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) m += __shfl_xor_sync(0xffffffffu, m, off);
@@ -318,60 +321,36 @@ __device__ __forceinline__ void finish_token(float (&p)[kMaxPerLane], int t, int
     }
     float h = 0.f;
 #pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) {
+    for (int i = 0; i < NS; ++i) {
       const int e = lane + 32 * i;
-      if (e < E && p[i] > 0.f) h -= p[i] * logf(p[i]);
+      const float p = q[i] / s;
+      if (e < E && p > 0.f) h -= p * logf(p);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) h += __shfl_xor_sync(0xffffffffu, h, off);
     if (lane == 0) out[n_groups] = h;
   }
 
-  // this lane's slots, sorted best first (invalid slots: value -1, index max)
-  float sv[kMaxPerLane];
-  int se[kMaxPerLane];
-#pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) {
-    const int e = lane + 32 * i;
-    sv[i] = (e < E) ? p[i] : -1.f;
-    se[i] = (e < E) ? e : 0x7fffffff;
-  }
-#pragma unroll
-  for (int size = 2; size <= kMaxPerLane; size <<= 1)
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1)
-#pragma unroll
-      for (int i = 0; i < kMaxPerLane; ++i) {
-        const int j = i ^ stride;
-        if (j > i) {
-          if ((i & size) == 0)
-            cx(sv[i], se[i], sv[j], se[j]);
-          else
-            cx(sv[j], se[j], sv[i], se[i]);
-        }
-      }
-
-  // Selection rounds on the lane heads: probabilities are >= 0, so their bit
-  // patterns order like the values; key = bits + 1 (0 marks an empty head).
-  // One warp max of the keys, then the lowest expert index among the heads
-  // holding it (ties to the lower index).
+  // Selection rounds.  Numerators are >= 0, so their bit patterns order like
+  // the values; key = bits + 1 (0 marks a lane with nothing left).
+  uint32_t taken = 0u;
+  int head = lane_head(q, taken, lane, E);
   float pk = 0.f, sel_sum = 0.f, my_p = 0.f;
   int my_e = 0;
   for (int j = 0; j <= k; ++j) {
-    const uint32_t hk = (se[0] != 0x7fffffff) ? __float_as_uint(sv[0]) + 1u : 0u;
-    const uint32_t mk = __reduce_max_sync(0xffffffffu, hk);
-    const int be = static_cast<int>(
-        __reduce_min_sync(0xffffffffu, (mk != 0u && hk == mk) ? static_cast<uint32_t>(se[0]) : 0x7fffffffu));
-    const float bv = mk ? __uint_as_float(mk - 1u) : -1.f;
-    if (j < k) {
-      if (be != 0x7fffffff && (be & 31) == lane) {  // the winner pops its head
+    float hq = 0.f;
 #pragma unroll
-        for (int i = 0; i < kMaxPerLane - 1; ++i) {
-          sv[i] = sv[i + 1];
-          se[i] = se[i + 1];
-        }
-        sv[kMaxPerLane - 1] = -1.f;
-        se[kMaxPerLane - 1] = 0x7fffffff;
+    for (int i = 0; i < NS; ++i)
+      if (i == head) hq = q[i];
+    const uint32_t hk = head >= 0 ? __float_as_uint(hq) + 1u : 0u;
+    const uint32_t mk = __reduce_max_sync(0xffffffffu, hk);
+    const uint32_t my_idx = head >= 0 ? static_cast<uint32_t>(lane + 32 * head) : 0x7fffffffu;
+    const int be = static_cast<int>(__reduce_min_sync(0xffffffffu, (mk != 0u && hk == mk) ? my_idx : 0x7fffffffu));
+    const float bv = mk ? __uint_as_float(mk - 1u) / s : -1.f;
+    if (j < k) {
+      if (be != 0x7fffffff && (be & 31) == lane) {  // the winner takes its head and finds the next one
+        taken |= 1u << head;
+        head = lane_head(q, taken, lane, E);
       }
       if (lane == j) {  // lane j keeps slot j
         my_e = be;
@@ -386,7 +365,7 @@ __device__ __forceinline__ void finish_token(float (&p)[kMaxPerLane], int t, int
   if (lane < k) {
     idx[static_cast<size_t>(t) * k + lane] = my_e;
     prob[static_cast<size_t>(t) * k + lane] = renorm ? my_p / sel_sum : my_p;
-    atomicAdd(&counts[my_e], 1);
+    if (counts != nullptr) atomicAdd(&counts[my_e], 1);
   }
 }
 
@@ -394,65 +373,81 @@ __device__ __forceinline__ void finish_token(float (&p)[kMaxPerLane], int t, int
 // partials s = w, w+4, ... in increasing s; warp 0 then adds the four partial
 // sums in warp order (a fixed order: logits are bit-identical run to run) and
 // finishes the token alone.
+template <int NS>
 __global__ void __launch_bounds__(kTopkWarps * 32) router_topk_kernel(const float* __restrict__ partial, int ksplit,
                                                                       int T, int E, int k, int renorm,
                                                                       int* __restrict__ idx,
                                                                       float* __restrict__ prob,
                                                                       float* __restrict__ gap, int* counts,
                                                                       float* __restrict__ tokstats, int n_groups) {
-  __shared__ float zs[kTopkWarps][kMaxExperts];
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float zs[kTopkWarps][32 * NS];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int t = blockIdx.x;
-  float p[kMaxPerLane];
+  float p[NS];
 #pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) p[i] = 0.f;
+  for (int i = 0; i < NS; ++i) p[i] = 0.f;
 #pragma unroll 4
   for (int s = warp; s < ksplit; s += kTopkWarps) {
     const float* row = partial + (static_cast<size_t>(s) * T + t) * E;
 #pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) {
+    for (int i = 0; i < NS; ++i) {
       const int e = lane + 32 * i;
       if (e < E) p[i] += __ldg(row + e);
     }
   }
 #pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) {
-    const int e = lane + 32 * i;
-    if (e < E) zs[warp][e] = p[i];
-  }
+  for (int i = 0; i < NS; ++i) zs[warp][lane + 32 * i] = p[i];
   __syncthreads();
   if (warp != 0) return;
 #pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) {
+  for (int i = 0; i < NS; ++i) {
     const int e = lane + 32 * i;
-    if (e < E) p[i] = ((zs[0][e] + zs[1][e]) + zs[2][e]) + zs[3][e];
+    p[i] = ((zs[0][e] + zs[1][e]) + zs[2][e]) + zs[3][e];
   }
-  finish_token(p, t, lane, E, k, renorm, idx, prob, gap, counts, tokstats, n_groups);
+  finish_token<NS>(p, t, lane, E, k, renorm, idx, prob, gap, counts, tokstats, n_groups);
 }
 
 // Many tokens (prefill): one warp per token, kTopkTokensPerBlock tokens per
 // block; the warp sums the K-split partials in increasing s and finishes the
 // token, so no warp waits on another.
 constexpr int kTopkTokensPerBlock = 8;
+template <int NS>
 __global__ void __launch_bounds__(kTopkTokensPerBlock * 32) router_topk_warp_kernel(
     const float* __restrict__ partial, int ksplit, int T, int E, int k, int renorm, int* __restrict__ idx,
     float* __restrict__ prob, float* __restrict__ gap, int* counts, float* __restrict__ tokstats, int n_groups) {
+  pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kTopkTokensPerBlock + (threadIdx.x >> 5);
   if (t >= T) return;
-  float p[kMaxPerLane];
+  float p[NS];
 #pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) p[i] = 0.f;
-#pragma unroll 4
+  for (int i = 0; i < NS; ++i) p[i] = 0.f;
+#pragma unroll 2
   for (int s = 0; s < ksplit; ++s) {
     const float* row = partial + (static_cast<size_t>(s) * T + t) * E;
 #pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) {
+    for (int i = 0; i < NS; ++i) {
       const int e = lane + 32 * i;
       if (e < E) p[i] += __ldg(row + e);
     }
   }
-  finish_token(p, t, lane, E, k, renorm, idx, prob, gap, counts, tokstats, n_groups);
+  finish_token<NS>(p, t, lane, E, k, renorm, idx, prob, gap, counts, tokstats, n_groups);
+}
+
+template <int NS>
+cudaError_t launch_topk_ns(const float* partial, int ksplit, int T, int E, int k, int renorm, int* idx, float* prob,
+                           float* gap, int* counts, float* tokstats, int n_groups, cudaStream_t stream) {
+  if (T >= kTopkWarpMinTokens) {
+    const int blocks = (T + kTopkTokensPerBlock - 1) / kTopkTokensPerBlock;
+    return launch_chain(router_topk_warp_kernel<NS>, dim3(blocks), dim3(kTopkTokensPerBlock * 32), 0, stream,
+                        partial, ksplit, T, E, k, renorm, idx, prob, gap, counts, tokstats, n_groups);
+  } else {
+    return launch_chain(router_topk_kernel<NS>, dim3(T), dim3(kTopkWarps * 32), 0, stream, partial, ksplit, T, E, k,
+                        renorm, idx, prob, gap, counts, tokstats, n_groups);
+  }
 }
 
 // Routing statistics over the tokens: group_p[g] = mean over tokens of the
@@ -464,6 +459,8 @@ __global__ void __launch_bounds__(kTopkTokensPerBlock * 32) router_topk_warp_ker
 __global__ void __launch_bounds__(256) route_stats_kernel(const float* __restrict__ tokstats, const int* counts,
                                                           int T, int E, int k, int n_groups, float* group_f,
                                                           float* group_p, float* summary) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float red[256];
   __shared__ float col_sum[kMaxStatGroups + 1];
   const int cols = n_groups + 1;
@@ -525,8 +522,8 @@ __global__ void split_router_kernel(const float* __restrict__ w, int E, int d, i
 template <int BN>
 cudaError_t launch_rg(const CUtensorMap* map_w3, const CUtensorMap* map_x, const RouterGemmArgs& a, int grid,
                       cudaStream_t stream) {
-  router_gemm_kernel<BN><<<grid, kThreads, RCfg<BN>::SMEM_BYTES, stream>>>(*map_w3, *map_x, a);
-  return cudaGetLastError();
+  return launch_chain(router_gemm_kernel<BN>, dim3(grid), dim3(kThreads), RCfg<BN>::SMEM_BYTES, stream, *map_w3,
+                      *map_x, a);
 }
 
 }  // namespace
@@ -564,21 +561,25 @@ cudaError_t launch_router_topk(const float* partial, int ksplit, int T, int E, i
                                float* prob, float* gap, int* counts, float* tokstats, int n_groups,
                                cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
-  if (T >= kTopkWarpMinTokens) {
-    const int blocks = (T + kTopkTokensPerBlock - 1) / kTopkTokensPerBlock;
-    router_topk_warp_kernel<<<blocks, kTopkTokensPerBlock * 32, 0, stream>>>(partial, ksplit, T, E, k, renorm, idx,
-                                                                           prob, gap, counts, tokstats, n_groups);
-  } else {
-    router_topk_kernel<<<T, kTopkWarps * 32, 0, stream>>>(partial, ksplit, T, E, k, renorm, idx, prob, gap,
-                                                         counts, tokstats, n_groups);
-  }
-  return cudaGetLastError();
+  // slots per lane: the fewest that hold E experts (of the instantiated widths)
+  if (E <= 64)
+    return launch_topk_ns<2>(partial, ksplit, T, E, k, renorm, idx, prob, gap, counts, tokstats, n_groups, stream);
+  if (E <= 128)
+    return launch_topk_ns<4>(partial, ksplit, T, E, k, renorm, idx, prob, gap, counts, tokstats, n_groups, stream);
+  if (E <= 256)
+    return launch_topk_ns<8>(partial, ksplit, T, E, k, renorm, idx, prob, gap, counts, tokstats, n_groups, stream);
+  if (E <= 288)
+    return launch_topk_ns<9>(partial, ksplit, T, E, k, renorm, idx, prob, gap, counts, tokstats, n_groups, stream);
+  if (E <= kMaxExperts)
+    return launch_topk_ns<kMaxExperts / 32>(partial, ksplit, T, E, k, renorm, idx, prob, gap, counts, tokstats,
+                                            n_groups, stream);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_route_stats(const float* tokstats, const int* counts, int T, int E, int k, int n_groups,
                                float* group_f, float* group_p, float* summary, cudaStream_t stream) {
-  route_stats_kernel<<<1, 256, 0, stream>>>(tokstats, counts, T, E, k, n_groups, group_f, group_p, summary);
-  return cudaGetLastError();
+  return launch_chain(route_stats_kernel, dim3(1), dim3(256), 0, stream, tokstats, counts, T, E, k, n_groups, group_f,
+                      group_p, summary);
 }
 
 cudaError_t launch_split_router(const float* w, int E, int d, int e_pad, bf16* w3, cudaStream_t stream) {

@@ -284,8 +284,10 @@ int moe_check(moe_handle* h, void* stream);
 
 /*
  * Number of kernels the last moe_forward / moe_forward_ex / moe_forward_host
- * on this handle enqueued (0 after a call with T = 0; otherwise the router
- * GEMM, top-k, dispatch, row gather, gate/up, down and combine kernels).
+ * on this handle enqueued (0 after a call with T = 0; otherwise 7: the router
+ * GEMM, top-k, dispatch, row gather, gate/up, down and combine kernels, and
+ * from 1024 tokens on 9: two more that count each expert's rows per 256-token
+ * chunk and scan those counts, in place of counters in the top-k kernel).
  * Host-only, never synchronises.  Returns -1 for an invalid handle.  No
  * counterpart in the pages: instrumentation for launch accounting.
  */

@@ -89,6 +89,40 @@ def test_many_tokens_small_layer(T):
     run_and_check(inp, tokens=64)
 
 
+@pytest.mark.parametrize("shape", [
+    synth.LayerShape(T=300, d=384, E=24, k=8, F=128, has_shared=False),  # 8 terms, no shared expert
+    synth.LayerShape(T=300, d=384, E=24, k=7, F=128),                    # 8 terms with the shared expert
+    synth.LayerShape(T=1500, d=256, E=32, k=8, F=128),                   # 9 terms, chunked dispatch
+    synth.LayerShape(T=1024, d=256, E=40, k=6, F=128),                   # first token count of the chunked path
+    synth.LayerShape(T=1025, d=128, E=300, k=8, F=128),                  # 16 slots per lane in the top-k
+])
+def test_combine_terms_and_chunked_dispatch(shape):
+    inp = synth.make_inputs(shape, seed=60 + shape.T % 11 + shape.k)
+    run_and_check(inp, tokens=96 if shape.T > 1000 else None)
+
+
+def test_chunked_dispatch_ties_and_one_hot():
+    # Many tokens choosing the same experts: W_r = 0 (every token picks 0..3,
+    # all rows of a chunk land in four experts) and a one-hot bias.
+    shape = synth.LayerShape(T=2000, d=256, E=16, k=4, F=128)
+    inp = synth.make_inputs(shape, seed=12)
+    inp.w_router.zero_()
+    layer, x = make_layer(inp)
+    idx, prob, perm, offsets, gap = layer.route(x)
+    assert np.all(cpu(idx) == np.arange(4)[None, :])
+    off = cpu(offsets)
+    assert list(off[:6]) == [0, 2000, 4000, 6000, 8000, 8000]
+    perm_h = cpu(perm)
+    for e in range(4):  # rows of expert e: tokens in order, slot e
+        np.testing.assert_array_equal(perm_h[e * 2000:(e + 1) * 2000], np.arange(2000) * 4 + e)
+    layer.close()
+    inp = synth.make_inputs(shape, seed=13)
+    inp.x[:, 0] = 1.0
+    inp.w_router[:, 0] = -20.0
+    inp.w_router[5, 0] = 20.0
+    run_and_check(inp, tokens=64)
+
+
 def test_several_weight_tiles_and_k_steps():
     # F = 256 -> 2 gate/up weight tiles, d = 512 -> 4 down weight tiles and 8 K steps.
     shape = synth.LayerShape(T=200, d=512, E=32, k=4, F=256)
@@ -101,6 +135,11 @@ def test_kernel_count_reported():
     layer, x = make_layer(inp)
     layer.forward(x)
     assert layer.last_kernel_count() == 7
+    big = synth.make_inputs(synth.TINY.with_tokens(1024), seed=42)
+    layer2, x2 = make_layer(big)
+    layer2.forward(x2)
+    assert layer2.last_kernel_count() == 9  # chunked dispatch from 1024 tokens on
+    layer2.close()
     binding.moe_forward(layer.handle, x[:0], 0, torch.empty_like(x[:0]))
     assert layer.last_kernel_count() == 0
     layer.close()
