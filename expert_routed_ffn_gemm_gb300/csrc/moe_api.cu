@@ -192,11 +192,23 @@ int enqueue_router(moe_handle* h, const void* x, int T, CallOpts o, int* idx, fl
   const int bn = h->router_tile ? h->router_tile : (T <= 32 ? 16 : (T <= 1024 ? 64 : (T <= 4096 ? 128 : 256)));
   const int n_tt = (T + bn - 1) / bn;
   const int k_total = 3 * c.d_model / moe::kBlockK;
-  // K splits: about four waves of work items over the SMs (balances the last
-  // wave at large T, fills the GPU at small T)
+  // K splits: up to about two waves of work items, the count that fills the
+  // waves best (the fewest splits among equals: every split adds a partial
+  // logit pass).  At 8192 tokens this is 3 splits of 288 items on 152 SMs,
+  // measured 8 us faster than 6 and 14 us faster than 1.
   const int base_items = n_tt * h->router_m_tiles;
-  int ks = (4 * h->num_sms + base_items / 2) / base_items;
-  ks = ks < 1 ? 1 : (ks > moe::kMaxKSplit ? moe::kMaxKSplit : ks);
+  const int ks_cap = std::min(moe::kMaxKSplit, std::max(1, (2 * h->num_sms + base_items - 1) / base_items));
+  int ks = 1;
+  double best = 0.0;
+  for (int cand = 1; cand <= ks_cap; ++cand) {
+    const long long items = static_cast<long long>(cand) * base_items;
+    const long long waves = (items + h->num_sms - 1) / h->num_sms;
+    const double fill = static_cast<double>(items) / static_cast<double>(waves * h->num_sms);
+    if (fill > best + 0.02) {
+      best = fill;
+      ks = cand;
+    }
+  }
   ks = ks > k_total ? k_total : ks;
   while (ks > 1 && static_cast<long long>(ks) * T > h->partial_rows) --ks;
   // every split must own at least one K step: ks = ceil(k_total / ceil(k_total / ks))
