@@ -7,6 +7,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstdint>
+#include <cstdio>
 #include <algorithm>
 #include <cstdlib>
 #include <cstring>
@@ -156,12 +157,48 @@ int choose_tile(double mean_rows, int cap) {
   return cap;
 }
 
-#define MOE_CUDA(call)                    \
-  do {                                    \
-    if ((call) != cudaSuccess) {          \
-      return MOE_ERR_CUDA;                \
-    }                                     \
+// MOE_TRACE_ERRORS=1 in the environment: every failing CUDA call is reported
+// on stderr with its source line and error name.
+bool trace_errors() {
+  static const bool on = [] {
+    const char* v = std::getenv("MOE_TRACE_ERRORS");
+    return v != nullptr && v[0] == '1';
+  }();
+  return on;
+}
+
+int cuda_failed(cudaError_t e, const char* what, int line) {
+  if (trace_errors()) std::fprintf(stderr, "moe: line %d: %s -> %s\n", line, what, cudaGetErrorName(e));
+  return MOE_ERR_CUDA;
+}
+
+#define MOE_CUDA(call)                                   \
+  do {                                                   \
+    const cudaError_t moe_e_ = (call);                   \
+    if (moe_e_ != cudaSuccess) {                         \
+      return cuda_failed(moe_e_, #call, __LINE__);       \
+    }                                                    \
   } while (0)
+
+// Every call on a handle runs with the handle's device current in the calling
+// thread (and puts the previous device back): a thread that has not used CUDA
+// yet gets the device's primary context before the first driver call (the
+// tensor-map encoding), and a caller working on another device is unaffected.
+struct DeviceGuard {
+  int prev = -1, dev;
+  explicit DeviceGuard(int d) : dev(d) {
+    if (cudaGetDevice(&prev) != cudaSuccess) {
+      cudaGetLastError();
+      prev = -1;
+    }
+    if (cudaSetDevice(dev) != cudaSuccess) cudaGetLastError();
+  }
+  ~DeviceGuard() {
+    if (prev >= 0 && prev != dev) cudaSetDevice(prev);
+  }
+  DeviceGuard(const DeviceGuard&) = delete;
+  DeviceGuard& operator=(const DeviceGuard&) = delete;
+};
 
 int check_call(const moe_handle* h, const void* x, int T) {
   if (!valid_handle(h)) return MOE_ERR_INVALID_ARG;
@@ -588,6 +625,7 @@ int moe_ep_dispatch(moe_handle* h, const void* x, int T, void* send_rows, float*
                     int* rows_per_rank, void* stream) {
   int rc = check_call(h, x, T);
   if (rc != MOE_OK) return rc;
+  DeviceGuard device_guard(h->device);
   if (h->ep_size == 0 || rows_per_rank == nullptr || send_counts == nullptr) return MOE_ERR_INVALID_ARG;
   const moe_config& c = h->cfg;
   const int k = c.top_k, E = c.n_experts;
@@ -621,6 +659,7 @@ int moe_ep_experts(moe_handle* h, const void* recv_rows, const int* recv_counts,
                    void* out_rows, void* out_exp, int* chunks_per_source, void* stream) {
   if (!valid_handle(h) || h->ep_size == 0 || recv_counts == nullptr || chunks_per_source == nullptr)
     return MOE_ERR_INVALID_ARG;
+  DeviceGuard device_guard(h->device);
   if (n_recv < 0) return MOE_ERR_INVALID_ARG;
   if (n_recv > h->max_recv) return MOE_ERR_TOO_MANY_TOKENS;
   if (!aligned(recv_counts, 4) || !is_device_ptr(recv_counts)) return MOE_ERR_INVALID_ARG;
@@ -662,6 +701,7 @@ int moe_ep_experts(moe_handle* h, const void* recv_rows, const int* recv_counts,
 
 int moe_ep_combine(moe_handle* h, const void* ret_rows, const void* ret_exp, void* y, void* stream) {
   if (!valid_handle(h) || h->ep_size == 0) return MOE_ERR_INVALID_ARG;
+  DeviceGuard device_guard(h->device);
   const moe_config& c = h->cfg;
   const int T = h->ep_T, k = c.top_k;
   if (T == 0) return MOE_OK;
@@ -702,6 +742,7 @@ int moe_route_ex(moe_handle* h, const void* x, int T, const moe_call_options* op
                  int* offsets, float* gap, void* stream) {
   int rc = check_call(h, x, T);
   if (rc != MOE_OK) return rc;
+  DeviceGuard device_guard(h->device);
   CallOpts o;
   if ((rc = resolve_opts(h, opt, &o)) != MOE_OK) return rc;
   if (idx == nullptr || prob == nullptr || perm == nullptr || offsets == nullptr) return MOE_ERR_INVALID_ARG;
@@ -722,6 +763,7 @@ int moe_route(moe_handle* h, const void* x, int T, int* idx, float* prob, int* p
 int moe_forward_ex(moe_handle* h, const void* x, int T, const moe_call_options* opt, void* y, void* stream) {
   int rc = check_call(h, x, T);
   if (rc != MOE_OK) return rc;
+  DeviceGuard device_guard(h->device);
   if (h->ep_size != 0) return MOE_ERR_INVALID_ARG;  // an expert-parallel handle holds only its experts
   CallOpts o;
   if ((rc = resolve_opts(h, opt, &o)) != MOE_OK) return rc;
@@ -740,6 +782,7 @@ int moe_route_stats(moe_handle* h, const void* x, int T, int n_groups, int* coun
                     float* group_p, float* summary, void* stream) {
   int rc = check_call(h, x, T);
   if (rc != MOE_OK) return rc;
+  DeviceGuard device_guard(h->device);
   const moe_config& c = h->cfg;
   if (n_groups < 1 || n_groups > moe::kMaxStatGroups || c.n_experts % n_groups != 0) return MOE_ERR_INVALID_ARG;
   if (counts == nullptr || group_f == nullptr || group_p == nullptr || summary == nullptr) return MOE_ERR_INVALID_ARG;
@@ -760,6 +803,7 @@ int moe_route_stats(moe_handle* h, const void* x, int T, int n_groups, int* coun
 
 int moe_forward_host(moe_handle* h, const void* x_host, int T, void* y_host, void* stream) {
   if (!valid_handle(h) || h->ep_size != 0) return MOE_ERR_INVALID_ARG;
+  DeviceGuard device_guard(h->device);
   if (T < 0) return MOE_ERR_INVALID_ARG;
   if (T > h->cfg.max_tokens) return MOE_ERR_TOO_MANY_TOKENS;
   if (T == 0) return MOE_OK;
@@ -783,6 +827,7 @@ int moe_last_kernel_count(const moe_handle* h) {
 
 int moe_check(moe_handle* h, void* stream) {
   if (!valid_handle(h)) return MOE_ERR_INVALID_ARG;
+  DeviceGuard device_guard(h->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
   uint32_t e = 0;
@@ -807,6 +852,7 @@ int moe_profile_enable(moe_handle* h, int enable) {
 
 int moe_profile_read(moe_handle* h, float* ms, int* n_calls) {
   if (!valid_handle(h) || ms == nullptr || n_calls == nullptr) return MOE_ERR_INVALID_ARG;
+  DeviceGuard device_guard(h->device);
   for (int i = 0; i < kProfStages; ++i) ms[i] = 0.f;
   *n_calls = h->n_prof;
   for (int c = 0; c < h->n_prof; ++c) {
@@ -824,6 +870,7 @@ int moe_profile_read(moe_handle* h, float* ms, int* n_calls) {
 
 int moe_free(moe_handle* h) {
   if (!valid_handle(h)) return MOE_ERR_INVALID_ARG;
+  DeviceGuard device_guard(h->device);
   h->magic = 0;
   const bool ok = cudaDeviceSynchronize() == cudaSuccess;
   for (auto& ev : h->prof)

@@ -24,6 +24,11 @@
  *     moe_check and moe_forward_host, which say so.
  *   - A handle holds one workspace: calls on one handle must be ordered (one
  *     stream, or ordered by the caller).  Different handles are independent.
+ *   - Any host thread may call: each call on a handle makes the handle's device
+ *     current for its duration (binding the device's primary context in a
+ *     thread that has not used CUDA yet) and restores the caller's device.
+ *   - MOE_TRACE_ERRORS=1 in the environment prints every failing CUDA call
+ *     (source line and error name) on stderr.
  *   - Return value: MOE_OK (0) or one of the MOE_ERR_* codes below.  Argument
  *     errors are found on the host before anything is enqueued; nothing traps
  *     on the device.  Device-side failures (a pipeline wait that exceeded its

@@ -59,7 +59,7 @@ def run_ranks(inp, xs, ep_size, max_recv):
     return ys
 
 
-@pytest.mark.parametrize("ep_size,Ts", [(1, [96]), (2, [70, 130]), (4, [40, 0, 65, 17])])
+@pytest.mark.parametrize("ep_size,Ts", [(1, [96]), (2, [70, 130]), (4, [40, 0, 65, 17]), (2, [1500, 300])])
 def test_expert_parallel_matches_whole_layer(ep_size, Ts):
     shape = synth.LayerShape(T=max(Ts), d=256, E=16, k=2, F=128)
     inp = synth.make_inputs(shape, seed=60 + ep_size)

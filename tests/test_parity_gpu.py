@@ -330,3 +330,30 @@ def test_forward_captured_in_a_cuda_graph():
         assert torch.equal(y, layer.forward(x))
     assert layer.check() == binding.MOE_OK
     layer.close()
+
+
+def test_forward_from_a_new_thread():
+    # A host thread that has not used CUDA yet: the library binds the handle's
+    # device before its first driver call (1500 tokens take the chunked
+    # dispatch, whose first call is the tensor-map encoding of x).
+    import threading
+
+    inp = synth.make_inputs(synth.LayerShape(T=1500, d=256, E=16, k=2, F=128), seed=47)
+    layer, x = make_layer(inp)
+    y_main = layer.forward(x)
+    torch.cuda.synchronize()
+    out, errs = {}, []
+
+    def work():
+        try:
+            out["y"] = layer.forward(x)
+            torch.cuda.synchronize()
+        except Exception as e:  # noqa: BLE001 - reported below
+            errs.append(e)
+
+    t = threading.Thread(target=work)
+    t.start()
+    t.join(timeout=120)
+    assert not errs, errs
+    assert torch.equal(out["y"], y_main)
+    layer.close()
