@@ -84,30 +84,6 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
-// Row gather: rows r0..r3 of a 2-D map whose box is 64 columns x 1 row land as
-// four consecutive 128-byte rows at smem_dst (the map's swizzle applied on the
-// shared-memory address, so four-row groups at 512-byte offsets of a
-// 1024-aligned tile form the same layout as one 8-row box).
-__device__ __forceinline__ void tma_gather4(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int32_t col,
-                                            int32_t r0, int32_t r1, int32_t r2, int32_t r3, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar)),
-      "l"(policy)
-      : "memory");
-}
-
-// The same, completing on an mbarrier of either CTA of a pair (shared::cluster address).
-__device__ __forceinline__ void tma_gather4_pair(void* smem_dst, const CUtensorMap* map, uint32_t bar, int32_t col,
-                                                 int32_t r0, int32_t r1, int32_t r2, int32_t r3, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes.cta_group::2"
-      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar), "l"(policy)
-      : "memory");
-}
-
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -308,7 +284,5 @@ __device__ __forceinline__ void tc_commit_pair(uint64_t* bar) {
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
-
-__device__ __forceinline__ bool elect_one_lane() { return (threadIdx.x & 31u) == 0u; }
 
 }  // namespace moe
