@@ -98,3 +98,9 @@ def test_fp8_without_shared_expert():
 def test_fp8_flash_decode(T):
     # d=4096, 288 routed + 1 shared, top-8, width 1280
     fp8_case(synth.FLASH_DECODE.with_tokens(T), seed=24, n_sample=None if T == 1 else 48)
+
+
+def test_fp8_many_tokens():
+    # 2000 tokens over 24 experts: chunked dispatch, every row (the shared
+    # expert's too) scattered as fp16, ~170 rows per group in 128-row tiles
+    fp8_case(synth.LayerShape(T=2000, d=512, E=24, k=2, F=256), seed=26, n_sample=64)
