@@ -275,6 +275,142 @@ __global__ void __launch_bounds__(256) scatter_rows_kernel(const bf16* __restric
   }
 }
 
+// FP8 token rows as two E4M3 terms (see launch_scatter_x2): one block of 128
+// threads per token, a pass for max|x|, then hi / lo of 8 values per thread
+// and step, written to each of the token's rows.
+__global__ void __launch_bounds__(128) scatter_rows_x2_kernel(const bf16* __restrict__ x,
+                                                              const int* __restrict__ inv, int T, int k, int d,
+                                                              int with_shared, uint8_t* __restrict__ xq,
+                                                              int lo_row0, float* __restrict__ inv_s) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float red[4];
+  const int t = blockIdx.x;
+  const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * d);
+  const int n8 = d / 8;
+  float amax = 0.f;
+  for (int c = threadIdx.x; c < n8; c += 128) {
+    const uint4 v = __ldg(src + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xffff0000u))));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  // s = 2^e, the largest power of two with s * amax <= 448 = 1.75 * 2^8
+  int e = 0;
+  if (amax > 0.f) {
+    const uint32_t b = __float_as_uint(amax);
+    const int ea = static_cast<int>((b >> 23) & 0xffu) - 127;
+    e = ((b & 0x7fffffu) <= 0x600000u ? 8 : 7) - ea;
+    e = min(120, max(-120, e));
+  }
+  const float s = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+  const int n_dst = k + (with_shared ? 1 : 0);
+  for (int j = threadIdx.x; j < n_dst; j += 128) {
+    const int pos = (j < k) ? __ldg(inv + static_cast<size_t>(t) * k + j) : T * k + t;
+    inv_s[pos] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+  }
+  for (int c = threadIdx.x; c < n8; c += 128) {
+    const uint4 v = __ldg(src + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t hi[2], lo[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = make_float2(__uint_as_float(w[i] << 16) * s, __uint_as_float(w[i] & 0xffff0000u) * s);
+      const __nv_fp8x2_storage_t h2 = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+      const float2 hf = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(h2, __NV_E4M3)));
+      const __nv_fp8x2_storage_t l2 =
+          __nv_cvt_float2_to_fp8x2(make_float2(f.x - hf.x, f.y - hf.y), __NV_SATFINITE, __NV_E4M3);
+      const int word = i >> 1;
+      if ((i & 1) == 0) {
+        hi[word] = h2;
+        lo[word] = l2;
+      } else {
+        hi[word] |= static_cast<uint32_t>(h2) << 16;
+        lo[word] |= static_cast<uint32_t>(l2) << 16;
+      }
+    }
+    for (int j = 0; j < n_dst; ++j) {
+      const int pos = (j < k) ? __ldg(inv + static_cast<size_t>(t) * k + j) : T * k + t;
+      reinterpret_cast<uint2*>(xq + static_cast<size_t>(pos) * d)[c] = make_uint2(hi[0], hi[1]);
+      reinterpret_cast<uint2*>(xq + static_cast<size_t>(lo_row0 + pos) * d)[c] = make_uint2(lo[0], lo[1]);
+    }
+  }
+}
+
+// H rows in place as two-term E4M3 rows (see launch_requant_rows_x2): one
+// block of 128 threads per row; every thread reads its 8-value chunks and the
+// row's largest magnitude is reduced before any byte of the row is written.
+constexpr int kRequantChunks = 8;  // chunks of 8 values per thread: F <= 8192
+__global__ void __launch_bounds__(128) requant_rows_x2_kernel(uint8_t* __restrict__ h, int F,
+                                                              float* __restrict__ inv_s) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float red[4];
+  uint8_t* row = h + static_cast<size_t>(blockIdx.x) * 2 * F;
+  const int n8 = F / 8;
+  uint4 v[kRequantChunks];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < kRequantChunks; ++i) {
+    const int c = threadIdx.x + i * 128;
+    if (c < n8) {
+      v[i] = reinterpret_cast<const uint4*>(row)[c];
+      const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
+        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();  // also: every chunk of the row has been read
+  amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  int e = 0;
+  if (amax > 0.f) {
+    const uint32_t b = __float_as_uint(amax);
+    const int ea = static_cast<int>((b >> 23) & 0xffu) - 127;
+    e = ((b & 0x7fffffu) <= 0x600000u ? 8 : 7) - ea;
+    e = min(120, max(-120, e));
+  }
+  const float s = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+  if (threadIdx.x == 0) inv_s[blockIdx.x] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+#pragma unroll
+  for (int i = 0; i < kRequantChunks; ++i) {
+    const int c = threadIdx.x + i * 128;
+    if (c >= n8) continue;
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+    uint32_t hi[2], lo[2];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
+      const float2 f = make_float2(f0.x * s, f0.y * s);
+      const __nv_fp8x2_storage_t h2 = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+      const float2 hf = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(h2, __NV_E4M3)));
+      const __nv_fp8x2_storage_t l2 =
+          __nv_cvt_float2_to_fp8x2(make_float2(f.x - hf.x, f.y - hf.y), __NV_SATFINITE, __NV_E4M3);
+      const int word = j >> 1;
+      if ((j & 1) == 0) {
+        hi[word] = h2;
+        lo[word] = l2;
+      } else {
+        hi[word] |= static_cast<uint32_t>(h2) << 16;
+        lo[word] |= static_cast<uint32_t>(l2) << 16;
+      }
+    }
+    reinterpret_cast<uint2*>(row)[c] = make_uint2(hi[0], hi[1]);
+    reinterpret_cast<uint2*>(row + F)[c] = make_uint2(lo[0], lo[1]);
+  }
+}
+
 constexpr int kCombineBatch = 5;  // terms whose loads are in flight together
 
 // 2^e for an int8 exponent in [-126, 113], exact.
@@ -494,6 +630,19 @@ cudaError_t launch_gather(const bf16* x, const int* inv, int T, int k, int d, in
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
   return launch_chain(to_f16 ? scatter_rows_kernel<true> : scatter_rows_kernel<false>,
                       dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, x, inv, T, k, d, has_shared, xp);
+}
+
+cudaError_t launch_scatter_x2(const bf16* x, const int* inv, int T, int k, int d, int has_shared, uint8_t* xq,
+                              int lo_row0, float* inv_s, cudaStream_t stream) {
+  if (T <= 0) return cudaSuccess;
+  return launch_chain(scatter_rows_x2_kernel, dim3(T), dim3(128), 0, stream, x, inv, T, k, d, has_shared, xq,
+                      lo_row0, inv_s);
+}
+
+cudaError_t launch_requant_rows_x2(void* h, int rows, int F, float* inv_s, cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  if (F % 8 != 0 || F / 8 > 128 * kRequantChunks) return cudaErrorInvalidValue;
+  return launch_chain(requant_rows_x2_kernel, dim3(rows), dim3(128), 0, stream, static_cast<uint8_t*>(h), F, inv_s);
 }
 
 // One block per row: the row's largest magnitude by a block reduction, then

@@ -210,23 +210,27 @@ __device__ __forceinline__ int block_exponent(uint32_t amax) {
 // (from the thread's own maximum, no exchange) goes to Ye[chunk0 + c0/16][feat]
 // and the values to Y as fp16 of value * 2^-e.  chunk0 = the exponent chunk of
 // the tile's first row (tile rows start at multiples of 16 inside the group).
+// lo_off > 0: the accumulator holds two terms per column, at c and at
+// lo_off + c (two-term E4M3 token rows), and acc[col] is their sum.
 template <int BN>
 __device__ __forceinline__ void epilogue_down(uint32_t taddr, int feat, int row0, int valid,
                                               const float (&wreg)[(BN + 31) / 32], __half* Y, int8_t* Ye, int ldy,
-                                              int chunk0, float row_scale = 1.0f) {
+                                              int chunk0, float row_scale = 1.0f, int lo_off = 0) {
   static_assert(kYpRows == 16, "one exponent chunk per 16-column TMEM load");
 #pragma unroll
   for (int c0 = 0; c0 < BN; c0 += 16) {
     if (c0 >= valid) break;
-    uint32_t v[16];
+    uint32_t v[16], vl[16];
     tmem_ld16(taddr + c0, v);
+    if (lo_off > 0) tmem_ld16(taddr + lo_off + c0, vl);
     tmem_ld_wait();
     float y[16];
     uint32_t amax = 0;
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
       const int col = c0 + c;
-      y[c] = __shfl_sync(0xffffffffu, wreg[col >> 5], col & 31) * (row_scale * __uint_as_float(v[c]));
+      const float acc = lo_off > 0 ? __uint_as_float(v[c]) + __uint_as_float(vl[c]) : __uint_as_float(v[c]);
+      y[c] = __shfl_sync(0xffffffffu, wreg[col >> 5], col & 31) * (row_scale * acc);
       amax = max(amax, __float_as_uint(y[c]) & 0x7fffffffu);
     }
     const int e = block_exponent(amax);

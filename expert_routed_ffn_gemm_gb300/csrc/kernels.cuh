@@ -127,6 +127,8 @@ struct GemmArgs {
   int reverse;         // 1: work items in reverse order (last group first)
   int w_group_base;    // weights of group g: w_group_base + (w_group_mod ? g % w_group_mod : g)
   int w_group_mod;
+  const float* tok_scale;  // FP8 gate/up with two-term tokens: 1/s of every dispatch row
+  int lo_row0, lo_col0;    // ... and where the lo terms of dispatch row 0 sit in the token map
   int act2_from;       // bf16 kernels: token rows from this dispatch position on come through
                        // map_act2 at row (position - act2_from); -1: all through map_act
 };
@@ -156,6 +158,25 @@ cudaError_t expert_gemm_pair_prepare();
 cudaError_t launch_expert_gemm_fp8(bool gateup, int tile_n, const CUtensorMap* map_w, const CUtensorMap* map_act,
                                    const GemmArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t expert_gemm_fp8_prepare();
+// K3 / K4 with E4M3 weights and two-term E4M3 token rows (tcgen05.mma
+// kind::f8f6f4): map_tok is a byte map whose boxes are tile_n rows x 128 bytes,
+// the hi terms of dispatch row r at row r and the lo terms at row
+// a.lo_row0 + r, column a.lo_col0 on; a.tok_scale holds 1/s of every dispatch
+// row.  K3 writes H as fp16, K4 writes Yp as expert_gemm.cu does.
+// tile_n = 16, 32, 64 or 128.
+cudaError_t launch_expert_gemm_fp8x(bool gateup, int tile_n, const CUtensorMap* map_w, const CUtensorMap* map_tok,
+                                    const GemmArgs& a, int num_sms, cudaStream_t stream);
+cudaError_t expert_gemm_fp8x_prepare();
+// H [rows][F] fp16, rewritten in place as two-term E4M3 rows: row r's 2F
+// bytes become hi (bytes 0..F-1) and lo (F..2F-1) of s_r * h, s_r the largest
+// power of two with s_r * max|h_r| <= 448; inv_s[r] = 1/s_r.
+cudaError_t launch_requant_rows_x2(void* h, int rows, int F, float* inv_s, cudaStream_t stream);
+// Token rows for it: per token a power-of-two scale s (largest with
+// s*max|x| <= 448), hi = e4m3(s*x) and lo = e4m3(s*x - hi) written to each of
+// the token's dispatch rows (xq[pos], xq[lo_row0 + pos], bytes) and
+// inv_s[pos] = 1/s; has_shared: also row T*k + t.
+cudaError_t launch_scatter_x2(const bf16* x, const int* inv, int T, int k, int d, int has_shared, uint8_t* xq,
+                              int lo_row0, float* inv_s, cudaStream_t stream);
 
 // Per-row E4M3 quantisation of bf16 rows: s[r] = max |w[r]| / 448, q = nearest
 // E4M3 (ties to even, saturating) of w / s (fp32 quotient); zero rows: s = 0, q = 0.

@@ -35,6 +35,9 @@ struct moe_handle {
   int tile_gateup;  // 0 = choose per call
   int tile_down;
   bool use_pairs;   // 256-row token tiles on CTA pairs (MOE_PAIR_TILES=0 turns it off)
+  bool fp8_x2;      // FP8 weights: gate/up on E4M3 tensor cores with two-term token rows (MOE_FP8_X2=0: off)
+  int rows_max;     // R = (k+1)*Tmax dispatch rows the row buffer holds
+  float* tok_scale; // [R] FP8 two-term token rows: 1/s of every dispatch row
   int router_tile;  // router token tile, 0 = by T (MOE_ROUTER_TILE = 16, 64, 128 or 256)
   int last_kernels;   // kernels enqueued by the last forward call
   bool fp8;           // E4M3 expert weights with per-row scales (moe_init_fp8)
@@ -78,6 +81,8 @@ struct moe_handle {
                                         // (fp8: E4M3 bytes, boxes 128 x 64 / 128 x 128)
   CUtensorMap map_xp[moe::kNumTileN];   // Xp   as [Rmax][d] bf16 (in yp), box 64 x BN
   CUtensorMap map_h[moe::kNumTileN];    // H    as [Rmax][F], box 64 x BN
+  CUtensorMap map_xq[moe::kNumTileN];   // FP8 two-term token rows as [2*Rmax][d] bytes, box 128 B x BN
+  CUtensorMap map_hq[moe::kNumTileN];   // FP8 two-term H rows as [Rmax][2F] bytes (hi | lo), box 128 B x BN
   // per-stage timing (moe_profile_enable)
   bool profiling;
   int n_prof;
@@ -322,10 +327,11 @@ cudaEvent_t* prof_slot(moe_handle* h) {
 // and yexp.  mean_rows: mean rows per group (picks the token tile width).
 // ev (or NULL): profiling events 3..5 around the two GEMMs.
 int enqueue_ffn(moe_handle* h, moe::GemmArgs a, double mean_rows, const CUtensorMap* map_rows, void* yout,
-                int8_t* yexp, cudaEvent_t* ev, cudaStream_t s, const void* rows2 = nullptr, int n_rows2 = 0) {
+                int8_t* yexp, cudaEvent_t* ev, cudaStream_t s, const void* rows2 = nullptr, int n_rows2 = 0,
+                int n_rows = 0) {
   const moe_config& c = h->cfg;
   const int cap = h->fp8 ? 128 : 256;
-  const int min_tile = h->fp8 ? 64 : 32;
+  const int min_tile = h->fp8 && !h->fp8_x2 ? 64 : 32;
   const int bn1 = h->tile_gateup ? std::min(h->tile_gateup, cap) : choose_tile(mean_rows, cap, min_tile);
   const int bn2 = h->tile_down ? std::min(h->tile_down, cap) : choose_tile(mean_rows, cap, min_tile);
   // 256-row token tiles run on CTA pairs (M = 256 weight rows per pair)
@@ -358,7 +364,12 @@ int enqueue_ffn(moe_handle* h, moe::GemmArgs a, double mean_rows, const CUtensor
   a.out_ld = c.ffn_width;
   const int i1 = tile_index(bn1), i2 = tile_index(bn2);
   a.w_scale = h->s_gate_up;
-  if (h->fp8)
+  if (h->fp8_x2) {
+    a.tok_scale = h->tok_scale;
+    a.lo_row0 = h->rows_max;
+    a.lo_col0 = 0;
+    MOE_CUDA(moe::launch_expert_gemm_fp8x(true, bn1, &h->map_wgu, &h->map_xq[i1], a, h->num_sms, s));
+  } else if (h->fp8)
     MOE_CUDA(moe::launch_expert_gemm_fp8(true, bn1, &h->map_wgu, &map_rows[i1], a, h->num_sms, s));
   else if (pair1)
     MOE_CUDA(moe::launch_expert_gemm_pair(true, &h->map_wgu, &map_rows[i128], map_act2, a, h->num_sms, s));
@@ -375,7 +386,15 @@ int enqueue_ffn(moe_handle* h, moe::GemmArgs a, double mean_rows, const CUtensor
   a.m_tiles = pair2 ? c.d_model / (2 * moe::kBlockM) : c.d_model / moe::kBlockM;
   a.out_ld = c.d_model;
   a.w_scale = h->s_down;
-  if (h->fp8)
+  if (h->fp8_x2) {
+    // H in place as two-term E4M3 rows, their 1/s in tok_scale (gate/up has
+    // read the token scales by now)
+    MOE_CUDA(moe::launch_requant_rows_x2(h->hbuf, n_rows, c.ffn_width, h->tok_scale, s));
+    a.tok_scale = h->tok_scale;
+    a.lo_row0 = 0;
+    a.lo_col0 = c.ffn_width;
+    MOE_CUDA(moe::launch_expert_gemm_fp8x(false, bn2, &h->map_wd, &h->map_hq[i2], a, h->num_sms, s));
+  } else if (h->fp8)
     MOE_CUDA(moe::launch_expert_gemm_fp8(false, bn2, &h->map_wd, &h->map_h[i2], a, h->num_sms, s));
   else if (pair2)
     MOE_CUDA(moe::launch_expert_gemm_pair(false, &h->map_wd, &h->map_h[i128], nullptr, a, h->num_sms, s));
@@ -400,8 +419,12 @@ int enqueue_forward(moe_handle* h, const void* x, int T, CallOpts o, void* y, cu
   // x itself, which its gate/up reads directly.  fp8 weights: every row, as
   // fp16 (the tensor cores' input type there).
   const bool shared_from_x = !h->fp8 && c.has_shared;
-  MOE_CUDA(moe::launch_gather(static_cast<const bf16*>(x), h->inv, T, o.k, c.d_model,
-                              shared_from_x ? 0 : c.has_shared, h->yp, h->fp8, s));
+  if (h->fp8_x2)
+    MOE_CUDA(moe::launch_scatter_x2(static_cast<const bf16*>(x), h->inv, T, o.k, c.d_model, c.has_shared,
+                                    static_cast<uint8_t*>(h->yp), h->rows_max, h->tok_scale, s));
+  else
+    MOE_CUDA(moe::launch_gather(static_cast<const bf16*>(x), h->inv, T, o.k, c.d_model,
+                                shared_from_x ? 0 : c.has_shared, h->yp, h->fp8, s));
   MOE_MARK(3);
   moe::GemmArgs a{};
   a.offsets = h->offsets;
@@ -412,15 +435,16 @@ int enqueue_forward(moe_handle* h, const void* x, int T, CallOpts o, void* y, cu
   a.chunk_base = h->chunk_base;
   a.act2_from = shared_from_x ? T * o.k : -1;
   if (int rc2 = enqueue_ffn(h, a, static_cast<double>(T) * o.k / c.n_experts, h->map_xp, h->yp, h->yexp, ev, s,
-                            x, T))
+                            x, T, T * o.k + (c.has_shared ? T : 0)))
     return rc2;
   MOE_CUDA(moe::launch_combine(static_cast<const __half*>(h->yp), h->yexp, nullptr, nullptr, h->idx, h->inv,
                                h->offsets, h->chunk_base, T, o.k, c.n_experts, c.d_model, c.has_shared, y, c.out_fp32,
                                s));
   MOE_MARK(6);
   // router GEMM, top-k, dispatch, gather, gate/up, down, combine; many
-  // tokens: two more for the chunk histograms and their scan
-  h->last_kernels = moe::chunked_dispatch(T) ? 9 : 7;
+  // tokens: two more for the chunk histograms and their scan; FP8 two-term
+  // rows: one more for the requantisation of H
+  h->last_kernels = (moe::chunked_dispatch(T) ? 9 : 7) + (h->fp8_x2 ? 1 : 0);
   return MOE_OK;
 }
 
@@ -496,7 +520,8 @@ int init_any(const moe_config* cfg, const moe_weights* w, const float* s_gu, con
     return MOE_ERR_INVALID_ARG;
   if (!load_encode()) return MOE_ERR_CUDA;
   if (moe::expert_gemm_prepare() != cudaSuccess || moe::expert_gemm_pair_prepare() != cudaSuccess ||
-      moe::router_gemm_prepare() != cudaSuccess || moe::expert_gemm_fp8_prepare() != cudaSuccess)
+      moe::router_gemm_prepare() != cudaSuccess || moe::expert_gemm_fp8_prepare() != cudaSuccess ||
+      moe::expert_gemm_fp8x_prepare() != cudaSuccess)
     return MOE_ERR_CUDA;
 
   moe_handle* h = new (std::nothrow) moe_handle();
@@ -518,6 +543,8 @@ int init_any(const moe_config* cfg, const moe_weights* w, const float* s_gu, con
   {
     const char* v = std::getenv("MOE_PAIR_TILES");
     h->use_pairs = !(v && v[0] == '0');
+    const char* vx = std::getenv("MOE_FP8_X2");
+    h->fp8_x2 = fp8 && !(vx && vx[0] == '0');
     const int rt = tile_from_env("MOE_ROUTER_TILE");
     h->router_tile = (rt == 16 || rt == 64 || rt == 128 || rt == 256) ? rt : 0;
   }
@@ -549,7 +576,7 @@ int init_any(const moe_config* cfg, const moe_weights* w, const float* s_gu, con
                o_epi = carve(4 * (static_cast<size_t>(ep.max_recv) + 1)),
                o_xs = carve(2 * Tmax * d),
                o_ys = carve((c.out_fp32 ? 4 : 2) * Tmax * d),
-               o_tok = carve(4 * Tmax * (moe::kMaxStatGroups + 1)),
+               o_tok = carve(4 * Tmax * (moe::kMaxStatGroups + 1)), o_tsc = carve(4 * R),
                o_ch = carve(4 * moe::chunk_hist_ints(static_cast<int>(Tmax), E));
   if (cudaMalloc(&h->ws, off) != cudaSuccess) {
     cudaGetLastError();
@@ -573,6 +600,8 @@ int init_any(const moe_config* cfg, const moe_weights* w, const float* s_gu, con
   h->x_stage = reinterpret_cast<bf16*>(b + o_xs);
   h->y_stage = b + o_ys;
   h->tokstats = reinterpret_cast<float*>(b + o_tok);
+  h->tok_scale = reinterpret_cast<float*>(b + o_tsc);
+  h->rows_max = static_cast<int>(R);
   h->chunk_hist = reinterpret_cast<int*>(b + o_ch);
   h->ep_offsets = reinterpret_cast<int*>(b + o_epo);
   h->ep_chunk_base = reinterpret_cast<int*>(b + o_epc);
@@ -590,6 +619,8 @@ int init_any(const moe_config* cfg, const moe_weights* w, const float* s_gu, con
   ok = ok && encode_2d(&h->map_wd, w->w_down, G * d, F, moe::kBlockM, fp8);
   for (int i = 0; ok && i < moe::kNumTileN; ++i) {
     ok = ok && encode_2d(&h->map_xp[i], h->yp, R, d, moe::kTileN[i]);
+    ok = ok && encode_2d(&h->map_xq[i], h->yp, 2 * R, d, moe::kTileN[i], true);
+    ok = ok && encode_2d(&h->map_hq[i], h->hbuf, RH, 2 * F, moe::kTileN[i], true);
     ok = ok && encode_2d(&h->map_h[i], h->hbuf, RH, F, moe::kTileN[i]);
   }
   ok = ok && cudaDeviceSynchronize() == cudaSuccess;

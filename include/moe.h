@@ -91,7 +91,7 @@ int moe_init(const moe_config* cfg, const moe_weights* w, moe_handle** out);
 
 /*
  * FP8 expert weights ("Step3.5 Flash 大模型技术深度解析" §8.1: FP8/FP16 mixed-
- * precision inference; format, scales and the fp16 activations are this
+ * precision inference; format, scales and the activations' form are this
  * library's reading of that line).  Device pointers, borrowed like moe_weights:
  *   w_router   fp32 [E][d]
  *   w_gate_up  [G][2F][d] bytes: OCP FP8 E4M3 codes, same row order as bf16
@@ -111,10 +111,16 @@ typedef struct moe_weights_fp8 {
 
 /*
  * moe_init for FP8 expert weights.  The handle then runs the same calls (route,
- * forward, forward_host, route_stats, ...); inside moe_forward the token rows
- * and H are fp16 and every product accumulates in fp32.  The activations x and
- * the gate output H must lie within the fp16 range (|v| < 65504); x's bf16
- * values in the fp16 normal range are carried over exactly.  Token tiles are
+ * forward, forward_host, route_stats, ...).  Inside moe_forward the E4M3 codes
+ * meet E4M3 activations on the tensor cores: every token row x (and every row
+ * of the gate output H, kept as fp16 in between) is carried as two E4M3 rows,
+ * hi = e4m3(s*v) and lo = e4m3(s*v - hi), with one power-of-two scale s per row
+ * (the largest with s*max|v| <= 448); hi + lo reproduces a bf16 x exactly
+ * except for entries below about 1/1000 of the row's largest (there to within
+ * 2^-18 of it), and H to 8 significant bits.  Products accumulate in fp32 and
+ * the weight row scales and 1/s are applied to the sums.  x and H must lie
+ * within the fp16 range (|v| < 65504).  MOE_FP8_X2=0 in the environment widens
+ * the codes to fp16 on chip instead and keeps x and H as fp16.  Token tiles are
  * at most 128 rows (no CTA-pair tiles).  Same errors as moe_init.
  */
 int moe_init_fp8(const moe_config* cfg, const moe_weights_fp8* w, moe_handle** out);
@@ -292,7 +298,9 @@ int moe_check(moe_handle* h, void* stream);
  * on this handle enqueued (0 after a call with T = 0; otherwise 7: the router
  * GEMM, top-k, dispatch, row gather, gate/up, down and combine kernels, and
  * from 1024 tokens on 9: two more that count each expert's rows per 256-token
- * chunk and scan those counts, in place of counters in the top-k kernel).
+ * chunk and scan those counts, in place of counters in the top-k kernel; one
+ * more on a handle with FP8 weights: the requantisation of H into two-term
+ * E4M3 rows).
  * Host-only, never synchronises.  Returns -1 for an invalid handle.  No
  * counterpart in the pages: instrumentation for launch accounting.
  */

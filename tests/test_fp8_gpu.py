@@ -37,13 +37,17 @@ def test_quantiser_bit_exact():
     np.testing.assert_array_equal(cpu(q), oq)
 
 
-def fp8_case(shape, seed, tiles=(0, 0), n_sample=None, max_tokens=None, out_fp32=False):
+def fp8_case(shape, seed, tiles=(0, 0), n_sample=None, max_tokens=None, out_fp32=False, x2=True):
+    """x2: the gate/up GEMM on E4M3 tensor cores with the token rows as two
+    E4M3 terms (the default), or on fp16 tensor cores with the weights widened
+    (MOE_FP8_X2=0)."""
     import os
     inp = synth.make_inputs(shape, seed=seed, device=DEV)
     q_gu, s_gu, q_d, s_d = quantised(inp)
     inp.w_gate_up = inp.w_down = None  # the bf16 copies are not needed any more
-    old = {k: os.environ.get(k) for k in ("MOE_TILE_N_GATEUP", "MOE_TILE_N_DOWN")}
+    old = {k: os.environ.get(k) for k in ("MOE_TILE_N_GATEUP", "MOE_TILE_N_DOWN", "MOE_FP8_X2")}
     os.environ["MOE_TILE_N_GATEUP"], os.environ["MOE_TILE_N_DOWN"] = str(tiles[0]), str(tiles[1])
+    os.environ["MOE_FP8_X2"] = "1" if x2 else "0"
     try:
         layer = binding.MoeLayer.fp8(inp.w_router, q_gu, s_gu, q_d, s_d, shape.k,
                                      max_tokens or shape.T, has_shared=shape.has_shared, out_fp32=out_fp32)
@@ -74,33 +78,71 @@ def fp8_case(shape, seed, tiles=(0, 0), n_sample=None, max_tokens=None, out_fp32
     return ratio
 
 
-def test_fp8_tiny():
-    fp8_case(synth.TINY, seed=0)
+@pytest.mark.parametrize("x2", [True, False])
+def test_fp8_tiny(x2):
+    fp8_case(synth.TINY, seed=0, x2=x2)
 
 
+@pytest.mark.parametrize("x2", [True, False])
 @pytest.mark.parametrize("tiles", [(16, 16), (32, 32), (64, 64), (128, 128), (16, 128), (128, 16), (256, 256)])
-def test_fp8_tile_widths_ragged(tiles):
+def test_fp8_tile_widths_ragged(tiles, x2):
     # 300 tokens, 16 experts, top-2: ragged tiles of every width; d = 512 gives
     # 4 K steps of 128 per gate/up tile (wraps the 4-slot A ring once)
-    fp8_case(synth.LayerShape(T=300, d=512, E=16, k=2, F=256), seed=21, tiles=tiles)
+    fp8_case(synth.LayerShape(T=300, d=512, E=16, k=2, F=256), seed=21, tiles=tiles, x2=x2)
 
 
-def test_fp8_long_k_and_fp32_output():
+@pytest.mark.parametrize("x2", [True, False])
+def test_fp8_long_k_and_fp32_output(x2):
     # d = 2048: 16 K steps per gate/up tile (rings wrap several times)
-    fp8_case(synth.LayerShape(T=96, d=2048, E=8, k=2, F=256), seed=22, out_fp32=True)
+    fp8_case(synth.LayerShape(T=96, d=2048, E=8, k=2, F=256), seed=22, out_fp32=True, x2=x2)
 
 
-def test_fp8_without_shared_expert():
-    fp8_case(synth.LayerShape(T=50, d=256, E=12, k=3, F=128, has_shared=False), seed=23)
+@pytest.mark.parametrize("x2", [True, False])
+def test_fp8_without_shared_expert(x2):
+    fp8_case(synth.LayerShape(T=50, d=256, E=12, k=3, F=128, has_shared=False), seed=23, x2=x2)
 
 
+def test_fp8_two_term_rows_with_wide_dynamic_range():
+    # token rows whose values span many binades (tiny and huge entries, a zero
+    # row): the per-token power-of-two scale and the lo terms below E4M3's
+    # normal range must still keep the output within the bound
+    shape = synth.LayerShape(T=64, d=256, E=8, k=2, F=128)
+    import os
+    inp = synth.make_inputs(shape, seed=27, device=DEV)
+    inp.x[3] = 0.0
+    inp.x[5] *= 1e-6
+    inp.x[7, :16] *= 300.0
+    inp.x[9, ::3] *= 1e-4
+    q_gu, s_gu, q_d, s_d = quantised(inp)
+    old = os.environ.get("MOE_FP8_X2")
+    os.environ["MOE_FP8_X2"] = "1"
+    try:
+        layer = binding.MoeLayer.fp8(inp.w_router, q_gu, s_gu, q_d, s_d, shape.k, shape.T)
+    finally:
+        if old is None:
+            os.environ.pop("MOE_FP8_X2", None)
+        else:
+            os.environ["MOE_FP8_X2"] = old
+    y = layer.forward(inp.x)
+    assert layer.check() == binding.MOE_OK
+    xb = synth.bf16_bits(inp.x)
+    wr = cpu(inp.w_router)
+    idx, _, _, _, _ = layer.route(inp.x)
+    fp8 = (cpu(q_gu), cpu(s_gu), cpu(q_d), cpu(s_d))
+    check_output(xb, wr, None, None, shape.k, cpu(y.float()), cpu(idx), fp8=fp8)
+    assert torch.all(y[3] == 0) or torch.isfinite(y[3].float()).all()
+    layer.close()
+
+
+@pytest.mark.parametrize("x2", [True, False])
 @pytest.mark.parametrize("T", [1, 128])
-def test_fp8_flash_decode(T):
+def test_fp8_flash_decode(T, x2):
     # d=4096, 288 routed + 1 shared, top-8, width 1280
-    fp8_case(synth.FLASH_DECODE.with_tokens(T), seed=24, n_sample=None if T == 1 else 48)
+    fp8_case(synth.FLASH_DECODE.with_tokens(T), seed=24, n_sample=None if T == 1 else 48, x2=x2)
 
 
-def test_fp8_many_tokens():
+@pytest.mark.parametrize("x2", [True, False])
+def test_fp8_many_tokens(x2):
     # 2000 tokens over 24 experts: chunked dispatch, every row (the shared
-    # expert's too) scattered as fp16, ~170 rows per group in 128-row tiles
-    fp8_case(synth.LayerShape(T=2000, d=512, E=24, k=2, F=256), seed=26, n_sample=64)
+    # expert's too) scattered, ~170 rows per group in 128-row tiles
+    fp8_case(synth.LayerShape(T=2000, d=512, E=24, k=2, F=256), seed=26, n_sample=64, x2=x2)
