@@ -191,24 +191,21 @@ def gateup_flops(shape):
 
 def measured_traffic(args):
     """DRAM bytes per launch of the gate/up GEMM from the committed ncu capture
-    of the decode workload (profiles/gate_up_decode_T128_dram.md); None for
-    other workloads or when the summary is missing."""
-    if args.workload != "decode" or args.experts or args.ffn_width or args.weights != "bf16":
+    of the decode workload (profiles/gate_up_decode_T128_dram.md, or
+    profiles/decode_T128_fp8.md with FP8 weights); None for other workloads or
+    when the summary is missing."""
+    if args.workload != "decode" or args.experts or args.ffn_width:
         return None
-    path = os.path.join(ROOT, "profiles", "gate_up_decode_T128_dram.md")
+    name = "decode_T128_fp8.md" if args.weights == "fp8" else "gate_up_decode_T128_dram.md"
+    path = os.path.join(ROOT, "profiles", name)
     try:
         with open(path) as f:
             for line in f:
                 if line.startswith("traffic_bytes_per_launch:"):
                     return float(line.split(":", 1)[1])
     except OSError:
-        pass
+        return None
     return None
-
-
-def layer_flops(shape):
-    d, F, E, T, k = shape.d, shape.F, shape.E, shape.T, shape.k
-    return T * ((k + (1 if shape.has_shared else 0)) * 6 * d * F + 2 * d * E)
 
 
 def cpu_oracle_rate(inp_host, shape, budget_s: float, max_tokens: int, fp8=None):
