@@ -208,6 +208,11 @@ def measured_traffic(args):
     return None
 
 
+def layer_flops(shape):
+    d, F, E, T, k = shape.d, shape.F, shape.E, shape.T, shape.k
+    return T * ((k + (1 if shape.has_shared else 0)) * 6 * d * F + 2 * d * E)
+
+
 def cpu_oracle_rate(inp_host, shape, budget_s: float, max_tokens: int, fp8=None):
     """CPU oracle throughput (tokens/s) on the batch's tokens in order, in
     chunks, cycling through the batch, until `budget_s` seconds are spent or
