@@ -157,15 +157,18 @@ int tile_index(int tile_n) {
 // Token-tile width for a mean of `mean_rows` rows per routed expert: the
 // smallest width that holds a typical group in one tile, at most `cap`.
 // Token tile width: the smallest listed width (from min_tile on) that holds
-// the mean rows per group with 15 % to spare, at most cap.  The MMAs' N
-// follows each tile's actual rows (rounded up to 16), so a wider tile costs
-// only its shared-memory ring depth: with bf16 weights, 32-row tiles (9 ring
-// stages) ran the decode batch 2.7-2.9 % faster than 16-row tiles (10 stages);
-// with FP8 weights, 64-row tiles (6 weight stages) 2 % faster than 16 (8).
-int choose_tile(double mean_rows, int cap, int min_tile) {
+// the mean rows per group times `slack`, at most cap.  The MMAs' N follows
+// each tile's actual rows (rounded up to 16), so a wider tile costs mostly its
+// shared-memory ring depth (measured on GB300, one call each):
+//  - bf16 weights, decode (3.6 rows per group): 32-row tiles (9 ring stages)
+//    2.7-2.9 % faster than 16-row tiles (10 stages); 512 tokens (14 rows):
+//    64-row tiles 1.3 % faster than 32-row ones;
+//  - FP8 two-term kernel (N = 2 x tile): 64-row tiles at 2048 tokens (57 rows)
+//    6 % faster than 128-row ones (4 stages of 48 KB).
+int choose_tile(double mean_rows, int cap, int min_tile, double slack = 1.15) {
   for (int i = 0; i < moe::kNumTileN; ++i) {
     if (moe::kTileN[i] < min_tile) continue;
-    if (moe::kTileN[i] >= cap || mean_rows * 1.15 <= moe::kTileN[i]) return moe::kTileN[i];
+    if (moe::kTileN[i] >= cap || mean_rows * slack <= moe::kTileN[i]) return moe::kTileN[i];
   }
   return cap;
 }
@@ -331,9 +334,10 @@ int enqueue_ffn(moe_handle* h, moe::GemmArgs a, double mean_rows, const CUtensor
                 int n_rows = 0) {
   const moe_config& c = h->cfg;
   const int cap = h->fp8 ? 128 : 256;
-  const int min_tile = h->fp8 && !h->fp8_x2 ? 64 : 32;
-  const int bn1 = h->tile_gateup ? std::min(h->tile_gateup, cap) : choose_tile(mean_rows, cap, min_tile);
-  const int bn2 = h->tile_down ? std::min(h->tile_down, cap) : choose_tile(mean_rows, cap, min_tile);
+  const int min_tile = (h->fp8 && !h->fp8_x2) || (!h->fp8 && mean_rows >= 8.0) ? 64 : 32;
+  const double slack = h->fp8_x2 ? 1.0 : 1.15;
+  const int bn1 = h->tile_gateup ? std::min(h->tile_gateup, cap) : choose_tile(mean_rows, cap, min_tile, slack);
+  const int bn2 = h->tile_down ? std::min(h->tile_down, cap) : choose_tile(mean_rows, cap, min_tile, slack);
   // 256-row token tiles run on CTA pairs (M = 256 weight rows per pair)
   const int i128 = tile_index(128);
   const bool pair1 = h->use_pairs && bn1 == 256;
