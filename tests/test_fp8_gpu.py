@@ -146,3 +146,25 @@ def test_fp8_many_tokens(x2):
     # 2000 tokens over 24 experts: chunked dispatch, every row (the shared
     # expert's too) scattered, ~170 rows per group in 128-row tiles
     fp8_case(synth.LayerShape(T=2000, d=512, E=24, k=2, F=256), seed=26, n_sample=64, x2=x2)
+
+
+def test_fp8_smaller_top_k_renormalized():
+    # per-call top-4 with renormalised weights on an FP8 handle built for top-8:
+    # the two-term scatter and the requantisation of H follow the call's k
+    shape = synth.LayerShape(T=100, d=256, E=32, k=8, F=128)
+    inp = synth.make_inputs(shape, seed=28, device=DEV)
+    q_gu, s_gu, q_d, s_d = quantised(inp)
+    layer = binding.MoeLayer.fp8(inp.w_router, q_gu, s_gu, q_d, s_d, shape.k, shape.T)
+    y = layer.forward(inp.x, top_k=4, renormalize=True)
+    assert layer.check() == binding.MOE_OK
+    assert layer.last_kernel_count() == 8  # 7 + the requantisation of H
+    xb = synth.bf16_bits(inp.x)
+    wr = cpu(inp.w_router)
+    idx, _, _, _, _ = layer.route(inp.x, top_k=4, renormalize=True)  # the GPU's selection (near-ties)
+    y_ref = oracle.forward_fp8(xb, wr, cpu(q_gu), cpu(s_gu), cpu(q_d), cpu(s_d), 4, sel=cpu(idx),
+                               renormalize=True)
+    rms = np.sqrt((y_ref ** 2).mean())
+    diff = np.abs(cpu(y.float()) - y_ref)
+    bound = 2e-2 * rms + np.ldexp(1.0, np.frexp(np.abs(y_ref))[1] - 9)
+    assert np.all(diff <= bound), f"max err {diff.max():.3e} vs rms {rms:.3e}"
+    layer.close()
