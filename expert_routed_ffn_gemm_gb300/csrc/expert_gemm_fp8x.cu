@@ -86,53 +86,6 @@ struct CfgX {
   static constexpr uint32_t IDESC = idesc_e4m3_f32(kBlockM, 2 * BN);
 };
 
-// The gate/up epilogue of one item: per 16-column chunk, hi + lo, times the
-// weight row's scale and the token's 1/s, then the gate/up exchange and
-// h = silu(g) * u as in epilogue_gateup (gemm_common.cuh).
-template <int BN>
-__device__ __forceinline__ void epilogue_gateup_x2(uint32_t taddr, int row, int feat_base, int row0, int valid,
-                                                   __half* H, int ldh, float* xchg, uint32_t& chunk_par,
-                                                   float scale, const float* __restrict__ tok_scale) {
-  const bool is_gate = row < 64;
-  const int fl = row & 63;
-  const int feat = feat_base + fl;
-#pragma unroll
-  for (int c0 = 0; c0 < BN; c0 += 16) {
-    if (c0 >= valid) break;
-    uint32_t vh[16], vl[16];
-    tmem_ld16(taddr + c0, vh);
-    tmem_ld16(taddr + BN + c0, vl);
-    tmem_ld_wait();
-    float v[16];
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const float ts = (c0 + c < valid) ? __ldg(tok_scale + row0 + c0 + c) : 0.f;
-      v[c] = (__uint_as_float(vh[c]) + __uint_as_float(vl[c])) * (scale * ts);
-    }
-    float* mine_out = xchg + ((chunk_par * 2 + (is_gate ? 1 : 0)) * 64 + fl) * 8;
-    const float* peer_in = xchg + ((chunk_par * 2 + (is_gate ? 0 : 1)) * 64 + fl) * 8;
-    float give[8], keep[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      give[c] = is_gate ? v[8 + c] : v[c];
-      keep[c] = is_gate ? v[c] : v[8 + c];
-    }
-    reinterpret_cast<float4*>(mine_out)[0] = make_float4(give[0], give[1], give[2], give[3]);
-    reinterpret_cast<float4*>(mine_out)[1] = make_float4(give[4], give[5], give[6], give[7]);
-    named_bar_sync(kEpilogueBar, 128);
-    const float4 p0 = reinterpret_cast<const float4*>(peer_in)[0];
-    const float4 p1 = reinterpret_cast<const float4*>(peer_in)[1];
-    const float peer[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-    const int col0 = c0 + (is_gate ? 0 : 8);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const float h = is_gate ? silu_mul(keep[c], peer[c]) : silu_mul(peer[c], keep[c]);
-      if (col0 + c < valid) H[static_cast<size_t>(row0 + col0 + c) * ldh + feat] = __float2half_rn(h);
-    }
-    chunk_par ^= 1u;
-  }
-}
-
 template <bool GATEUP, int BN>
 __global__ void __launch_bounds__(kThreadsX, 1)
     expert_gemm_fp8x_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_tok,
@@ -298,7 +251,7 @@ __global__ void __launch_bounds__(kThreadsX, 1)
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ACC_COLS;
       if (GATEUP)
         epilogue_gateup_x2<BN>(taddr, row, it.m * (kBlockM / 2), row0, valid, static_cast<__half*>(args.out),
-                               args.out_ld, xchg, chunk_par, scale, args.tok_scale);
+                               args.out_ld, xchg, chunk_par, scale, args.tok_scale, BN);
       else
         epilogue_down<BN>(taddr, it.m * kBlockM + row, row0, valid, wreg, static_cast<__half*>(args.out),
                           args.out_exp, args.out_ld, __ldg(args.chunk_base + it.g) + it.n * (BN / kYpRows), scale, BN);

@@ -198,6 +198,54 @@ __device__ __forceinline__ void load_gate_weights(float (&wreg)[(BN + 31) / 32],
 // the block scaled by 2^-e is an fp16 normal or zero below 2^15 (no overflow)
 // carrying 11 significant bits relative to the block's largest value.  Clamped
 // to [-126, kYpExpMax] so that 2^-e and 2^e are fp32 normals.
+// K3 epilogue for two-term E4M3 token rows: per 16-column chunk, the hi term
+// (column c) + the lo term (column lo_off + c), times the weight row's scale
+// and the token's 1/s (tok_scale of the dispatch row), then the gate/up
+// exchange and h = silu(g) * u as in epilogue_gateup; H as fp16.
+template <int BN>
+__device__ __forceinline__ void epilogue_gateup_x2(uint32_t taddr, int row, int feat_base, int row0, int valid,
+                                                   __half* H, int ldh, float* xchg, uint32_t& chunk_par,
+                                                   float scale, const float* __restrict__ tok_scale, int lo_off) {
+  const bool is_gate = row < 64;
+  const int fl = row & 63;
+  const int feat = feat_base + fl;
+#pragma unroll
+  for (int c0 = 0; c0 < BN; c0 += 16) {
+    if (c0 >= valid) break;
+    uint32_t vh[16], vl[16];
+    tmem_ld16(taddr + c0, vh);
+    tmem_ld16(taddr + lo_off + c0, vl);
+    tmem_ld_wait();
+    float v[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const float ts = (c0 + c < valid) ? __ldg(tok_scale + row0 + c0 + c) : 0.f;
+      v[c] = (__uint_as_float(vh[c]) + __uint_as_float(vl[c])) * (scale * ts);
+    }
+    float* mine_out = xchg + ((chunk_par * 2 + (is_gate ? 1 : 0)) * 64 + fl) * 8;
+    const float* peer_in = xchg + ((chunk_par * 2 + (is_gate ? 0 : 1)) * 64 + fl) * 8;
+    float give[8], keep[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      give[c] = is_gate ? v[8 + c] : v[c];
+      keep[c] = is_gate ? v[c] : v[8 + c];
+    }
+    reinterpret_cast<float4*>(mine_out)[0] = make_float4(give[0], give[1], give[2], give[3]);
+    reinterpret_cast<float4*>(mine_out)[1] = make_float4(give[4], give[5], give[6], give[7]);
+    named_bar_sync(kEpilogueBar, 128);
+    const float4 p0 = reinterpret_cast<const float4*>(peer_in)[0];
+    const float4 p1 = reinterpret_cast<const float4*>(peer_in)[1];
+    const float peer[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+    const int col0 = c0 + (is_gate ? 0 : 8);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const float h = is_gate ? silu_mul(keep[c], peer[c]) : silu_mul(peer[c], keep[c]);
+      if (col0 + c < valid) H[static_cast<size_t>(row0 + col0 + c) * ldh + feat] = __float2half_rn(h);
+    }
+    chunk_par ^= 1u;
+  }
+}
+
 __device__ __forceinline__ int block_exponent(uint32_t amax) {
   const int e = static_cast<int>((amax >> 23) & 0xffu) - 141;
   return e < -126 ? -126 : (e > kYpExpMax ? kYpExpMax : e);

@@ -168,3 +168,9 @@ def test_fp8_smaller_top_k_renormalized():
     bound = 2e-2 * rms + np.ldexp(1.0, np.frexp(np.abs(y_ref))[1] - 9)
     assert np.all(diff <= bound), f"max err {diff.max():.3e} vs rms {rms:.3e}"
     layer.close()
+
+
+def test_fp8_two_term_128_row_tiles():
+    # 128-row tiles of the two-term kernel (N = 256, 4 ring stages): ~150 rows
+    # per group, ragged second tiles, d = 1024 gives 8 K steps per gate/up tile
+    fp8_case(synth.LayerShape(T=1200, d=1024, E=16, k=2, F=256), seed=29, tiles=(128, 128), n_sample=64)
