@@ -1,4 +1,4 @@
-// K2 dispatch, the row gather, and K5 combine.
+// K2 dispatch, the row scatter into dispatch order, and K5 combine.
 //
 // "Step3.5 Flash 大模型技术深度解析" (jsqmd.com) §3.2.2: every token runs its 8
 // chosen routed experts plus the shared expert, and the 9 outputs are summed

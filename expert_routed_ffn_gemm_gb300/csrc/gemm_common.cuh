@@ -22,8 +22,9 @@ struct Item {
 
 // item -> (group, token tile inside the group, weight tile); tile_start[g] is
 // the first token tile of group g (prefix over groups of ceil(rows/tile)).
-// With `reverse` the items run from the last group to the first (see the
-// gate/up launch: the rows written last by the gather are the ones still in L2).
+// With `reverse` the items run from the last group to the first (the gate/up
+// launch: the H rows it writes last are the first groups', which the down
+// projection reads first).
 __device__ __forceinline__ Item decode_item(int item, int m_tiles, const int* tile_start, int G, int n_items,
                                             int reverse) {
   if (reverse) item = n_items - 1 - item;

@@ -1,7 +1,7 @@
 // C ABI of libmoe.so (declared in include/moe.h): argument checks, workspace,
 // TMA descriptors and the launch sequence of the layer of "Step3.5 Flash
 // 大模型技术深度解析" (jsqmd.com) §3.2.1-§3.2.2:
-//   router (K1) -> dispatch (K2) -> row gather -> gate/up GEMM (K3)
+//   router (K1) -> dispatch (K2) -> row scatter -> gate/up GEMM (K3)
 //   -> down GEMM (K4) -> combine (K5),
 // all enqueued on the caller's stream with no host synchronisation.
 #include <cudaTypedefs.h>
@@ -357,9 +357,9 @@ int enqueue_ffn(moe_handle* h, moe::GemmArgs a, double mean_rows, const CUtensor
   a.wait_limit_ns = h->wait_limit_ns;
   a.F = c.ffn_width;
 
-  // gate/up runs its items last group first: the gather wrote the rows of the
-  // last groups last, so they are the ones still in L2; the down projection
-  // then runs first group first, over the H rows gate/up wrote last
+  // gate/up runs its items last group first, so the H rows it writes last are
+  // those of the first groups, which the down projection (first group first)
+  // then reads while they are still in L2
   a.reverse = 1;
   a.out = h->hbuf;
   a.K = c.d_model;
