@@ -129,3 +129,29 @@ def test_forward_fp8_of_quantised_weights_tracks_bf16_forward():
     y16 = oracle.forward(xb, wr, gu_bits, d_bits, shape.k)
     rel = np.sqrt(((y8 - y16) ** 2).mean()) / np.sqrt((y16 ** 2).mean())
     assert 1e-3 < rel < 5e-2
+
+
+def test_two_term_e4m3_rows_reproduce_bf16_values():
+    # The reading behind the FP8 kernels' activations: with s the largest power
+    # of two keeping s*max|x| <= 448, hi = e4m3(s*x) and lo = e4m3(s*x - hi)
+    # give hi + lo == s*x exactly for a bf16 x whenever |s*x| >= 2^-2 (the
+    # remainder of an 8-bit significand after rounding to 4 bits has at most 4
+    # bits, and its lowest bit stays on E4M3's 2^-9 grid), and within 2^-10
+    # below that.  Checked with the oracle's codec (pinned above) on bf16 rows
+    # spanning many binades.
+    rng = np.random.default_rng(11)
+    rows = rng.standard_normal((64, 512)) * np.exp2(rng.integers(-30, 30, size=(64, 1)))
+    rows *= np.exp2(rng.integers(-12, 3, size=rows.shape))  # entries far below the row maximum
+    x = torch.from_numpy(rows.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    amax = np.abs(x).max(axis=1, keepdims=True)
+    e = np.floor(np.log2(448.0 / amax))
+    s = np.exp2(e)
+    assert np.all(s * amax <= 448.0) and np.all(2 * s * amax > 448.0)
+    v = x * s  # exact: power-of-two scaling
+    hi = oracle.e4m3_decode(oracle.e4m3_encode(v.astype(np.float32)))
+    lo = oracle.e4m3_decode(oracle.e4m3_encode((v - hi).astype(np.float32)))
+    err = np.abs(hi + lo - v)
+    big = np.abs(v) >= 0.25
+    assert big.sum() > 1000 and (~big).sum() > 1000
+    assert np.all(err[big] == 0.0)
+    assert np.all(err[~big] <= 2.0 ** -10)
