@@ -8,12 +8,14 @@ d=4096, 288+1 experts, top-8, expert width 1280 (bf16 weights, 9.09 GB).
 Prints one JSON line.  `value` = tokens/s over the timed steps (device time,
 CUDA events, inputs resident in HBM); `e2e` = the same through the host-buffer
 entry point (pinned host x in, host y out, copies inside the timed region);
-`roofline` = the gate/up grouped GEMM (the dominant kernel) against the
-measured HBM copy bandwidth; `cpu_baseline` = the CPU oracle on a bounded
-sample of the same workload.
+`roofline` = the gate/up grouped GEMM (the dominant kernel) against its binding
+roof (HBM copy bandwidth or sustained bf16 tensor rate), its time from a
+second pass of the same steps with per-stage events; `cpu_baseline` = the CPU
+oracle on a bounded sample of the same workload.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
-                  [--workload decode|prefill|skew|T=<n>]
+                  [--workload decode|prefill|skew|T=<n>] [--weights bf16|fp8]
+                  [--experts E] [--ffn-width F] [--no-cpu-baseline]
 
 Multi-GPU (torchrun, one rank per GPU): every rank runs its own replica of
 the layer on its own batch (weak scaling, no data-path collective); the
