@@ -548,7 +548,8 @@ int init_any(const moe_config* cfg, const moe_weights* w, const float* s_gu, con
     const char* v = std::getenv("MOE_PAIR_TILES");
     h->use_pairs = !(v && v[0] == '0');
     const char* vx = std::getenv("MOE_FP8_X2");
-    h->fp8_x2 = fp8 && !(vx && vx[0] == '0');
+    // the in-place requantisation of H holds a row in registers: F <= 8192
+    h->fp8_x2 = fp8 && !(vx && vx[0] == '0') && c.ffn_width <= 8192;
     const int rt = tile_from_env("MOE_ROUTER_TILE");
     h->router_tile = (rt == 16 || rt == 64 || rt == 128 || rt == 256) ? rt : 0;
   }
