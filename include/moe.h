@@ -119,8 +119,9 @@ typedef struct moe_weights_fp8 {
  * except for entries below about 1/1000 of the row's largest (there to within
  * 2^-18 of it), and H to 8 significant bits.  Products accumulate in fp32 and
  * the weight row scales and 1/s are applied to the sums.  x and H must lie
- * within the fp16 range (|v| < 65504).  MOE_FP8_X2=0 in the environment widens
- * the codes to fp16 on chip instead and keeps x and H as fp16.  Token tiles are
+ * within the fp16 range (|v| < 65504).  MOE_FP8_X2=0 in the environment (and
+ * ffn_width > 8192) widens the codes to fp16 on chip instead and keeps x and H
+ * as fp16.  Token tiles are
  * at most 128 rows (no CTA-pair tiles).  Same errors as moe_init.
  */
 int moe_init_fp8(const moe_config* cfg, const moe_weights_fp8* w, moe_handle** out);
