@@ -110,15 +110,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  const int n_items = tile_start[G] * args.m_tiles;
+  const int n_base = tile_start[G] * args.m_tiles;
+  const int ks = (BN <= 32 && args.ksplit > 1 && n_base * args.ksplit <= args.ksplit_cap) ? args.ksplit : 1;
+  const int n_items = n_base * ks;  // work items: (item, K part), the parts of an item adjacent
   const uint64_t limit = args.wait_limit_ns;
+  // K steps of part p of an item: [p * k_per, min(k_steps, (p + 1) * k_per)),
+  // never empty (the host picks ks so that every part has one)
+  const int k_steps_all = args.K / kBlockK;
+  const int k_per = (k_steps_all + ks - 1) / ks;
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------------- producer --
       const uint64_t pol_w = policy_evict_first();   // weights: streamed once
       const uint64_t pol_act = policy_evict_last();  // token rows: re-read by the other weight tiles
-      const int k_steps = args.K / kBlockK;
       // K3: gate rows 64m.. of group g, then the up rows F + 64m..; K4: rows 128m..
       auto weight_row = [&](const Item& it) {
         return weight_group(args, it.g) * args.rows_per_group + it.m * (GATEUP ? kBlockM / 2 : kBlockM);
@@ -127,10 +132,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       long issued = 0;
       bool ok = true;
       for (int item = blockIdx.x; ok && item < n_items && !*abort_flag; item += gridDim.x) {
-        const Item it = decode_item(item, args.m_tiles, tile_start, G, n_items, args.reverse);
+        const Item it = decode_item(item / ks, args.m_tiles, tile_start, G, n_items / ks, args.reverse);
         const int row_w = weight_row(it);
         const int row_act = __ldg(args.offsets + it.g) + it.n * BN;
-        for (int kb = 0; kb < k_steps; ++kb) {
+        const int part = item % ks;
+        const int kb1 = min(k_steps_all, (part + 1) * k_per);
+        for (int kb = part * k_per; kb < kb1; ++kb) {
           if (!wait_or_abort(&empty[stage], phase ^ 1u, limit, abort_flag)) {
             record_abort(abort_flag, args.err);
             ok = false;
@@ -162,22 +169,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // --------------------------------------------------------------- MMA --
-      const int k_steps = args.K / kBlockK;
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool issued_any = false, ok = true;
       // N of the MMAs: the tile's rows rounded up to 16 (ragged tails); the
       // next item's descriptor is worked out while this item's MMAs run
-      uint32_t next_idesc =
-          item_idesc(blockIdx.x, n_items, args.reverse, args.m_tiles, tile_start, G, args.offsets, kBlockM, 16, BN);
+      auto idesc_of = [&](int item) {
+        return item < n_items ? item_idesc(item / ks, n_items / ks, args.reverse, args.m_tiles, tile_start, G,
+                                           args.offsets, kBlockM, 16, BN)
+                              : 0u;
+      };
+      uint32_t next_idesc = idesc_of(blockIdx.x);
       for (int item = blockIdx.x; ok && item < n_items && !*abort_flag; item += gridDim.x) {
         const uint32_t idesc = next_idesc;
+        const int part = item % ks;
+        const int kb0 = part * k_per, kb1 = min(k_steps_all, (part + 1) * k_per);
         if (!wait_or_abort(&acc_empty[acc], acc_phase ^ 1u, limit, abort_flag)) {
           record_abort(abort_flag, args.err);
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < k_steps; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_or_abort(&full[stage], phase, limit, abort_flag)) {
             record_abort(abort_flag, args.err);
             ok = false;
@@ -189,16 +201,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t b = smem_desc_sw128(st + C::A_BYTES);
 #pragma unroll
           for (int kk = 0; kk < kBlockK / 16; ++kk)  // +32 B along K = +2 in the address field
-            tc_mma_bf16(d_tmem, a + 2 * kk, b + 2 * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            tc_mma_bf16(d_tmem, a + 2 * kk, b + 2 * kk, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
           issued_any = true;
           tc_commit(&empty[stage]);
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
-          if (kb == 0)
-            next_idesc = item_idesc(item + gridDim.x, n_items, args.reverse, args.m_tiles, tile_start, G, args.offsets, kBlockM,
-                                    16, BN);
+          if (kb == kb0) next_idesc = idesc_of(item + gridDim.x);
         }
         if (!ok) break;
         tc_commit(&acc_full[acc]);
@@ -218,8 +228,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
     uint32_t acc = 0, acc_phase = 0, it_par = 0, chunk_par = 0;
+    volatile int* s_last = reinterpret_cast<volatile int*>(tmem_holder + 2);
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-      const Item it = decode_item(item, args.m_tiles, tile_start, G, n_items, args.reverse);
+      const Item it = decode_item(item / ks, args.m_tiles, tile_start, G, n_items / ks, args.reverse);
       const int g_row0 = __ldg(args.offsets + it.g);
       const int g_rows = __ldg(args.offsets + it.g + 1) - g_row0;
       const int row0 = g_row0 + it.n * BN;
@@ -230,6 +241,84 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!epilogue_wait(&acc_full[acc], acc_phase, limit, abort_flag, s_ok, it_par, q, lane, args.err)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      if constexpr (BN <= 32) {
+        if (ks > 1) {
+          // this part's accumulator row to the part buffer, tensor memory back
+          // to the MMA, then the last part of the item sums the parts in order
+          float* mine = args.ksplit_part + (static_cast<size_t>(item) * kBlockM + row) * BN;
+#pragma unroll
+          for (int c0 = 0; c0 < BN; c0 += 16) {
+            if (c0 >= valid) break;  // the epilogue reads the 16-column chunks holding valid columns
+            uint32_t v[16];
+            tmem_ld16(taddr + c0, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 16; c += 4)
+              __stcg(reinterpret_cast<float4*>(mine + c0 + c),
+                     make_float4(__uint_as_float(v[c]), __uint_as_float(v[c + 1]), __uint_as_float(v[c + 2]),
+                                 __uint_as_float(v[c + 3])));
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[acc]);
+          if (++acc == C::NACC) {
+            acc = 0;
+            acc_phase ^= 1u;
+          }
+          // the part is published by one release after the CTA barrier (the
+          // cumulative fence covers the rows the other threads wrote)
+          named_bar_sync(kEpilogueBar, 128);
+          const int base = item / ks;
+          if (q == 0 && lane == 0) {
+            __threadfence();
+            const int last = atomicAdd(args.ksplit_cnt + base, 1) == ks - 1;
+            if (last) __threadfence();  // acquire: the other parts' rows are visible
+            *s_last = last;
+          }
+          named_bar_sync(kEpilogueBar, 128);
+          if (*s_last) {
+            float sum[BN];
+            const float* src = args.ksplit_part + (static_cast<size_t>(base * ks) * kBlockM + row) * BN;
+#pragma unroll
+            for (int c0 = 0; c0 < BN; c0 += 16) {
+              if (c0 >= valid) break;
+              // every part's 16 columns in flight at once, summed in part order
+              float4 f[kMaxGemmKSplit][4];
+#pragma unroll
+              for (int p = 0; p < kMaxGemmKSplit; ++p)
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  f[p][j] = p < ks ? __ldcg(reinterpret_cast<const float4*>(
+                                         src + static_cast<size_t>(p) * kBlockM * BN + c0 + 4 * j))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                float4 a = f[0][j];
+#pragma unroll
+                for (int p = 1; p < kMaxGemmKSplit; ++p) {
+                  a.x += f[p][j].x;
+                  a.y += f[p][j].y;
+                  a.z += f[p][j].z;
+                  a.w += f[p][j].w;
+                }
+                sum[c0 + 4 * j] = a.x;
+                sum[c0 + 4 * j + 1] = a.y;
+                sum[c0 + 4 * j + 2] = a.z;
+                sum[c0 + 4 * j + 3] = a.w;
+              }
+            }
+            if (GATEUP)
+              epilogue_gateup<BN>(0u, row, it.m * (kBlockM / 2), row0, valid, static_cast<bf16*>(args.out),
+                                  args.out_ld, xchg, chunk_par, 1.0f, sum);
+            else
+              epilogue_down<BN>(0u, it.m * kBlockM + row, row0, valid, wreg, static_cast<__half*>(args.out),
+                                args.out_exp, args.out_ld, __ldg(args.chunk_base + it.g) + it.n * (BN / kYpRows),
+                                1.0f, 0, sum);
+            if (q == 0 && lane == 0) args.ksplit_cnt[base] = 0;  // ready for the next launch
+          }
+          continue;
+        }
+      }
       if (GATEUP) {
         // rows 0..63: gate of feature 64m + row; rows 64..127: up of feature 64m + row - 64
         epilogue_gateup<BN>(taddr, row, it.m * (kBlockM / 2), row0, valid, static_cast<bf16*>(args.out),

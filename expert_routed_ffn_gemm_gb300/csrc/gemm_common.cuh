@@ -144,10 +144,12 @@ __device__ __forceinline__ __half to_out(float v, __half*) { return __float2half
 // hands back 0..7; H[row0 + col][feat_base + (row & 63)] = silu(g) * u, where
 // g and u are the accumulators times the `scale` of their own weight row (1
 // for bf16 weights).  H is bf16 or fp16 (OutT).
+// vals (or NULL): this thread's row of the accumulator, already summed over K
+// parts, used in place of tensor memory.
 template <int BN, typename OutT>
 __device__ __forceinline__ void epilogue_gateup(uint32_t taddr, int row, int feat_base, int row0, int valid,
                                                 OutT* H, int ldh, float* xchg, uint32_t& chunk_par,
-                                                float scale = 1.0f) {
+                                                float scale = 1.0f, const float* vals = nullptr) {
   const bool is_gate = row < 64;
   const int fl = row & 63;
   const int feat = feat_base + fl;
@@ -155,8 +157,13 @@ __device__ __forceinline__ void epilogue_gateup(uint32_t taddr, int row, int fea
   for (int c0 = 0; c0 < BN; c0 += 16) {
     if (c0 >= valid) break;
     uint32_t v[16];
-    tmem_ld16(taddr + c0, v);
-    tmem_ld_wait();
+    if (vals != nullptr) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) v[c] = __float_as_uint(vals[c0 + c]);
+    } else {
+      tmem_ld16(taddr + c0, v);
+      tmem_ld_wait();
+    }
     float* mine_out = xchg + ((chunk_par * 2 + (is_gate ? 1 : 0)) * 64 + fl) * 8;
     const float* peer_in = xchg + ((chunk_par * 2 + (is_gate ? 0 : 1)) * 64 + fl) * 8;
     float give[8], keep[8];  // compile-time register indices only
@@ -264,15 +271,24 @@ __device__ __forceinline__ int block_exponent(uint32_t amax) {
 template <int BN>
 __device__ __forceinline__ void epilogue_down(uint32_t taddr, int feat, int row0, int valid,
                                               const float (&wreg)[(BN + 31) / 32], __half* Y, int8_t* Ye, int ldy,
-                                              int chunk0, float row_scale = 1.0f, int lo_off = 0) {
+                                              int chunk0, float row_scale = 1.0f, int lo_off = 0,
+                                              const float* vals = nullptr) {
   static_assert(kYpRows == 16, "one exponent chunk per 16-column TMEM load");
 #pragma unroll
   for (int c0 = 0; c0 < BN; c0 += 16) {
     if (c0 >= valid) break;
     uint32_t v[16], vl[16];
-    tmem_ld16(taddr + c0, v);
-    if (lo_off > 0) tmem_ld16(taddr + lo_off + c0, vl);
-    tmem_ld_wait();
+    if (vals != nullptr) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        v[c] = __float_as_uint(vals[c0 + c]);
+        vl[c] = 0u;
+      }
+    } else {
+      tmem_ld16(taddr + c0, v);
+      if (lo_off > 0) tmem_ld16(taddr + lo_off + c0, vl);
+      tmem_ld_wait();
+    }
     float y[16];
     uint32_t amax = 0;
 #pragma unroll

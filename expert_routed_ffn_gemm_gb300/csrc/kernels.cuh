@@ -47,6 +47,7 @@ constexpr int kBlockK = 64;   // K elements per pipeline stage (one 128-byte swi
 constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 32;
 constexpr int kMaxKSplit = 16;  // K splits of the router GEMM
+constexpr int kMaxGemmKSplit = 4;  // K parts of the bf16 expert GEMMs (small token counts)
 constexpr int kMaxStatGroups = 64;  // expert groups of the routing statistics
 
 // Expert outputs Yp (one row per dispatch position) are kept as fp16 with a
@@ -127,6 +128,16 @@ struct GemmArgs {
   int reverse;         // 1: work items in reverse order (last group first)
   int w_group_base;    // weights of group g: w_group_base + (w_group_mod ? g % w_group_mod : g)
   int w_group_mod;
+  // K split (bf16 single-CTA kernels, few work items): ksplit > 1 cuts every
+  // item's K range into ksplit parts run as separate items; each part writes
+  // its fp32 accumulator to ksplit_part and the last part to finish (counted
+  // in ksplit_cnt, which it resets) sums the parts in part order and runs the
+  // epilogue on the sum.  With more part items than ksplit_cap, or token tiles
+  // wider than 32, the kernel runs unsplit.
+  int ksplit;
+  int ksplit_cap;      // part items ksplit_part and ksplit_cnt hold
+  float* ksplit_part;  // [ksplit_cap][128][BN]
+  int* ksplit_cnt;     // [ksplit_cap], zero between launches
   const float* tok_scale;  // FP8 gate/up with two-term tokens: 1/s of every dispatch row
   int lo_row0, lo_col0;    // ... and where the lo terms of dispatch row 0 sit in the token map
   int act2_from;       // bf16 kernels: token rows from this dispatch position on come through

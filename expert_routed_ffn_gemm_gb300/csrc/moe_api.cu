@@ -36,6 +36,10 @@ struct moe_handle {
   int tile_down;
   bool use_pairs;   // 256-row token tiles on CTA pairs (MOE_PAIR_TILES=0 turns it off)
   bool fp8_x2;      // FP8 weights: gate/up on E4M3 tensor cores with two-term token rows (MOE_FP8_X2=0: off)
+  int gemm_ksplit;  // K split of the bf16 expert GEMMs: -1 = by work items, 1 = off, 2..4 = forced
+  int ksplit_cap;   // work items (item, K part) the part buffer holds
+  float* ksplit_part;  // [ksplit_cap][128][32] fp32 partial accumulators
+  int* ksplit_cnt;     // [ksplit_cap] parts finished per item (zero between launches)
   int rows_max;     // R = (k+1)*Tmax dispatch rows the row buffer holds
   float* tok_scale; // [R] FP8 two-term token rows: 1/s of every dispatch row
   int router_tile;  // router token tile, 0 = by T (MOE_ROUTER_TILE = 16, 64, 128 or 256)
@@ -329,6 +333,36 @@ cudaEvent_t* prof_slot(moe_handle* h) {
 // behind map_rows (one map per tile width) into H, then down into yout (fp16)
 // and yexp.  mean_rows: mean rows per group (picks the token tile width).
 // ev (or NULL): profiling events 3..5 around the two GEMMs.
+// K parts for a bf16 single-CTA expert GEMM with token tile bn.  The work
+// items (weight tiles x token tiles, at most items_ub) run in waves over the
+// SMs; with few items the last wave leaves SMs idle and cutting every item's
+// K range into ks parts evens the load.  Estimated time: waves of part items
+// x (K steps per part + a fixed cost per item worth kItemSteps K steps, which
+// covers the pipeline start and the part reduction); the split is taken when
+// it beats the unsplit estimate by 5 %.
+int choose_ksplit(const moe_handle* h, int bn, long long items_ub, int k_steps) {
+  if (h->fp8 || bn > 32 || h->gemm_ksplit == 1 || items_ub <= 0) return 1;
+  const int sms = h->num_sms;
+  auto fits = [&](int ks) {  // every part has a K step and the part buffer room
+    return (ks - 1) * ((k_steps + ks - 1) / ks) < k_steps && items_ub * ks <= h->ksplit_cap;
+  };
+  if (h->gemm_ksplit >= 2) return fits(h->gemm_ksplit) ? h->gemm_ksplit : 1;
+  constexpr double kItemSteps = 8.0;
+  auto cost = [&](int ks) {
+    return static_cast<double>((items_ub * ks + sms - 1) / sms) * (static_cast<double>(k_steps) / ks + kItemSteps);
+  };
+  const double base = cost(1);
+  int best = 1;
+  double best_cost = base;
+  for (int ks = 2; ks <= moe::kMaxGemmKSplit && fits(ks); ++ks) {
+    if (cost(ks) < best_cost) {
+      best = ks;
+      best_cost = cost(ks);
+    }
+  }
+  return best_cost < 0.95 * base ? best : 1;
+}
+
 int enqueue_ffn(moe_handle* h, moe::GemmArgs a, double mean_rows, const CUtensorMap* map_rows, void* yout,
                 int8_t* yexp, cudaEvent_t* ev, cudaStream_t s, const void* rows2 = nullptr, int n_rows2 = 0,
                 int n_rows = 0) {
@@ -356,6 +390,12 @@ int enqueue_ffn(moe_handle* h, moe::GemmArgs a, double mean_rows, const CUtensor
   a.err = h->err;
   a.wait_limit_ns = h->wait_limit_ns;
   a.F = c.ffn_width;
+  a.ksplit_part = h->ksplit_part;
+  a.ksplit_cnt = h->ksplit_cnt;
+  a.ksplit_cap = h->ksplit_cap;
+  // token tiles: at most one per group that has rows plus rows / bn
+  const long long rows = n_rows > 0 ? n_rows : std::llround(mean_rows * a.G);
+  auto tiles_ub = [&](int bn) { return std::min<long long>(a.G, rows) + rows / bn; };
 
   // gate/up runs its items last group first, so the H rows it writes last are
   // those of the first groups, which the down projection (first group first)
@@ -377,8 +417,10 @@ int enqueue_ffn(moe_handle* h, moe::GemmArgs a, double mean_rows, const CUtensor
     MOE_CUDA(moe::launch_expert_gemm_fp8(true, bn1, &h->map_wgu, &map_rows[i1], a, h->num_sms, s));
   else if (pair1)
     MOE_CUDA(moe::launch_expert_gemm_pair(true, &h->map_wgu, &map_rows[i128], map_act2, a, h->num_sms, s));
-  else
+  else {
+    a.ksplit = choose_ksplit(h, bn1, tiles_ub(bn1) * a.m_tiles, a.K / moe::kBlockK);
     MOE_CUDA(moe::launch_expert_gemm(true, bn1, &h->map_wgu, &map_rows[i1], map_act2, a, h->num_sms, s));
+  }
   MOE_MARK(4);
 
   a.reverse = 0;
@@ -402,8 +444,10 @@ int enqueue_ffn(moe_handle* h, moe::GemmArgs a, double mean_rows, const CUtensor
     MOE_CUDA(moe::launch_expert_gemm_fp8(false, bn2, &h->map_wd, &h->map_h[i2], a, h->num_sms, s));
   else if (pair2)
     MOE_CUDA(moe::launch_expert_gemm_pair(false, &h->map_wd, &h->map_h[i128], nullptr, a, h->num_sms, s));
-  else
+  else {
+    a.ksplit = choose_ksplit(h, bn2, tiles_ub(bn2) * a.m_tiles, a.K / moe::kBlockK);
     MOE_CUDA(moe::launch_expert_gemm(false, bn2, &h->map_wd, &h->map_h[i2], nullptr, a, h->num_sms, s));
+  }
   MOE_MARK(5);
   return MOE_OK;
 }
@@ -550,6 +594,9 @@ int init_any(const moe_config* cfg, const moe_weights* w, const float* s_gu, con
     const char* vx = std::getenv("MOE_FP8_X2");
     // the in-place requantisation of H holds a row in registers: F <= 8192
     h->fp8_x2 = fp8 && !(vx && vx[0] == '0') && c.ffn_width <= 8192;
+    const char* vk = std::getenv("MOE_GEMM_KSPLIT");
+    const int ksv = vk ? std::atoi(vk) : -1;
+    h->gemm_ksplit = (vk == nullptr || ksv < 0) ? -1 : (ksv <= 1 ? 1 : std::min(ksv, moe::kMaxGemmKSplit));
     const int rt = tile_from_env("MOE_ROUTER_TILE");
     h->router_tile = (rt == 16 || rt == 64 || rt == 128 || rt == 256) ? rt : 0;
   }
@@ -572,8 +619,11 @@ int init_any(const moe_config* cfg, const moe_weights* w, const float* s_gu, con
     off = align_up(off + bytes, 256);
     return at;
   };
+  // K split part buffer: up to 8 waves of part items of token tile <= 32
+  h->ksplit_cap = 8 * h->num_sms;
+  const size_t kcap = static_cast<size_t>(h->ksplit_cap);
   const size_t o_counts = carve(4 * E), o_err = carve(16), o_offsets = carve(4 * (E + 2)),
-               o_partial = carve(4 * p_rows * E), o_w3 = carve(2 * 3 * e_pad * d), o_idx = carve(4 * Tmax * k),
+               o_kcnt = carve(4 * kcap), o_partial = carve(4 * p_rows * E), o_w3 = carve(2 * 3 * e_pad * d), o_idx = carve(4 * Tmax * k),
                o_prob = carve(4 * Tmax * k), o_perm = carve(4 * Tmax * k), o_inv = carve(4 * Tmax * k),
                o_yp = carve(2 * R * d), o_ye = carve((R / moe::kYpRows + E + 2) * d), o_cb = carve(4 * (E + 2)),
                o_h = carve(2 * RH * F),
@@ -582,7 +632,8 @@ int init_any(const moe_config* cfg, const moe_weights* w, const float* s_gu, con
                o_xs = carve(2 * Tmax * d),
                o_ys = carve((c.out_fp32 ? 4 : 2) * Tmax * d),
                o_tok = carve(4 * Tmax * (moe::kMaxStatGroups + 1)), o_tsc = carve(4 * R),
-               o_ch = carve(4 * moe::chunk_hist_ints(static_cast<int>(Tmax), E));
+               o_ch = carve(4 * moe::chunk_hist_ints(static_cast<int>(Tmax), E)),
+               o_kpart = carve(4 * kcap * moe::kBlockM * 32);
   if (cudaMalloc(&h->ws, off) != cudaSuccess) {
     cudaGetLastError();
     delete h;
@@ -608,12 +659,14 @@ int init_any(const moe_config* cfg, const moe_weights* w, const float* s_gu, con
   h->tok_scale = reinterpret_cast<float*>(b + o_tsc);
   h->rows_max = static_cast<int>(R);
   h->chunk_hist = reinterpret_cast<int*>(b + o_ch);
+  h->ksplit_cnt = reinterpret_cast<int*>(b + o_kcnt);
+  h->ksplit_part = reinterpret_cast<float*>(b + o_kpart);
   h->ep_offsets = reinterpret_cast<int*>(b + o_epo);
   h->ep_chunk_base = reinterpret_cast<int*>(b + o_epc);
   h->ep_chunks_src = reinterpret_cast<int*>(b + o_eps);
   h->ep_iota = reinterpret_cast<int*>(b + o_epi);
 
-  bool ok = cudaMemset(h->ws, 0, o_partial) == cudaSuccess;  // counts, error word, offsets
+  bool ok = cudaMemset(h->ws, 0, o_partial) == cudaSuccess;  // counts, error word, offsets, K split counters
   ok = ok && moe::launch_split_router(w->w_router, c.n_experts, c.d_model, static_cast<int>(e_pad), h->w3,
                                       nullptr) == cudaSuccess;
   // weight groups held by this handle: all, or (EP) the local experts + shared

@@ -234,7 +234,9 @@ int moe_route(moe_handle* h, const void* x, int T, int* idx, float* prob, int* p
  * expert as one more group), and the gate-weighted combine
  *   y[t] = sum_{j<k} prob[t][j] * y_{idx[t][j]}(x_t)  +  y_shared(x_t),
  * summed in slot order then the shared expert, in fp32, without atomics
- * (bit-identical run to run).
+ * (bit-identical run to run).  With few tokens the bf16 expert GEMMs may cut
+ * K into parts (MOE_GEMM_KSPLIT in the environment: 1 = never, 2..4 = that
+ * many); the parts are summed in a fixed order, so this holds there too.
  *   x  bf16 [T][d], device;  y  [T][d] bf16 or fp32 (cfg.out_fp32), device.
  * 0 <= T <= max_tokens; T == 0 enqueues nothing.
  */

@@ -123,6 +123,26 @@ def test_chunked_dispatch_ties_and_one_hot():
     run_and_check(inp, tokens=64)
 
 
+@pytest.mark.parametrize("parts", ["2", "3", "4", "auto"])
+@pytest.mark.parametrize("T,d,F,tiles", [(1, 256, 128, (32, 32)), (3, 512, 256, (16, 32)),
+                                         (20, 512, 256, (16, 16)), (7, 256, 128, (32, 16))])
+def test_gemm_k_split(parts, T, d, F, tiles):
+    # Few work items: every item's K range in 2..4 parts (fewer where K has
+    # fewer steps of 64), summed in part order by the last part to finish.
+    shape = synth.LayerShape(T=T, d=d, E=16, k=2, F=F)
+    inp = synth.make_inputs(shape, seed=70 + T + d // 128)
+    env = {} if parts == "auto" else {"MOE_GEMM_KSPLIT": parts}
+    layer, x = make_layer(inp, tiles=tiles, env=env)
+    y1 = layer.forward(x)
+    y2 = layer.forward(x)
+    assert layer.check() == binding.MOE_OK
+    assert torch.equal(y1, y2)  # fixed summation order: run to run identical
+    xb, wr, wgu, wd = host_bits(inp)
+    idx, prob, perm, offsets, gap = layer.route(x)
+    check_output(xb, wr, wgu, wd, shape.k, cpu(y1.float()), cpu(idx), tokens=np.arange(T, dtype=np.int32))
+    layer.close()
+
+
 def test_several_weight_tiles_and_k_steps():
     # F = 256 -> 2 gate/up weight tiles, d = 512 -> 4 down weight tiles and 8 K steps.
     shape = synth.LayerShape(T=200, d=512, E=32, k=4, F=256)
