@@ -44,29 +44,34 @@ __device__ __forceinline__ Item decode_item(int item, int m_tiles, const int* ti
   return it;
 }
 
-// tile_start[0..G] from the dispatch offsets, by one warp: each lane scans a
-// contiguous run of groups, then a warp prefix sum.
+// tile_start[0..G] from the dispatch offsets, by one warp: lane l takes
+// groups 32c + l; the tile counts of eight such runs of 32 groups are loaded
+// together (coalesced, one load latency per eight runs), then each run is a
+// warp prefix sum on top of the running total.
 __device__ __forceinline__ void build_tile_start(const int* offsets, int G, int tile, int* tile_start, int lane) {
-  const int per = (G + 31) / 32;
-  const int b = lane * per, e = min(G, b + per);
-  int local = 0;
-  for (int g = b; g < e; ++g) {
-    const int rows = __ldg(offsets + g + 1) - __ldg(offsets + g);
-    local += (rows + tile - 1) / tile;
-  }
-  int incl = local;
+  constexpr int kRuns = 8;
+  int carry = 0;
+  for (int g0 = 0; g0 < G; g0 += 32 * kRuns) {
+    int tiles[kRuns];
 #pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int o = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += o;
+    for (int j = 0; j < kRuns; ++j) {
+      const int g = g0 + 32 * j + lane;
+      tiles[j] = g < G ? (__ldg(offsets + g + 1) - __ldg(offsets + g) + tile - 1) / tile : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < kRuns; ++j) {
+      int incl = tiles[j];
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      const int g = g0 + 32 * j + lane;
+      if (g < G) tile_start[g] = carry + incl - tiles[j];
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
   }
-  int run = incl - local;
-  for (int g = b; g < e; ++g) {
-    tile_start[g] = run;
-    const int rows = __ldg(offsets + g + 1) - __ldg(offsets + g);
-    run += (rows + tile - 1) / tile;
-  }
-  if (lane == 31) tile_start[G] = incl;
+  if (lane == 0) tile_start[G] = carry;
 }
 
 // MMA width for a token tile with `valid` rows: the rows rounded up to a

@@ -339,14 +339,17 @@ cudaEvent_t* prof_slot(moe_handle* h) {
 // K range into ks parts evens the load.  Estimated time: waves of part items
 // x (K steps per part + a fixed cost per item worth kItemSteps K steps, which
 // covers the pipeline start and the part reduction); the split is taken when
-// it beats the unsplit estimate by 5 %.
+// it beats the unsplit estimate by 5 %.  Unforced, only K ranges of at least
+// kMinSplitSteps steps are cut (shorter ones gain too little).
 int choose_ksplit(const moe_handle* h, int bn, long long items_ub, int k_steps) {
   if (h->fp8 || bn > 32 || h->gemm_ksplit == 1 || items_ub <= 0) return 1;
+  constexpr int kMinSplitSteps = 32;
   const int sms = h->num_sms;
   auto fits = [&](int ks) {  // every part has a K step and the part buffer room
     return (ks - 1) * ((k_steps + ks - 1) / ks) < k_steps && items_ub * ks <= h->ksplit_cap;
   };
   if (h->gemm_ksplit >= 2) return fits(h->gemm_ksplit) ? h->gemm_ksplit : 1;
+  if (k_steps < kMinSplitSteps) return 1;
   constexpr double kItemSteps = 8.0;
   auto cost = [&](int ks) {
     return static_cast<double>((items_ub * ks + sms - 1) / sms) * (static_cast<double>(k_steps) / ks + kItemSteps);

@@ -60,7 +60,10 @@ def run_ranks(inp, xs, ep_size, max_recv):
 
 
 @pytest.mark.parametrize("ep_size,Ts", [(1, [96]), (2, [70, 130]), (4, [40, 0, 65, 17]), (2, [1500, 300])])
-def test_expert_parallel_matches_whole_layer(ep_size, Ts):
+def test_expert_parallel_matches_whole_layer(ep_size, Ts, monkeypatch):
+    # Bit-identical when both calls run each GEMM with the same K parts: no
+    # K split in either (a split sums the parts in another order).
+    monkeypatch.setenv("MOE_GEMM_KSPLIT", "1")
     shape = synth.LayerShape(T=max(Ts), d=256, E=16, k=2, F=128)
     inp = synth.make_inputs(shape, seed=60 + ep_size)
     xs = [synth.make_tokens(shape.with_tokens(T), seed=70 + r, device=DEV) for r, T in enumerate(Ts)]
@@ -78,8 +81,10 @@ def test_expert_parallel_matches_whole_layer(ep_size, Ts):
     whole.close()
 
 
-def test_expert_parallel_flash_shape():
-    # d=4096, 288 routed experts over 8 ranks (36 each, the pages' EP = 8), top-8
+def test_expert_parallel_flash_shape(monkeypatch):
+    # d=4096, 288 routed experts over 8 ranks (36 each, the pages' EP = 8), top-8;
+    # bit-identical without K split (the whole-layer call on 1 token splits)
+    monkeypatch.setenv("MOE_GEMM_KSPLIT", "1")
     shape = synth.FLASH_DECODE.with_tokens(16)
     inp = synth.make_inputs(shape, seed=80, device=DEV)
     Ts = [16, 9, 0, 16, 3, 16, 12, 1]
