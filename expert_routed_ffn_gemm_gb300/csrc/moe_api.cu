@@ -935,6 +935,9 @@ int moe_check(moe_handle* h, void* stream) {
   MOE_CUDA(cudaMemcpyAsync(&e, h->err, sizeof e, cudaMemcpyDeviceToHost, s));
   MOE_CUDA(cudaMemsetAsync(h->err, 0, sizeof e, s));
   MOE_CUDA(cudaStreamSynchronize(s));
+  // a GEMM that gave up may have left K split part counts behind: the next
+  // call on the handle starts from zero
+  if (e) MOE_CUDA(cudaMemset(h->ksplit_cnt, 0, sizeof(int) * static_cast<size_t>(h->ksplit_cap)));
   return e ? MOE_ERR_DEVICE : MOE_OK;
 }
 

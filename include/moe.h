@@ -292,7 +292,10 @@ int moe_forward_host(moe_handle* h, const void* x_host, int T, void* y_host, voi
 /*
  * Synchronises `stream`, then reads and clears the handle's device error word.
  * Returns MOE_OK, MOE_ERR_DEVICE if a kernel since the last check gave up on a
- * pipeline wait, or MOE_ERR_CUDA if the stream reports an error.
+ * pipeline wait, or MOE_ERR_CUDA if the stream reports an error.  After
+ * MOE_ERR_DEVICE the outputs of the calls since the last check are undefined;
+ * the check also clears the handle's K split part counts, so the handle is
+ * usable again.
  */
 int moe_check(moe_handle* h, void* stream);
 
