@@ -46,7 +46,7 @@ constexpr int kBlockM = 128;  // weight rows per tensor-core tile (M of tcgen05.
 constexpr int kBlockK = 64;   // K elements per pipeline stage (one 128-byte swizzle row)
 constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 32;
-constexpr int kMaxKSplit = 16;  // K splits of the router GEMM
+constexpr int kMaxKSplit = 48;  // K splits of the router GEMM
 constexpr int kMaxGemmKSplit = 4;  // K parts of the bf16 expert GEMMs (small token counts)
 constexpr int kMaxStatGroups = 64;  // expert groups of the routing statistics
 
@@ -70,7 +70,7 @@ struct RouterGemmArgs {
   int T, d, E;
   int e_pad;    // rows per slice of the split router weights (multiple of 128)
   int m_tiles;  // e_pad / 128
-  int ksplit;   // K splits (1..16)
+  int ksplit;   // K splits (1..kMaxKSplit)
 };
 cudaError_t launch_router_gemm(int tile_n, const CUtensorMap* map_w3, const CUtensorMap* map_x,
                                const RouterGemmArgs& a, int num_sms, cudaStream_t stream);

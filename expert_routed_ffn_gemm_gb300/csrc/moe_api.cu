@@ -613,8 +613,11 @@ int init_any(const moe_config* cfg, const moe_weights* w, const float* s_gu, con
   const size_t RH = R > static_cast<size_t>(ep.max_recv) ? R : static_cast<size_t>(ep.max_recv);
   const size_t n_epg = static_cast<size_t>(ep.size) * (ep.size ? c.n_experts / ep.size : 0) + 1;
   const size_t e_pad = static_cast<size_t>(h->router_m_tiles) * moe::kBlockM;
-  // partial logits: room for 16 K splits of up to 2048 tokens, or one of Tmax
-  const size_t p_rows = Tmax > 16 * 2048 ? Tmax : (Tmax < 2048 ? 16 * Tmax : 16 * 2048);
+  // partial logits: room for kMaxKSplit K splits of Tmax tokens, at most
+  // 32768 rows (the router splits K only while token tiles are few), or one
+  // split of Tmax
+  const size_t p_cap = 32768;
+  const size_t p_rows = Tmax > p_cap ? Tmax : std::min(static_cast<size_t>(moe::kMaxKSplit) * Tmax, p_cap);
   h->partial_rows = static_cast<long long>(p_rows);
   size_t off = 0;
   auto carve = [&](size_t bytes) {

@@ -388,14 +388,26 @@ __global__ void __launch_bounds__(kTopkWarps * 32) router_topk_kernel(const floa
   float p[NS];
 #pragma unroll
   for (int i = 0; i < NS; ++i) p[i] = 0.f;
-#pragma unroll 4
-  for (int s = warp; s < ksplit; s += kTopkWarps) {
-    const float* row = partial + (static_cast<size_t>(s) * T + t) * E;
+  // this warp's splits in batches of six whose loads are in flight together
+  // (one memory latency per batch), added in increasing s
+  constexpr int kBatch = 6;
+  for (int s0 = warp; s0 < ksplit; s0 += kBatch * kTopkWarps) {
+    float v[kBatch][NS];
 #pragma unroll
-    for (int i = 0; i < NS; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E) p[i] += __ldg(row + e);
+    for (int u = 0; u < kBatch; ++u) {
+      const int s = s0 + u * kTopkWarps;
+      const float* row = partial + (static_cast<size_t>(s) * T + t) * E;
+#pragma unroll
+      for (int i = 0; i < NS; ++i) {
+        const int e = lane + 32 * i;
+        v[u][i] = (s < ksplit && e < E) ? __ldg(row + e) : 0.f;
+      }
     }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u)
+#pragma unroll
+      for (int i = 0; i < NS; ++i)
+        if (s0 + u * kTopkWarps < ksplit) p[i] += v[u][i];
   }
 #pragma unroll
   for (int i = 0; i < NS; ++i) zs[warp][lane + 32 * i] = p[i];
