@@ -245,19 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ks > 1) {
           // this part's accumulator row to the part buffer, tensor memory back
           // to the MMA, then the last part of the item sums the parts in order
-          float* mine = args.ksplit_part + (static_cast<size_t>(item) * kBlockM + row) * BN;
-#pragma unroll
-          for (int c0 = 0; c0 < BN; c0 += 16) {
-            if (c0 >= valid) break;  // the epilogue reads the 16-column chunks holding valid columns
-            uint32_t v[16];
-            tmem_ld16(taddr + c0, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int c = 0; c < 16; c += 4)
-              __stcg(reinterpret_cast<float4*>(mine + c0 + c),
-                     make_float4(__uint_as_float(v[c]), __uint_as_float(v[c + 1]), __uint_as_float(v[c + 2]),
-                                 __uint_as_float(v[c + 3])));
-          }
+          ksplit_store_part<BN>(taddr, 0, valid, args.ksplit_part + (static_cast<size_t>(item) * kBlockM + row) * BN);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[acc]);
@@ -265,48 +253,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             acc = 0;
             acc_phase ^= 1u;
           }
-          // the part is published by one release after the CTA barrier (the
-          // cumulative fence covers the rows the other threads wrote)
-          named_bar_sync(kEpilogueBar, 128);
           const int base = item / ks;
-          if (q == 0 && lane == 0) {
-            __threadfence();
-            const int last = atomicAdd(args.ksplit_cnt + base, 1) == ks - 1;
-            if (last) __threadfence();  // acquire: the other parts' rows are visible
-            *s_last = last;
-          }
-          named_bar_sync(kEpilogueBar, 128);
-          if (*s_last) {
+          if (ksplit_arrive(args.ksplit_cnt + base, ks, s_last, q == 0 && lane == 0)) {
             float sum[BN];
-            const float* src = args.ksplit_part + (static_cast<size_t>(base * ks) * kBlockM + row) * BN;
-#pragma unroll
-            for (int c0 = 0; c0 < BN; c0 += 16) {
-              if (c0 >= valid) break;
-              // every part's 16 columns in flight at once, summed in part order
-              float4 f[kMaxGemmKSplit][4];
-#pragma unroll
-              for (int p = 0; p < kMaxGemmKSplit; ++p)
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                  f[p][j] = p < ks ? __ldcg(reinterpret_cast<const float4*>(
-                                         src + static_cast<size_t>(p) * kBlockM * BN + c0 + 4 * j))
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                float4 a = f[0][j];
-#pragma unroll
-                for (int p = 1; p < kMaxGemmKSplit; ++p) {
-                  a.x += f[p][j].x;
-                  a.y += f[p][j].y;
-                  a.z += f[p][j].z;
-                  a.w += f[p][j].w;
-                }
-                sum[c0 + 4 * j] = a.x;
-                sum[c0 + 4 * j + 1] = a.y;
-                sum[c0 + 4 * j + 2] = a.z;
-                sum[c0 + 4 * j + 3] = a.w;
-              }
-            }
+            ksplit_sum_parts<BN>(args.ksplit_part + (static_cast<size_t>(base * ks) * kBlockM + row) * BN, ks, valid,
+                                 sum);
             if (GATEUP)
               epilogue_gateup<BN>(0u, row, it.m * (kBlockM / 2), row0, valid, static_cast<bf16*>(args.out),
                                   args.out_ld, xchg, chunk_par, 1.0f, sum);

@@ -44,7 +44,7 @@ namespace {
 using namespace gemm;
 
 constexpr int kThreadsX = 192;
-constexpr int kKStepX = 128;  // K elements (bytes) per stage
+constexpr int kKStepX = kKStepE4M3;  // K elements (bytes) per stage
 
 // E4M3 x E4M3 -> fp32 MMA from shared memory, K = 32 per instruction.
 __device__ __forceinline__ void tc_mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -134,9 +134,14 @@ __global__ void __launch_bounds__(kThreadsX, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  const int n_items = tile_start[G] * args.m_tiles;
+  const int n_base = tile_start[G] * args.m_tiles;
+  // K split (token tiles <= 32, few items): part p of an item takes the K
+  // steps [p * k_per, min(k_steps, (p + 1) * k_per)), the parts adjacent
+  const int ks = (BN <= 32 && args.ksplit > 1 && n_base * args.ksplit <= args.ksplit_cap) ? args.ksplit : 1;
+  const int n_items = n_base * ks;
   const uint64_t limit = args.wait_limit_ns;
   const int k_steps = args.K / kKStepX;
+  const int k_per = (k_steps + ks - 1) / ks;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -147,10 +152,12 @@ __global__ void __launch_bounds__(kThreadsX, 1)
       long issued = 0;
       bool ok = true;
       for (int item = blockIdx.x; ok && item < n_items && !*abort_flag; item += gridDim.x) {
-        const Item it = decode_item(item, args.m_tiles, tile_start, G, n_items, args.reverse);
+        const Item it = decode_item(item / ks, args.m_tiles, tile_start, G, n_base, args.reverse);
         const int row_w = weight_group(args, it.g) * args.rows_per_group + it.m * (GATEUP ? kBlockM / 2 : kBlockM);
         const int row_act = __ldg(args.offsets + it.g) + it.n * BN;
-        for (int kb = 0; kb < k_steps; ++kb) {
+        const int part = item % ks;
+        const int kb1 = min(k_steps, (part + 1) * k_per);
+        for (int kb = part * k_per; kb < kb1; ++kb) {
           if (!wait_or_abort(&empty[stage], phase ^ 1u, limit, abort_flag)) {
             record_abort(abort_flag, args.err);
             ok = false;
@@ -188,7 +195,9 @@ __global__ void __launch_bounds__(kThreadsX, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * C::ACC_COLS;
-        for (int kb = 0; kb < k_steps; ++kb) {
+        const int part = item % ks;
+        const int kb0 = part * k_per, kb1 = min(k_steps, (part + 1) * k_per);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_or_abort(&full[stage], phase, limit, abort_flag)) {
             record_abort(abort_flag, args.err);
             ok = false;
@@ -200,7 +209,7 @@ __global__ void __launch_bounds__(kThreadsX, 1)
           const uint64_t b = smem_desc_sw128(st + C::A_BYTES);  // hi rows, then lo rows: N = 2*BN
 #pragma unroll
           for (int kk = 0; kk < kKStepX / 32; ++kk)  // +32 B along K = +2 in the address field
-            tc_mma_e4m3(d_tmem, a + 2 * kk, b + 2 * kk, C::IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
+            tc_mma_e4m3(d_tmem, a + 2 * kk, b + 2 * kk, C::IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
           issued_any = true;
           tc_commit(&empty[stage]);
           if (++stage == C::STAGES) {
@@ -225,8 +234,9 @@ __global__ void __launch_bounds__(kThreadsX, 1)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
     uint32_t acc = 0, acc_phase = 0, it_par = 0, chunk_par = 0;
+    volatile int* s_last = reinterpret_cast<volatile int*>(tmem_holder + 2);
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-      const Item it = decode_item(item, args.m_tiles, tile_start, G, n_items, args.reverse);
+      const Item it = decode_item(item / ks, args.m_tiles, tile_start, G, n_base, args.reverse);
       const int g_row0 = __ldg(args.offsets + it.g);
       const int g_rows = __ldg(args.offsets + it.g + 1) - g_row0;
       const int row0 = g_row0 + it.n * BN;
@@ -249,6 +259,35 @@ __global__ void __launch_bounds__(kThreadsX, 1)
       if (!epilogue_wait(&acc_full[acc], acc_phase, limit, abort_flag, s_ok, it_par, q, lane, args.err)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ACC_COLS;
+      if constexpr (BN <= 32) {
+        if (ks > 1) {
+          // this part's hi + lo row to the part buffer, tensor memory back to
+          // the MMA, then the last part of the item sums the parts in order
+          ksplit_store_part<BN>(taddr, BN, valid, args.ksplit_part + (static_cast<size_t>(item) * kBlockM + row) * BN);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[acc]);
+          if (++acc == C::NACC) {
+            acc = 0;
+            acc_phase ^= 1u;
+          }
+          const int base = item / ks;
+          if (ksplit_arrive(args.ksplit_cnt + base, ks, s_last, q == 0 && lane == 0)) {
+            float sum[BN];
+            ksplit_sum_parts<BN>(args.ksplit_part + (static_cast<size_t>(base * ks) * kBlockM + row) * BN, ks, valid,
+                                 sum);
+            if (GATEUP)
+              epilogue_gateup_x2<BN>(0u, row, it.m * (kBlockM / 2), row0, valid, static_cast<__half*>(args.out),
+                                     args.out_ld, xchg, chunk_par, scale, args.tok_scale, BN, sum);
+            else
+              epilogue_down<BN>(0u, it.m * kBlockM + row, row0, valid, wreg, static_cast<__half*>(args.out),
+                                args.out_exp, args.out_ld, __ldg(args.chunk_base + it.g) + it.n * (BN / kYpRows),
+                                scale, 0, sum);
+            if (q == 0 && lane == 0) args.ksplit_cnt[base] = 0;  // ready for the next launch
+          }
+          continue;
+        }
+      }
       if (GATEUP)
         epilogue_gateup_x2<BN>(taddr, row, it.m * (kBlockM / 2), row0, valid, static_cast<__half*>(args.out),
                                args.out_ld, xchg, chunk_par, scale, args.tok_scale, BN);

@@ -193,6 +193,78 @@ __device__ __forceinline__ void epilogue_gateup(uint32_t taddr, int row, int fea
   }
 }
 
+// K split (few work items: every item's K range in ks parts run as separate
+// items).  ksplit_store_part: this thread's accumulator row of one part (the
+// hi + lo sum when lo_off > 0) to the part buffer, the 16-column chunks that
+// hold valid columns only.
+template <int BN>
+__device__ __forceinline__ void ksplit_store_part(uint32_t taddr, int lo_off, int valid, float* mine) {
+#pragma unroll
+  for (int c0 = 0; c0 < BN; c0 += 16) {
+    if (c0 >= valid) break;
+    uint32_t v[16], vl[16];
+    tmem_ld16(taddr + c0, v);
+    if (lo_off > 0) tmem_ld16(taddr + lo_off + c0, vl);
+    tmem_ld_wait();
+    float f[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c)
+      f[c] = lo_off > 0 ? __uint_as_float(v[c]) + __uint_as_float(vl[c]) : __uint_as_float(v[c]);
+#pragma unroll
+    for (int c = 0; c < 16; c += 4)
+      __stcg(reinterpret_cast<float4*>(mine + c0 + c), make_float4(f[c], f[c + 1], f[c + 2], f[c + 3]));
+  }
+}
+
+// After every epilogue thread of the CTA stored its row of a part: one
+// release (the cumulative fence after the barrier covers the other threads'
+// rows) and the count of the item's finished parts.  True in every thread of
+// the CTA that finished the item's last part (which then sees all parts).
+__device__ __forceinline__ bool ksplit_arrive(int* cnt, int ks, volatile int* s_last, bool leader) {
+  named_bar_sync(kEpilogueBar, 128);
+  if (leader) {
+    __threadfence();
+    const int last = atomicAdd(cnt, 1) == ks - 1;
+    if (last) __threadfence();  // acquire: the other parts' rows are visible
+    *s_last = last;
+  }
+  named_bar_sync(kEpilogueBar, 128);
+  return *s_last != 0;
+}
+
+// The ks parts of this thread's row (part p at src + p * 128 * BN), summed
+// in part order; every part's 16 columns are loaded at once.
+template <int BN>
+__device__ __forceinline__ void ksplit_sum_parts(const float* src, int ks, int valid, float (&sum)[BN]) {
+#pragma unroll
+  for (int c0 = 0; c0 < BN; c0 += 16) {
+    if (c0 >= valid) break;
+    float4 f[kMaxGemmKSplit][4];
+#pragma unroll
+    for (int p = 0; p < kMaxGemmKSplit; ++p)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        f[p][j] = p < ks ? __ldcg(reinterpret_cast<const float4*>(src + static_cast<size_t>(p) * kBlockM * BN + c0 +
+                                                                   4 * j))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float4 a = f[0][j];
+#pragma unroll
+      for (int p = 1; p < kMaxGemmKSplit; ++p) {
+        a.x += f[p][j].x;
+        a.y += f[p][j].y;
+        a.z += f[p][j].z;
+        a.w += f[p][j].w;
+      }
+      sum[c0 + 4 * j] = a.x;
+      sum[c0 + 4 * j + 1] = a.y;
+      sum[c0 + 4 * j + 2] = a.z;
+      sum[c0 + 4 * j + 3] = a.w;
+    }
+  }
+}
+
 // K4: the gate weight of every column of a tile, lane l holding columns
 // l, l+32, ... (rows at dispatch positions >= Tk are shared-expert rows: 1).
 template <int BN>
@@ -218,7 +290,8 @@ __device__ __forceinline__ void load_gate_weights(float (&wreg)[(BN + 31) / 32],
 template <int BN>
 __device__ __forceinline__ void epilogue_gateup_x2(uint32_t taddr, int row, int feat_base, int row0, int valid,
                                                    __half* H, int ldh, float* xchg, uint32_t& chunk_par,
-                                                   float scale, const float* __restrict__ tok_scale, int lo_off) {
+                                                   float scale, const float* __restrict__ tok_scale, int lo_off,
+                                                   const float* vals = nullptr) {
   const bool is_gate = row < 64;
   const int fl = row & 63;
   const int feat = feat_base + fl;
@@ -226,9 +299,17 @@ __device__ __forceinline__ void epilogue_gateup_x2(uint32_t taddr, int row, int 
   for (int c0 = 0; c0 < BN; c0 += 16) {
     if (c0 >= valid) break;
     uint32_t vh[16], vl[16];
-    tmem_ld16(taddr + c0, vh);
-    tmem_ld16(taddr + lo_off + c0, vl);
-    tmem_ld_wait();
+    if (vals != nullptr) {  // hi + lo already summed over the K parts
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        vh[c] = __float_as_uint(vals[c0 + c]);
+        vl[c] = 0u;
+      }
+    } else {
+      tmem_ld16(taddr + c0, vh);
+      tmem_ld16(taddr + lo_off + c0, vl);
+      tmem_ld_wait();
+    }
     float v[16];
 #pragma unroll
     for (int c = 0; c < 16; ++c) {

@@ -47,7 +47,8 @@ constexpr int kBlockK = 64;   // K elements per pipeline stage (one 128-byte swi
 constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 32;
 constexpr int kMaxKSplit = 48;  // K splits of the router GEMM
-constexpr int kMaxGemmKSplit = 4;  // K parts of the bf16 expert GEMMs (small token counts)
+constexpr int kMaxGemmKSplit = 4;  // K parts of the expert GEMMs (small token counts)
+constexpr int kKStepE4M3 = 128;    // K per pipeline stage of the E4M3 expert GEMMs (128 bytes)
 constexpr int kMaxStatGroups = 64;  // expert groups of the routing statistics
 
 // Expert outputs Yp (one row per dispatch position) are kept as fp16 with a
@@ -128,7 +129,7 @@ struct GemmArgs {
   int reverse;         // 1: work items in reverse order (last group first)
   int w_group_base;    // weights of group g: w_group_base + (w_group_mod ? g % w_group_mod : g)
   int w_group_mod;
-  // K split (bf16 single-CTA kernels, few work items): ksplit > 1 cuts every
+  // K split (single-CTA bf16 and two-term E4M3 kernels, few work items): ksplit > 1 cuts every
   // item's K range into ksplit parts run as separate items; each part writes
   // its fp32 accumulator to ksplit_part and the last part to finish (counted
   // in ksplit_cnt, which it resets) sums the parts in part order and runs the

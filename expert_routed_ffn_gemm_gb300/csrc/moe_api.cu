@@ -333,7 +333,8 @@ cudaEvent_t* prof_slot(moe_handle* h) {
 // behind map_rows (one map per tile width) into H, then down into yout (fp16)
 // and yexp.  mean_rows: mean rows per group (picks the token tile width).
 // ev (or NULL): profiling events 3..5 around the two GEMMs.
-// K parts for a bf16 single-CTA expert GEMM with token tile bn.  The work
+// K parts for a single-CTA bf16 or two-term E4M3 expert GEMM with token tile
+// bn (k_steps: its pipeline stages along K, 16 KB of weights each).  The work
 // items (weight tiles x token tiles, at most items_ub) run in waves over the
 // SMs; with few items the last wave leaves SMs idle and cutting every item's
 // K range into ks parts evens the load.  Estimated time: waves of part items
@@ -342,14 +343,17 @@ cudaEvent_t* prof_slot(moe_handle* h) {
 // it beats the unsplit estimate by 5 %.  Unforced, only K ranges of at least
 // kMinSplitSteps steps are cut (shorter ones gain too little).
 int choose_ksplit(const moe_handle* h, int bn, long long items_ub, int k_steps) {
-  if (h->fp8 || bn > 32 || h->gemm_ksplit == 1 || items_ub <= 0) return 1;
+  if ((h->fp8 && !h->fp8_x2) || bn > 32 || h->gemm_ksplit == 1 || items_ub <= 0) return 1;
   constexpr int kMinSplitSteps = 32;
   const int sms = h->num_sms;
   auto fits = [&](int ks) {  // every part has a K step and the part buffer room
     return (ks - 1) * ((k_steps + ks - 1) / ks) < k_steps && items_ub * ks <= h->ksplit_cap;
   };
   if (h->gemm_ksplit >= 2) return fits(h->gemm_ksplit) ? h->gemm_ksplit : 1;
-  if (k_steps < kMinSplitSteps) return 1;
+  // E4M3 items carry half the bytes of bf16 ones, so the fixed cost per part
+  // outweighs the fuller last wave (T=1 gate/up: 31 us unsplit, 37 and 43 us
+  // in 2 and 3 parts): split only when forced
+  if (h->fp8 || k_steps < kMinSplitSteps) return 1;
   constexpr double kItemSteps = 8.0;
   auto cost = [&](int ks) {
     return static_cast<double>((items_ub * ks + sms - 1) / sms) * (static_cast<double>(k_steps) / ks + kItemSteps);
@@ -411,10 +415,12 @@ int enqueue_ffn(moe_handle* h, moe::GemmArgs a, double mean_rows, const CUtensor
   a.out_ld = c.ffn_width;
   const int i1 = tile_index(bn1), i2 = tile_index(bn2);
   a.w_scale = h->s_gate_up;
+  a.ksplit = 1;
   if (h->fp8_x2) {
     a.tok_scale = h->tok_scale;
     a.lo_row0 = h->rows_max;
     a.lo_col0 = 0;
+    a.ksplit = choose_ksplit(h, bn1, tiles_ub(bn1) * a.m_tiles, a.K / moe::kKStepE4M3);
     MOE_CUDA(moe::launch_expert_gemm_fp8x(true, bn1, &h->map_wgu, &h->map_xq[i1], a, h->num_sms, s));
   } else if (h->fp8)
     MOE_CUDA(moe::launch_expert_gemm_fp8(true, bn1, &h->map_wgu, &map_rows[i1], a, h->num_sms, s));
@@ -435,6 +441,7 @@ int enqueue_ffn(moe_handle* h, moe::GemmArgs a, double mean_rows, const CUtensor
   a.m_tiles = pair2 ? c.d_model / (2 * moe::kBlockM) : c.d_model / moe::kBlockM;
   a.out_ld = c.d_model;
   a.w_scale = h->s_down;
+  a.ksplit = 1;
   if (h->fp8_x2) {
     // H in place as two-term E4M3 rows, their 1/s in tok_scale (gate/up has
     // read the token scales by now)
@@ -442,6 +449,7 @@ int enqueue_ffn(moe_handle* h, moe::GemmArgs a, double mean_rows, const CUtensor
     a.tok_scale = h->tok_scale;
     a.lo_row0 = 0;
     a.lo_col0 = c.ffn_width;
+    a.ksplit = choose_ksplit(h, bn2, tiles_ub(bn2) * a.m_tiles, a.K / moe::kKStepE4M3);
     MOE_CUDA(moe::launch_expert_gemm_fp8x(false, bn2, &h->map_wd, &h->map_hq[i2], a, h->num_sms, s));
   } else if (h->fp8)
     MOE_CUDA(moe::launch_expert_gemm_fp8(false, bn2, &h->map_wd, &h->map_h[i2], a, h->num_sms, s));

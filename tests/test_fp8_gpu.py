@@ -37,17 +37,22 @@ def test_quantiser_bit_exact():
     np.testing.assert_array_equal(cpu(q), oq)
 
 
-def fp8_case(shape, seed, tiles=(0, 0), n_sample=None, max_tokens=None, out_fp32=False, x2=True):
+def fp8_case(shape, seed, tiles=(0, 0), n_sample=None, max_tokens=None, out_fp32=False, x2=True, ksplit=None):
     """x2: the gate/up GEMM on E4M3 tensor cores with the token rows as two
     E4M3 terms (the default), or on fp16 tensor cores with the weights widened
-    (MOE_FP8_X2=0)."""
+    (MOE_FP8_X2=0).  ksplit: K parts forced on the expert GEMMs (None: by
+    work items)."""
     import os
     inp = synth.make_inputs(shape, seed=seed, device=DEV)
     q_gu, s_gu, q_d, s_d = quantised(inp)
     inp.w_gate_up = inp.w_down = None  # the bf16 copies are not needed any more
-    old = {k: os.environ.get(k) for k in ("MOE_TILE_N_GATEUP", "MOE_TILE_N_DOWN", "MOE_FP8_X2")}
+    old = {k: os.environ.get(k) for k in ("MOE_TILE_N_GATEUP", "MOE_TILE_N_DOWN", "MOE_FP8_X2", "MOE_GEMM_KSPLIT")}
     os.environ["MOE_TILE_N_GATEUP"], os.environ["MOE_TILE_N_DOWN"] = str(tiles[0]), str(tiles[1])
     os.environ["MOE_FP8_X2"] = "1" if x2 else "0"
+    if ksplit is None:
+        os.environ.pop("MOE_GEMM_KSPLIT", None)
+    else:
+        os.environ["MOE_GEMM_KSPLIT"] = str(ksplit)
     try:
         layer = binding.MoeLayer.fp8(inp.w_router, q_gu, s_gu, q_d, s_d, shape.k,
                                      max_tokens or shape.T, has_shared=shape.has_shared, out_fp32=out_fp32)
@@ -174,3 +179,14 @@ def test_fp8_two_term_128_row_tiles():
     # 128-row tiles of the two-term kernel (N = 256, 4 ring stages): ~150 rows
     # per group, ragged second tiles, d = 1024 gives 8 K steps per gate/up tile
     fp8_case(synth.LayerShape(T=1200, d=1024, E=16, k=2, F=256), seed=29, tiles=(128, 128), n_sample=64)
+
+
+@pytest.mark.parametrize("parts", [2, 3, 4])
+@pytest.mark.parametrize("T,d,F,tiles", [(1, 512, 256, (32, 32)), (5, 1024, 512, (16, 32)), (20, 512, 256, (16, 16))])
+def test_fp8_gemm_k_split(parts, T, d, F, tiles):
+    # Two-term E4M3 GEMMs with every item's K range in parts (fewer where K
+    # has fewer steps of 128): each part's hi + lo sum, the parts summed in
+    # order, then the row and token scales; run to run identical (fp8_case).
+    shape = synth.LayerShape(T=T, d=d, E=16, k=2, F=F)
+    fp8_case(shape, seed=90 + T + parts, tiles=tiles, max_tokens=64, ksplit=parts)
+
