@@ -77,41 +77,78 @@ def workload(name: str, experts: int = 0, ffn_width: int = 0):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons, sampled every 20 ms by a
+    background nvidia-smi whose lines a reader thread timestamps.  Entering
+    waits (up to 5 s) for the first sample, so the sampler is running before
+    the timed region starts; mark_start() / mark_end() bracket the timed
+    region, and summary() keeps the samples taken inside it (plus the first
+    one after it, which covers its last interval)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 20
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.out = None
+        self.lines = []  # (time.perf_counter(), line)
+        self.t0 = self.t1 = None
+        self._reader = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.perf_counter(), line))
 
     def __enter__(self):
+        import threading
+
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.INTERVAL_MS)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
+            return self
+        self._reader = threading.Thread(target=self._read, daemon=True)
+        self._reader.start()
+        deadline = time.perf_counter() + 5.0
+        while not self.lines and time.perf_counter() < deadline and self.proc.poll() is None:
+            time.sleep(0.005)
         return self
+
+    def mark_start(self):
+        self.t0 = time.perf_counter()
+
+    def mark_end(self):
+        self.t1 = time.perf_counter()
 
     def __exit__(self, *exc):
         if self.proc is not None:
+            time.sleep(2 * self.INTERVAL_MS / 1000.0)  # the sample that covers the end of the region
             self.proc.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
-                self.out = ""
+            if self._reader is not None:
+                self._reader.join(timeout=5)
+
+    def window(self):
+        """The sampled lines of the timed region (all lines if it was not marked)."""
+        if self.t0 is None or self.t1 is None:
+            return [l for _, l in self.lines]
+        inside = [l for t, l in self.lines if self.t0 <= t <= self.t1]
+        after = [l for t, l in self.lines if t > self.t1]
+        return inside + after[:1]
 
     def summary(self):
-        if not self.out:
+        lines = self.window()
+        if not lines:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
         sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.out.strip().splitlines():
+        for line in lines:
             f = [v.strip() for v in line.split(",")]
             if len(f) < 9:
                 continue
@@ -125,7 +162,7 @@ class ClockSampler:
                     reasons.add(n)
         load = [v for v in sm if smax and v > 0.3 * smax] or sm
         return {"sm_mhz": statistics.median(load) if load else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "interval_ms": self.INTERVAL_MS}
 
 
 def dist_setup(n_gpus: int):
@@ -338,6 +375,7 @@ def run_native(args, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        clk.mark_start()
         ev0.record(stream)
         launches = 0
         for i in range(args.steps):
@@ -345,6 +383,7 @@ def run_native(args, world, rank, local):
             launches += layer.last_kernel_count()
         ev1.record(stream)
         torch.cuda.synchronize()
+        clk.mark_end()
     kernels_per_step = launches // max(1, args.steps)
     barrier(world)
     ms = ev0.elapsed_time(ev1)

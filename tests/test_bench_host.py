@@ -50,3 +50,23 @@ def test_workloads_resolve():
         assert shape.d == 4096 and shape.E == 288
     shape, _ = bench.workload("prefill", experts=32, ffn_width=128)
     assert shape.E == 32 and shape.F == 128 and shape.T == 8192
+
+
+def test_clock_window_and_summary():
+    # Samples before the timed region are dropped, the first one after it is
+    # kept; throttle reasons are collected and the median taken under load.
+    clk = bench.ClockSampler(0)
+    row = "0, {sm}, 2070, 900.0, 0x0, Not Active, Not Active, {thermal}, Active"
+    clk.lines = [(0.9, row.format(sm=345, thermal="Not Active")),
+                 (1.01, row.format(sm=2070, thermal="Not Active")),
+                 (1.03, row.format(sm=2055, thermal="Active")),
+                 (1.05, row.format(sm=2070, thermal="Not Active")),
+                 (1.07, row.format(sm=1000, thermal="Not Active"))]
+    clk.t0, clk.t1 = 1.0, 1.04
+    s = clk.summary()
+    assert s["samples"] == 3
+    assert s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap", "sw_thermal_slowdown"]
+    clk.t0 = clk.t1 = None  # unmarked: every sample
+    assert clk.summary()["samples"] == 5
+    assert bench.ClockSampler(0).summary()["reasons"] == ["unsampled"]
