@@ -437,14 +437,25 @@ __global__ void __launch_bounds__(kTopkTokensPerBlock * 32) router_topk_warp_ker
   float p[NS];
 #pragma unroll
   for (int i = 0; i < NS; ++i) p[i] = 0.f;
-#pragma unroll 2
-  for (int s = 0; s < ksplit; ++s) {
-    const float* row = partial + (static_cast<size_t>(s) * T + t) * E;
+  // the splits in batches of four whose loads are in flight together, added
+  // in increasing s
+  constexpr int kBatch = 4;
+  for (int s0 = 0; s0 < ksplit; s0 += kBatch) {
+    float v[kBatch][NS];
 #pragma unroll
-    for (int i = 0; i < NS; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E) p[i] += __ldg(row + e);
+    for (int u = 0; u < kBatch; ++u) {
+      const float* row = partial + (static_cast<size_t>(s0 + u) * T + t) * E;
+#pragma unroll
+      for (int i = 0; i < NS; ++i) {
+        const int e = lane + 32 * i;
+        v[u][i] = (s0 + u < ksplit && e < E) ? __ldg(row + e) : 0.f;
+      }
     }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u)
+#pragma unroll
+      for (int i = 0; i < NS; ++i)
+        if (s0 + u < ksplit) p[i] += v[u][i];
   }
   finish_token<NS>(p, t, lane, E, k, renorm, idx, prob, gap, counts, tokstats, n_groups);
 }
