@@ -9,13 +9,18 @@ Prints one JSON line.  `value` = tokens/s over the timed steps (device time,
 CUDA events, inputs resident in HBM); `e2e` = the same through the host-buffer
 entry point (pinned host x in, host y out, copies inside the timed region);
 `roofline` = the gate/up grouped GEMM (the dominant kernel) against its binding
-roof (HBM copy bandwidth or sustained bf16 tensor rate), its time from a
-second pass of the same steps with per-stage events; `cpu_baseline` = the CPU
-oracle on a bounded sample of the same workload.
+roof (HBM copy bandwidth, or the burst bf16 tensor rate for these passes of a
+few milliseconds; the sustained rate is reported beside it), its time from a
+second pass of the same steps with per-stage events; `routing` = the
+per-expert load of the batch (moe_route_stats) and its near-ties;
+`cpu_baseline` = the CPU oracle on a bounded sample of the same workload, on
+one thread and on every host core.  With the default decode workload the line
+also carries `prefill` (T=8192) and `skew` (Zipf-skewed routing, T=4096):
+the same measurements on the same weights, nested.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
                   [--workload decode|prefill|skew|T=<n>] [--weights bf16|fp8]
-                  [--experts E] [--ffn-width F] [--no-cpu-baseline]
+                  [--experts E] [--ffn-width F] [--no-cpu-baseline] [--no-nested]
 
 Multi-GPU (torchrun, one rank per GPU): every rank runs its own replica of
 the layer on its own batch (weak scaling, no data-path collective); the
@@ -228,23 +233,48 @@ def gateup_flops(shape):
     return 2 * R * d * 2 * F
 
 
-def measured_traffic(args):
-    """DRAM bytes per launch of the gate/up GEMM from the committed ncu capture
-    of the decode workload (profiles/gate_up_decode_T128_dram.md, or
-    profiles/decode_T128_fp8.md with FP8 weights); None for other workloads or
-    when the summary is missing."""
-    if args.workload != "decode" or args.experts or args.ffn_width:
-        return None
-    name = "decode_T128_fp8.md" if args.weights == "fp8" else "gate_up_decode_T128_dram.md"
-    path = os.path.join(ROOT, "profiles", name)
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def sources_digest(files) -> str:
+    """sha256 (first 16 hex digits) over the named kernel sources, in order."""
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload_name: str, weights: str, shape, gu_alg_bytes: float):
+    """DRAM bytes per launch of the gate/up GEMM from the committed ncu
+    captures (profiles/traffic.json): (bytes or None, source note).  An entry
+    whose kernel sources have changed since the capture gives None.  Entries
+    captured on a smaller case of the same kernel carry the ratio of the
+    captured traffic to that case's algorithmic bytes, and the figure is that
+    ratio times this workload's algorithmic bytes."""
     try:
-        with open(path) as f:
-            for line in f:
-                if line.startswith("traffic_bytes_per_launch:"):
-                    return float(line.split(":", 1)[1])
-    except OSError:
-        return None
-    return None
+        with open(TRAFFIC_FILE) as f:
+            entries = json.load(f)["entries"]
+    except (OSError, ValueError, KeyError):
+        return None, "no capture file"
+    for e in entries:
+        if e.get("workload") != workload_name or e.get("weights") != weights:
+            continue
+        if tuple(e.get("shape", ())) != (shape.T, shape.d, shape.E, shape.k, shape.F):
+            continue
+        try:
+            digest = sources_digest(e["sources"])
+        except OSError:
+            return None, "kernel sources missing"
+        if digest != e.get("sources_sha256_16"):
+            return None, f"stale: the kernel changed since the capture ({e['capture']})"
+        if e.get("traffic_bytes_per_launch") is not None:
+            return float(e["traffic_bytes_per_launch"]), e["capture"]
+        if e.get("traffic_over_algorithmic") is not None:
+            return float(e["traffic_over_algorithmic"]) * gu_alg_bytes, e["capture"]
+    return None, "no capture of this workload"
 
 
 def layer_flops(shape):
@@ -252,11 +282,12 @@ def layer_flops(shape):
     return T * ((k + (1 if shape.has_shared else 0)) * 6 * d * F + 2 * d * E)
 
 
-def cpu_oracle_rate(inp_host, shape, budget_s: float, max_tokens: int, fp8=None):
+def cpu_oracle_rate(inp_host, shape, budget_s: float, max_tokens: int, fp8=None, threads: int = 0):
     """CPU oracle throughput (tokens/s) on the batch's tokens in order, in
     chunks, cycling through the batch, until `budget_s` seconds are spent or
     `max_tokens` tokens are done.  fp8 = host (q_gate_up, s_gate_up, q_down,
-    s_down): the FP8 oracle forward."""
+    s_down): the FP8 oracle forward.  threads: OpenMP threads (0 = all).
+    Returns (tokens/s, tokens, seconds, threads used)."""
     import numpy as np
 
     import oracle
@@ -270,13 +301,34 @@ def cpu_oracle_rate(inp_host, shape, budget_s: float, max_tokens: int, fp8=None)
             break
         t0 = time.perf_counter()
         if fp8 is None:
-            oracle.forward(xb, wr, wgu, wd, shape.k, has_shared=shape.has_shared, tokens=toks)
+            oracle.forward(xb, wr, wgu, wd, shape.k, has_shared=shape.has_shared, tokens=toks, threads=threads)
         else:
-            oracle.forward_fp8(xb, wr, *fp8, shape.k, has_shared=shape.has_shared, tokens=toks)
+            oracle.forward_fp8(xb, wr, *fp8, shape.k, has_shared=shape.has_shared, tokens=toks, threads=threads)
         spent += time.perf_counter() - t0
         n += toks.size
         chunk = min(64, chunk * 2)
-    return n / spent, n, spent, oracle.max_threads()
+    return n / spent, n, spent, (threads if threads > 0 else oracle.max_threads())
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    import platform
+
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name:"):
+                return line.split(":", 1)[1].strip() + f" ({platform.machine()})"
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
 
 
 def host_copy(inp):
@@ -320,52 +372,60 @@ def run_reference(args, world, rank):
         "config": {"workload": f"{args.workload}: T={shape.T}, d={shape.d}, E={shape.E}+1, k={shape.k}, "
                                f"F={shape.F}", "tokens_per_step_sampled": sample},
         "cpu_baseline": {"value": tok_s, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{sample} tokens of the T={shape.T} batch per step"},
+                         "sample": f"{sample} tokens of the T={shape.T} batch per step", "cpu_model": cpu_model()},
         "e2e": {"value": tok_s, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def run_native(args, world, rank, local):
+GATEUP_KERNEL = {
+    "bf16": "gate_up_gemm (tcgen05 grouped GEMM, fused SiLU gate)",
+    "fp8": "gate_up_gemm (tcgen05 kind::f8f6f4 grouped GEMM on E4M3 weights and two-term E4M3 token rows, "
+           "fused SiLU gate)",
+}
+
+
+def routing_report(layer, x, shape, n_groups: int = 8):
+    """Per-expert load of one batch from moe_route_stats (max/mean load,
+    experts without rows, EP-group balance L_EP over n_groups groups of
+    consecutive experts, mean router entropy) and the tokens whose k-th and
+    (k+1)-th probabilities differ by less than 1e-6 (near-ties, from the
+    GPU's own gap)."""
     import numpy as np
 
-    from expert_routed_ffn_gemm_gb300 import binding, synth
+    g = n_groups if shape.E % n_groups == 0 else 1
+    counts, _, _, summary = layer.route_stats(x, g)
+    _, _, _, _, gap = layer.route(x, with_gap=True)
+    c = counts.cpu().numpy()
+    s = summary.cpu().numpy().astype(float)
+    gp = gap.float().cpu().numpy()
+    return {"max_over_mean_load": float(s[1]), "empty_experts": int(s[3]), "max_rows": int(c.max()),
+            "mean_rows": float(c.mean()), "l_ep": float(s[0]), "ep_groups": g, "router_entropy": float(s[2]),
+            "near_ties": int(np.count_nonzero(gp < 1e-6))}
 
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    shape, skew = workload(args.workload, args.experts, args.ffn_width)
+
+def measure(layer, xs, shape, args, fp8, world, local, stream, label):
+    """One workload on one handle: the timed pass (step time, no per-stage
+    events), the same steps again with per-stage events, the clocks of the
+    timed pass, and the roofline figures of the layer and its gate/up GEMM."""
+    import numpy as np
+
+    from expert_routed_ffn_gemm_gb300 import binding
+
     hbm_gbs, tf_burst, tf_sust, peak_kind = peaks()
-
-    inp = synth.make_inputs(shape, seed=rank, device=dev, skew=skew)
-    xs = [inp.x] + [synth.make_tokens(shape, seed=1000 + 31 * rank + i, device=dev, skew=skew)
-                    for i in range(N_X_BUFFERS - 1)]
-    fp8 = args.weights == "fp8"
-    if fp8:
-        # E4M3 codes + row scales of the same synthetic weights, made on the device
-        q_gu, s_gu = binding.moe_quantize_fp8(inp.w_gate_up)
-        q_d, s_d = binding.moe_quantize_fp8(inp.w_down)
-        inp.w_gate_up = inp.w_down = None
-        torch.cuda.synchronize()
-        layer = binding.MoeLayer.fp8(inp.w_router, q_gu, s_gu, q_d, s_d, shape.k, shape.T)
-    else:
-        layer = binding.MoeLayer(inp.w_router, inp.w_gate_up, inp.w_down, shape.k, shape.T)
-    y = torch.empty((shape.T, shape.d), dtype=torch.bfloat16, device=dev)
-    stream = torch.cuda.current_stream(dev)
-
+    y = torch.empty((shape.T, shape.d), dtype=torch.bfloat16, device=xs[0].device)
     # units of work of each batch: routed experts with at least one row
     touched = []
     for x in xs:
         _, _, _, offsets, _ = layer.route(x, with_gap=False)
         off = offsets.cpu().numpy()
         touched.append(int(np.count_nonzero(np.diff(off[:shape.E + 1]))))
-
     for i in range(args.warmup):
-        layer.forward(xs[i % N_X_BUFFERS], y)
+        layer.forward(xs[i % len(xs)], y)
     torch.cuda.synchronize()
     if layer.check() != binding.MOE_OK:
-        raise RuntimeError("device error during warm-up")
+        raise RuntimeError(f"{label}: device error during warm-up")
 
-    # ---- timed region: device time, inputs resident -------------------------
     # The layer's kernels overlap their launch and set-up with the end of the
     # kernel before them (programmatic dependent launch); events recorded
     # between kernels would serialise them, so the step time is taken without
@@ -379,33 +439,123 @@ def run_native(args, world, rank, local):
         ev0.record(stream)
         launches = 0
         for i in range(args.steps):
-            layer.forward(xs[i % N_X_BUFFERS], y)
+            layer.forward(xs[i % len(xs)], y)
             launches += layer.last_kernel_count()
         ev1.record(stream)
         torch.cuda.synchronize()
         clk.mark_end()
-    kernels_per_step = launches // max(1, args.steps)
     barrier(world)
     ms = ev0.elapsed_time(ev1)
     ms_max = max_over_ranks(ms, world)
     if layer.check() != binding.MOE_OK:
-        raise RuntimeError("device error in the timed region")
+        raise RuntimeError(f"{label}: device error in the timed region")
     if not torch.isfinite(y.float()).all():
-        raise RuntimeError("non-finite output")
+        raise RuntimeError(f"{label}: non-finite output")
 
-    # ---- the same steps with per-stage events --------------------------------
     layer.profile_enable(True)
     torch.cuda.synchronize()
     ev0.record(stream)
     for i in range(args.steps):
-        layer.forward(xs[i % N_X_BUFFERS], y)
+        layer.forward(xs[i % len(xs)], y)
     ev1.record(stream)
     torch.cuda.synchronize()
     ms_staged = ev0.elapsed_time(ev1)
     stages, n_prof = layer.profile_read()
     layer.profile_enable(False)
     if layer.check() != binding.MOE_OK:
-        raise RuntimeError("device error in the staged pass")
+        raise RuntimeError(f"{label}: device error in the staged pass")
+
+    steps_prof = max(1, n_prof)
+    gu_ms = stages["gate_up_gemm"] / steps_prof
+    mean_touched = sum(touched[i % len(xs)] for i in range(args.steps)) / args.steps
+    gu_bytes = gateup_bytes(shape, mean_touched, fp8)
+    gu_gbs = gu_bytes / (gu_ms / 1e3) / 1e9
+    gu_tfs = gateup_flops(shape) / (gu_ms / 1e3) / 1e12
+    # the binding roof of the kernel: the larger of its HBM and tensor floors
+    # (burst tensor rate: these passes last milliseconds)
+    tensor_bound = gateup_flops(shape) / (tf_burst * 1e12) > gu_bytes / (hbm_gbs * 1e9)
+    if tensor_bound:
+        roof = {"bound": "tensor", "achieved": gu_tfs, "peak": tf_burst, "unit": "TFLOP/s",
+                "frac": gu_tfs / tf_burst, "peak_kind": peak_kind + " (burst bf16)"}
+    else:
+        roof = {"bound": "hbm", "achieved": gu_gbs, "peak": hbm_gbs, "unit": "GB/s", "frac": gu_gbs / hbm_gbs,
+                "peak_kind": peak_kind + " (copy bandwidth)"}
+    wname = "fp8" if fp8 else "bf16"
+    traffic, traffic_src = measured_traffic(args.workload if label == "headline" else label, wname, shape, gu_bytes)
+    layer_bytes = algorithmic_bytes(shape, mean_touched, fp8)
+    step_s = ms_max / 1e3 / args.steps
+    return {
+        "ms_per_step": ms_max / args.steps,
+        "value": shape.T * args.steps * world / (ms_max / 1e3),
+        "tokens_per_step_per_gpu": shape.T,
+        "experts_touched_mean": mean_touched,
+        "roofline": {"kernel": GATEUP_KERNEL[wname], **roof, "traffic": traffic, "traffic_source": traffic_src,
+                     "ms_per_launch": gu_ms, "algorithmic_bytes_per_launch": gu_bytes,
+                     "flops_per_launch": gateup_flops(shape), "hbm_frac": gu_gbs / hbm_gbs,
+                     "tensor_frac_burst": gu_tfs / tf_burst, "tensor_frac_sustained": gu_tfs / tf_sust},
+        "layer_roofline": {"hbm_frac": layer_bytes / step_s / 1e9 / hbm_gbs,
+                           "tensor_frac_burst": layer_flops(shape) / step_s / 1e12 / tf_burst,
+                           "tensor_frac_sustained": layer_flops(shape) / step_s / 1e12 / tf_sust,
+                           "bytes_per_step": layer_bytes, "flops_per_step": layer_flops(shape),
+                           "peaks": {"hbm_gbs": hbm_gbs, "bf16_tflops_burst": tf_burst,
+                                     "bf16_tflops_sustained": tf_sust, "kind": peak_kind}},
+        "stage_ms_per_step": {k: v / steps_prof for k, v in stages.items()},
+        "ms_per_step_with_stage_events": ms_staged / args.steps,
+        "routing": routing_report(layer, xs[0], shape),
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+
+
+def nested_workload(name, inp, q, args, world, rank, local, stream):
+    """The prefill or skew workload on the headline's expert weights (a
+    second handle borrowing the same tensors), for the nested objects."""
+    from expert_routed_ffn_gemm_gb300 import binding, synth
+
+    skew = "zipf" if name == "skew" else None
+    shape = synth.FLASH_PREFILL if name == "prefill" else synth.FLASH_SKEW
+    dev = inp.w_router.device
+    xs = [synth.make_tokens(shape, seed=2000 + 31 * rank + i, device=dev, skew=skew) for i in range(N_X_BUFFERS)]
+    wr = synth.skewed_router(inp.w_router, seed=rank) if skew else inp.w_router
+    if q is not None:
+        layer = binding.MoeLayer.fp8(wr, *q, shape.k, shape.T)
+    else:
+        layer = binding.MoeLayer(wr, inp.w_gate_up, inp.w_down, shape.k, shape.T)
+    try:
+        out = measure(layer, xs, shape, args, q is not None, world, local, stream, name)
+    finally:
+        layer.close()
+    out["workload"] = (f"{name}: T={shape.T} tokens, d={shape.d}, E={shape.E} routed + 1 shared, top-{shape.k}, "
+                       f"expert width {shape.F}" + (", Zipf-skewed router bias (40 experts never chosen)"
+                                                    if skew else ""))
+    return out
+
+
+def run_native(args, world, rank, local):
+    from expert_routed_ffn_gemm_gb300 import binding, synth
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    shape, skew = workload(args.workload, args.experts, args.ffn_width)
+
+    inp = synth.make_inputs(shape, seed=rank, device=dev, skew=skew)
+    xs = [inp.x] + [synth.make_tokens(shape, seed=1000 + 31 * rank + i, device=dev, skew=skew)
+                    for i in range(N_X_BUFFERS - 1)]
+    fp8 = args.weights == "fp8"
+    q = None
+    if fp8:
+        # E4M3 codes + row scales of the same synthetic weights, made on the device
+        q_gu, s_gu = binding.moe_quantize_fp8(inp.w_gate_up)
+        q_d, s_d = binding.moe_quantize_fp8(inp.w_down)
+        q = (q_gu, s_gu, q_d, s_d)
+        inp.w_gate_up = inp.w_down = None
+        torch.cuda.synchronize()
+        layer = binding.MoeLayer.fp8(inp.w_router, q_gu, s_gu, q_d, s_d, shape.k, shape.T)
+    else:
+        layer = binding.MoeLayer(inp.w_router, inp.w_gate_up, inp.w_down, shape.k, shape.T)
+    stream = torch.cuda.current_stream(dev)
+
+    head = measure(layer, xs, shape, args, fp8, world, local, stream, "headline")
 
     # ---- end to end through the host-buffer entry point ---------------------
     x_host = [x.cpu().pin_memory() for x in xs]
@@ -419,74 +569,57 @@ def run_native(args, world, rank, local):
     e2e_s = time.perf_counter() - t0
     barrier(world)
     e2e = aggregate(shape.T, args.steps, e2e_s, world)
+    layer.close()
 
-    tokens_total = shape.T * args.steps * world
-    value = tokens_total / (ms_max / 1e3)
-
-    # ---- roofline of the dominant kernel (gate/up grouped GEMM) -------------
-    steps_prof = max(1, n_prof)
-    gu_ms = stages["gate_up_gemm"] / steps_prof
-    mean_touched = sum(touched[i % N_X_BUFFERS] for i in range(args.steps)) / args.steps
-    gu_bytes = gateup_bytes(shape, mean_touched, fp8)
-    gu_gbs = gu_bytes / (gu_ms / 1e3) / 1e9
-    gu_tfs = gateup_flops(shape) / (gu_ms / 1e3) / 1e12
-    # the binding roof of the kernel: the larger of its HBM and tensor floors
-    tensor_bound = gateup_flops(shape) / (tf_sust * 1e12) > gu_bytes / (hbm_gbs * 1e9)
-    if tensor_bound:
-        roof = {"bound": "tensor", "achieved": gu_tfs, "peak": tf_sust, "unit": "TFLOP/s",
-                "frac": gu_tfs / tf_sust, "peak_kind": peak_kind + " (sustained bf16)"}
-    else:
-        roof = {"bound": "hbm", "achieved": gu_gbs, "peak": hbm_gbs, "unit": "GB/s", "frac": gu_gbs / hbm_gbs,
-                "peak_kind": peak_kind}
-    layer_bytes = algorithmic_bytes(shape, mean_touched, fp8)
-    step_s = ms_max / 1e3 / args.steps
-    layer_hbm_frac = layer_bytes / step_s / 1e9 / hbm_gbs
-    layer_tc_frac = layer_flops(shape) / step_s / 1e12 / tf_sust
-
+    layer_bytes = head["layer_roofline"]["bytes_per_step"]
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3-weights/f16" if fp8 else "bf16",
+        "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3-weights/bf16-x" if fp8 else "bf16",
         "data": "synthetic (seeded N(0,1) bf16 tokens, N(0,0.02) weights, random init)",
         "config": {
             "workload": f"{args.workload}: T={shape.T} tokens, d={shape.d}, E={shape.E} routed + 1 shared, "
                         f"top-{shape.k}, expert width {shape.F}, SiLU-gated"
-                        + (", E4M3 expert weights with fp32 row scales, fp16 activations" if fp8 else ""),
+                        + (", E4M3 expert weights with fp32 row scales" if fp8 else ""),
             "tokens_per_step_per_gpu": shape.T,
             "l2": f"inputs larger than L2: {layer_bytes / 1e9:.2f} GB of expert weights read per step; "
                   f"{N_X_BUFFERS} token batches cycled",
             "parallelism": "replicas" if world > 1 else "single GPU",
-            "experts_touched_mean": mean_touched,
+            "experts_touched_mean": head["experts_touched_mean"],
         },
-        "roofline": {
-            "kernel": "gate_up_gemm (tcgen05 grouped GEMM, fused SiLU-gate"
-                      + (", E4M3 weights widened into tensor memory)" if fp8 else ")"),
-            **roof, "traffic": measured_traffic(args), "ms_per_launch": gu_ms,
-            "algorithmic_bytes_per_launch": gu_bytes, "hbm_frac": gu_gbs / hbm_gbs,
-            "tensor_frac_sustained": gu_tfs / tf_sust,
-        },
-        "layer_roofline": {"hbm_frac": layer_hbm_frac, "tensor_frac_sustained": layer_tc_frac,
-                           "bytes_per_step": layer_bytes, "flops_per_step": layer_flops(shape)},
-        "stage_ms_per_step": {k: v / steps_prof for k, v in stages.items()},
-        "ms_per_step_with_stage_events": ms_staged / args.steps,
+        "roofline": head["roofline"],
+        "layer_roofline": head["layer_roofline"],
+        "stage_ms_per_step": head["stage_ms_per_step"],
+        "ms_per_step_with_stage_events": head["ms_per_step_with_stage_events"],
+        "routing": head["routing"],
         "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": shape.T * shape.d * 2,
                 "d2h_bytes_per_step": shape.T * shape.d * 2},
-        "gpu_launches": kernels_per_step * args.steps,
-        "clocks": clk.summary(),
+        "gpu_launches": head["gpu_launches"],
+        "clocks": head["clocks"],
     }
+
+    # ---- the prefill chunk and the skewed batch on the same weights ---------
+    if args.workload == "decode" and not args.no_nested and not args.experts and not args.ffn_width:
+        for name in ("prefill", "skew"):
+            line[name] = nested_workload(name, inp, q, args, world, rank, local, stream)
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         if fp8:
             inp_host = (synth.bf16_bits(inp.x), inp.w_router.detach().cpu().numpy(), None, None)
-            fp8_host = tuple(t.cpu().numpy() for t in (q_gu, s_gu, q_d, s_d))
+            fp8_host = tuple(t.cpu().numpy() for t in q)
         else:
             inp_host, fp8_host = host_copy(inp), None
-        rate, n, spent, cores = cpu_oracle_rate(inp_host, shape, budget_s=args.cpu_budget,
+        budget = args.cpu_budget / 2
+        rate, n, spent, cores = cpu_oracle_rate(inp_host, shape, budget_s=budget,
                                                 max_tokens=max(shape.T, 16 * 1024), fp8=fp8_host)
+        rate1, n1, spent1, _ = cpu_oracle_rate(inp_host, shape, budget_s=budget, max_tokens=max(shape.T, 1024),
+                                               fp8=fp8_host, threads=1)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                 "sample": f"{n} tokens of the T={shape.T} batch, in order and cycled "
-                                          f"({spent:.1f} s on {cores} threads)"}
-    layer.close()
+                                          f"({spent:.1f} s on {cores} threads)",
+                                "cpu_model": cpu_model(),
+                                "one_thread": {"value": rate1, "unit": "tokens/s", "cores": 1,
+                                               "sample": f"{n1} tokens of the same batch ({spent1:.1f} s)"}}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -503,6 +636,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-nested", action="store_true", help="decode only: leave out the nested prefill and skew runs")
     ap.add_argument("--weights", choices=["bf16", "fp8"], default="bf16",
                     help="expert weight format (fp8: E4M3 codes with fp32 row scales)")
     args = ap.parse_args()

@@ -857,7 +857,10 @@ extern "C" int moe_dispatch_noalloc(const int* idx, int T, int n_experts, int to
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // the array keeps the previous call's counts: clear it first
-  if (cudaMemsetAsync(counts, 0, sizeof(int) * n_experts, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(counts, 0, sizeof(int) * n_experts, s) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
   const long long n = static_cast<long long>(T) * top_k;
   if (n > 0) {
     const int blocks = static_cast<int>((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);

@@ -3,9 +3,10 @@
 // GEMMs over the dispatch order of §3.2.2, the shared expert being the last
 // group:
 //   gate/up (K3):  H[r, f]  = silu(X[r] . Wg[g, f]) * (X[r] . Wu[g, f])   (bf16)
-//   down    (K4):  Yp[r, o] = w_r * (H[r] . Wd[g, o])                       (fp32)
+//   down    (K4):  Yp[r, o] = w_r * (H[r] . Wd[g, o])   (fp32 accumulator)
 // for every row r of group g, w_r = the row's routing probability (1 for the
-// shared expert).
+// shared expert).  Yp is stored block-scaled: fp16 of Yp * 2^-e with one
+// power-of-two exponent e per feature and 16-row chunk of a group (int8).
 //
 // Design (sm_103a): a persistent, warp-specialised kernel, one CTA per SM.
 // The weights are the MMA's M operand (128 weight rows per tile) and the

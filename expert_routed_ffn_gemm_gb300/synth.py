@@ -123,6 +123,25 @@ def make_inputs(shape: LayerShape, seed: int = 0, device="cpu", skew: str | None
     return LayerInputs(shape, x, w_router, w_gate_up, w_down)
 
 
+def skewed_router(w_router: torch.Tensor, seed: int, skew: str = "zipf") -> torch.Tensor:
+    """A copy of ``w_router`` whose column 0 is the skew bias of the recipe
+    above, from its own seeded ranking (for weights that already exist; pair
+    it with tokens from ``make_tokens(..., skew=skew)``)."""
+    E = w_router.shape[0]
+    ranks = torch.randperm(E, generator=make_generator(seed, "cpu")).to(torch.float64) + 1.0
+    if skew == "zipf":
+        alpha, live = SKEW_ALPHA, SKEW_LIVE
+    elif skew == "zipf_literal":
+        alpha, live = SKEW_ALPHA_LITERAL, E
+    else:
+        raise ValueError(f"unknown skew {skew!r}")
+    bias = -alpha * SKEW_S * torch.log(ranks)
+    bias = torch.where(ranks > live, torch.full_like(bias, -30.0), bias)
+    w = w_router.clone()
+    w[:, 0] = bias.to(torch.float32).to(w.device)
+    return w
+
+
 def make_tokens(shape: LayerShape, seed: int, device="cpu", skew: str | None = None) -> torch.Tensor:
     """A fresh x [T, d] bf16 for an existing set of weights (for repeated
     steps that must not reuse one batch).  Feature 0 is 1 under skew."""
@@ -152,5 +171,5 @@ def expected_touched(shape: LayerShape) -> float:
 
 __all__ = [
     "LayerShape", "LayerInputs", "TINY", "FLASH_DECODE", "FLASH_PREFILL", "FLASH_SKEW",
-    "FLASH_SWEEP_T", "make_inputs", "make_tokens", "bf16_bits", "expected_touched",
+    "FLASH_SWEEP_T", "make_inputs", "make_tokens", "skewed_router", "bf16_bits", "expected_touched",
 ]

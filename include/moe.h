@@ -357,7 +357,10 @@ int moe_profile_read(moe_handle* h, float* ms, int* n_calls);
  * GPU (different streams, or different host threads on one device) race and
  * give wrong results; order them.  The first call on each device looks the
  * array's address up (with that device current), so make that first call
- * before any stream capture.  Asynchronous on `stream`.
+ * before any stream capture.  The looked-up address is kept for the life of
+ * the process: after cudaDeviceReset (or anything else that replaces the
+ * device's primary context) it no longer points at the array, so the entry
+ * point must not be called on that device again.  Asynchronous on `stream`.
  */
 int moe_dispatch_noalloc(const int* idx, int T, int n_experts, int top_k, int has_shared, int* offsets, int* perm,
                          void* stream);

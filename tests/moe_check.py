@@ -1,18 +1,26 @@
 """Shared checks of the CUDA path against the CPU oracle (test helpers).
 
 Tolerances (stated once, used by every parity test):
-* routing: expert indices and the dispatch permutation bit-exact, except for
-  tokens whose oracle gap between the k-th and (k+1)-th probability is below
-  NEAR_TIE (1e-6); for those the GPU's choice must still be a valid top-k
-  under the oracle's probabilities to within NEAR_TIE, and the output is
-  compared with the oracle recomputed for the GPU's choice;
-* probabilities: within the fp32 error bound derived in ``prob_bound``;
-* layer output: |y_gpu - y_oracle| <= OUT_TOL * RMS(y_oracle) everywhere
-  when y is fp32.  When y is stored as bf16, the storage itself moves each
-  value by up to half a bf16 ulp of y (2^-9 relative), which past about
-  5 RMS alone exceeds 2e-2 RMS; that half ulp of y_oracle is added to the
-  bound element by element, so the check measures the computation and not
-  the output format.
+* routing: expert indices and the dispatch permutation bit-exact, except at
+  near-ties, which are counted and reported (parity_log):
+  - boundary near-ties, where the oracle's gap between the k-th and the
+    (k+1)-th probability is below NEAR_TIE (1e-6): the GPU's choice must still
+    be k distinct experts, none more than NEAR_TIE below the oracle's k-th
+    probability, and the output is compared with the oracle recomputed for
+    the GPU's choice;
+  - slot-order near-ties: the GPU chose the oracle's set but ordered two of
+    its experts the other way round.  Allowed only where the oracle's two
+    probabilities differ by less than NEAR_TIE and by no more than the GPU's
+    own measured errors on them (each within the derived fp32 router bound,
+    ``prob_bound``), i.e. where the rounding of the router itself explains
+    the swap;
+* probabilities: within the fp32 error bound derived in ``prob_bound``, and
+  non-increasing along the slots (the order the GPU chose);
+* layer output: |y_gpu - y_oracle| <= OUT_TOL * RMS(y_oracle) everywhere.
+  Only the cases that pass ``storage_slack=True`` (each named where it is
+  called, with the measurement that needs it) add half a bf16 ulp of
+  y_oracle to the bound: storing y as bf16 moves each value by up to that
+  much, which past about 5 RMS alone is half the budget.
 """
 from __future__ import annotations
 
@@ -21,6 +29,8 @@ import torch
 
 import oracle
 from expert_routed_ffn_gemm_gb300 import synth
+
+import parity_log
 
 NEAR_TIE = 1e-6
 OUT_TOL = 2e-2
@@ -64,48 +74,57 @@ def prob_bound(x_bits, w_router, tokens, o_p):
 
 
 def check_routing(x_bits, w_router, k, idx, prob, gap=None, perm=None, offsets=None, has_shared=True):
-    """Returns (near-tie token list, oracle idx).
+    """Returns (exempt token list, oracle idx); records the near-tie counts.
 
-    Near-ties come in two kinds.  Boundary: the oracle's gap between the
-    k-th and (k+1)-th probability is below NEAR_TIE, so the chosen set itself
-    is decided by rounding.  Order: two adjacent probabilities inside the
-    top-k are closer than NEAR_TIE, so only their order (the slot index j)
-    is decided by rounding.  Every other token must match the oracle's idx
-    bit for bit; order near-ties must match as a set, with an order that is
-    non-increasing under the oracle's probabilities to within NEAR_TIE;
-    boundary near-ties must pick k distinct experts none of which is more
-    than NEAR_TIE below the oracle's k-th probability.
+    Every token must match the oracle's idx bit for bit, except boundary
+    near-ties (oracle gap between the k-th and (k+1)-th probability below
+    NEAR_TIE: a valid top-k under the oracle's probabilities to within
+    NEAR_TIE) and slot-order swaps of the oracle's own set where the swapped
+    probabilities differ by less than NEAR_TIE in the oracle and the GPU's
+    own probabilities (checked within the derived bound, and non-increasing
+    along the GPU's slots) put them in the GPU's order.
     """
     T = x_bits.shape[0]
     E = w_router.shape[0]
     o_idx, o_w, o_gap, o_p = oracle.route(x_bits, w_router, k, want_p=True)
-    boundary = o_gap < NEAR_TIE
-    order = np.zeros(T, bool)
-    if k > 1:
-        order = (np.diff(o_w, axis=1) > -NEAR_TIE).any(axis=1) & ~boundary
-    sure = ~boundary & ~order
     assert idx.shape == (T, k)
-    np.testing.assert_array_equal(idx[sure], o_idx[sure])
-    assert idx.min() >= 0 and idx.max() < E
-    for t in np.nonzero(order)[0]:
-        assert sorted(idx[t].tolist()) == sorted(o_idx[t].tolist())
-        assert np.all(np.diff(o_p[t, idx[t]]) <= NEAR_TIE)
-    for t in np.nonzero(boundary)[0]:
+    assert T == 0 or (idx.min() >= 0 and idx.max() < E)
+    boundary = o_gap < NEAR_TIE
+    order_cand = np.zeros(T, bool)
+    if k > 1 and T > 0:
+        order_cand = (np.diff(o_w, axis=1) > -NEAR_TIE).any(axis=1) & ~boundary
+    differ = ~(idx == o_idx).all(axis=1) if T > 0 else np.zeros(0, bool)
+    # the GPU's probabilities are non-increasing along its own slots
+    if k > 1 and T > 0:
+        assert np.all(np.diff(prob.astype(np.float64), axis=1) <= 0.0), "probabilities not ordered by slot"
+    same_set = np.array([sorted(idx[t].tolist()) == sorted(o_idx[t].tolist()) for t in np.nonzero(differ)[0]],
+                        bool)
+    differ_tok = np.nonzero(differ)[0]
+    order_diff = differ_tok[same_set] if differ_tok.size else differ_tok
+    set_diff = differ_tok[~same_set] if differ_tok.size else differ_tok
+    # a different set only at boundary near-ties
+    assert np.all(boundary[set_diff]), f"tokens {set_diff[~boundary[set_diff]][:8]} chose another set"
+    for t in set_diff:
         assert len(set(idx[t].tolist())) == k
-        kth = o_w[t, k - 1]
-        assert np.all(o_p[t, idx[t]] >= kth - NEAR_TIE)
-    near = np.nonzero(~sure)[0]
+        assert np.all(o_p[t, idx[t]] >= o_w[t, k - 1] - NEAR_TIE)
+    # a different order of the same set only across oracle near-ties
+    for t in order_diff:
+        po = o_p[t, idx[t]]  # the oracle's probabilities in the GPU's slot order
+        for i in range(k):
+            for j in range(i + 1, k):
+                if po[i] < po[j]:  # swapped against the oracle
+                    assert po[j] - po[i] < NEAR_TIE, f"token {t}: slots {i},{j} swapped across {po[j] - po[i]:.3e}"
     # probabilities of the chosen experts
     tok = np.arange(T)
-    bound = prob_bound(x_bits, w_router, tok, o_p)
+    bound = prob_bound(x_bits, w_router, tok, o_p) if T > 0 else np.zeros((0, E))
     p_ref = o_p[tok[:, None], idx]
     b_sel = bound[tok[:, None], idx]
-    assert np.all(np.abs(prob.astype(np.float64) - p_ref) <= b_sel), \
-        f"prob error {np.abs(prob - p_ref).max():.3e}"
+    err = np.abs(prob.astype(np.float64) - p_ref)
+    assert np.all(err <= b_sel), f"prob error {err.max():.3e}"
     if gap is not None:
-        gb = 2 * bound.max(axis=1)
+        gb = 2 * bound.max(axis=1) if T > 0 else np.zeros(0)
         g_ref = np.where(np.isinf(o_gap), np.inf, o_gap)
-        fin = ~np.isinf(g_ref) & sure
+        fin = ~np.isinf(g_ref) & ~boundary & ~differ
         assert np.all(np.abs(gap[fin].astype(np.float64) - g_ref[fin]) <= gb[fin] + 1e-12)
         assert np.all(np.isinf(gap[np.isinf(g_ref)]))
     if perm is not None:
@@ -113,7 +132,12 @@ def check_routing(x_bits, w_router, k, idx, prob, gap=None, perm=None, offsets=N
         np.testing.assert_array_equal(offsets[:E + 1], off_ref[:E + 1])
         assert offsets[E + 1] == off_ref[E] + (T if has_shared else 0)
         np.testing.assert_array_equal(perm, perm_ref)
-    return near, o_idx
+    p_rel = float((err / np.maximum(p_ref, 1e-300)).max()) if T > 0 else 0.0
+    parity_log.record("routing", T=T, k=k, boundary_near_ties=int(boundary.sum()),
+                      boundary_chose_other=int(set_diff.size), order_near_ties=int(order_cand.sum()),
+                      order_swapped=int(order_diff.size), max_prob_rel_err=p_rel)
+    exempt = np.nonzero(boundary | order_cand | differ)[0]
+    return exempt, o_idx
 
 
 def half_ulp_bf16(v: np.ndarray) -> np.ndarray:
@@ -123,11 +147,13 @@ def half_ulp_bf16(v: np.ndarray) -> np.ndarray:
 
 
 def check_output(x_bits, w_router, wgu_bits, wd_bits, k, y_gpu, sel, tokens=None, has_shared=True, tol=OUT_TOL,
-                 out_bf16=True, fp8=None):
+                 out_bf16=True, fp8=None, storage_slack=False):
     """Compares y_gpu (rows = tokens) with the oracle for the GPU's selection;
-    returns max|err| / RMS.  fp8 = (q_gate_up, s_gate_up, q_down, s_down):
-    the expert weights are E4M3 codes with row scales (wgu_bits / wd_bits
-    unused)."""
+    returns max|err| / RMS and records it.  fp8 = (q_gate_up, s_gate_up,
+    q_down, s_down): the expert weights are E4M3 codes with row scales
+    (wgu_bits / wd_bits unused).  The bound is tol * RMS(y_oracle) on every
+    element; storage_slack=True (bf16 y only) adds half a bf16 ulp of
+    y_oracle per element."""
     T = x_bits.shape[0]
     if tokens is None:
         tokens = np.arange(T, dtype=np.int32)
@@ -137,17 +163,32 @@ def check_output(x_bits, w_router, wgu_bits, wd_bits, k, y_gpu, sel, tokens=None
                                sel=sel_t)
     else:
         y_ref = oracle.forward_fp8(x_bits, w_router, *fp8, k, has_shared=has_shared, tokens=tokens, sel=sel_t)
-    y = y_gpu.astype(np.float64)
+    return compare(y_gpu, y_ref, tol=tol, out_bf16=out_bf16, storage_slack=storage_slack)
+
+
+def compare(y_gpu, y_ref, tol=OUT_TOL, out_bf16=True, storage_slack=False):
+    """|y_gpu - y_ref| <= tol * RMS(y_ref) on every element (storage_slack,
+    bf16 y only: plus half a bf16 ulp of y_ref); records and returns
+    max|err| / RMS."""
+    y = np.asarray(y_gpu, dtype=np.float64)
     assert np.all(np.isfinite(y))
     if not y.size:
         return 0.0
     diff = np.abs(y - y_ref)
     rms = np.sqrt((y_ref ** 2).mean())
-    bound = tol * rms + (half_ulp_bf16(y_ref) if out_bf16 else 0.0)
-    worst = np.unravel_index(np.argmax(diff - bound), diff.shape)
-    assert np.all(diff <= bound), (f"|err| {diff[worst]:.4e} > bound {bound[worst] if out_bf16 else bound:.4e} "
-                                   f"at {worst} (y_ref {y_ref[worst]:.4e}, rms {rms:.4e})")
-    return diff.max() / rms
+    plain = tol * rms
+    over = int((diff > plain).sum())
+    ratio = float(diff.max() / rms) if rms > 0 else float(diff.max())
+    slack = storage_slack and out_bf16
+    parity_log.record("output", y="bf16" if out_bf16 else "fp32", elements=int(diff.size),
+                      max_err_over_rms=ratio, over_plain_bound=over, slack=int(slack))
+    bound = plain + (half_ulp_bf16(y_ref) if slack else 0.0)
+    excess = diff - bound
+    worst = np.unravel_index(np.argmax(excess), diff.shape)
+    assert np.all(excess <= 0), (f"|err| {diff[worst]:.4e} > bound {np.broadcast_to(bound, diff.shape)[worst]:.4e} "
+                                 f"at {worst} (y_ref {y_ref[worst]:.4e}, rms {rms:.4e}, "
+                                 f"{over} elements over {tol:g} RMS)")
+    return ratio
 
 
 def sample_tokens(T, idx, n_random, seed, extra=()):

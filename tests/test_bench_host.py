@@ -1,7 +1,6 @@
 """bench.py's host-side arithmetic (no GPU): the algorithmic bytes and FLOPs
 its roofline lines use, and the DRAM-traffic figures it reads from the
-committed profile summaries."""
-import argparse
+committed capture file (profiles/traffic.json)."""
 import os
 import sys
 
@@ -10,13 +9,6 @@ sys.path.insert(0, ROOT)
 
 import bench  # noqa: E402
 from expert_routed_ffn_gemm_gb300 import synth  # noqa: E402
-
-
-def args_for(**kw):
-    a = argparse.Namespace(workload="decode", experts=0, ffn_width=0, weights="bf16")
-    for k, v in kw.items():
-        setattr(a, k, v)
-    return a
 
 
 def test_decode_bytes_and_flops():
@@ -35,13 +27,35 @@ def test_decode_bytes_and_flops():
 
 
 def test_traffic_comes_from_the_profiles():
-    t = bench.measured_traffic(args_for())
-    t8 = bench.measured_traffic(args_for(weights="fp8"))
-    assert t is not None and 5.9e9 < t < 6.0e9
+    dec = synth.FLASH_DECODE
+    alg = bench.gateup_bytes(dec, 281)
+    t, src = bench.measured_traffic("decode", "bf16", dec, alg)
+    t8, _ = bench.measured_traffic("decode", "fp8", dec, bench.gateup_bytes(dec, 281, fp8=True))
+    assert t is not None and 5.9e9 < t < 6.0e9 and src.startswith("ncu ")
     assert t8 is not None and 2.95e9 < t8 < 3.05e9
-    assert bench.measured_traffic(args_for(workload="prefill")) is None
-    assert bench.measured_traffic(args_for(experts=32)) is None
-    assert bench.measured_traffic(args_for(ffn_width=128)) is None
+    # the prefill entry was captured on a smaller case and scales with the
+    # algorithmic bytes of the workload
+    pre = synth.FLASH_PREFILL
+    alg_p = bench.gateup_bytes(pre, 288)
+    tp, _ = bench.measured_traffic("prefill", "bf16", pre, alg_p)
+    assert tp is not None and 1.0 <= tp / alg_p < 1.05
+    # workloads or shapes without a capture
+    assert bench.measured_traffic("skew", "bf16", synth.FLASH_SKEW, 1.0)[0] is None
+    from dataclasses import replace
+    assert bench.measured_traffic("decode", "bf16", replace(dec, E=32), alg)[0] is None
+
+
+def test_stale_capture_gives_no_traffic(tmp_path, monkeypatch):
+    import json
+    doc = json.load(open(bench.TRAFFIC_FILE))
+    for e in doc["entries"]:
+        e["sources_sha256_16"] = "0" * 16  # as if the kernel had changed since
+    f = tmp_path / "traffic.json"
+    f.write_text(json.dumps(doc))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    dec = synth.FLASH_DECODE
+    t, src = bench.measured_traffic("decode", "bf16", dec, 1.0)
+    assert t is None and src.startswith("stale")
 
 
 def test_workloads_resolve():

@@ -77,7 +77,10 @@ def test_expert_parallel_matches_whole_layer(ep_size, Ts, monkeypatch):
         y_ref = whole.forward(x)
         assert torch.equal(y, y_ref), f"rank {r}: EP output differs from the whole-layer call"
         idx, _, _, _, _ = whole.route(x)
-        check_output(synth.bf16_bits(x), wr_h, wgu_h, wd_h, shape.k, cpu(y.float()), cpu(idx))
+        # bf16 y: measured max|err|/RMS 2.27e-2 on (2, [1500, 300]), two
+        # elements near 6 RMS where half a bf16 ulp of y alone is 2.0e-2 RMS
+        check_output(synth.bf16_bits(x), wr_h, wgu_h, wd_h, shape.k, cpu(y.float()), cpu(idx),
+                     storage_slack=True)
     whole.close()
 
 
@@ -91,9 +94,13 @@ def test_expert_parallel_flash_shape(monkeypatch):
     xs = [synth.make_tokens(shape.with_tokens(T), seed=90 + r, device=DEV) for r, T in enumerate(Ts)]
     ys = run_ranks(inp, xs, 8, max_recv=sum(Ts) * shape.k)
     whole = binding.MoeLayer(inp.w_router, inp.w_gate_up, inp.w_down, shape.k, 16)
+    _, wr_h, wgu_h, wd_h = host_bits(inp)
     for x, y in zip(xs, ys):
         if x.shape[0]:
             assert torch.equal(y, whole.forward(x))
+            # and the oracle, for the GPU's own selection (near-ties)
+            idx, _, _, _, _ = whole.route(x)
+            check_output(synth.bf16_bits(x), wr_h, wgu_h, wd_h, shape.k, cpu(y.float()), cpu(idx))
     whole.close()
 
 

@@ -10,7 +10,7 @@ import torch
 import oracle
 from expert_routed_ffn_gemm_gb300 import binding, synth
 
-from moe_check import check_output, check_routing, cpu, sample_tokens
+from moe_check import check_output, check_routing, compare, cpu, sample_tokens
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -37,11 +37,12 @@ def test_quantiser_bit_exact():
     np.testing.assert_array_equal(cpu(q), oq)
 
 
-def fp8_case(shape, seed, tiles=(0, 0), n_sample=None, max_tokens=None, out_fp32=False, x2=True, ksplit=None):
+def fp8_case(shape, seed, tiles=(0, 0), n_sample=None, max_tokens=None, out_fp32=False, x2=True, ksplit=None,
+             storage_slack=False):
     """x2: the gate/up GEMM on E4M3 tensor cores with the token rows as two
     E4M3 terms (the default), or on fp16 tensor cores with the weights widened
     (MOE_FP8_X2=0).  ksplit: K parts forced on the expert GEMMs (None: by
-    work items)."""
+    work items).  storage_slack: see moe_check.check_output."""
     import os
     inp = synth.make_inputs(shape, seed=seed, device=DEV)
     q_gu, s_gu, q_d, s_d = quantised(inp)
@@ -76,16 +77,19 @@ def fp8_case(shape, seed, tiles=(0, 0), n_sample=None, max_tokens=None, out_fp32
                                                                                       seed, near)
     y_h = cpu(y[torch.from_numpy(tokens).long().to(DEV)].float())
     ratio = check_output(xb, wr, None, None, shape.k, y_h, idx_h, tokens=tokens, has_shared=shape.has_shared,
-                         out_bf16=not out_fp32, fp8=fp8)
+                         out_bf16=not out_fp32, fp8=fp8, storage_slack=storage_slack)
     y2 = layer.forward(x)
     assert torch.equal(y, y2)
     layer.close()
     return ratio
 
 
+@pytest.mark.parametrize("out_fp32", [False, True])
 @pytest.mark.parametrize("x2", [True, False])
-def test_fp8_tiny(x2):
-    fp8_case(synth.TINY, seed=0, x2=x2)
+def test_fp8_tiny(x2, out_fp32):
+    # bf16 y: measured max|err|/RMS 2.21e-2, one element at 6.1 RMS where half
+    # a bf16 ulp of y alone is 2.0e-2 RMS; fp32 y meets the plain bound
+    fp8_case(synth.TINY, seed=0, x2=x2, out_fp32=out_fp32, storage_slack=not out_fp32)
 
 
 @pytest.mark.parametrize("x2", [True, False])
@@ -134,8 +138,11 @@ def test_fp8_two_term_rows_with_wide_dynamic_range():
     wr = cpu(inp.w_router)
     idx, _, _, _, _ = layer.route(inp.x)
     fp8 = (cpu(q_gu), cpu(s_gu), cpu(q_d), cpu(s_d))
-    check_output(xb, wr, None, None, shape.k, cpu(y.float()), cpu(idx), fp8=fp8)
-    assert torch.all(y[3] == 0) or torch.isfinite(y[3].float()).all()
+    # bf16 y: rows scaled by 300 put y at up to 16 RMS, where half a bf16 ulp
+    # of y alone is 4.8e-2 RMS (measured max|err|/RMS 5.55e-2)
+    check_output(xb, wr, None, None, shape.k, cpu(y.float()), cpu(idx), fp8=fp8, storage_slack=True)
+    # a zero token row: every expert's input is zero, so is every output
+    assert torch.all(y[3] == 0)
     layer.close()
 
 
@@ -168,10 +175,7 @@ def test_fp8_smaller_top_k_renormalized():
     idx, _, _, _, _ = layer.route(inp.x, top_k=4, renormalize=True)  # the GPU's selection (near-ties)
     y_ref = oracle.forward_fp8(xb, wr, cpu(q_gu), cpu(s_gu), cpu(q_d), cpu(s_d), 4, sel=cpu(idx),
                                renormalize=True)
-    rms = np.sqrt((y_ref ** 2).mean())
-    diff = np.abs(cpu(y.float()) - y_ref)
-    bound = 2e-2 * rms + np.ldexp(1.0, np.frexp(np.abs(y_ref))[1] - 9)
-    assert np.all(diff <= bound), f"max err {diff.max():.3e} vs rms {rms:.3e}"
+    compare(cpu(y.float()), y_ref)
     layer.close()
 
 
@@ -190,3 +194,68 @@ def test_fp8_gemm_k_split(parts, T, d, F, tiles):
     shape = synth.LayerShape(T=T, d=d, E=16, k=2, F=F)
     fp8_case(shape, seed=90 + T + parts, tiles=tiles, max_tokens=64, ksplit=parts)
 
+
+
+# ---------------------------------------------------------------- full size --
+
+@pytest.fixture(scope="module")
+def flash_fp8_weights():
+    """E4M3 codes and scales of the flash-shaped layer's weights (d=4096, 288
+    routed + 1 shared, width 1280), made once for the module."""
+    shape = synth.FLASH_DECODE
+    inp = synth.make_inputs(shape, seed=0, device=DEV)
+    q = quantised(inp)
+    wr = inp.w_router
+    del inp
+    host = tuple(cpu(t) for t in q)
+    yield wr, q, host
+
+
+def flash_fp8_case(weights, T, seed, x2, n_sample=64, skew=None):
+    """T tokens on the flash-shaped FP8 layer: routing and dispatch on every
+    token, the output on a seeded sample plus every near-tie token plus one
+    token per expert used."""
+    import os
+    wr, (q_gu, s_gu, q_d, s_d), fp8_host = weights
+    shape = synth.FLASH_DECODE.with_tokens(T)
+    x = synth.make_tokens(shape, seed=seed, device=DEV, skew=skew)
+    if skew is not None:
+        wr = synth.skewed_router(wr, seed, skew)
+    old = os.environ.get("MOE_FP8_X2")
+    os.environ["MOE_FP8_X2"] = "1" if x2 else "0"
+    try:
+        layer = binding.MoeLayer.fp8(wr, q_gu, s_gu, q_d, s_d, shape.k, T)
+    finally:
+        if old is None:
+            os.environ.pop("MOE_FP8_X2", None)
+        else:
+            os.environ["MOE_FP8_X2"] = old
+    idx, prob, perm, offsets, gap = layer.route(x)
+    y = layer.forward(x)
+    assert layer.check() == binding.MOE_OK
+    xb = synth.bf16_bits(x)
+    wr_h = cpu(wr)
+    idx_h = cpu(idx)
+    near, _ = check_routing(xb, wr_h, shape.k, idx_h, cpu(prob), cpu(gap), cpu(perm), cpu(offsets))
+    tokens = sample_tokens(T, idx_h, n_sample, seed, near)
+    y_h = cpu(y[torch.from_numpy(tokens).long().to(DEV)].float())
+    ratio = check_output(xb, wr_h, None, None, shape.k, y_h, idx_h, tokens=tokens, fp8=fp8_host)
+    y2 = layer.forward(x)
+    assert torch.equal(y, y2)
+    layer.close()
+    return ratio
+
+
+@pytest.mark.parametrize("x2", [True, False])
+@pytest.mark.parametrize("T", [512, 2048, 8192])
+def test_fp8_flash_many_tokens(flash_fp8_weights, T, x2):
+    # the E4M3 kernels at the flash shape with many rows per group: 64- and
+    # 128-row tiles, thousands of two-term rows, the chunked dispatch
+    flash_fp8_case(flash_fp8_weights, T, seed=300 + T, x2=x2)
+
+
+@pytest.mark.parametrize("x2", [True, False])
+def test_fp8_flash_skewed(flash_fp8_weights, x2):
+    # Zipf-skewed routing, T=4096: the hottest expert ~10x the mean rows,
+    # 40 experts unused
+    flash_fp8_case(flash_fp8_weights, 4096, seed=102, x2=x2, skew="zipf")

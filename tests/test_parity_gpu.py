@@ -37,7 +37,7 @@ def make_layer(inp, max_tokens=None, tiles=(0, 0), out_fp32=False, has_shared=Tr
     return layer, x
 
 
-def run_and_check(inp, tiles=(0, 0), tokens=None, out_fp32=False, max_tokens=None):
+def run_and_check(inp, tiles=(0, 0), tokens=None, out_fp32=False, max_tokens=None, storage_slack=False):
     shape = inp.shape
     layer, x = make_layer(inp, max_tokens=max_tokens, tiles=tiles, out_fp32=out_fp32,
                           has_shared=shape.has_shared)
@@ -54,7 +54,7 @@ def run_and_check(inp, tiles=(0, 0), tokens=None, out_fp32=False, max_tokens=Non
     else:
         tokens = sample_tokens(shape.T, idx_h, tokens, seed=1, extra=near)
     ratio = check_output(xb, wr, wgu, wd, shape.k, y_h[tokens], idx_h, tokens=tokens,
-                         has_shared=shape.has_shared, out_bf16=not out_fp32)
+                         has_shared=shape.has_shared, out_bf16=not out_fp32, storage_slack=storage_slack)
     layer.close()
     return ratio, len(near)
 
@@ -96,9 +96,13 @@ def test_many_tokens_small_layer(T):
     synth.LayerShape(T=1024, d=256, E=40, k=6, F=128),                   # first token count of the chunked path
     synth.LayerShape(T=1025, d=128, E=300, k=8, F=128),                  # 16 slots per lane in the top-k
 ])
-def test_combine_terms_and_chunked_dispatch(shape):
+@pytest.mark.parametrize("out_fp32", [False, True])
+def test_combine_terms_and_chunked_dispatch(shape, out_fp32):
+    # bf16 y: measured max|err|/RMS 2.62e-2 on the 1024-token case, two
+    # elements near 6 RMS where half a bf16 ulp of y alone is 2.0e-2 RMS; fp32
+    # y meets the plain bound
     inp = synth.make_inputs(shape, seed=60 + shape.T % 11 + shape.k)
-    run_and_check(inp, tokens=96 if shape.T > 1000 else None)
+    run_and_check(inp, tokens=96 if shape.T > 1000 else None, out_fp32=out_fp32, storage_slack=not out_fp32)
 
 
 def test_chunked_dispatch_ties_and_one_hot():
@@ -280,11 +284,7 @@ def flash_case(flash_weights, T, seed, n_sample=None, skew=None, out_fp32=False)
     wr = inp.w_router
     wr_h2 = wr_h
     if skew is not None:
-        wr = inp.w_router.clone()
-        ranks = torch.randperm(shape.E, generator=synth.make_generator(seed, "cpu")).double() + 1.0
-        bias = -synth.SKEW_ALPHA * synth.SKEW_S * torch.log(ranks)
-        bias = torch.where(ranks > synth.SKEW_LIVE, torch.full_like(bias, -30.0), bias)
-        wr[:, 0] = bias.to(torch.float32).to(DEV)
+        wr = synth.skewed_router(inp.w_router, seed, skew)
         wr_h2 = cpu(wr)
     layer = binding.MoeLayer(wr, inp.w_gate_up, inp.w_down, shape.k, T, out_fp32=out_fp32)
     idx, prob, perm, offsets, gap = layer.route(x)
