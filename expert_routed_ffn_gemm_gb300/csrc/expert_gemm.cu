@@ -129,13 +129,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto weight_row = [&](const Item& it) {
         return weight_group(args, it.g) * args.rows_per_group + it.m * (GATEUP ? kBlockM / 2 : kBlockM);
       };
+      auto rows_of = [&](int item, int& row_w, int& row_act) {
+        const Item it = decode_item(item / ks, args.m_tiles, tile_start, G, n_items / ks, args.reverse);
+        row_w = weight_row(it);
+        row_act = __ldg(args.offsets + it.g) + it.n * BN;
+      };
       uint32_t stage = 0, phase = 0;
       long issued = 0;
       bool ok = true;
+      int next_w = 0, next_act = 0;
+      if (static_cast<int>(blockIdx.x) < n_items) rows_of(blockIdx.x, next_w, next_act);
       for (int item = blockIdx.x; ok && item < n_items && !*abort_flag; item += gridDim.x) {
-        const Item it = decode_item(item / ks, args.m_tiles, tile_start, G, n_items / ks, args.reverse);
-        const int row_w = weight_row(it);
-        const int row_act = __ldg(args.offsets + it.g) + it.n * BN;
+        const int row_w = next_w, row_act = next_act;
         const int part = item % ks;
         const int kb1 = min(k_steps_all, (part + 1) * k_per);
         for (int kb = part * k_per; kb < kb1; ++kb) {
@@ -157,6 +162,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             stage = 0;
             phase ^= 1u;
           }
+          // the next item's rows, worked out while this item's loads are in
+          // flight (its offsets come from global memory)
+          if (kb == part * k_per && item + static_cast<int>(gridDim.x) < n_items)
+            rows_of(item + gridDim.x, next_w, next_act);
         }
       }
       // Drain: the last load issued into each stage must have landed before

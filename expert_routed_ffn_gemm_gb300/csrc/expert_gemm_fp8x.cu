@@ -148,13 +148,18 @@ __global__ void __launch_bounds__(kThreadsX, 1)
       // ---------------------------------------------------------- producer --
       const uint64_t pol_w = policy_evict_first();   // weights: streamed once
       const uint64_t pol_act = policy_evict_last();  // token rows: re-read by the other weight tiles
+      auto rows_of = [&](int item, int& row_w, int& row_act) {
+        const Item it = decode_item(item / ks, args.m_tiles, tile_start, G, n_base, args.reverse);
+        row_w = weight_group(args, it.g) * args.rows_per_group + it.m * (GATEUP ? kBlockM / 2 : kBlockM);
+        row_act = __ldg(args.offsets + it.g) + it.n * BN;
+      };
       uint32_t stage = 0, phase = 0;
       long issued = 0;
       bool ok = true;
+      int next_w = 0, next_act = 0;
+      if (static_cast<int>(blockIdx.x) < n_items) rows_of(blockIdx.x, next_w, next_act);
       for (int item = blockIdx.x; ok && item < n_items && !*abort_flag; item += gridDim.x) {
-        const Item it = decode_item(item / ks, args.m_tiles, tile_start, G, n_base, args.reverse);
-        const int row_w = weight_group(args, it.g) * args.rows_per_group + it.m * (GATEUP ? kBlockM / 2 : kBlockM);
-        const int row_act = __ldg(args.offsets + it.g) + it.n * BN;
+        const int row_w = next_w, row_act = next_act;
         const int part = item % ks;
         const int kb1 = min(k_steps, (part + 1) * k_per);
         for (int kb = part * k_per; kb < kb1; ++kb) {
@@ -175,6 +180,10 @@ __global__ void __launch_bounds__(kThreadsX, 1)
             stage = 0;
             phase ^= 1u;
           }
+          // the next item's rows, worked out while this item's loads are in
+          // flight (its offsets come from global memory)
+          if (kb == part * k_per && item + static_cast<int>(gridDim.x) < n_items)
+            rows_of(item + gridDim.x, next_w, next_act);
         }
       }
       for (int s = 0; s < C::STAGES; ++s) {

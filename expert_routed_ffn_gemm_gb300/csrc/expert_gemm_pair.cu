@@ -28,6 +28,10 @@ using namespace gemm;
 constexpr int kThreads = 192;
 constexpr int kPairN = 256;  // token rows of a pair tile (N of the pair MMA)
 constexpr int kHalfN = 128;  // token rows each CTA loads
+// N of an M = 256 pair MMA: any multiple of 16 up to 256, so a tile's rows are
+// rounded up to 16 (8 from each CTA); 32 would add 8 columns per tile on
+// average at prefill sizes (~228 rows per group).
+constexpr int kPairStep = 16;
 constexpr int kSettleNs = 200000;
 
 template <bool GATEUP>
@@ -133,21 +137,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_act = policy_evict_last();
       const int k_steps = args.K / kBlockK;
+      // the rows an item loads: K3: 64 gate rows (+ the matching 64 up rows
+      // at +F) per CTA, 128 features per pair tile; K4: 128 rows per CTA, 256
+      // per pair tile.  The pair MMA takes N/2 token rows from each CTA: N =
+      // the tile's rows rounded up to kPairStep, so the odd CTA's rows start at
+      // N/2.
+      auto rows_of = [&](int item, int& row_w, int& row_act) {
+        const Item it = decode_item(item, args.m_tiles, tile_start, G, n_items, args.reverse);
+        const int wg = weight_group(args, it.g);
+        row_w = GATEUP ? wg * args.rows_per_group + it.m * kBlockM + static_cast<int>(rank) * 64
+                       : wg * args.rows_per_group + it.m * 2 * kBlockM + static_cast<int>(rank) * kBlockM;
+        const int g_row0 = __ldg(args.offsets + it.g);
+        const int n_mma = mma_width(__ldg(args.offsets + it.g + 1) - g_row0 - it.n * kPairN, kPairStep, kPairN);
+        row_act = g_row0 + it.n * kPairN + static_cast<int>(rank) * (n_mma / 2);
+      };
       uint32_t stage = 0, phase = 0;
       long issued = 0;
       bool ok = true;
+      int row_w = 0, row_act = 0, next_w = 0, next_act = 0;
+      if (pair < n_items) rows_of(pair, next_w, next_act);
       for (int item = pair; ok && item < n_items && !*abort_flag; item += n_pairs) {
-        const Item it = decode_item(item, args.m_tiles, tile_start, G, n_items, args.reverse);
-        // K3: 64 gate rows (+ the matching 64 up rows at +F) per CTA, 128
-        // features per pair tile; K4: 128 rows per CTA, 256 per pair tile.
-        const int wg = weight_group(args, it.g);
-        const int row_w = GATEUP ? wg * args.rows_per_group + it.m * kBlockM + static_cast<int>(rank) * 64
-                                 : wg * args.rows_per_group + it.m * 2 * kBlockM + static_cast<int>(rank) * kBlockM;
-        // the pair MMA takes N/2 token rows from each CTA: N = the tile's rows
-        // rounded up to 32, so the odd CTA's rows start at N/2
-        const int g_row0 = __ldg(args.offsets + it.g);
-        const int n_mma = mma_width(__ldg(args.offsets + it.g + 1) - g_row0 - it.n * kPairN, 32, kPairN);
-        const int row_act = g_row0 + it.n * kPairN + static_cast<int>(rank) * (n_mma / 2);
+        row_w = next_w;
+        row_act = next_act;
         for (int kb = 0; kb < k_steps; ++kb) {
           if (!wait_cluster(&empty[stage], phase ^ 1u, limit, abort_flag)) {
             record_abort(abort_flag, args.err);
@@ -168,6 +179,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             stage = 0;
             phase ^= 1u;
           }
+          // the next item's rows, worked out while this item's loads are in
+          // flight (its offsets come from global memory)
+          if (kb == 0 && item + n_pairs < n_items) rows_of(item + n_pairs, next_w, next_act);
         }
       }
       if (rank == 0) {
@@ -186,10 +200,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int k_steps = args.K / kBlockK;
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool issued_any = false, ok = true;
-      // N of the pair MMAs: the tile's rows rounded up to 32; the next
+      // N of the pair MMAs: the tile's rows rounded up to kPairStep; the next
       // item's descriptor is worked out while this item's MMAs run
       uint32_t next_idesc =
-          item_idesc(pair, n_items, args.reverse, args.m_tiles, tile_start, G, args.offsets, 2 * kBlockM, 32, kPairN);
+          item_idesc(pair, n_items, args.reverse, args.m_tiles, tile_start, G, args.offsets, 2 * kBlockM, kPairStep,
+                     kPairN);
       for (int item = pair; ok && item < n_items && !*abort_flag; item += n_pairs) {
         const uint32_t idesc = next_idesc;
         if (!wait_cluster(&acc_empty[acc], acc_phase ^ 1u, limit, abort_flag)) {
@@ -219,7 +234,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           if (kb == 0)
             next_idesc = item_idesc(item + n_pairs, n_items, args.reverse, args.m_tiles, tile_start, G, args.offsets,
-                                    2 * kBlockM, 32, kPairN);
+                                    2 * kBlockM, kPairStep, kPairN);
         }
         if (!ok) break;
         tc_commit_pair_multicast(&acc_full[acc], 0x3);
@@ -238,14 +253,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int row = q * 32 + lane;
     uint32_t acc = 0, acc_phase = 0, it_par = 0, chunk_par = 0;
-    for (int item = pair; item < n_items; item += n_pairs) {
-      const Item it = decode_item(item, args.m_tiles, tile_start, G, n_items, args.reverse);
+    auto tile_rows = [&](int item, Item& it, int& row0, int& valid) {
+      it = decode_item(item, args.m_tiles, tile_start, G, n_items, args.reverse);
       const int g_row0 = __ldg(args.offsets + it.g);
       const int g_rows = __ldg(args.offsets + it.g + 1) - g_row0;
-      const int row0 = g_row0 + it.n * kPairN;
-      const int valid = min(kPairN, g_rows - it.n * kPairN);
-      float wreg[kPairN / 32];
-      if (!GATEUP) load_gate_weights<kPairN>(wreg, row0, valid, lane, args.perm, args.prob, args.Tk);
+      row0 = g_row0 + it.n * kPairN;
+      valid = min(kPairN, g_rows - it.n * kPairN);
+    };
+    // K4: the gate weights of an item are fetched one item ahead — the
+    // permutation entries while the previous item's accumulator is stored,
+    // the probabilities they point at right after — so no dependent load sits
+    // between an accumulator becoming ready and its stores
+    float wreg[kPairN / 32];
+    int pe[kPairN / 32];
+    if (!GATEUP && pair < n_items) {
+      Item it0;
+      int r0, v0;
+      tile_rows(pair, it0, r0, v0);
+      gate_perm_entries<kPairN>(pe, r0, v0, lane, args.perm, args.Tk);
+      gate_probs<kPairN>(wreg, pe, args.prob);
+    }
+    for (int item = pair; item < n_items; item += n_pairs) {
+      Item it;
+      int row0, valid;
+      tile_rows(item, it, row0, valid);
+      const bool has_next = item + n_pairs < n_items;
       // one decision for all four epilogue warps (they meet at named barriers)
       const bool ok = __all_sync(0xffffffffu, wait_cluster(&acc_full[acc], acc_phase, limit, abort_flag));
       if (lane == 0) s_ok[it_par * 4 + q] = ok ? 1 : 0;
@@ -263,9 +295,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         epilogue_gateup<kPairN>(taddr, row, it.m * kBlockM + static_cast<int>(rank) * 64, row0, valid,
                                 static_cast<bf16*>(args.out), args.out_ld, xchg, chunk_par);
       } else {
-        epilogue_down<kPairN>(taddr, it.m * 2 * kBlockM + static_cast<int>(rank) * kBlockM + row, row0, valid,
-                              wreg, static_cast<__half*>(args.out), args.out_exp, args.out_ld,
-                              __ldg(args.chunk_base + it.g) + it.n * (kPairN / kYpRows));
+        Item it_n;
+        int row0_n = 0, valid_n = 0;
+        if (has_next) {
+          tile_rows(item + n_pairs, it_n, row0_n, valid_n);
+          gate_perm_entries<kPairN>(pe, row0_n, valid_n, lane, args.perm, args.Tk);
+        }
+        epilogue_down_pipelined<kPairN>(taddr, it.m * 2 * kBlockM + static_cast<int>(rank) * kBlockM + row, row0,
+                                        valid, wreg, static_cast<__half*>(args.out), args.out_exp, args.out_ld,
+                                        __ldg(args.chunk_base + it.g) + it.n * (kPairN / kYpRows));
+        if (has_next) gate_probs<kPairN>(wreg, pe, args.prob);
       }
       tc_fence_before();
       __syncwarp();

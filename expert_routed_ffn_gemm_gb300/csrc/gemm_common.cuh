@@ -75,7 +75,7 @@ __device__ __forceinline__ void build_tile_start(const int* offsets, int G, int 
 }
 
 // MMA width for a token tile with `valid` rows: the rows rounded up to a
-// multiple of `step` (16 for one CTA; 32 for a pair, 16 rows per CTA),
+// multiple of `step` (16 for one CTA and for a pair, 8 rows per CTA),
 // at most the tile width.  Columns past it are neither loaded into the MMA
 // nor computed; the epilogue only reads the valid columns.
 __device__ __forceinline__ int mma_width(int valid, int step, int tile) {
@@ -145,8 +145,11 @@ __device__ __forceinline__ __half to_out(float v, __half*) { return __float2half
 // K3 epilogue over the `valid` columns of a BN-column accumulator whose TMEM
 // rows 0..63 hold gate values and rows 64..127 the up values of the same 64
 // features.  Gate-row threads keep columns 0..7 of each 16-column chunk and
-// hand 8..15 to their up-row partner through xchg ([2][2][64][8] fp32), which
-// hands back 0..7; H[row0 + col][feat_base + (row & 63)] = silu(g) * u, where
+// hand 8..15 to their up-row partner through xchg, which hands back 0..7;
+// xchg is float4 [2 chunk parities][2 sides][2 halves][64 features], so the
+// 32 lanes of a warp store and load 512 contiguous bytes per float4 (four
+// shared-memory wavefronts, no bank conflicts).
+// H[row0 + col][feat_base + (row & 63)] = silu(g) * u, where
 // g and u are the accumulators times the `scale` of their own weight row (1
 // for bf16 weights).  H is bf16 or fp16 (OutT).
 // vals (or NULL): this thread's row of the accumulator, already summed over K
@@ -169,19 +172,19 @@ __device__ __forceinline__ void epilogue_gateup(uint32_t taddr, int row, int fea
       tmem_ld16(taddr + c0, v);
       tmem_ld_wait();
     }
-    float* mine_out = xchg + ((chunk_par * 2 + (is_gate ? 1 : 0)) * 64 + fl) * 8;
-    const float* peer_in = xchg + ((chunk_par * 2 + (is_gate ? 0 : 1)) * 64 + fl) * 8;
+    float4* mine_out = reinterpret_cast<float4*>(xchg) + (chunk_par * 2 + (is_gate ? 1 : 0)) * 128 + fl;
+    const float4* peer_in = reinterpret_cast<const float4*>(xchg) + (chunk_par * 2 + (is_gate ? 0 : 1)) * 128 + fl;
     float give[8], keep[8];  // compile-time register indices only
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
       give[c] = scale * __uint_as_float(is_gate ? v[8 + c] : v[c]);
       keep[c] = scale * __uint_as_float(is_gate ? v[c] : v[8 + c]);
     }
-    reinterpret_cast<float4*>(mine_out)[0] = make_float4(give[0], give[1], give[2], give[3]);
-    reinterpret_cast<float4*>(mine_out)[1] = make_float4(give[4], give[5], give[6], give[7]);
+    mine_out[0] = make_float4(give[0], give[1], give[2], give[3]);
+    mine_out[64] = make_float4(give[4], give[5], give[6], give[7]);
     named_bar_sync(kEpilogueBar, 128);
-    const float4 p0 = reinterpret_cast<const float4*>(peer_in)[0];
-    const float4 p1 = reinterpret_cast<const float4*>(peer_in)[1];
+    const float4 p0 = peer_in[0];
+    const float4 p1 = peer_in[64];
     const float peer[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
     const int col0 = c0 + (is_gate ? 0 : 8);
 #pragma unroll
@@ -278,6 +281,28 @@ __device__ __forceinline__ void load_gate_weights(float (&wreg)[(BN + 31) / 32],
   }
 }
 
+// load_gate_weights in two phases, for fetching the next item's weights
+// during this item's epilogue: gate_perm_entries loads the permutation entry
+// of every column (-1: a shared-expert row, weight 1; -2: past the tile's
+// valid columns, weight 0), gate_probs then the probabilities they point at.
+template <int BN>
+__device__ __forceinline__ void gate_perm_entries(int (&pe)[(BN + 31) / 32], int row0, int valid, int lane,
+                                                  const int* perm, int Tk) {
+#pragma unroll
+  for (int i = 0; i < (BN + 31) / 32; ++i) {
+    const int c = i * 32 + lane;
+    const int pos = row0 + c;
+    pe[i] = (c < valid) ? ((pos < Tk) ? __ldg(perm + pos) : -1) : -2;
+  }
+}
+
+template <int BN>
+__device__ __forceinline__ void gate_probs(float (&wreg)[(BN + 31) / 32], const int (&pe)[(BN + 31) / 32],
+                                           const float* prob) {
+#pragma unroll
+  for (int i = 0; i < (BN + 31) / 32; ++i) wreg[i] = pe[i] >= 0 ? __ldg(prob + pe[i]) : (pe[i] == -1 ? 1.0f : 0.0f);
+}
+
 // Power-of-two exponent for a block of values whose largest magnitude has the
 // fp32 bit pattern `amax`: 2^-e * amax lands in [2^14, 2^15), so every value of
 // the block scaled by 2^-e is an fp16 normal or zero below 2^15 (no overflow)
@@ -316,19 +341,19 @@ __device__ __forceinline__ void epilogue_gateup_x2(uint32_t taddr, int row, int 
       const float ts = (c0 + c < valid) ? __ldg(tok_scale + row0 + c0 + c) : 0.f;
       v[c] = (__uint_as_float(vh[c]) + __uint_as_float(vl[c])) * (scale * ts);
     }
-    float* mine_out = xchg + ((chunk_par * 2 + (is_gate ? 1 : 0)) * 64 + fl) * 8;
-    const float* peer_in = xchg + ((chunk_par * 2 + (is_gate ? 0 : 1)) * 64 + fl) * 8;
+    float4* mine_out = reinterpret_cast<float4*>(xchg) + (chunk_par * 2 + (is_gate ? 1 : 0)) * 128 + fl;
+    const float4* peer_in = reinterpret_cast<const float4*>(xchg) + (chunk_par * 2 + (is_gate ? 0 : 1)) * 128 + fl;
     float give[8], keep[8];
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
       give[c] = is_gate ? v[8 + c] : v[c];
       keep[c] = is_gate ? v[c] : v[8 + c];
     }
-    reinterpret_cast<float4*>(mine_out)[0] = make_float4(give[0], give[1], give[2], give[3]);
-    reinterpret_cast<float4*>(mine_out)[1] = make_float4(give[4], give[5], give[6], give[7]);
+    mine_out[0] = make_float4(give[0], give[1], give[2], give[3]);
+    mine_out[64] = make_float4(give[4], give[5], give[6], give[7]);
     named_bar_sync(kEpilogueBar, 128);
-    const float4 p0 = reinterpret_cast<const float4*>(peer_in)[0];
-    const float4 p1 = reinterpret_cast<const float4*>(peer_in)[1];
+    const float4 p0 = peer_in[0];
+    const float4 p1 = peer_in[64];
     const float peer[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
     const int col0 = c0 + (is_gate ? 0 : 8);
 #pragma unroll
@@ -354,6 +379,59 @@ __device__ __forceinline__ int block_exponent(uint32_t amax) {
 // the tile's first row (tile rows start at multiples of 16 inside the group).
 // lo_off > 0: the accumulator holds two terms per column, at c and at
 // lo_off + c (two-term E4M3 token rows), and acc[col] is their sum.
+// One 16-column chunk of epilogue_down from its accumulator values acc[16].
+template <int BN>
+__device__ __forceinline__ void down_chunk(const float (&acc)[16], int c0, int feat, int row0, int valid,
+                                           const float (&wreg)[(BN + 31) / 32], __half* Y, int8_t* Ye, int ldy,
+                                           int chunk0, float row_scale) {
+  float y[16];
+  uint32_t amax = 0;
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    const int col = c0 + c;
+    y[c] = __shfl_sync(0xffffffffu, wreg[col >> 5], col & 31) * (row_scale * acc[c]);
+    amax = max(amax, __float_as_uint(y[c]) & 0x7fffffffu);
+  }
+  const int e = block_exponent(amax);
+  const float down = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, exact
+  Ye[static_cast<size_t>(chunk0 + c0 / 16) * ldy + feat] = static_cast<int8_t>(e);
+#pragma unroll
+  for (int c = 0; c < 16; ++c)
+    if (c0 + c < valid) Y[static_cast<size_t>(row0 + c0 + c) * ldy + feat] = __float2half_rn(y[c] * down);
+}
+
+// epilogue_down for one accumulator term read from tensor memory, with the
+// next chunk's tensor-memory load in flight while a chunk is scaled and
+// stored (the same arithmetic, chunk by chunk, as epilogue_down).
+template <int BN>
+__device__ __forceinline__ void epilogue_down_pipelined(uint32_t taddr, int feat, int row0, int valid,
+                                                        const float (&wreg)[(BN + 31) / 32], __half* Y, int8_t* Ye,
+                                                        int ldy, int chunk0, float row_scale = 1.0f) {
+  static_assert(kYpRows == 16 && BN % 32 == 0, "16-column chunks, in pairs");
+  uint32_t va[16], vb[16];
+  tmem_ld16(taddr, va);
+  tmem_ld_wait_regs(va);
+#pragma unroll
+  for (int c0 = 0; c0 < BN; c0 += 32) {
+    if (c0 >= valid) break;
+    const bool more_b = c0 + 16 < valid;
+    if (more_b) tmem_ld16(taddr + c0 + 16, vb);
+    float acc[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) acc[c] = __uint_as_float(va[c]);
+    down_chunk<BN>(acc, c0, feat, row0, valid, wreg, Y, Ye, ldy, chunk0, row_scale);
+    if (!more_b) break;
+    tmem_ld_wait_regs(vb);
+    const bool more_a = c0 + 32 < valid;
+    if (more_a) tmem_ld16(taddr + c0 + 32, va);
+#pragma unroll
+    for (int c = 0; c < 16; ++c) acc[c] = __uint_as_float(vb[c]);
+    down_chunk<BN>(acc, c0 + 16, feat, row0, valid, wreg, Y, Ye, ldy, chunk0, row_scale);
+    if (!more_a) break;
+    tmem_ld_wait_regs(va);
+  }
+}
+
 template <int BN>
 __device__ __forceinline__ void epilogue_down(uint32_t taddr, int feat, int row0, int valid,
                                               const float (&wreg)[(BN + 31) / 32], __half* Y, int8_t* Ye, int ldy,
