@@ -44,7 +44,7 @@ struct PairCfg {
   static constexpr int TMEM_COLS = 512;
   static constexpr int NUM_BARS = 2 * STAGES + 2 * NACC + 1;
   static constexpr int XCHG_BYTES = GATEUP ? 2 * 2 * 64 * 8 * 4 : 0;
-  static constexpr int AUX_BYTES = NUM_BARS * 8 + 16 + 32 + (kMaxGroups + 1) * 4;
+  static constexpr int AUX_BYTES = NUM_BARS * 8 + 16 + 32 + 2 * (kMaxGroups + 1) * 4;  // + tile starts, offsets
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + XCHG_BYTES + AUX_BYTES;
   static_assert(SMEM_BYTES <= 232448, "exceeds shared memory per block");
   static constexpr uint32_t IDESC = idesc_bf16_f32(2 * kBlockM, kPairN);
@@ -96,6 +96,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* s_ok = reinterpret_cast<volatile int*>(tmem_holder + 4);
   int* tile_start = reinterpret_cast<int*>(tmem_holder + 12);
+  int* s_off = tile_start + kMaxGroups + 1;  // the dispatch offsets, copied here once
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs, 1: peer
@@ -123,7 +124,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tmem_relinquish_pair();
   }
   pdl_wait();  // offsets, rows and outputs belong to earlier work in the stream until here
-  if (warp == kEpilogueWarp0) build_tile_start(args.offsets, G, kPairN, tile_start, lane);
+  if (warp == kEpilogueWarp0) build_tile_start(args.offsets, G, kPairN, tile_start, lane, s_off);
   tc_fence_before();
   cluster_sync();  // barrier inits of both CTAs visible before any remote arrive
   tc_fence_after();
@@ -147,8 +148,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int wg = weight_group(args, it.g);
         row_w = GATEUP ? wg * args.rows_per_group + it.m * kBlockM + static_cast<int>(rank) * 64
                        : wg * args.rows_per_group + it.m * 2 * kBlockM + static_cast<int>(rank) * kBlockM;
-        const int g_row0 = __ldg(args.offsets + it.g);
-        const int n_mma = mma_width(__ldg(args.offsets + it.g + 1) - g_row0 - it.n * kPairN, kPairStep, kPairN);
+        const int g_row0 = s_off[it.g];
+        const int n_mma = mma_width(s_off[it.g + 1] - g_row0 - it.n * kPairN, kPairStep, kPairN);
         row_act = g_row0 + it.n * kPairN + static_cast<int>(rank) * (n_mma / 2);
       };
       uint32_t stage = 0, phase = 0;
@@ -203,8 +204,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // N of the pair MMAs: the tile's rows rounded up to kPairStep; the next
       // item's descriptor is worked out while this item's MMAs run
       uint32_t next_idesc =
-          item_idesc(pair, n_items, args.reverse, args.m_tiles, tile_start, G, args.offsets, 2 * kBlockM, kPairStep,
-                     kPairN);
+          item_idesc(pair, n_items, args.reverse, args.m_tiles, tile_start, G, s_off, 2 * kBlockM, kPairStep, kPairN);
       for (int item = pair; ok && item < n_items && !*abort_flag; item += n_pairs) {
         const uint32_t idesc = next_idesc;
         if (!wait_cluster(&acc_empty[acc], acc_phase ^ 1u, limit, abort_flag)) {
@@ -233,7 +233,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             phase ^= 1u;
           }
           if (kb == 0)
-            next_idesc = item_idesc(item + n_pairs, n_items, args.reverse, args.m_tiles, tile_start, G, args.offsets,
+            next_idesc = item_idesc(item + n_pairs, n_items, args.reverse, args.m_tiles, tile_start, G, s_off,
                                     2 * kBlockM, kPairStep, kPairN);
         }
         if (!ok) break;
@@ -255,8 +255,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t acc = 0, acc_phase = 0, it_par = 0, chunk_par = 0;
     auto tile_rows = [&](int item, Item& it, int& row0, int& valid) {
       it = decode_item(item, args.m_tiles, tile_start, G, n_items, args.reverse);
-      const int g_row0 = __ldg(args.offsets + it.g);
-      const int g_rows = __ldg(args.offsets + it.g + 1) - g_row0;
+      const int g_row0 = s_off[it.g];
+      const int g_rows = s_off[it.g + 1] - g_row0;
       row0 = g_row0 + it.n * kPairN;
       valid = min(kPairN, g_rows - it.n * kPairN);
     };
@@ -266,12 +266,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // between an accumulator becoming ready and its stores
     float wreg[kPairN / 32];
     int pe[kPairN / 32];
+    int cbase = 0, cbase_next = 0;  // the item's first exponent chunk of its group (K4)
     if (!GATEUP && pair < n_items) {
       Item it0;
       int r0, v0;
       tile_rows(pair, it0, r0, v0);
       gate_perm_entries<kPairN>(pe, r0, v0, lane, args.perm, args.Tk);
       gate_probs<kPairN>(wreg, pe, args.prob);
+      cbase_next = __ldg(args.chunk_base + it0.g);
     }
     for (int item = pair; item < n_items; item += n_pairs) {
       Item it;
@@ -295,15 +297,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         epilogue_gateup<kPairN>(taddr, row, it.m * kBlockM + static_cast<int>(rank) * 64, row0, valid,
                                 static_cast<bf16*>(args.out), args.out_ld, xchg, chunk_par);
       } else {
+        cbase = cbase_next;
         Item it_n;
         int row0_n = 0, valid_n = 0;
         if (has_next) {
           tile_rows(item + n_pairs, it_n, row0_n, valid_n);
           gate_perm_entries<kPairN>(pe, row0_n, valid_n, lane, args.perm, args.Tk);
+          cbase_next = __ldg(args.chunk_base + it_n.g);
         }
         epilogue_down_pipelined<kPairN>(taddr, it.m * 2 * kBlockM + static_cast<int>(rank) * kBlockM + row, row0,
                                         valid, wreg, static_cast<__half*>(args.out), args.out_exp, args.out_ld,
-                                        __ldg(args.chunk_base + it.g) + it.n * (kPairN / kYpRows));
+                                        cbase + it.n * (kPairN / kYpRows));
         if (has_next) gate_probs<kPairN>(wreg, pe, args.prob);
       }
       tc_fence_before();

@@ -48,7 +48,10 @@ __device__ __forceinline__ Item decode_item(int item, int m_tiles, const int* ti
 // groups 32c + l; the tile counts of eight such runs of 32 groups are loaded
 // together (coalesced, one load latency per eight runs), then each run is a
 // warp prefix sum on top of the running total.
-__device__ __forceinline__ void build_tile_start(const int* offsets, int G, int tile, int* tile_start, int lane) {
+// With s_off (or NULL) the offsets[0..G] are also copied to shared memory,
+// so that the roles of the kernel decode their items without a global load.
+__device__ __forceinline__ void build_tile_start(const int* offsets, int G, int tile, int* tile_start, int lane,
+                                                 int* s_off = nullptr) {
   constexpr int kRuns = 8;
   int carry = 0;
   for (int g0 = 0; g0 < G; g0 += 32 * kRuns) {
@@ -56,7 +59,13 @@ __device__ __forceinline__ void build_tile_start(const int* offsets, int G, int 
 #pragma unroll
     for (int j = 0; j < kRuns; ++j) {
       const int g = g0 + 32 * j + lane;
-      tiles[j] = g < G ? (__ldg(offsets + g + 1) - __ldg(offsets + g) + tile - 1) / tile : 0;
+      const int lo = g < G ? __ldg(offsets + g) : 0;
+      const int hi = g < G ? __ldg(offsets + g + 1) : 0;
+      tiles[j] = g < G ? (hi - lo + tile - 1) / tile : 0;
+      if (s_off != nullptr && g < G) {
+        s_off[g] = lo;
+        if (g == G - 1) s_off[G] = hi;
+      }
     }
 #pragma unroll
     for (int j = 0; j < kRuns; ++j) {
@@ -90,7 +99,7 @@ __device__ __forceinline__ uint32_t item_idesc(int item, int n_items, int revers
                                                int tile) {
   if (item >= n_items) return 0;
   const Item it = decode_item(item, m_tiles, tile_start, G, n_items, reverse);
-  const int rows = __ldg(offsets + it.g + 1) - __ldg(offsets + it.g) - it.n * tile;
+  const int rows = offsets[it.g + 1] - offsets[it.g] - it.n * tile;  // global or shared memory
   return idesc_bf16_f32(M, mma_width(rows, step, tile));
 }
 
