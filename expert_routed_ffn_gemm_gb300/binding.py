@@ -78,7 +78,9 @@ _lock = threading.Lock()
 
 
 def library_path() -> str:
-    return _build.LIB_PATH
+    """libmoe.so, or libmoe_debug.so (the build with the kernels' bounds
+    checks) when MOE_LIBRARY=debug is set in the environment."""
+    return _build.DEBUG_LIB_PATH if os.environ.get("MOE_LIBRARY") == "debug" else _build.LIB_PATH
 
 
 def load():

@@ -115,8 +115,10 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(const int* _
     if (jsel >= 0) {
       const int pos = base_e + running + r;
       const int a = t * k + jsel;
-      perm[pos] = a;
-      inv[a] = pos;
+      if (MOE_DBG_OK(pos >= 0 && pos < T * k)) {
+        perm[pos] = a;
+        inv[a] = pos;
+      }
     }
     running += chunk_total;
   }
@@ -225,6 +227,7 @@ __global__ void __launch_bounds__(kChunkTokens) chunk_place_kernel(const int* __
     int pos = base[e] + __popc(mask[w * E + e] & below);
     for (int q = 0; q < w; ++q) pos += __popc(mask[q * E + e]);
     const int a = t * k + j;
+    if (!MOE_DBG_OK(pos >= 0 && pos < T * k)) continue;
     perm[pos] = a;
     inv[a] = pos;
   }
@@ -268,6 +271,7 @@ __global__ void __launch_bounds__(256) scatter_rows_kernel(const bf16* __restric
   const int n_dst = k + (with_shared ? 1 : 0);
   for (int j = 0; j < n_dst; ++j) {
     const int row = (j < k) ? __ldg(inv + static_cast<size_t>(t) * k + j) : T * k + t;
+    if (!MOE_DBG_OK(row >= 0 && row < T * k + (with_shared ? T : 0))) continue;
     uint4* dst = static_cast<uint4*>(xp) + static_cast<size_t>(row) * n16;
 #pragma unroll
     for (int b = 0; b < kScatterVec; ++b)
@@ -313,6 +317,7 @@ __global__ void __launch_bounds__(128) scatter_rows_x2_kernel(const bf16* __rest
   const int n_dst = k + (with_shared ? 1 : 0);
   for (int j = threadIdx.x; j < n_dst; j += 128) {
     const int pos = (j < k) ? __ldg(inv + static_cast<size_t>(t) * k + j) : T * k + t;
+    if (!MOE_DBG_OK(pos >= 0 && pos < T * k + (with_shared ? T : 0))) continue;
     inv_s[pos] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
   }
   for (int c = threadIdx.x; c < n8; c += 128) {
@@ -337,6 +342,7 @@ __global__ void __launch_bounds__(128) scatter_rows_x2_kernel(const bf16* __rest
     }
     for (int j = 0; j < n_dst; ++j) {
       const int pos = (j < k) ? __ldg(inv + static_cast<size_t>(t) * k + j) : T * k + t;
+      if (!MOE_DBG_OK(pos >= 0 && pos < T * k + (with_shared ? T : 0))) continue;
       reinterpret_cast<uint2*>(xq + static_cast<size_t>(pos) * d)[c] = make_uint2(hi[0], hi[1]);
       reinterpret_cast<uint2*>(xq + static_cast<size_t>(lo_row0 + pos) * d)[c] = make_uint2(lo[0], lo[1]);
     }
@@ -437,10 +443,17 @@ __global__ void __launch_bounds__(1024, 1) combine_kernel(const __half* __restri
   __shared__ int chunk[kMaxTopK + 1];
   if (threadIdx.x <= k) {
     const int j = threadIdx.x;
-    const int g = (j < k) ? __ldg(idx + static_cast<size_t>(t) * k + j) : E;
-    const int p = (j < k) ? __ldg(inv + static_cast<size_t>(t) * k + j) : T * k + t;
+    int g = (j < k) ? __ldg(idx + static_cast<size_t>(t) * k + j) : E;
+    int p = (j < k) ? __ldg(inv + static_cast<size_t>(t) * k + j) : T * k + t;
+    if (!MOE_DBG_OK(g >= 0 && g <= E)) g = E;
+    int ch = __ldg(chunk_base + g) + (p - __ldg(offsets + g)) / kYpRows;
+    // the row inside its group's row block, the chunk inside its group's chunks
+    if (!MOE_DBG_OK(p >= __ldg(offsets + g) && p < __ldg(offsets + g + 1) && ch < __ldg(chunk_base + g + 1))) {
+      p = T * k + t;
+      ch = __ldg(chunk_base + E);
+    }
     pos[j] = p;
-    chunk[j] = __ldg(chunk_base + g) + (p - __ldg(offsets + g)) / kYpRows;
+    chunk[j] = ch;
   }
   __syncthreads();
   const int nterms = k + (has_shared ? 1 : 0);
@@ -535,9 +548,15 @@ __global__ void __launch_bounds__(512, 2) combine_nt_kernel(const __half* __rest
   if (threadIdx.x < NT) {
     const int j = threadIdx.x;
     const bool routed = j < k;
-    const int g = routed ? __ldg(idx + static_cast<size_t>(t) * k + j) : E;
-    const int p = routed ? __ldg(inv + static_cast<size_t>(t) * k + j) : T * k + t;
-    const int ch = __ldg(chunk_base + g) + (p - __ldg(offsets + g)) / kYpRows;
+    int g = routed ? __ldg(idx + static_cast<size_t>(t) * k + j) : E;
+    int p = routed ? __ldg(inv + static_cast<size_t>(t) * k + j) : T * k + t;
+    if (!MOE_DBG_OK(g >= 0 && g <= E)) g = E;
+    int ch = __ldg(chunk_base + g) + (p - __ldg(offsets + g)) / kYpRows;
+    // the row inside its group's row block, the chunk inside its group's chunks
+    if (!MOE_DBG_OK(p >= __ldg(offsets + g) && p < __ldg(offsets + g + 1) && ch < __ldg(chunk_base + g + 1))) {
+      p = T * k + t;
+      ch = __ldg(chunk_base + E);
+    }
     const __half* ybuf = (routed && yp_routed) ? yp_routed : yp;
     const int8_t* ebuf = (routed && yp_routed) ? yexp_routed : yexp;
     rows[j] = reinterpret_cast<const uint4*>(ybuf + static_cast<size_t>(p) * d);
@@ -586,6 +605,8 @@ __global__ void __launch_bounds__(512, 2) combine_nt_kernel(const __half* __rest
 }
 
 }  // namespace
+
+MOE_DBG_DEFINE_TAKE(dbg_take_dispatch)
 
 bool pdl_enabled() {
   static const bool on = [] {

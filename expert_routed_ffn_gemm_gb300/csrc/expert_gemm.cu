@@ -244,7 +244,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int g_row0 = __ldg(args.offsets + it.g);
       const int g_rows = __ldg(args.offsets + it.g + 1) - g_row0;
       const int row0 = g_row0 + it.n * BN;
-      const int valid = min(BN, g_rows - it.n * BN);
+      const int chunk0 = GATEUP ? -1 : __ldg(args.chunk_base + it.g) + it.n * (BN / kYpRows);
+      const int valid = checked_valid(args, min(BN, g_rows - it.n * BN), row0, chunk0);
       // K4: the gate weight of every column, loaded while the MMAs still run
       float wreg[(BN + 31) / 32];
       if (!GATEUP) load_gate_weights<BN>(wreg, row0, valid, lane, args.perm, args.prob, args.Tk);
@@ -273,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   args.out_ld, xchg, chunk_par, 1.0f, sum);
             else
               epilogue_down<BN>(0u, it.m * kBlockM + row, row0, valid, wreg, static_cast<__half*>(args.out),
-                                args.out_exp, args.out_ld, __ldg(args.chunk_base + it.g) + it.n * (BN / kYpRows),
+                                args.out_exp, args.out_ld, chunk0,
                                 1.0f, 0, sum);
             if (q == 0 && lane == 0) args.ksplit_cnt[base] = 0;  // ready for the next launch
           }
@@ -286,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             args.out_ld, xchg, chunk_par);
       } else {
         epilogue_down<BN>(taddr, it.m * kBlockM + row, row0, valid, wreg, static_cast<__half*>(args.out),
-                          args.out_exp, args.out_ld, __ldg(args.chunk_base + it.g) + it.n * (BN / kYpRows));
+                          args.out_exp, args.out_ld, chunk0);
       }
       tc_fence_before();
       __syncwarp();
@@ -358,6 +359,8 @@ __global__ void wait_selftest_kernel(uint32_t* err, unsigned long long limit_ns)
 }
 
 }  // namespace
+
+MOE_DBG_DEFINE_TAKE(dbg_take_expert_gemm)
 
 cudaError_t launch_expert_gemm(bool gateup, int tile_n, const CUtensorMap* map_w, const CUtensorMap* map_act,
                                const CUtensorMap* map_act2, const GemmArgs& a, int num_sms, cudaStream_t stream) {

@@ -300,7 +300,8 @@ __global__ void __launch_bounds__(kThreads8, 1)
       const int g_row0 = __ldg(args.offsets + it.g);
       const int g_rows = __ldg(args.offsets + it.g + 1) - g_row0;
       const int row0 = g_row0 + it.n * BN;
-      const int valid = min(BN, g_rows - it.n * BN);
+      const int chunk0 = GATEUP ? -1 : __ldg(args.chunk_base + it.g) + it.n * (BN / kYpRows);
+      const int valid = checked_valid(args, min(BN, g_rows - it.n * BN), row0, chunk0);
       float wreg[(BN + 31) / 32];
       if (!GATEUP) load_gate_weights<BN>(wreg, row0, valid, lane, args.perm, args.prob, args.Tk);
       // the scale of this thread's weight row
@@ -318,7 +319,7 @@ __global__ void __launch_bounds__(kThreads8, 1)
                             args.out_ld, xchg, chunk_par, scale);
       } else {
         epilogue_down<BN>(taddr, it.m * kBlockM + row, row0, valid, wreg, static_cast<__half*>(args.out),
-                          args.out_exp, args.out_ld, __ldg(args.chunk_base + it.g) + it.n * (BN / kYpRows), scale);
+                          args.out_exp, args.out_ld, chunk0, scale);
       }
       tc_fence_before();
       __syncwarp();
@@ -378,6 +379,8 @@ cudaError_t dispatch8_bn(int tile_n, const CUtensorMap* map_w, const CUtensorMap
 }
 
 }  // namespace
+
+MOE_DBG_DEFINE_TAKE(dbg_take_expert_gemm_fp8)
 
 cudaError_t launch_expert_gemm_fp8(bool gateup, int tile_n, const CUtensorMap* map_w, const CUtensorMap* map_act,
                                    const GemmArgs& a, int num_sms, cudaStream_t stream) {

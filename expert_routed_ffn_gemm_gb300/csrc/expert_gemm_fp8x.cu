@@ -249,7 +249,8 @@ __global__ void __launch_bounds__(kThreadsX, 1)
       const int g_row0 = __ldg(args.offsets + it.g);
       const int g_rows = __ldg(args.offsets + it.g + 1) - g_row0;
       const int row0 = g_row0 + it.n * BN;
-      const int valid = min(BN, g_rows - it.n * BN);
+      const int chunk0 = GATEUP ? -1 : __ldg(args.chunk_base + it.g) + it.n * (BN / kYpRows);
+      const int valid = checked_valid(args, min(BN, g_rows - it.n * BN), row0, chunk0);
       const size_t wrow0 = static_cast<size_t>(weight_group(args, it.g)) * args.rows_per_group;
       // K3 rows 0..63: gate of feature 64m + row; rows 64..127: up of feature 64m + row - 64
       const float scale = GATEUP ? __ldg(args.w_scale + wrow0 + (row < 64 ? 0 : args.F) + it.m * (kBlockM / 2) +
@@ -290,7 +291,7 @@ __global__ void __launch_bounds__(kThreadsX, 1)
                                      args.out_ld, xchg, chunk_par, scale, args.tok_scale, BN, sum);
             else
               epilogue_down<BN>(0u, it.m * kBlockM + row, row0, valid, wreg, static_cast<__half*>(args.out),
-                                args.out_exp, args.out_ld, __ldg(args.chunk_base + it.g) + it.n * (BN / kYpRows),
+                                args.out_exp, args.out_ld, chunk0,
                                 scale, 0, sum);
             if (q == 0 && lane == 0) args.ksplit_cnt[base] = 0;  // ready for the next launch
           }
@@ -302,7 +303,7 @@ __global__ void __launch_bounds__(kThreadsX, 1)
                                args.out_ld, xchg, chunk_par, scale, args.tok_scale, BN);
       else
         epilogue_down<BN>(taddr, it.m * kBlockM + row, row0, valid, wreg, static_cast<__half*>(args.out),
-                          args.out_exp, args.out_ld, __ldg(args.chunk_base + it.g) + it.n * (BN / kYpRows), scale, BN);
+                          args.out_exp, args.out_ld, chunk0, scale, BN);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
@@ -361,6 +362,8 @@ cudaError_t preparex_all() {
 }
 
 }  // namespace
+
+MOE_DBG_DEFINE_TAKE(dbg_take_expert_gemm_fp8x)
 
 cudaError_t launch_expert_gemm_fp8x(bool gateup, int tile_n, const CUtensorMap* map_w, const CUtensorMap* map_tok,
                                     const GemmArgs& a, int num_sms, cudaStream_t stream) {

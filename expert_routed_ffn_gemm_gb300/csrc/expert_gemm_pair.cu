@@ -279,6 +279,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       Item it;
       int row0, valid;
       tile_rows(item, it, row0, valid);
+      cbase = cbase_next;
+      valid = checked_valid(args, valid, row0, GATEUP ? -1 : cbase + it.n * (kPairN / kYpRows));
       const bool has_next = item + n_pairs < n_items;
       // one decision for all four epilogue warps (they meet at named barriers)
       const bool ok = __all_sync(0xffffffffu, wait_cluster(&acc_full[acc], acc_phase, limit, abort_flag));
@@ -297,7 +299,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         epilogue_gateup<kPairN>(taddr, row, it.m * kBlockM + static_cast<int>(rank) * 64, row0, valid,
                                 static_cast<bf16*>(args.out), args.out_ld, xchg, chunk_par);
       } else {
-        cbase = cbase_next;
         Item it_n;
         int row0_n = 0, valid_n = 0;
         if (has_next) {
@@ -342,6 +343,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }
 
 }  // namespace
+
+MOE_DBG_DEFINE_TAKE(dbg_take_expert_gemm_pair)
 
 cudaError_t expert_gemm_pair_prepare() {
   cudaError_t e = cudaFuncSetAttribute(expert_gemm_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,

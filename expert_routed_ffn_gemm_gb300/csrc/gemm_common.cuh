@@ -103,6 +103,20 @@ __device__ __forceinline__ uint32_t item_idesc(int item, int n_items, int revers
   return idesc_bf16_f32(M, mma_width(rows, step, tile));
 }
 
+// Debug builds: a tile's rows [row0, row0 + valid) inside the row buffers
+// (a.rows_cap rows) and, for the down projection (chunk0 >= 0), its exponent
+// chunks inside the exponent buffer (a.chunks_cap chunks); 0 valid rows
+// (nothing stored) if not.  Release builds return `valid`.
+__device__ __forceinline__ int checked_valid(const GemmArgs& a, int valid, int row0, int chunk0) {
+  (void)a;
+  (void)row0;
+  (void)chunk0;
+  return MOE_DBG_OK(valid > 0 && row0 >= 0 && row0 + valid <= a.rows_cap &&
+                    (chunk0 < 0 || chunk0 + (valid + kYpRows - 1) / kYpRows <= a.chunks_cap))
+             ? valid
+             : 0;
+}
+
 // Weight group of row group g (expert parallelism maps (source, expert) row
 // groups onto the local experts; otherwise the identity).
 __device__ __forceinline__ int weight_group(const GemmArgs& a, int g) {
@@ -286,7 +300,12 @@ __device__ __forceinline__ void load_gate_weights(float (&wreg)[(BN + 31) / 32],
   for (int i = 0; i < (BN + 31) / 32; ++i) {
     const int c = i * 32 + lane;
     const int pos = row0 + c;
-    wreg[i] = (c < valid) ? ((pos < Tk) ? __ldg(prob + __ldg(perm + pos)) : 1.0f) : 0.0f;
+    int a = -1;
+    if (c < valid && pos < Tk && MOE_DBG_OK(pos >= 0)) {
+      a = __ldg(perm + pos);
+      if (!MOE_DBG_OK(a >= 0 && a < Tk)) a = -2;  // an assignment id outside [0, T*k)
+    }
+    wreg[i] = (c < valid) ? ((pos < Tk) ? (a >= 0 ? __ldg(prob + a) : 0.0f) : 1.0f) : 0.0f;
   }
 }
 
@@ -301,7 +320,8 @@ __device__ __forceinline__ void gate_perm_entries(int (&pe)[(BN + 31) / 32], int
   for (int i = 0; i < (BN + 31) / 32; ++i) {
     const int c = i * 32 + lane;
     const int pos = row0 + c;
-    pe[i] = (c < valid) ? ((pos < Tk) ? __ldg(perm + pos) : -1) : -2;
+    pe[i] = (c < valid && MOE_DBG_OK(pos >= 0)) ? ((pos < Tk) ? __ldg(perm + pos) : -1) : -2;
+    if (pe[i] >= 0 && !MOE_DBG_OK(pe[i] < Tk)) pe[i] = -2;  // an assignment id outside [0, T*k)
   }
 }
 

@@ -42,6 +42,45 @@ cudaError_t launch_chain(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t
 
 using bf16 = __nv_bfloat16;
 
+// Debug builds (-DMOE_DEBUG, libmoe_debug.so): the kernels check every index
+// they take from the dispatch (dispatch positions, row blocks, exponent
+// chunks, permutation entries) against the bounds the dispatch guarantees.  A
+// failed check skips the access it guards and ORs 2 (the bounds bit) into a
+// debug word of its translation unit; moe_check collects and clears the
+// words (dbg_take_* below) and reports MOE_ERR_DEVICE.  Nothing traps.  In
+// release builds MOE_DBG_OK(cond) is the constant true and cond is not
+// evaluated.
+#ifdef MOE_DEBUG
+namespace {
+__device__ uint32_t g_dbg_word;  // one per translation unit
+__device__ __forceinline__ bool dbg_check(bool ok) {
+  if (!ok) atomicOr(&g_dbg_word, 2u);
+  return ok;
+}
+}  // namespace
+#define MOE_DBG_OK(cond) (::moe::dbg_check(cond))
+// Defines uint32_t name(): this translation unit's debug word, then clears it.
+#define MOE_DBG_DEFINE_TAKE(name)                                                \
+  uint32_t name() {                                                              \
+    uint32_t v = 0;                                                              \
+    if (cudaMemcpyFromSymbol(&v, g_dbg_word, sizeof v) != cudaSuccess) {         \
+      cudaGetLastError();                                                        \
+      return 0;                                                                  \
+    }                                                                            \
+    const uint32_t z = 0;                                                        \
+    if (v && cudaMemcpyToSymbol(g_dbg_word, &z, sizeof z) != cudaSuccess) cudaGetLastError(); \
+    return v;                                                                    \
+  }
+uint32_t dbg_take_dispatch();
+uint32_t dbg_take_expert_gemm();
+uint32_t dbg_take_expert_gemm_pair();
+uint32_t dbg_take_expert_gemm_fp8();
+uint32_t dbg_take_expert_gemm_fp8x();
+#else
+#define MOE_DBG_OK(cond) (true)
+#define MOE_DBG_DEFINE_TAKE(name)
+#endif
+
 constexpr int kBlockM = 128;  // weight rows per tensor-core tile (M of tcgen05.mma)
 constexpr int kBlockK = 64;   // K elements per pipeline stage (one 128-byte swizzle row)
 constexpr int kMaxExperts = 512;
@@ -143,6 +182,8 @@ struct GemmArgs {
   int lo_row0, lo_col0;    // ... and where the lo terms of dispatch row 0 sit in the token map
   int act2_from;       // bf16 kernels: token rows from this dispatch position on come through
                        // map_act2 at row (position - act2_from); -1: all through map_act
+  int rows_cap;        // rows of the dispatch-ordered buffers (token rows, H, Yp)
+  int chunks_cap;      // exponent chunks the Yp exponent buffer holds
 };
 
 // K3/K4: tcgen05 grouped GEMMs over the groups' row blocks.  `tile_n` must be

@@ -397,6 +397,10 @@ int enqueue_ffn(moe_handle* h, moe::GemmArgs a, double mean_rows, const CUtensor
   a.err = h->err;
   a.wait_limit_ns = h->wait_limit_ns;
   a.F = c.ffn_width;
+  // bounds of the debug build's checks: the rows of this call when known
+  // (every row block lies below them), else the row buffers' capacity
+  a.rows_cap = n_rows > 0 ? n_rows : h->rows_max;
+  a.chunks_cap = std::max(a.rows_cap, h->rows_max) / moe::kYpRows + c.n_experts + 2;
   a.ksplit_part = h->ksplit_part;
   a.ksplit_cnt = h->ksplit_cnt;
   a.ksplit_cap = h->ksplit_cap;
@@ -808,7 +812,7 @@ int moe_ep_experts(moe_handle* h, const void* recv_rows, const int* recv_counts,
   a.chunk_base = h->ep_chunk_base;
   a.w_group_mod = El;
   return enqueue_ffn(h, a, static_cast<double>(n_recv) / G, maps, out_rows, static_cast<int8_t*>(out_exp), nullptr,
-                     s);
+                     s, nullptr, 0, n_recv);
 }
 
 int moe_ep_combine(moe_handle* h, const void* ret_rows, const void* ret_exp, void* y, void* stream) {
@@ -946,6 +950,11 @@ int moe_check(moe_handle* h, void* stream) {
   MOE_CUDA(cudaMemcpyAsync(&e, h->err, sizeof e, cudaMemcpyDeviceToHost, s));
   MOE_CUDA(cudaMemsetAsync(h->err, 0, sizeof e, s));
   MOE_CUDA(cudaStreamSynchronize(s));
+#ifdef MOE_DEBUG
+  // the bounds checks' words of every kernel source (a debug build only)
+  e |= moe::dbg_take_dispatch() | moe::dbg_take_expert_gemm() | moe::dbg_take_expert_gemm_pair() |
+       moe::dbg_take_expert_gemm_fp8() | moe::dbg_take_expert_gemm_fp8x();
+#endif
   // a GEMM that gave up may have left K split part counts behind: the next
   // call on the handle starts from zero
   if (e) MOE_CUDA(cudaMemset(h->ksplit_cnt, 0, sizeof(int) * static_cast<size_t>(h->ksplit_cap)));

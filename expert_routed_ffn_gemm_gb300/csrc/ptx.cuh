@@ -10,6 +10,7 @@ namespace moe {
 // Device error word bits (OR-ed into Workspace::err by any kernel).
 enum : uint32_t {
   kErrWaitTimeout = 1u,  // an mbarrier wait exceeded the handle's limit
+  kErrBounds = 2u,       // debug builds: an index from the dispatch failed its bounds check
 };
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {

@@ -26,7 +26,20 @@ def test_decode_bytes_and_flops():
     assert bench.layer_flops(shape) == T * ((k + 1) * 6 * d * F + 2 * d * E)
 
 
-def test_traffic_comes_from_the_profiles():
+def _capture_file(tmp_path, monkeypatch, fresh: bool):
+    """The committed capture file with its source digests set as if the
+    kernels were (fresh) or were not (stale) the ones captured."""
+    import json
+    doc = json.load(open(bench.TRAFFIC_FILE))
+    for e in doc["entries"]:
+        e["sources_sha256_16"] = bench.sources_digest(e["sources"]) if fresh else "0" * 16
+    f = tmp_path / "traffic.json"
+    f.write_text(json.dumps(doc))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+
+
+def test_traffic_comes_from_the_profiles(tmp_path, monkeypatch):
+    _capture_file(tmp_path, monkeypatch, fresh=True)
     dec = synth.FLASH_DECODE
     alg = bench.gateup_bytes(dec, 281)
     t, src = bench.measured_traffic("decode", "bf16", dec, alg)
@@ -46,16 +59,16 @@ def test_traffic_comes_from_the_profiles():
 
 
 def test_stale_capture_gives_no_traffic(tmp_path, monkeypatch):
-    import json
-    doc = json.load(open(bench.TRAFFIC_FILE))
-    for e in doc["entries"]:
-        e["sources_sha256_16"] = "0" * 16  # as if the kernel had changed since
-    f = tmp_path / "traffic.json"
-    f.write_text(json.dumps(doc))
-    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
-    dec = synth.FLASH_DECODE
-    t, src = bench.measured_traffic("decode", "bf16", dec, 1.0)
+    _capture_file(tmp_path, monkeypatch, fresh=False)
+    t, src = bench.measured_traffic("decode", "bf16", synth.FLASH_DECODE, 1.0)
     assert t is None and src.startswith("stale")
+
+
+def test_committed_captures_name_existing_sources():
+    import json
+    for e in json.load(open(bench.TRAFFIC_FILE))["entries"]:
+        assert e["capture"].startswith("ncu ") and "--clock-control none" in e["capture"]
+        bench.sources_digest(e["sources"])  # every file exists
 
 
 def test_workloads_resolve():
