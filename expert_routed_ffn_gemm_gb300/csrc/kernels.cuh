@@ -122,6 +122,29 @@ cudaError_t launch_router_topk(const float* partial, int ksplit, int T, int E, i
 // Routing statistics from tokstats and counts (one block, fixed summation order).
 cudaError_t launch_route_stats(const float* tokstats, const int* counts, int T, int E, int k, int n_groups,
                                float* group_f, float* group_p, float* summary, cudaStream_t stream);
+// A few tokens: router (fp32 FMA dot products), softmax / top-k and the
+// dispatch in one launch (see router_gemm.cu).  logits [T][E] scratch; done
+// an unsigned int that is zero between launches.  Usable when
+// route_small_fits(T, d, E).
+// ex: two weight regions to prefetch into L2 while routing (pf*, NULL / 0
+// for none; 16-byte multiples), and xp (or NULL): the buffer [T*k][d] bf16
+// the routed rows are copied into in dispatch order.
+// (up to 4 tokens: measured at 1, 2 and 4 tokens on the flash shape 4-8 %
+// faster per call than the router GEMM + top-k + dispatch chain, at 8 tokens
+// the same)
+constexpr int kSmallRouteMaxTokens = 4;
+struct SmallRouteExtras {
+  const void* pf0;
+  long long pf0_bytes;
+  const void* pf1;
+  long long pf1_bytes;
+  void* xp;
+};
+bool route_small_fits(int T, int d, int E);
+cudaError_t launch_route_small(const bf16* x, const float* w_router, int T, int d, int E, int k, int renorm,
+                               int has_shared, float* logits, unsigned int* done, int* idx, float* prob, float* gap,
+                               int* counts, int* offsets, int* perm, int* inv, int* chunk_base,
+                               const SmallRouteExtras& ex, cudaStream_t stream);
 // W_r fp32 [E][d] -> bf16 slices [3][e_pad][d] with hi + mid + lo = W_r.
 cudaError_t launch_split_router(const float* w, int E, int d, int e_pad, bf16* w3, cudaStream_t stream);
 cudaError_t router_gemm_prepare();

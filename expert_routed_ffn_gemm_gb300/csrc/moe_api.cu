@@ -24,6 +24,7 @@ using moe::bf16;
 constexpr int kProfStages = 6;
 constexpr int kProfEvents = kProfStages + 1;
 constexpr int kProfMaxCalls = 4096;
+constexpr int kFusedGatherMaxTokens = 2;  // the few-token routing launch also copies the rows up to here
 
 struct moe_handle {
   uint32_t magic;
@@ -35,6 +36,7 @@ struct moe_handle {
   int tile_gateup;  // 0 = choose per call
   int tile_down;
   bool use_pairs;   // 256-row token tiles on CTA pairs (MOE_PAIR_TILES=0 turns it off)
+  bool small_route; // routing and dispatch in one launch for a few tokens (MOE_SMALL_ROUTE=0 turns it off)
   bool fp8_x2;      // FP8 weights: gate/up on E4M3 tensor cores with two-term token rows (MOE_FP8_X2=0: off)
   int gemm_ksplit;  // K split of the bf16 expert GEMMs: -1 = by work items, 1 = off, 2..4 = forced
   int ksplit_cap;   // work items (item, K part) the part buffer holds
@@ -78,6 +80,7 @@ struct moe_handle {
   bf16* x_stage;   // [Tmax][d] (host entry point)
   void* y_stage;   // [Tmax][d] bf16 or fp32 (host entry point)
   uint32_t* err;   // device error word
+  unsigned int* route_done;  // arrival count of the few-token routing kernel, zero between launches
   float* tokstats; // [Tmax][kMaxStatGroups + 1] per-token group masses and entropy
   CUtensorMap map_w3;                   // W_r slices as [3*e_pad][d], box 64 x 128
   CUtensorMap map_wgu;                  // W_gu as [G*2F][d], box 64 x 64
@@ -291,9 +294,20 @@ int enqueue_router(moe_handle* h, const void* x, int T, CallOpts o, int* idx, fl
 }
 
 // K1 + K2 into the given buffers.
+// A few tokens: K1 and K2 in one launch (the few-token routing kernel).
+bool small_route(const moe_handle* h, int T) {
+  return h->small_route && moe::route_small_fits(T, h->cfg.d_model, h->cfg.n_experts);
+}
+
 int enqueue_route(moe_handle* h, const void* x, int T, CallOpts o, int* idx, float* prob, int* perm, int* offsets,
                   float* gap, cudaStream_t s) {
   const moe_config& c = h->cfg;
+  if (small_route(h, T)) {
+    MOE_CUDA(moe::launch_route_small(static_cast<const bf16*>(x), h->w.w_router, T, c.d_model, c.n_experts, o.k,
+                                     o.renorm, c.has_shared, h->partial, h->route_done, idx, prob, gap, h->counts,
+                                     offsets, perm, h->inv, h->chunk_base, moe::SmallRouteExtras{}, s));
+    return MOE_OK;
+  }
   const int rc = enqueue_router(h, x, T, o, idx, prob, gap, nullptr, 0, s);
   if (rc != MOE_OK) return rc;
   MOE_CUDA(moe::launch_dispatch(idx, h->counts, T, c.n_experts, o.k, c.has_shared, offsets, perm, h->inv,
@@ -471,11 +485,32 @@ int enqueue_forward(moe_handle* h, const void* x, int T, CallOpts o, void* y, cu
   const moe_config& c = h->cfg;
   cudaEvent_t* ev = prof_slot(h);
   MOE_MARK(0);
-  const int rc = enqueue_router(h, x, T, o, h->idx, h->prob, nullptr, nullptr, 0, s);
-  if (rc != MOE_OK) return rc;
-  MOE_MARK(1);
-  MOE_CUDA(moe::launch_dispatch(h->idx, h->counts, T, c.n_experts, o.k, c.has_shared, h->offsets, h->perm, h->inv,
-                                h->chunk_base, h->chunk_hist, s));
+  const bool fused_route = small_route(h, T);
+  // with one or two tokens (bf16 weights) that launch also copies the routed
+  // rows into dispatch order (a handful of rows: one block is enough)
+  const bool fused_gather = fused_route && !h->fp8 && T <= kFusedGatherMaxTokens;
+  if (fused_route) {
+    moe::SmallRouteExtras ex{};
+    if (c.has_shared) {
+      // the shared expert's weights are read by every call: into L2 while routing
+      const size_t wb = h->fp8 ? 1 : 2, F = c.ffn_width, d = c.d_model, E = c.n_experts;
+      ex.pf0 = static_cast<const char*>(h->w.w_gate_up) + E * 2 * F * d * wb;
+      ex.pf0_bytes = static_cast<long long>(2 * F * d * wb);
+      ex.pf1 = static_cast<const char*>(h->w.w_down) + E * d * F * wb;
+      ex.pf1_bytes = static_cast<long long>(d * F * wb);
+    }
+    ex.xp = fused_gather ? h->yp : nullptr;
+    MOE_CUDA(moe::launch_route_small(static_cast<const bf16*>(x), h->w.w_router, T, c.d_model, c.n_experts, o.k,
+                                     o.renorm, c.has_shared, h->partial, h->route_done, h->idx, h->prob, nullptr,
+                                     h->counts, h->offsets, h->perm, h->inv, h->chunk_base, ex, s));
+    MOE_MARK(1);
+  } else {
+    const int rc = enqueue_router(h, x, T, o, h->idx, h->prob, nullptr, nullptr, 0, s);
+    if (rc != MOE_OK) return rc;
+    MOE_MARK(1);
+    MOE_CUDA(moe::launch_dispatch(h->idx, h->counts, T, c.n_experts, o.k, c.has_shared, h->offsets, h->perm, h->inv,
+                                  h->chunk_base, h->chunk_hist, s));
+  }
   MOE_MARK(2);
   // token rows in dispatch order (the yp buffer holds them until the down
   // GEMM).  bf16 weights: the routed rows only — the shared expert's rows are
@@ -485,7 +520,7 @@ int enqueue_forward(moe_handle* h, const void* x, int T, CallOpts o, void* y, cu
   if (h->fp8_x2)
     MOE_CUDA(moe::launch_scatter_x2(static_cast<const bf16*>(x), h->inv, T, o.k, c.d_model, c.has_shared,
                                     static_cast<uint8_t*>(h->yp), h->rows_max, h->tok_scale, s));
-  else
+  else if (!fused_gather)
     MOE_CUDA(moe::launch_gather(static_cast<const bf16*>(x), h->inv, T, o.k, c.d_model,
                                 shared_from_x ? 0 : c.has_shared, h->yp, h->fp8, s));
   MOE_MARK(3);
@@ -505,9 +540,10 @@ int enqueue_forward(moe_handle* h, const void* x, int T, CallOpts o, void* y, cu
                                s));
   MOE_MARK(6);
   // router GEMM, top-k, dispatch, gather, gate/up, down, combine; many
-  // tokens: two more for the chunk histograms and their scan; FP8 two-term
-  // rows: one more for the requantisation of H
-  h->last_kernels = (moe::chunked_dispatch(T) ? 9 : 7) + (h->fp8_x2 ? 1 : 0);
+  // tokens: two more for the chunk histograms and their scan; a few tokens:
+  // routing and dispatch in one (one or two tokens: and the gather); FP8
+  // two-term rows: one more for the requantisation of H
+  h->last_kernels = (fused_route ? (fused_gather ? 4 : 5) : moe::chunked_dispatch(T) ? 9 : 7) + (h->fp8_x2 ? 1 : 0);
   return MOE_OK;
 }
 
@@ -606,6 +642,8 @@ int init_any(const moe_config* cfg, const moe_weights* w, const float* s_gu, con
   {
     const char* v = std::getenv("MOE_PAIR_TILES");
     h->use_pairs = !(v && v[0] == '0');
+    const char* vs = std::getenv("MOE_SMALL_ROUTE");
+    h->small_route = !(vs && vs[0] == '0');
     const char* vx = std::getenv("MOE_FP8_X2");
     // the in-place requantisation of H holds a row in registers: F <= 8192
     h->fp8_x2 = fp8 && !(vx && vx[0] == '0') && c.ffn_width <= 8192;
@@ -660,6 +698,7 @@ int init_any(const moe_config* cfg, const moe_weights* w, const float* s_gu, con
   char* b = static_cast<char*>(h->ws);
   h->counts = reinterpret_cast<int*>(b + o_counts);
   h->err = reinterpret_cast<uint32_t*>(b + o_err);
+  h->route_done = reinterpret_cast<unsigned int*>(b + o_err + 4);  // zeroed below with the error word
   h->offsets = reinterpret_cast<int*>(b + o_offsets);
   h->partial = reinterpret_cast<float*>(b + o_partial);
   h->w3 = reinterpret_cast<bf16*>(b + o_w3);
@@ -751,13 +790,23 @@ int moe_ep_dispatch(moe_handle* h, const void* x, int T, void* send_rows, float*
   if (!aligned(send_counts, 4) || !is_device_ptr(send_counts)) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   h->ep_T = T;
-  rc = enqueue_router(h, x, T, CallOpts{k, 0}, h->idx, h->prob, nullptr, nullptr, 0, s);
-  if (rc != MOE_OK) return rc;
+  // the routing and dispatch of the whole-layer call on the same tokens (so
+  // that both give the same rows and weights)
+  const bool fused_route = small_route(h, T);
+  if (fused_route) {
+    MOE_CUDA(moe::launch_route_small(static_cast<const bf16*>(x), h->w.w_router, T, c.d_model, E, k, 0, c.has_shared,
+                                     h->partial, h->route_done, h->idx, h->prob, nullptr, h->counts, h->offsets,
+                                     h->perm, h->inv, h->chunk_base, moe::SmallRouteExtras{}, s));
+  } else {
+    rc = enqueue_router(h, x, T, CallOpts{k, 0}, h->idx, h->prob, nullptr, nullptr, 0, s);
+    if (rc != MOE_OK) return rc;
+  }
   MOE_CUDA(cudaMemcpyAsync(send_counts, h->counts, sizeof(int) * E, cudaMemcpyDeviceToDevice, s));
   for (int q = 0; q < h->ep_size; ++q) rows_per_rank[q] = 0;
   if (T == 0) return cudaStreamSynchronize(s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
-  MOE_CUDA(moe::launch_dispatch(h->idx, h->counts, T, E, k, c.has_shared, h->offsets, h->perm, h->inv,
-                                h->chunk_base, h->chunk_hist, s));
+  if (!fused_route)
+    MOE_CUDA(moe::launch_dispatch(h->idx, h->counts, T, E, k, c.has_shared, h->offsets, h->perm, h->inv,
+                                  h->chunk_base, h->chunk_hist, s));
   // every row in dispatch order (the shared expert's rows stay here for
   // moe_ep_combine); the routed rows, expert-major, go out rank by rank
   MOE_CUDA(moe::launch_gather(static_cast<const bf16*>(x), h->inv, T, k, c.d_model, c.has_shared, h->yp, false, s));

@@ -19,6 +19,7 @@
 #include "kernels.cuh"
 #include "ptx.cuh"
 
+#include <algorithm>
 #include <cfloat>
 
 namespace moe {
@@ -460,6 +461,178 @@ __global__ void __launch_bounds__(kTopkTokensPerBlock * 32) router_topk_warp_ker
   finish_token<NS>(p, t, lane, E, k, renorm, idx, prob, gap, counts, tokstats, n_groups);
 }
 
+// A few tokens (decode of one to kSmallRouteMaxTokens tokens): the router,
+// softmax / top-k and the dispatch in one launch.  The logit GEMM is T small
+// dot products per expert, bounded by reading W_r (fp32, 4.7 MB at the flash
+// shape) once: block e computes expert e for every token with fp32 FMAs,
+// warp w over the w-th quarter of the columns (lane l takes the float4
+// columns l, l + 32, ... of it in increasing order, their loads in flight
+// together), the lanes' sums meet in a fixed xor-butterfly and the four
+// warps' sums are added in warp order.  The block that finishes last (an
+// integer arrival count, reset for the next launch) ranks every token with
+// finish_token and lays the rows out: counts, offsets and chunk bases by a
+// block scan over the experts, and each assignment a = t*k + j at
+// offsets[e] + the number of earlier tokens that chose e (the stable expert,
+// token order of dispatch_kernel).  Every result is a function of x and W_r
+// alone (fixed summation orders): bit-identical run to run.
+constexpr int kSmallRouteWarps = 4;
+constexpr long long kPrefetchChunk = 64 * 1024;
+
+template <int NS>
+__global__ void __launch_bounds__(kSmallRouteWarps * 32) route_small_kernel(
+    const bf16* __restrict__ x, const float* __restrict__ w_router, int T, int d, int E, int k, int renorm,
+    int has_shared, float* __restrict__ logits, unsigned int* done, int* __restrict__ idx, float* __restrict__ prob,
+    float* __restrict__ gap, int* __restrict__ counts, int* __restrict__ offsets, int* __restrict__ perm,
+    int* __restrict__ inv, int* __restrict__ chunk_base, SmallRouteExtras ex) {
+  pdl_trigger();
+  // weights every call reads whatever the routing (the shared expert's),
+  // into L2 while the routing runs: chunks of kPrefetchChunk bytes, block b
+  // taking chunks b, b + gridDim.x, ...
+  if (threadIdx.x == 0) {
+    for (int r = 0; r < 2; ++r) {
+      const char* base = static_cast<const char*>(r == 0 ? ex.pf0 : ex.pf1);
+      const long long n = r == 0 ? ex.pf0_bytes : ex.pf1_bytes;
+      for (long long o = static_cast<long long>(blockIdx.x) * kPrefetchChunk; o < n;
+           o += static_cast<long long>(gridDim.x) * kPrefetchChunk)
+        l2_prefetch_bulk(base + o, static_cast<uint32_t>(n - o < kPrefetchChunk ? n - o : kPrefetchChunk));
+    }
+  }
+  __shared__ int s_last;
+  __shared__ int s_scan[kSmallRouteWarps];
+  __shared__ float s_part[kSmallRouteWarps][kSmallRouteMaxTokens];
+  __shared__ int s_cnt[kMaxExperts], s_off[kMaxExperts];
+  __shared__ int s_idx[kSmallRouteMaxTokens * kMaxTopK];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  pdl_wait();  // x, and the routing buffers read by earlier work in the stream
+  const int e = blockIdx.x;
+  {
+    float acc[kSmallRouteMaxTokens];
+#pragma unroll
+    for (int t = 0; t < kSmallRouteMaxTokens; ++t) acc[t] = 0.f;
+    const int q4 = d / 16;  // float4 columns of a quarter
+    const float4* wr = reinterpret_cast<const float4*>(w_router + static_cast<size_t>(e) * d) + warp * q4;
+#pragma unroll 8
+    for (int c = lane; c < q4; c += 32) {
+      const float4 w = __ldg(wr + c);
+#pragma unroll
+      for (int t = 0; t < kSmallRouteMaxTokens; ++t) {
+        if (t < T) {
+          const uint2 xv = __ldg(reinterpret_cast<const uint2*>(x + static_cast<size_t>(t) * d) + warp * q4 + c);
+          acc[t] = fmaf(__uint_as_float(xv.x << 16), w.x, acc[t]);
+          acc[t] = fmaf(__uint_as_float(xv.x & 0xffff0000u), w.y, acc[t]);
+          acc[t] = fmaf(__uint_as_float(xv.y << 16), w.z, acc[t]);
+          acc[t] = fmaf(__uint_as_float(xv.y & 0xffff0000u), w.w, acc[t]);
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < kSmallRouteMaxTokens; ++t) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], off);
+      if (lane == 0) s_part[warp][t] = acc[t];
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < T)
+    logits[static_cast<size_t>(threadIdx.x) * E + e] =
+        ((s_part[0][threadIdx.x] + s_part[1][threadIdx.x]) + s_part[2][threadIdx.x]) + s_part[3][threadIdx.x];
+  // the block that finishes last sees every logit
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(done, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int t = warp; t < T; t += kSmallRouteWarps) {
+    float q[NS];
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+      const int ee = lane + 32 * i;
+      q[i] = ee < E ? __ldcg(logits + static_cast<size_t>(t) * E + ee) : 0.f;
+    }
+    finish_token<NS>(q, t, lane, E, k, renorm, idx, prob, gap, nullptr, nullptr, 0);
+  }
+  __syncthreads();  // every token's idx written (and visible to the block)
+  for (int a = threadIdx.x; a < T * k; a += blockDim.x) s_idx[a] = __ldcg(idx + a);
+  for (int i = threadIdx.x; i < E; i += blockDim.x) s_cnt[i] = 0;
+  __syncthreads();
+  // counts per expert (shared-memory integer atomics: order-independent)
+  for (int a = threadIdx.x; a < T * k; a += blockDim.x) atomicAdd(&s_cnt[s_idx[a]], 1);
+  __syncthreads();
+  // offsets and chunk bases: each thread scans a contiguous run of experts
+  const int per = (E + blockDim.x - 1) / blockDim.x;
+  const int b0 = threadIdx.x * per, b1 = min(E, b0 + per);
+  for (int pass = 0; pass < 2; ++pass) {
+    int local = 0;
+    for (int i = b0; i < b1; ++i) local += pass == 0 ? s_cnt[i] : (s_cnt[i] + kYpRows - 1) / kYpRows;
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    if (lane == 31) s_scan[warp] = incl;
+    __syncthreads();
+    int run = incl - local, total = 0;
+    for (int w = 0; w < kSmallRouteWarps; ++w) {
+      run += w < warp ? s_scan[w] : 0;
+      total += s_scan[w];
+    }
+    for (int i = b0; i < b1; ++i) {
+      if (pass == 0) {
+        offsets[i] = run;
+        s_off[i] = run;
+        counts[i] = s_cnt[i];
+        run += s_cnt[i];
+      } else {
+        chunk_base[i] = run;
+        run += (s_cnt[i] + kYpRows - 1) / kYpRows;
+      }
+    }
+    if (threadIdx.x == 0) {
+      if (pass == 0) {
+        offsets[E] = total;
+        offsets[E + 1] = total + (has_shared ? T : 0);
+      } else {
+        chunk_base[E] = total;
+        chunk_base[E + 1] = total + (has_shared ? (T + kYpRows - 1) / kYpRows : 0);
+      }
+    }
+    __syncthreads();
+  }
+  // assignment a = t*k + j of expert e2: after the rows of the earlier tokens
+  // that chose e2 (a token chooses an expert at most once)
+  for (int a = threadIdx.x; a < T * k; a += blockDim.x) {
+    const int t = a / k, e2 = s_idx[a];
+    int rank = 0;
+    for (int a2 = 0; a2 < t * k; ++a2) rank += s_idx[a2] == e2;
+    const int pos = s_off[e2] + rank;
+    perm[pos] = a;
+    inv[a] = pos;
+    s_cnt[a] = pos;  // the counts are written: the positions of the row copy below
+  }
+  if (threadIdx.x == 0) *done = 0u;  // ready for the next launch
+  if (ex.xp == nullptr) return;
+  // the routed rows in dispatch order, xp[pos(a)] = x[a / k], by this block
+  // (T * k rows of d bf16: 16-byte vectors, a warp per row)
+  __syncthreads();
+  const int n16 = d / 8;
+  for (int a = warp; a < T * k; a += kSmallRouteWarps) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(a / k) * d);
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<bf16*>(ex.xp) + static_cast<size_t>(s_cnt[a]) * d);
+    for (int c = lane; c < n16; c += 32) dst[c] = __ldg(src + c);
+  }
+}
+
+template <int NS>
+cudaError_t launch_route_small_ns(const bf16* x, const float* w_router, int T, int d, int E, int k, int renorm,
+                                  int has_shared, float* logits, unsigned int* done, int* idx, float* prob,
+                                  float* gap, int* counts, int* offsets, int* perm, int* inv, int* chunk_base,
+                                  const SmallRouteExtras& ex, cudaStream_t stream) {
+  return launch_chain(route_small_kernel<NS>, dim3(E), dim3(kSmallRouteWarps * 32), 0, stream, x, w_router, T, d, E,
+                      k, renorm, has_shared, logits, done, idx, prob, gap, counts, offsets, perm, inv, chunk_base, ex);
+}
+
 template <int NS>
 cudaError_t launch_topk_ns(const float* partial, int ksplit, int T, int E, int k, int renorm, int* idx, float* prob,
                            float* gap, int* counts, float* tokstats, int n_groups, cudaStream_t stream) {
@@ -597,6 +770,26 @@ cudaError_t launch_router_topk(const float* partial, int ksplit, int T, int E, i
     return launch_topk_ns<kMaxExperts / 32>(partial, ksplit, T, E, k, renorm, idx, prob, gap, counts, tokstats,
                                             n_groups, stream);
   return cudaErrorInvalidValue;
+}
+
+bool route_small_fits(int T, int d, int E) {
+  return T >= 1 && T <= kSmallRouteMaxTokens && d % 16 == 0 && E <= kMaxExperts;
+}
+
+cudaError_t launch_route_small(const bf16* x, const float* w_router, int T, int d, int E, int k, int renorm,
+                               int has_shared, float* logits, unsigned int* done, int* idx, float* prob, float* gap,
+                               int* counts, int* offsets, int* perm, int* inv, int* chunk_base,
+                               const SmallRouteExtras& ex, cudaStream_t stream) {
+  if (!route_small_fits(T, d, E)) return cudaErrorInvalidValue;
+#define MOE_ROUTE_SMALL(NS_)                                                                                  \
+  return launch_route_small_ns<NS_>(x, w_router, T, d, E, k, renorm, has_shared, logits, done, idx, prob, gap, \
+                                    counts, offsets, perm, inv, chunk_base, ex, stream)
+  if (E <= 64) MOE_ROUTE_SMALL(2);
+  if (E <= 128) MOE_ROUTE_SMALL(4);
+  if (E <= 256) MOE_ROUTE_SMALL(8);
+  if (E <= 288) MOE_ROUTE_SMALL(9);
+  MOE_ROUTE_SMALL(kMaxExperts / 32);
+#undef MOE_ROUTE_SMALL
 }
 
 cudaError_t launch_route_stats(const float* tokstats, const int* counts, int T, int E, int k, int n_groups,

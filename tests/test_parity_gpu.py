@@ -377,3 +377,25 @@ def test_forward_from_a_new_thread():
     assert not errs, errs
     assert torch.equal(out["y"], y_main)
     layer.close()
+
+
+@pytest.mark.parametrize("fused", ["1", "0"])
+@pytest.mark.parametrize("T,d,E,k", [(1, 256, 16, 2), (3, 512, 64, 4), (4, 256, 300, 8), (4, 1024, 24, 8)])
+def test_few_token_routing_both_paths(fused, T, d, E, k):
+    # From 1 to 4 tokens routing and dispatch run as one launch (fp32 FMA dot
+    # products, MOE_SMALL_ROUTE=0 turns it off for the tensor-core router):
+    # both paths against the oracle.
+    shape = synth.LayerShape(T=T, d=d, E=E, k=k, F=128)
+    inp = synth.make_inputs(shape, seed=400 + T + E)
+    layer, x = make_layer(inp, env={"MOE_SMALL_ROUTE": fused})
+    idx, prob, perm, offsets, gap = layer.route(x)
+    y = layer.forward(x)
+    assert layer.check() == binding.MOE_OK
+    # fused: one launch for routing and dispatch, with one or two tokens also the row copy
+    assert layer.last_kernel_count() == ((4 if T <= 2 else 5) if fused == "1" else 7)
+    xb, wr, wgu, wd = host_bits(inp)
+    check_routing(xb, wr, k, cpu(idx), cpu(prob), cpu(gap), cpu(perm), cpu(offsets))
+    check_output(xb, wr, wgu, wd, k, cpu(y.float()), cpu(idx), storage_slack=False)
+    y2 = layer.forward(x)
+    assert torch.equal(y, y2)
+    layer.close()
