@@ -111,6 +111,10 @@ struct RouterGemmArgs {
   int e_pad;    // rows per slice of the split router weights (multiple of 128)
   int m_tiles;  // e_pad / 128
   int ksplit;   // K splits (1..kMaxKSplit)
+  // weights to prefetch into L2 while the router runs (NULL / 0: none;
+  // 16-byte multiples): the shared expert's, which every layer call reads
+  const void* pf[2];
+  long long pf_bytes[2];
 };
 cudaError_t launch_router_gemm(int tile_n, const CUtensorMap* map_w3, const CUtensorMap* map_x,
                                const RouterGemmArgs& a, int num_sms, cudaStream_t stream);

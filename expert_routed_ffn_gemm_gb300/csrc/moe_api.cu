@@ -238,11 +238,26 @@ struct CallOpts {
   int renorm;
 };
 
+// The shared expert's gate/up and down weights (pointers and bytes), or
+// nothing without a shared expert: a layer call reads them whatever the
+// routing, so the routing kernels prefetch them into L2.
+void shared_weights(const moe_handle* h, const void* (&p)[2], long long (&n)[2]) {
+  const moe_config& c = h->cfg;
+  p[0] = p[1] = nullptr;
+  n[0] = n[1] = 0;
+  if (!c.has_shared) return;
+  const size_t wb = h->fp8 ? 1 : 2, F = c.ffn_width, d = c.d_model, E = c.n_experts;
+  p[0] = static_cast<const char*>(h->w.w_gate_up) + E * 2 * F * d * wb;
+  n[0] = static_cast<long long>(2 * F * d * wb);
+  p[1] = static_cast<const char*>(h->w.w_down) + E * d * F * wb;
+  n[1] = static_cast<long long>(d * F * wb);
+}
+
 // K1: router GEMM (K split across CTAs when there are few token tiles) and
 // softmax/top-k into idx/prob/gap, counts per expert; with tokstats, the
 // per-token group masses and entropy for the routing statistics.
 int enqueue_router(moe_handle* h, const void* x, int T, CallOpts o, int* idx, float* prob, float* gap,
-                   float* tokstats, int n_groups, cudaStream_t s) {
+                   float* tokstats, int n_groups, cudaStream_t s, bool prefetch_shared = false) {
   const moe_config& c = h->cfg;
   // many tokens: the counts come from per-chunk histograms after the top-k
   // kernel (no atomics); otherwise the top-k kernel counts into zeroed counts
@@ -286,6 +301,7 @@ int enqueue_router(moe_handle* h, const void* x, int T, CallOpts o, int* idx, fl
   ra.e_pad = h->router_m_tiles * moe::kBlockM;
   ra.m_tiles = h->router_m_tiles;
   ra.ksplit = ks;
+  if (prefetch_shared) shared_weights(h, ra.pf, ra.pf_bytes);
   MOE_CUDA(moe::launch_router_gemm(bn, &h->map_w3, &map_x, ra, h->num_sms, s));
   MOE_CUDA(moe::launch_router_topk(h->partial, ks, T, c.n_experts, o.k, o.renorm, idx, prob, gap,
                                    chunked ? nullptr : h->counts, tokstats, n_groups, s));
@@ -491,21 +507,20 @@ int enqueue_forward(moe_handle* h, const void* x, int T, CallOpts o, void* y, cu
   const bool fused_gather = fused_route && !h->fp8 && T <= kFusedGatherMaxTokens;
   if (fused_route) {
     moe::SmallRouteExtras ex{};
-    if (c.has_shared) {
-      // the shared expert's weights are read by every call: into L2 while routing
-      const size_t wb = h->fp8 ? 1 : 2, F = c.ffn_width, d = c.d_model, E = c.n_experts;
-      ex.pf0 = static_cast<const char*>(h->w.w_gate_up) + E * 2 * F * d * wb;
-      ex.pf0_bytes = static_cast<long long>(2 * F * d * wb);
-      ex.pf1 = static_cast<const char*>(h->w.w_down) + E * d * F * wb;
-      ex.pf1_bytes = static_cast<long long>(d * F * wb);
-    }
+    const void* pf[2];
+    long long pfn[2];
+    shared_weights(h, pf, pfn);  // read by every call: into L2 while routing
+    ex.pf0 = pf[0];
+    ex.pf0_bytes = pfn[0];
+    ex.pf1 = pf[1];
+    ex.pf1_bytes = pfn[1];
     ex.xp = fused_gather ? h->yp : nullptr;
     MOE_CUDA(moe::launch_route_small(static_cast<const bf16*>(x), h->w.w_router, T, c.d_model, c.n_experts, o.k,
                                      o.renorm, c.has_shared, h->partial, h->route_done, h->idx, h->prob, nullptr,
                                      h->counts, h->offsets, h->perm, h->inv, h->chunk_base, ex, s));
     MOE_MARK(1);
   } else {
-    const int rc = enqueue_router(h, x, T, o, h->idx, h->prob, nullptr, nullptr, 0, s);
+    const int rc = enqueue_router(h, x, T, o, h->idx, h->prob, nullptr, nullptr, 0, s, true);
     if (rc != MOE_OK) return rc;
     MOE_MARK(1);
     MOE_CUDA(moe::launch_dispatch(h->idx, h->counts, T, c.n_experts, o.k, c.has_shared, h->offsets, h->perm, h->inv,

@@ -27,6 +27,7 @@ namespace {
 
 constexpr int kThreads = 192;
 constexpr uint64_t kDrainLimitNs = 2000000000ull;
+constexpr long long kPrefetchChunk = 64 * 1024;  // bytes per L2 prefetch instruction
 
 template <int BN>
 struct RCfg {
@@ -113,6 +114,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tmem_alloc(tmem_holder, C::TMEM_COLS);
     tmem_relinquish();
+  }
+  if (warp == 2 && lane == 0) {
+    // the shared expert's weights into L2 (chunks of kPrefetchChunk bytes,
+    // CTA b taking chunks b, b + gridDim.x, ...); constant inputs, so no
+    // wait on earlier work
+    for (int r = 0; r < 2; ++r) {
+      const char* base = static_cast<const char*>(args.pf[r]);
+      const long long n = args.pf_bytes[r];
+      for (long long o = static_cast<long long>(blockIdx.x) * kPrefetchChunk; o < n;
+           o += static_cast<long long>(gridDim.x) * kPrefetchChunk)
+        l2_prefetch_bulk(base + o, static_cast<uint32_t>(n - o < kPrefetchChunk ? n - o : kPrefetchChunk));
+    }
   }
   pdl_wait();  // x and the partial-logit buffer belong to earlier work in the stream until here
   tc_fence_before();
@@ -476,7 +489,6 @@ __global__ void __launch_bounds__(kTopkTokensPerBlock * 32) router_topk_warp_ker
 // token order of dispatch_kernel).  Every result is a function of x and W_r
 // alone (fixed summation orders): bit-identical run to run.
 constexpr int kSmallRouteWarps = 4;
-constexpr long long kPrefetchChunk = 64 * 1024;
 
 template <int NS>
 __global__ void __launch_bounds__(kSmallRouteWarps * 32) route_small_kernel(
