@@ -29,20 +29,26 @@ constexpr int kThreads = 192;
 constexpr uint64_t kDrainLimitNs = 2000000000ull;
 constexpr long long kPrefetchChunk = 64 * 1024;  // bytes per L2 prefetch instruction
 
+// Two rings: token tiles (x, BN rows x 64 columns) and weight tiles (one
+// 128-row slice tile each).  Every K step loads one x tile and the three
+// slices' tiles of the same columns, and the three MMAs of the step read the
+// one x tile: x crosses from L2 into shared memory once per K step instead of
+// once per slice.
 template <int BN>
 struct RCfg {
-  static constexpr int A_BYTES = kBlockM * kBlockK * 2;
-  static constexpr int B_BYTES = BN * kBlockK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES_RAW = (192 * 1024) / STAGE_BYTES;
-  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+  static constexpr int W_BYTES = kBlockM * kBlockK * 2;  // one slice tile
+  static constexpr int X_BYTES = BN * kBlockK * 2;       // one token tile
+  static constexpr int WS = 6;                           // two K steps of three slices
+  static constexpr int XS_RAW = (200 * 1024 - WS * W_BYTES) / X_BYTES;
+  static constexpr int XS = XS_RAW > 8 ? 8 : XS_RAW;
   static constexpr int NACC = (2 * BN <= 512) ? 2 : 1;
   static constexpr int TMEM_RAW = NACC * BN;
   static constexpr int TMEM_COLS = TMEM_RAW <= 32 ? 32 : TMEM_RAW <= 64 ? 64 : TMEM_RAW <= 128 ? 128
                                                                        : TMEM_RAW <= 256 ? 256 : 512;
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * NACC + 1;
-  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARS * 8 + 16;
-  static_assert(STAGES >= 2, "ring too shallow");
+  static constexpr int NUM_BARS = 2 * WS + 2 * XS + 2 * NACC + 1;
+  static constexpr int SMEM_BYTES = 1024 + WS * W_BYTES + XS * X_BYTES + NUM_BARS * 8 + 16;
+  static_assert(XS >= 2, "token ring too shallow");
+  static_assert(SMEM_BYTES <= 232448, "exceeds shared memory per block");
   static constexpr uint32_t IDESC = idesc_bf16_f32(kBlockM, BN);
 };
 
@@ -79,11 +85,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = RCfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* ring = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + C::STAGES;
-  uint64_t* acc_full = bars + 2 * C::STAGES;
+  uint8_t* wring = smem;
+  uint8_t* xring = smem + C::WS * C::W_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(xring + C::XS * C::X_BYTES);
+  uint64_t* w_full = bars;
+  uint64_t* w_empty = bars + C::WS;
+  uint64_t* x_full = bars + 2 * C::WS;
+  uint64_t* x_empty = x_full + C::XS;
+  uint64_t* acc_full = x_empty + C::XS;
   uint64_t* acc_empty = acc_full + C::NACC;
   uint64_t* drain = acc_empty + C::NACC;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
@@ -92,14 +101,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tt = (args.T + BN - 1) / BN;
   const int n_items = n_tt * args.m_tiles * args.ksplit;
-  const int k_total = 3 * (args.d / kBlockK);                     // hi, mid, lo slices
-  const int k_per = (k_total + args.ksplit - 1) / args.ksplit;    // K steps per split
-  const int kd = args.d / kBlockK;
+  const int kd = args.d / kBlockK;                       // K steps (each with the three slices)
+  const int k_per = (kd + args.ksplit - 1) / args.ksplit;  // K steps per split
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < C::WS; ++s) {
+      mbar_init(&w_full[s], 1);
+      mbar_init(&w_empty[s], 1);
+    }
+    for (int s = 0; s < C::XS; ++s) {
+      mbar_init(&x_full[s], 1);
+      mbar_init(&x_empty[s], 1);
     }
     for (int a = 0; a < C::NACC; ++a) {
       mbar_init(&acc_full[a], 1);
@@ -137,44 +149,63 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       const uint64_t pol = policy_evict_last();  // W slices and x are re-read by other CTAs
-      uint32_t stage = 0, phase = 0;
-      long issued = 0;
+      uint32_t ws = 0, wph = 0, xs = 0, xph = 0;
+      long w_issued = 0, x_issued = 0;
       bool ok = true;
       for (int item = blockIdx.x; ok && item < n_items && !*abort_flag; item += gridDim.x) {
         const RItem it = decode_ritem(item, args.m_tiles, args.ksplit);
-        const int kb0 = it.ks * k_per, kb1 = min(k_total, kb0 + k_per);
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!rwait(&empty[stage], phase ^ 1u, limit, abort_flag)) {
-            *abort_flag = 1;
-            atomicOr(args.err, kErrWaitTimeout);
+        const int kb0 = it.ks * k_per, kb1 = min(kd, kb0 + k_per);
+        for (int kb = kb0; ok && kb < kb1; ++kb) {
+          const int kc = kb * kBlockK;
+          if (!rwait(&x_empty[xs], xph ^ 1u, limit, abort_flag)) {
             ok = false;
             break;
           }
-          const int slice = kb / kd, kc = (kb - slice * kd) * kBlockK;
-          uint8_t* st = ring + stage * C::STAGE_BYTES;
-          mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-          tma_load_2d(st, &map_w3, &full[stage], kc, slice * args.e_pad + it.m * kBlockM, pol);
-          tma_load_2d(st + C::A_BYTES, &map_x, &full[stage], kc, it.tt * BN, pol);
-          ++issued;
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1u;
+          mbar_arrive_expect_tx(&x_full[xs], C::X_BYTES);
+          tma_load_2d(xring + xs * C::X_BYTES, &map_x, &x_full[xs], kc, it.tt * BN, pol);
+          ++x_issued;
+          if (++xs == C::XS) {
+            xs = 0;
+            xph ^= 1u;
+          }
+          for (int slice = 0; slice < 3; ++slice) {
+            if (!rwait(&w_empty[ws], wph ^ 1u, limit, abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&w_full[ws], C::W_BYTES);
+            tma_load_2d(wring + ws * C::W_BYTES, &map_w3, &w_full[ws], kc, slice * args.e_pad + it.m * kBlockM, pol);
+            ++w_issued;
+            if (++ws == C::WS) {
+              ws = 0;
+              wph ^= 1u;
+            }
           }
         }
       }
-      for (int s = 0; s < C::STAGES; ++s) {
-        if (issued <= s) break;
-        const long last = s + ((issued - 1 - s) / C::STAGES) * C::STAGES;
-        mbar_wait(&full[s], static_cast<uint32_t>((last / C::STAGES) & 1), kDrainLimitNs);
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(args.err, kErrWaitTimeout);
+      }
+      // every load issued must have landed before the CTA may exit
+      for (int s = 0; s < C::WS; ++s) {
+        if (w_issued <= s) break;
+        const long last = s + ((w_issued - 1 - s) / C::WS) * C::WS;
+        mbar_wait(&w_full[s], static_cast<uint32_t>((last / C::WS) & 1), kDrainLimitNs);
+      }
+      for (int s = 0; s < C::XS; ++s) {
+        if (x_issued <= s) break;
+        const long last = s + ((x_issued - 1 - s) / C::XS) * C::XS;
+        mbar_wait(&x_full[s], static_cast<uint32_t>((last / C::XS) & 1), kDrainLimitNs);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      uint32_t ws = 0, wph = 0, xs = 0, xph = 0, acc = 0, acc_phase = 0;
       bool issued_any = false, ok = true;
       for (int item = blockIdx.x; ok && item < n_items && !*abort_flag; item += gridDim.x) {
         const RItem it = decode_ritem(item, args.m_tiles, args.ksplit);
-        const int kb0 = it.ks * k_per, kb1 = min(k_total, kb0 + k_per);
+        const int kb0 = it.ks * k_per, kb1 = min(kd, kb0 + k_per);
         if (!rwait(&acc_empty[acc], acc_phase ^ 1u, limit, abort_flag)) {
           *abort_flag = 1;
           atomicOr(args.err, kErrWaitTimeout);
@@ -182,28 +213,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!rwait(&full[stage], phase, limit, abort_flag)) {
-            *abort_flag = 1;
-            atomicOr(args.err, kErrWaitTimeout);
+        for (int kb = kb0; ok && kb < kb1; ++kb) {
+          if (!rwait(&x_full[xs], xph, limit, abort_flag)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          const uint32_t st = smem_u32(ring + stage * C::STAGE_BYTES);
-          const uint64_t a = smem_desc_sw128(st);
-          const uint64_t b = smem_desc_sw128(st + C::A_BYTES);
+          const uint64_t b = smem_desc_sw128(smem_u32(xring + xs * C::X_BYTES));
+          for (int slice = 0; slice < 3; ++slice) {
+            if (!rwait(&w_full[ws], wph, limit, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t a = smem_desc_sw128(smem_u32(wring + ws * C::W_BYTES));
 #pragma unroll
-          for (int kk = 0; kk < kBlockK / 16; ++kk)
-            tc_mma_bf16(d_tmem, a + 2 * kk, b + 2 * kk, C::IDESC, (kb > kb0 || kk > 0) ? 1u : 0u);
-          issued_any = true;
-          tc_commit(&empty[stage]);
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1u;
+            for (int kk = 0; kk < kBlockK / 16; ++kk)
+              tc_mma_bf16(d_tmem, a + 2 * kk, b + 2 * kk, C::IDESC, (kb > kb0 || slice > 0 || kk > 0) ? 1u : 0u);
+            issued_any = true;
+            tc_commit(&w_empty[ws]);
+            if (++ws == C::WS) {
+              ws = 0;
+              wph ^= 1u;
+            }
+          }
+          if (!ok) break;
+          tc_commit(&x_empty[xs]);  // after the three slices' MMAs that read it
+          if (++xs == C::XS) {
+            xs = 0;
+            xph ^= 1u;
           }
         }
-        if (!ok) break;
+        if (!ok) {
+          *abort_flag = 1;
+          atomicOr(args.err, kErrWaitTimeout);
+          break;
+        }
         tc_commit(&acc_full[acc]);
         if (++acc == C::NACC) {
           acc = 0;
