@@ -250,10 +250,11 @@ def sources_digest(files) -> str:
 def measured_traffic(workload_name: str, weights: str, shape, gu_alg_bytes: float):
     """DRAM bytes per launch of the gate/up GEMM from the committed ncu
     captures (profiles/traffic.json): (bytes or None, source note).  An entry
-    whose kernel sources have changed since the capture gives None.  Entries
-    captured on a smaller case of the same kernel carry the ratio of the
-    captured traffic to that case's algorithmic bytes, and the figure is that
-    ratio times this workload's algorithmic bytes."""
+    whose kernel sources have changed since the capture gives None.  Each
+    entry was captured on a smaller case of the same kernel and carries the
+    ratio of its traffic to its algorithmic bytes without the shared expert's
+    weights (the routing kernels prefetch those into L2); the figure is that
+    ratio times this workload's algorithmic bytes without them."""
     try:
         with open(TRAFFIC_FILE) as f:
             entries = json.load(f)["entries"]
@@ -270,11 +271,15 @@ def measured_traffic(workload_name: str, weights: str, shape, gu_alg_bytes: floa
             return None, "kernel sources missing"
         if digest != e.get("sources_sha256_16"):
             return None, f"stale: the kernel changed since the capture ({e['capture']})"
-        if e.get("traffic_bytes_per_launch") is not None:
-            return float(e["traffic_bytes_per_launch"]), e["capture"]
-        if e.get("traffic_over_algorithmic") is not None:
-            return float(e["traffic_over_algorithmic"]) * gu_alg_bytes, e["capture"]
+        if e.get("traffic_over_algorithmic_without_shared") is not None:
+            shared = shared_weight_bytes(shape, weights == "fp8") if shape.has_shared else 0
+            return float(e["traffic_over_algorithmic_without_shared"]) * (gu_alg_bytes - shared), e["capture"]
     return None, "no capture of this workload"
+
+
+def shared_weight_bytes(shape, fp8: bool = False) -> int:
+    """The shared expert's gate/up weight bytes (codes and row scales for FP8)."""
+    return 2 * shape.F * shape.d + 2 * shape.F * 4 if fp8 else 2 * shape.F * shape.d * 2
 
 
 def layer_flops(shape):

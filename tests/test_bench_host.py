@@ -44,8 +44,8 @@ def test_traffic_comes_from_the_profiles(tmp_path, monkeypatch):
     alg = bench.gateup_bytes(dec, 281)
     t, src = bench.measured_traffic("decode", "bf16", dec, alg)
     t8, _ = bench.measured_traffic("decode", "fp8", dec, bench.gateup_bytes(dec, 281, fp8=True))
-    assert t is not None and 5.9e9 < t < 6.0e9 and src.startswith("ncu ")
-    assert t8 is not None and 2.95e9 < t8 < 3.05e9
+    assert t is not None and 5.85e9 < t < 6.0e9 and src.startswith("ncu ")
+    assert t8 is not None and 2.9e9 < t8 < 3.1e9
     # the prefill entry was captured on a smaller case and scales with the
     # algorithmic bytes of the workload
     pre = synth.FLASH_PREFILL
