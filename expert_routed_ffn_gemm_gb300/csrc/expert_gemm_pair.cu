@@ -124,7 +124,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tmem_relinquish_pair();
   }
   pdl_wait();  // offsets, rows and outputs belong to earlier work in the stream until here
-  if (warp == kEpilogueWarp0) build_tile_start(args.offsets, G, kPairN, tile_start, lane, s_off);
+  if (warp == kEpilogueWarp0) {
+    if (args.offsets != nullptr) {
+      build_tile_start(args.offsets, G, kPairN, tile_start, lane, s_off);
+    } else if (lane == 0) {
+      // one group whose rows the host knows (G == 1): no dispatch offsets
+      // needed, so the launch may run before the dispatch
+      s_off[0] = args.off_const[0];
+      s_off[1] = args.off_const[1];
+      tile_start[0] = 0;
+      tile_start[1] = (args.off_const[1] - args.off_const[0] + kPairN - 1) / kPairN;
+    }
+  }
   tc_fence_before();
   cluster_sync();  // barrier inits of both CTAs visible before any remote arrive
   tc_fence_after();

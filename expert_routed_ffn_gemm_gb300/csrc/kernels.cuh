@@ -211,6 +211,7 @@ struct GemmArgs {
                        // map_act2 at row (position - act2_from); -1: all through map_act
   int rows_cap;        // rows of the dispatch-ordered buffers (token rows, H, Yp)
   int chunks_cap;      // exponent chunks the Yp exponent buffer holds
+  int off_const[2];    // pair kernels with offsets == NULL: the one group's rows [off_const[0], off_const[1])
 };
 
 // K3/K4: tcgen05 grouped GEMMs over the groups' row blocks.  `tile_n` must be

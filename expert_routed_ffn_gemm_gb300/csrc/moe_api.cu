@@ -25,6 +25,7 @@ constexpr int kProfStages = 6;
 constexpr int kProfEvents = kProfStages + 1;
 constexpr int kProfMaxCalls = 4096;
 constexpr int kFusedGatherMaxTokens = 2;  // the few-token routing launch also copies the rows up to here
+constexpr int kSharedOverlapMinTokens = 2048;  // the shared expert's gate/up on a second stream from here
 
 struct moe_handle {
   uint32_t magic;
@@ -37,6 +38,11 @@ struct moe_handle {
   int tile_down;
   bool use_pairs;   // 256-row token tiles on CTA pairs (MOE_PAIR_TILES=0 turns it off)
   bool small_route; // routing and dispatch in one launch for a few tokens (MOE_SMALL_ROUTE=0 turns it off)
+  // Many tokens: the shared expert's gate/up on a second stream, beside the
+  // dispatch and the row scatter (MOE_SHARED_OVERLAP=0 turns it off)
+  bool shared_overlap;
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   bool fp8_x2;      // FP8 weights: gate/up on E4M3 tensor cores with two-term token rows (MOE_FP8_X2=0: off)
   int gemm_ksplit;  // K split of the bf16 expert GEMMs: -1 = by work items, 1 = off, 2..4 = forced
   int ksplit_cap;   // work items (item, K part) the part buffer holds
@@ -256,8 +262,11 @@ void shared_weights(const moe_handle* h, const void* (&p)[2], long long (&n)[2])
 // K1: router GEMM (K split across CTAs when there are few token tiles) and
 // softmax/top-k into idx/prob/gap, counts per expert; with tokstats, the
 // per-token group masses and entropy for the routing statistics.
+int enqueue_shared_gateup_side(moe_handle* h, const void* x, int T, int k, cudaStream_t s);
+
 int enqueue_router(moe_handle* h, const void* x, int T, CallOpts o, int* idx, float* prob, float* gap,
-                   float* tokstats, int n_groups, cudaStream_t s, bool prefetch_shared = false) {
+                   float* tokstats, int n_groups, cudaStream_t s, bool prefetch_shared = false,
+                   bool fork_shared = false) {
   const moe_config& c = h->cfg;
   // many tokens: the counts come from per-chunk histograms after the top-k
   // kernel (no atomics); otherwise the top-k kernel counts into zeroed counts
@@ -304,6 +313,10 @@ int enqueue_router(moe_handle* h, const void* x, int T, CallOpts o, int* idx, fl
   ra.ksplit = ks;
   if (prefetch_shared) shared_weights(h, ra.pf, ra.pf_bytes);
   MOE_CUDA(moe::launch_router_gemm(bn, &h->map_w3, &map_x, ra, h->num_sms, s));
+  if (fork_shared) {
+    const int rc = enqueue_shared_gateup_side(h, x, T, o.k, s);
+    if (rc != MOE_OK) return rc;
+  }
   MOE_CUDA(moe::launch_router_topk(h->partial, ks, T, c.n_experts, o.k, o.renorm, idx, prob, gap,
                                    chunked ? nullptr : h->counts, tokstats, n_groups, s));
   if (chunked) MOE_CUDA(moe::launch_chunk_counts(idx, T, c.n_experts, o.k, h->chunk_hist, h->counts, s));
@@ -359,11 +372,6 @@ cudaEvent_t* prof_slot(moe_handle* h) {
 #define MOE_MARK(i) \
   if (ev) MOE_CUDA(cudaEventRecord(ev[i], s))
 
-// The grouped FFN over the row groups of `base` (offsets, G, perm/prob/Tk for
-// the gate weights, chunk_base, weight-group mapping): gate/up from the rows
-// behind map_rows (one map per tile width) into H, then down into yout (fp16)
-// and yexp.  mean_rows: mean rows per group (picks the token tile width).
-// ev (or NULL): profiling events 3..5 around the two GEMMs.
 // K parts for a single-CTA bf16 or two-term E4M3 expert GEMM with token tile
 // bn (k_steps: its pipeline stages along K, 16 KB of weights each).  The work
 // items (weight tiles x token tiles, at most items_ub) run in waves over the
@@ -401,30 +409,25 @@ int choose_ksplit(const moe_handle* h, int bn, long long items_ub, int k_steps) 
   return best_cost < 0.95 * base ? best : 1;
 }
 
-int enqueue_ffn(moe_handle* h, moe::GemmArgs a, double mean_rows, const CUtensorMap* map_rows, void* yout,
-                int8_t* yexp, cudaEvent_t* ev, cudaStream_t s, const void* rows2 = nullptr, int n_rows2 = 0,
-                int n_rows = 0) {
+// Token-tile widths and the CTA-pair choice of a grouped FFN call (mean_rows:
+// mean rows per group; n_rows: the call's rows when known), and the arguments
+// both of its GEMMs share.
+struct FfnPlan {
+  int bn1, bn2;        // token tiles of gate/up and down
+  bool pair1, pair2;   // 256-row tiles on CTA pairs
+  long long rows;      // rows of the call (estimated from mean_rows when not known)
+};
+
+FfnPlan plan_ffn(moe_handle* h, moe::GemmArgs& a, double mean_rows, int n_rows) {
   const moe_config& c = h->cfg;
+  FfnPlan p;
   const int cap = h->fp8 ? 128 : 256;
   const int min_tile = (h->fp8 && !h->fp8_x2) || (!h->fp8 && mean_rows >= 8.0) ? 64 : 32;
   const double slack = h->fp8_x2 ? 1.0 : 1.15;
-  const int bn1 = h->tile_gateup ? std::min(h->tile_gateup, cap) : choose_tile(mean_rows, cap, min_tile, slack);
-  const int bn2 = h->tile_down ? std::min(h->tile_down, cap) : choose_tile(mean_rows, cap, min_tile, slack);
-  // 256-row token tiles run on CTA pairs (M = 256 weight rows per pair)
-  const int i128 = tile_index(128);
-  const bool pair1 = h->use_pairs && bn1 == 256;
-  const bool pair2 = h->use_pairs && bn2 == 256 && c.d_model % 256 == 0;
-  // gate/up rows from a.act2_from on come from rows2 [n_rows2][d] (bf16 only)
-  CUtensorMap map2;
-  const CUtensorMap* map_act2 = nullptr;
-  if (a.act2_from >= 0 && rows2 != nullptr && !h->fp8) {
-    if (!encode_2d(&map2, rows2, static_cast<uint64_t>(n_rows2), static_cast<uint64_t>(c.d_model),
-                   pair1 ? 128u : static_cast<uint32_t>(bn1)))
-      return MOE_ERR_CUDA;
-    map_act2 = &map2;
-  } else {
-    a.act2_from = -1;
-  }
+  p.bn1 = h->tile_gateup ? std::min(h->tile_gateup, cap) : choose_tile(mean_rows, cap, min_tile, slack);
+  p.bn2 = h->tile_down ? std::min(h->tile_down, cap) : choose_tile(mean_rows, cap, min_tile, slack);
+  p.pair1 = h->use_pairs && p.bn1 == 256;
+  p.pair2 = h->use_pairs && p.bn2 == 256 && c.d_model % 256 == 0;
   a.err = h->err;
   a.wait_limit_ns = h->wait_limit_ns;
   a.F = c.ffn_width;
@@ -435,10 +438,31 @@ int enqueue_ffn(moe_handle* h, moe::GemmArgs a, double mean_rows, const CUtensor
   a.ksplit_part = h->ksplit_part;
   a.ksplit_cnt = h->ksplit_cnt;
   a.ksplit_cap = h->ksplit_cap;
-  // token tiles: at most one per group that has rows plus rows / bn
-  const long long rows = n_rows > 0 ? n_rows : std::llround(mean_rows * a.G);
-  auto tiles_ub = [&](int bn) { return std::min<long long>(a.G, rows) + rows / bn; };
+  p.rows = n_rows > 0 ? n_rows : std::llround(mean_rows * a.G);
+  return p;
+}
 
+// token tiles: at most one per group that has rows plus rows / bn
+long long tiles_ub(const moe::GemmArgs& a, const FfnPlan& p, int bn) {
+  return std::min<long long>(a.G, p.rows) + p.rows / bn;
+}
+
+// K3: gate/up from the rows behind map_rows (one map per tile width), rows
+// from a.act2_from on from rows2 [n_rows2][d], into H.
+int enqueue_gateup(moe_handle* h, moe::GemmArgs a, double mean_rows, const CUtensorMap* map_rows, cudaEvent_t* ev,
+                   cudaStream_t s, const void* rows2, int n_rows2, int n_rows) {
+  const moe_config& c = h->cfg;
+  const FfnPlan p = plan_ffn(h, a, mean_rows, n_rows);
+  CUtensorMap map2;
+  const CUtensorMap* map_act2 = nullptr;
+  if (a.act2_from >= 0 && rows2 != nullptr && !h->fp8) {
+    if (!encode_2d(&map2, rows2, static_cast<uint64_t>(n_rows2), static_cast<uint64_t>(c.d_model),
+                   p.pair1 ? 128u : static_cast<uint32_t>(p.bn1)))
+      return MOE_ERR_CUDA;
+    map_act2 = &map2;
+  } else {
+    a.act2_from = -1;
+  }
   // gate/up runs its items last group first, so the H rows it writes last are
   // those of the first groups, which the down projection (first group first)
   // then reads while they are still in L2
@@ -446,37 +470,45 @@ int enqueue_ffn(moe_handle* h, moe::GemmArgs a, double mean_rows, const CUtensor
   a.out = h->hbuf;
   a.K = c.d_model;
   a.rows_per_group = 2 * c.ffn_width;
-  a.m_tiles = pair1 ? c.ffn_width / moe::kBlockM : c.ffn_width / (moe::kBlockM / 2);
+  a.m_tiles = p.pair1 ? c.ffn_width / moe::kBlockM : c.ffn_width / (moe::kBlockM / 2);
   a.out_ld = c.ffn_width;
-  const int i1 = tile_index(bn1), i2 = tile_index(bn2);
+  const int i1 = tile_index(p.bn1), i128 = tile_index(128);
   a.w_scale = h->s_gate_up;
   a.ksplit = 1;
   if (h->fp8_x2) {
     a.tok_scale = h->tok_scale;
     a.lo_row0 = h->rows_max;
     a.lo_col0 = 0;
-    a.ksplit = choose_ksplit(h, bn1, tiles_ub(bn1) * a.m_tiles, a.K / moe::kKStepE4M3);
-    MOE_CUDA(moe::launch_expert_gemm_fp8x(true, bn1, &h->map_wgu, &h->map_xq[i1], a, h->num_sms, s));
+    a.ksplit = choose_ksplit(h, p.bn1, tiles_ub(a, p, p.bn1) * a.m_tiles, a.K / moe::kKStepE4M3);
+    MOE_CUDA(moe::launch_expert_gemm_fp8x(true, p.bn1, &h->map_wgu, &h->map_xq[i1], a, h->num_sms, s));
   } else if (h->fp8)
-    MOE_CUDA(moe::launch_expert_gemm_fp8(true, bn1, &h->map_wgu, &map_rows[i1], a, h->num_sms, s));
-  else if (pair1)
+    MOE_CUDA(moe::launch_expert_gemm_fp8(true, p.bn1, &h->map_wgu, &map_rows[i1], a, h->num_sms, s));
+  else if (p.pair1)
     MOE_CUDA(moe::launch_expert_gemm_pair(true, &h->map_wgu, &map_rows[i128], map_act2, a, h->num_sms, s));
   else {
-    a.ksplit = choose_ksplit(h, bn1, tiles_ub(bn1) * a.m_tiles, a.K / moe::kBlockK);
-    MOE_CUDA(moe::launch_expert_gemm(true, bn1, &h->map_wgu, &map_rows[i1], map_act2, a, h->num_sms, s));
+    a.ksplit = choose_ksplit(h, p.bn1, tiles_ub(a, p, p.bn1) * a.m_tiles, a.K / moe::kBlockK);
+    MOE_CUDA(moe::launch_expert_gemm(true, p.bn1, &h->map_wgu, &map_rows[i1], map_act2, a, h->num_sms, s));
   }
   MOE_MARK(4);
+  return MOE_OK;
+}
 
+// K4: down from H into yout (fp16, scaled) and yexp.
+int enqueue_down(moe_handle* h, moe::GemmArgs a, double mean_rows, void* yout, int8_t* yexp, cudaEvent_t* ev,
+                 cudaStream_t s, int n_rows) {
+  const moe_config& c = h->cfg;
+  const FfnPlan p = plan_ffn(h, a, mean_rows, n_rows);
   a.reverse = 0;
   a.act2_from = -1;
   a.out = yout;
   a.out_exp = yexp;
   a.K = c.ffn_width;
   a.rows_per_group = c.d_model;
-  a.m_tiles = pair2 ? c.d_model / (2 * moe::kBlockM) : c.d_model / moe::kBlockM;
+  a.m_tiles = p.pair2 ? c.d_model / (2 * moe::kBlockM) : c.d_model / moe::kBlockM;
   a.out_ld = c.d_model;
   a.w_scale = h->s_down;
   a.ksplit = 1;
+  const int i2 = tile_index(p.bn2), i128 = tile_index(128);
   if (h->fp8_x2) {
     // H in place as two-term E4M3 rows, their 1/s in tok_scale (gate/up has
     // read the token scales by now)
@@ -484,17 +516,54 @@ int enqueue_ffn(moe_handle* h, moe::GemmArgs a, double mean_rows, const CUtensor
     a.tok_scale = h->tok_scale;
     a.lo_row0 = 0;
     a.lo_col0 = c.ffn_width;
-    a.ksplit = choose_ksplit(h, bn2, tiles_ub(bn2) * a.m_tiles, a.K / moe::kKStepE4M3);
-    MOE_CUDA(moe::launch_expert_gemm_fp8x(false, bn2, &h->map_wd, &h->map_hq[i2], a, h->num_sms, s));
+    a.ksplit = choose_ksplit(h, p.bn2, tiles_ub(a, p, p.bn2) * a.m_tiles, a.K / moe::kKStepE4M3);
+    MOE_CUDA(moe::launch_expert_gemm_fp8x(false, p.bn2, &h->map_wd, &h->map_hq[i2], a, h->num_sms, s));
   } else if (h->fp8)
-    MOE_CUDA(moe::launch_expert_gemm_fp8(false, bn2, &h->map_wd, &h->map_h[i2], a, h->num_sms, s));
-  else if (pair2)
+    MOE_CUDA(moe::launch_expert_gemm_fp8(false, p.bn2, &h->map_wd, &h->map_h[i2], a, h->num_sms, s));
+  else if (p.pair2)
     MOE_CUDA(moe::launch_expert_gemm_pair(false, &h->map_wd, &h->map_h[i128], nullptr, a, h->num_sms, s));
   else {
-    a.ksplit = choose_ksplit(h, bn2, tiles_ub(bn2) * a.m_tiles, a.K / moe::kBlockK);
-    MOE_CUDA(moe::launch_expert_gemm(false, bn2, &h->map_wd, &h->map_h[i2], nullptr, a, h->num_sms, s));
+    a.ksplit = choose_ksplit(h, p.bn2, tiles_ub(a, p, p.bn2) * a.m_tiles, a.K / moe::kBlockK);
+    MOE_CUDA(moe::launch_expert_gemm(false, p.bn2, &h->map_wd, &h->map_h[i2], nullptr, a, h->num_sms, s));
   }
   MOE_MARK(5);
+  return MOE_OK;
+}
+
+// The grouped FFN over the row groups of `a` (offsets, G, perm/prob/Tk for
+// the gate weights, chunk_base, weight-group mapping): gate/up from the rows
+// behind map_rows (one map per tile width) into H, then down into yout (fp16)
+// and yexp.  mean_rows: mean rows per group (picks the token tile width).
+// ev (or NULL): profiling events around the two GEMMs.
+int enqueue_ffn(moe_handle* h, moe::GemmArgs a, double mean_rows, const CUtensorMap* map_rows, void* yout,
+                int8_t* yexp, cudaEvent_t* ev, cudaStream_t s, const void* rows2 = nullptr, int n_rows2 = 0,
+                int n_rows = 0) {
+  const int rc = enqueue_gateup(h, a, mean_rows, map_rows, ev, s, rows2, n_rows2, n_rows);
+  if (rc != MOE_OK) return rc;
+  return enqueue_down(h, a, mean_rows, yout, yexp, ev, s, n_rows);
+}
+
+// The shared expert's gate/up on the handle's second stream: it needs x
+// alone, so it runs on CTA pairs beside the routing's later kernels, the
+// dispatch and the row copy (which use few tensor cores), writing rows
+// [T*k, T*k + T) of H; ev_join marks its end.
+int enqueue_shared_gateup_side(moe_handle* h, const void* x, int T, int k, cudaStream_t s) {
+  const moe_config& c = h->cfg;
+  MOE_CUDA(cudaEventRecord(h->ev_fork, s));
+  MOE_CUDA(cudaStreamWaitEvent(h->side, h->ev_fork, 0));
+  moe::GemmArgs sa{};
+  sa.offsets = nullptr;  // one group, rows [T*k, T*k + T): known here
+  sa.off_const[0] = T * k;
+  sa.off_const[1] = T * k + T;
+  sa.G = 1;
+  sa.perm = h->perm;
+  sa.prob = h->prob;
+  sa.Tk = T * k;
+  sa.w_group_base = c.n_experts;
+  sa.act2_from = T * k;
+  const int rc = enqueue_gateup(h, sa, static_cast<double>(T), h->map_xp, nullptr, h->side, x, T, T * k + T);
+  if (rc != MOE_OK) return rc;
+  MOE_CUDA(cudaEventRecord(h->ev_join, h->side));
   return MOE_OK;
 }
 
@@ -503,6 +572,8 @@ int enqueue_forward(moe_handle* h, const void* x, int T, CallOpts o, void* y, cu
   cudaEvent_t* ev = prof_slot(h);
   MOE_MARK(0);
   const bool fused_route = small_route(h, T);
+  const bool overlap_shared = h->shared_overlap && h->use_pairs && !h->fp8 && c.has_shared && !fused_route &&
+                              T >= kSharedOverlapMinTokens;
   // with one or two tokens (bf16 weights) that launch also copies the routed
   // rows into dispatch order (a handful of rows: one block is enough)
   const bool fused_gather = fused_route && !h->fp8 && T <= kFusedGatherMaxTokens;
@@ -521,7 +592,9 @@ int enqueue_forward(moe_handle* h, const void* x, int T, CallOpts o, void* y, cu
                                      h->counts, h->offsets, h->perm, h->inv, h->chunk_base, ex, s));
     MOE_MARK(1);
   } else {
-    const int rc = enqueue_router(h, x, T, o, h->idx, h->prob, nullptr, nullptr, 0, s, true);
+    // many tokens: the shared expert's gate/up forks off after the router
+    // GEMM (see enqueue_shared_gateup_side), joined back before the down GEMM
+    const int rc = enqueue_router(h, x, T, o, h->idx, h->prob, nullptr, nullptr, 0, s, true, overlap_shared);
     if (rc != MOE_OK) return rc;
     MOE_MARK(1);
     MOE_CUDA(moe::launch_dispatch(h->idx, h->counts, T, c.n_experts, o.k, c.has_shared, h->offsets, h->perm, h->inv,
@@ -548,22 +621,36 @@ int enqueue_forward(moe_handle* h, const void* x, int T, CallOpts o, void* y, cu
   a.Tk = T * o.k;
   a.chunk_base = h->chunk_base;
   a.act2_from = shared_from_x ? T * o.k : -1;
-  if (int rc2 = enqueue_ffn(h, a, static_cast<double>(T) * o.k / c.n_experts, h->map_xp, h->yp, h->yexp, ev, s,
-                            x, T, T * o.k + (c.has_shared ? T : 0)))
-    return rc2;
+  const double mean_rows = static_cast<double>(T) * o.k / c.n_experts;
+  const int n_rows = T * o.k + (c.has_shared ? T : 0);
+  moe::GemmArgs ag = a;
+  if (overlap_shared) ag.G = c.n_experts;  // the routed groups; the shared one runs on the second stream
+  if (int rc2 = enqueue_gateup(h, ag, mean_rows, h->map_xp, ev, s, x, T, n_rows)) return rc2;
+  if (overlap_shared) MOE_CUDA(cudaStreamWaitEvent(s, h->ev_join, 0));
+  if (int rc2 = enqueue_down(h, a, mean_rows, h->yp, h->yexp, ev, s, n_rows)) return rc2;
   MOE_CUDA(moe::launch_combine(static_cast<const __half*>(h->yp), h->yexp, nullptr, nullptr, h->idx, h->inv,
                                h->offsets, h->chunk_base, T, o.k, c.n_experts, c.d_model, c.has_shared, y, c.out_fp32,
                                s));
   MOE_MARK(6);
   // router GEMM, top-k, dispatch, gather, gate/up, down, combine; many
-  // tokens: two more for the chunk histograms and their scan; a few tokens:
+  // tokens: two more for the chunk histograms and their scan, and one more
+  // for the shared expert's gate/up on the second stream; a few tokens:
   // routing and dispatch in one (one or two tokens: and the gather); FP8
   // two-term rows: one more for the requantisation of H
-  h->last_kernels = (fused_route ? (fused_gather ? 4 : 5) : moe::chunked_dispatch(T) ? 9 : 7) + (h->fp8_x2 ? 1 : 0);
+  h->last_kernels = (fused_route ? (fused_gather ? 4 : 5) : moe::chunked_dispatch(T) ? 9 : 7) + (h->fp8_x2 ? 1 : 0) +
+                    (overlap_shared ? 1 : 0);
   return MOE_OK;
 }
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+void release_streams(moe_handle* h) {
+  if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+  if (h->ev_join) cudaEventDestroy(h->ev_join);
+  if (h->side) cudaStreamDestroy(h->side);
+  h->ev_fork = h->ev_join = nullptr;
+  h->side = nullptr;
+}
 
 }  // namespace
 
@@ -660,6 +747,8 @@ int init_any(const moe_config* cfg, const moe_weights* w, const float* s_gu, con
     h->use_pairs = !(v && v[0] == '0');
     const char* vs = std::getenv("MOE_SMALL_ROUTE");
     h->small_route = !(vs && vs[0] == '0');
+    const char* vo = std::getenv("MOE_SHARED_OVERLAP");
+    h->shared_overlap = !(vo && vo[0] == '0');
     const char* vx = std::getenv("MOE_FP8_X2");
     // the in-place requantisation of H holds a row in registers: F <= 8192
     h->fp8_x2 = fp8 && !(vx && vx[0] == '0') && c.ffn_width <= 8192;
@@ -754,9 +843,13 @@ int init_any(const moe_config* cfg, const moe_weights* w, const float* s_gu, con
     ok = ok && encode_2d(&h->map_hq[i], h->hbuf, RH, 2 * F, moe::kTileN[i], true);
     ok = ok && encode_2d(&h->map_h[i], h->hbuf, RH, F, moe::kTileN[i]);
   }
+  ok = ok && cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) == cudaSuccess;
+  ok = ok && cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) == cudaSuccess;
+  ok = ok && cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) == cudaSuccess;
   ok = ok && cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
+    release_streams(h);
     cudaFree(h->ws);
     delete h;
     return MOE_ERR_CUDA;
@@ -809,6 +902,8 @@ int moe_ep_dispatch(moe_handle* h, const void* x, int T, void* send_rows, float*
   // the routing and dispatch of the whole-layer call on the same tokens (so
   // that both give the same rows and weights)
   const bool fused_route = small_route(h, T);
+  const bool overlap_shared = h->shared_overlap && h->use_pairs && !h->fp8 && c.has_shared && !fused_route &&
+                              T >= kSharedOverlapMinTokens;
   if (fused_route) {
     MOE_CUDA(moe::launch_route_small(static_cast<const bf16*>(x), h->w.w_router, T, c.d_model, E, k, 0, c.has_shared,
                                      h->partial, h->route_done, h->idx, h->prob, nullptr, h->counts, h->offsets,
@@ -1064,6 +1159,7 @@ int moe_free(moe_handle* h) {
   const bool ok = cudaDeviceSynchronize() == cudaSuccess;
   for (auto& ev : h->prof)
     for (auto e : ev) cudaEventDestroy(e);
+  release_streams(h);
   const bool freed = cudaFree(h->ws) == cudaSuccess;
   delete h;
   return (ok && freed) ? MOE_OK : MOE_ERR_CUDA;

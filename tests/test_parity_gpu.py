@@ -399,3 +399,40 @@ def test_few_token_routing_both_paths(fused, T, d, E, k):
     y2 = layer.forward(x)
     assert torch.equal(y, y2)
     layer.close()
+
+
+@pytest.mark.parametrize("overlap", ["1", "0"])
+def test_shared_expert_on_a_second_stream(overlap):
+    # From 2048 tokens on the shared expert's gate/up runs on a second stream
+    # beside the dispatch and row scatter (MOE_SHARED_OVERLAP=0: in the one
+    # gate/up launch): same results bit for bit, against the oracle, and the
+    # fork and join capture into a CUDA graph whose replays match the eager call.
+    shape = synth.LayerShape(T=2500, d=256, E=16, k=2, F=128)
+    inp = synth.make_inputs(shape, seed=501)
+    layer, x = make_layer(inp, env={"MOE_SHARED_OVERLAP": overlap})
+    y = layer.forward(x)
+    assert layer.check() == binding.MOE_OK
+    assert layer.last_kernel_count() == (10 if overlap == "1" else 9)
+    other, _ = make_layer(inp, env={"MOE_SHARED_OVERLAP": "0" if overlap == "1" else "1"})
+    assert torch.equal(y, other.forward(x))
+    other.close()
+    idx, prob, perm, offsets, gap = layer.route(x)
+    xb, wr, wgu, wd = host_bits(inp)
+    near, _ = check_routing(xb, wr, shape.k, cpu(idx), cpu(prob), cpu(gap), cpu(perm), cpu(offsets))
+    tokens = sample_tokens(shape.T, cpu(idx), 96, seed=5, extra=near)
+    check_output(xb, wr, wgu, wd, shape.k, cpu(y.float())[tokens], cpu(idx), tokens=tokens)
+    yg = torch.empty_like(y)
+    layer.forward(x, yg)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        with torch.cuda.graph(g, stream=st):
+            layer.forward(x, yg, stream=st)
+    for seed in (502, 503):
+        x.copy_(synth.make_tokens(shape, seed=seed, device=DEV))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(yg, layer.forward(x))
+    assert layer.check() == binding.MOE_OK
+    layer.close()
