@@ -45,11 +45,12 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* 
 }
 
 // offsets[0..E+1] (exclusive prefix of the counts, then the shared expert's T
-// rows) and chunk_base[0..E+1] (the same over ceil(count / kYpRows)), by one
+// rows) and chunk_base[0..E+1] (the same over ceil(count / kYpRows), the
+// shared expert's chunks from shared_chunk0(T, k, E) on), by one
 // block whose threads each scan a contiguous run of experts.  base (shared
 // memory, or NULL) gets offsets[0..E-1] too.
-__device__ void write_offsets(const int* __restrict__ counts, int T, int E, int has_shared, int* __restrict__ offsets,
-                              int* __restrict__ chunk_base, int* warp_sums, int* base) {
+__device__ void write_offsets(const int* __restrict__ counts, int T, int E, int k, int has_shared,
+                              int* __restrict__ offsets, int* __restrict__ chunk_base, int* warp_sums, int* base) {
   const int per = (E + kDispatchThreads - 1) / kDispatchThreads;
   const int b = threadIdx.x * per;
   int local = 0;
@@ -76,8 +77,8 @@ __device__ void write_offsets(const int* __restrict__ counts, int T, int E, int 
     run += (counts[i] + kYpRows - 1) / kYpRows;
   }
   if (threadIdx.x == 0) {
-    chunk_base[E] = total;
-    chunk_base[E + 1] = total + (has_shared ? (T + kYpRows - 1) / kYpRows : 0);
+    chunk_base[E] = shared_chunk0(T, k, E);  // the routed chunks end at total <= this
+    chunk_base[E + 1] = chunk_base[E] + (has_shared ? (T + kYpRows - 1) / kYpRows : 0);
   }
 }
 
@@ -99,7 +100,7 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(const int* _
   int base_e;
   block_exclusive_scan(part, warp_sums, &base_e);
 
-  if (e == 0) write_offsets(counts, T, E, has_shared, offsets, chunk_base, warp_sums, nullptr);
+  if (e == 0) write_offsets(counts, T, E, k, has_shared, offsets, chunk_base, warp_sums, nullptr);
 
   int running = 0;
   for (int t0 = 0; t0 < T; t0 += kDispatchThreads) {
@@ -212,7 +213,7 @@ __global__ void __launch_bounds__(kChunkTokens) chunk_place_kernel(const int* __
   uint32_t* mask = sm;
   int* base = reinterpret_cast<int*>(sm + kChunkWarps * E);
   const bool first = blockIdx.x == 0;
-  write_offsets(counts, T, E, has_shared, first ? offsets : nullptr, chunk_base, warp_sums, base);
+  write_offsets(counts, T, E, k, has_shared, first ? offsets : nullptr, chunk_base, warp_sums, base);
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += kChunkTokens) base[e] += chunk_first[static_cast<size_t>(blockIdx.x) * E + e];
   chunk_masks(idx, T, E, k, mask);  // its barriers also publish base[]

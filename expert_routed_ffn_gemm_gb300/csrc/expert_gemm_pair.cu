@@ -284,7 +284,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tile_rows(pair, it0, r0, v0);
       gate_perm_entries<kPairN>(pe, r0, v0, lane, args.perm, args.Tk);
       gate_probs<kPairN>(wreg, pe, args.prob);
-      cbase_next = __ldg(args.chunk_base + it0.g);
+      cbase_next = args.chunk_base != nullptr ? __ldg(args.chunk_base + it0.g) : args.chunk_const;
     }
     for (int item = pair; item < n_items; item += n_pairs) {
       Item it;
@@ -315,7 +315,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (has_next) {
           tile_rows(item + n_pairs, it_n, row0_n, valid_n);
           gate_perm_entries<kPairN>(pe, row0_n, valid_n, lane, args.perm, args.Tk);
-          cbase_next = __ldg(args.chunk_base + it_n.g);
+          cbase_next = args.chunk_base != nullptr ? __ldg(args.chunk_base + it_n.g) : args.chunk_const;
         }
         epilogue_down_pipelined<kPairN>(taddr, it.m * 2 * kBlockM + static_cast<int>(rank) * kBlockM + row, row0,
                                         valid, wreg, static_cast<__half*>(args.out), args.out_exp, args.out_ld,

@@ -97,6 +97,10 @@ constexpr int kMaxStatGroups = 64;  // expert groups of the routing statistics
 // sum over g' < g of ceil(rows(g') / kYpRows); the exponents are [chunk][d].
 constexpr int kYpRows = 16;
 constexpr int kYpExpMax = 113;
+// The shared expert's chunks start at a place fixed by T, k and E (past every
+// chunk the routed experts can have: their rows rounded up per expert), so a
+// launch can write them before the dispatch has counted the routed rows.
+__host__ __device__ inline int shared_chunk0(int T, int k, int E) { return (T * k + kYpRows - 1) / kYpRows + E; }
 
 // Token-tile widths (N of tcgen05.mma) the grouped GEMMs are built for.
 constexpr int kNumTileN = 5;
@@ -212,6 +216,7 @@ struct GemmArgs {
   int rows_cap;        // rows of the dispatch-ordered buffers (token rows, H, Yp)
   int chunks_cap;      // exponent chunks the Yp exponent buffer holds
   int off_const[2];    // pair kernels with offsets == NULL: the one group's rows [off_const[0], off_const[1])
+  int chunk_const;     // ... and with chunk_base == NULL (down): the group's first exponent chunk
 };
 
 // K3/K4: tcgen05 grouped GEMMs over the groups' row blocks.  `tile_n` must be

@@ -262,7 +262,7 @@ void shared_weights(const moe_handle* h, const void* (&p)[2], long long (&n)[2])
 // K1: router GEMM (K split across CTAs when there are few token tiles) and
 // softmax/top-k into idx/prob/gap, counts per expert; with tokstats, the
 // per-token group masses and entropy for the routing statistics.
-int enqueue_shared_gateup_side(moe_handle* h, const void* x, int T, int k, cudaStream_t s);
+int enqueue_shared_ffn_side(moe_handle* h, const void* x, int T, int k, cudaStream_t s);
 
 int enqueue_router(moe_handle* h, const void* x, int T, CallOpts o, int* idx, float* prob, float* gap,
                    float* tokstats, int n_groups, cudaStream_t s, bool prefetch_shared = false,
@@ -314,7 +314,7 @@ int enqueue_router(moe_handle* h, const void* x, int T, CallOpts o, int* idx, fl
   if (prefetch_shared) shared_weights(h, ra.pf, ra.pf_bytes);
   MOE_CUDA(moe::launch_router_gemm(bn, &h->map_w3, &map_x, ra, h->num_sms, s));
   if (fork_shared) {
-    const int rc = enqueue_shared_gateup_side(h, x, T, o.k, s);
+    const int rc = enqueue_shared_ffn_side(h, x, T, o.k, s);
     if (rc != MOE_OK) return rc;
   }
   MOE_CUDA(moe::launch_router_topk(h->partial, ks, T, c.n_experts, o.k, o.renorm, idx, prob, gap,
@@ -543,11 +543,13 @@ int enqueue_ffn(moe_handle* h, moe::GemmArgs a, double mean_rows, const CUtensor
   return enqueue_down(h, a, mean_rows, yout, yexp, ev, s, n_rows);
 }
 
-// The shared expert's gate/up on the handle's second stream: it needs x
-// alone, so it runs on CTA pairs beside the routing's later kernels, the
-// dispatch and the row copy (which use few tensor cores), writing rows
-// [T*k, T*k + T) of H; ev_join marks its end.
-int enqueue_shared_gateup_side(moe_handle* h, const void* x, int T, int k, cudaStream_t s) {
+// The shared expert's FFN on the handle's second stream: it needs x alone,
+// so it runs on CTA pairs beside the routing's later kernels, the dispatch
+// and the row copy (which use few tensor cores): gate/up into rows
+// [T*k, T*k + T) of H, then down into the same rows of Yp and the exponent
+// chunks from shared_chunk0 on (where the dispatch places them); ev_join
+// marks its end.
+int enqueue_shared_ffn_side(moe_handle* h, const void* x, int T, int k, cudaStream_t s) {
   const moe_config& c = h->cfg;
   MOE_CUDA(cudaEventRecord(h->ev_fork, s));
   MOE_CUDA(cudaStreamWaitEvent(h->side, h->ev_fork, 0));
@@ -561,7 +563,11 @@ int enqueue_shared_gateup_side(moe_handle* h, const void* x, int T, int k, cudaS
   sa.Tk = T * k;
   sa.w_group_base = c.n_experts;
   sa.act2_from = T * k;
-  const int rc = enqueue_gateup(h, sa, static_cast<double>(T), h->map_xp, nullptr, h->side, x, T, T * k + T);
+  int rc = enqueue_gateup(h, sa, static_cast<double>(T), h->map_xp, nullptr, h->side, x, T, T * k + T);
+  if (rc != MOE_OK) return rc;
+  sa.chunk_base = nullptr;
+  sa.chunk_const = moe::shared_chunk0(T, k, c.n_experts);
+  rc = enqueue_down(h, sa, static_cast<double>(T), h->yp, h->yexp, nullptr, h->side, T * k + T);
   if (rc != MOE_OK) return rc;
   MOE_CUDA(cudaEventRecord(h->ev_join, h->side));
   return MOE_OK;
@@ -592,8 +598,8 @@ int enqueue_forward(moe_handle* h, const void* x, int T, CallOpts o, void* y, cu
                                      h->counts, h->offsets, h->perm, h->inv, h->chunk_base, ex, s));
     MOE_MARK(1);
   } else {
-    // many tokens: the shared expert's gate/up forks off after the router
-    // GEMM (see enqueue_shared_gateup_side), joined back before the down GEMM
+    // many tokens: the shared expert's FFN forks off after the router GEMM
+    // (see enqueue_shared_ffn_side), joined back before the combine
     const int rc = enqueue_router(h, x, T, o, h->idx, h->prob, nullptr, nullptr, 0, s, true, overlap_shared);
     if (rc != MOE_OK) return rc;
     MOE_MARK(1);
@@ -623,22 +629,21 @@ int enqueue_forward(moe_handle* h, const void* x, int T, CallOpts o, void* y, cu
   a.act2_from = shared_from_x ? T * o.k : -1;
   const double mean_rows = static_cast<double>(T) * o.k / c.n_experts;
   const int n_rows = T * o.k + (c.has_shared ? T : 0);
-  moe::GemmArgs ag = a;
-  if (overlap_shared) ag.G = c.n_experts;  // the routed groups; the shared one runs on the second stream
-  if (int rc2 = enqueue_gateup(h, ag, mean_rows, h->map_xp, ev, s, x, T, n_rows)) return rc2;
-  if (overlap_shared) MOE_CUDA(cudaStreamWaitEvent(s, h->ev_join, 0));
+  if (overlap_shared) a.G = c.n_experts;  // the routed groups; the shared one runs on the second stream
+  if (int rc2 = enqueue_gateup(h, a, mean_rows, h->map_xp, ev, s, x, T, n_rows)) return rc2;
   if (int rc2 = enqueue_down(h, a, mean_rows, h->yp, h->yexp, ev, s, n_rows)) return rc2;
+  if (overlap_shared) MOE_CUDA(cudaStreamWaitEvent(s, h->ev_join, 0));  // the shared expert's Yp rows
   MOE_CUDA(moe::launch_combine(static_cast<const __half*>(h->yp), h->yexp, nullptr, nullptr, h->idx, h->inv,
                                h->offsets, h->chunk_base, T, o.k, c.n_experts, c.d_model, c.has_shared, y, c.out_fp32,
                                s));
   MOE_MARK(6);
   // router GEMM, top-k, dispatch, gather, gate/up, down, combine; many
-  // tokens: two more for the chunk histograms and their scan, and one more
-  // for the shared expert's gate/up on the second stream; a few tokens:
+  // tokens: two more for the chunk histograms and their scan, and two more
+  // for the shared expert's gate/up and down on the second stream; a few tokens:
   // routing and dispatch in one (one or two tokens: and the gather); FP8
   // two-term rows: one more for the requantisation of H
   h->last_kernels = (fused_route ? (fused_gather ? 4 : 5) : moe::chunked_dispatch(T) ? 9 : 7) + (h->fp8_x2 ? 1 : 0) +
-                    (overlap_shared ? 1 : 0);
+                    (overlap_shared ? 2 : 0);
   return MOE_OK;
 }
 

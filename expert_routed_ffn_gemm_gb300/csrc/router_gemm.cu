@@ -650,8 +650,8 @@ __global__ void __launch_bounds__(kSmallRouteWarps * 32) route_small_kernel(
         offsets[E] = total;
         offsets[E + 1] = total + (has_shared ? T : 0);
       } else {
-        chunk_base[E] = total;
-        chunk_base[E + 1] = total + (has_shared ? (T + kYpRows - 1) / kYpRows : 0);
+        chunk_base[E] = shared_chunk0(T, k, E);  // the routed chunks end at total <= this
+        chunk_base[E + 1] = chunk_base[E] + (has_shared ? (T + kYpRows - 1) / kYpRows : 0);
       }
     }
     __syncthreads();

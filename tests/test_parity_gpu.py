@@ -412,7 +412,7 @@ def test_shared_expert_on_a_second_stream(overlap):
     layer, x = make_layer(inp, env={"MOE_SHARED_OVERLAP": overlap})
     y = layer.forward(x)
     assert layer.check() == binding.MOE_OK
-    assert layer.last_kernel_count() == (10 if overlap == "1" else 9)
+    assert layer.last_kernel_count() == (11 if overlap == "1" else 9)
     other, _ = make_layer(inp, env={"MOE_SHARED_OVERLAP": "0" if overlap == "1" else "1"})
     assert torch.equal(y, other.forward(x))
     other.close()
