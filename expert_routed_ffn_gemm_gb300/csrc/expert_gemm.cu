@@ -111,14 +111,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  const int n_base = tile_start[G] * args.m_tiles;
-  const int ks = (BN <= 32 && args.ksplit > 1 && n_base * args.ksplit <= args.ksplit_cap) ? args.ksplit : 1;
-  const int n_items = n_base * ks;  // work items: (item, K part), the parts of an item adjacent
+  const int n_base = tile_start[G] * args.m_tiles;  // work items (group, token tile, weight tile)
+  const int k_all = args.K / kBlockK;
+  // K split (token tiles of at most 32 rows, few items): balanced ranges of K
+  // steps when the host asks for them, else ksplit equal parts per item, as
+  // long as the part buffer holds the parts; otherwise whole items
+  int mode = kWhole;
+  if (BN <= 32 && args.ksplit > 1) {
+    if (args.kbalance && 2 * static_cast<int>(gridDim.x) <= args.ksplit_cap)
+      mode = kBalanced;
+    else if (!args.kbalance && n_base * args.ksplit <= args.ksplit_cap)
+      mode = kEqualK;
+  }
   const uint64_t limit = args.wait_limit_ns;
-  // K steps of part p of an item: [p * k_per, min(k_steps, (p + 1) * k_per)),
-  // never empty (the host picks ks so that every part has one)
-  const int k_steps_all = args.K / kBlockK;
-  const int k_per = (k_steps_all + ks - 1) / ks;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -130,20 +135,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         return weight_group(args, it.g) * args.rows_per_group + it.m * (GATEUP ? kBlockM / 2 : kBlockM);
       };
       auto rows_of = [&](int item, int& row_w, int& row_act) {
-        const Item it = decode_item(item / ks, args.m_tiles, tile_start, G, n_items / ks, args.reverse);
+        const Item it = decode_item(item, args.m_tiles, tile_start, G, n_base, args.reverse);
         row_w = weight_row(it);
         row_act = __ldg(args.offsets + it.g) + it.n * BN;
       };
+      UnitCursor cur;
+      cur.init(mode, n_base, k_all, args.ksplit);
+      WorkUnit u, nu;
+      bool has = cur.next(u);
+      bool has_next = has && cur.next(nu);
       uint32_t stage = 0, phase = 0;
       long issued = 0;
       bool ok = true;
       int next_w = 0, next_act = 0;
-      if (static_cast<int>(blockIdx.x) < n_items) rows_of(blockIdx.x, next_w, next_act);
-      for (int item = blockIdx.x; ok && item < n_items && !*abort_flag; item += gridDim.x) {
+      if (has) rows_of(u.item, next_w, next_act);
+      while (ok && has && !*abort_flag) {
         const int row_w = next_w, row_act = next_act;
-        const int part = item % ks;
-        const int kb1 = min(k_steps_all, (part + 1) * k_per);
-        for (int kb = part * k_per; kb < kb1; ++kb) {
+        for (int kb = u.kb0; kb < u.kb1; ++kb) {
           if (!wait_or_abort(&empty[stage], phase ^ 1u, limit, abort_flag)) {
             record_abort(abort_flag, args.err);
             ok = false;
@@ -162,11 +170,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             stage = 0;
             phase ^= 1u;
           }
-          // the next item's rows, worked out while this item's loads are in
+          // the next unit's rows, worked out while this unit's loads are in
           // flight (its offsets come from global memory)
-          if (kb == part * k_per && item + static_cast<int>(gridDim.x) < n_items)
-            rows_of(item + gridDim.x, next_w, next_act);
+          if (kb == u.kb0 && has_next) rows_of(nu.item, next_w, next_act);
         }
+        u = nu;
+        has = has_next;
+        if (has) has_next = cur.next(nu);
       }
       // Drain: the last load issued into each stage must have landed before
       // this CTA may exit (they always complete; the wait is bounded anyway).
@@ -182,24 +192,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool issued_any = false, ok = true;
       // N of the MMAs: the tile's rows rounded up to 16 (ragged tails); the
-      // next item's descriptor is worked out while this item's MMAs run
+      // next unit's descriptor is worked out while this unit's MMAs run
       auto idesc_of = [&](int item) {
-        return item < n_items ? item_idesc(item / ks, n_items / ks, args.reverse, args.m_tiles, tile_start, G,
-                                           args.offsets, kBlockM, 16, BN)
-                              : 0u;
+        return item_idesc(item, n_base, args.reverse, args.m_tiles, tile_start, G, args.offsets, kBlockM, 16, BN);
       };
-      uint32_t next_idesc = idesc_of(blockIdx.x);
-      for (int item = blockIdx.x; ok && item < n_items && !*abort_flag; item += gridDim.x) {
+      UnitCursor cur;
+      cur.init(mode, n_base, k_all, args.ksplit);
+      WorkUnit u, nu;
+      bool has = cur.next(u);
+      bool has_next = has && cur.next(nu);
+      uint32_t next_idesc = has ? idesc_of(u.item) : 0u;
+      while (ok && has && !*abort_flag) {
         const uint32_t idesc = next_idesc;
-        const int part = item % ks;
-        const int kb0 = part * k_per, kb1 = min(k_steps_all, (part + 1) * k_per);
         if (!wait_or_abort(&acc_empty[acc], acc_phase ^ 1u, limit, abort_flag)) {
           record_abort(abort_flag, args.err);
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int kb = u.kb0; kb < u.kb1; ++kb) {
           if (!wait_or_abort(&full[stage], phase, limit, abort_flag)) {
             record_abort(abort_flag, args.err);
             ok = false;
@@ -211,14 +222,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t b = smem_desc_sw128(st + C::A_BYTES);
 #pragma unroll
           for (int kk = 0; kk < kBlockK / 16; ++kk)  // +32 B along K = +2 in the address field
-            tc_mma_bf16(d_tmem, a + 2 * kk, b + 2 * kk, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+            tc_mma_bf16(d_tmem, a + 2 * kk, b + 2 * kk, idesc, (kb > u.kb0 || kk > 0) ? 1u : 0u);
           issued_any = true;
           tc_commit(&empty[stage]);
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
-          if (kb == kb0) next_idesc = idesc_of(item + gridDim.x);
+          if (kb == u.kb0 && has_next) next_idesc = idesc_of(nu.item);
         }
         if (!ok) break;
         tc_commit(&acc_full[acc]);
@@ -226,6 +237,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc = 0;
           acc_phase ^= 1u;
         }
+        u = nu;
+        has = has_next;
+        if (has) has_next = cur.next(nu);
       }
       if (issued_any) {
         // every MMA of this CTA has finished before tensor memory is freed
@@ -239,8 +253,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = q * 32 + lane;
     uint32_t acc = 0, acc_phase = 0, it_par = 0, chunk_par = 0;
     volatile int* s_last = reinterpret_cast<volatile int*>(tmem_holder + 2);
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-      const Item it = decode_item(item / ks, args.m_tiles, tile_start, G, n_items / ks, args.reverse);
+    UnitCursor cur;
+    cur.init(mode, n_base, k_all, args.ksplit);
+    WorkUnit u;
+    while (cur.next(u)) {
+      const Item it = decode_item(u.item, args.m_tiles, tile_start, G, n_base, args.reverse);
       const int g_row0 = __ldg(args.offsets + it.g);
       const int g_rows = __ldg(args.offsets + it.g + 1) - g_row0;
       const int row0 = g_row0 + it.n * BN;
@@ -253,10 +270,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       if constexpr (BN <= 32) {
-        if (ks > 1) {
+        if (u.parts > 1) {
           // this part's accumulator row to the part buffer, tensor memory back
           // to the MMA, then the last part of the item sums the parts in order
-          ksplit_store_part<BN>(taddr, 0, valid, args.ksplit_part + (static_cast<size_t>(item) * kBlockM + row) * BN);
+          ksplit_store_part<BN>(taddr, 0, valid,
+                                args.ksplit_part + (static_cast<size_t>(u.slot) * kBlockM + row) * BN);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[acc]);
@@ -264,11 +282,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             acc = 0;
             acc_phase ^= 1u;
           }
-          const int base = item / ks;
-          if (ksplit_arrive(args.ksplit_cnt + base, ks, s_last, q == 0 && lane == 0)) {
+          if (ksplit_arrive(args.ksplit_cnt + u.slot0, u.parts, s_last, q == 0 && lane == 0)) {
             float sum[BN];
-            ksplit_sum_parts<BN>(args.ksplit_part + (static_cast<size_t>(base * ks) * kBlockM + row) * BN, ks, valid,
-                                 sum);
+            ksplit_sum_units<BN>(args.ksplit_part, cur, u, row, valid, sum);
             if (GATEUP)
               epilogue_gateup<BN>(0u, row, it.m * (kBlockM / 2), row0, valid, static_cast<bf16*>(args.out),
                                   args.out_ld, xchg, chunk_par, 1.0f, sum);
@@ -276,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               epilogue_down<BN>(0u, it.m * kBlockM + row, row0, valid, wreg, static_cast<__half*>(args.out),
                                 args.out_exp, args.out_ld, chunk0,
                                 1.0f, 0, sum);
-            if (q == 0 && lane == 0) args.ksplit_cnt[base] = 0;  // ready for the next launch
+            if (q == 0 && lane == 0) args.ksplit_cnt[u.slot0] = 0;  // ready for the next launch
           }
           continue;
         }

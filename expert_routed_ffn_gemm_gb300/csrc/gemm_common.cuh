@@ -219,6 +219,128 @@ __device__ __forceinline__ void epilogue_gateup(uint32_t taddr, int row, int fea
   }
 }
 
+// Work units of one CTA of a persistent grouped GEMM: (item, K steps
+// [kb0, kb1)), in the order the CTA's roles take them.
+//   kWhole     whole items blockIdx.x, blockIdx.x + gridDim.x, ...
+//   kEqualK    every item's K range in ks equal parts, the (item, part) pairs
+//              dealt out the same way (part buffer slot = item * ks + part)
+//   kBalanced  the launch's n_items * k_all K steps cut into gridDim.x
+//              contiguous ranges of `per` steps, one per CTA: a unit is the
+//              overlap of the CTA's range with one item, so every CTA streams
+//              the same number of K steps whatever the item count.  The parts
+//              of an item are the ranges its steps fall in (at most
+//              kMaxGemmKSplit: per >= k_all / (kMaxGemmKSplit - 1)); only a
+//              CTA's first and last units can be parts, so CTA c keeps them in
+//              part buffer slots 2c and 2c + 1.
+// A unit with parts > 1 stores its accumulator in slot `slot`; the item's
+// arrival count lives at index slot0 (the slot of part 0).
+enum UnitMode { kWhole = 0, kEqualK = 1, kBalanced = 2 };
+
+struct WorkUnit {
+  int item, kb0, kb1;
+  int part, parts;
+  int slot, slot0;
+};
+
+struct UnitCursor {
+  int mode, k_all, ks, k_per, per, cta, stride;
+  long long pos, end;
+
+  __device__ __forceinline__ void init(int mode_, int n_items, int k_all_, int ks_) {
+    mode = mode_;
+    k_all = k_all_;
+    ks = mode == kEqualK ? ks_ : 1;
+    k_per = (k_all + ks - 1) / ks;
+    cta = static_cast<int>(blockIdx.x);
+    stride = static_cast<int>(gridDim.x);
+    per = 1;
+    if (mode == kBalanced) {
+      const long long S = static_cast<long long>(n_items) * k_all;
+      const long long even = (S + stride - 1) / stride;
+      const int floor_per = (k_all + kMaxGemmKSplit - 2) / (kMaxGemmKSplit - 1);
+      per = static_cast<int>(even > floor_per ? even : floor_per);
+      pos = min(S, static_cast<long long>(cta) * per);
+      end = min(S, static_cast<long long>(cta + 1) * per);
+    } else {
+      pos = cta;
+      end = static_cast<long long>(n_items) * ks;
+    }
+  }
+  // part buffer slot of CTA c's part of the item starting at K step i0
+  __device__ __forceinline__ int slot_of(long long i0, int c) const {
+    return 2 * c + (static_cast<long long>(c) * per < i0 ? 1 : 0);
+  }
+  __device__ __forceinline__ int part_slot(const WorkUnit& u, int p) const {
+    if (mode != kBalanced) return u.slot0 + p;
+    const long long i0 = static_cast<long long>(u.item) * k_all;
+    return slot_of(i0, static_cast<int>(i0 / per) + p);
+  }
+  __device__ __forceinline__ bool next(WorkUnit& u) {
+    if (pos >= end) return false;
+    if (mode == kBalanced) {
+      u.item = static_cast<int>(pos / k_all);
+      const long long i0 = static_cast<long long>(u.item) * k_all;
+      u.kb0 = static_cast<int>(pos - i0);
+      u.kb1 = static_cast<int>(min(static_cast<long long>(k_all), end - i0));
+      const int c0 = static_cast<int>(i0 / per), c1 = static_cast<int>((i0 + k_all - 1) / per);
+      u.parts = c1 - c0 + 1;
+      u.part = cta - c0;
+      u.slot = slot_of(i0, cta);
+      u.slot0 = slot_of(i0, c0);
+      pos = i0 + u.kb1;
+      return true;
+    }
+    const int idx = static_cast<int>(pos);
+    pos += stride;
+    u.item = idx / ks;
+    u.part = idx - u.item * ks;
+    u.parts = ks;
+    u.kb0 = u.part * k_per;
+    u.kb1 = min(k_all, u.kb0 + k_per);
+    u.slot = idx;
+    u.slot0 = u.item * ks;
+    return true;
+  }
+};
+
+// The parts of this thread's row of a unit's item (part p in slot
+// cur.part_slot(u, p)), summed in part order; every part's 16 columns are
+// loaded at once.
+template <int BN>
+__device__ __forceinline__ void ksplit_sum_units(const float* buf, const UnitCursor& cur, const WorkUnit& u, int row,
+                                                 int valid, float (&sum)[BN]) {
+  const float* src[kMaxGemmKSplit];
+#pragma unroll
+  for (int p = 0; p < kMaxGemmKSplit; ++p)
+    src[p] = buf + (static_cast<size_t>(cur.part_slot(u, p < u.parts ? p : 0)) * kBlockM + row) * BN;
+#pragma unroll
+  for (int c0 = 0; c0 < BN; c0 += 16) {
+    if (c0 >= valid) break;
+    float4 f[kMaxGemmKSplit][4];
+#pragma unroll
+    for (int p = 0; p < kMaxGemmKSplit; ++p)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        f[p][j] = p < u.parts ? __ldcg(reinterpret_cast<const float4*>(src[p] + c0 + 4 * j))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float4 a = f[0][j];
+#pragma unroll
+      for (int p = 1; p < kMaxGemmKSplit; ++p) {
+        a.x += f[p][j].x;
+        a.y += f[p][j].y;
+        a.z += f[p][j].z;
+        a.w += f[p][j].w;
+      }
+      sum[c0 + 4 * j] = a.x;
+      sum[c0 + 4 * j + 1] = a.y;
+      sum[c0 + 4 * j + 2] = a.z;
+      sum[c0 + 4 * j + 3] = a.w;
+    }
+  }
+}
+
 // K split (few work items: every item's K range in ks parts run as separate
 // items).  ksplit_store_part: this thread's accumulator row of one part (the
 // hi + lo sum when lo_off > 0) to the part buffer, the 16-column chunks that

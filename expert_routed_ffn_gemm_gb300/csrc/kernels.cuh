@@ -206,6 +206,11 @@ struct GemmArgs {
   // epilogue on the sum.  With more part items than ksplit_cap, or token tiles
   // wider than 32, the kernel runs unsplit.
   int ksplit;
+  // single-CTA bf16 kernel: with ksplit > 1 and kbalance = 1 the K steps of
+  // all items are instead cut into one contiguous range per CTA (an item's
+  // parts are the ranges its steps fall in, at most kMaxGemmKSplit; CTA c
+  // keeps its parts in slots 2c and 2c + 1 of the part buffer)
+  int kbalance;
   int ksplit_cap;      // part items ksplit_part and ksplit_cnt hold
   float* ksplit_part;  // [ksplit_cap][128][BN]
   int* ksplit_cnt;     // [ksplit_cap], zero between launches

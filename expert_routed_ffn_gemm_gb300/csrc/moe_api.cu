@@ -44,7 +44,8 @@ struct moe_handle {
   cudaStream_t side = nullptr;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   bool fp8_x2;      // FP8 weights: gate/up on E4M3 tensor cores with two-term token rows (MOE_FP8_X2=0: off)
-  int gemm_ksplit;  // K split of the bf16 expert GEMMs: -1 = by work items, 1 = off, 2..4 = forced
+  int gemm_ksplit;  // K split of the bf16 expert GEMMs: -1 = by work items, 0 = balanced ranges forced,
+                    // 1 = off, 2..4 = that many equal parts forced
   int ksplit_cap;   // work items (item, K part) the part buffer holds
   float* ksplit_part;  // [ksplit_cap][128][32] fp32 partial accumulators
   int* ksplit_cnt;     // [ksplit_cap] parts finished per item (zero between launches)
@@ -380,8 +381,12 @@ cudaEvent_t* prof_slot(moe_handle* h) {
 // x (K steps per part + a fixed cost per item worth kItemSteps K steps, which
 // covers the pipeline start and the part reduction); the split is taken when
 // it beats the unsplit estimate by 5 %.  Unforced, only K ranges of at least
-// kMinSplitSteps steps are cut (shorter ones gain too little).
-int choose_ksplit(const moe_handle* h, int bn, long long items_ub, int k_steps) {
+// kMinSplitSteps steps are cut (shorter ones gain too little).  The bf16
+// kernel (balanced != NULL) instead takes balanced ranges when they win: the
+// K steps of all items in one contiguous range per CTA, estimated as the
+// range's steps + kItemSteps per unit it runs; *balanced = 1 then.
+int choose_ksplit(const moe_handle* h, int bn, long long items_ub, int k_steps, int* balanced = nullptr) {
+  if (balanced != nullptr) *balanced = 0;
   if ((h->fp8 && !h->fp8_x2) || bn > 32 || h->gemm_ksplit == 1 || items_ub <= 0) return 1;
   constexpr int kMinSplitSteps = 32;
   const int sms = h->num_sms;
@@ -389,6 +394,11 @@ int choose_ksplit(const moe_handle* h, int bn, long long items_ub, int k_steps) 
     return (ks - 1) * ((k_steps + ks - 1) / ks) < k_steps && items_ub * ks <= h->ksplit_cap;
   };
   if (h->gemm_ksplit >= 2) return fits(h->gemm_ksplit) ? h->gemm_ksplit : 1;
+  if (h->gemm_ksplit == 0) {  // balanced ranges forced (bf16 kernel only)
+    if (balanced == nullptr || 2 * sms > h->ksplit_cap) return 1;
+    *balanced = 1;
+    return moe::kMaxGemmKSplit;
+  }
   // E4M3 items carry half the bytes of bf16 ones, so the fixed cost per part
   // outweighs the fuller last wave (T=1 gate/up: 31 us unsplit, 37 and 43 us
   // in 2 and 3 parts): split only when forced
@@ -398,6 +408,20 @@ int choose_ksplit(const moe_handle* h, int bn, long long items_ub, int k_steps) 
     return static_cast<double>((items_ub * ks + sms - 1) / sms) * (static_cast<double>(k_steps) / ks + kItemSteps);
   };
   const double base = cost(1);
+  if (balanced != nullptr && 2 * sms <= h->ksplit_cap) {
+    // one contiguous range of K steps per CTA: the most steps any CTA streams,
+    // plus the fixed cost of each unit it runs (its range starts and ends
+    // inside items)
+    const long long S = items_ub * k_steps;
+    const long long per = std::max<long long>((S + sms - 1) / sms, (k_steps + moe::kMaxGemmKSplit - 2) /
+                                                                       (moe::kMaxGemmKSplit - 1));
+    const double bal = static_cast<double>(per) + static_cast<double>((per + k_steps - 1) / k_steps + 1) * kItemSteps;
+    if (bal < 0.95 * base) {
+      *balanced = 1;
+      return moe::kMaxGemmKSplit;
+    }
+    return 1;
+  }
   int best = 1;
   double best_cost = base;
   for (int ks = 2; ks <= moe::kMaxGemmKSplit && fits(ks); ++ks) {
@@ -475,6 +499,7 @@ int enqueue_gateup(moe_handle* h, moe::GemmArgs a, double mean_rows, const CUten
   const int i1 = tile_index(p.bn1), i128 = tile_index(128);
   a.w_scale = h->s_gate_up;
   a.ksplit = 1;
+  a.kbalance = 0;
   if (h->fp8_x2) {
     a.tok_scale = h->tok_scale;
     a.lo_row0 = h->rows_max;
@@ -486,7 +511,10 @@ int enqueue_gateup(moe_handle* h, moe::GemmArgs a, double mean_rows, const CUten
   else if (p.pair1)
     MOE_CUDA(moe::launch_expert_gemm_pair(true, &h->map_wgu, &map_rows[i128], map_act2, a, h->num_sms, s));
   else {
-    a.ksplit = choose_ksplit(h, p.bn1, tiles_ub(a, p, p.bn1) * a.m_tiles, a.K / moe::kBlockK);
+    // the second stream's launches run beside the first's: no K split there
+    // (one part buffer)
+    if (s != h->side)
+      a.ksplit = choose_ksplit(h, p.bn1, tiles_ub(a, p, p.bn1) * a.m_tiles, a.K / moe::kBlockK, &a.kbalance);
     MOE_CUDA(moe::launch_expert_gemm(true, p.bn1, &h->map_wgu, &map_rows[i1], map_act2, a, h->num_sms, s));
   }
   MOE_MARK(4);
@@ -508,6 +536,7 @@ int enqueue_down(moe_handle* h, moe::GemmArgs a, double mean_rows, void* yout, i
   a.out_ld = c.d_model;
   a.w_scale = h->s_down;
   a.ksplit = 1;
+  a.kbalance = 0;
   const int i2 = tile_index(p.bn2), i128 = tile_index(128);
   if (h->fp8_x2) {
     // H in place as two-term E4M3 rows, their 1/s in tok_scale (gate/up has
@@ -523,7 +552,8 @@ int enqueue_down(moe_handle* h, moe::GemmArgs a, double mean_rows, void* yout, i
   else if (p.pair2)
     MOE_CUDA(moe::launch_expert_gemm_pair(false, &h->map_wd, &h->map_h[i128], nullptr, a, h->num_sms, s));
   else {
-    a.ksplit = choose_ksplit(h, p.bn2, tiles_ub(a, p, p.bn2) * a.m_tiles, a.K / moe::kBlockK);
+    if (s != h->side)
+      a.ksplit = choose_ksplit(h, p.bn2, tiles_ub(a, p, p.bn2) * a.m_tiles, a.K / moe::kBlockK, &a.kbalance);
     MOE_CUDA(moe::launch_expert_gemm(false, p.bn2, &h->map_wd, &h->map_h[i2], nullptr, a, h->num_sms, s));
   }
   MOE_MARK(5);
@@ -760,6 +790,7 @@ int init_any(const moe_config* cfg, const moe_weights* w, const float* s_gu, con
     const char* vk = std::getenv("MOE_GEMM_KSPLIT");
     const int ksv = vk ? std::atoi(vk) : -1;
     h->gemm_ksplit = (vk == nullptr || ksv < 0) ? -1 : (ksv <= 1 ? 1 : std::min(ksv, moe::kMaxGemmKSplit));
+    if (vk != nullptr && vk[0] == 'b') h->gemm_ksplit = 0;
     const int rt = tile_from_env("MOE_ROUTER_TILE");
     h->router_tile = (rt == 16 || rt == 64 || rt == 128 || rt == 256) ? rt : 0;
   }

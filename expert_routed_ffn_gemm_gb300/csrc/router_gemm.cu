@@ -346,7 +346,7 @@ template <int NS>
 __device__ __forceinline__ void finish_token(float (&q)[NS], int t, int lane, int E, int k, int renorm,
                                              int* __restrict__ idx, float* __restrict__ prob,
                                              float* __restrict__ gap, int* counts, float* __restrict__ tokstats,
-                                             int n_groups) {
+                                             int n_groups, int* sel = nullptr) {
   float zmax = -FLT_MAX;
 #pragma unroll
   for (int i = 0; i < NS; ++i)
@@ -424,6 +424,7 @@ __device__ __forceinline__ void finish_token(float (&q)[NS], int t, int lane, in
     idx[static_cast<size_t>(t) * k + lane] = my_e;
     prob[static_cast<size_t>(t) * k + lane] = renorm ? my_p / sel_sum : my_p;
     if (counts != nullptr) atomicAdd(&counts[my_e], 1);
+    if (sel != nullptr) sel[t * k + lane] = my_e;
   }
 }
 
@@ -606,10 +607,8 @@ __global__ void __launch_bounds__(kSmallRouteWarps * 32) route_small_kernel(
       const int ee = lane + 32 * i;
       q[i] = ee < E ? __ldcg(logits + static_cast<size_t>(t) * E + ee) : 0.f;
     }
-    finish_token<NS>(q, t, lane, E, k, renorm, idx, prob, gap, nullptr, nullptr, 0);
+    finish_token<NS>(q, t, lane, E, k, renorm, idx, prob, gap, nullptr, nullptr, 0, s_idx);
   }
-  __syncthreads();  // every token's idx written (and visible to the block)
-  for (int a = threadIdx.x; a < T * k; a += blockDim.x) s_idx[a] = __ldcg(idx + a);
   for (int i = threadIdx.x; i < E; i += blockDim.x) s_cnt[i] = 0;
   __syncthreads();
   // counts per expert (shared-memory integer atomics: order-independent)
@@ -669,14 +668,33 @@ __global__ void __launch_bounds__(kSmallRouteWarps * 32) route_small_kernel(
   }
   if (threadIdx.x == 0) *done = 0u;  // ready for the next launch
   if (ex.xp == nullptr) return;
-  // the routed rows in dispatch order, xp[pos(a)] = x[a / k], by this block
-  // (T * k rows of d bf16: 16-byte vectors, a warp per row)
+  // the routed rows in dispatch order, xp[pos(a)] = x[a / k], by this block:
+  // each thread loads kGatherVecs 16-byte vectors of every token's row at
+  // once, then stores each to the token's k positions
   __syncthreads();
+  constexpr int kGatherVecs = 4;
   const int n16 = d / 8;
-  for (int a = warp; a < T * k; a += kSmallRouteWarps) {
-    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(a / k) * d);
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<bf16*>(ex.xp) + static_cast<size_t>(s_cnt[a]) * d);
-    for (int c = lane; c < n16; c += 32) dst[c] = __ldg(src + c);
+  const uint4* xv = reinterpret_cast<const uint4*>(x);
+  uint4* xpv = reinterpret_cast<uint4*>(ex.xp);
+  for (int c0 = threadIdx.x; c0 < n16; c0 += kGatherVecs * blockDim.x) {
+    uint4 v[kGatherVecs][kSmallRouteMaxTokens];
+#pragma unroll
+    for (int u = 0; u < kGatherVecs; ++u) {
+      const int c = c0 + u * blockDim.x;
+#pragma unroll
+      for (int t = 0; t < kSmallRouteMaxTokens; ++t)
+        if (t < T && c < n16) v[u][t] = __ldg(xv + static_cast<size_t>(t) * n16 + c);
+    }
+#pragma unroll
+    for (int u = 0; u < kGatherVecs; ++u) {
+      const int c = c0 + u * blockDim.x;
+      if (c >= n16) break;
+#pragma unroll
+      for (int t = 0; t < kSmallRouteMaxTokens; ++t) {
+        if (t >= T) break;
+        for (int j = 0; j < k; ++j) xpv[static_cast<size_t>(s_cnt[t * k + j]) * n16 + c] = v[u][t];
+      }
+    }
   }
 }
 

@@ -64,6 +64,8 @@ def main():
         ("pairs over many tokens", lambda: case(S(T=5000, d=256, E=16, k=2, F=128), 5, n_sample=64)),
         ("K split in 3 parts", lambda: case(S(T=3, d=512, E=16, k=2, F=256), 6, tiles=(16, 32),
                                             env={"MOE_GEMM_KSPLIT": "3"})),
+        ("K split in balanced ranges", lambda: case(S(T=5, d=1024, E=16, k=2, F=384), 8, tiles=(32, 32),
+                                                    env={"MOE_GEMM_KSPLIT": "b"})),
         ("FP8 two-term rows", lambda: case(S(T=600, d=512, E=24, k=2, F=256), 7, fp8=True, n_sample=64)),
     ]
     for name, run in cases:

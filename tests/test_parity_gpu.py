@@ -127,12 +127,15 @@ def test_chunked_dispatch_ties_and_one_hot():
     run_and_check(inp, tokens=64)
 
 
-@pytest.mark.parametrize("parts", ["2", "3", "4", "auto"])
+@pytest.mark.parametrize("parts", ["2", "3", "4", "b", "auto"])
 @pytest.mark.parametrize("T,d,F,tiles", [(1, 256, 128, (32, 32)), (3, 512, 256, (16, 32)),
-                                         (20, 512, 256, (16, 16)), (7, 256, 128, (32, 16))])
+                                         (20, 512, 256, (16, 16)), (7, 256, 128, (32, 16)),
+                                         (5, 1024, 384, (32, 32)), (2, 4096, 128, (16, 16))])
 def test_gemm_k_split(parts, T, d, F, tiles):
     # Few work items: every item's K range in 2..4 parts (fewer where K has
-    # fewer steps of 64), summed in part order by the last part to finish.
+    # fewer steps of 64), summed in part order by the last part to finish;
+    # "b": the K steps of all items in one contiguous range per CTA (an
+    # item's parts are the ranges it spans, 1..4 of them).
     shape = synth.LayerShape(T=T, d=d, E=16, k=2, F=F)
     inp = synth.make_inputs(shape, seed=70 + T + d // 128)
     env = {} if parts == "auto" else {"MOE_GEMM_KSPLIT": parts}
