@@ -573,6 +573,13 @@ int enqueue_ffn(moe_handle* h, moe::GemmArgs a, double mean_rows, const CUtensor
   return enqueue_down(h, a, mean_rows, yout, yexp, ev, s, n_rows);
 }
 
+// The shared expert may run on the second stream: bf16 weights and its
+// launches on CTA pairs (they take its rows from the host, not the offsets).
+bool shared_overlap_ok(const moe_handle* h) {
+  return h->shared_overlap && h->use_pairs && !h->fp8 && (h->tile_gateup == 0 || h->tile_gateup == 256) &&
+         (h->tile_down == 0 || h->tile_down == 256);
+}
+
 // The shared expert's FFN on the handle's second stream: it needs x alone,
 // so it runs on CTA pairs beside the routing's later kernels, the dispatch
 // and the row copy (which use few tensor cores): gate/up into rows
@@ -608,8 +615,7 @@ int enqueue_forward(moe_handle* h, const void* x, int T, CallOpts o, void* y, cu
   cudaEvent_t* ev = prof_slot(h);
   MOE_MARK(0);
   const bool fused_route = small_route(h, T);
-  const bool overlap_shared = h->shared_overlap && h->use_pairs && !h->fp8 && c.has_shared && !fused_route &&
-                              T >= kSharedOverlapMinTokens;
+  const bool overlap_shared = shared_overlap_ok(h) && c.has_shared && !fused_route && T >= kSharedOverlapMinTokens;
   // with one or two tokens (bf16 weights) that launch also copies the routed
   // rows into dispatch order (a handful of rows: one block is enough)
   const bool fused_gather = fused_route && !h->fp8 && T <= kFusedGatherMaxTokens;
@@ -938,8 +944,7 @@ int moe_ep_dispatch(moe_handle* h, const void* x, int T, void* send_rows, float*
   // the routing and dispatch of the whole-layer call on the same tokens (so
   // that both give the same rows and weights)
   const bool fused_route = small_route(h, T);
-  const bool overlap_shared = h->shared_overlap && h->use_pairs && !h->fp8 && c.has_shared && !fused_route &&
-                              T >= kSharedOverlapMinTokens;
+  const bool overlap_shared = shared_overlap_ok(h) && c.has_shared && !fused_route && T >= kSharedOverlapMinTokens;
   if (fused_route) {
     MOE_CUDA(moe::launch_route_small(static_cast<const bf16*>(x), h->w.w_router, T, c.d_model, E, k, 0, c.has_shared,
                                      h->partial, h->route_done, h->idx, h->prob, nullptr, h->counts, h->offsets,

@@ -542,18 +542,6 @@ __global__ void __launch_bounds__(kSmallRouteWarps * 32) route_small_kernel(
     float* __restrict__ gap, int* __restrict__ counts, int* __restrict__ offsets, int* __restrict__ perm,
     int* __restrict__ inv, int* __restrict__ chunk_base, SmallRouteExtras ex) {
   pdl_trigger();
-  // weights every call reads whatever the routing (the shared expert's),
-  // into L2 while the routing runs: chunks of kPrefetchChunk bytes, block b
-  // taking chunks b, b + gridDim.x, ...
-  if (threadIdx.x == 0) {
-    for (int r = 0; r < 2; ++r) {
-      const char* base = static_cast<const char*>(r == 0 ? ex.pf0 : ex.pf1);
-      const long long n = r == 0 ? ex.pf0_bytes : ex.pf1_bytes;
-      for (long long o = static_cast<long long>(blockIdx.x) * kPrefetchChunk; o < n;
-           o += static_cast<long long>(gridDim.x) * kPrefetchChunk)
-        l2_prefetch_bulk(base + o, static_cast<uint32_t>(n - o < kPrefetchChunk ? n - o : kPrefetchChunk));
-    }
-  }
   __shared__ int s_last;
   __shared__ int s_scan[kSmallRouteWarps];
   __shared__ float s_part[kSmallRouteWarps][kSmallRouteMaxTokens];
@@ -589,6 +577,13 @@ __global__ void __launch_bounds__(kSmallRouteWarps * 32) route_small_kernel(
       if (lane == 0) s_part[warp][t] = acc[t];
     }
   }
+  // One token: its k routed rows are k copies of it at dispatch positions
+  // 0..k-1 whatever the experts, so blocks 0..k-1 copy them now
+  if (ex.xp != nullptr && T == 1 && e < k) {
+    const uint4* src = reinterpret_cast<const uint4*>(x);
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<bf16*>(ex.xp) + static_cast<size_t>(e) * d);
+    for (int c = threadIdx.x; c < d / 8; c += blockDim.x) dst[c] = __ldg(src + c);
+  }
   __syncthreads();
   if (threadIdx.x < T)
     logits[static_cast<size_t>(threadIdx.x) * E + e] =
@@ -596,7 +591,20 @@ __global__ void __launch_bounds__(kSmallRouteWarps * 32) route_small_kernel(
   // the block that finishes last sees every logit
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(done, 1u) == gridDim.x - 1;
+  if (threadIdx.x == 0) {
+    s_last = atomicAdd(done, 1u) == gridDim.x - 1;
+    // weights every call reads whatever the routing (the shared expert's),
+    // into L2 while the routing finishes — after this block's loads of W_r,
+    // which they would otherwise delay: chunks of kPrefetchChunk bytes, block
+    // b taking chunks b, b + gridDim.x, ...
+    for (int r = 0; r < 2; ++r) {
+      const char* base = static_cast<const char*>(r == 0 ? ex.pf0 : ex.pf1);
+      const long long n = r == 0 ? ex.pf0_bytes : ex.pf1_bytes;
+      for (long long o = static_cast<long long>(blockIdx.x) * kPrefetchChunk; o < n;
+           o += static_cast<long long>(gridDim.x) * kPrefetchChunk)
+        l2_prefetch_bulk(base + o, static_cast<uint32_t>(n - o < kPrefetchChunk ? n - o : kPrefetchChunk));
+    }
+  }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
@@ -667,7 +675,7 @@ __global__ void __launch_bounds__(kSmallRouteWarps * 32) route_small_kernel(
     s_cnt[a] = pos;  // the counts are written: the positions of the row copy below
   }
   if (threadIdx.x == 0) *done = 0u;  // ready for the next launch
-  if (ex.xp == nullptr) return;
+  if (ex.xp == nullptr || T == 1) return;
   // the routed rows in dispatch order, xp[pos(a)] = x[a / k], by this block:
   // each thread loads kGatherVecs 16-byte vectors of every token's row at
   // once, then stores each to the token's k positions

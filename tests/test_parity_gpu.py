@@ -404,19 +404,22 @@ def test_few_token_routing_both_paths(fused, T, d, E, k):
     layer.close()
 
 
+@pytest.mark.parametrize("tiles", [(0, 0), (128, 128)])
 @pytest.mark.parametrize("overlap", ["1", "0"])
-def test_shared_expert_on_a_second_stream(overlap):
+def test_shared_expert_on_a_second_stream(overlap, tiles):
     # From 2048 tokens on the shared expert's gate/up runs on a second stream
     # beside the dispatch and row scatter (MOE_SHARED_OVERLAP=0: in the one
     # gate/up launch): same results bit for bit, against the oracle, and the
     # fork and join capture into a CUDA graph whose replays match the eager call.
+    # tiles (128, 128): single-CTA token tiles forced, the shared expert stays
+    # in the routed launches either way.
     shape = synth.LayerShape(T=2500, d=256, E=16, k=2, F=128)
     inp = synth.make_inputs(shape, seed=501)
-    layer, x = make_layer(inp, env={"MOE_SHARED_OVERLAP": overlap})
+    layer, x = make_layer(inp, tiles=tiles, env={"MOE_SHARED_OVERLAP": overlap})
     y = layer.forward(x)
     assert layer.check() == binding.MOE_OK
-    assert layer.last_kernel_count() == (11 if overlap == "1" else 9)
-    other, _ = make_layer(inp, env={"MOE_SHARED_OVERLAP": "0" if overlap == "1" else "1"})
+    assert layer.last_kernel_count() == (11 if overlap == "1" and tiles == (0, 0) else 9)
+    other, _ = make_layer(inp, tiles=tiles, env={"MOE_SHARED_OVERLAP": "0" if overlap == "1" else "1"})
     assert torch.equal(y, other.forward(x))
     other.close()
     idx, prob, perm, offsets, gap = layer.route(x)
