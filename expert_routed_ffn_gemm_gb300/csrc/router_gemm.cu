@@ -528,10 +528,12 @@ __global__ void __launch_bounds__(kTopkTokensPerBlock * 32) router_topk_warp_ker
 // together), the lanes' sums meet in a fixed xor-butterfly and the four
 // warps' sums are added in warp order.  The block that finishes last (an
 // integer arrival count, reset for the next launch) ranks every token with
-// finish_token and lays the rows out: counts, offsets and chunk bases by a
-// block scan over the experts, and each assignment a = t*k + j at
-// offsets[e] + the number of earlier tokens that chose e (the stable expert,
-// token order of dispatch_kernel).  Every result is a function of x and W_r
+// finish_token and lays the rows out: counts, offsets and chunk bases as
+// counts over the T*k picks, and each assignment a = t*k + j at offsets[e] +
+// the number of earlier tokens that chose e (the stable expert, token order
+// of dispatch_kernel).  With one token its k rows are copies of it whatever
+// the experts, so blocks 0..k-1 copy them beside their dot products; with
+// two the last block copies them.  Every result is a function of x and W_r
 // alone (fixed summation orders): bit-identical run to run.
 constexpr int kSmallRouteWarps = 4;
 
@@ -543,10 +545,9 @@ __global__ void __launch_bounds__(kSmallRouteWarps * 32) route_small_kernel(
     int* __restrict__ inv, int* __restrict__ chunk_base, SmallRouteExtras ex) {
   pdl_trigger();
   __shared__ int s_last;
-  __shared__ int s_scan[kSmallRouteWarps];
   __shared__ float s_part[kSmallRouteWarps][kSmallRouteMaxTokens];
-  __shared__ int s_cnt[kMaxExperts], s_off[kMaxExperts];
-  __shared__ int s_idx[kSmallRouteMaxTokens * kMaxTopK];
+  __shared__ int s_idx[kSmallRouteMaxTokens * kMaxTopK], s_first[kSmallRouteMaxTokens * kMaxTopK],
+      s_pos[kSmallRouteMaxTokens * kMaxTopK];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   pdl_wait();  // x, and the routing buffers read by earlier work in the stream
   const int e = blockIdx.x;
@@ -588,11 +589,14 @@ __global__ void __launch_bounds__(kSmallRouteWarps * 32) route_small_kernel(
   if (threadIdx.x < T)
     logits[static_cast<size_t>(threadIdx.x) * E + e] =
         ((s_part[0][threadIdx.x] + s_part[1][threadIdx.x]) + s_part[2][threadIdx.x]) + s_part[3][threadIdx.x];
-  // the block that finishes last sees every logit
-  __threadfence();
+  // the block that finishes last sees every logit (the barrier orders this
+  // block's logit stores before thread 0's release fence and count)
   __syncthreads();
   if (threadIdx.x == 0) {
-    s_last = atomicAdd(done, 1u) == gridDim.x - 1;
+    __threadfence();
+    const bool last = atomicAdd(done, 1u) == gridDim.x - 1;
+    if (last) __threadfence();  // acquire: every block's logits are visible
+    s_last = last;
     // weights every call reads whatever the routing (the shared expert's),
     // into L2 while the routing finishes — after this block's loads of W_r,
     // which they would otherwise delay: chunks of kPrefetchChunk bytes, block
@@ -607,7 +611,6 @@ __global__ void __launch_bounds__(kSmallRouteWarps * 32) route_small_kernel(
   }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
   for (int t = warp; t < T; t += kSmallRouteWarps) {
     float q[NS];
 #pragma unroll
@@ -617,62 +620,47 @@ __global__ void __launch_bounds__(kSmallRouteWarps * 32) route_small_kernel(
     }
     finish_token<NS>(q, t, lane, E, k, renorm, idx, prob, gap, nullptr, nullptr, 0, s_idx);
   }
-  for (int i = threadIdx.x; i < E; i += blockDim.x) s_cnt[i] = 0;
-  __syncthreads();
-  // counts per expert (shared-memory integer atomics: order-independent)
-  for (int a = threadIdx.x; a < T * k; a += blockDim.x) atomicAdd(&s_cnt[s_idx[a]], 1);
-  __syncthreads();
-  // offsets and chunk bases: each thread scans a contiguous run of experts
-  const int per = (E + blockDim.x - 1) / blockDim.x;
-  const int b0 = threadIdx.x * per, b1 = min(E, b0 + per);
-  for (int pass = 0; pass < 2; ++pass) {
-    int local = 0;
-    for (int i = b0; i < b1; ++i) local += pass == 0 ? s_cnt[i] : (s_cnt[i] + kYpRows - 1) / kYpRows;
-    int incl = local;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += o;
-    }
-    if (lane == 31) s_scan[warp] = incl;
-    __syncthreads();
-    int run = incl - local, total = 0;
-    for (int w = 0; w < kSmallRouteWarps; ++w) {
-      run += w < warp ? s_scan[w] : 0;
-      total += s_scan[w];
-    }
-    for (int i = b0; i < b1; ++i) {
-      if (pass == 0) {
-        offsets[i] = run;
-        s_off[i] = run;
-        counts[i] = s_cnt[i];
-        run += s_cnt[i];
-      } else {
-        chunk_base[i] = run;
-        run += (s_cnt[i] + kYpRows - 1) / kYpRows;
-      }
-    }
-    if (threadIdx.x == 0) {
-      if (pass == 0) {
-        offsets[E] = total;
-        offsets[E + 1] = total + (has_shared ? T : 0);
-      } else {
-        chunk_base[E] = shared_chunk0(T, k, E);  // the routed chunks end at total <= this
-        chunk_base[E + 1] = chunk_base[E] + (has_shared ? (T + kYpRows - 1) / kYpRows : 0);
-      }
-    }
-    __syncthreads();
+  // The dispatch of the T * k picks.  With T <= kSmallRouteMaxTokens < 16
+  // rows an expert's group takes exactly one exponent chunk when it has rows,
+  // so every value is a count over the picks: offsets[e] = picks of experts
+  // below e, chunk_base[e] = experts below e with a pick, and pick a = t*k + j
+  // goes to offsets[e] + the earlier picks of its expert (the expert, token
+  // order of dispatch_kernel; a token picks an expert at most once).
+  static_assert(kSmallRouteMaxTokens < kYpRows, "one exponent chunk per group");
+  const int Tk = T * k;
+  __syncthreads();  // every pick in s_idx
+  for (int a = threadIdx.x; a < Tk; a += blockDim.x) {
+    const int e2 = s_idx[a];
+    int first = 1;
+    for (int a2 = 0; a2 < a; ++a2) first &= s_idx[a2] != e2;
+    s_first[a] = first;
   }
-  // assignment a = t*k + j of expert e2: after the rows of the earlier tokens
-  // that chose e2 (a token chooses an expert at most once)
-  for (int a = threadIdx.x; a < T * k; a += blockDim.x) {
-    const int t = a / k, e2 = s_idx[a];
-    int rank = 0;
-    for (int a2 = 0; a2 < t * k; ++a2) rank += s_idx[a2] == e2;
-    const int pos = s_off[e2] + rank;
+  __syncthreads();
+  for (int e2 = threadIdx.x; e2 < E; e2 += blockDim.x) {
+    int below = 0, cnt = 0, groups = 0;
+    for (int a = 0; a < Tk; ++a) {
+      const int v = s_idx[a];
+      below += v < e2;
+      cnt += v == e2;
+      groups += (v < e2) & s_first[a];
+    }
+    offsets[e2] = below;
+    counts[e2] = cnt;
+    chunk_base[e2] = groups;
+  }
+  if (threadIdx.x == 0) {
+    offsets[E] = Tk;
+    offsets[E + 1] = Tk + (has_shared ? T : 0);
+    chunk_base[E] = shared_chunk0(T, k, E);  // the routed chunks end at <= Tk <= this
+    chunk_base[E + 1] = chunk_base[E] + (has_shared ? (T + kYpRows - 1) / kYpRows : 0);
+  }
+  for (int a = threadIdx.x; a < Tk; a += blockDim.x) {
+    const int e2 = s_idx[a];
+    int pos = 0;
+    for (int a2 = 0; a2 < Tk; ++a2) pos += (s_idx[a2] < e2) | ((a2 < a) & (s_idx[a2] == e2));
     perm[pos] = a;
     inv[a] = pos;
-    s_cnt[a] = pos;  // the counts are written: the positions of the row copy below
+    s_pos[a] = pos;  // the positions of the row copy below
   }
   if (threadIdx.x == 0) *done = 0u;  // ready for the next launch
   if (ex.xp == nullptr || T == 1) return;
@@ -700,7 +688,7 @@ __global__ void __launch_bounds__(kSmallRouteWarps * 32) route_small_kernel(
 #pragma unroll
       for (int t = 0; t < kSmallRouteMaxTokens; ++t) {
         if (t >= T) break;
-        for (int j = 0; j < k; ++j) xpv[static_cast<size_t>(s_cnt[t * k + j]) * n16 + c] = v[u][t];
+        for (int j = 0; j < k; ++j) xpv[static_cast<size_t>(s_pos[t * k + j]) * n16 + c] = v[u][t];
       }
     }
   }
