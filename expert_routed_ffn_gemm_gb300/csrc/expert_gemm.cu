@@ -266,10 +266,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       // K4: the gate weight of every column, loaded while the MMAs still run
       float wreg[(BN + 31) / 32];
       if (!GATEUP) load_gate_weights<BN>(wreg, row0, valid, lane, args.perm, args.prob, args.Tk);
-      if (!epilogue_wait(&acc_full[acc], acc_phase, limit, abort_flag, s_ok, it_par, q, lane, args.err)) break;
+      // a part of a split item: if every other part is already stored (the
+      // count, read before the wait, says so) this one is the last, and sums
+      // the parts straight from tensor memory
+      int others_done = 0;
+      if (u.parts > 1 && q == 0 && lane == 0)
+        others_done = ld_acquire_gpu(args.ksplit_cnt + u.slot0) == u.parts - 1;
+      int fast = 0;
+      if (!epilogue_wait(&acc_full[acc], acc_phase, limit, abort_flag, s_ok, it_par, q, lane, args.err, others_done,
+                         &fast))
+        break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       if constexpr (BN <= 32) {
+        if (u.parts > 1 && fast) {
+          float sum[BN];
+          ksplit_sum_units_own<BN>(args.ksplit_part, cur, u, row, valid, taddr, sum);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[acc]);
+          if (++acc == C::NACC) {
+            acc = 0;
+            acc_phase ^= 1u;
+          }
+          if (GATEUP)
+            epilogue_gateup<BN>(0u, row, it.m * (kBlockM / 2), row0, valid, static_cast<bf16*>(args.out),
+                                args.out_ld, xchg, chunk_par, 1.0f, sum);
+          else
+            epilogue_down<BN>(0u, it.m * kBlockM + row, row0, valid, wreg, static_cast<__half*>(args.out),
+                              args.out_exp, args.out_ld, chunk0, 1.0f, 0, sum);
+          if (q == 0 && lane == 0) args.ksplit_cnt[u.slot0] = 0;  // ready for the next launch
+          continue;
+        }
         if (u.parts > 1) {
           // this part's accumulator row to the part buffer, tensor memory back
           // to the MMA, then the last part of the item sums the parts in order

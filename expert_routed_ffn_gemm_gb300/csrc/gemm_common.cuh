@@ -150,13 +150,16 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
 // The epilogue warps' common wait on an accumulator: every warp waits, then
 // all four take one decision (they meet at named barriers afterwards).
 // s_ok is [2][4] ints, it_par alternates per item.  Returns false to abort.
+// flag (or NULL): a yes/no of lane 0 of epilogue warp 0 (its `mine`), handed
+// to all four warps through the same barrier.
 __device__ __forceinline__ bool epilogue_wait(uint64_t* acc_full, uint32_t parity, uint64_t limit,
                                               volatile int* abort_flag, volatile int* s_ok, uint32_t& it_par,
-                                              int q, int lane, uint32_t* err) {
+                                              int q, int lane, uint32_t* err, int mine = 0, int* flag = nullptr) {
   const bool ok = __all_sync(0xffffffffu, wait_or_abort(acc_full, parity, limit, abort_flag));
-  if (lane == 0) s_ok[it_par * 4 + q] = ok ? 1 : 0;
+  if (lane == 0) s_ok[it_par * 4 + q] = ok ? 1 + (q == 0 ? mine : 0) : 0;
   named_bar_sync(kEpilogueBar, 128);
   const bool all_ok = s_ok[it_par * 4 + 0] && s_ok[it_par * 4 + 1] && s_ok[it_par * 4 + 2] && s_ok[it_par * 4 + 3];
+  if (flag != nullptr) *flag = s_ok[it_par * 4 + 0] == 2;
   it_par ^= 1u;
   if (!all_ok && lane == 0 && !ok) record_abort(abort_flag, err);
   return all_ok;
@@ -323,6 +326,55 @@ __device__ __forceinline__ void ksplit_sum_units(const float* buf, const UnitCur
       for (int j = 0; j < 4; ++j)
         f[p][j] = p < u.parts ? __ldcg(reinterpret_cast<const float4*>(src[p] + c0 + 4 * j))
                               : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float4 a = f[0][j];
+#pragma unroll
+      for (int p = 1; p < kMaxGemmKSplit; ++p) {
+        a.x += f[p][j].x;
+        a.y += f[p][j].y;
+        a.z += f[p][j].z;
+        a.w += f[p][j].w;
+      }
+      sum[c0 + 4 * j] = a.x;
+      sum[c0 + 4 * j + 1] = a.y;
+      sum[c0 + 4 * j + 2] = a.z;
+      sum[c0 + 4 * j + 3] = a.w;
+    }
+  }
+}
+
+// The same sum for the one part still in tensor memory (this thread's
+// accumulator row at taddr, part u.part) when every other part is stored:
+// the same values in the same order as ksplit_sum_units after storing it.
+template <int BN>
+__device__ __forceinline__ void ksplit_sum_units_own(const float* buf, const UnitCursor& cur, const WorkUnit& u,
+                                                     int row, int valid, uint32_t taddr, float (&sum)[BN]) {
+  const float* src[kMaxGemmKSplit];
+#pragma unroll
+  for (int p = 0; p < kMaxGemmKSplit; ++p)
+    src[p] = buf + (static_cast<size_t>(cur.part_slot(u, p < u.parts ? p : 0)) * kBlockM + row) * BN;
+#pragma unroll
+  for (int c0 = 0; c0 < BN; c0 += 16) {
+    if (c0 >= valid) break;
+    uint32_t own[16];
+    tmem_ld16(taddr + c0, own);
+    float4 f[kMaxGemmKSplit][4];
+#pragma unroll
+    for (int p = 0; p < kMaxGemmKSplit; ++p)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        f[p][j] = (p < u.parts && p != u.part)
+                      ? __ldcg(reinterpret_cast<const float4*>(src[p] + c0 + 4 * j))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    tmem_ld_wait_regs(own);
+#pragma unroll
+    for (int p = 0; p < kMaxGemmKSplit; ++p)
+      if (p == u.part)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          f[p][j] = make_float4(__uint_as_float(own[4 * j]), __uint_as_float(own[4 * j + 1]),
+                                __uint_as_float(own[4 * j + 2]), __uint_as_float(own[4 * j + 3]));
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       float4 a = f[0][j];
