@@ -251,10 +251,11 @@ def measured_traffic(workload_name: str, weights: str, shape, gu_alg_bytes: floa
     """DRAM bytes per launch of the gate/up GEMM from the committed ncu
     captures (profiles/traffic.json): (bytes or None, source note).  An entry
     whose kernel sources have changed since the capture gives None.  Each
-    entry was captured on a smaller case of the same kernel and carries the
-    ratio of its traffic to its algorithmic bytes without the shared expert's
-    weights (the routing kernels prefetch those into L2); the figure is that
-    ratio times this workload's algorithmic bytes without them."""
+    entry was captured on a smaller case of the same kernel, with L2 emptied
+    before the kernel, and carries the ratio of its traffic to its
+    algorithmic bytes; in a layer call the routing kernels have already
+    brought the shared expert's weights into L2, so the figure is that ratio
+    times this workload's algorithmic bytes without them."""
     try:
         with open(TRAFFIC_FILE) as f:
             entries = json.load(f)["entries"]
@@ -271,9 +272,9 @@ def measured_traffic(workload_name: str, weights: str, shape, gu_alg_bytes: floa
             return None, "kernel sources missing"
         if digest != e.get("sources_sha256_16"):
             return None, f"stale: the kernel changed since the capture ({e['capture']})"
-        if e.get("traffic_over_algorithmic_without_shared") is not None:
+        if e.get("traffic_over_algorithmic") is not None:
             shared = shared_weight_bytes(shape, weights == "fp8") if shape.has_shared else 0
-            return float(e["traffic_over_algorithmic_without_shared"]) * (gu_alg_bytes - shared), e["capture"]
+            return float(e["traffic_over_algorithmic"]) * (gu_alg_bytes - shared), e["capture"]
     return None, "no capture of this workload"
 
 
