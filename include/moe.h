@@ -236,7 +236,8 @@ int moe_route(moe_handle* h, const void* x, int T, int* idx, float* prob, int* p
  * summed in slot order then the shared expert, in fp32, without atomics
  * (bit-identical run to run).  With few tokens the bf16 expert GEMMs may cut
  * K into parts (MOE_GEMM_KSPLIT in the environment: 1 = never, 2..4 = that
- * many); the parts are summed in a fixed order, so this holds there too.
+ * many per work item, b = equal contiguous ranges of K steps per CTA); the
+ * parts are summed in a fixed order, so this holds there too.
  *   x  bf16 [T][d], device;  y  [T][d] bf16 or fp32 (cfg.out_fp32), device.
  * 0 <= T <= max_tokens; T == 0 enqueues nothing.
  */
