@@ -321,8 +321,10 @@ def test_flash_skewed_sampled(flash_weights, out_fp32):
     flash_case(flash_weights, 4096, seed=102, n_sample=64, skew="zipf", out_fp32=out_fp32)
 
 
-@pytest.mark.parametrize("T", [1, 8, 32, 512, 2048])
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 8, 32, 512, 2048])
 def test_flash_sweep_points(flash_weights, T):
+    # 1 to 3 tokens: balanced K ranges in the gate/up GEMM; 1 to 4: the
+    # few-token routing launch (with one or two tokens also the row copy)
     flash_case(flash_weights, T, seed=200 + T, n_sample=None if T <= 32 else 64)
 
 
