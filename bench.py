@@ -86,8 +86,10 @@ class ClockSampler:
     background nvidia-smi whose lines a reader thread timestamps.  Entering
     waits (up to 5 s) for the first sample, so the sampler is running before
     the timed region starts; mark_start() / mark_end() bracket the timed
-    region, and summary() keeps the samples taken inside it (plus the first
-    one after it, which covers its last interval)."""
+    region, and summary() keeps the samples taken inside it plus the first
+    one after it, which covers its last interval: its throttle reasons count,
+    but its clock only when the region holds no sample (the GPU idles while
+    the sampler stops, so that sample's clock can be an idle one)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -140,12 +142,13 @@ class ClockSampler:
                 self._reader.join(timeout=5)
 
     def window(self):
-        """The sampled lines of the timed region (all lines if it was not marked)."""
+        """The timed region's sampled lines as (line, its clock counts) pairs
+        (every line, counted, if the region was not marked)."""
         if self.t0 is None or self.t1 is None:
-            return [l for _, l in self.lines]
+            return [(l, True) for _, l in self.lines]
         inside = [l for t, l in self.lines if self.t0 <= t <= self.t1]
-        after = [l for t, l in self.lines if t > self.t1]
-        return inside + after[:1]
+        after = [l for t, l in self.lines if t > self.t1][:1]
+        return [(l, True) for l in inside] + [(l, not inside) for l in after]
 
     def summary(self):
         lines = self.window()
@@ -153,15 +156,16 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
         sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in lines:
+        for line, clock_counts in lines:
             f = [v.strip() for v in line.split(",")]
             if len(f) < 9:
                 continue
             try:
-                sm.append(float(f[1]))
-                smax = float(f[2])
+                clock, smax = float(f[1]), float(f[2])
             except ValueError:
                 continue
+            if clock_counts:
+                sm.append(clock)
             for n, v in zip(names, f[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)

@@ -80,20 +80,25 @@ def test_workloads_resolve():
 
 
 def test_clock_window_and_summary():
-    # Samples before the timed region are dropped, the first one after it is
-    # kept; throttle reasons are collected and the median taken under load.
+    # Samples before the timed region are dropped; the first one after it
+    # adds its throttle reasons, and its clock only when the region holds no
+    # sample; the median is taken under load.
     clk = bench.ClockSampler(0)
-    row = "0, {sm}, 2070, 900.0, 0x0, Not Active, Not Active, {thermal}, Active"
-    clk.lines = [(0.9, row.format(sm=345, thermal="Not Active")),
-                 (1.01, row.format(sm=2070, thermal="Not Active")),
-                 (1.03, row.format(sm=2055, thermal="Active")),
-                 (1.05, row.format(sm=2070, thermal="Not Active")),
-                 (1.07, row.format(sm=1000, thermal="Not Active"))]
+    row = "0, {sm}, 2070, 900.0, 0x0, {hw}, Not Active, {thermal}, Active"
+    clk.lines = [(0.9, row.format(sm=345, hw="Not Active", thermal="Not Active")),
+                 (1.01, row.format(sm=2070, hw="Not Active", thermal="Not Active")),
+                 (1.02, row.format(sm=2070, hw="Not Active", thermal="Not Active")),
+                 (1.03, row.format(sm=2055, hw="Not Active", thermal="Active")),
+                 (1.05, row.format(sm=1500, hw="Active", thermal="Not Active")),
+                 (1.07, row.format(sm=1000, hw="Not Active", thermal="Not Active"))]
     clk.t0, clk.t1 = 1.0, 1.04
     s = clk.summary()
     assert s["samples"] == 3
     assert s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0
-    assert s["reasons"] == ["sw_power_cap", "sw_thermal_slowdown"]
+    assert s["reasons"] == ["hw_slowdown", "sw_power_cap", "sw_thermal_slowdown"]
+    clk.t0, clk.t1 = 1.035, 1.04  # no sample inside: the one after it
+    s = clk.summary()
+    assert s["samples"] == 1 and s["sm_mhz"] == 1500.0
     clk.t0 = clk.t1 = None  # unmarked: every sample
-    assert clk.summary()["samples"] == 5
+    assert clk.summary()["samples"] == 6
     assert bench.ClockSampler(0).summary()["reasons"] == ["unsampled"]
