@@ -438,7 +438,6 @@ __global__ void __launch_bounds__(1024, 1) combine_kernel(const __half* __restri
                                                           int d, int has_shared, void* __restrict__ y,
                                                           int out_fp32) {
   pdl_trigger();
-  pdl_wait();
   const int t = blockIdx.x;
   __shared__ int pos[kMaxTopK + 1];
   __shared__ int chunk[kMaxTopK + 1];
@@ -457,6 +456,7 @@ __global__ void __launch_bounds__(1024, 1) combine_kernel(const __half* __restri
     chunk[j] = ch;
   }
   __syncthreads();
+  pdl_wait();  // the expert outputs from here on (the routing results above are older, as in combine_nt_kernel)
   const int nterms = k + (has_shared ? 1 : 0);
   // routed rows (slots j < k) from yp_routed / yexp_routed when given
   // (expert parallelism: the rows the experts' owners sent back)
@@ -541,7 +541,6 @@ __global__ void __launch_bounds__(512, 2) combine_nt_kernel(const __half* __rest
                                                             const int* __restrict__ chunk_base, int T, int k, int E,
                                                             int d, void* __restrict__ y, int out_fp32) {
   pdl_trigger();
-  pdl_wait();
   constexpr int B1 = (NT + 1) / 2;
   const int t = blockIdx.x;
   __shared__ const uint4* rows[NT];
@@ -564,6 +563,11 @@ __global__ void __launch_bounds__(512, 2) combine_nt_kernel(const __half* __rest
     exps[j] = reinterpret_cast<const uint2*>(ebuf + static_cast<size_t>(ch) * d);
   }
   __syncthreads();
+  // Only now the expert outputs.  The routing and dispatch results read
+  // above are older: the kernel before this one (the down GEMM) starts its
+  // dependents only at its end, after its own wait for the gate/up, which
+  // waited for the kernels that wrote them.
+  pdl_wait();
   for (int c = threadIdx.x; c < d / 8; c += blockDim.x) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     {

@@ -17,8 +17,10 @@ namespace moe {
 // reads or writes (it returns once those grids have completed and their
 // writes are visible) and pdl_trigger() once the next kernel may be placed:
 // short kernels on entry, the persistent GEMMs at their end (without the
-// launch attribute both are no-ops).  MOE_PDL=0 in the environment turns the
-// attribute off.
+// launch attribute both are no-ops).  One exception: the combine reads the
+// routing and dispatch results before its wait, since the down GEMM before
+// it triggers only at its end, when everything older has completed.
+// MOE_PDL=0 in the environment turns the attribute off.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 bool pdl_enabled();
