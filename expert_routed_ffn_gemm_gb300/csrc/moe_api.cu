@@ -382,13 +382,15 @@ cudaEvent_t* prof_slot(moe_handle* h) {
 // covers the pipeline start and the part reduction); the split is taken when
 // it beats the unsplit estimate by 5 %.  Unforced, only K ranges of at least
 // kMinSplitSteps steps are cut (shorter ones gain too little).  The bf16
-// kernel (balanced != NULL) instead takes balanced ranges when they win: the
-// K steps of all items in one contiguous range per CTA, estimated as the
-// range's steps + kItemSteps per unit it runs; *balanced = 1 then.
+// kernel (balanced != NULL) instead takes balanced ranges where they are
+// estimated no slower: the K steps of all items in one contiguous range per
+// CTA, estimated as the range's steps + kItemSteps per unit it runs;
+// *balanced = 1 then.
 int choose_ksplit(const moe_handle* h, int bn, long long items_ub, int k_steps, int* balanced = nullptr) {
   if (balanced != nullptr) *balanced = 0;
   if ((h->fp8 && !h->fp8_x2) || bn > 32 || h->gemm_ksplit == 1 || items_ub <= 0) return 1;
   constexpr int kMinSplitSteps = 32;
+  constexpr int kBalancedMaxWaves = 20;
   const int sms = h->num_sms;
   auto fits = [&](int ks) {  // every part has a K step and the part buffer room
     return (ks - 1) * ((k_steps + ks - 1) / ks) < k_steps && items_ub * ks <= h->ksplit_cap;
@@ -416,7 +418,11 @@ int choose_ksplit(const moe_handle* h, int bn, long long items_ub, int k_steps, 
     const long long per = std::max<long long>((S + sms - 1) / sms, (k_steps + moe::kMaxGemmKSplit - 2) /
                                                                        (moe::kMaxGemmKSplit - 1));
     const double bal = static_cast<double>(per) + static_cast<double>((per + k_steps - 1) / k_steps + 1) * kItemSteps;
-    if (bal < 0.95 * base) {
+    // taken where the estimate is no worse, up to kBalancedMaxWaves waves of
+    // items (flash shape, gate/up, forced against unsplit: 4 tokens 119 ->
+    // 108 us, 8 tokens 186 -> 184 us, 16 tokens 329 -> 327 us; 32 and 64
+    // tokens about 1 % slower)
+    if (bal <= base && items_ub <= kBalancedMaxWaves * sms) {
       *balanced = 1;
       return moe::kMaxGemmKSplit;
     }
