@@ -444,3 +444,33 @@ def test_shared_expert_on_a_second_stream(overlap, tiles):
         assert torch.equal(yg, layer.forward(x))
     assert layer.check() == binding.MOE_OK
     layer.close()
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_random_small_layers(case):
+    # Seeded random small layers (token count, width, experts, top-k, expert
+    # width, token tiles, K split) against the oracle, run to run identical:
+    # the corners of the work decomposition (balanced K ranges whose parts
+    # span 1..4 CTAs, ragged token tiles, groups without rows) that the named
+    # cases may miss.
+    rng = np.random.default_rng(900 + case)
+    T = int(rng.integers(1, 48))
+    d = int(rng.choice([256, 512, 1024, 2048]))
+    E = int(rng.integers(4, 65))
+    k = int(rng.integers(1, min(8, E) + 1))
+    F = int(rng.choice([128, 256, 384]))
+    tiles = [(0, 0), (16, 16), (32, 32), (16, 32)][int(rng.integers(0, 4))]
+    split = ["auto", "b", "2", "1"][int(rng.integers(0, 4))]
+    shape = synth.LayerShape(T=T, d=d, E=E, k=k, F=F)
+    inp = synth.make_inputs(shape, seed=910 + case)
+    env = {} if split == "auto" else {"MOE_GEMM_KSPLIT": split}
+    # fp32 y: the bound then measures the arithmetic, not y's bf16 storage
+    layer, x = make_layer(inp, tiles=tiles, env=env, out_fp32=True)
+    y = layer.forward(x)
+    assert layer.check() == binding.MOE_OK
+    assert torch.equal(layer.forward(x), y)
+    idx, prob, perm, offsets, gap = layer.route(x)
+    xb, wr, wgu, wd = host_bits(inp)
+    check_routing(xb, wr, k, cpu(idx), cpu(prob), cpu(gap), cpu(perm), cpu(offsets))
+    check_output(xb, wr, wgu, wd, k, cpu(y), cpu(idx), out_bf16=False)
+    layer.close()
