@@ -38,6 +38,28 @@ namespace {
 using namespace gemm;
 
 constexpr int kThreads = 192;
+constexpr int kPrefetchChunk = 64 * 1024;  // bytes per L2 prefetch instruction
+
+// The weights of the down launch's items blockIdx.x + w * gridDim.x (w <
+// a.pf_waves) into L2: each item is 128 consecutive weight rows of one group,
+// one contiguous block.  Items of a group's later token tiles read the same
+// rows as its first and are skipped.  tile_start: this launch's token tiles,
+// which the down launch shares.
+__device__ __forceinline__ void prefetch_next_items(const GemmArgs& a, const int* tile_start, int G) {
+  const int n_items = tile_start[G] * a.pf_m_tiles;
+  const long long item_bytes = static_cast<long long>(kBlockM) * a.pf_row_bytes;
+  const char* base = static_cast<const char*>(a.pf_w);
+  int i = static_cast<int>(blockIdx.x);
+  for (int w = 0; w < a.pf_waves && i < n_items; ++w, i += static_cast<int>(gridDim.x)) {
+    const Item it = decode_item(i, a.pf_m_tiles, tile_start, G, n_items, 0);
+    if (it.n > 0) continue;
+    const long long row0 =
+        static_cast<long long>(weight_group(a, it.g)) * a.pf_rows_per_group + static_cast<long long>(it.m) * kBlockM;
+    const char* p = base + row0 * a.pf_row_bytes;
+    for (long long o = 0; o < item_bytes; o += kPrefetchChunk)
+      l2_prefetch_bulk(p + o, static_cast<uint32_t>(min(item_bytes - o, static_cast<long long>(kPrefetchChunk))));
+  }
+}
 
 template <bool GATEUP, int BN>
 struct Cfg {
@@ -178,6 +200,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         has = has_next;
         if (has) has_next = cur.next(nu);
       }
+      // gate/up: every load of this CTA is issued; the down launch's first
+      // weights stream in while the last stages, the epilogue and that
+      // launch's start run
+      if (GATEUP && ok && args.pf_w != nullptr && !*abort_flag) prefetch_next_items(args, tile_start, G);
       // Drain: the last load issued into each stage must have landed before
       // this CTA may exit (they always complete; the wait is bounded anyway).
       for (int s = 0; s < C::STAGES; ++s) {

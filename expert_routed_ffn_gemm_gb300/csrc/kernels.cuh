@@ -224,6 +224,17 @@ struct GemmArgs {
   int chunks_cap;      // exponent chunks the Yp exponent buffer holds
   int off_const[2];    // pair kernels with offsets == NULL: the one group's rows [off_const[0], off_const[1])
   int chunk_const;     // ... and with chunk_base == NULL (down): the group's first exponent chunk
+  // Single-CTA gate/up: once a CTA has issued its last load it brings into L2
+  // the weights of the down launch that follows it, which deals whole items
+  // (group, weight tile of 128 rows) over the same token tiles to a grid of
+  // the same size: CTA c takes that launch's items c + w * gridDim.x, w <
+  // pf_waves, i.e. the first ones each of its CTAs runs.  pf_w: the down
+  // weights [G][pf_rows_per_group][pf_row_bytes bytes]; NULL: no prefetch.
+  const void* pf_w;
+  int pf_waves;
+  int pf_m_tiles;         // weight tiles per group of that launch
+  int pf_rows_per_group;
+  int pf_row_bytes;       // multiple of 16
 };
 
 // K3/K4: tcgen05 grouped GEMMs over the groups' row blocks.  `tile_n` must be
