@@ -150,6 +150,28 @@ def test_gemm_k_split(parts, T, d, F, tiles):
     layer.close()
 
 
+@pytest.mark.parametrize("T,d,E,F,tiles", [(1, 512, 16, 256, (0, 0)), (24, 256, 16, 128, (32, 32)),
+                                           (128, 1024, 8, 128, (16, 16)), (6, 256, 40, 384, (32, 32))])
+def test_down_weight_prefetch(T, d, E, F, tiles):
+    # The single-CTA gate/up brings the down launch's first weights into L2
+    # when that launch has at most two waves of items (all of these): a hint
+    # only, so the output is bit-identical with it off, with one or two waves
+    # of it, and within the bound of the oracle.
+    shape = synth.LayerShape(T=T, d=d, E=E, k=2, F=F)
+    inp = synth.make_inputs(shape, seed=90 + T + E)
+    ys = []
+    for waves in ("0", "1", "2"):
+        layer, x = make_layer(inp, tiles=tiles, env={"MOE_PF_DOWN_WAVES": waves})
+        ys.append(layer.forward(x))
+        assert layer.check() == binding.MOE_OK
+        if waves == "1":
+            idx = layer.route(x)[0]
+        layer.close()
+    assert torch.equal(ys[0], ys[1]) and torch.equal(ys[0], ys[2])
+    xb, wr, wgu, wd = host_bits(inp)
+    check_output(xb, wr, wgu, wd, shape.k, cpu(ys[1].float()), cpu(idx), tokens=np.arange(T, dtype=np.int32))
+
+
 def test_several_weight_tiles_and_k_steps():
     # F = 256 -> 2 gate/up weight tiles, d = 512 -> 4 down weight tiles and 8 K steps.
     shape = synth.LayerShape(T=200, d=512, E=32, k=4, F=256)
