@@ -254,7 +254,7 @@ __device__ __forceinline__ void cluster_sync() {
 
 // Arrive on an mbarrier given by its shared::cluster address (may be the peer's).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // TMA tile load into this CTA's shared memory whose completion is counted on
