@@ -441,8 +441,9 @@ __global__ void __launch_bounds__(1024, 1) combine_kernel(const __half* __restri
   const int t = blockIdx.x;
   __shared__ int pos[kMaxTopK + 1];
   __shared__ int chunk[kMaxTopK + 1];
-  if (threadIdx.x <= k) {
-    const int j = threadIdx.x;
+  // the k + 1 terms' rows (a block can have fewer threads than terms: 32
+  // threads for d = 256 against up to 33 terms)
+  for (int j = threadIdx.x; j <= k; j += blockDim.x) {
     int g = (j < k) ? __ldg(idx + static_cast<size_t>(t) * k + j) : E;
     int p = (j < k) ? __ldg(inv + static_cast<size_t>(t) * k + j) : T * k + t;
     if (!MOE_DBG_OK(g >= 0 && g <= E)) g = E;
