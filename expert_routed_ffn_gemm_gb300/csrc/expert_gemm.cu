@@ -31,6 +31,7 @@
 // Every wait is bounded (wait_limit_ns); on timeout the kernel records an error,
 // drains the copies and MMAs it started, frees tensor memory and returns.
 #include "gemm_common.cuh"
+#include "topk.cuh"
 
 namespace moe {
 namespace {
@@ -39,6 +40,77 @@ using namespace gemm;
 
 constexpr int kThreads = 192;
 constexpr int kPrefetchChunk = 64 * 1024;  // bytes per L2 prefetch instruction
+constexpr int kRouteSlots = kMaxExperts / 32;                   // logits per lane, any E
+constexpr int kRoutePicks = kSmallRouteMaxTokens * kMaxTopK;    // T*k picks at most
+constexpr int kRouteAux = (4 * kRoutePicks + 4 * 16) * 4;      // their shared-memory tables
+
+// The routing of a few tokens inside the gate/up launch (GemmArgs::route_logits):
+// warp t ranks token t from its logits with the routing kernels' softmax and
+// top-k (the same bits in every CTA), then every CTA works out the dispatch
+// position of each pick a = t*k + j (the picks of experts below its own, then
+// the earlier tokens that picked the same expert: the expert, token order of
+// the dispatch) and the tile starts of the groups (each group with rows has
+// one token tile: at most T*k + T rows).  CTA 0 also writes the routing and
+// dispatch results where the routing kernels would.  Every thread of the CTA
+// takes part (it calls __syncthreads).
+__device__ void fused_route_prologue(const GemmArgs& a, int* tile_start, int* s_idx, float* s_prob, int* s_first,
+                                     int* s_pos, int warp, int lane) {
+  const int T = a.route_T, E = a.route_E, k = a.route_k, Tk = T * k;
+  if (warp < T) {
+    float q[kRouteSlots];
+#pragma unroll
+    for (int i = 0; i < kRouteSlots; ++i) {
+      const int e = lane + 32 * i;
+      q[i] = e < E ? __ldcg(a.route_logits + static_cast<size_t>(warp) * E + e) : 0.f;
+    }
+    finish_token<kRouteSlots>(q, warp, lane, E, k, a.route_renorm, s_idx, s_prob, nullptr, nullptr, nullptr, 0);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < Tk; i += blockDim.x) {
+    const int e = s_idx[i];
+    int first = 1, pos = 0;
+    for (int i2 = 0; i2 < Tk; ++i2) {
+      const int v = s_idx[i2];
+      first &= (i2 >= i) | (v != e);
+      pos += (v < e) | ((i2 < i) & (v == e));
+    }
+    s_first[i] = first;
+    s_pos[i] = pos;
+  }
+  __syncthreads();
+  for (int g = threadIdx.x; g <= a.G; g += blockDim.x) {
+    int groups = 0;
+    for (int i = 0; i < Tk; ++i) groups += (s_idx[i] < g) & s_first[i];
+    tile_start[g] = groups + (g > E ? 1 : 0);  // the shared group (index E) has one tile
+  }
+  if (blockIdx.x == 0) {
+    for (int i = threadIdx.x; i < Tk; i += blockDim.x) {
+      a.route_idx[i] = s_idx[i];
+      a.route_prob[i] = s_prob[i];
+      a.route_perm[s_pos[i]] = i;
+      a.route_inv[i] = s_pos[i];
+    }
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      int below = 0, cnt = 0, groups = 0;
+      for (int i = 0; i < Tk; ++i) {
+        const int v = s_idx[i];
+        below += v < e;
+        cnt += v == e;
+        groups += (v < e) & s_first[i];
+      }
+      a.route_offsets[e] = below;
+      a.route_counts[e] = cnt;
+      a.route_chunk_base[e] = groups;  // one exponent chunk per group with rows (fewer than 16 rows)
+    }
+    if (threadIdx.x == 0) {
+      a.route_offsets[E] = Tk;
+      a.route_offsets[E + 1] = Tk + (a.route_has_shared ? T : 0);
+      a.route_chunk_base[E] = shared_chunk0(T, k, E);
+      a.route_chunk_base[E + 1] = a.route_chunk_base[E] + (a.route_has_shared ? (T + kYpRows - 1) / kYpRows : 0);
+    }
+  }
+  __syncthreads();
+}
 
 // The weights of the down launch's items blockIdx.x + w * gridDim.x (w <
 // a.pf_waves) into L2: each item is 128 consecutive weight rows of one group,
@@ -76,7 +148,7 @@ struct Cfg {
   // barriers: full[S], empty[S], acc_full[NACC], acc_empty[NACC], drain
   static constexpr int NUM_BARS = 2 * STAGES + 2 * NACC + 1;
   static constexpr int XCHG_BYTES = GATEUP ? 2 * 2 * 64 * 8 * 4 : 0;  // [parity][dir][64 f][8 cols] fp32
-  static constexpr int AUX_BYTES = NUM_BARS * 8 + 16 + 32 + (kMaxGroups + 1) * 4;
+  static constexpr int AUX_BYTES = NUM_BARS * 8 + 16 + 32 + (kMaxGroups + 1) * 4 + (GATEUP ? kRouteAux : 0);
   static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STAGES * STAGE_BYTES + XCHG_BYTES + AUX_BYTES;
   static_assert(STAGE_BYTES % 1024 == 0, "stage must keep 1024-byte alignment");
   static_assert(STAGES >= 2, "ring too shallow");
@@ -103,9 +175,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* s_ok = reinterpret_cast<volatile int*>(tmem_holder + 4);  // [2 parities][4 warps]
   int* tile_start = reinterpret_cast<int*>(tmem_holder + 12);
+  // gate/up with the routing in this launch: the picks, their weights,
+  // first-of-expert flags and dispatch positions, and each epilogue warp's
+  // map from token column to H row
+  int* s_idx = tile_start + kMaxGroups + 1;
+  float* s_prob = reinterpret_cast<float*>(s_idx + kRoutePicks);
+  int* s_first = s_idx + 2 * kRoutePicks;
+  int* s_pos = s_idx + 3 * kRoutePicks;
+  int* s_rowmap = s_idx + 4 * kRoutePicks;  // [4 warps][16]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = args.G;
+  const bool fused = GATEUP && BN <= 32 && args.route_logits != nullptr;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -128,7 +209,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   pdl_wait();  // offsets, rows and outputs belong to earlier work in the stream until here
-  if (warp == kEpilogueWarp0) build_tile_start(args.offsets, G, BN, tile_start, lane);
+  if (fused)
+    fused_route_prologue(args, tile_start, s_idx, s_prob, s_first, s_pos, warp, lane);
+  else if (warp == kEpilogueWarp0)
+    build_tile_start(args.offsets, G, BN, tile_start, lane);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -159,7 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto rows_of = [&](int item, int& row_w, int& row_act) {
         const Item it = decode_item(item, args.m_tiles, tile_start, G, n_base, args.reverse);
         row_w = weight_row(it);
-        row_act = __ldg(args.offsets + it.g) + it.n * BN;
+        // routing in this launch: every group's tile is the token matrix's rows 0..T-1
+        row_act = fused ? 0 : __ldg(args.offsets + it.g) + it.n * BN;
       };
       UnitCursor cur;
       cur.init(mode, n_base, k_all, args.ksplit);
@@ -220,6 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // N of the MMAs: the tile's rows rounded up to 16 (ragged tails); the
       // next unit's descriptor is worked out while this unit's MMAs run
       auto idesc_of = [&](int item) {
+        if (fused) return item < n_base ? idesc_bf16_f32(kBlockM, mma_width(args.route_T, 16, BN)) : 0u;
         return item_idesc(item, n_base, args.reverse, args.m_tiles, tile_start, G, args.offsets, kBlockM, 16, BN);
       };
       UnitCursor cur;
@@ -284,11 +370,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     WorkUnit u;
     while (cur.next(u)) {
       const Item it = decode_item(u.item, args.m_tiles, tile_start, G, n_base, args.reverse);
-      const int g_row0 = __ldg(args.offsets + it.g);
-      const int g_rows = __ldg(args.offsets + it.g + 1) - g_row0;
+      const int g_row0 = fused ? 0 : __ldg(args.offsets + it.g);
+      const int g_rows = fused ? args.route_T : __ldg(args.offsets + it.g + 1) - g_row0;
       const int row0 = g_row0 + it.n * BN;
       const int chunk0 = GATEUP ? -1 : __ldg(args.chunk_base + it.g) + it.n * (BN / kYpRows);
       const int valid = checked_valid(args, min(BN, g_rows - it.n * BN), row0, chunk0);
+      // routing in this launch: column t (token t) goes to the H row of token t's
+      // pick of this group, or nowhere; the shared group's rows are T*k + t
+      int* rowmap = nullptr;
+      if (fused) {
+        rowmap = s_rowmap + q * 16;
+        if (lane < args.route_T) {
+          const int k = args.route_k;
+          int r = -1;
+          if (it.g >= args.route_E) {
+            r = args.route_T * k + lane;
+          } else {
+            for (int j = 0; j < k; ++j)
+              if (s_idx[lane * k + j] == it.g) r = s_pos[lane * k + j];
+          }
+          rowmap[lane] = r;
+        }
+        __syncwarp();
+      }
       // K4: the gate weight of every column, loaded while the MMAs still run
       float wreg[(BN + 31) / 32];
       if (!GATEUP) load_gate_weights<BN>(wreg, row0, valid, lane, args.perm, args.prob, args.Tk);
@@ -317,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (GATEUP)
             epilogue_gateup<BN>(0u, row, it.m * (kBlockM / 2), row0, valid, static_cast<bf16*>(args.out),
-                                args.out_ld, xchg, chunk_par, 1.0f, sum);
+                                args.out_ld, xchg, chunk_par, 1.0f, sum, rowmap);
           else
             epilogue_down<BN>(0u, it.m * kBlockM + row, row0, valid, wreg, static_cast<__half*>(args.out),
                               args.out_exp, args.out_ld, chunk0, 1.0f, 0, sum);
@@ -341,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ksplit_sum_units<BN>(args.ksplit_part, cur, u, row, valid, sum);
             if (GATEUP)
               epilogue_gateup<BN>(0u, row, it.m * (kBlockM / 2), row0, valid, static_cast<bf16*>(args.out),
-                                  args.out_ld, xchg, chunk_par, 1.0f, sum);
+                                  args.out_ld, xchg, chunk_par, 1.0f, sum, rowmap);
             else
               epilogue_down<BN>(0u, it.m * kBlockM + row, row0, valid, wreg, static_cast<__half*>(args.out),
                                 args.out_exp, args.out_ld, chunk0,
@@ -354,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (GATEUP) {
         // rows 0..63: gate of feature 64m + row; rows 64..127: up of feature 64m + row - 64
         epilogue_gateup<BN>(taddr, row, it.m * (kBlockM / 2), row0, valid, static_cast<bf16*>(args.out),
-                            args.out_ld, xchg, chunk_par);
+                            args.out_ld, xchg, chunk_par, 1.0f, nullptr, rowmap);
       } else {
         epilogue_down<BN>(taddr, it.m * kBlockM + row, row0, valid, wreg, static_cast<__half*>(args.out),
                           args.out_exp, args.out_ld, chunk0);

@@ -179,11 +179,13 @@ __device__ __forceinline__ __half to_out(float v, __half*) { return __float2half
 // g and u are the accumulators times the `scale` of their own weight row (1
 // for bf16 weights).  H is bf16 or fp16 (OutT).
 // vals (or NULL): this thread's row of the accumulator, already summed over K
-// parts, used in place of tensor memory.
+// parts, used in place of tensor memory.  rowmap (or NULL): the H row of each
+// column in place of row0 + col (negative: the column is not stored).
 template <int BN, typename OutT>
 __device__ __forceinline__ void epilogue_gateup(uint32_t taddr, int row, int feat_base, int row0, int valid,
                                                 OutT* H, int ldh, float* xchg, uint32_t& chunk_par,
-                                                float scale = 1.0f, const float* vals = nullptr) {
+                                                float scale = 1.0f, const float* vals = nullptr,
+                                                const int* rowmap = nullptr) {
   const bool is_gate = row < 64;
   const int fl = row & 63;
   const int feat = feat_base + fl;
@@ -216,7 +218,10 @@ __device__ __forceinline__ void epilogue_gateup(uint32_t taddr, int row, int fea
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
       const float h = is_gate ? silu_mul(keep[c], peer[c]) : silu_mul(peer[c], keep[c]);
-      if (col0 + c < valid) H[static_cast<size_t>(row0 + col0 + c) * ldh + feat] = to_out(h, H);
+      if (col0 + c < valid) {
+        const int r = rowmap != nullptr ? rowmap[col0 + c] : row0 + col0 + c;
+        if (r >= 0) H[static_cast<size_t>(r) * ldh + feat] = to_out(h, H);
+      }
     }
     chunk_par ^= 1u;
   }

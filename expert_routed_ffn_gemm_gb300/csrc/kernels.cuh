@@ -149,6 +149,7 @@ struct SmallRouteExtras {
   const void* pf1;
   long long pf1_bytes;
   void* xp;
+  int logits_only;  // 1: the logits (and the prefetch) only; the gate/up launch ranks the tokens
 };
 bool route_small_fits(int T, int d, int E);
 cudaError_t launch_route_small(const bf16* x, const float* w_router, int T, int d, int E, int k, int renorm,
@@ -235,6 +236,25 @@ struct GemmArgs {
   int pf_m_tiles;         // weight tiles per group of that launch
   int pf_rows_per_group;
   int pf_row_bytes;       // multiple of 16
+  // Few tokens (at most kSmallRouteMaxTokens), bf16 gate/up on one CTA per
+  // SM: the routing finished in this launch.  With route_logits [T][E] fp32
+  // non-NULL every CTA ranks each token's experts from the logits (the same
+  // softmax and top-k as the routing kernels), lays the dispatch out in shared
+  // memory, reads the token rows straight from the token matrix behind map_act
+  // (its rows 0..T-1 for every group; the columns of tokens that did not pick a
+  // group are computed and not stored) and stores H at the dispatch
+  // positions; CTA 0 writes the routing and dispatch results (route_* below,
+  // as the routing kernels lay them out) for the down projection and the
+  // combine.  offsets is unused then.
+  const float* route_logits;
+  int route_T, route_E, route_k, route_renorm, route_has_shared;
+  int* route_idx;
+  float* route_prob;
+  int* route_counts;
+  int* route_offsets;  // [E + 2]
+  int* route_perm;
+  int* route_inv;
+  int* route_chunk_base;  // [E + 2]
 };
 
 // K3/K4: tcgen05 grouped GEMMs over the groups' row blocks.  `tile_n` must be

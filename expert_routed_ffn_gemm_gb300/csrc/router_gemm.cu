@@ -18,6 +18,7 @@
 // bits); ties go to the lower expert index.
 #include "kernels.cuh"
 #include "ptx.cuh"
+#include "topk.cuh"
 
 #include <algorithm>
 #include <cfloat>
@@ -315,118 +316,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 constexpr int kTopkWarps = 4;
 constexpr int kTopkWarpMinTokens = 1024;  // from this many tokens on: one warp per token
 
-// Best slot of a lane not yet taken: highest softmax numerator, then lowest
-// slot (= lowest expert index, e = lane + 32 i); -1 when none is left.
-template <int NS>
-__device__ __forceinline__ int lane_head(const float (&q)[NS], uint32_t taken, int lane, int E) {
-  int h = -1;
-  float hv = 0.f;
-#pragma unroll
-  for (int i = 0; i < NS; ++i) {
-    const bool ok = !((taken >> i) & 1u) && lane + 32 * i < E;
-    if (ok && (h < 0 || q[i] > hv)) {
-      h = i;
-      hv = q[i];
-    }
-  }
-  return h;
-}
-
-// Softmax, top-k (ties: lower index), gap, per-expert counts (counts != NULL)
-// and the optional per-token statistics of token t, by one warp whose lane l
-// holds the summed logits of experts l, l+32, ..., l+32(NS-1) in z.  The
-// ranking uses the softmax numerators q_e = exp(z_e - max z), which order the
-// experts as the probabilities q_e / sum q do; each of the k+1 selection
-// rounds is one warp max over the lanes' heads, then the lowest expert index
-// among the heads holding it; only the winning lane finds its next head.
-// renorm != 0: the k weights are divided by their sum (slot order).  tokstats
-// (or NULL): the probability mass of each of n_groups equal expert groups,
-// then the entropy -sum p ln p ([T][n_groups+1]).
-template <int NS>
-__device__ __forceinline__ void finish_token(float (&q)[NS], int t, int lane, int E, int k, int renorm,
-                                             int* __restrict__ idx, float* __restrict__ prob,
-                                             float* __restrict__ gap, int* counts, float* __restrict__ tokstats,
-                                             int n_groups, int* sel = nullptr) {
-  float zmax = -FLT_MAX;
-#pragma unroll
-  for (int i = 0; i < NS; ++i)
-    if (lane + 32 * i < E) zmax = fmaxf(zmax, q[i]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, off));
-  float s = 0.f;
-#pragma unroll
-  for (int i = 0; i < NS; ++i) {
-    q[i] = (lane + 32 * i < E) ? expf(q[i] - zmax) : 0.f;
-    s += q[i];
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-
-  if (tokstats != nullptr) {
-    // group masses (group of expert e = e / (E / n_groups)) and entropy
-    const int per_group = E / n_groups;
-    float* out = tokstats + static_cast<size_t>(t) * (n_groups + 1);
-    for (int g = 0; g < n_groups; ++g) {
-      float m = 0.f;
-#pragma unroll
-      for (int i = 0; i < NS; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && e / per_group == g) m += q[i] / s;
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) m += __shfl_xor_sync(0xffffffffu, m, off);
-      if (lane == 0) out[g] = m;
-    }
-    float h = 0.f;
-#pragma unroll
-    for (int i = 0; i < NS; ++i) {
-      const int e = lane + 32 * i;
-      const float p = q[i] / s;
-      if (e < E && p > 0.f) h -= p * logf(p);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) h += __shfl_xor_sync(0xffffffffu, h, off);
-    if (lane == 0) out[n_groups] = h;
-  }
-
-  // Selection rounds.  Numerators are >= 0, so their bit patterns order like
-  // the values; key = bits + 1 (0 marks a lane with nothing left).
-  uint32_t taken = 0u;
-  int head = lane_head(q, taken, lane, E);
-  float pk = 0.f, sel_sum = 0.f, my_p = 0.f;
-  int my_e = 0;
-  for (int j = 0; j <= k; ++j) {
-    float hq = 0.f;
-#pragma unroll
-    for (int i = 0; i < NS; ++i)
-      if (i == head) hq = q[i];
-    const uint32_t hk = head >= 0 ? __float_as_uint(hq) + 1u : 0u;
-    const uint32_t mk = __reduce_max_sync(0xffffffffu, hk);
-    const uint32_t my_idx = head >= 0 ? static_cast<uint32_t>(lane + 32 * head) : 0x7fffffffu;
-    const int be = static_cast<int>(__reduce_min_sync(0xffffffffu, (mk != 0u && hk == mk) ? my_idx : 0x7fffffffu));
-    const float bv = mk ? __uint_as_float(mk - 1u) / s : -1.f;
-    if (j < k) {
-      if (be != 0x7fffffff && (be & 31) == lane) {  // the winner takes its head and finds the next one
-        taken |= 1u << head;
-        head = lane_head(q, taken, lane, E);
-      }
-      if (lane == j) {  // lane j keeps slot j
-        my_e = be;
-        my_p = bv;
-      }
-      sel_sum += bv;  // same value and order in every lane
-      pk = bv;
-    } else if (gap != nullptr && lane == 0) {
-      gap[t] = (be == 0x7fffffff) ? __int_as_float(0x7f800000) : (pk - bv);
-    }
-  }
-  if (lane < k) {
-    idx[static_cast<size_t>(t) * k + lane] = my_e;
-    prob[static_cast<size_t>(t) * k + lane] = renorm ? my_p / sel_sum : my_p;
-    if (counts != nullptr) atomicAdd(&counts[my_e], 1);
-    if (sel != nullptr) sel[t * k + lane] = my_e;
-  }
-}
 
 // Few tokens (decode): one block of 4 warps per token.  Warp w sums the K-split
 // partials s = w, w+4, ... in increasing s; warp 0 then adds the four partial
@@ -534,7 +423,9 @@ __global__ void __launch_bounds__(kTopkTokensPerBlock * 32) router_topk_warp_ker
 // of dispatch_kernel).  With one token its k rows are copies of it whatever
 // the experts, so blocks 0..k-1 copy them beside their dot products; with
 // two the last block copies them.  Every result is a function of x and W_r
-// alone (fixed summation orders): bit-identical run to run.
+// alone (fixed summation orders): bit-identical run to run.  With
+// ex.logits_only the blocks stop at their logits (no count, no last block):
+// the gate/up launch after this one ranks the tokens itself.
 constexpr int kSmallRouteWarps = 4;
 
 template <int NS>
@@ -589,6 +480,23 @@ __global__ void __launch_bounds__(kSmallRouteWarps * 32) route_small_kernel(
   if (threadIdx.x < T)
     logits[static_cast<size_t>(threadIdx.x) * E + e] =
         ((s_part[0][threadIdx.x] + s_part[1][threadIdx.x]) + s_part[2][threadIdx.x]) + s_part[3][threadIdx.x];
+  // weights every call reads whatever the routing (the shared expert's),
+  // into L2 while the routing finishes — after this block's loads of W_r,
+  // which they would otherwise delay: chunks of kPrefetchChunk bytes, block
+  // b taking chunks b, b + gridDim.x, ...
+  auto prefetch_shared = [&] {
+    for (int r = 0; r < 2; ++r) {
+      const char* base = static_cast<const char*>(r == 0 ? ex.pf0 : ex.pf1);
+      const long long n = r == 0 ? ex.pf0_bytes : ex.pf1_bytes;
+      for (long long o = static_cast<long long>(blockIdx.x) * kPrefetchChunk; o < n;
+           o += static_cast<long long>(gridDim.x) * kPrefetchChunk)
+        l2_prefetch_bulk(base + o, static_cast<uint32_t>(n - o < kPrefetchChunk ? n - o : kPrefetchChunk));
+    }
+  };
+  if (ex.logits_only) {  // the gate/up launch after this one ranks the tokens
+    if (threadIdx.x == 0) prefetch_shared();
+    return;
+  }
   // the block that finishes last sees every logit (the barrier orders this
   // block's logit stores before thread 0's release fence and count)
   __syncthreads();
@@ -597,17 +505,7 @@ __global__ void __launch_bounds__(kSmallRouteWarps * 32) route_small_kernel(
     const bool last = atomicAdd(done, 1u) == gridDim.x - 1;
     if (last) __threadfence();  // acquire: every block's logits are visible
     s_last = last;
-    // weights every call reads whatever the routing (the shared expert's),
-    // into L2 while the routing finishes — after this block's loads of W_r,
-    // which they would otherwise delay: chunks of kPrefetchChunk bytes, block
-    // b taking chunks b, b + gridDim.x, ...
-    for (int r = 0; r < 2; ++r) {
-      const char* base = static_cast<const char*>(r == 0 ? ex.pf0 : ex.pf1);
-      const long long n = r == 0 ? ex.pf0_bytes : ex.pf1_bytes;
-      for (long long o = static_cast<long long>(blockIdx.x) * kPrefetchChunk; o < n;
-           o += static_cast<long long>(gridDim.x) * kPrefetchChunk)
-        l2_prefetch_bulk(base + o, static_cast<uint32_t>(n - o < kPrefetchChunk ? n - o : kPrefetchChunk));
-    }
+    prefetch_shared();
   }
   __syncthreads();
   if (!s_last) return;
