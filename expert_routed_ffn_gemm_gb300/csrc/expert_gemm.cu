@@ -243,8 +243,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto rows_of = [&](int item, int& row_w, int& row_act) {
         const Item it = decode_item(item, args.m_tiles, tile_start, G, n_base, args.reverse);
         row_w = weight_row(it);
-        // routing in this launch: every group's tile is the token matrix's rows 0..T-1
-        row_act = fused ? 0 : __ldg(args.offsets + it.g) + it.n * BN;
+        // routing in this launch: every group's tile is this CTA's copy of the T token rows
+        row_act = fused ? static_cast<int>(blockIdx.x % max(1, args.route_replicas)) * args.route_T
+                        : __ldg(args.offsets + it.g) + it.n * BN;
       };
       UnitCursor cur;
       cur.init(mode, n_base, k_all, args.ksplit);

@@ -150,6 +150,7 @@ struct SmallRouteExtras {
   long long pf1_bytes;
   void* xp;
   int logits_only;  // 1: the logits (and the prefetch) only; the gate/up launch ranks the tokens
+  int replicas;     // logits only: copies of the T token rows written to xp for that launch
 };
 bool route_small_fits(int T, int d, int E);
 cudaError_t launch_route_small(const bf16* x, const float* w_router, int T, int d, int E, int k, int renorm,
@@ -240,14 +241,15 @@ struct GemmArgs {
   // SM: the routing finished in this launch.  With route_logits [T][E] fp32
   // non-NULL every CTA ranks each token's experts from the logits (the same
   // softmax and top-k as the routing kernels), lays the dispatch out in shared
-  // memory, reads the token rows straight from the token matrix behind map_act
-  // (its rows 0..T-1 for every group; the columns of tokens that did not pick a
-  // group are computed and not stored) and stores H at the dispatch
+  // memory, reads every group's token tile from a copy of the T token rows
+  // behind map_act (the columns of tokens that did not pick a group, and any
+  // rows past the T, are computed and not stored) and stores H at the dispatch
   // positions; CTA 0 writes the routing and dispatch results (route_* below,
   // as the routing kernels lay them out) for the down projection and the
   // combine.  offsets is unused then.
   const float* route_logits;
   int route_T, route_E, route_k, route_renorm, route_has_shared;
+  int route_replicas;  // copies of the T token rows behind map_act: CTA c reads rows (c mod it) * T ...
   int* route_idx;
   float* route_prob;
   int* route_counts;

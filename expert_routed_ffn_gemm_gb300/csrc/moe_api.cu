@@ -25,13 +25,6 @@ constexpr int kProfStages = 6;
 constexpr int kProfEvents = kProfStages + 1;
 constexpr int kProfMaxCalls = 4096;
 constexpr int kFusedGatherMaxTokens = 2;  // the few-token routing launch also copies the rows up to here
-// The top-k and dispatch in the gate/up launch for these token counts (flash
-// shape, three A/B rounds: 2 tokens 0.1111 -> 0.1086 ms, 3 tokens 0.1475 ->
-// 0.1462 ms; 1 token 0.0694 -> 0.0699 ms, where the routing launch's last
-// block has little to do and its L2 prefetch of the shared expert helps, and
-// 4 tokens 0.1753 -> 0.1788 ms, where every CTA lays out 32 picks)
-constexpr int kRouteInGemmMinTokens = 2;
-constexpr int kRouteInGemmMaxTokens = 3;
 constexpr int kSharedOverlapMinTokens = 2048;  // the shared expert's gate/up on a second stream from here
 
 struct moe_handle {
@@ -46,10 +39,8 @@ struct moe_handle {
   bool use_pairs;   // 256-row token tiles on CTA pairs (MOE_PAIR_TILES=0 turns it off)
   bool small_route; // routing and dispatch in one launch for a few tokens (MOE_SMALL_ROUTE=0 turns it off)
   // ... and with bf16 weights the top-k and dispatch in the gate/up launch
-  // instead, which reads the token rows from x: -1 from kRouteInGemmMinTokens to
-  // kRouteInGemmMaxTokens tokens, 0 never, 1 whenever the routing launch is used
-  // (MOE_ROUTE_IN_GEMM)
-  int route_in_gemm;
+  // instead, which reads copies of the token rows (MOE_ROUTE_IN_GEMM=0 turns it off)
+  bool route_in_gemm;
   // Many tokens: the shared expert's gate/up on a second stream, beside the
   // dispatch and the row scatter (MOE_SHARED_OVERLAP=0 turns it off)
   bool shared_overlap;
@@ -341,6 +332,14 @@ int enqueue_router(moe_handle* h, const void* x, int T, CallOpts o, int* idx, fl
 
 // K1 + K2 into the given buffers.
 // A few tokens: K1 and K2 in one launch (the few-token routing kernel).
+// Copies of the T token rows the routing launch writes to the row buffer
+// when the gate/up launch finishes the routing (its CTAs read them round
+// robin): up to 16, as many as the buffer's rows hold, one per block of the
+// routing launch (a block per expert).
+int token_replicas(const moe_handle* h, int T) {
+  return std::max(1, std::min({16, h->rows_max / T, h->cfg.n_experts}));
+}
+
 bool small_route(const moe_handle* h, int T) {
   return h->small_route && moe::route_small_fits(T, h->cfg.d_model, h->cfg.n_experts);
 }
@@ -522,15 +521,10 @@ int enqueue_gateup(moe_handle* h, moe::GemmArgs a, double mean_rows, const CUten
   const FfnPlan p = plan_ffn(h, a, mean_rows, n_rows);
   CUtensorMap map2;
   const CUtensorMap* map_act2 = nullptr;
-  const CUtensorMap* map_x = nullptr;  // the token rows when the routing finishes in this launch
   if (a.route_logits != nullptr) {
-    // the routing finishes in this launch: every group's token tile is
-    // rows 0..T-1 of x (rows2), zero-filled past them
-    if (rows2 == nullptr || h->fp8 || p.pair1 || p.bn1 > 32 ||
-        !encode_2d(&map2, rows2, static_cast<uint64_t>(n_rows2), static_cast<uint64_t>(c.d_model),
-                   static_cast<uint32_t>(p.bn1)))
-      return MOE_ERR_CUDA;
-    map_x = &map2;
+    // the routing finishes in this launch: every group's token tile is a
+    // copy of the T token rows in the row buffer (written by the routing launch)
+    if (h->fp8 || p.pair1 || p.bn1 > 32) return MOE_ERR_UNSUPPORTED;
     a.act2_from = -1;
   } else if (a.act2_from >= 0 && rows2 != nullptr && !h->fp8) {
     if (!encode_2d(&map2, rows2, static_cast<uint64_t>(n_rows2), static_cast<uint64_t>(c.d_model),
@@ -570,8 +564,7 @@ int enqueue_gateup(moe_handle* h, moe::GemmArgs a, double mean_rows, const CUten
       a.ksplit = choose_ksplit(h, p.bn1, tiles_ub(a, p, p.bn1) * a.m_tiles, a.K / moe::kBlockK, &a.kbalance);
       set_down_prefetch(h, a, p);
     }
-    MOE_CUDA(moe::launch_expert_gemm(true, p.bn1, &h->map_wgu, map_x != nullptr ? map_x : &map_rows[i1], map_act2, a,
-                                     h->num_sms, s));
+    MOE_CUDA(moe::launch_expert_gemm(true, p.bn1, &h->map_wgu, &map_rows[i1], map_act2, a, h->num_sms, s));
   }
   MOE_MARK(4);
   return MOE_OK;
@@ -676,12 +669,14 @@ int enqueue_forward(moe_handle* h, const void* x, int T, CallOpts o, void* y, cu
   const double mean_rows = static_cast<double>(T) * o.k / c.n_experts;
   const int n_rows = T * o.k + (c.has_shared ? T : 0);
   // bf16 weights, one CTA per SM and token tiles of at most 32 rows: the
-  // few-token routing launch writes the logits only, and the gate/up launch
-  // ranks the tokens, lays out the dispatch and reads the token rows from x
+  // few-token routing launch writes the logits (and copies of the token
+  // rows) only, and the gate/up launch ranks the tokens, lays out the
+  // dispatch and reads the rows from the copies (flash shape, three A/B
+  // rounds against the routing launch doing it all: 1 token 0.0688 ->
+  // 0.0683 ms, 2 tokens 0.1097 -> 0.1070, 3 tokens 0.1451 -> 0.1437, 4 tokens
+  // 0.1723 -> 0.1714)
   bool route_in_gemm = false;
-  const bool route_in_gemm_rows =
-      h->route_in_gemm > 0 || (h->route_in_gemm < 0 && T >= kRouteInGemmMinTokens && T <= kRouteInGemmMaxTokens);
-  if (fused_route && route_in_gemm_rows && !h->fp8) {
+  if (fused_route && h->route_in_gemm && !h->fp8) {
     moe::GemmArgs probe{};
     const FfnPlan p = plan_ffn(h, probe, mean_rows, n_rows);
     route_in_gemm = !p.pair1 && p.bn1 <= 32;
@@ -694,14 +689,15 @@ int enqueue_forward(moe_handle* h, const void* x, int T, CallOpts o, void* y, cu
     const void* pf[2];
     long long pfn[2];
     shared_weights(h, pf, pfn);  // read by every call: into L2 while routing
-    if (!route_in_gemm) {  // a launch that ends at its logits waits for no prefetch
+    if (!route_in_gemm) {  // (a launch that stops at its logits ends before the prefetch could help)
       ex.pf0 = pf[0];
       ex.pf0_bytes = pfn[0];
       ex.pf1 = pf[1];
       ex.pf1_bytes = pfn[1];
     }
-    ex.xp = fused_gather ? h->yp : nullptr;
+    ex.xp = fused_gather || route_in_gemm ? h->yp : nullptr;
     ex.logits_only = route_in_gemm ? 1 : 0;
+    ex.replicas = route_in_gemm ? token_replicas(h, T) : 0;
     MOE_CUDA(moe::launch_route_small(static_cast<const bf16*>(x), h->w.w_router, T, c.d_model, c.n_experts, o.k,
                                      o.renorm, c.has_shared, h->partial, h->route_done, h->idx, h->prob, nullptr,
                                      h->counts, h->offsets, h->perm, h->inv, h->chunk_base, ex, s));
@@ -738,6 +734,7 @@ int enqueue_forward(moe_handle* h, const void* x, int T, CallOpts o, void* y, cu
   a.act2_from = shared_from_x ? T * o.k : -1;
   if (route_in_gemm) {
     a.route_logits = h->partial;
+    a.route_replicas = token_replicas(h, T);
     a.route_T = T;
     a.route_E = c.n_experts;
     a.route_k = o.k;
@@ -762,9 +759,9 @@ int enqueue_forward(moe_handle* h, const void* x, int T, CallOpts o, void* y, cu
   // router GEMM, top-k, dispatch, gather, gate/up, down, combine; many
   // tokens: two more for the chunk histograms and their scan, and two more
   // for the shared expert's gate/up and down on the second stream; a few tokens:
-  // routing and dispatch in one (one or two tokens: and the gather; bf16
-  // weights: the logits, the rest in the gate/up launch, no gather); FP8
-  // two-term rows: one more for the requantisation of H
+  // routing and dispatch in one (bf16 weights: the logits and the row
+  // copies, the rest in the gate/up launch; else with one or two tokens also
+  // the gather); FP8 two-term rows: one more for the requantisation of H
   h->last_kernels = (fused_route ? (fused_gather || route_in_gemm ? 4 : 5) : moe::chunked_dispatch(T) ? 9 : 7) +
                     (h->fp8_x2 ? 1 : 0) + (overlap_shared ? 2 : 0);
   return MOE_OK;
@@ -876,7 +873,7 @@ int init_any(const moe_config* cfg, const moe_weights* w, const float* s_gu, con
     const char* vs = std::getenv("MOE_SMALL_ROUTE");
     h->small_route = !(vs && vs[0] == '0');
     const char* vrg = std::getenv("MOE_ROUTE_IN_GEMM");
-    h->route_in_gemm = vrg == nullptr ? -1 : (vrg[0] == '0' ? 0 : 1);
+    h->route_in_gemm = !(vrg && vrg[0] == '0');
     const char* vo = std::getenv("MOE_SHARED_OVERLAP");
     h->shared_overlap = !(vo && vo[0] == '0');
     const char* vx = std::getenv("MOE_FP8_X2");

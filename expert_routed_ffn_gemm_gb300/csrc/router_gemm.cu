@@ -471,10 +471,19 @@ __global__ void __launch_bounds__(kSmallRouteWarps * 32) route_small_kernel(
   }
   // One token: its k routed rows are k copies of it at dispatch positions
   // 0..k-1 whatever the experts, so blocks 0..k-1 copy them now
-  if (ex.xp != nullptr && T == 1 && e < k) {
+  if (ex.xp != nullptr && !ex.logits_only && T == 1 && e < k) {
     const uint4* src = reinterpret_cast<const uint4*>(x);
     uint4* dst = reinterpret_cast<uint4*>(static_cast<bf16*>(ex.xp) + static_cast<size_t>(e) * d);
     for (int c = threadIdx.x; c < d / 8; c += blockDim.x) dst[c] = __ldg(src + c);
+  }
+  // Logits only: the gate/up launch reads every group's token tile from one
+  // of ex.replicas copies of the T rows (rows r*T .. r*T + T-1 of xp, CTA c
+  // reading copy c mod replicas), so its CTAs do not all load the same few
+  // lines; block r < replicas writes copy r
+  if (ex.xp != nullptr && ex.logits_only && e < ex.replicas) {
+    const uint4* src = reinterpret_cast<const uint4*>(x);
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<bf16*>(ex.xp) + static_cast<size_t>(e) * T * d);
+    for (int c = threadIdx.x; c < T * d / 8; c += blockDim.x) dst[c] = __ldg(src + c);
   }
   __syncthreads();
   if (threadIdx.x < T)

@@ -307,12 +307,12 @@ int moe_check(moe_handle* h, void* stream);
  * from 1024 tokens on 9: two more that count each expert's rows per 256-token
  * chunk and scan those counts, in place of counters in the top-k kernel; from
  * 2048 tokens on 11 with bf16 weights: the shared expert's gate/up and down on
- * a second stream; from 1 to 4 tokens 4 or 5: one launch for the router, the
- * top-k and the dispatch (with one token also the row copy; with bf16 weights
- * and two or three tokens the logits only, the gate/up launch finishing the
- * routing and reading the rows itself), the row gather where still needed,
- * gate/up, down and combine; one more on a handle with FP8 weights: the
- * requantisation of H into two-term E4M3 rows).
+ * a second stream; from 1 to 4 tokens with bf16 weights 4: one launch for the
+ * router's logits and copies of the token rows (the gate/up launch finishing
+ * the top-k and the dispatch), gate/up, down and combine; with FP8 weights 5:
+ * the routing launch also does the top-k and dispatch, and the row gather
+ * follows it; one more on a handle with two-term E4M3 rows: the
+ * requantisation of H).
  * Host-only, never synchronises.  Returns -1 for an invalid handle.  No
  * counterpart in the pages: instrumentation for launch accounting.
  */

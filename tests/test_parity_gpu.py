@@ -418,10 +418,9 @@ def test_few_token_routing_both_paths(fused, T, d, E, k):
     idx, prob, perm, offsets, gap = layer.route(x)
     y = layer.forward(x)
     assert layer.check() == binding.MOE_OK
-    # fused: one launch for routing and dispatch, with one token also the row
-    # copy; with two or three tokens the logits only (the top-k and dispatch
-    # in the gate/up launch, which reads the rows from x); with four a gather
-    assert layer.last_kernel_count() == ((4 if T <= 3 else 5) if fused == "1" else 7)
+    # fused: one launch for the logits and copies of the token rows, the
+    # top-k and dispatch in the gate/up launch
+    assert layer.last_kernel_count() == (4 if fused == "1" else 7)
     xb, wr, wgu, wd = host_bits(inp)
     check_routing(xb, wr, k, cpu(idx), cpu(prob), cpu(gap), cpu(perm), cpu(offsets))
     check_output(xb, wr, wgu, wd, k, cpu(y.float()), cpu(idx), storage_slack=False)
@@ -436,16 +435,17 @@ def test_few_token_routing_both_paths(fused, T, d, E, k):
     (3, 256, 300, 8, 128, False, None, False),
     (4, 1024, 24, 8, 384, True, 4, True),
     (4, 256, 512, 32, 128, True, None, False),  # T*k = 128 picks over 512 experts, the limits
+    (3, 256, 6, 2, 128, True, None, False),  # fewer experts (routing blocks) than copies of the rows
 ])
 def test_routing_in_gate_up_launch(T, d, E, k, F, shared, top_k, renorm):
-    # Few tokens, bf16 weights (by default 2 and 3 tokens; MOE_ROUTE_IN_GEMM=1
-    # forces it from 1 to 4): the routing launch writes the logits only and
-    # every gate/up CTA ranks the tokens (the same softmax and top-k code),
-    # lays out the dispatch and reads the token rows from x; CTA 0 writes the
-    # routing results for the down GEMM and the combine.  Bit-identical to the
-    # routing launch doing it all (MOE_ROUTE_IN_GEMM=0), with per-call top-k and
-    # renormalisation too, and against the oracle.  The last case also has more
-    # terms per token (33) than the combine has threads (32 for d = 256).
+    # 1 to 4 tokens, bf16 weights: the routing launch writes the logits and
+    # copies of the token rows only, and every gate/up CTA ranks the tokens
+    # (the same softmax and top-k code), lays out the dispatch and reads its
+    # copy of the rows; CTA 0 writes the routing results for the down GEMM and
+    # the combine.  Bit-identical to the routing launch doing it all
+    # (MOE_ROUTE_IN_GEMM=0), with per-call top-k and renormalisation too, and
+    # against the oracle.  The last case also has more terms per token (33)
+    # than the combine has threads (32 for d = 256).
     shape = synth.LayerShape(T=T, d=d, E=E, k=k, F=F, has_shared=shared)
     inp = synth.make_inputs(shape, seed=700 + T + E)
     ys = {}
