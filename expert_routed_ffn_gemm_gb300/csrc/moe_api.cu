@@ -332,16 +332,16 @@ int enqueue_router(moe_handle* h, const void* x, int T, CallOpts o, int* idx, fl
 
 // K1 + K2 into the given buffers.
 // A few tokens: K1 and K2 in one launch (the few-token routing kernel).
+bool small_route(const moe_handle* h, int T) {
+  return h->small_route && moe::route_small_fits(T, h->cfg.d_model, h->cfg.n_experts);
+}
+
 // Copies of the T token rows the routing launch writes to the row buffer
 // when the gate/up launch finishes the routing (its CTAs read them round
 // robin): up to 16, as many as the buffer's rows hold, one per block of the
 // routing launch (a block per expert).
 int token_replicas(const moe_handle* h, int T) {
   return std::max(1, std::min({16, h->rows_max / T, h->cfg.n_experts}));
-}
-
-bool small_route(const moe_handle* h, int T) {
-  return h->small_route && moe::route_small_fits(T, h->cfg.d_model, h->cfg.n_experts);
 }
 
 int enqueue_route(moe_handle* h, const void* x, int T, CallOpts o, int* idx, float* prob, int* perm, int* offsets,
