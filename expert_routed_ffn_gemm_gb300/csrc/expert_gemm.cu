@@ -381,6 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int* rowmap = nullptr;
       if (fused) {
         rowmap = s_rowmap + q * 16;
+        __syncwarp();  // every lane has stored the previous item's columns
         if (lane < args.route_T) {
           const int k = args.route_k;
           int r = -1;
