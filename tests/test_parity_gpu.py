@@ -355,12 +355,16 @@ def test_flash_largest_sweep_point(flash_weights):
     flash_case(flash_weights, 32768, seed=232, n_sample=48, out_fp32=True)
 
 
-def test_forward_captured_in_a_cuda_graph():
+@pytest.mark.parametrize("T,d,F", [(200, 256, 128), (1, 2048, 256), (3, 2048, 256)])
+def test_forward_captured_in_a_cuda_graph(T, d, F):
     # moe_forward enqueues only kernels and a memset on the caller's stream
     # (no host synchronisation, no allocation), so it can be captured once
     # and replayed; replays on new inputs match the eager call bit for bit.
-    shape = synth.LayerShape(T=200, d=256, E=16, k=2, F=128)
-    inp = synth.make_inputs(shape, seed=16)
+    # 1 and 3 tokens: the routing finished in the gate/up launch, K split in
+    # balanced ranges (the part counters reset by each launch), and with one
+    # token the L2 prefetch of the down launch's first weights.
+    shape = synth.LayerShape(T=T, d=d, E=16, k=2, F=F)
+    inp = synth.make_inputs(shape, seed=16 + T)
     layer, x = make_layer(inp)
     y = torch.empty((shape.T, shape.d), dtype=torch.bfloat16, device=DEV)
     layer.forward(x, y)  # warm-up outside the capture
