@@ -441,9 +441,11 @@ __global__ void __launch_bounds__(1024, 1) combine_kernel(const __half* __restri
   const int t = blockIdx.x;
   __shared__ int pos[kMaxTopK + 1];
   __shared__ int chunk[kMaxTopK + 1];
-  // the k + 1 terms' rows (a block can have fewer threads than terms: 32
-  // threads for d = 256 against up to 33 terms)
-  for (int j = threadIdx.x; j <= k; j += blockDim.x) {
+  // the terms' rows: k routed, then the shared expert's when the layer has
+  // one (a block can have fewer threads than terms: 32 threads for d = 256
+  // against up to 33 terms)
+  const int nterms = k + (has_shared ? 1 : 0);
+  for (int j = threadIdx.x; j < nterms; j += blockDim.x) {
     int g = (j < k) ? __ldg(idx + static_cast<size_t>(t) * k + j) : E;
     int p = (j < k) ? __ldg(inv + static_cast<size_t>(t) * k + j) : T * k + t;
     if (!MOE_DBG_OK(g >= 0 && g <= E)) g = E;
@@ -458,7 +460,6 @@ __global__ void __launch_bounds__(1024, 1) combine_kernel(const __half* __restri
   }
   __syncthreads();
   pdl_wait();  // the expert outputs from here on (the routing results above are older, as in combine_nt_kernel)
-  const int nterms = k + (has_shared ? 1 : 0);
   // routed rows (slots j < k) from yp_routed / yexp_routed when given
   // (expert parallelism: the rows the experts' owners sent back)
   const __half* yp_r = yp_routed ? yp_routed : yp;

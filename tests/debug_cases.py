@@ -28,9 +28,11 @@ def case(shape, seed, tiles=(0, 0), env=None, n_sample=None, fp8=False):
     try:
         if fp8:
             q = binding.moe_quantize_fp8(inp.w_gate_up) + binding.moe_quantize_fp8(inp.w_down)
-            layer = binding.MoeLayer.fp8(inp.w_router, *q, shape.k, shape.T, out_fp32=True)
+            layer = binding.MoeLayer.fp8(inp.w_router, *q, shape.k, shape.T, has_shared=shape.has_shared,
+                                         out_fp32=True)
         else:
-            layer = binding.MoeLayer(inp.w_router, inp.w_gate_up, inp.w_down, shape.k, shape.T, out_fp32=True)
+            layer = binding.MoeLayer(inp.w_router, inp.w_gate_up, inp.w_down, shape.k, shape.T,
+                                     has_shared=shape.has_shared, out_fp32=True)
     finally:
         for k, v in old.items():
             if v is None:
@@ -43,12 +45,13 @@ def case(shape, seed, tiles=(0, 0), env=None, n_sample=None, fp8=False):
     assert rc == binding.MOE_OK, f"device error word set: {binding.moe_status_string(rc)}"
     xb, wr, wgu, wd = host_bits(inp)
     idx_h = cpu(idx)
-    near, _ = check_routing(xb, wr, shape.k, idx_h, cpu(prob), cpu(gap), cpu(perm), cpu(offsets))
+    near, _ = check_routing(xb, wr, shape.k, idx_h, cpu(prob), cpu(gap), cpu(perm), cpu(offsets),
+                            has_shared=shape.has_shared)
     tokens = np.arange(shape.T, dtype=np.int32) if n_sample is None else sample_tokens(shape.T, idx_h, n_sample, seed,
                                                                                       near)
     fp8_h = tuple(cpu(t) for t in q) if fp8 else None
-    ratio = check_output(xb, wr, wgu, wd, shape.k, cpu(y.float())[tokens], idx_h, tokens=tokens, out_bf16=False,
-                         fp8=fp8_h)
+    ratio = check_output(xb, wr, wgu, wd, shape.k, cpu(y.float())[tokens], idx_h, tokens=tokens,
+                         has_shared=shape.has_shared, out_bf16=False, fp8=fp8_h)
     layer.close()
     return ratio
 
@@ -67,6 +70,9 @@ def main():
         ("K split in balanced ranges", lambda: case(S(T=5, d=1024, E=16, k=2, F=384), 8, tiles=(32, 32),
                                                     env={"MOE_GEMM_KSPLIT": "b"})),
         ("FP8 two-term rows", lambda: case(S(T=600, d=512, E=24, k=2, F=256), 7, fp8=True, n_sample=64)),
+        # no shared expert: k terms per token in the combine, no shared group
+        ("no shared expert, generic combine", lambda: case(S(T=50, d=256, E=12, k=3, F=128, has_shared=False), 9)),
+        ("no shared expert, FP8", lambda: case(S(T=70, d=256, E=12, k=3, F=128, has_shared=False), 10, fp8=True)),
     ]
     for name, run in cases:
         r = run()

@@ -24,4 +24,4 @@ def test_debug_build_runs_clean_against_the_oracle():
                        text=True, timeout=900)
     print(r.stdout)
     assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
-    assert r.stdout.count("ok  ") == 8
+    assert r.stdout.count("ok  ") == 10
