@@ -1,0 +1,71 @@
+"""Layer calls enqueued back to back, with no host synchronisation between
+them, give bit for bit what each gives alone.
+
+Consecutive calls overlap on the device: every kernel may start while the one
+before it ends (programmatic dependent launch), and from 2048 tokens on the
+shared expert's GEMMs run on a second stream.  A call that read a buffer the
+previous call was still writing, or wrote one it was still reading, would
+show up here: the sequence switches between two inputs, token counts from
+every dispatch regime (1-4 tokens with the routing finished in the gate/up
+launch, the single-block dispatch with K-split GEMMs, the chunked dispatch,
+256-token tiles on CTA pairs, the second stream) and per-call top-k, so a
+stale value from the call before is never the right one.  The reference for
+every (input, token count, top-k) is the same call run alone and synchronised.
+"""
+import pytest
+import torch
+
+from expert_routed_ffn_gemm_gb300 import binding, synth
+
+from moe_check import to_dev
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+# (tokens, top_k or None for the layer's k, renormalise)
+SEQUENCE = [(1, None, False), (37, None, False), (4, None, False), (600, None, False), (2500, None, False),
+            (3, None, False), (130, 1, True), (2048, None, False), (1, None, False), (2, None, False),
+            (1100, None, False), (4, 1, True), (2500, 1, True), (37, None, False)]
+
+
+def _layer(fp8: bool):
+    shape = synth.LayerShape(T=2500, d=256, E=16, k=2, F=128)
+    inp = synth.make_inputs(shape, seed=901)
+    x, wr, wgu, wd = to_dev(inp, DEV)
+    if fp8:
+        q = binding.moe_quantize_fp8(wgu) + binding.moe_quantize_fp8(wd)
+        layer = binding.MoeLayer.fp8(wr, *q, shape.k, shape.T)
+    else:
+        layer = binding.MoeLayer(wr, wgu, wd, shape.k, shape.T)
+    x2 = to_dev(synth.make_inputs(shape, seed=902), DEV)[0]
+    return layer, (x, x2)
+
+
+def _call(layer, x, T, top_k, renorm, y):
+    if top_k is None:
+        return layer.forward(x[:T], y)
+    return layer.forward(x[:T], y, top_k=top_k, renormalize=renorm)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_back_to_back_calls_match_calls_alone(fp8):
+    layer, xs = _layer(fp8)
+    calls = [(i % 2, T, kk, rn) for i, (T, kk, rn) in enumerate(SEQUENCE * 3)]
+    ref = {}
+    for c in dict.fromkeys(calls):
+        w, T, kk, rn = c
+        y = torch.empty((T, 256), dtype=torch.bfloat16, device=DEV)
+        _call(layer, xs[w], T, kk, rn, y)
+        torch.cuda.synchronize()
+        assert layer.check() == binding.MOE_OK
+        ref[c] = y.clone()
+    outs = [torch.full((T, 256), float("nan"), dtype=torch.bfloat16, device=DEV) for (_, T, _, _) in calls]
+    torch.cuda.synchronize()
+    for c, y in zip(calls, outs):
+        w, T, kk, rn = c
+        _call(layer, xs[w], T, kk, rn, y)
+    torch.cuda.synchronize()
+    assert layer.check() == binding.MOE_OK
+    bad = [i for i, (c, y) in enumerate(zip(calls, outs)) if not torch.equal(y, ref[c])]
+    assert not bad, [calls[i] for i in bad]
+    layer.close()

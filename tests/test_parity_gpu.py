@@ -325,6 +325,35 @@ def flash_case(flash_weights, T, seed, n_sample=None, skew=None, out_fp32=False)
     return ratio
 
 
+def test_flash_back_to_back_calls_match_calls_alone(flash_weights):
+    # The flash shape's regimes (1-4 tokens with the routing finished in the
+    # gate/up launch over replicated token rows, the decode batch, 37 tokens
+    # with K-split GEMMs, the chunked dispatch with CTA pairs and the second
+    # stream) enqueued back to back with no host synchronisation, switching
+    # between two token sets: every result bit for bit that of the same call
+    # run alone (consecutive calls overlap on the device; a stale or clobbered
+    # buffer would show).
+    inp, _ = flash_weights
+    shape = synth.FLASH_PREFILL
+    xs = [synth.make_tokens(shape, seed=s, device=DEV) for s in (71, 72)]
+    layer = binding.MoeLayer(inp.w_router, inp.w_gate_up, inp.w_down, shape.k, shape.T)
+    calls = [(i % 2, T) for i, T in enumerate([1, 128, 4, 8192, 2, 37, 2048, 3, 1, 128] * 2)]
+    ref = {}
+    for w, T in sorted(set(calls)):
+        ref[(w, T)] = layer.forward(xs[w][:T]).clone()
+        torch.cuda.synchronize()
+        assert layer.check() == binding.MOE_OK
+    outs = [torch.empty((T, shape.d), dtype=torch.bfloat16, device=DEV) for _, T in calls]
+    torch.cuda.synchronize()
+    for (w, T), y in zip(calls, outs):
+        layer.forward(xs[w][:T], y)
+    torch.cuda.synchronize()
+    assert layer.check() == binding.MOE_OK
+    bad = [c for c, y in zip(calls, outs) if not torch.equal(y, ref[c])]
+    assert not bad, bad
+    layer.close()
+
+
 @pytest.mark.parametrize("out_fp32", [False, True])
 def test_flash_decode_all_tokens(flash_weights, out_fp32):
     # d=4096, 288 routed + 1 shared, top-8, width 1280, T=128 (decode batch)
