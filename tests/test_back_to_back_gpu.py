@@ -28,23 +28,23 @@ SEQUENCE = [(1, None, False), (37, None, False), (4, None, False), (600, None, F
             (1100, None, False), (4, 1, True), (2500, 1, True), (37, None, False)]
 
 
-def _layer(fp8: bool):
+def _layer(fp8: bool, seed: int = 901):
     shape = synth.LayerShape(T=2500, d=256, E=16, k=2, F=128)
-    inp = synth.make_inputs(shape, seed=901)
+    inp = synth.make_inputs(shape, seed=seed)
     x, wr, wgu, wd = to_dev(inp, DEV)
     if fp8:
         q = binding.moe_quantize_fp8(wgu) + binding.moe_quantize_fp8(wd)
         layer = binding.MoeLayer.fp8(wr, *q, shape.k, shape.T)
     else:
         layer = binding.MoeLayer(wr, wgu, wd, shape.k, shape.T)
-    x2 = to_dev(synth.make_inputs(shape, seed=902), DEV)[0]
+    x2 = to_dev(synth.make_inputs(shape, seed=seed + 1), DEV)[0]
     return layer, (x, x2)
 
 
-def _call(layer, x, T, top_k, renorm, y):
+def _call(layer, x, T, top_k, renorm, y, stream=None):
     if top_k is None:
-        return layer.forward(x[:T], y)
-    return layer.forward(x[:T], y, top_k=top_k, renormalize=renorm)
+        return layer.forward(x[:T], y, stream=stream)
+    return layer.forward(x[:T], y, stream=stream, top_k=top_k, renormalize=renorm)
 
 
 @pytest.mark.parametrize("fp8", [False, True])
@@ -69,3 +69,37 @@ def test_back_to_back_calls_match_calls_alone(fp8):
     bad = [i for i, (c, y) in enumerate(zip(calls, outs)) if not torch.equal(y, ref[c])]
     assert not bad, [calls[i] for i in bad]
     layer.close()
+
+
+def test_two_layers_on_two_streams_at_once():
+    # Two handles (bf16 and FP8 weights, different seeds) each enqueue on a
+    # stream of their own, their calls alternating and running side by side on
+    # the device with no synchronisation: nothing is shared between handles,
+    # so each result is bit for bit that of the same call alone.
+    layers = [_layer(False, seed=911), _layer(True, seed=921)]
+    seqs = [[(T, None, False) for T in (2500, 4, 600, 1, 2048, 37, 130, 3)],
+            [(T, None, False) for T in (1, 2048, 37, 2500, 3, 600, 4, 1100)]]
+    seqs[1][2] = (37, 1, True)
+    refs = [[], []]
+    for h in range(2):
+        layer, xs = layers[h]
+        for i, (T, kk, rn) in enumerate(seqs[h]):
+            y = torch.empty((T, 256), dtype=torch.bfloat16, device=DEV)
+            _call(layer, xs[i % 2], T, kk, rn, y)
+            torch.cuda.synchronize()
+            assert layer.check() == binding.MOE_OK
+            refs[h].append(y)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [[torch.empty((T, 256), dtype=torch.bfloat16, device=DEV) for T, _, _ in seqs[h]] for h in range(2)]
+    torch.cuda.synchronize()
+    for i in range(len(seqs[0])):
+        for h in range(2):
+            layer, xs = layers[h]
+            T, kk, rn = seqs[h][i]
+            _call(layer, xs[i % 2], T, kk, rn, outs[h][i], stream=streams[h])
+    torch.cuda.synchronize()
+    for h in range(2):
+        assert layers[h][0].check() == binding.MOE_OK
+        bad = [seqs[h][i] for i in range(len(seqs[h])) if not torch.equal(outs[h][i], refs[h][i])]
+        assert not bad, (h, bad)
+        layers[h][0].close()
