@@ -103,3 +103,51 @@ def test_two_layers_on_two_streams_at_once():
         bad = [seqs[h][i] for i in range(len(seqs[h])) if not torch.equal(outs[h][i], refs[h][i])]
         assert not bad, (h, bad)
         layers[h][0].close()
+
+
+def test_two_host_threads_each_with_a_handle():
+    # Two host threads, each driving its own handle on its own stream (the
+    # library's host code holds no per-call global state): every result bit for
+    # bit the same call alone.
+    import threading
+
+    layers = [_layer(False, seed=931), _layer(False, seed=941)]
+    seq = [(T, None, False) for T in (2500, 1, 600, 4, 2048, 37, 3, 130)]
+    refs = [[], []]
+    for h in range(2):
+        layer, xs = layers[h]
+        for i, (T, kk, rn) in enumerate(seq):
+            y = torch.empty((T, 256), dtype=torch.bfloat16, device=DEV)
+            _call(layer, xs[i % 2], T, kk, rn, y)
+            torch.cuda.synchronize()
+            refs[h].append(y)
+    outs = [[[torch.empty((T, 256), dtype=torch.bfloat16, device=DEV) for T, _, _ in seq] for _ in range(5)]
+            for _ in range(2)]
+    torch.cuda.synchronize()
+    errors = []
+
+    def drive(h):
+        try:
+            layer, xs = layers[h]
+            st = torch.cuda.Stream()
+            for rep in range(5):
+                for i, (T, kk, rn) in enumerate(seq):
+                    _call(layer, xs[i % 2], T, kk, rn, outs[h][rep][i], stream=st)
+            st.synchronize()
+        except Exception as e:  # reported by the main thread
+            errors.append((h, repr(e)))
+
+    threads = [threading.Thread(target=drive, args=(h,)) for h in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join(timeout=120)
+    assert not any(th.is_alive() for th in threads)
+    assert not errors, errors
+    torch.cuda.synchronize()
+    for h in range(2):
+        assert layers[h][0].check() == binding.MOE_OK
+        bad = [(rep, seq[i]) for rep in range(5) for i in range(len(seq))
+               if not torch.equal(outs[h][rep][i], refs[h][i])]
+        assert not bad, (h, bad)
+        layers[h][0].close()
