@@ -16,8 +16,13 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "moe_oracle.c")
-_LIB = os.path.join(_HERE, "libmoe_oracle.so")
+# MOE_ORACLE_SOURCE names another copy of the oracle's C source to compile and
+# load instead (beside it): the test that plants one mistake per copy and
+# checks that the pins fail on each uses it.  Unset: moe_oracle.c here.
+_VARIANT = os.environ.get("MOE_ORACLE_SOURCE")
+_SRC = os.path.abspath(_VARIANT) if _VARIANT else os.path.join(_HERE, "moe_oracle.c")
+_LIB = os.path.join(os.path.dirname(_SRC), "libmoe_oracle_variant.so") if _VARIANT else os.path.join(
+    _HERE, "libmoe_oracle.so")
 _lock = threading.Lock()
 _lib = None
 
