@@ -14,8 +14,9 @@ Tolerances (stated once, used by every parity test):
     own measured errors on them (each within the derived fp32 router bound,
     ``prob_bound``), i.e. where the rounding of the router itself explains
     the swap;
-* probabilities: within the fp32 error bound derived in ``prob_bound``, and
-  non-increasing along the slots (the order the GPU chose);
+* probabilities: within the fp32 error bound derived in ``prob_bound``, within
+  the empirical guard PROB_GUARD of relative error, and non-increasing along
+  the slots (the order the GPU chose);
 * layer output: |y_gpu - y_oracle| <= OUT_TOL * RMS(y_oracle) everywhere.
   Only the cases that pass ``storage_slack=True`` (each named where it is
   called, with the measurement that needs it) add half a bf16 ulp of
@@ -34,6 +35,14 @@ import parity_log
 
 NEAR_TIE = 1e-6
 OUT_TOL = 2e-2
+# Beside the derived bound (the worst case of fp32 summation, linear in 3d:
+# 17 % of p at d = 4096) an empirical guard on the selected probabilities'
+# relative error: every GPU run so far stayed below 6.4e-5 (the 32768-token
+# flash case); 1e-3 fails a router that lost precision, e.g. one computing with
+# a bf16 copy of W_r (about 6.5e-3 at the flash shape).  A router that dropped
+# only the third bf16 slice (about 9e-6) is below the fp32 rounding noise and
+# no such guard could tell it apart.
+PROB_GUARD = 1e-3
 
 
 def to_dev(inp: synth.LayerInputs, dev):
@@ -133,6 +142,7 @@ def check_routing(x_bits, w_router, k, idx, prob, gap=None, perm=None, offsets=N
         assert offsets[E + 1] == off_ref[E] + (T if has_shared else 0)
         np.testing.assert_array_equal(perm, perm_ref)
     p_rel = float((err / np.maximum(p_ref, 1e-300)).max()) if T > 0 else 0.0
+    assert p_rel <= PROB_GUARD, f"relative probability error {p_rel:.3e} above the guard {PROB_GUARD:g}"
     parity_log.record("routing", T=T, k=k, boundary_near_ties=int(boundary.sum()),
                       boundary_chose_other=int(set_diff.size), order_near_ties=int(order_cand.sum()),
                       order_swapped=int(order_diff.size), max_prob_rel_err=p_rel)

@@ -13,7 +13,7 @@ import torch
 import oracle
 from expert_routed_ffn_gemm_gb300 import synth
 
-from moe_check import OUT_TOL, check_output, check_routing, host_bits, prob_bound
+from moe_check import OUT_TOL, PROB_GUARD, check_output, check_routing, host_bits, prob_bound
 
 SHAPE = synth.LayerShape(T=48, d=128, E=16, k=4, F=64)
 
@@ -88,6 +88,28 @@ def test_a_probability_beyond_its_bound_is_rejected(layer, sign):
     prob[t] = np.sort(prob[t])[::-1]  # still ordered along the slots
     with pytest.raises(AssertionError):
         _routing(layer, prob=prob)
+
+
+def test_a_bf16_router_is_rejected_where_the_derived_bound_is_loose():
+    # d = 4096: the derived bound allows some 17 % of p; probabilities from a
+    # bf16 copy of W_r (errors of a few 1e-3 of p) must still fail, on the
+    # empirical guard
+    shape = synth.LayerShape(T=16, d=4096, E=32, k=4, F=64)
+    inp = synth.make_inputs(shape, seed=79)
+    xb, wr, _, _ = host_bits(inp)
+    idx, w, gap, p = oracle.route(xb, wr, shape.k, want_p=True)
+    _, off, perm = oracle.dispatch(idx, shape.E)
+    off[shape.E + 1] = off[shape.E] + shape.T
+    check_routing(xb, wr, shape.k, idx, w.astype(np.float32), gap.astype(np.float32), perm, off)
+    wr16 = torch.from_numpy(wr).to(torch.bfloat16).float().numpy()
+    _, _, _, p16 = oracle.route(xb, wr16, shape.k, want_p=True)
+    prob16 = p16[np.arange(shape.T)[:, None], idx]
+    rel = np.abs(prob16 - w) / w
+    assert rel.max() > PROB_GUARD  # the bf16 router's error
+    assert np.all(np.abs(prob16 - w) <= prob_bound(xb, wr, np.arange(shape.T), p)[np.arange(shape.T)[:, None], idx])
+    with pytest.raises(AssertionError, match="guard"):
+        check_routing(xb, wr, shape.k, idx, np.sort(prob16, axis=1)[:, ::-1].astype(np.float32),
+                      gap.astype(np.float32), perm, off)
 
 
 def test_dispatch_errors_are_rejected(layer):
